@@ -1,0 +1,171 @@
+"""fp64 CPU oracle of the Lightning Attention RNN mixer (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` are the only
+callers.  The product package never imports this module and shares no code with
+it.  The arithmetic lives in ``hla_oracle.c`` (plain C, fp64, OpenMP over the
+independent (b, h) recurrences); this file only compiles it with gcc and
+marshals numpy arrays.
+
+Every function follows arXiv 2601.22156 ("Hybrid Linear Attention Done
+Right"), Appendix A, Eq. 18 (RNN layers) and Eq. 19 (forget gate).  Arrays are
+float64, C-contiguous, activations [B, T, H, d], state [B, H, d, d]
+(d_k rows, d_v fastest).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "hla_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libhla_oracle.so")
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+
+
+def build(force: bool = False) -> str:
+    """Compile hla_oracle.c into a shared library (gcc -O2 -fopenmp)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_BUILD)
+    os.close(fd)
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    i, d64, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+    lib.hla_oracle_threads.restype = i
+    lib.hla_oracle_gamma.argtypes = [i, _dp]
+    lib.hla_oracle_feature.argtypes = [i, _dp, d64, dbl, dbl, dbl, _dp]
+    lib.hla_oracle_prefill.argtypes = [i, i, i, i, _dp, _dp, _dp, _dp, _dp, _dp, d64, dbl, dbl,
+                                       _dp, _dp, _dp]
+    lib.hla_oracle_prefill.restype = i
+    lib.hla_oracle_prefill_chunked.argtypes = [i, i, i, i, i, _dp, _dp, _dp, _dp, _dp, _dp, d64,
+                                               dbl, dbl, _dp, _dp, _dp]
+    lib.hla_oracle_prefill_chunked.restype = i
+    lib.hla_oracle_decode.argtypes = [i, i, i, _dp, _dp, _dp, _dp, _dp, _i64p, _dp, dbl, dbl,
+                                      _dp, _dp, _dp]
+    lib.hla_oracle_decode.restype = i
+    lib.hla_oracle_backward.argtypes = [i, i, i, i, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, d64,
+                                        dbl, dbl, _dp, _dp, _dp, _dp, _dp]
+    lib.hla_oracle_backward.restype = i
+    _lib = lib
+    return lib
+
+
+def _f64(x):
+    if x is None:
+        return None
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(x):
+    if x is None:
+        return ctypes.cast(None, _dp)
+    return x.ctypes.data_as(_dp)
+
+
+def threads() -> int:
+    """OpenMP threads the oracle uses (all host cores unless OMP_NUM_THREADS)."""
+    return int(_load().hla_oracle_threads())
+
+
+def gamma(H: int) -> np.ndarray:
+    """Eq. 19 forget rates gamma_h = exp(-2^(-8(h+1)/H)), 0-based head h, fp64."""
+    out = np.zeros(H, dtype=np.float64)
+    _load().hla_oracle_gamma(H, _ptr(out))
+    return out
+
+
+def feature(x, pos: int, base: float, eps: float = 1e-6, scale: float = 1.0) -> np.ndarray:
+    """Norm(x), rotated by RoPE at position ``pos``, times ``scale`` (one row)."""
+    x = _f64(x)
+    out = np.zeros_like(x)
+    _load().hla_oracle_feature(x.shape[-1], _ptr(x), int(pos), float(base), float(eps),
+                               float(scale), _ptr(out))
+    return out
+
+
+def _dims(q):
+    if q.ndim != 4:
+        raise ValueError("activations must be [B, T, H, d]")
+    return q.shape
+
+
+def prefill(q, k, v, g, gam, state_in=None, pos_offset=0, base=1e4, eps=1e-6):
+    """Per-timestep recurrence of Eq. 18.  Returns (y, o, state_out)."""
+    q, k, v, g, gam, state_in = map(_f64, (q, k, v, g, gam, state_in))
+    B, T, H, d = _dims(q)
+    y, o = np.zeros_like(q), np.zeros_like(q)
+    st = np.zeros((B, H, d, d), dtype=np.float64)
+    rc = _load().hla_oracle_prefill(B, T, H, d, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(gam),
+                                    _ptr(state_in), int(pos_offset), float(base), float(eps),
+                                    _ptr(y), _ptr(o), _ptr(st))
+    if rc:
+        raise RuntimeError(f"oracle prefill failed ({rc})")
+    return y, o, st
+
+
+def prefill_chunked(q, k, v, g, gam, chunk, state_in=None, pos_offset=0, base=1e4, eps=1e-6):
+    """Block (chunked) evaluation of the same mixer.  Returns (y, o, state_out)."""
+    q, k, v, g, gam, state_in = map(_f64, (q, k, v, g, gam, state_in))
+    B, T, H, d = _dims(q)
+    y, o = np.zeros_like(q), np.zeros_like(q)
+    st = np.zeros((B, H, d, d), dtype=np.float64)
+    rc = _load().hla_oracle_prefill_chunked(B, T, H, d, int(chunk), _ptr(q), _ptr(k), _ptr(v),
+                                            _ptr(g), _ptr(gam), _ptr(state_in), int(pos_offset),
+                                            float(base), float(eps), _ptr(y), _ptr(o), _ptr(st))
+    if rc:
+        raise RuntimeError(f"oracle chunked prefill failed ({rc})")
+    return y, o, st
+
+
+def decode_step(q, k, v, g, gam, pos, state_in, base=1e4, eps=1e-6):
+    """One token per sequence ([B, 1, H, d]); pos[b] is its RoPE position."""
+    q, k, v, g, gam, state_in = map(_f64, (q, k, v, g, gam, state_in))
+    B, T, H, d = _dims(q)
+    if T != 1:
+        raise ValueError("decode takes T == 1")
+    pos = np.ascontiguousarray(np.asarray(pos, dtype=np.int64).reshape(B))
+    y, o = np.zeros_like(q), np.zeros_like(q)
+    st = np.zeros((B, H, d, d), dtype=np.float64)
+    rc = _load().hla_oracle_decode(B, H, d, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(gam),
+                                   pos.ctypes.data_as(_i64p), _ptr(state_in), float(base),
+                                   float(eps), _ptr(y), _ptr(o), _ptr(st))
+    if rc:
+        raise RuntimeError(f"oracle decode failed ({rc})")
+    return y, o, st
+
+
+def backward(q, k, v, g, gam, dy, state_in=None, dstate_out=None, pos_offset=0, base=1e4,
+             eps=1e-6):
+    """Chain-rule gradients.  Returns (dq, dk, dv, dg, dstate_in)."""
+    q, k, v, g, gam, dy, state_in, dstate_out = map(
+        _f64, (q, k, v, g, gam, dy, state_in, dstate_out))
+    B, T, H, d = _dims(q)
+    dq, dk, dv, dg = (np.zeros_like(q) for _ in range(4))
+    dst = np.zeros((B, H, d, d), dtype=np.float64)
+    rc = _load().hla_oracle_backward(B, T, H, d, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(gam),
+                                     _ptr(state_in), _ptr(dy), _ptr(dstate_out), int(pos_offset),
+                                     float(base), float(eps), _ptr(dq), _ptr(dk), _ptr(dv),
+                                     _ptr(dg), _ptr(dst))
+    if rc:
+        raise RuntimeError(f"oracle backward failed ({rc})")
+    return dq, dk, dv, dg, dst
