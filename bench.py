@@ -1,0 +1,412 @@
+#!/usr/bin/env python
+"""Benchmark of the Lightning Attention RNN mixer on GB300 (one JSON line).
+
+Headline: hla_prefill over B=1, T=524288, H=16, d=128 bf16 (inputs resident in
+HBM, 8 GiB, far larger than L2), reported as Mtok/s and as a fraction of the
+HBM roofline.  The same line carries the batched decode step (B=64, H=32,
+d=128, state from a 4096-token prefill, L2 flushed between steps) and the
+distillation-shaped forward+backward (B=8, T=16384, H=32), the end-to-end
+figure through the public API with pinned host buffers, the fp64 CPU oracle
+timed on a bounded sample, and the SM clocks sampled during the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs an independent replica (weak scaling); rank 0
+prints the line.  ``--impl reference`` times the CPU oracle alone.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Lightning-attn prefill Mtok/s @512K + decode tok/s (B=64), % of roofline"
+BF16 = 2
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--no-backward", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target CPU time of the oracle sample")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+
+def oracle_sample(w, seconds: float):
+    """Time the fp64 oracle on a bounded sample of workload ``w`` (all H heads of
+    one sequence, the first n tokens), growing n until the sample takes about
+    ``seconds``.  Returns (tokens/s, n_tokens, threads)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from rnn_sequence_mixer_gb300 import inputs
+
+    gam = oracle.gamma(w.H).astype(np.float32).astype(np.float64)
+    n, spent = 256, 0.0
+    while True:
+        inp = inputs.mixer_inputs(1, n, w.H, w.d, w.dtype, w.seed, device="cpu")
+        arr = {k: v.to(torch.float64).numpy() for k, v in inp.items()}
+        t0 = time.perf_counter()
+        oracle.prefill(arr["q"], arr["k"], arr["v"], arr["gate"], gam, base=w.rope_base, eps=w.eps)
+        dt = time.perf_counter() - t0
+        spent += dt
+        if dt >= seconds / 4 or n >= w.T or spent >= seconds:
+            return n / dt, n, oracle.threads(), dt
+        n = min(w.T, max(2 * n, int(n * (seconds / 4) / max(dt, 1e-3))))
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle on bounded samples of the headline workload."""
+    from rnn_sequence_mixer_gb300 import workloads
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = workloads.PREFILL_512K
+    per = max(1.0, min(20.0, 60.0 / max(1, args.steps + args.warmup)))
+    tok_s, n, cores, _ = oracle_sample(w, per)
+    times = []
+    import numpy as np
+    import torch
+
+    import oracle
+    from rnn_sequence_mixer_gb300 import inputs
+    gam = oracle.gamma(w.H).astype(np.float32).astype(np.float64)
+    inp = inputs.mixer_inputs(1, n, w.H, w.d, w.dtype, w.seed, device="cpu")
+    arr = {k: v.to(torch.float64).numpy() for k, v in inp.items()}
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.prefill(arr["q"], arr["k"], arr["v"], arr["gate"], gam, base=w.rope_base, eps=w.eps)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    value = n / (ms / 1e3) / 1e6
+    sample = f"first {n} tokens of sequence 0, all {w.H} heads, fp64"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "Mtok/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "sample_tokens": n},
+        "cpu_baseline": {"value": value, "unit": "Mtok/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "Mtok/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+# ----------------------------------------------------------------------------- GPU arms
+
+
+def timed(fn, steps, warmup, stream, dist_ctx, trace_count=0):
+    """Run fn(i, trace) warmup + steps times; returns (ms per step, per-pass ms lists)."""
+    import torch
+    for i in range(warmup):
+        fn(i, None)
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    torch.cuda.synchronize()
+    traces = []
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        tr = [torch.cuda.Event(enable_timing=True) for _ in range(trace_count)] or None
+        fn(warmup + i, tr)
+        traces.append(tr)
+    end.record(stream)
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    ms = start.elapsed_time(end) / steps
+    passes = []
+    if trace_count:
+        for tr in traces:
+            passes.append([tr[j].elapsed_time(tr[j + 1]) for j in range(trace_count - 1)])
+    return ms, passes
+
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("nccl")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], device=f"cuda:{self.local}")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+
+def run_ours(args):
+    import torch
+
+    import oracle  # noqa: F401  (cpu_baseline leg only)
+    from rnn_sequence_mixer_gb300 import _lib, api, inputs, workloads
+
+    D = Dist()
+    torch.cuda.set_device(D.local)
+    dev = torch.device(f"cuda:{D.local}")
+    _lib.load()
+    hbm_peak, tc_peak, peak_src = peaks()
+    stream = torch.cuda.current_stream(dev)
+    launches = 0
+    out = {}
+
+    # ---------------------------------------------------------------- prefill @512K
+    w = workloads.PREFILL_512K
+    gam = api.gamma_schedule(w.H)
+    inp = inputs.mixer_inputs(w.B, w.T, w.H, w.d, w.dtype, w.seed + 1000 * D.rank, device=dev)
+    y = torch.empty_like(inp["q"])
+    st = torch.empty((w.B, w.H, w.d, w.d), dtype=torch.float32, device=dev)
+    ws = torch.empty(api.prefill_workspace_size(api.make_shape(w.B, w.T, w.H, w.d, chunk=w.chunk)),
+                     dtype=torch.uint8, device=dev)
+    n_pass = 3
+
+    def prefill_step(i, trace):
+        api.prefill(inp["q"], inp["k"], inp["v"], inp["gate"], gam, chunk=w.chunk,
+                    rope_base=w.rope_base, eps=w.eps, y=y, state_out=st, workspace=ws, trace=trace)
+
+    with ClockSampler(D.local) as clk:
+        ms, passes = timed(prefill_step, args.steps, args.warmup, stream, D, n_pass + 1)
+    launches += n_pass * args.steps
+    ms = D.max(ms)
+    tokens = w.B * w.T
+    value = D.world * tokens / (ms / 1e3) / 1e6
+    pass_names = ["seg_state", "state_scan", "seg_output"]
+    pass_ms = [statistics.mean(p[j] for p in passes) for j in range(n_pass)]
+    dom = max(range(n_pass), key=lambda j: pass_ms[j])
+    th = w.B * w.T * w.H
+    nseg_bytes = ws.numel()
+    alg = {  # algorithmic bytes per launch of each pass
+        "seg_state": th * 2 * w.d * BF16 + nseg_bytes,
+        "state_scan": 2 * nseg_bytes,
+        "seg_output": th * 5 * w.d * BF16,
+    }
+    a_bytes = alg[pass_names[dom]]
+    achieved = a_bytes / (pass_ms[dom] / 1e3) / 1e9
+    whole = th * 5 * w.d * BF16 / (ms / 1e3) / 1e9
+    roof = {"kernel": pass_names[dom], "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
+            "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
+            "peak_source": f"hbm_gbs of {peak_src}",
+            "pass_ms": dict(zip(pass_names, pass_ms)),
+            "whole_call": {"alg_bytes": th * 5 * w.d * BF16, "achieved": whole,
+                           "frac": whole / hbm_peak}}
+    config = {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "d": w.d, "chunk": w.chunk,
+              "rope_base": w.rope_base, "l2": "inputs larger than L2 (8 GiB resident per step)",
+              "replicas": D.world}
+
+    # ---------------------------------------------------------------- e2e through the API
+    e2e = None
+    if not args.no_e2e:
+        host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in inp.items()}
+        for k in host:
+            host[k].copy_(inp[k])
+        y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+        st_host = torch.empty(st.shape, dtype=st.dtype, pin_memory=True)
+        dbuf = {k: torch.empty_like(v) for k, v in inp.items()}
+
+        def e2e_step(i, trace):
+            for k in dbuf:
+                dbuf[k].copy_(host[k], non_blocking=True)
+            api.prefill(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["gate"], gam, chunk=w.chunk,
+                        rope_base=w.rope_base, eps=w.eps, y=y, state_out=st, workspace=ws)
+            y_host.copy_(y, non_blocking=True)
+            st_host.copy_(st, non_blocking=True)
+
+        e_steps = max(1, min(args.steps, 5))
+        e_ms, _ = timed(e2e_step, e_steps, 1, stream, D)
+        launches += n_pass * e_steps
+        e_ms = D.max(e_ms)
+        e2e = {"value": D.world * tokens / (e_ms / 1e3) / 1e6, "unit": "Mtok/s",
+               "ms_per_step": e_ms,
+               "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
+               "d2h_bytes_per_step": y_host.numel() * 2 + st_host.numel() * 4}
+        del host, y_host, st_host, dbuf
+    del inp, y, ws
+    torch.cuda.empty_cache()
+
+    # ---------------------------------------------------------------- decode B=64
+    if not args.no_decode:
+        wd = workloads.DECODE_B64
+        gd = api.gamma_schedule(wd.H)
+        pre = inputs.mixer_inputs(wd.B, wd.prefill_T, wd.H, wd.d, wd.dtype, wd.seed + 1000 * D.rank,
+                                  device=dev)
+        _, _, state = api.prefill(pre["q"], pre["k"], pre["v"], pre["gate"], gd, chunk=wd.chunk,
+                                  rope_base=wd.rope_base, eps=wd.eps)
+        del pre
+        steps = inputs.decode_inputs(wd.steps, wd.B, wd.H, wd.d, wd.dtype, wd.seed + 100, device=dev)
+        pos = torch.full((wd.B,), wd.prefill_T, dtype=torch.int64, device=dev)
+        yd = torch.empty((wd.B, 1, wd.H, wd.d), dtype=wd.dtype, device=dev)
+        flush = torch.empty(512 * 2**20 // 4, dtype=torch.float32, device=dev)
+        torch.cuda.synchronize()
+        D.barrier()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(wd.steps)]
+        for s in range(wd.steps):
+            flush.fill_(float(s))  # evict the state from L2 before each step
+            ev[s][0].record(stream)
+            api.decode_step(steps["q"][s], steps["k"][s], steps["v"][s], steps["gate"][s], gd,
+                            state, pos, rope_base=wd.rope_base, eps=wd.eps, y=yd)
+            ev[s][1].record(stream)
+            pos.add_(1)
+        torch.cuda.synchronize()
+        per = [a.elapsed_time(b) for a, b in ev]
+        launches += wd.steps
+        us = D.max(1e3 * statistics.mean(per))
+        bytes_step = wd.B * wd.H * (2 * wd.d * wd.d * 4 + 5 * wd.d * BF16)
+        ach = bytes_step / (us / 1e6) / 1e9
+        out["decode"] = {"workload": wd.name, "tok_s": D.world * wd.B / (us / 1e6),
+                         "us_per_step": us, "us_per_step_median": 1e3 * statistics.median(per),
+                         "steps": wd.steps, "l2": "flushed (512 MiB write) before every step",
+                         "roofline": {"kernel": "decode_step", "bound": "hbm", "achieved": ach,
+                                      "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
+                                      "alg_bytes": bytes_step, "traffic": None}}
+        del steps, state, flush
+        torch.cuda.empty_cache()
+
+    # ---------------------------------------------------------------- forward + backward
+    if not args.no_backward:
+        wb = workloads.FWD_BWD_16K
+        gb = api.gamma_schedule(wb.H)
+        ib = inputs.mixer_inputs(wb.B, wb.T, wb.H, wb.d, wb.dtype, wb.seed + 1000 * D.rank,
+                                 device=dev, with_dy=True)
+        shp = api.make_shape(wb.B, wb.T, wb.H, wb.d, chunk=wb.chunk)
+        wsb = torch.empty(api.backward_workspace_size(shp), dtype=torch.uint8, device=dev)
+        wsf = torch.empty(api.prefill_workspace_size(shp), dtype=torch.uint8, device=dev)
+        yb = torch.empty_like(ib["q"])
+
+        def fb_step(i, trace):
+            api.prefill(ib["q"], ib["k"], ib["v"], ib["gate"], gb, chunk=wb.chunk,
+                        rope_base=wb.rope_base, eps=wb.eps, y=yb, want_state=False, workspace=wsf)
+            api.prefill_backward(ib["q"], ib["k"], ib["v"], ib["gate"], gb, ib["dy"],
+                                 chunk=wb.chunk, rope_base=wb.rope_base, eps=wb.eps, workspace=wsb)
+
+        b_steps = max(1, min(args.steps, 5))
+        b_ms, _ = timed(fb_step, b_steps, 1, stream, D)
+        launches += 9 * b_steps
+        b_ms = D.max(b_ms)
+        thb = wb.B * wb.T * wb.H
+        alg_b = thb * (5 * wb.d * BF16 + 9 * wb.d * BF16)  # fwd 5 d-rows + bwd 5 in / 4 out
+        out["fwd_bwd"] = {"workload": wb.name, "ms_per_step": b_ms,
+                          "Mtok_s": D.world * wb.B * wb.T / (b_ms / 1e3) / 1e6,
+                          "alg_bytes": alg_b, "frac_hbm": alg_b / (b_ms / 1e3) / 1e9 / hbm_peak}
+        del ib, wsb, wsf, yb
+        torch.cuda.empty_cache()
+
+    # ---------------------------------------------------------------- CPU oracle
+    cpu = None
+    if D.rank == 0 and not args.no_cpu_baseline:
+        tok_s, n, cores, dt = oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": tok_s / 1e6, "unit": "Mtok/s", "cores": cores, "kind": "oracle",
+               "sample": f"first {n} tokens of sequence 0 of the 512K workload, all {w.H} heads, "
+                         f"fp64, {dt:.1f} s"}
+
+    if D.rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "Mtok/s", "n_gpus": D.world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic", "config": config, "roofline": roof, "cpu_baseline": cpu,
+                "e2e": e2e, "gpu_launches": launches, "clocks": clk.summary()}
+        line.update(out)
+        print(json.dumps(line))
+    if D.pg:
+        D.pg.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * hla.h — C ABI of the GB300 Lightning Attention RNN mixer library (libhla.so).
+ *
+ * The mixer is the RNN layer of HypeNet, arXiv 2601.22156 ("Hybrid Linear
+ * Attention Done Right"), Appendix A, Eq. 18, with the fixed per-head forget
+ * rate of Eq. 19.  Per sequence b and head h, with row vectors and a state
+ * S in R^{d x d} (d_k rows, d_v columns):
+ *
+ *   q_t  = Norm(q_raw_t),  k_t = Norm(k_raw_t)          QK-RMSNorm (Eq. 12)
+ *   q~_t = RoPE_p(q_t),    k~_t = RoPE_p(k_t) / sqrt(d)  HyPE RoPE in RNN layers
+ *   S_t  = gamma_h S_{t-1} + k~_t^T v_t
+ *   o_t  = q~_t S_t
+ *   y_t  = Norm(o_t) * sigmoid(gate_t)                   output norm + gate (Eq. 14)
+ *
+ * Norm is RMSNorm x / sqrt(mean(x^2) + norm_eps) with unit weight.  RoPE uses
+ * the rotate-half pairing (x_i, x_{i+d/2}), i < d/2, rotated by the angle
+ * p * rope_base^(-2i/d), at position p = pos_offset + t (0-based).  The
+ * projections x W_{q,k,v,z} and W_o lie outside this library: q, k, v are the
+ * projected per-head rows and gate is the pre-sigmoid logit x W_z.  Every RNN
+ * head owns its own k and v (the paper's GQA-to-MHA decoupling, Eq. 13), so
+ * q, k, v and gate all carry H heads.
+ *
+ * Conventions shared by every entry point
+ *   - Activations q, k, v, gate, y, dy, dq, dk, dv, dgate: device memory,
+ *     [B, T, H, d] contiguous (d fastest), element type shape->dtype
+ *     (fp32 or bf16).  o (optional): fp32 [B, T, H, d].
+ *   - States: device memory, fp32 [B, H, d, d], d_v index fastest.
+ *   - gamma: HOST memory, fp32 [H], every value in (0, 1].  It is read during
+ *     the call and copied into the launch parameters (so a captured CUDA graph
+ *     keeps the values it saw at capture time).
+ *   - Every device pointer must be 16-byte aligned.  The caller owns and
+ *     allocates every buffer, including the workspace; the library never
+ *     allocates, frees or synchronizes.  All work is enqueued on `stream`
+ *     (NULL = the legacy default stream) of the current device.
+ *   - Arguments are validated before anything is launched: a bad argument
+ *     returns HLA_ERR_INVALID_ARG / HLA_ERR_UNSUPPORTED / HLA_ERR_WORKSPACE and
+ *     enqueues nothing.  HLA_ERR_CUDA means a launch was rejected by the CUDA
+ *     runtime; faults during execution surface at the caller's next sync.
+ *   - No C++ exception crosses the ABI.  There is no mutable global state:
+ *     calls on different streams may run concurrently from several threads.
+ *   - Supported: d_k == d_v in {64, 128}; chunk in {64, 128}; T >= 1;
+ *     1 <= H <= 256; 0 <= pos_offset and pos_offset + T < 2^62.
+ */
+#ifndef HLA_H_
+#define HLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HLA_ABI_VERSION 1
+
+typedef enum {
+  HLA_OK = 0,
+  HLA_ERR_INVALID_ARG = 1, /* NULL/misaligned pointer, non-positive size, bad gamma/eps/base */
+  HLA_ERR_UNSUPPORTED = 2, /* valid but not implemented here (d, chunk, dtype, H range)      */
+  HLA_ERR_WORKSPACE = 3,   /* workspace pointer NULL or ws_bytes below the required size     */
+  HLA_ERR_CUDA = 4,        /* the CUDA runtime rejected a launch or an attribute call        */
+  HLA_ERR_TIMEOUT = 5      /* reserved: a bounded device-side wait gave up                   */
+} hla_status;
+
+typedef enum { HLA_F32 = 0, HLA_BF16 = 1 } hla_dtype;
+
+/* Problem description shared by all entry points. */
+typedef struct {
+  int32_t B;          /* sequences                                              */
+  int32_t T;          /* tokens per sequence in this call (1 for a decode step)  */
+  int32_t H;          /* heads                                                  */
+  int32_t dk;         /* key/query head dim d_k                                 */
+  int32_t dv;         /* value head dim d_v (must equal dk)                     */
+  int32_t chunk;      /* token tile of the chunked prefill: 64 or 128           */
+  int32_t dtype;      /* hla_dtype of q, k, v, gate, y and the gradients        */
+  int32_t reserved;   /* must be 0                                              */
+  int64_t pos_offset; /* RoPE position of token 0 (prefill and backward)        */
+  double rope_base;   /* RoPE base theta (1e6 for HypeNet-2B/5B/9B, Table 6)    */
+  float norm_eps;     /* RMSNorm epsilon of the QK norms and the output norm    */
+} hla_shape;
+
+typedef void *hla_stream; /* a cudaStream_t */
+
+/*
+ * Optional per-pass tracing (the last argument of hla_prefill and
+ * hla_prefill_backward; NULL = none).  events[i] are caller-created
+ * cudaEvent_t handles; the library records events[i] on `stream` right before
+ * its i-th kernel launch and events[n_passes] after the last one, for every
+ * i < count.  Elapsed times between consecutive events are the device times
+ * of the individual passes.  The library creates, destroys and synchronizes
+ * nothing.
+ */
+#define HLA_TRACE_MAX 16
+typedef struct {
+  void *events[HLA_TRACE_MAX];
+  int32_t count;
+} hla_trace;
+
+/* ABI version of the loaded library (HLA_ABI_VERSION). */
+int hla_abi_version(void);
+
+/* Static, human-readable name of a status code. */
+const char *hla_status_string(hla_status status);
+
+/*
+ * Eq. 19 forget rates: gamma_out[h] = exp(-2^(-8(h+1)/H)) for the 0-based
+ * head h (the paper's head h+1), evaluated in fp64 and rounded to fp32.
+ * Host memory; returns HLA_ERR_INVALID_ARG for H < 1 or a NULL pointer.
+ */
+hla_status hla_gamma_schedule(int32_t H, float *gamma_out);
+
+/* Device workspace bytes hla_prefill needs for this shape (0 on a bad shape). */
+size_t hla_prefill_workspace_size(const hla_shape *shape);
+
+/*
+ * Forward over T tokens (prefill), Eq. 18 for every (b, h, t).
+ *   q, k, v, gate  in:  [B, T, H, d], shape->dtype, raw (pre-norm, pre-RoPE,
+ *                       pre-sigmoid)
+ *   gamma          in:  HOST fp32 [H]
+ *   state_in       in:  fp32 [B, H, d, d] state before token 0; NULL = zeros
+ *   state_out      out: fp32 [B, H, d, d] state after token T-1; NULL = skip;
+ *                       may be the same pointer as state_in
+ *   y              out: [B, T, H, d], shape->dtype
+ *   o              out: fp32 [B, T, H, d] mixer output before the output
+ *                       norm; NULL = skip
+ *   ws, ws_bytes   device scratch of at least hla_prefill_workspace_size()
+ *                  bytes; its contents on entry are ignored
+ *   trace          optional pass events (see hla_trace); NULL = none
+ * The output of token t depends on all tokens <= t of its sequence and on
+ * state_in; sequences and heads are independent.
+ */
+hla_status hla_prefill(const hla_shape *shape, const void *q, const void *k, const void *v,
+                       const void *gate, const float *gamma, const float *state_in,
+                       float *state_out, void *y, float *o, void *ws, size_t ws_bytes,
+                       hla_stream stream, const hla_trace *trace);
+
+/*
+ * One decode step: Eq. 18 for a single new token per sequence (shape->T must
+ * be 1).  The state is read once and written once.
+ *   q, k, v, gate  in:  [B, 1, H, d], shape->dtype
+ *   gamma          in:  HOST fp32 [H]
+ *   pos            in:  device int64 [B], RoPE position of each sequence's
+ *                       token; NULL = every sequence at shape->pos_offset
+ *   state_in       in:  fp32 [B, H, d, d] (required)
+ *   state_out      out: fp32 [B, H, d, d]; may equal state_in (in-place)
+ *   y              out: [B, 1, H, d], shape->dtype
+ *   o              out: fp32 [B, 1, H, d] before the output norm; NULL = skip
+ */
+hla_status hla_decode_step(const hla_shape *shape, const void *q, const void *k, const void *v,
+                           const void *gate, const float *gamma, const int64_t *pos,
+                           const float *state_in, float *state_out, void *y, float *o,
+                           hla_stream stream);
+
+/* Device workspace bytes hla_prefill_backward needs (0 on a bad shape). */
+size_t hla_backward_workspace_size(const hla_shape *shape);
+
+/*
+ * Backward of hla_prefill: gradients of L = <dy, y> + <dstate_out, state_out>
+ * with respect to the raw inputs (the chain rule through Eq. 18; gamma is a
+ * fixed constant of the method, Eq. 19, and gets no gradient).
+ *   q, k, v, gate, gamma, state_in   the forward call's inputs (state_in NULL = zeros)
+ *   dy          in:  [B, T, H, d], shape->dtype, gradient of y
+ *   dstate_out  in:  fp32 [B, H, d, d] gradient of state_out; NULL = zeros
+ *   dq, dk, dv, dgate  out: [B, T, H, d], shape->dtype
+ *   dstate_in   out: fp32 [B, H, d, d] gradient of state_in; NULL = skip
+ *   ws, ws_bytes     device scratch of hla_backward_workspace_size() bytes
+ * The forward quantities it needs (o and the per-chunk states) are
+ * recomputed, not stored by hla_prefill.
+ */
+hla_status hla_prefill_backward(const hla_shape *shape, const void *q, const void *k,
+                                const void *v, const void *gate, const float *gamma,
+                                const float *state_in, const void *dy, const float *dstate_out,
+                                void *dq, void *dk, void *dv, void *dgate, float *dstate_in,
+                                void *ws, size_t ws_bytes, hla_stream stream,
+                                const hla_trace *trace);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HLA_H_ */

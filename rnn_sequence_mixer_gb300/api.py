@@ -1,0 +1,182 @@
+"""PyTorch-facing binding of the C ABI (``include/hla.h``).
+
+Each function checks that its tensors are CUDA, contiguous and of one dtype,
+allocates outputs and workspace through PyTorch's caching allocator, and calls
+the library entry point of the same name on the current CUDA stream.  It does
+no arithmetic of the mixer: there is no CPU path and no fallback, and a missing
+``libhla.so`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib
+
+_DTYPES = {torch.float32: _lib.HLA_F32, torch.bfloat16: _lib.HLA_BF16}
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _host_gamma(gamma, H: int):
+    g = torch.as_tensor(gamma, dtype=torch.float32, device="cpu").contiguous()
+    if g.numel() != H:
+        raise ValueError(f"gamma must have H={H} entries, got {g.numel()}")
+    return g, ctypes.cast(ctypes.c_void_p(g.data_ptr()), ctypes.POINTER(ctypes.c_float))
+
+
+def _check_acts(*ts: torch.Tensor):
+    ref = ts[0]
+    if not ref.is_cuda:
+        raise ValueError("libhla runs on CUDA tensors only (no CPU path)")
+    if ref.dim() != 4:
+        raise ValueError("activations must be [B, T, H, d]")
+    if ref.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {ref.dtype}")
+    for t in ts:
+        if t.shape != ref.shape or t.dtype != ref.dtype or t.device != ref.device:
+            raise ValueError("q, k, v, gate (and dy) must share shape, dtype and device")
+        if not t.is_contiguous():
+            raise ValueError("activations must be contiguous")
+
+
+def _check_state(s: Optional[torch.Tensor], B, H, d, device):
+    if s is None:
+        return
+    if s.dtype != torch.float32 or not s.is_contiguous() or s.device != device:
+        raise ValueError("states are contiguous fp32 tensors on the activations' device")
+    if tuple(s.shape) != (B, H, d, d):
+        raise ValueError(f"state must be [B, H, d, d] = {(B, H, d, d)}")
+
+
+def make_shape(B, T, H, d, *, chunk=64, dtype=torch.bfloat16, pos_offset=0, rope_base=1e4,
+               eps=1e-6) -> _lib.HlaShape:
+    return _lib.HlaShape(B=B, T=T, H=H, dk=d, dv=d, chunk=chunk, dtype=_DTYPES[dtype], reserved=0,
+                         pos_offset=int(pos_offset), rope_base=float(rope_base),
+                         norm_eps=float(eps))
+
+
+def gamma_schedule(H: int) -> torch.Tensor:
+    """Eq. 19 forget rates for H heads as a host fp32 tensor (hla_gamma_schedule)."""
+    out = torch.empty(H, dtype=torch.float32)
+    st = _lib.load().hla_gamma_schedule(H, ctypes.cast(ctypes.c_void_p(out.data_ptr()),
+                                                       ctypes.POINTER(ctypes.c_float)))
+    _lib.check(st, "hla_gamma_schedule")
+    return out
+
+
+def prefill_workspace_size(shape: _lib.HlaShape) -> int:
+    return int(_lib.load().hla_prefill_workspace_size(ctypes.byref(shape)))
+
+
+def backward_workspace_size(shape: _lib.HlaShape) -> int:
+    return int(_lib.load().hla_backward_workspace_size(ctypes.byref(shape)))
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _trace(events, device):
+    """hla_trace from a list of torch.cuda.Event (None = no tracing)."""
+    if not events:
+        return None
+    if len(events) > _lib.HLA_TRACE_MAX:
+        raise ValueError(f"at most {_lib.HLA_TRACE_MAX} trace events")
+    tr = _lib.HlaTrace()
+    stream = torch.cuda.current_stream(device)
+    for i, ev in enumerate(events):
+        if not ev.cuda_event:  # torch creates the event on its first record
+            ev.record(stream)
+        tr.events[i] = ev.cuda_event
+    tr.count = len(events)
+    return ctypes.byref(tr), tr
+
+
+def prefill(q, k, v, gate, gamma: Sequence[float] | torch.Tensor, state_in=None, *, chunk=64,
+            pos_offset=0, rope_base=1e4, eps=1e-6, want_o=False, want_state=True, y=None,
+            state_out=None, workspace=None, trace=None):
+    """hla_prefill.  Returns (y, o or None, state_out or None).  ``trace``: optional
+    list of torch.cuda.Event recorded before each pass and after the last."""
+    _check_acts(q, k, v, gate)
+    B, T, H, d = q.shape
+    _check_state(state_in, B, H, d, q.device)
+    shape = make_shape(B, T, H, d, chunk=chunk, dtype=q.dtype, pos_offset=pos_offset,
+                       rope_base=rope_base, eps=eps)
+    lib = _lib.load()
+    g_host, g_ptr = _host_gamma(gamma, H)
+    if y is None:
+        y = torch.empty_like(q)
+    o = torch.empty(q.shape, dtype=torch.float32, device=q.device) if want_o else None
+    if want_state and state_out is None:
+        state_out = torch.empty((B, H, d, d), dtype=torch.float32, device=q.device)
+    if not want_state:
+        state_out = None
+    ws_bytes = prefill_workspace_size(shape)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    tr = _trace(trace, q.device)
+    st = lib.hla_prefill(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(gate), g_ptr,
+                         _ptr(state_in), _ptr(state_out), _ptr(y), _ptr(o), _ptr(workspace),
+                         workspace.numel(), _stream(q.device), tr[0] if tr else None)
+    _lib.check(st, "hla_prefill")
+    del g_host
+    return y, o, state_out
+
+
+def decode_step(q, k, v, gate, gamma, state, pos=None, *, pos_offset=0, rope_base=1e4, eps=1e-6,
+                state_out=None, want_o=False, y=None):
+    """hla_decode_step on [B, 1, H, d] rows.  ``state_out`` defaults to ``state``
+    (in-place update).  ``pos`` is an optional int64 CUDA tensor [B]."""
+    _check_acts(q, k, v, gate)
+    B, T, H, d = q.shape
+    _check_state(state, B, H, d, q.device)
+    if state_out is None:
+        state_out = state
+    _check_state(state_out, B, H, d, q.device)
+    if pos is not None and (pos.dtype != torch.int64 or not pos.is_cuda or pos.numel() != B):
+        raise ValueError("pos must be an int64 CUDA tensor with B entries")
+    shape = make_shape(B, T, H, d, dtype=q.dtype, pos_offset=pos_offset, rope_base=rope_base,
+                       eps=eps)
+    lib = _lib.load()
+    g_host, g_ptr = _host_gamma(gamma, H)
+    if y is None:
+        y = torch.empty_like(q)
+    o = torch.empty(q.shape, dtype=torch.float32, device=q.device) if want_o else None
+    st = lib.hla_decode_step(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(gate), g_ptr,
+                             _ptr(pos), _ptr(state), _ptr(state_out), _ptr(y), _ptr(o),
+                             _stream(q.device))
+    _lib.check(st, "hla_decode_step")
+    del g_host
+    return y, o, state_out
+
+
+def prefill_backward(q, k, v, gate, gamma, dy, state_in=None, dstate_out=None, *, chunk=64,
+                     pos_offset=0, rope_base=1e4, eps=1e-6, want_dstate_in=False,
+                     workspace=None, trace=None):
+    """hla_prefill_backward.  Returns (dq, dk, dv, dgate, dstate_in or None)."""
+    _check_acts(q, k, v, gate, dy)
+    B, T, H, d = q.shape
+    _check_state(state_in, B, H, d, q.device)
+    _check_state(dstate_out, B, H, d, q.device)
+    shape = make_shape(B, T, H, d, chunk=chunk, dtype=q.dtype, pos_offset=pos_offset,
+                       rope_base=rope_base, eps=eps)
+    lib = _lib.load()
+    g_host, g_ptr = _host_gamma(gamma, H)
+    dq, dk, dv, dg = (torch.empty_like(q) for _ in range(4))
+    dsi = torch.empty((B, H, d, d), dtype=torch.float32, device=q.device) if want_dstate_in else None
+    ws_bytes = backward_workspace_size(shape)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    tr = _trace(trace, q.device)
+    st = lib.hla_prefill_backward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(gate), g_ptr,
+                                  _ptr(state_in), _ptr(dy), _ptr(dstate_out), _ptr(dq), _ptr(dk),
+                                  _ptr(dv), _ptr(dg), _ptr(dsi), _ptr(workspace), workspace.numel(),
+                                  _stream(q.device), tr[0] if tr else None)
+    _lib.check(st, "hla_prefill_backward")
+    del g_host
+    return dq, dk, dv, dg, dsi

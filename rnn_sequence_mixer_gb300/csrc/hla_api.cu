@@ -1,0 +1,303 @@
+// hla_api.cu — the extern "C" entry points of libhla.so: argument validation,
+// the segment plan, workspace carving and kernel dispatch.  Nothing here
+// allocates, frees or synchronizes.
+#include <math.h>
+#include <string.h>
+
+#include <new>
+
+#include "hla_internal.cuh"
+
+namespace hla {
+
+namespace {
+
+// Target number of (b, h, segment) work units of the prefill passes: two per
+// SM of a 152-SM GB300, so both passes fill the GPU even at B = 1, H = 16.
+constexpr int kTargetUnits = 2 * 152;
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+hla_status check_shape(const hla_shape *s, bool decode) {
+  if (!s) return HLA_ERR_INVALID_ARG;
+  if (s->B < 1 || s->T < 1 || s->H < 1 || s->dk < 1 || s->dv < 1) return HLA_ERR_INVALID_ARG;
+  if (s->reserved != 0) return HLA_ERR_INVALID_ARG;
+  if (!(s->rope_base > 0.0) || !isfinite(s->rope_base)) return HLA_ERR_INVALID_ARG;
+  if (!(s->norm_eps >= 0.0f) || !isfinite(s->norm_eps)) return HLA_ERR_INVALID_ARG;
+  if (s->pos_offset < 0 || s->pos_offset > (1LL << 62) - (long long)s->T) return HLA_ERR_INVALID_ARG;
+  if (s->dtype != HLA_F32 && s->dtype != HLA_BF16) return HLA_ERR_UNSUPPORTED;
+  if (s->dk != s->dv || (s->dk != 64 && s->dk != 128)) return HLA_ERR_UNSUPPORTED;
+  if (s->H > kMaxHeads) return HLA_ERR_UNSUPPORTED;
+  if (decode) {
+    if (s->T != 1) return HLA_ERR_INVALID_ARG;
+  } else if (s->chunk != 64 && s->chunk != 128) {
+    return HLA_ERR_UNSUPPORTED;
+  }
+  // Element counts must stay well inside 64-bit and grid limits.
+  long long rows = (long long)s->B * s->T * s->H;
+  if (rows > (1LL << 40)) return HLA_ERR_UNSUPPORTED;
+  if (s->B > 65535 || s->H > 65535) return HLA_ERR_UNSUPPORTED;
+  return HLA_OK;
+}
+
+hla_status check_gamma(const float *gamma, int H) {
+  if (!gamma) return HLA_ERR_INVALID_ARG;
+  for (int h = 0; h < H; ++h)
+    if (!(gamma[h] > 0.0f && gamma[h] <= 1.0f)) return HLA_ERR_INVALID_ARG;
+  return HLA_OK;
+}
+
+hla_status need(const void *p) { return (p && aligned16(p)) ? HLA_OK : HLA_ERR_INVALID_ARG; }
+hla_status maybe(const void *p) { return (!p || aligned16(p)) ? HLA_OK : HLA_ERR_INVALID_ARG; }
+
+#define HLA_TRY(x)                          \
+  do {                                      \
+    hla_status _s = (x);                    \
+    if (_s != HLA_OK) return _s;            \
+  } while (0)
+
+#define HLA_LAUNCH(x)                                   \
+  do {                                                  \
+    cudaError_t _e = (x);                               \
+    if (_e != cudaSuccess) return HLA_ERR_CUDA;         \
+  } while (0)
+
+// Records trace->events[i] before pass i (and after the last pass).
+struct Tracer {
+  const hla_trace *t;
+  cudaStream_t st;
+  int next = 0;
+  cudaError_t mark() {
+    cudaError_t e = cudaSuccess;
+    if (t && next < t->count && next < HLA_TRACE_MAX && t->events[next])
+      e = cudaEventRecord((cudaEvent_t)t->events[next], st);
+    ++next;
+    return e;
+  }
+};
+
+hla_status check_trace(const hla_trace *t) {
+  if (t && (t->count < 0 || t->count > HLA_TRACE_MAX)) return HLA_ERR_INVALID_ARG;
+  return HLA_OK;
+}
+
+void fill_common(MixerParams &P, const hla_shape &s, const float *gamma) {
+  memset(&P, 0, sizeof(P));
+  P.B = s.B;
+  P.T = s.T;
+  P.H = s.H;
+  P.D = s.dk;
+  P.chunk = s.chunk;
+  P.pos_offset = s.pos_offset;
+  P.eps = s.norm_eps;
+  P.kscale = (float)(1.0 / sqrt((double)s.dk));
+  for (int h = 0; h < s.H; ++h) P.gamma[h] = gamma[h];
+  fill_rope(P, s.dk, s.rope_base);
+}
+
+}  // namespace
+
+Plan make_plan(const hla_shape &s) {
+  Plan p;
+  p.nchunk = ceil_div(s.T, s.chunk);
+  long long units = (long long)s.B * s.H;
+  int nseg = (int)((kTargetUnits + units - 1) / units);
+  if (nseg < 1) nseg = 1;
+  if (nseg > p.nchunk) nseg = p.nchunk;
+  int chunks_per_seg = ceil_div(p.nchunk, nseg);
+  p.nseg = ceil_div(p.nchunk, chunks_per_seg);
+  p.seg_len = chunks_per_seg * s.chunk;
+  return p;
+}
+
+size_t seg_bytes(const hla_shape &s, const Plan &p) {
+  return (size_t)s.B * s.H * p.nseg * (size_t)s.dk * s.dv * sizeof(float);
+}
+
+void fill_rope(MixerParams &P, int D, double base) {
+  // One-entry per-thread cache: the table depends only on (base, D).
+  thread_local double cached_base = -1.0;
+  thread_local int cached_D = 0;
+  thread_local unsigned long long cached[kMaxPairs];
+  if (cached_base != base || cached_D != D) {
+    const double two_pi = 6.283185307179586476925286766559;
+    for (int i = 0; i < D / 2; ++i) {
+      double u = pow(base, -2.0 * (double)i / (double)D) / two_pi;
+      u -= floor(u);
+      double scaled = ldexp(u, 64);
+      cached[i] = scaled >= 18446744073709551615.0 ? 0ull : (unsigned long long)scaled;
+    }
+    cached_base = base;
+    cached_D = D;
+  }
+  for (int i = 0; i < D / 2; ++i) P.rope_u[i] = cached[i];
+}
+
+}  // namespace hla
+
+using namespace hla;
+
+extern "C" {
+
+int hla_abi_version(void) { return HLA_ABI_VERSION; }
+
+const char *hla_status_string(hla_status s) {
+  switch (s) {
+    case HLA_OK: return "HLA_OK";
+    case HLA_ERR_INVALID_ARG: return "HLA_ERR_INVALID_ARG: invalid argument";
+    case HLA_ERR_UNSUPPORTED: return "HLA_ERR_UNSUPPORTED: unsupported shape or dtype";
+    case HLA_ERR_WORKSPACE: return "HLA_ERR_WORKSPACE: workspace missing or too small";
+    case HLA_ERR_CUDA: return "HLA_ERR_CUDA: CUDA launch failed";
+    case HLA_ERR_TIMEOUT: return "HLA_ERR_TIMEOUT: device wait timed out";
+  }
+  return "HLA_ERR_UNKNOWN";
+}
+
+hla_status hla_gamma_schedule(int32_t H, float *gamma_out) {
+  if (H < 1 || !gamma_out) return HLA_ERR_INVALID_ARG;
+  for (int h = 0; h < H; ++h)
+    gamma_out[h] = (float)exp(-pow(2.0, -8.0 * (double)(h + 1) / (double)H));
+  return HLA_OK;
+}
+
+size_t hla_prefill_workspace_size(const hla_shape *s) {
+  if (check_shape(s, false) != HLA_OK) return 0;
+  return seg_bytes(*s, make_plan(*s));
+}
+
+size_t hla_backward_workspace_size(const hla_shape *s) {
+  if (check_shape(s, false) != HLA_OK) return 0;
+  Plan p = make_plan(*s);
+  size_t rows = (size_t)s->B * s->T * s->H;
+  return 2 * seg_bytes(*s, p) + rows * (size_t)s->dv * sizeof(float);
+}
+
+hla_status hla_prefill(const hla_shape *s, const void *q, const void *k, const void *v,
+                       const void *gate, const float *gamma, const float *state_in,
+                       float *state_out, void *y, float *o, void *ws, size_t ws_bytes,
+                       hla_stream stream, const hla_trace *trace) {
+  HLA_TRY(check_shape(s, false));
+  HLA_TRY(check_gamma(gamma, s->H));
+  HLA_TRY(need(q));
+  HLA_TRY(need(k));
+  HLA_TRY(need(v));
+  HLA_TRY(need(gate));
+  HLA_TRY(need(y));
+  HLA_TRY(maybe(state_in));
+  HLA_TRY(maybe(state_out));
+  HLA_TRY(maybe(o));
+  HLA_TRY(check_trace(trace));
+  Plan plan = make_plan(*s);
+  size_t need_ws = seg_bytes(*s, plan);
+  if (!ws || !aligned16(ws) || ws_bytes < need_ws) return HLA_ERR_WORKSPACE;
+
+  MixerParams P;
+  fill_common(P, *s, gamma);
+  P.nseg = plan.nseg;
+  P.seg_len = plan.seg_len;
+  P.q = q; P.k = k; P.v = v; P.g = gate;
+  P.state_in = state_in;
+  P.state_out = state_out;
+  P.y = y;
+  P.o = o;
+  P.seg = (float *)ws;
+  cudaStream_t st = (cudaStream_t)stream;
+  Tracer tr{trace, st};
+  HLA_LAUNCH(tr.mark());
+  HLA_LAUNCH(launch_simt_seg_state(P, s->dtype, st));
+  HLA_LAUNCH(tr.mark());
+  HLA_LAUNCH(launch_state_scan(P, state_out != nullptr, st));
+  HLA_LAUNCH(tr.mark());
+  HLA_LAUNCH(launch_simt_seg_output(P, s->dtype, st));
+  HLA_LAUNCH(tr.mark());
+  return HLA_OK;
+}
+
+hla_status hla_decode_step(const hla_shape *s, const void *q, const void *k, const void *v,
+                           const void *gate, const float *gamma, const int64_t *pos,
+                           const float *state_in, float *state_out, void *y, float *o,
+                           hla_stream stream) {
+  HLA_TRY(check_shape(s, true));
+  HLA_TRY(check_gamma(gamma, s->H));
+  HLA_TRY(need(q));
+  HLA_TRY(need(k));
+  HLA_TRY(need(v));
+  HLA_TRY(need(gate));
+  HLA_TRY(need(y));
+  HLA_TRY(need(state_in));
+  HLA_TRY(need(state_out));
+  HLA_TRY(maybe(o));
+  if (pos && ((uintptr_t)pos & 7u)) return HLA_ERR_INVALID_ARG;
+  // In-place is allowed; any other overlap of the two state buffers is not.
+  size_t sb = (size_t)s->B * s->H * s->dk * s->dv * sizeof(float);
+  const char *a = (const char *)state_in, *b = (const char *)state_out;
+  if (a != b && a < b + sb && b < a + sb) return HLA_ERR_INVALID_ARG;
+  MixerParams P;
+  fill_common(P, *s, gamma);
+  P.q = q; P.k = k; P.v = v; P.g = gate;
+  P.pos = (const long long *)pos;
+  P.state_in = state_in;
+  P.state_out = state_out;
+  P.y = y;
+  P.o = o;
+  HLA_LAUNCH(launch_decode(P, s->dtype, (cudaStream_t)stream));
+  return HLA_OK;
+}
+
+hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k, const void *v,
+                                const void *gate, const float *gamma, const float *state_in,
+                                const void *dy, const float *dstate_out, void *dq, void *dk,
+                                void *dv, void *dgate, float *dstate_in, void *ws,
+                                size_t ws_bytes, hla_stream stream, const hla_trace *trace) {
+  HLA_TRY(check_shape(s, false));
+  HLA_TRY(check_gamma(gamma, s->H));
+  HLA_TRY(need(q));
+  HLA_TRY(need(k));
+  HLA_TRY(need(v));
+  HLA_TRY(need(gate));
+  HLA_TRY(need(dy));
+  HLA_TRY(need(dq));
+  HLA_TRY(need(dk));
+  HLA_TRY(need(dv));
+  HLA_TRY(need(dgate));
+  HLA_TRY(maybe(state_in));
+  HLA_TRY(maybe(dstate_out));
+  HLA_TRY(maybe(dstate_in));
+  HLA_TRY(check_trace(trace));
+  Plan plan = make_plan(*s);
+  size_t sbytes = seg_bytes(*s, plan);
+  size_t need_ws = hla_backward_workspace_size(s);
+  if (!ws || !aligned16(ws) || ws_bytes < need_ws) return HLA_ERR_WORKSPACE;
+
+  MixerParams P;
+  fill_common(P, *s, gamma);
+  P.nseg = plan.nseg;
+  P.seg_len = plan.seg_len;
+  P.q = q; P.k = k; P.v = v; P.g = gate;
+  P.state_in = state_in;
+  P.dy = dy;
+  P.dstate_out = dstate_out;
+  P.dq = dq; P.dk = dk; P.dv = dv; P.dg = dgate;
+  P.dstate_in = dstate_in;
+  P.seg = (float *)ws;
+  P.seg2 = (float *)((char *)ws + sbytes);
+  P.dO = (float *)((char *)ws + 2 * sbytes);
+  cudaStream_t st = (cudaStream_t)stream;
+  Tracer tr{trace, st};
+  HLA_LAUNCH(tr.mark());
+  HLA_LAUNCH(launch_simt_seg_state(P, s->dtype, st));
+  HLA_LAUNCH(tr.mark());
+  HLA_LAUNCH(launch_state_scan(P, false, st));
+  HLA_LAUNCH(tr.mark());
+  HLA_LAUNCH(launch_simt_bwd_dq(P, s->dtype, st));
+  HLA_LAUNCH(tr.mark());
+  HLA_LAUNCH(launch_simt_seg_gstate(P, s->dtype, st));
+  HLA_LAUNCH(tr.mark());
+  HLA_LAUNCH(launch_grad_scan(P, dstate_in != nullptr, st));
+  HLA_LAUNCH(tr.mark());
+  HLA_LAUNCH(launch_simt_bwd_dkdv(P, s->dtype, st));
+  HLA_LAUNCH(tr.mark());
+  return HLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,83 @@
+// scan.cu — fp32 scans over the segments of each (b, h) sequence.
+//
+// Forward (state_scan): segment g holds on entry its local state
+//   Delta_g = sum_{s in g} gamma^{end_g - s} k~_s^T v_s        (zero initial state)
+// and on exit the state entering it, S_g; the recurrence is the segment-level
+// form of Eq. 18 (arXiv 2601.22156, Appendix A):
+//   S_0 = state_in (or 0),   S_{g+1} = gamma^{L_g} S_g + Delta_g,
+// and S_nseg is the final state.  Every element of the d x d state is an
+// independent linear recurrence, so one thread walks one element through the
+// segments; consecutive threads own consecutive elements (coalesced).
+//
+// Backward (grad_scan) runs the mirror recurrence from the end: segment g
+// holds on entry
+//   DeltaG_g = sum_{s in g} gamma^{s - start_g + 1} q~_s^T do_s
+// and on exit E_g, the gradient reaching the state at g's last token from
+// later tokens (dstate_out for the last segment):
+//   E_{nseg-1} = dstate_out,   E_{g-1} = gamma^{L_g} E_g + DeltaG_g,
+// and dstate_in = E_{-1}.
+#include "hla_internal.cuh"
+
+namespace hla {
+
+namespace {
+
+constexpr int kScanThreads = 256;
+
+__global__ void __launch_bounds__(kScanThreads) state_scan_kernel(const MixerParams P,
+                                                                  int write_out) {
+  const size_t DD = (size_t)P.D * P.D;
+  const size_t e = (size_t)blockIdx.y * kScanThreads + threadIdx.x;
+  if (e >= DD) return;
+  const int bh = blockIdx.x;
+  const int h = bh % P.H;
+  const float l2g = log2f(P.gamma[h]);
+  const int last_len = P.T - (P.nseg - 1) * P.seg_len;
+  const float carry_full = exp2f((float)P.seg_len * l2g);
+  const float carry_last = exp2f((float)last_len * l2g);
+  float S = P.state_in ? P.state_in[(size_t)bh * DD + e] : 0.f;
+  float *seg = P.seg + (size_t)bh * P.nseg * DD + e;
+  for (int g = 0; g < P.nseg; ++g) {
+    const float delta = seg[(size_t)g * DD];
+    seg[(size_t)g * DD] = S;
+    S = fmaf(g == P.nseg - 1 ? carry_last : carry_full, S, delta);
+  }
+  if (write_out) P.state_out[(size_t)bh * DD + e] = S;
+}
+
+__global__ void __launch_bounds__(kScanThreads) grad_scan_kernel(const MixerParams P,
+                                                                 int write_out) {
+  const size_t DD = (size_t)P.D * P.D;
+  const size_t e = (size_t)blockIdx.y * kScanThreads + threadIdx.x;
+  if (e >= DD) return;
+  const int bh = blockIdx.x;
+  const int h = bh % P.H;
+  const float l2g = log2f(P.gamma[h]);
+  const int last_len = P.T - (P.nseg - 1) * P.seg_len;
+  const float carry_full = exp2f((float)P.seg_len * l2g);
+  const float carry_last = exp2f((float)last_len * l2g);
+  float E = P.dstate_out ? P.dstate_out[(size_t)bh * DD + e] : 0.f;
+  float *seg = P.seg2 + (size_t)bh * P.nseg * DD + e;
+  for (int g = P.nseg - 1; g >= 0; --g) {
+    const float delta = seg[(size_t)g * DD];
+    seg[(size_t)g * DD] = E;
+    E = fmaf(g == P.nseg - 1 ? carry_last : carry_full, E, delta);
+  }
+  if (write_out) P.dstate_in[(size_t)bh * DD + e] = E;
+}
+
+}  // namespace
+
+cudaError_t launch_state_scan(const MixerParams &P, bool write_state_out, cudaStream_t st) {
+  dim3 grid(P.B * P.H, ceil_div((long long)P.D * P.D, kScanThreads));
+  state_scan_kernel<<<grid, kScanThreads, 0, st>>>(P, write_state_out ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grad_scan(const MixerParams &P, bool write_dstate_in, cudaStream_t st) {
+  dim3 grid(P.B * P.H, ceil_div((long long)P.D * P.D, kScanThreads));
+  grad_scan_kernel<<<grid, kScanThreads, 0, st>>>(P, write_dstate_in ? 1 : 0);
+  return cudaGetLastError();
+}
+
+}  // namespace hla

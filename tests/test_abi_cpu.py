@@ -1,0 +1,177 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every entry point include/hla.h declares, computes the Eq. 19 schedule, and
+rejects bad arguments with the documented status before any launch.
+
+Every call below carries at least one invalid argument, so validation returns
+before the library touches the CUDA runtime; the fake device addresses are
+never dereferenced."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from rnn_sequence_mixer_gb300 import _lib, api, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hla.h")
+FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hla_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (hla_\w+)", out))
+    missing = set(declared_functions()) - exported
+    assert not missing, missing
+    for name in declared_functions():
+        assert hasattr(lib, name)
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.hla_abi_version() == 1
+    for code in range(6):
+        assert _lib.status_string(code).startswith("HLA_")
+    assert "UNKNOWN" in _lib.status_string(99)
+
+
+def test_gamma_schedule_matches_oracle_and_table(lib):
+    for H in (1, 2, 16, 32, 256):
+        mine = api.gamma_schedule(H).numpy()
+        ref = oracle.gamma(H).astype(np.float32)
+        assert np.max(np.abs(mine - ref) / np.spacing(ref)) <= 1.0
+    rows = [float(l) for l in open(os.path.join(ROOT, "tests", "golden", "gamma_H32.txt"))
+            if l.strip() and not l.startswith("#")]
+    table = np.array(rows, dtype=np.float32)
+    assert np.max(np.abs(api.gamma_schedule(32).numpy() - table) / np.spacing(table)) <= 1.0
+    assert lib.hla_gamma_schedule(0, None) == _lib.HLA_ERR_INVALID_ARG
+
+
+def shape(**kw):
+    base = dict(B=1, T=128, H=2, d=64, chunk=64, dtype=torch.bfloat16, pos_offset=0,
+                rope_base=1e4, eps=1e-6)
+    base.update(kw)
+    return api.make_shape(base.pop("B"), base.pop("T"), base.pop("H"), base.pop("d"), **base)
+
+
+def test_workspace_sizes():
+    s = shape(B=1, T=524288, H=16, d=128)
+    n = api.prefill_workspace_size(s)
+    assert n > 0 and n % (128 * 128 * 4) == 0
+    bw = api.backward_workspace_size(s)
+    assert bw >= 2 * n + 524288 * 16 * 128 * 4
+    bad = shape(d=96)
+    assert api.prefill_workspace_size(bad) == 0
+    assert api.backward_workspace_size(bad) == 0
+    # one segment state per (b, h, segment), at least one segment per (b, h)
+    tiny = shape(B=1, T=1, H=1, d=64)
+    assert api.prefill_workspace_size(tiny) == 64 * 64 * 4
+
+
+def _gamma(H, value=0.9):
+    arr = (ctypes.c_float * H)(*([value] * H))
+    return ctypes.cast(arr, ctypes.POINTER(ctypes.c_float)), arr
+
+
+def call_prefill(lib, s, gamma=None, q=FAKE, y=FAKE, ws=FAKE, ws_bytes=1 << 40):
+    gp, keep = _gamma(s.H) if gamma is None else gamma
+    return lib.hla_prefill(ctypes.byref(s), q, FAKE, FAKE, FAKE, gp, None, None, y, None, ws,
+                           ws_bytes, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), _lib.HLA_ERR_UNSUPPORTED),
+    (dict(chunk=32), _lib.HLA_ERR_UNSUPPORTED),
+    (dict(T=0), _lib.HLA_ERR_INVALID_ARG),
+    (dict(B=0), _lib.HLA_ERR_INVALID_ARG),
+    (dict(H=257), _lib.HLA_ERR_UNSUPPORTED),
+    (dict(pos_offset=-1), _lib.HLA_ERR_INVALID_ARG),
+    (dict(rope_base=0.0), _lib.HLA_ERR_INVALID_ARG),
+    (dict(eps=float("nan")), _lib.HLA_ERR_INVALID_ARG),
+])
+def test_prefill_rejects_bad_shapes(lib, kw, code):
+    assert call_prefill(lib, shape(**kw)) == code
+
+
+def test_prefill_rejects_bad_pointers_gamma_and_workspace(lib):
+    s = shape()
+    assert lib.hla_prefill(None, FAKE, FAKE, FAKE, FAKE, _gamma(2)[0], None, None, FAKE, None,
+                           FAKE, 1 << 40, None, None) == _lib.HLA_ERR_INVALID_ARG
+    bad_trace = _lib.HlaTrace()
+    bad_trace.count = _lib.HLA_TRACE_MAX + 1
+    assert lib.hla_prefill(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, _gamma(2)[0], None, None, FAKE,
+                           None, FAKE, 1 << 40, None,
+                           ctypes.byref(bad_trace)) == _lib.HLA_ERR_INVALID_ARG
+    assert call_prefill(lib, s, q=None) == _lib.HLA_ERR_INVALID_ARG
+    assert call_prefill(lib, s, q=FAKE + 8) == _lib.HLA_ERR_INVALID_ARG
+    assert call_prefill(lib, s, y=FAKE + 2) == _lib.HLA_ERR_INVALID_ARG
+    for bad in (0.0, -0.5, 1.0001, float("nan"), float("inf")):
+        assert call_prefill(lib, s, gamma=_gamma(2, bad)) == _lib.HLA_ERR_INVALID_ARG
+    need = api.prefill_workspace_size(s)
+    assert call_prefill(lib, s, ws=None) == _lib.HLA_ERR_WORKSPACE
+    assert call_prefill(lib, s, ws_bytes=need - 1) == _lib.HLA_ERR_WORKSPACE
+    assert call_prefill(lib, s, ws=FAKE + 4) == _lib.HLA_ERR_WORKSPACE
+    r = s
+    r.reserved = 1
+    assert call_prefill(lib, r) == _lib.HLA_ERR_INVALID_ARG
+
+
+def test_decode_rejects_bad_arguments(lib):
+    gp, keep = _gamma(2)
+    s = shape(T=2)
+    assert lib.hla_decode_step(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, gp, None, FAKE, FAKE, FAKE,
+                               None, None) == _lib.HLA_ERR_INVALID_ARG
+    s = shape(T=1)
+    # state buffers overlapping without being the same buffer
+    assert lib.hla_decode_step(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, gp, None, FAKE, FAKE + 256,
+                               FAKE, None, None) == _lib.HLA_ERR_INVALID_ARG
+    assert lib.hla_decode_step(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, gp, FAKE + 4, FAKE, FAKE,
+                               FAKE, None, None) == _lib.HLA_ERR_INVALID_ARG
+    assert lib.hla_decode_step(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, gp, None, None, FAKE, FAKE,
+                               None, None) == _lib.HLA_ERR_INVALID_ARG
+    assert lib.hla_decode_step(ctypes.byref(shape(T=1, d=32)), FAKE, FAKE, FAKE, FAKE, gp, None,
+                               FAKE, FAKE, FAKE, None, None) == _lib.HLA_ERR_UNSUPPORTED
+
+
+def test_backward_rejects_bad_arguments(lib):
+    gp, keep = _gamma(2)
+    s = shape()
+    need = api.backward_workspace_size(s)
+    args = lambda **kw: [kw.get(n, FAKE) for n in ("q", "k", "v", "g")]
+    assert lib.hla_prefill_backward(ctypes.byref(s), *args(), gp, None, FAKE, None, FAKE, FAKE,
+                                    FAKE, FAKE, None, FAKE, need - 16,
+                                    None, None) == _lib.HLA_ERR_WORKSPACE
+    assert lib.hla_prefill_backward(ctypes.byref(s), *args(), gp, None, None, None, FAKE, FAKE,
+                                    FAKE, FAKE, None, FAKE, need, None,
+                                    None) == _lib.HLA_ERR_INVALID_ARG
+    assert lib.hla_prefill_backward(ctypes.byref(s), *args(), gp, None, FAKE, None, FAKE, FAKE,
+                                    FAKE, FAKE + 1, None, FAKE, need,
+                                    None, None) == _lib.HLA_ERR_INVALID_ARG
+
+
+def test_python_api_has_no_cpu_path():
+    x = torch.zeros(1, 4, 2, 64)
+    with pytest.raises(ValueError):
+        api.prefill(x, x, x, x, [0.5, 0.5])
+    with pytest.raises(ValueError):
+        api.decode_step(x[:, :1], x[:, :1], x[:, :1], x[:, :1], [0.5, 0.5],
+                        torch.zeros(1, 2, 64, 64))
