@@ -43,6 +43,8 @@ def parse():
     p.add_argument("--no-backward", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle sample")
+    p.add_argument("--prefill-T", type=int, default=0,
+                   help="override T of the prefill workload (small cases for ncu captures)")
     return p.parse_args()
 
 
@@ -241,6 +243,9 @@ def run_ours(args):
 
     # ---------------------------------------------------------------- prefill @512K
     w = workloads.PREFILL_512K
+    if args.prefill_T:
+        import dataclasses
+        w = dataclasses.replace(w, T=args.prefill_T, name=f"prefill_B1_T{args.prefill_T}_H16_d128_bf16")
     gam = api.gamma_schedule(w.H)
     inp = inputs.mixer_inputs(w.B, w.T, w.H, w.d, w.dtype, w.seed + 1000 * D.rank, device=dev)
     y = torch.empty_like(inp["q"])
