@@ -135,6 +135,39 @@ hla_status hla_prefill(const hla_shape *shape, const void *q, const void *k, con
                        hla_stream stream, const hla_trace *trace);
 
 /*
+ * hla_prefill for callers that cannot allocate device memory.  The paper has
+ * no counterpart to this entry point; it exists for deployments where the
+ * caller may not call cudaMalloc: a plugin inside an engine that owns all
+ * device memory through its own pool, a serving loop that must not allocate
+ * (or risk an allocation failure or an implicit synchronization) once it is
+ * running, or a certified build that forbids allocation after start-up.
+ *
+ * Same arguments and results as hla_prefill, minus the workspace: the
+ * per-segment states live in a fixed scratch array of
+ * HLA_NOALLOC_SCRATCH_BYTES inside the library's own device memory, which
+ * every GPU that loads the library holds until the process exits.  The call
+ * allocates nothing.
+ *   - Limit: B * H * d * d * 4 bytes (one fp32 state per sequence and head)
+ *     must fit in HLA_NOALLOC_SCRATCH_BYTES, i.e. B * H <= 512 at d = 128;
+ *     larger problems return HLA_ERR_WORKSPACE before anything is launched.
+ *     Within the limit the T axis is cut into fewer, longer segments when
+ *     needed, so results match hla_prefill up to fp32 rounding.
+ *   - Set-up: the first call on a device looks up that device's address of
+ *     the scratch array (cudaGetSymbolAddress, with the device current) and
+ *     caches it; make that first call before any stream capture.
+ *   - Sharing: every call on a device uses the same scratch array, which keeps
+ *     the last call's contents (the first pass overwrites all of it, so
+ *     nothing needs clearing).  Calls that overlap on the GPU race on it:
+ *     the caller must not run two of them at the same time on one device
+ *     (different streams or threads included).
+ */
+#define HLA_NOALLOC_SCRATCH_BYTES (32u << 20)
+hla_status hla_prefill_noalloc(const hla_shape *shape, const void *q, const void *k,
+                               const void *v, const void *gate, const float *gamma,
+                               const float *state_in, float *state_out, void *y, float *o,
+                               hla_stream stream);
+
+/*
  * One decode step: Eq. 18 for a single new token per sequence (shape->T must
  * be 1).  The state is read once and written once.
  *   q, k, v, gate  in:  [B, 1, H, d], shape->dtype

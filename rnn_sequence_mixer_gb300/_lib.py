@@ -28,6 +28,7 @@ EXPORTS = (
     "hla_decode_step",
     "hla_backward_workspace_size",
     "hla_prefill_backward",
+    "hla_prefill_noalloc",
 )
 
 
@@ -98,6 +99,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.hla_prefill_backward.restype = ctypes.c_int
     lib.hla_prefill_backward.argtypes = [shp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_float), f32p,
                                          vp, f32p, vp, vp, vp, vp, f32p, vp, sz, vp, trp]
+    lib.hla_prefill_noalloc.restype = ctypes.c_int
+    lib.hla_prefill_noalloc.argtypes = [shp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_float), f32p,
+                                        f32p, vp, f32p, vp]
     _lib = lib
     return lib
 

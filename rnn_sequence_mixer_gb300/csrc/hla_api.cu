@@ -16,6 +16,8 @@ namespace {
 // SM of a 152-SM GB300, so both passes fill the GPU even at B = 1, H = 16.
 constexpr int kTargetUnits = 2 * 152;
 
+}  // namespace
+
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 hla_status check_shape(const hla_shape *s, bool decode) {
@@ -50,6 +52,8 @@ hla_status check_gamma(const float *gamma, int H) {
 hla_status need(const void *p) { return (p && aligned16(p)) ? HLA_OK : HLA_ERR_INVALID_ARG; }
 hla_status maybe(const void *p) { return (!p || aligned16(p)) ? HLA_OK : HLA_ERR_INVALID_ARG; }
 
+namespace {
+
 #define HLA_TRY(x)                          \
   do {                                      \
     hla_status _s = (x);                    \
@@ -81,6 +85,8 @@ hla_status check_trace(const hla_trace *t) {
   return HLA_OK;
 }
 
+}  // namespace
+
 void fill_common(MixerParams &P, const hla_shape &s, const float *gamma) {
   memset(&P, 0, sizeof(P));
   P.B = s.B;
@@ -94,8 +100,6 @@ void fill_common(MixerParams &P, const hla_shape &s, const float *gamma) {
   for (int h = 0; h < s.H; ++h) P.gamma[h] = gamma[h];
   fill_rope(P, s.dk, s.rope_base);
 }
-
-}  // namespace
 
 Plan make_plan(const hla_shape &s) {
   Plan p;

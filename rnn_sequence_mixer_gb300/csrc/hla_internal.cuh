@@ -93,6 +93,12 @@ __device__ __forceinline__ float gpow(float log2g, float m) { return exp2f(m * l
 // ------------------------------------------------------------------ host side
 
 Plan make_plan(const hla_shape &s);
+bool aligned16(const void *p);
+hla_status check_shape(const hla_shape *s, bool decode);
+hla_status check_gamma(const float *gamma, int H);
+hla_status need(const void *p);
+hla_status maybe(const void *p);
+void fill_common(MixerParams &P, const hla_shape &s, const float *gamma);
 size_t seg_bytes(const hla_shape &s, const Plan &p);
 void fill_rope(MixerParams &P, int D, double base);
 
