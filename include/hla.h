@@ -124,7 +124,11 @@ size_t hla_prefill_workspace_size(const hla_shape *shape);
  *   o              out: fp32 [B, T, H, d] mixer output before the output
  *                       norm; NULL = skip
  *   ws, ws_bytes   device scratch of at least hla_prefill_workspace_size()
- *                  bytes; its contents on entry are ignored
+ *                  bytes; its contents on entry are ignored.  Its last 256
+ *                  bytes hold a uint32 device status word, cleared by the
+ *                  call: non-zero after the call completes means a bounded
+ *                  device-side wait gave up (HLA_ERR_TIMEOUT) and the outputs
+ *                  of the affected segments are not valid
  *   trace          optional pass events (see hla_trace); NULL = none
  * The output of token t depends on all tokens <= t of its sequence and on
  * state_in; sequences and heads are independent.

@@ -12,9 +12,10 @@ namespace hla {
 
 namespace {
 
-// Target number of (b, h, segment) work units of the prefill passes: two per
-// SM of a 152-SM GB300, so both passes fill the GPU even at B = 1, H = 16.
-constexpr int kTargetUnits = 2 * 152;
+// Target number of (b, h, segment) work units of the prefill passes: four per
+// SM of a 152-SM GB300 (one resident CTA per SM in the tensor-core passes), so
+// a single long sequence with 16 heads still fills every SM in equal waves.
+constexpr int kTargetUnits = 4 * 152;
 
 }  // namespace
 
@@ -166,7 +167,7 @@ hla_status hla_gamma_schedule(int32_t H, float *gamma_out) {
 
 size_t hla_prefill_workspace_size(const hla_shape *s) {
   if (check_shape(s, false) != HLA_OK) return 0;
-  return seg_bytes(*s, make_plan(*s));
+  return seg_bytes(*s, make_plan(*s)) + kStatusBytes;
 }
 
 size_t hla_backward_workspace_size(const hla_shape *s) {
@@ -192,7 +193,7 @@ hla_status hla_prefill(const hla_shape *s, const void *q, const void *k, const v
   HLA_TRY(maybe(o));
   HLA_TRY(check_trace(trace));
   Plan plan = make_plan(*s);
-  size_t need_ws = seg_bytes(*s, plan);
+  size_t need_ws = seg_bytes(*s, plan) + kStatusBytes;
   if (!ws || !aligned16(ws) || ws_bytes < need_ws) return HLA_ERR_WORKSPACE;
 
   MixerParams P;
@@ -205,14 +206,17 @@ hla_status hla_prefill(const hla_shape *s, const void *q, const void *k, const v
   P.y = y;
   P.o = o;
   P.seg = (float *)ws;
+  P.err = (unsigned int *)((char *)ws + seg_bytes(*s, plan));
   cudaStream_t st = (cudaStream_t)stream;
+  const bool tc = tc_supported(P, s->dtype);
   Tracer tr{trace, st};
+  HLA_LAUNCH(cudaMemsetAsync(P.err, 0, sizeof(unsigned int), st));
   HLA_LAUNCH(tr.mark());
-  HLA_LAUNCH(launch_simt_seg_state(P, s->dtype, st));
+  HLA_LAUNCH(tc ? launch_tc_seg_state(P, st) : launch_simt_seg_state(P, s->dtype, st));
   HLA_LAUNCH(tr.mark());
   HLA_LAUNCH(launch_state_scan(P, state_out != nullptr, st));
   HLA_LAUNCH(tr.mark());
-  HLA_LAUNCH(launch_simt_seg_output(P, s->dtype, st));
+  HLA_LAUNCH(tc ? launch_tc_seg_output(P, st) : launch_simt_seg_output(P, s->dtype, st));
   HLA_LAUNCH(tr.mark());
   return HLA_OK;
 }

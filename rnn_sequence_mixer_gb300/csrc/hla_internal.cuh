@@ -38,6 +38,7 @@ struct MixerParams {
   const float *dstate_out;
   void *dq, *dk, *dv, *dg;
   float *dstate_in;
+  unsigned int *err;       // device status word: bits set when a bounded wait gave up
   float gamma[kMaxHeads];
   // RoPE phase increment of pair i, in units of 2^-64 turns:
   // round(frac(rope_base^(-2i/D) / (2 pi)) * 2^64).  The angle of position p is
@@ -111,5 +112,11 @@ cudaError_t launch_simt_seg_output(const MixerParams &P, int dtype, cudaStream_t
 cudaError_t launch_simt_bwd_dq(const MixerParams &P, int dtype, cudaStream_t st);
 cudaError_t launch_simt_seg_gstate(const MixerParams &P, int dtype, cudaStream_t st);
 cudaError_t launch_simt_bwd_dkdv(const MixerParams &P, int dtype, cudaStream_t st);
+bool tc_supported(const MixerParams &P, int dtype);
+cudaError_t launch_tc_seg_state(const MixerParams &P, cudaStream_t st);
+cudaError_t launch_tc_seg_output(const MixerParams &P, cudaStream_t st);
+
+// Bytes reserved at the end of a workspace for the device status word.
+constexpr size_t kStatusBytes = 256;
 
 }  // namespace hla

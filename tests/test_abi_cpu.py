@@ -76,15 +76,15 @@ def shape(**kw):
 def test_workspace_sizes():
     s = shape(B=1, T=524288, H=16, d=128)
     n = api.prefill_workspace_size(s)
-    assert n > 0 and n % (128 * 128 * 4) == 0
+    assert n > 256 and (n - 256) % (128 * 128 * 4) == 0
     bw = api.backward_workspace_size(s)
-    assert bw >= 2 * n + 524288 * 16 * 128 * 4
+    assert bw >= 2 * (n - 256) + 524288 * 16 * 128 * 4
     bad = shape(d=96)
     assert api.prefill_workspace_size(bad) == 0
     assert api.backward_workspace_size(bad) == 0
     # one segment state per (b, h, segment), at least one segment per (b, h)
     tiny = shape(B=1, T=1, H=1, d=64)
-    assert api.prefill_workspace_size(tiny) == 64 * 64 * 4
+    assert api.prefill_workspace_size(tiny) == 64 * 64 * 4 + 256
 
 
 def _gamma(H, value=0.9):

@@ -139,3 +139,19 @@ def test_prefill_512k_workload_sampled(dev):
     assert_state_close(gather_state(st, pairs), rs, 2e-2, "final state")
     del inp, y, st
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64)])
+def test_status_word_is_clear(dev, dtype, d):
+    """The last 256 bytes of the workspace hold the device status word; it is
+    cleared by every call and stays 0 when no bounded wait gave up."""
+    B, T, H = 1, 3000, 8
+    inp = inputs.mixer_inputs(B, T, H, d, dtype, 77, device=dev)
+    shape = api.make_shape(B, T, H, d, chunk=128, dtype=dtype)
+    n = api.prefill_workspace_size(shape)
+    ws = torch.full((n,), 0xAB, dtype=torch.uint8, device=dev)
+    api.prefill(inp["q"], inp["k"], inp["v"], inp["gate"], torch.from_numpy(gamma32(H)),
+                chunk=128, workspace=ws)
+    torch.cuda.synchronize()
+    status = ws[n - 256:n - 252].view(torch.int32).item()
+    assert status == 0
