@@ -3,13 +3,18 @@
 // The chunked form of Eq. 18 (arXiv 2601.22156, Appendix A): for a tile of
 // c <= 128 tokens entering with state S,
 //   P     = Q~ K~^T                                  MMA1  (M=128, N=128, K=d)
-//   O_int = Q~ S                                     MMA2  (K = d_k, S as bf16)
+//   O_int = Q~ S                                     MMA2  (K = d_k)
 //   S'    = gamma^c S + (diag(gamma^{c-1-j}) K~)^T V MMA4  (accumulated onto S in TMEM)
 //   O_in  = (P (.) D) V,  D_ij = gamma^{i-j}, i >= j MMA3
 //   o_i   = gamma^{i+1} O_int[i] + O_in[i],  y = Norm(o) * sigmoid(gate)
 // The accumulators (P, O_int, O_in and the fp32 state S) live in the 512
-// columns of tensor memory; operands are bf16 tiles in shared memory in the
-// 128-byte-swizzled layout of umma.cuh.  One CTA of 512 threads owns one
+// columns of tensor memory; operands are 16-bit tiles in shared memory in the
+// 128-byte-swizzled layout of umma.cuh.  Q~, K~ and S enter MMA1/MMA2 as fp16
+// (11-bit significand): with bf16 there, the rounding of q~ . k~ dominates the
+// error of y wherever o nearly cancels (fast-decaying heads), which fp16 cuts
+// fourfold.  S is scaled by a power of two into fp16 range each tile and the
+// scale is undone in the epilogue.  P (.) D, K~dec and V stay bf16 (V is a
+// bf16 input; MMA3/MMA4 run bf16 x bf16).  One CTA of 512 threads owns one
 // (b, h, segment); every CUDA-core phase maps thread (warp w, lane l) to tile
 // row i = 32 (w % 4) + l and column quarter (w / 4), which is also the TMEM
 // lane / column block that warp may access.  Thread 0 issues the MMAs.
@@ -20,6 +25,8 @@
 //                     decay weight of every key row is folded into K~).
 //   tc_output_kernel: the outputs of the segment from the entering state
 //                     written by the fp32 scan (scan.cu).
+#include <cuda_fp16.h>
+
 #include "hla_internal.cuh"
 #include "umma.cuh"
 
@@ -53,6 +60,16 @@ __device__ __forceinline__ uint4 pack8(const float *f) {
   return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
 }
 
+__device__ __forceinline__ uint32_t pack2h(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint4 pack8h(const float *f) {
+  return make_uint4(pack2h(f[0], f[1]), pack2h(f[2], f[3]), pack2h(f[4], f[5]),
+                    pack2h(f[6], f[7]));
+}
+
 __device__ __forceinline__ void st_tile(unsigned char *tile, int row, int chunk, const uint4 &v) {
   *reinterpret_cast<uint4 *>(tile + umma::sw128_off(row, chunk, ROWS)) = v;
 }
@@ -73,6 +90,7 @@ struct Shared {
   float red_o[4][ROWS];
   float2 rb[D / 2];
   float pw[ROWS + 1];
+  float smax[NT / 32];
   uint64_t bar[2];
   uint32_t tmem_base;
 };
@@ -127,19 +145,20 @@ __device__ __forceinline__ void rotate(const uint4 (&r)[4], float scale, const f
   }
 }
 
-// Store 32 values (pairs lo/hi of this thread) into a K-major feature tile row.
+// Store 32 values (pairs lo/hi of this thread) into a K-major feature tile
+// row, as bf16 or (half = true) fp16.
 __device__ __forceinline__ void store_pairs(unsigned char *tile, int row, int qd,
                                             const float (&lo)[16], const float (&hi)[16],
-                                            float mul) {
+                                            float mul, bool half = false) {
   float t[16];
 #pragma unroll
   for (int u = 0; u < 16; ++u) t[u] = lo[u] * mul;
-  st_tile(tile, row, 2 * qd, pack8(&t[0]));
-  st_tile(tile, row, 2 * qd + 1, pack8(&t[8]));
+  st_tile(tile, row, 2 * qd, half ? pack8h(&t[0]) : pack8(&t[0]));
+  st_tile(tile, row, 2 * qd + 1, half ? pack8h(&t[8]) : pack8(&t[8]));
 #pragma unroll
   for (int u = 0; u < 16; ++u) t[u] = hi[u] * mul;
-  st_tile(tile, row, 8 + 2 * qd, pack8(&t[0]));
-  st_tile(tile, row, 9 + 2 * qd, pack8(&t[8]));
+  st_tile(tile, row, 8 + 2 * qd, half ? pack8h(&t[0]) : pack8(&t[0]));
+  st_tile(tile, row, 9 + 2 * qd, half ? pack8h(&t[8]) : pack8(&t[8]));
 }
 
 __device__ __forceinline__ void sync_tc() {
@@ -306,9 +325,10 @@ __global__ void __launch_bounds__(NT, 1) tc_output_kernel(const __grid_constant_
     umma::tmem_wait_st();
   }
 
-  const uint32_t id_qk = umma::idesc_bf16(128, 128, false, false);
-  const uint32_t id_kn = umma::idesc_bf16(128, 128, false, true);
-  const uint32_t id_mn = umma::idesc_bf16(128, 128, true, true);
+  const uint32_t id_qk = umma::idesc_bf16(128, 128, false, false, true);  // fp16 Q~ K~^T
+  const uint32_t id_qs = umma::idesc_bf16(128, 128, false, true, true);   // fp16 Q~ S
+  const uint32_t id_pv = umma::idesc_bf16(128, 128, false, true);         // bf16 Pm V
+  const uint32_t id_mn = umma::idesc_bf16(128, 128, true, true);          // bf16 K~dec^T V
   const int ntile = ceil_div(t1 - t0, CV);
   uint4 qr[4], kr[4];
   {
@@ -329,20 +349,44 @@ __global__ void __launch_bounds__(NT, 1) tc_output_kernel(const __grid_constant_
     }
     uint4 vr[4];
     load_quarter(vr, row_ptr(P.v, P, b, h, valid ? c0 + i : c0), qd, valid);
-    // State phase: S (fp32, TMEM) -> bf16 operand tile Sb; S <- gamma^c S.
+    // State phase, part 1: max |S| over the tile (S is fp32 in TMEM).
     {
       float v[32];
       umma::tmem_ld32(tS + lane_base + 32 * qd, v);
+      float m = 0.f;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) st_tile(Sb, i, 4 * qd + u, pack8(&v[8 * u]));
-      const float carry = sh.pw[c];
+      for (int e = 0; e < 32; ++e) m = fmaxf(m, fabsf(v[e]));
 #pragma unroll
-      for (int e = 0; e < 32; ++e) v[e] *= carry;
-      umma::tmem_st32(tS + lane_base + 32 * qd, v);
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) sh.smax[warp] = m;
     }
     sh.red_q[qd][i] = sumsq_pairs(qr);
     sh.red_k[qd][i] = sumsq_pairs(kr);
     __syncthreads();
+    // State phase, part 2: Sb = fp16(S * 2^-e) with 2^e >= max |S|; then S <- gamma^c S.
+    float s_inv;  // 2^e: multiplies Q~ Sb back to the scale of S
+    {
+      float m = 0.f;
+#pragma unroll
+      for (int w = 0; w < NT / 32; ++w) m = fmaxf(m, sh.smax[w]);
+      int e = 0;
+      if (m > 0.f) frexpf(m, &e);
+      const float s_fwd = ldexpf(1.f, -e);
+      s_inv = ldexpf(1.f, e);
+      float v[32];
+      umma::tmem_ld32(tS + lane_base + 32 * qd, v);
+      float t[8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+#pragma unroll
+        for (int e2 = 0; e2 < 8; ++e2) t[e2] = v[8 * u + e2] * s_fwd;
+        st_tile(Sb, i, 4 * qd + u, pack8h(t));
+      }
+      const float carry = sh.pw[c];
+#pragma unroll
+      for (int e2 = 0; e2 < 32; ++e2) v[e2] *= carry;
+      umma::tmem_st32(tS + lane_base + 32 * qd, v);
+    }
     // Feature map: q~ = RoPE(Norm(q)), k~ = RoPE(Norm(k)) / sqrt(d), k~dec = gamma^{c-1-i} k~.
     {
       const float rq = rsqrtf((sh.red_q[0][i] + sh.red_q[1][i] + sh.red_q[2][i] + sh.red_q[3][i]) /
@@ -358,9 +402,9 @@ __global__ void __launch_bounds__(NT, 1) tc_output_kernel(const __grid_constant_
       }
       float lo[16], hi[16];
       rotate(qr, rq, cs, sn, lo, hi);
-      store_pairs(Qt, i, qd, lo, hi, 1.f);
+      store_pairs(Qt, i, qd, lo, hi, 1.f, true);
       rotate(kr, rk * P.kscale, cs, sn, lo, hi);
-      store_pairs(Kt, i, qd, lo, hi, 1.f);
+      store_pairs(Kt, i, qd, lo, hi, 1.f, true);
       store_pairs(Kd, i, qd, lo, hi, valid ? sh.pw[c - 1 - i] : 0.f);
 #pragma unroll
       for (int u = 0; u < 4; ++u) st_tile(Vs, i, 4 * qd + u, vr[u]);
@@ -384,7 +428,7 @@ __global__ void __launch_bounds__(NT, 1) tc_output_kernel(const __grid_constant_
                      kk > 0);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        umma::mma_ss(tOi, umma::desc_kmajor(aq, kk, ROWS), umma::desc_mnmajor(as, kk, ROWS), id_kn,
+        umma::mma_ss(tOi, umma::desc_kmajor(aq, kk, ROWS), umma::desc_mnmajor(as, kk, ROWS), id_qs,
                      kk > 0);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
@@ -420,7 +464,7 @@ __global__ void __launch_bounds__(NT, 1) tc_output_kernel(const __grid_constant_
       const uint32_t ap = umma::smem_u32(Pm), av = umma::smem_u32(Vs);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        umma::mma_ss(tOa, umma::desc_kmajor(ap, kk, ROWS), umma::desc_mnmajor(av, kk, ROWS), id_kn,
+        umma::mma_ss(tOa, umma::desc_kmajor(ap, kk, ROWS), umma::desc_mnmajor(av, kk, ROWS), id_pv,
                      kk > 0);
       umma::commit(&sh.bar[1]);
     }
@@ -438,7 +482,7 @@ __global__ void __launch_bounds__(NT, 1) tc_output_kernel(const __grid_constant_
       float a[32];
       umma::tmem_ld32(tOi + lane_base + 32 * qd, a);
       umma::tmem_ld32(tOa + lane_base + 32 * qd, o);
-      const float inter = sh.pw[i + 1];
+      const float inter = sh.pw[i + 1] * s_inv;
       float ss = 0.f;
 #pragma unroll
       for (int e = 0; e < 32; ++e) {

@@ -54,11 +54,13 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk, int rows
   return make_desc(addr, (uint32_t)(rows * 128), 1024);
 }
 
-// Instruction descriptor of kind::f16 with bf16 A/B and fp32 accumulation.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4)                     // D format: fp32
-         | (1u << 7)                   // A format: bf16
-         | (1u << 10)                  // B format: bf16
+// Instruction descriptor of kind::f16 with fp32 accumulation; A and B are
+// both bf16 (fp16 = false) or both fp16 (fp16 = true).
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn,
+                                                  bool fp16 = false) {
+  return (1u << 4)                          // D format: fp32
+         | ((fp16 ? 0u : 1u) << 7)          // A format: 0 = fp16, 1 = bf16
+         | ((fp16 ? 0u : 1u) << 10)         // B format
          | ((a_mn ? 1u : 0u) << 15)    // A major: 0 = K, 1 = MN
          | ((b_mn ? 1u : 0u) << 16)    // B major
          | ((uint32_t)(N >> 3) << 17)  // N / 8
