@@ -3,28 +3,35 @@
 // The chunked form of Eq. 18 (arXiv 2601.22156, Appendix A): for a tile of
 // c <= 128 tokens entering with state S,
 //   P     = Q~ K~^T                                  MMA1  (M=128, N=128, K=d)
-//   O_int = Q~ S                                     MMA2  (K = d_k)
-//   S'    = gamma^c S + (diag(gamma^{c-1-j}) K~)^T V MMA4  (accumulated onto S in TMEM)
-//   O_in  = (P (.) D) V,  D_ij = gamma^{i-j}, i >= j MMA3
-//   o_i   = gamma^{i+1} O_int[i] + O_in[i],  y = Norm(o) * sigmoid(gate)
-// The accumulators (P, O_int, O_in and the fp32 state S) live in the 512
-// columns of tensor memory; operands are 16-bit tiles in shared memory in the
-// 128-byte-swizzled layout of umma.cuh.  Q~, K~ and S enter MMA1/MMA2 as fp16
-// (11-bit significand): with bf16 there, the rounding of q~ . k~ dominates the
-// error of y wherever o nearly cancels (fast-decaying heads), which fp16 cuts
-// fourfold.  S is scaled by a power of two into fp16 range each tile and the
-// scale is undone in the epilogue.  P (.) D, K~dec and V stay bf16 (V is a
-// bf16 input; MMA3/MMA4 run bf16 x bf16).  One CTA of 512 threads owns one
-// (b, h, segment); every CUDA-core phase maps thread (warp w, lane l) to tile
-// row i = 32 (w % 4) + l and column quarter (w / 4), which is also the TMEM
-// lane / column block that warp may access.  Thread 0 issues the MMAs.
+//   O     = Q~ S                                     MMA2  (K = d_k)
+//   O    <- diag(gamma^{i+1}) O  (in TMEM), then
+//   O    += (P (.) D) V,   D_ij = gamma^{i-j}, i >= j MMA3
+//   S    <- gamma^c S + (diag(gamma^{c-1-j}) K~)^T V  MMA4  (accumulated onto S in TMEM)
+//   y_i   = Norm(o_i) * sigmoid(gate_i)
+// Accumulators live in the 512 columns of tensor memory: P, two O buffers
+// (tile n accumulates while tile n - 1 drains) and the fp32 state S.
+// Operands are 16-bit tiles in shared memory in the 128-byte-swizzled layout
+// of umma.cuh.  Raw q, k and v tiles arrive by TMA straight into the operand
+// buffers and are transformed in place (q -> q~, k -> k~ -> k~dec), so no
+// register ever waits on a global load.
 //
-//   tc_state_kernel:  the segment's local state, S_seg = sum over its tokens
-//                     of gamma^{end-s} k~_s^T v_s, one MMA per tile
-//                     accumulated in TMEM (no rescaling between tiles: the
-//                     decay weight of every key row is folded into K~).
+// Precision: Q~, K~ and S enter MMA1/MMA2 as fp16 (11-bit significand).  With
+// bf16 there, the rounding of q~ . k~ dominates the error of y wherever o
+// nearly cancels (fast-decaying heads); fp16 cuts that fourfold.  S is scaled
+// by a power of two into fp16 range each tile and the scale is undone on O.
+// P (.) D, K~dec and V stay bf16 (V is a bf16 input; MMA3/MMA4 run bf16).
+//
+// Threads: one CTA of 512 per (b, h, segment).  Every CUDA-core phase maps
+// thread (warp w, lane l) to tile row i = 32 (w % 4) + l and column quarter
+// qd = w / 4, which is also the TMEM lane and column block that warp may
+// access.  Thread 0 issues the TMA copies and the MMAs.
+//
+//   tc_state_kernel:  the segment's local state, sum over its tokens of
+//                     gamma^{end-s} k~_s^T v_s, one MMA per tile accumulated in
+//                     TMEM (the decay weight of each key row is folded into K~).
 //   tc_output_kernel: the outputs of the segment from the entering state
 //                     written by the fp32 scan (scan.cu).
+#include <cuda.h>
 #include <cuda_fp16.h>
 
 #include "hla_internal.cuh"
@@ -36,9 +43,10 @@ namespace tc {
 namespace {
 
 constexpr int D = 128;
-constexpr int ROWS = 128;       // rows of every operand tile
-constexpr int NT = 512;         // threads per CTA
-constexpr int TILE = ROWS * D * 2;  // bytes of one bf16 tile (32 KiB)
+constexpr int ROWS = 128;           // rows of every operand tile
+constexpr int NT = 512;             // threads per CTA
+constexpr int TILE = ROWS * D * 2;  // bytes of one 16-bit tile (32 KiB)
+constexpr int HALF_TILE = TILE / 2; // one 64-column block
 
 // ------------------------------------------------------------------ small helpers
 
@@ -51,69 +59,61 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
   }
 }
 
+__device__ __forceinline__ void unpack8h(const uint4 &u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t *>(&h);
 }
-
 __device__ __forceinline__ uint4 pack8(const float *f) {
   return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
 }
-
 __device__ __forceinline__ uint32_t pack2h(float a, float b) {
   __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t *>(&h);
 }
-
 __device__ __forceinline__ uint4 pack8h(const float *f) {
   return make_uint4(pack2h(f[0], f[1]), pack2h(f[2], f[3]), pack2h(f[4], f[5]),
                     pack2h(f[6], f[7]));
 }
 
-__device__ __forceinline__ void st_tile(unsigned char *tile, int row, int chunk, const uint4 &v) {
-  *reinterpret_cast<uint4 *>(tile + umma::sw128_off(row, chunk, ROWS)) = v;
+__device__ __forceinline__ uint4 *tile_at(unsigned char *tile, int row, int chunk) {
+  return reinterpret_cast<uint4 *>(tile + umma::sw128_off(row, chunk, ROWS));
 }
 
 __device__ __forceinline__ uint4 ldg16(const void *p) {
   return __ldg(reinterpret_cast<const uint4 *>(p));
 }
 
-// Row `i` of token tile starting at c0 of a [B, T, H, D] bf16 tensor, uint4 index u (0..15).
+// Row t of a [B, T, H, D] bf16 tensor for (b, h).
 __device__ __forceinline__ const __nv_bfloat16 *row_ptr(const void *X, const MixerParams &P, int b,
                                                         int h, long long t) {
   return (const __nv_bfloat16 *)X + (((size_t)b * P.T + t) * P.H + h) * D;
 }
 
-struct Shared {
-  float red_q[4][ROWS];
-  float red_k[4][ROWS];
-  float red_o[4][ROWS];
-  float2 rb[D / 2];
-  float pw[ROWS + 1];
-  float smax[NT / 32];
-  uint64_t bar[2];
-  uint32_t tmem_base;
-};
-
-// Loads of this thread's part of a q or k row: elements [16 qd, 16 qd + 16)
-// and [64 + 16 qd, 64 + 16 qd + 16) (the two halves of its 16 RoPE pairs).
-__device__ __forceinline__ void load_pairs(uint4 (&r)[4], const __nv_bfloat16 *row, int qd,
-                                           bool valid) {
-  if (valid) {
-    r[0] = ldg16(row + 16 * qd);
-    r[1] = ldg16(row + 16 * qd + 8);
-    r[2] = ldg16(row + 64 + 16 * qd);
-    r[3] = ldg16(row + 64 + 16 * qd + 8);
-  } else {
-    r[0] = r[1] = r[2] = r[3] = make_uint4(0, 0, 0, 0);
-  }
-}
-
-// Loads of elements [32 qd, 32 qd + 32) of a row.
+// Elements [32 qd, 32 qd + 32) of a row.
 __device__ __forceinline__ void load_quarter(uint4 (&r)[4], const __nv_bfloat16 *row, int qd,
                                              bool valid) {
 #pragma unroll
   for (int u = 0; u < 4; ++u) r[u] = valid ? ldg16(row + 32 * qd + 8 * u) : make_uint4(0, 0, 0, 0);
+}
+
+// This thread's 16 RoPE pairs of a row sit in chunks {2qd, 2qd+1} (elements
+// 16qd..16qd+15) and {8+2qd, 9+2qd} (elements 64+16qd..): read them from an
+// operand tile.
+__device__ __forceinline__ void ld_pairs(unsigned char *tile, int row, int qd, uint4 (&r)[4]) {
+  r[0] = *tile_at(tile, row, 2 * qd);
+  r[1] = *tile_at(tile, row, 2 * qd + 1);
+  r[2] = *tile_at(tile, row, 8 + 2 * qd);
+  r[3] = *tile_at(tile, row, 9 + 2 * qd);
 }
 
 __device__ __forceinline__ float sumsq_pairs(const uint4 (&r)[4]) {
@@ -128,37 +128,82 @@ __device__ __forceinline__ float sumsq_pairs(const uint4 (&r)[4]) {
   return s;
 }
 
-// Rotate this thread's 16 pairs of a raw row (scaled by `scale`) with the
-// per-pair cos/sin in (c, s); writes the 32 rotated values into lo/hi halves.
-__device__ __forceinline__ void rotate(const uint4 (&r)[4], float scale, const float (&c)[16],
-                                       const float (&s)[16], float (&lo)[16], float (&hi)[16]) {
-  float a[16], b[16];
-  unpack8(r[0], *reinterpret_cast<float(*)[8]>(&a[0]));
-  unpack8(r[1], *reinterpret_cast<float(*)[8]>(&a[8]));
-  unpack8(r[2], *reinterpret_cast<float(*)[8]>(&b[0]));
-  unpack8(r[3], *reinterpret_cast<float(*)[8]>(&b[8]));
+// cos / sin of the RoPE angle of pair u at position p on the special-function
+// unit: the exact fixed-point phase reduced to [-pi, pi), then __sincosf
+// (absolute error ~1e-6, far below the 16-bit rounding of the operands).
+__device__ __forceinline__ void rope_fast(long long p, unsigned long long u, float &c, float &s) {
+  const unsigned long long ph = (unsigned long long)p * u;
+  const float x = (float)(int)(ph >> 32) * 1.4629180792671596e-09f;  // 2 pi / 2^32
+  __sincosf(x, &s, &c);
+}
+
+// sigmoid via the hardware tanh: 1 / (1 + e^-z) = 0.5 + 0.5 tanh(z / 2).
+__device__ __forceinline__ float sigmoid_fast(float z) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * z));
+  return fmaf(0.5f, t, 0.5f);
+}
+
+// Rotate this thread's 16 pairs of raw row `r` (times `scale`) at position p
+// and store them, as fp16 (half) or bf16, into the same chunks of `tile`.
+__device__ __forceinline__ void feature_store(const uint4 (&r)[4], float scale, long long p, int qd,
+                                              const MixerParams &P, unsigned char *tile, int row,
+                                              bool half) {
 #pragma unroll
-  for (int u = 0; u < 16; ++u) {
-    const float x0 = a[u] * scale, x1 = b[u] * scale;
-    lo[u] = x0 * c[u] - x1 * s[u];
-    hi[u] = x0 * s[u] + x1 * c[u];
+  for (int hf = 0; hf < 2; ++hf) {
+    float a[8], bb[8], lo[8], hi[8];
+    unpack8(r[hf], a);
+    unpack8(r[2 + hf], bb);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float c, s;
+      rope_fast(p, P.rope_u[16 * qd + 8 * hf + e], c, s);
+      const float x0 = a[e] * scale, x1 = bb[e] * scale;
+      lo[e] = x0 * c - x1 * s;
+      hi[e] = x0 * s + x1 * c;
+    }
+    *tile_at(tile, row, 2 * qd + hf) = half ? pack8h(lo) : pack8(lo);
+    *tile_at(tile, row, 8 + 2 * qd + hf) = half ? pack8h(hi) : pack8(hi);
   }
 }
 
-// Store 32 values (pairs lo/hi of this thread) into a K-major feature tile
-// row, as bf16 or (half = true) fp16.
-__device__ __forceinline__ void store_pairs(unsigned char *tile, int row, int qd,
-                                            const float (&lo)[16], const float (&hi)[16],
-                                            float mul, bool half = false) {
-  float t[16];
+// q~ and k~ of one row at once (shared angles), both fp16, in place.
+__device__ __forceinline__ void feature_qk_store(const uint4 (&qr)[4], const uint4 (&kr)[4],
+                                                 float rq, float rk, long long p, int qd,
+                                                 const MixerParams &P, unsigned char *Qt,
+                                                 unsigned char *Kt, int row) {
 #pragma unroll
-  for (int u = 0; u < 16; ++u) t[u] = lo[u] * mul;
-  st_tile(tile, row, 2 * qd, half ? pack8h(&t[0]) : pack8(&t[0]));
-  st_tile(tile, row, 2 * qd + 1, half ? pack8h(&t[8]) : pack8(&t[8]));
+  for (int hf = 0; hf < 2; ++hf) {
+    float c[8], s[8];
 #pragma unroll
-  for (int u = 0; u < 16; ++u) t[u] = hi[u] * mul;
-  st_tile(tile, row, 8 + 2 * qd, half ? pack8h(&t[0]) : pack8(&t[0]));
-  st_tile(tile, row, 9 + 2 * qd, half ? pack8h(&t[8]) : pack8(&t[8]));
+    for (int e = 0; e < 8; ++e) rope_fast(p, P.rope_u[16 * qd + 8 * hf + e], c[e], s[e]);
+    {
+      float a[8], bb[8], lo[8], hi[8];
+      unpack8(qr[hf], a);
+      unpack8(qr[2 + hf], bb);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float x0 = a[e] * rq, x1 = bb[e] * rq;
+        lo[e] = x0 * c[e] - x1 * s[e];
+        hi[e] = x0 * s[e] + x1 * c[e];
+      }
+      *tile_at(Qt, row, 2 * qd + hf) = pack8h(lo);
+      *tile_at(Qt, row, 8 + 2 * qd + hf) = pack8h(hi);
+    }
+    {
+      float a[8], bb[8], lo[8], hi[8];
+      unpack8(kr[hf], a);
+      unpack8(kr[2 + hf], bb);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float x0 = a[e] * rk, x1 = bb[e] * rk;
+        lo[e] = x0 * c[e] - x1 * s[e];
+        hi[e] = x0 * s[e] + x1 * c[e];
+      }
+      *tile_at(Kt, row, 2 * qd + hf) = pack8h(lo);
+      *tile_at(Kt, row, 8 + 2 * qd + hf) = pack8h(hi);
+    }
+  }
 }
 
 __device__ __forceinline__ void sync_tc() {
@@ -167,14 +212,39 @@ __device__ __forceinline__ void sync_tc() {
   umma::fence_after();
 }
 
+// Bounded wait on an mbarrier phase, with a CTA-wide vote so that every
+// thread leaves together when any of them gives up.
+__device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
+  const bool late = !umma::mbar_wait(bar, parity);
+  umma::fence_after();
+  return __syncthreads_or(late) != 0;
+}
+
+// TMA of one raw [rows, 128] bf16 tile (rows = chunk) of token rows
+// [c0, c0 + rows) for (b, h): two boxes of 64 columns.
+__device__ __forceinline__ void tma_tile(unsigned char *dst, const CUtensorMap *map, int b, int h,
+                                         int c0, uint64_t *bar) {
+  umma::tma_load_4d(dst, map, 0, h, c0, b, bar);
+  umma::tma_load_4d(dst + HALF_TILE, map, 64, h, c0, b, bar);
+}
+
 // ------------------------------------------------------------------ local state pass
 
-__global__ void __launch_bounds__(NT, 1) tc_state_kernel(const __grid_constant__ MixerParams P) {
+struct StateShared {
+  float red_k[4][ROWS];
+  uint64_t bar_mma[2];
+  uint64_t bar_tma[2];
+  uint32_t tmem_base;
+};
+
+__global__ void __launch_bounds__(NT, 1)
+    tc_state_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  unsigned char *Kd[2] = {base, base + 2 * TILE};
-  unsigned char *Vs[2] = {base + TILE, base + 3 * TILE};
-  Shared &sh = *reinterpret_cast<Shared *>(base + 4 * TILE);
+  unsigned char *Kb[2] = {base, base + 2 * TILE};
+  unsigned char *Vb[2] = {base + TILE, base + 3 * TILE};
+  StateShared &sh = *reinterpret_cast<StateShared *>(base + 4 * TILE);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sub = warp & 3, qd = warp >> 2, i = 32 * sub + lane;
@@ -182,88 +252,79 @@ __global__ void __launch_bounds__(NT, 1) tc_state_kernel(const __grid_constant__
   const int t0 = g * P.seg_len, t1 = min(P.T, t0 + P.seg_len);
   const int CV = P.chunk;
   const int L = t1 - t0;
+  const int ntile = ceil_div(L, CV);
   const float l2g = log2f(P.gamma[h]);
+  const uint32_t tile_bytes = (uint32_t)CV * D * 2;
 
   if (tid == 0) {
-    umma::mbar_init(&sh.bar[0], 1);
-    umma::mbar_init(&sh.bar[1], 1);
+    for (int j = 0; j < 2; ++j) {
+      umma::mbar_init(&sh.bar_mma[j], 1);
+      umma::mbar_init(&sh.bar_tma[j], 1);
+    }
     umma::mbar_fence_init();
   }
   if (warp == 0) umma::tmem_alloc(&sh.tmem_base, 128);
-  // Per-thread rotation of its 16 pairs at offset i within a tile.
-  float rc[16], rs[16];
-#pragma unroll
-  for (int u = 0; u < 16; ++u) rope_cs(i, P.rope_u[16 * qd + u], rc[u], rs[u]);
+  // rows [CV, 128) of the V buffers are never written by TMA: clear them once
+  if (CV < ROWS)
+    for (int e = tid; e < 2 * (ROWS - CV) * 16; e += NT) {
+      const int bufi = e / ((ROWS - CV) * 16), r = e % ((ROWS - CV) * 16);
+      *tile_at(Vb[bufi], CV + r / 16, r % 16) = make_uint4(0, 0, 0, 0);
+    }
   sync_tc();
   const uint32_t tm = sh.tmem_base;
   const uint32_t idesc = umma::idesc_bf16(128, 128, true, true);
-
-  const int ntile = ceil_div(L, CV);
-  bool failed = false;
-  uint4 kr[4], vr[4];
-  {
-    const bool ok = i < min(CV, L);
-    load_pairs(kr, row_ptr(P.k, P, b, h, t0 + (ok ? i : 0)), qd, ok);
-    load_quarter(vr, row_ptr(P.v, P, b, h, t0 + (ok ? i : 0)), qd, ok);
-  }
-  for (int n = 0; n < ntile; ++n) {
-    const int c0 = t0 + n * CV, c = min(CV, t1 - c0);
-    const int buf = n & 1;
-    // base rotation of this tile
-    if (tid < D / 2) {
-      float cc, ss;
-      rope_cs(P.pos_offset + c0, P.rope_u[tid], cc, ss);
-      sh.rb[tid] = make_float2(cc, ss);
+  if (tid == 0) {
+    for (int n = 0; n < 2 && n < ntile; ++n) {
+      umma::mbar_expect_tx(&sh.bar_tma[n], 2 * tile_bytes);
+      tma_tile(Kb[n], &tmk, b, h, t0 + n * CV, &sh.bar_tma[n]);
+      tma_tile(Vb[n], &tmv, b, h, t0 + n * CV, &sh.bar_tma[n]);
     }
-    sh.red_k[qd][i] = sumsq_pairs(kr);
-    // buffer `buf` was read by the MMA of tile n - 2
-    const bool late = n >= 2 && !umma::mbar_wait(&sh.bar[buf], ((n >> 1) - 1) & 1);
-    umma::fence_after();
-    if (__syncthreads_or(late)) {
+  }
+
+  bool failed = false;
+  for (int n = 0; n < ntile; ++n) {
+    const int buf = n & 1;
+    const int c0 = t0 + n * CV, c = min(CV, t1 - c0);
+    if (wait_all(&sh.bar_tma[buf], (n >> 1) & 1)) {
       failed = true;
       break;
     }
+    uint4 kr[4];
+    ld_pairs(Kb[buf], i, qd, kr);
+    if (i >= c)  // rows past the tile hold stale bytes: use zeros
+      kr[0] = kr[1] = kr[2] = kr[3] = make_uint4(0, 0, 0, 0);
+    sh.red_k[qd][i] = sumsq_pairs(kr);
+    __syncthreads();
     const float rk = rsqrtf((sh.red_k[0][i] + sh.red_k[1][i] + sh.red_k[2][i] + sh.red_k[3][i]) /
                                 (float)D + P.eps);
-    float cs[16], sn[16];
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const float2 bb = sh.rb[16 * qd + u];
-      cs[u] = bb.x * rc[u] - bb.y * rs[u];
-      sn[u] = bb.y * rc[u] + bb.x * rs[u];
-    }
-    float lo[16], hi[16];
-    rotate(kr, rk * P.kscale, cs, sn, lo, hi);
-    // decay weight of this key row towards the end of the segment
+    // decay weight of this key row towards the end of the segment (0 past the tile)
     const float wgt = i < c ? exp2f((float)(L - 1 - (c0 - t0 + i)) * l2g) : 0.f;
-    store_pairs(Kd[buf], i, qd, lo, hi, wgt);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) st_tile(Vs[buf], i, 4 * qd + u, vr[u]);
-    // prefetch the next tile
-    if (n + 1 < ntile) {
-      const int n0 = c0 + CV;
-      const bool ok = i < min(CV, t1 - n0);
-      load_pairs(kr, row_ptr(P.k, P, b, h, ok ? n0 + i : n0), qd, ok);
-      load_quarter(vr, row_ptr(P.v, P, b, h, ok ? n0 + i : n0), qd, ok);
-    }
+    feature_store(kr, rk * P.kscale * wgt, P.pos_offset + c0 + i, qd, P, Kb[buf], i, false);
     umma::fence_async_smem();
     sync_tc();
     if (tid == 0) {
-      const uint32_t a = umma::smem_u32(Kd[buf]), bv = umma::smem_u32(Vs[buf]);
+      const uint32_t a = umma::smem_u32(Kb[buf]), bv = umma::smem_u32(Vb[buf]);
 #pragma unroll
       for (int kk = 0; kk < ROWS / 16; ++kk)
         umma::mma_ss(tm, umma::desc_mnmajor(a, kk, ROWS), umma::desc_mnmajor(bv, kk, ROWS), idesc,
                      (n > 0 || kk > 0) ? 1u : 0u);
-      umma::commit(&sh.bar[buf]);
+      umma::commit(&sh.bar_mma[buf]);
+    }
+    // refill this buffer pair with tile n + 2 once MMA n has read it
+    if (n + 2 < ntile) {
+      if (wait_all(&sh.bar_mma[buf], (n >> 1) & 1)) {
+        failed = true;
+        break;
+      }
+      if (tid == 0) {
+        umma::mbar_expect_tx(&sh.bar_tma[buf], 2 * tile_bytes);
+        tma_tile(Kb[buf], &tmk, b, h, c0 + 2 * CV, &sh.bar_tma[buf]);
+        tma_tile(Vb[buf], &tmv, b, h, c0 + 2 * CV, &sh.bar_tma[buf]);
+      }
     }
   }
-  // wait for the last MMA (its completion covers all earlier ones)
-  if (!failed) {
-    const int last = ntile - 1;
-    const bool late = !umma::mbar_wait(&sh.bar[last & 1], (last >> 1) & 1);
-    umma::fence_after();
-    failed = __syncthreads_or(late);
-  }
+  // the last MMA's completion covers all earlier ones
+  if (!failed) failed = wait_all(&sh.bar_mma[(ntile - 1) & 1], ((ntile - 1) >> 1) & 1);
   float *out = P.seg + (((size_t)b * P.H + h) * P.nseg + g) * (size_t)D * D;
   if (!failed) {
     float v[32];
@@ -274,7 +335,7 @@ __global__ void __launch_bounds__(NT, 1) tc_state_kernel(const __grid_constant__
   } else {
     const float nan = __int_as_float(0x7fc00000);
     for (int e = tid; e < D * D; e += NT) out[e] = nan;
-    if (P.err) atomicOr(P.err, 1u);
+    if (tid == 0 && P.err) atomicOr(P.err, 1u);
   }
   sync_tc();
   if (warp == 0) umma::tmem_dealloc(tm, 128);
@@ -282,35 +343,74 @@ __global__ void __launch_bounds__(NT, 1) tc_state_kernel(const __grid_constant__
 
 // ------------------------------------------------------------------ output pass
 
-__global__ void __launch_bounds__(NT, 1) tc_output_kernel(const __grid_constant__ MixerParams P) {
+struct OutShared {
+  float red_q[4][ROWS];
+  float red_k[4][ROWS];
+  float red_o[4][ROWS];
+  float pw[ROWS + 1];
+  float smax[NT / 32];
+  uint64_t bar_mma[2];  // [0]: MMA1 + MMA2 done, [1]: MMA3 + MMA4 done
+  uint64_t bar_qk[2];   // TMA of raw q, k into buffer pair 0 / 1
+  uint64_t bar_v;       // TMA of raw v
+  uint32_t tmem_base;
+};
+
+// Software-pipelined output pass over the tiles of one segment.  Iteration n:
+//   [A] wait for raw q, k of tile n (TMA, issued one iteration earlier)
+//   [W] wait for MMA3/MMA4 of tile n - 1; TMA v(n) and q, k(n + 1) into the freed buffers
+//   [B] max |S|, row sums of squares; [C] Sb = fp16 S 2^-e, S <- gamma^c S
+//   [D] q~, k~ in place; issue MMA1 (P) and MMA2 (O = Q~ Sb)
+//   [E] epilogue of tile n - 1 (overlaps MMA1/MMA2)
+//   [F] mask P -> Pm, scale O, k~ -> k~dec in place; issue MMA3 and MMA4
+// Shared memory: two (Q, K) buffer pairs, V, and one buffer shared by Sb and
+// Pm (Sb is dead once MMA2 is done, Pm is dead once MMA3 is done).
+__global__ void __launch_bounds__(NT, 1)
+    tc_output_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmq,
+                     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  unsigned char *Qt = base, *Kt = base + TILE, *Kd = base + 2 * TILE, *Vs = base + 3 * TILE,
-                *Pm = base + 4 * TILE, *Sb = base + 5 * TILE;
-  Shared &sh = *reinterpret_cast<Shared *>(base + 6 * TILE);
+  unsigned char *Qb[2] = {base, base + 2 * TILE};
+  unsigned char *Kb[2] = {base + TILE, base + 3 * TILE};
+  unsigned char *Vs = base + 4 * TILE, *SP = base + 5 * TILE;
+  OutShared &sh = *reinterpret_cast<OutShared *>(base + 6 * TILE);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sub = warp & 3, qd = warp >> 2, i = 32 * sub + lane;
   const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int t0 = g * P.seg_len, t1 = min(P.T, t0 + P.seg_len);
   const int CV = P.chunk;
-  const float l2g = log2f(P.gamma[h]);
+  const int ntile = ceil_div(t1 - t0, CV);
+  const float gm = P.gamma[h];
+  const float l2g = log2f(gm);
+  const uint32_t tile_bytes = (uint32_t)CV * D * 2;
 
   if (tid == 0) {
-    umma::mbar_init(&sh.bar[0], 1);
-    umma::mbar_init(&sh.bar[1], 1);
+    for (int j = 0; j < 2; ++j) {
+      umma::mbar_init(&sh.bar_mma[j], 1);
+      umma::mbar_init(&sh.bar_qk[j], 1);
+    }
+    umma::mbar_init(&sh.bar_v, 1);
     umma::mbar_fence_init();
   }
   if (tid <= ROWS) sh.pw[tid] = exp2f((float)tid * l2g);
   if (warp == 0) umma::tmem_alloc(&sh.tmem_base, 512);
-  float rc[16], rs[16];
-#pragma unroll
-  for (int u = 0; u < 16; ++u) rope_cs(i, P.rope_u[16 * qd + u], rc[u], rs[u]);
+  if (CV < ROWS)  // rows [CV, 128) of V are never written by TMA: clear them once
+    for (int e = tid; e < (ROWS - CV) * 16; e += NT)
+      *tile_at(Vs, CV + e / 16, e % 16) = make_uint4(0, 0, 0, 0);
   sync_tc();
   const uint32_t tm = sh.tmem_base;
   const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
-  const uint32_t tP = tm, tOi = tm + 128, tOa = tm + 256, tS = tm + 384;
-
+  const uint32_t tP = tm, tS = tm + 384;
+  const uint32_t myS = tS + lane_base + 32 * qd, myP = tP + lane_base + 32 * qd;
+  if (tid == 0) {
+    for (int n = 0; n < 2 && n < ntile; ++n) {
+      umma::mbar_expect_tx(&sh.bar_qk[n], 2 * tile_bytes);
+      tma_tile(Qb[n], &tmq, b, h, t0 + n * CV, &sh.bar_qk[n]);
+      tma_tile(Kb[n], &tmk, b, h, t0 + n * CV, &sh.bar_qk[n]);
+    }
+    umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
+    tma_tile(Vs, &tmv, b, h, t0, &sh.bar_v);
+  }
   // entering state of the segment -> TMEM (fp32)
   {
     const float *sin_ = P.seg + (((size_t)b * P.H + h) * P.nseg + g) * (size_t)D * D;
@@ -321,7 +421,7 @@ __global__ void __launch_bounds__(NT, 1) tc_output_kernel(const __grid_constant_
       const float4 x = s4[u];
       v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
     }
-    umma::tmem_st32(tS + lane_base + 32 * qd, v);
+    umma::tmem_st32(myS, v);
     umma::tmem_wait_st();
   }
 
@@ -329,188 +429,240 @@ __global__ void __launch_bounds__(NT, 1) tc_output_kernel(const __grid_constant_
   const uint32_t id_qs = umma::idesc_bf16(128, 128, false, true, true);   // fp16 Q~ S
   const uint32_t id_pv = umma::idesc_bf16(128, 128, false, true);         // bf16 Pm V
   const uint32_t id_mn = umma::idesc_bf16(128, 128, true, true);          // bf16 K~dec^T V
-  const int ntile = ceil_div(t1 - t0, CV);
-  uint4 qr[4], kr[4];
-  {
-    const bool ok = i < min(CV, t1 - t0);
-    load_pairs(qr, row_ptr(P.q, P, b, h, ok ? t0 + i : t0), qd, ok);
-    load_pairs(kr, row_ptr(P.k, P, b, h, ok ? t0 + i : t0), qd, ok);
-  }
   __nv_bfloat16 *y = (__nv_bfloat16 *)P.y;
 
   bool failed = false;
-  for (int n = 0; n < ntile; ++n) {
-    const int c0 = t0 + n * CV, c = min(CV, t1 - c0);
+  int prev_c0 = 0, prev_c = 0;
+  for (int n = 0; n <= ntile; ++n) {
+    const bool have = n < ntile, drain = n >= 1;
+    const int c0 = t0 + n * CV, c = have ? min(CV, t1 - c0) : 0;
+    const int buf = n & 1;
     const bool valid = i < c;
-    if (tid < D / 2) {
-      float cc, ss;
-      rope_cs(P.pos_offset + c0, P.rope_u[tid], cc, ss);
-      sh.rb[tid] = make_float2(cc, ss);
-    }
-    uint4 vr[4];
-    load_quarter(vr, row_ptr(P.v, P, b, h, valid ? c0 + i : c0), qd, valid);
-    // State phase, part 1: max |S| over the tile (S is fp32 in TMEM).
-    {
-      float v[32];
-      umma::tmem_ld32(tS + lane_base + 32 * qd, v);
-      float m = 0.f;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) m = fmaxf(m, fabsf(v[e]));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) sh.smax[warp] = m;
-    }
-    sh.red_q[qd][i] = sumsq_pairs(qr);
-    sh.red_k[qd][i] = sumsq_pairs(kr);
-    __syncthreads();
-    // State phase, part 2: Sb = fp16(S * 2^-e) with 2^e >= max |S|; then S <- gamma^c S.
-    float s_inv;  // 2^e: multiplies Q~ Sb back to the scale of S
-    {
-      float m = 0.f;
-#pragma unroll
-      for (int w = 0; w < NT / 32; ++w) m = fmaxf(m, sh.smax[w]);
-      int e = 0;
-      if (m > 0.f) frexpf(m, &e);
-      const float s_fwd = ldexpf(1.f, -e);
-      s_inv = ldexpf(1.f, e);
-      float v[32];
-      umma::tmem_ld32(tS + lane_base + 32 * qd, v);
-      float t[8];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-#pragma unroll
-        for (int e2 = 0; e2 < 8; ++e2) t[e2] = v[8 * u + e2] * s_fwd;
-        st_tile(Sb, i, 4 * qd + u, pack8h(t));
-      }
-      const float carry = sh.pw[c];
-#pragma unroll
-      for (int e2 = 0; e2 < 32; ++e2) v[e2] *= carry;
-      umma::tmem_st32(tS + lane_base + 32 * qd, v);
-    }
-    // Feature map: q~ = RoPE(Norm(q)), k~ = RoPE(Norm(k)) / sqrt(d), k~dec = gamma^{c-1-i} k~.
-    {
-      const float rq = rsqrtf((sh.red_q[0][i] + sh.red_q[1][i] + sh.red_q[2][i] + sh.red_q[3][i]) /
-                                  (float)D + P.eps);
-      const float rk = rsqrtf((sh.red_k[0][i] + sh.red_k[1][i] + sh.red_k[2][i] + sh.red_k[3][i]) /
-                                  (float)D + P.eps);
-      float cs[16], sn[16];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const float2 bb = sh.rb[16 * qd + u];
-        cs[u] = bb.x * rc[u] - bb.y * rs[u];
-        sn[u] = bb.y * rc[u] + bb.x * rs[u];
-      }
-      float lo[16], hi[16];
-      rotate(qr, rq, cs, sn, lo, hi);
-      store_pairs(Qt, i, qd, lo, hi, 1.f, true);
-      rotate(kr, rk * P.kscale, cs, sn, lo, hi);
-      store_pairs(Kt, i, qd, lo, hi, 1.f, true);
-      store_pairs(Kd, i, qd, lo, hi, valid ? sh.pw[c - 1 - i] : 0.f);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) st_tile(Vs, i, 4 * qd + u, vr[u]);
-    }
-    // prefetch the next tile's q and k rows
-    if (n + 1 < ntile) {
-      const int n0 = c0 + CV;
-      const bool ok = i < min(CV, t1 - n0);
-      load_pairs(qr, row_ptr(P.q, P, b, h, ok ? n0 + i : n0), qd, ok);
-      load_pairs(kr, row_ptr(P.k, P, b, h, ok ? n0 + i : n0), qd, ok);
-    }
-    umma::tmem_wait_st();
-    umma::fence_async_smem();
-    sync_tc();
-    if (tid == 0) {
-      const uint32_t aq = umma::smem_u32(Qt), ak = umma::smem_u32(Kt), ad = umma::smem_u32(Kd),
-                     av = umma::smem_u32(Vs), as = umma::smem_u32(Sb);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        umma::mma_ss(tP, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(ak, kk, ROWS), id_qk,
-                     kk > 0);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        umma::mma_ss(tOi, umma::desc_kmajor(aq, kk, ROWS), umma::desc_mnmajor(as, kk, ROWS), id_qs,
-                     kk > 0);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        umma::mma_ss(tS, umma::desc_mnmajor(ad, kk, ROWS), umma::desc_mnmajor(av, kk, ROWS), id_mn,
-                     1u);
-      umma::commit(&sh.bar[0]);
-    }
+    const uint32_t oc = tm + 128 + 128 * buf;          // O buffer of tile n
+    const uint32_t op = tm + 128 + 128 * (buf ^ 1);    // O buffer of tile n - 1
+    unsigned char *Qt = Qb[buf], *Kt = Kb[buf];
     uint4 gr[4];
-    load_quarter(gr, row_ptr(P.g, P, b, h, valid ? c0 + i : c0), qd, valid);
-    {
-      const bool late = !umma::mbar_wait(&sh.bar[0], n & 1);
-      umma::fence_after();
-      if (__syncthreads_or(late)) {
+    if (drain) {  // gate rows of tile n - 1, for its epilogue in [E]
+      const bool okp = i < prev_c;
+      load_quarter(gr, row_ptr(P.g, P, b, h, okp ? prev_c0 + i : prev_c0), qd, okp);
+    }
+    uint4 qr[4], kr[4];
+    if (have) {
+      // [A] raw q, k of tile n are in Qt / Kt
+      if (wait_all(&sh.bar_qk[buf], (n >> 1) & 1)) {
         failed = true;
         break;
       }
+      ld_pairs(Qt, i, qd, qr);
+      ld_pairs(Kt, i, qd, kr);
+      if (!valid)  // rows past the tile hold stale bytes: use zeros
+        qr[0] = qr[1] = qr[2] = qr[3] = kr[0] = kr[1] = kr[2] = kr[3] = make_uint4(0, 0, 0, 0);
+      sh.red_q[qd][i] = sumsq_pairs(qr);
+      sh.red_k[qd][i] = sumsq_pairs(kr);
     }
-    // Mask: Pm = bf16((Q~ K~^T) (.) D), causal with gamma^{i-j}.
-    {
-      float v[32];
-      umma::tmem_ld32(tP + lane_base + 32 * qd, v);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int j = 32 * qd + e;
-        v[e] = (j <= i && valid) ? v[e] * sh.pw[i - j] : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) st_tile(Pm, i, 4 * qd + u, pack8(&v[8 * u]));
-    }
-    umma::fence_async_smem();
-    sync_tc();
-    if (tid == 0) {
-      const uint32_t ap = umma::smem_u32(Pm), av = umma::smem_u32(Vs);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        umma::mma_ss(tOa, umma::desc_kmajor(ap, kk, ROWS), umma::desc_mnmajor(av, kk, ROWS), id_pv,
-                     kk > 0);
-      umma::commit(&sh.bar[1]);
-    }
-    {
-      const bool late = !umma::mbar_wait(&sh.bar[1], n & 1);
-      umma::fence_after();
-      if (__syncthreads_or(late)) {
+    if (drain) {
+      // [W] MMA3 / MMA4 of tile n - 1 are done: O(n-1) final, S current, V and
+      //     SP free, buffer pair (n + 1) & 1 free.
+      if (wait_all(&sh.bar_mma[1], (n - 1) & 1)) {
         failed = true;
         break;
       }
+      if (tid == 0) {
+        if (have) {
+          umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
+          tma_tile(Vs, &tmv, b, h, c0, &sh.bar_v);
+        }
+        if (n + 1 < ntile) {
+          umma::mbar_expect_tx(&sh.bar_qk[buf ^ 1], 2 * tile_bytes);
+          tma_tile(Qb[buf ^ 1], &tmq, b, h, c0 + CV, &sh.bar_qk[buf ^ 1]);
+          tma_tile(Kb[buf ^ 1], &tmk, b, h, c0 + CV, &sh.bar_qk[buf ^ 1]);
+        }
+      }
     }
-    // Epilogue: o = gamma^{i+1} O_int + O_in; y = Norm(o) * sigmoid(gate).
-    float o[32];
-    {
-      float a[32];
-      umma::tmem_ld32(tOi + lane_base + 32 * qd, a);
-      umma::tmem_ld32(tOa + lane_base + 32 * qd, o);
-      const float inter = sh.pw[i + 1] * s_inv;
+    float s_inv = 1.f;
+    if (have) {
+      // [B] max |S| over the tile (S is fp32 in TMEM)
+      {
+        float m = 0.f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float v[16];
+          umma::tmem_ld16(myS + 16 * hf, v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(v[e]));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) sh.smax[warp] = m;
+      }
+      __syncthreads();
+      // [C] Sb = fp16(S 2^-e) with 2^e >= max |S|, then S <- gamma^c S
+      {
+        float m = 0.f;
+#pragma unroll
+        for (int w = 0; w < NT / 32; ++w) m = fmaxf(m, sh.smax[w]);
+        int e = 0;
+        if (m > 0.f) frexpf(m, &e);
+        const float s_fwd = ldexpf(1.f, -e);
+        s_inv = ldexpf(1.f, e);
+        const float carry = sh.pw[c];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float v[16];
+          umma::tmem_ld16(myS + 16 * hf, v);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            float t[8];
+#pragma unroll
+            for (int e2 = 0; e2 < 8; ++e2) t[e2] = v[8 * u + e2] * s_fwd;
+            *tile_at(SP, i, 4 * qd + 2 * hf + u) = pack8h(t);
+          }
+#pragma unroll
+          for (int e2 = 0; e2 < 16; ++e2) v[e2] *= carry;
+          umma::tmem_st16(myS + 16 * hf, v);
+        }
+      }
+      // [D] q~ = RoPE(Norm(q)), k~ = RoPE(Norm(k)) / sqrt(d), fp16, in place (0 past the tile)
+      {
+        const float rq = rsqrtf((sh.red_q[0][i] + sh.red_q[1][i] + sh.red_q[2][i] +
+                                 sh.red_q[3][i]) / (float)D + P.eps);
+        const float rk = rsqrtf((sh.red_k[0][i] + sh.red_k[1][i] + sh.red_k[2][i] +
+                                 sh.red_k[3][i]) / (float)D + P.eps) * P.kscale;
+        feature_qk_store(qr, kr, valid ? rq : 0.f, valid ? rk : 0.f, P.pos_offset + c0 + i, qd, P,
+                         Qt, Kt, i);
+      }
+      umma::tmem_wait_st();
+      umma::fence_async_smem();
+      sync_tc();
+      if (tid == 0) {
+        const uint32_t aq = umma::smem_u32(Qt), ak = umma::smem_u32(Kt), as = umma::smem_u32(SP);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma::mma_ss(tP, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(ak, kk, ROWS), id_qk,
+                       kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma::mma_ss(oc, umma::desc_kmajor(aq, kk, ROWS), umma::desc_mnmajor(as, kk, ROWS), id_qs,
+                       kk > 0);
+        umma::commit(&sh.bar_mma[0]);
+      }
+    }
+    // [E] epilogue of tile n - 1 (overlaps MMA1 / MMA2 of tile n)
+    if (drain) {
+      const uint32_t myO = op + lane_base + 32 * qd;
       float ss = 0.f;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        o[e] = fmaf(inter, a[e], o[e]);
-        ss = fmaf(o[e], o[e], ss);
+      for (int hf = 0; hf < 2; ++hf) {
+        float o[16];
+        umma::tmem_ld16(myO + 16 * hf, o);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) ss = fmaf(o[e], o[e], ss);
       }
       sh.red_o[qd][i] = ss;
-    }
-    __syncthreads();
-    if (valid) {
-      const float ro = rsqrtf((sh.red_o[0][i] + sh.red_o[1][i] + sh.red_o[2][i] + sh.red_o[3][i]) /
-                                  (float)D + P.eps);
-      const size_t row = (((size_t)b * P.T + c0 + i) * P.H + h) * D + 32 * qd;
+      __syncthreads();
+      const bool okp = i < prev_c;
+      const float ro = rsqrtf((sh.red_o[0][i] + sh.red_o[1][i] + sh.red_o[2][i] +
+                               sh.red_o[3][i]) / (float)D + P.eps);
+      const size_t row = (((size_t)b * P.T + prev_c0 + (okp ? i : 0)) * P.H + h) * D + 32 * qd;
       uint4 *y4 = reinterpret_cast<uint4 *>(y + row);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        float gf[8], t[8];
-        unpack8(gr[u], gf);
+      for (int hf = 0; hf < 2; ++hf) {
+        float o[16];
+        umma::tmem_ld16(myO + 16 * hf, o);
+        if (okp) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) t[e] = o[8 * u + e] * ro * sigmoidf_(gf[e]);
-        y4[u] = pack8(t);
-      }
-      if (P.o) {
-        float4 *o4 = reinterpret_cast<float4 *>(P.o + row);
+          for (int u = 0; u < 2; ++u) {
+            float gf[8], t[8];
+            unpack8(gr[2 * hf + u], gf);
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          o4[u] = make_float4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+            for (int e = 0; e < 8; ++e) t[e] = o[8 * u + e] * ro * sigmoid_fast(gf[e]);
+            y4[2 * hf + u] = pack8(t);
+          }
+          if (P.o) {
+            float4 *o4 = reinterpret_cast<float4 *>(P.o + row + 16 * hf);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              o4[u] = make_float4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+          }
+        }
       }
+    }
+    if (have) {
+      // [F] MMA1 / MMA2 of tile n done
+      if (wait_all(&sh.bar_mma[0], n & 1)) {
+        failed = true;
+        break;
+      }
+      // mask: Pm = bf16((Q~ K~^T) (.) D) into SP (Sb is dead)
+      {
+        const int jlo = 32 * qd;
+        const int jm = min(i, jlo + 31);
+        float w = (valid && jm >= jlo) ? sh.pw[i - jm] : 0.f;
+#pragma unroll
+        for (int hf = 1; hf >= 0; --hf) {
+          float v[16];
+          umma::tmem_ld16(myP + 16 * hf, v);
+#pragma unroll
+          for (int e = 15; e >= 0; --e) {
+            if (jlo + 16 * hf + e <= i) {
+              v[e] *= w;
+              w *= gm;
+            } else {
+              v[e] = 0.f;
+            }
+          }
+          *tile_at(SP, i, 4 * qd + 2 * hf) = pack8(&v[0]);
+          *tile_at(SP, i, 4 * qd + 2 * hf + 1) = pack8(&v[8]);
+        }
+      }
+      // O <- gamma^{i+1} 2^e O  (the Q~ S part, before MMA3 adds Pm V)
+      {
+        const uint32_t myO = oc + lane_base + 32 * qd;
+        const float f = sh.pw[i + 1] * s_inv;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float v[16];
+          umma::tmem_ld16(myO + 16 * hf, v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] *= f;
+          umma::tmem_st16(myO + 16 * hf, v);
+        }
+      }
+      // k~dec = gamma^{c-1-i} k~ as bf16, in place (K~ is dead once MMA1 is done)
+      {
+        const float wk = valid ? sh.pw[c - 1 - i] : 0.f;
+        const int ch[4] = {2 * qd, 2 * qd + 1, 8 + 2 * qd, 9 + 2 * qd};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint4 *p = tile_at(Kt, i, ch[u]);
+          float f[8];
+          unpack8h(*p, f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] *= wk;
+          *p = pack8(f);
+        }
+      }
+      if (wait_all(&sh.bar_v, n & 1)) {  // raw v of tile n is in Vs
+        failed = true;
+        break;
+      }
+      umma::tmem_wait_st();
+      umma::fence_async_smem();
+      sync_tc();
+      if (tid == 0) {
+        const uint32_t ap = umma::smem_u32(SP), av = umma::smem_u32(Vs), ad = umma::smem_u32(Kt);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma::mma_ss(oc, umma::desc_kmajor(ap, kk, ROWS), umma::desc_mnmajor(av, kk, ROWS), id_pv,
+                       1u);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma::mma_ss(tS, umma::desc_mnmajor(ad, kk, ROWS), umma::desc_mnmajor(av, kk, ROWS), id_mn,
+                       1u);
+        umma::commit(&sh.bar_mma[1]);
+      }
+      prev_c0 = c0;
+      prev_c = c;
     }
   }
   if (failed && tid == 0 && P.err) atomicOr(P.err, 2u);
@@ -518,8 +670,44 @@ __global__ void __launch_bounds__(NT, 1) tc_output_kernel(const __grid_constant_
   if (warp == 0) umma::tmem_dealloc(tm, 512);
 }
 
-constexpr size_t kStateSmem = 4 * TILE + sizeof(Shared) + 1024;
-constexpr size_t kOutputSmem = 6 * TILE + sizeof(Shared) + 1024;
+constexpr size_t kStateSmem = 4 * TILE + sizeof(StateShared) + 1024;
+constexpr size_t kOutputSmem = 6 * TILE + sizeof(OutShared) + 1024;
+
+// ------------------------------------------------------------------ host side
+
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                              const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                              const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeFn>(p);
+  }();
+  return fn;
+}
+
+// 4-D map over a [B, T, H, 128] bf16 tensor with a box of 64 columns x 1 head
+// x `rows` tokens x 1 sequence, 128-byte swizzled (the operand tile layout).
+cudaError_t make_map(CUtensorMap *map, const void *ptr, const MixerParams &P, int rows) {
+  EncodeFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)P.H, (cuuint64_t)P.T, (cuuint64_t)P.B};
+  const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)P.H * D * 2,
+                                 (cuuint64_t)P.T * P.H * D * 2};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 }  // namespace
 }  // namespace tc
@@ -527,20 +715,27 @@ constexpr size_t kOutputSmem = 6 * TILE + sizeof(Shared) + 1024;
 bool tc_supported(const MixerParams &P, int dtype) { return dtype == HLA_BF16 && P.D == 128; }
 
 cudaError_t launch_tc_seg_state(const MixerParams &P, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(tc::tc_state_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)tc::kStateSmem);
+  CUtensorMap mk, mv;
+  cudaError_t e;
+  if ((e = tc::make_map(&mk, P.k, P, P.chunk)) != cudaSuccess) return e;
+  if ((e = tc::make_map(&mv, P.v, P, P.chunk)) != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc::tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)tc::kStateSmem);
   if (e != cudaSuccess) return e;
-  tc::tc_state_kernel<<<dim3(P.nseg, P.H, P.B), tc::NT, tc::kStateSmem, st>>>(P);
+  tc::tc_state_kernel<<<dim3(P.nseg, P.H, P.B), tc::NT, tc::kStateSmem, st>>>(P, mk, mv);
   return cudaGetLastError();
 }
 
 cudaError_t launch_tc_seg_output(const MixerParams &P, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(tc::tc_output_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)tc::kOutputSmem);
+  CUtensorMap mq, mk, mv;
+  cudaError_t e;
+  if ((e = tc::make_map(&mq, P.q, P, P.chunk)) != cudaSuccess) return e;
+  if ((e = tc::make_map(&mk, P.k, P, P.chunk)) != cudaSuccess) return e;
+  if ((e = tc::make_map(&mv, P.v, P, P.chunk)) != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc::tc_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)tc::kOutputSmem);
   if (e != cudaSuccess) return e;
-  tc::tc_output_kernel<<<dim3(P.nseg, P.H, P.B), tc::NT, tc::kOutputSmem, st>>>(P);
+  tc::tc_output_kernel<<<dim3(P.nseg, P.H, P.B), tc::NT, tc::kOutputSmem, st>>>(P, mq, mk, mv);
   return cudaGetLastError();
 }
 
