@@ -23,6 +23,7 @@ namespace hla {
 namespace {
 
 constexpr int kScanThreads = 256;
+constexpr int kBatch = 8;
 
 __global__ void __launch_bounds__(kScanThreads) state_scan_kernel(const MixerParams P,
                                                                   int write_out) {
@@ -37,10 +38,21 @@ __global__ void __launch_bounds__(kScanThreads) state_scan_kernel(const MixerPar
   const float carry_last = exp2f((float)last_len * l2g);
   float S = P.state_in ? P.state_in[(size_t)bh * DD + e] : 0.f;
   float *seg = P.seg + (size_t)bh * P.nseg * DD + e;
-  for (int g = 0; g < P.nseg; ++g) {
-    const float delta = seg[(size_t)g * DD];
-    seg[(size_t)g * DD] = S;
-    S = fmaf(g == P.nseg - 1 ? carry_last : carry_full, S, delta);
+  // Batches of independent loads ahead of the dependent chain (the slots are
+  // overwritten in place, so each batch is loaded before any of it is stored).
+  for (int g0 = 0; g0 < P.nseg; g0 += kBatch) {
+    float delta[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+      delta[j] = g0 + j < P.nseg ? seg[(size_t)(g0 + j) * DD] : 0.f;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int g = g0 + j;
+      if (g < P.nseg) {
+        seg[(size_t)g * DD] = S;
+        S = fmaf(g == P.nseg - 1 ? carry_last : carry_full, S, delta[j]);
+      }
+    }
   }
   if (write_out) P.state_out[(size_t)bh * DD + e] = S;
 }
@@ -58,10 +70,18 @@ __global__ void __launch_bounds__(kScanThreads) grad_scan_kernel(const MixerPara
   const float carry_last = exp2f((float)last_len * l2g);
   float E = P.dstate_out ? P.dstate_out[(size_t)bh * DD + e] : 0.f;
   float *seg = P.seg2 + (size_t)bh * P.nseg * DD + e;
-  for (int g = P.nseg - 1; g >= 0; --g) {
-    const float delta = seg[(size_t)g * DD];
-    seg[(size_t)g * DD] = E;
-    E = fmaf(g == P.nseg - 1 ? carry_last : carry_full, E, delta);
+  for (int g1 = P.nseg - 1; g1 >= 0; g1 -= kBatch) {
+    float delta[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) delta[j] = g1 - j >= 0 ? seg[(size_t)(g1 - j) * DD] : 0.f;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int g = g1 - j;
+      if (g >= 0) {
+        seg[(size_t)g * DD] = E;
+        E = fmaf(g == P.nseg - 1 ? carry_last : carry_full, E, delta[j]);
+      }
+    }
   }
   if (write_out) P.dstate_in[(size_t)bh * DD + e] = E;
 }

@@ -242,8 +242,7 @@ __global__ void __launch_bounds__(NT, 1)
                     const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  unsigned char *Kb[2] = {base, base + 2 * TILE};
-  unsigned char *Vb[2] = {base + TILE, base + 3 * TILE};
+  // buffer pair j: K at base + 2 j TILE, V at base + (2 j + 1) TILE
   StateShared &sh = *reinterpret_cast<StateShared *>(base + 4 * TILE);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -268,7 +267,7 @@ __global__ void __launch_bounds__(NT, 1)
   if (CV < ROWS)
     for (int e = tid; e < 2 * (ROWS - CV) * 16; e += NT) {
       const int bufi = e / ((ROWS - CV) * 16), r = e % ((ROWS - CV) * 16);
-      *tile_at(Vb[bufi], CV + r / 16, r % 16) = make_uint4(0, 0, 0, 0);
+      *tile_at(base + (2 * bufi + 1) * TILE, CV + r / 16, r % 16) = make_uint4(0, 0, 0, 0);
     }
   sync_tc();
   const uint32_t tm = sh.tmem_base;
@@ -276,21 +275,22 @@ __global__ void __launch_bounds__(NT, 1)
   if (tid == 0) {
     for (int n = 0; n < 2 && n < ntile; ++n) {
       umma::mbar_expect_tx(&sh.bar_tma[n], 2 * tile_bytes);
-      tma_tile(Kb[n], &tmk, b, h, t0 + n * CV, &sh.bar_tma[n]);
-      tma_tile(Vb[n], &tmv, b, h, t0 + n * CV, &sh.bar_tma[n]);
+      tma_tile(base + 2 * n * TILE, &tmk, b, h, t0 + n * CV, &sh.bar_tma[n]);
+      tma_tile(base + (2 * n + 1) * TILE, &tmv, b, h, t0 + n * CV, &sh.bar_tma[n]);
     }
   }
 
   bool failed = false;
   for (int n = 0; n < ntile; ++n) {
     const int buf = n & 1;
+    unsigned char *Kt = base + 2 * buf * TILE, *Vt = Kt + TILE;
     const int c0 = t0 + n * CV, c = min(CV, t1 - c0);
     if (wait_all(&sh.bar_tma[buf], (n >> 1) & 1)) {
       failed = true;
       break;
     }
     uint4 kr[4];
-    ld_pairs(Kb[buf], i, qd, kr);
+    ld_pairs(Kt, i, qd, kr);
     if (i >= c)  // rows past the tile hold stale bytes: use zeros
       kr[0] = kr[1] = kr[2] = kr[3] = make_uint4(0, 0, 0, 0);
     sh.red_k[qd][i] = sumsq_pairs(kr);
@@ -299,11 +299,11 @@ __global__ void __launch_bounds__(NT, 1)
                                 (float)D + P.eps);
     // decay weight of this key row towards the end of the segment (0 past the tile)
     const float wgt = i < c ? exp2f((float)(L - 1 - (c0 - t0 + i)) * l2g) : 0.f;
-    feature_store(kr, rk * P.kscale * wgt, P.pos_offset + c0 + i, qd, P, Kb[buf], i, false);
+    feature_store(kr, rk * P.kscale * wgt, P.pos_offset + c0 + i, qd, P, Kt, i, false);
     umma::fence_async_smem();
     sync_tc();
     if (tid == 0) {
-      const uint32_t a = umma::smem_u32(Kb[buf]), bv = umma::smem_u32(Vb[buf]);
+      const uint32_t a = umma::smem_u32(Kt), bv = umma::smem_u32(Vt);
 #pragma unroll
       for (int kk = 0; kk < ROWS / 16; ++kk)
         umma::mma_ss(tm, umma::desc_mnmajor(a, kk, ROWS), umma::desc_mnmajor(bv, kk, ROWS), idesc,
@@ -318,8 +318,8 @@ __global__ void __launch_bounds__(NT, 1)
       }
       if (tid == 0) {
         umma::mbar_expect_tx(&sh.bar_tma[buf], 2 * tile_bytes);
-        tma_tile(Kb[buf], &tmk, b, h, c0 + 2 * CV, &sh.bar_tma[buf]);
-        tma_tile(Vb[buf], &tmv, b, h, c0 + 2 * CV, &sh.bar_tma[buf]);
+        tma_tile(Kt, &tmk, b, h, c0 + 2 * CV, &sh.bar_tma[buf]);
+        tma_tile(Vt, &tmv, b, h, c0 + 2 * CV, &sh.bar_tma[buf]);
       }
     }
   }
@@ -357,9 +357,9 @@ struct OutShared {
 
 // Software-pipelined output pass over the tiles of one segment.  Iteration n:
 //   [A] wait for raw q, k of tile n (TMA, issued one iteration earlier)
+//   [D] q~, k~ in place (hides MMA3/MMA4 of tile n - 1)
 //   [W] wait for MMA3/MMA4 of tile n - 1; TMA v(n) and q, k(n + 1) into the freed buffers
-//   [B] max |S|, row sums of squares; [C] Sb = fp16 S 2^-e, S <- gamma^c S
-//   [D] q~, k~ in place; issue MMA1 (P) and MMA2 (O = Q~ Sb)
+//   [B] max |S|; [C] Sb = fp16 S 2^-e, S <- gamma^c S; issue MMA1 (P), MMA2 (O = Q~ Sb)
 //   [E] epilogue of tile n - 1 (overlaps MMA1/MMA2)
 //   [F] mask P -> Pm, scale O, k~ -> k~dec in place; issue MMA3 and MMA4
 // Shared memory: two (Q, K) buffer pairs, V, and one buffer shared by Sb and
@@ -369,8 +369,7 @@ __global__ void __launch_bounds__(NT, 1)
                      const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  unsigned char *Qb[2] = {base, base + 2 * TILE};
-  unsigned char *Kb[2] = {base + TILE, base + 3 * TILE};
+  // buffer pair j: Q at base + 2 j TILE, K at base + (2 j + 1) TILE
   unsigned char *Vs = base + 4 * TILE, *SP = base + 5 * TILE;
   OutShared &sh = *reinterpret_cast<OutShared *>(base + 6 * TILE);
 
@@ -405,8 +404,8 @@ __global__ void __launch_bounds__(NT, 1)
   if (tid == 0) {
     for (int n = 0; n < 2 && n < ntile; ++n) {
       umma::mbar_expect_tx(&sh.bar_qk[n], 2 * tile_bytes);
-      tma_tile(Qb[n], &tmq, b, h, t0 + n * CV, &sh.bar_qk[n]);
-      tma_tile(Kb[n], &tmk, b, h, t0 + n * CV, &sh.bar_qk[n]);
+      tma_tile(base + 2 * n * TILE, &tmq, b, h, t0 + n * CV, &sh.bar_qk[n]);
+      tma_tile(base + (2 * n + 1) * TILE, &tmk, b, h, t0 + n * CV, &sh.bar_qk[n]);
     }
     umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
     tma_tile(Vs, &tmv, b, h, t0, &sh.bar_v);
@@ -440,25 +439,34 @@ __global__ void __launch_bounds__(NT, 1)
     const bool valid = i < c;
     const uint32_t oc = tm + 128 + 128 * buf;          // O buffer of tile n
     const uint32_t op = tm + 128 + 128 * (buf ^ 1);    // O buffer of tile n - 1
-    unsigned char *Qt = Qb[buf], *Kt = Kb[buf];
+    unsigned char *Qt = base + 2 * buf * TILE, *Kt = Qt + TILE;
+    unsigned char *Qn = base + 2 * (buf ^ 1) * TILE, *Kn = Qn + TILE;  // the other pair
     uint4 gr[4];
     if (drain) {  // gate rows of tile n - 1, for its epilogue in [E]
       const bool okp = i < prev_c;
       load_quarter(gr, row_ptr(P.g, P, b, h, okp ? prev_c0 + i : prev_c0), qd, okp);
     }
-    uint4 qr[4], kr[4];
     if (have) {
-      // [A] raw q, k of tile n are in Qt / Kt
+      // [A] raw q, k of tile n are in Qt / Kt: row sums of squares
       if (wait_all(&sh.bar_qk[buf], (n >> 1) & 1)) {
         failed = true;
         break;
       }
+      uint4 qr[4], kr[4];
       ld_pairs(Qt, i, qd, qr);
       ld_pairs(Kt, i, qd, kr);
       if (!valid)  // rows past the tile hold stale bytes: use zeros
         qr[0] = qr[1] = qr[2] = qr[3] = kr[0] = kr[1] = kr[2] = kr[3] = make_uint4(0, 0, 0, 0);
       sh.red_q[qd][i] = sumsq_pairs(qr);
       sh.red_k[qd][i] = sumsq_pairs(kr);
+      __syncthreads();
+      // [D] q~ = RoPE(Norm(q)), k~ = RoPE(Norm(k)) / sqrt(d), fp16, in place.  Needs
+      //     nothing from the MMAs of tile n - 1, so it hides their latency.
+      const float rq = rsqrtf((sh.red_q[0][i] + sh.red_q[1][i] + sh.red_q[2][i] +
+                               sh.red_q[3][i]) / (float)D + P.eps);
+      const float rk = rsqrtf((sh.red_k[0][i] + sh.red_k[1][i] + sh.red_k[2][i] +
+                               sh.red_k[3][i]) / (float)D + P.eps) * P.kscale;
+      feature_qk_store(qr, kr, rq, rk, P.pos_offset + c0 + i, qd, P, Qt, Kt, i);
     }
     if (drain) {
       // [W] MMA3 / MMA4 of tile n - 1 are done: O(n-1) final, S current, V and
@@ -474,23 +482,20 @@ __global__ void __launch_bounds__(NT, 1)
         }
         if (n + 1 < ntile) {
           umma::mbar_expect_tx(&sh.bar_qk[buf ^ 1], 2 * tile_bytes);
-          tma_tile(Qb[buf ^ 1], &tmq, b, h, c0 + CV, &sh.bar_qk[buf ^ 1]);
-          tma_tile(Kb[buf ^ 1], &tmk, b, h, c0 + CV, &sh.bar_qk[buf ^ 1]);
+          tma_tile(Qn, &tmq, b, h, c0 + CV, &sh.bar_qk[buf ^ 1]);
+          tma_tile(Kn, &tmk, b, h, c0 + CV, &sh.bar_qk[buf ^ 1]);
         }
       }
     }
     float s_inv = 1.f;
     if (have) {
       // [B] max |S| over the tile (S is fp32 in TMEM)
+      float sv[32];
+      umma::tmem_ld2x16(myS, sv);
       {
         float m = 0.f;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          float v[16];
-          umma::tmem_ld16(myS + 16 * hf, v);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) m = fmaxf(m, fabsf(v[e]));
-        }
+        for (int e = 0; e < 32; ++e) m = fmaxf(m, fabsf(sv[e]));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (lane == 0) sh.smax[warp] = m;
@@ -507,29 +512,20 @@ __global__ void __launch_bounds__(NT, 1)
         s_inv = ldexpf(1.f, e);
         const float carry = sh.pw[c];
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          float v[16];
-          umma::tmem_ld16(myS + 16 * hf, v);
+        for (int u = 0; u < 4; ++u) {
+          float t[8];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            float t[8];
-#pragma unroll
-            for (int e2 = 0; e2 < 8; ++e2) t[e2] = v[8 * u + e2] * s_fwd;
-            *tile_at(SP, i, 4 * qd + 2 * hf + u) = pack8h(t);
-          }
-#pragma unroll
-          for (int e2 = 0; e2 < 16; ++e2) v[e2] *= carry;
-          umma::tmem_st16(myS + 16 * hf, v);
+          for (int e2 = 0; e2 < 8; ++e2) t[e2] = sv[8 * u + e2] * s_fwd;
+          *tile_at(SP, i, 4 * qd + u) = pack8h(t);
         }
-      }
-      // [D] q~ = RoPE(Norm(q)), k~ = RoPE(Norm(k)) / sqrt(d), fp16, in place (0 past the tile)
-      {
-        const float rq = rsqrtf((sh.red_q[0][i] + sh.red_q[1][i] + sh.red_q[2][i] +
-                                 sh.red_q[3][i]) / (float)D + P.eps);
-        const float rk = rsqrtf((sh.red_k[0][i] + sh.red_k[1][i] + sh.red_k[2][i] +
-                                 sh.red_k[3][i]) / (float)D + P.eps) * P.kscale;
-        feature_qk_store(qr, kr, valid ? rq : 0.f, valid ? rk : 0.f, P.pos_offset + c0 + i, qd, P,
-                         Qt, Kt, i);
+        float lo[16], hi[16];
+#pragma unroll
+        for (int e2 = 0; e2 < 16; ++e2) {
+          lo[e2] = sv[e2] * carry;
+          hi[e2] = sv[16 + e2] * carry;
+        }
+        umma::tmem_st16(myS, lo);
+        umma::tmem_st16(myS + 16, hi);
       }
       umma::tmem_wait_st();
       umma::fence_async_smem();
@@ -549,41 +545,31 @@ __global__ void __launch_bounds__(NT, 1)
     }
     // [E] epilogue of tile n - 1 (overlaps MMA1 / MMA2 of tile n)
     if (drain) {
-      const uint32_t myO = op + lane_base + 32 * qd;
+      float o[32];
+      umma::tmem_ld2x16(op + lane_base + 32 * qd, o);
       float ss = 0.f;
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float o[16];
-        umma::tmem_ld16(myO + 16 * hf, o);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) ss = fmaf(o[e], o[e], ss);
-      }
+      for (int e = 0; e < 32; ++e) ss = fmaf(o[e], o[e], ss);
       sh.red_o[qd][i] = ss;
       __syncthreads();
-      const bool okp = i < prev_c;
-      const float ro = rsqrtf((sh.red_o[0][i] + sh.red_o[1][i] + sh.red_o[2][i] +
-                               sh.red_o[3][i]) / (float)D + P.eps);
-      const size_t row = (((size_t)b * P.T + prev_c0 + (okp ? i : 0)) * P.H + h) * D + 32 * qd;
-      uint4 *y4 = reinterpret_cast<uint4 *>(y + row);
+      if (i < prev_c) {
+        const float ro = rsqrtf((sh.red_o[0][i] + sh.red_o[1][i] + sh.red_o[2][i] +
+                                 sh.red_o[3][i]) / (float)D + P.eps);
+        const size_t row = (((size_t)b * P.T + prev_c0 + i) * P.H + h) * D + 32 * qd;
+        uint4 *y4 = reinterpret_cast<uint4 *>(y + row);
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float o[16];
-        umma::tmem_ld16(myO + 16 * hf, o);
-        if (okp) {
+        for (int u = 0; u < 4; ++u) {
+          float gf[8], t[8];
+          unpack8(gr[u], gf);
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            float gf[8], t[8];
-            unpack8(gr[2 * hf + u], gf);
+          for (int e = 0; e < 8; ++e) t[e] = o[8 * u + e] * ro * sigmoid_fast(gf[e]);
+          y4[u] = pack8(t);
+        }
+        if (P.o) {
+          float4 *o4 = reinterpret_cast<float4 *>(P.o + row);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) t[e] = o[8 * u + e] * ro * sigmoid_fast(gf[e]);
-            y4[2 * hf + u] = pack8(t);
-          }
-          if (P.o) {
-            float4 *o4 = reinterpret_cast<float4 *>(P.o + row + 16 * hf);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              o4[u] = make_float4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
-          }
+          for (int u = 0; u < 8; ++u)
+            o4[u] = make_float4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
         }
       }
     }
@@ -593,40 +579,35 @@ __global__ void __launch_bounds__(NT, 1)
         failed = true;
         break;
       }
-      // mask: Pm = bf16((Q~ K~^T) (.) D) into SP (Sb is dead)
       {
+        float pv[32], ov[32];
+        umma::tmem_ld2x16(myP, pv);
+        umma::tmem_ld2x16(oc + lane_base + 32 * qd, ov);
+        // mask: Pm = bf16((Q~ K~^T) (.) D) into SP (Sb is dead)
         const int jlo = 32 * qd;
         const int jm = min(i, jlo + 31);
         float w = (valid && jm >= jlo) ? sh.pw[i - jm] : 0.f;
 #pragma unroll
-        for (int hf = 1; hf >= 0; --hf) {
-          float v[16];
-          umma::tmem_ld16(myP + 16 * hf, v);
-#pragma unroll
-          for (int e = 15; e >= 0; --e) {
-            if (jlo + 16 * hf + e <= i) {
-              v[e] *= w;
-              w *= gm;
-            } else {
-              v[e] = 0.f;
-            }
+        for (int e = 31; e >= 0; --e) {
+          if (jlo + e <= i) {
+            pv[e] *= w;
+            w *= gm;
+          } else {
+            pv[e] = 0.f;
           }
-          *tile_at(SP, i, 4 * qd + 2 * hf) = pack8(&v[0]);
-          *tile_at(SP, i, 4 * qd + 2 * hf + 1) = pack8(&v[8]);
         }
-      }
-      // O <- gamma^{i+1} 2^e O  (the Q~ S part, before MMA3 adds Pm V)
-      {
-        const uint32_t myO = oc + lane_base + 32 * qd;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) *tile_at(SP, i, 4 * qd + u) = pack8(&pv[8 * u]);
+        // O <- gamma^{i+1} 2^e O  (the Q~ S part, before MMA3 adds Pm V)
         const float f = sh.pw[i + 1] * s_inv;
+        float lo[16], hi[16];
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          float v[16];
-          umma::tmem_ld16(myO + 16 * hf, v);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] *= f;
-          umma::tmem_st16(myO + 16 * hf, v);
+        for (int e = 0; e < 16; ++e) {
+          lo[e] = ov[e] * f;
+          hi[e] = ov[16 + e] * f;
         }
+        umma::tmem_st16(oc + lane_base + 32 * qd, lo);
+        umma::tmem_st16(oc + lane_base + 32 * qd + 16, hi);
       }
       // k~dec = gamma^{c-1-i} k~ as bf16, in place (K~ is dead once MMA1 is done)
       {
