@@ -343,28 +343,60 @@ __global__ void __launch_bounds__(NT, 1)
 
 // ------------------------------------------------------------------ output pass
 
+constexpr int NWORK = 16;              // worker warps (CUDA-core work), 4 warpgroups
+constexpr int NTO = (NWORK + 4) * 32;  // + one warpgroup: its first warp issues MMAs / TMA copies
+                                       // (registers are granted per warpgroup, so a lone 17th
+                                       // warp would cost as much as four)
+
 struct OutShared {
-  float red_q[4][ROWS];
-  float red_k[4][ROWS];
   float red_o[4][ROWS];
   float pw[ROWS + 1];
-  float smax[NT / 32];
-  uint64_t bar_mma[2];  // [0]: MMA1 + MMA2 done, [1]: MMA3 + MMA4 done
+  float smax[NWORK];
+  uint64_t bar_mma[2];  // [0]: MMA1 + MMA2 of a tile done, [1]: MMA3 + MMA4 done (commits)
   uint64_t bar_qk[2];   // TMA of raw q, k into buffer pair 0 / 1
   uint64_t bar_v;       // TMA of raw v
+  uint64_t bar_feat;    // workers: q~, k~ of the tile written (one arrive per warp)
+  uint64_t bar_sb;      // workers: Sb written and S rescaled
+  uint64_t bar_pm;      // workers: Pm, scaled O and k~dec written
   uint32_t tmem_base;
+  uint32_t failed;
 };
 
-// Software-pipelined output pass over the tiles of one segment.  Iteration n:
-//   [A] wait for raw q, k of tile n (TMA, issued one iteration earlier)
-//   [D] q~, k~ in place (hides MMA3/MMA4 of tile n - 1)
-//   [W] wait for MMA3/MMA4 of tile n - 1; TMA v(n) and q, k(n + 1) into the freed buffers
-//   [B] max |S|; [C] Sb = fp16 S 2^-e, S <- gamma^c S; issue MMA1 (P), MMA2 (O = Q~ Sb)
-//   [E] epilogue of tile n - 1 (overlaps MMA1/MMA2)
-//   [F] mask P -> Pm, scale O, k~ -> k~dec in place; issue MMA3 and MMA4
-// Shared memory: two (Q, K) buffer pairs, V, and one buffer shared by Sb and
-// Pm (Sb is dead once MMA2 is done, Pm is dead once MMA3 is done).
-__global__ void __launch_bounds__(NT, 1)
+// Named barrier among `nthreads` threads (ids 1..15; id 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Bounded wait that becomes a no-op once this thread has seen a timeout, so a
+// failure never strands other warps at a barrier: the loop runs to its end
+// with invalid data and the status word reports it.
+__device__ __forceinline__ void wait_or_fail(uint64_t *bar, uint32_t parity, bool &failed) {
+  if (!failed && !umma::mbar_wait(bar, parity)) failed = true;
+  umma::fence_after();
+}
+
+// One elected arrive per warp on a worker-count barrier, after the warp's
+// shared-memory writes (generic proxy) and TMEM stores are complete.
+__device__ __forceinline__ void warp_arrive(uint64_t *bar, int lane) {
+  umma::fence_async_smem();
+  umma::fence_before();
+  __syncwarp();
+  if (lane == 0) umma::mbar_arrive(bar);
+}
+
+// Output pass over the tiles of one segment, warp-specialized.
+//   Issuer warp (warp 16): per tile n, waits for the workers' barriers and
+//   issues MMA1 (P = Q~ K~^T), MMA2 (O = Q~ Sb), MMA3 (O += Pm V) and MMA4
+//   (S += K~dec^T V), then the TMA copies that refill the freed buffers.
+//   Worker warps (0..15), per tile n:
+//     [A]/[D] raw q, k -> row norms (warp shuffles) -> q~, k~ fp16 in place
+//     [B]/[C] after MMA3/MMA4 of tile n - 1: Sb = fp16(S 2^-e) with one power
+//             of two per column quarter, S <- gamma^c S
+//     [E]     epilogue of tile n - 1 (overlaps MMA1/MMA2 of tile n)
+//     [F]     after MMA1/MMA2: mask P -> Pm, O <- gamma^{i+1} 2^e O, k~ -> k~dec
+// The only CTA-wide barriers are outside the tile loop; the two reductions
+// (max |S| per column quarter, the RMS of o per row) use 4-warp named barriers.
+__global__ void __launch_bounds__(NTO, 1)
     tc_output_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmq,
                      const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ unsigned char smem_raw[];
@@ -374,7 +406,6 @@ __global__ void __launch_bounds__(NT, 1)
   OutShared &sh = *reinterpret_cast<OutShared *>(base + 6 * TILE);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int sub = warp & 3, qd = warp >> 2, i = 32 * sub + lane;
   const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int t0 = g * P.seg_len, t1 = min(P.T, t0 + P.seg_len);
   const int CV = P.chunk;
@@ -389,128 +420,160 @@ __global__ void __launch_bounds__(NT, 1)
       umma::mbar_init(&sh.bar_qk[j], 1);
     }
     umma::mbar_init(&sh.bar_v, 1);
+    umma::mbar_init(&sh.bar_feat, NWORK);
+    umma::mbar_init(&sh.bar_sb, NWORK);
+    umma::mbar_init(&sh.bar_pm, NWORK);
     umma::mbar_fence_init();
+    sh.failed = 0;
   }
   if (tid <= ROWS) sh.pw[tid] = exp2f((float)tid * l2g);
   if (warp == 0) umma::tmem_alloc(&sh.tmem_base, 512);
   if (CV < ROWS)  // rows [CV, 128) of V are never written by TMA: clear them once
-    for (int e = tid; e < (ROWS - CV) * 16; e += NT)
+    for (int e = tid; e < (ROWS - CV) * 16; e += NTO)
       *tile_at(Vs, CV + e / 16, e % 16) = make_uint4(0, 0, 0, 0);
   sync_tc();
   const uint32_t tm = sh.tmem_base;
-  const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
   const uint32_t tP = tm, tS = tm + 384;
-  const uint32_t myS = tS + lane_base + 32 * qd, myP = tP + lane_base + 32 * qd;
-  if (tid == 0) {
-    for (int n = 0; n < 2 && n < ntile; ++n) {
-      umma::mbar_expect_tx(&sh.bar_qk[n], 2 * tile_bytes);
-      tma_tile(base + 2 * n * TILE, &tmq, b, h, t0 + n * CV, &sh.bar_qk[n]);
-      tma_tile(base + (2 * n + 1) * TILE, &tmk, b, h, t0 + n * CV, &sh.bar_qk[n]);
-    }
-    umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
-    tma_tile(Vs, &tmv, b, h, t0, &sh.bar_v);
-  }
-  // entering state of the segment -> TMEM (fp32)
-  {
-    const float *sin_ = P.seg + (((size_t)b * P.H + h) * P.nseg + g) * (size_t)D * D;
-    const float4 *s4 = reinterpret_cast<const float4 *>(sin_ + (size_t)i * D + 32 * qd);
-    float v[32];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float4 x = s4[u];
-      v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
-    }
-    umma::tmem_st32(myS, v);
-    umma::tmem_wait_st();
-  }
-
-  const uint32_t id_qk = umma::idesc_bf16(128, 128, false, false, true);  // fp16 Q~ K~^T
-  const uint32_t id_qs = umma::idesc_bf16(128, 128, false, true, true);   // fp16 Q~ S
-  const uint32_t id_pv = umma::idesc_bf16(128, 128, false, true);         // bf16 Pm V
-  const uint32_t id_mn = umma::idesc_bf16(128, 128, true, true);          // bf16 K~dec^T V
-  __nv_bfloat16 *y = (__nv_bfloat16 *)P.y;
-
   bool failed = false;
-  int prev_c0 = 0, prev_c = 0;
-  for (int n = 0; n <= ntile; ++n) {
-    const bool have = n < ntile, drain = n >= 1;
-    const int c0 = t0 + n * CV, c = have ? min(CV, t1 - c0) : 0;
-    const int buf = n & 1;
-    const bool valid = i < c;
-    const uint32_t oc = tm + 128 + 128 * buf;          // O buffer of tile n
-    const uint32_t op = tm + 128 + 128 * (buf ^ 1);    // O buffer of tile n - 1
-    unsigned char *Qt = base + 2 * buf * TILE, *Kt = Qt + TILE;
-    unsigned char *Qn = base + 2 * (buf ^ 1) * TILE, *Kn = Qn + TILE;  // the other pair
-    uint4 gr[4];
-    if (drain) {  // gate rows of tile n - 1, for its epilogue in [E]
-      const bool okp = i < prev_c;
-      load_quarter(gr, row_ptr(P.g, P, b, h, okp ? prev_c0 + i : prev_c0), qd, okp);
-    }
-    if (have) {
-      // [A] raw q, k of tile n are in Qt / Kt: row sums of squares
-      if (wait_all(&sh.bar_qk[buf], (n >> 1) & 1)) {
-        failed = true;
-        break;
+
+  if (warp >= NWORK) {
+    // ---------------------------------------------------------------- issuer warpgroup
+    if (warp == NWORK && lane == 0) {
+      const uint32_t id_qk = umma::idesc_bf16(128, 128, false, false, true);  // fp16 Q~ K~^T
+      const uint32_t id_qs = umma::idesc_bf16(128, 128, false, true, true);   // fp16 Q~ S
+      const uint32_t id_pv = umma::idesc_bf16(128, 128, false, true);         // bf16 Pm V
+      const uint32_t id_mn = umma::idesc_bf16(128, 128, true, true);          // bf16 K~dec^T V
+      for (int n = 0; n < 2 && n < ntile; ++n) {
+        umma::mbar_expect_tx(&sh.bar_qk[n], 2 * tile_bytes);
+        tma_tile(base + 2 * n * TILE, &tmq, b, h, t0 + n * CV, &sh.bar_qk[n]);
+        tma_tile(base + (2 * n + 1) * TILE, &tmk, b, h, t0 + n * CV, &sh.bar_qk[n]);
       }
-      uint4 qr[4], kr[4];
-      ld_pairs(Qt, i, qd, qr);
-      ld_pairs(Kt, i, qd, kr);
-      if (!valid)  // rows past the tile hold stale bytes: use zeros
-        qr[0] = qr[1] = qr[2] = qr[3] = kr[0] = kr[1] = kr[2] = kr[3] = make_uint4(0, 0, 0, 0);
-      sh.red_q[qd][i] = sumsq_pairs(qr);
-      sh.red_k[qd][i] = sumsq_pairs(kr);
-      __syncthreads();
-      // [D] q~ = RoPE(Norm(q)), k~ = RoPE(Norm(k)) / sqrt(d), fp16, in place.  Needs
-      //     nothing from the MMAs of tile n - 1, so it hides their latency.
-      const float rq = rsqrtf((sh.red_q[0][i] + sh.red_q[1][i] + sh.red_q[2][i] +
-                               sh.red_q[3][i]) / (float)D + P.eps);
-      const float rk = rsqrtf((sh.red_k[0][i] + sh.red_k[1][i] + sh.red_k[2][i] +
-                               sh.red_k[3][i]) / (float)D + P.eps) * P.kscale;
-      feature_qk_store(qr, kr, rq, rk, P.pos_offset + c0 + i, qd, P, Qt, Kt, i);
-    }
-    if (drain) {
-      // [W] MMA3 / MMA4 of tile n - 1 are done: O(n-1) final, S current, V and
-      //     SP free, buffer pair (n + 1) & 1 free.
-      if (wait_all(&sh.bar_mma[1], (n - 1) & 1)) {
-        failed = true;
-        break;
-      }
-      if (tid == 0) {
-        if (have) {
-          umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
-          tma_tile(Vs, &tmv, b, h, c0, &sh.bar_v);
+      umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
+      tma_tile(Vs, &tmv, b, h, t0, &sh.bar_v);
+      for (int n = 0; n < ntile; ++n) {
+        const int buf = n & 1;
+        const uint32_t aq = umma::smem_u32(base + 2 * buf * TILE);
+        const uint32_t ak = aq + TILE;
+        const uint32_t as = umma::smem_u32(SP), av = umma::smem_u32(Vs);
+        const uint32_t ocur = tm + 128 + 128 * buf;
+        wait_or_fail(&sh.bar_feat, n & 1, failed);
+        if (!failed)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma::mma_ss(tP, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(ak, kk, ROWS),
+                         id_qk, kk > 0);
+        wait_or_fail(&sh.bar_sb, n & 1, failed);
+        if (!failed) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma::mma_ss(ocur, umma::desc_kmajor(aq, kk, ROWS), umma::desc_mnmajor(as, kk, ROWS),
+                         id_qs, kk > 0);
+          umma::commit(&sh.bar_mma[0]);
         }
-        if (n + 1 < ntile) {
-          umma::mbar_expect_tx(&sh.bar_qk[buf ^ 1], 2 * tile_bytes);
-          tma_tile(Qn, &tmq, b, h, c0 + CV, &sh.bar_qk[buf ^ 1]);
-          tma_tile(Kn, &tmk, b, h, c0 + CV, &sh.bar_qk[buf ^ 1]);
+        wait_or_fail(&sh.bar_pm, n & 1, failed);
+        wait_or_fail(&sh.bar_v, n & 1, failed);
+        if (!failed) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma::mma_ss(ocur, umma::desc_kmajor(as, kk, ROWS), umma::desc_mnmajor(av, kk, ROWS),
+                         id_pv, 1u);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma::mma_ss(tS, umma::desc_mnmajor(ak, kk, ROWS), umma::desc_mnmajor(av, kk, ROWS),
+                         id_mn, 1u);
+          umma::commit(&sh.bar_mma[1]);
+        }
+        // MMA3 / MMA4 done: V and buffer pair `buf` are free for the next copies
+        wait_or_fail(&sh.bar_mma[1], n & 1, failed);
+        if (!failed) {
+          const int c0 = t0 + n * CV;
+          if (n + 1 < ntile) {
+            umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
+            tma_tile(Vs, &tmv, b, h, c0 + CV, &sh.bar_v);
+          }
+          if (n + 2 < ntile) {
+            umma::mbar_expect_tx(&sh.bar_qk[buf], 2 * tile_bytes);
+            tma_tile(base + 2 * buf * TILE, &tmq, b, h, c0 + 2 * CV, &sh.bar_qk[buf]);
+            tma_tile(base + (2 * buf + 1) * TILE, &tmk, b, h, c0 + 2 * CV, &sh.bar_qk[buf]);
+          }
         }
       }
     }
-    float s_inv = 1.f;
-    if (have) {
-      // [B] max |S| over the tile (S is fp32 in TMEM)
-      float sv[32];
-      umma::tmem_ld2x16(myS, sv);
-      {
+  } else {
+    // ---------------------------------------------------------------- worker warps
+    const int sub = warp & 3, qd = warp >> 2, i = 32 * sub + lane;  // TMEM phases
+    const int fr = 8 * warp + (lane >> 2), fu = lane & 3;           // feature map: row, quarter
+    const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
+    const uint32_t col = 32 * qd;
+    const uint32_t myS = tS + lane_base + col, myP = tP + lane_base + col;
+    // entering state of the segment -> TMEM (fp32)
+    {
+      const float *sin_ = P.seg + (((size_t)b * P.H + h) * P.nseg + g) * (size_t)D * D;
+      const float4 *s4 = reinterpret_cast<const float4 *>(sin_ + (size_t)i * D + col);
+      float v[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float4 x = s4[u];
+        v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
+      }
+      umma::tmem_st32(myS, v);
+      umma::tmem_wait_st();
+    }
+    __nv_bfloat16 *y = (__nv_bfloat16 *)P.y;
+    int prev_c0 = 0, prev_c = 0;
+    for (int n = 0; n <= ntile; ++n) {
+      const bool have = n < ntile, drain = n >= 1;
+      const int c0 = t0 + n * CV, c = have ? min(CV, t1 - c0) : 0;
+      const int buf = n & 1;
+      const bool valid = i < c;
+      const uint32_t ocur = tm + 128 + 128 * buf;        // O buffer of tile n
+      const uint32_t oprev = tm + 128 + 128 * (buf ^ 1); // O buffer of tile n - 1
+      unsigned char *Qt = base + 2 * buf * TILE, *Kt = Qt + TILE;
+      uint4 gr[4];
+      if (drain) {  // gate of tile n - 1, for [E]
+        const bool okp = i < prev_c;
+        load_quarter(gr, row_ptr(P.g, P, b, h, okp ? prev_c0 + i : prev_c0), qd, okp);
+      }
+      if (have) {
+        // [A] raw q, k of tile n: row fr, pairs [16 fu, 16 fu + 16); norms by shuffles
+        wait_or_fail(&sh.bar_qk[buf], (n >> 1) & 1, failed);
+        uint4 qr[4], kr[4];
+        ld_pairs(Qt, fr, fu, qr);
+        ld_pairs(Kt, fr, fu, kr);
+        const bool fvalid = fr < c;
+        if (!fvalid)  // rows past the tile hold stale bytes: use zeros
+          qr[0] = qr[1] = qr[2] = qr[3] = kr[0] = kr[1] = kr[2] = kr[3] = make_uint4(0, 0, 0, 0);
+        float sq = sumsq_pairs(qr), sk = sumsq_pairs(kr);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+        sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+        sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+        // [D] q~ = RoPE(Norm(q)), k~ = RoPE(Norm(k)) / sqrt(d), fp16, in place
+        const float rq = rsqrtf(sq / (float)D + P.eps);
+        const float rk = rsqrtf(sk / (float)D + P.eps) * P.kscale;
+        feature_qk_store(qr, kr, rq, rk, P.pos_offset + c0 + fr, fu, P, Qt, Kt, fr);
+        warp_arrive(&sh.bar_feat, lane);
+      }
+      if (drain) wait_or_fail(&sh.bar_mma[1], (n - 1) & 1, failed);  // O(n-1), S, SP ready
+      float s_inv = 1.f;
+      if (have) {
+        // [B] max |S| over this column quarter (4 warps)
+        float sv[32];
+        umma::tmem_ld2x16(myS, sv);
         float m = 0.f;
 #pragma unroll
         for (int e = 0; e < 32; ++e) m = fmaxf(m, fabsf(sv[e]));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (lane == 0) sh.smax[warp] = m;
-      }
-      __syncthreads();
-      // [C] Sb = fp16(S 2^-e) with 2^e >= max |S|, then S <- gamma^c S
-      {
-        float m = 0.f;
-#pragma unroll
-        for (int w = 0; w < NT / 32; ++w) m = fmaxf(m, sh.smax[w]);
+        named_sync(1 + qd, 128);
+        m = fmaxf(fmaxf(sh.smax[4 * qd], sh.smax[4 * qd + 1]),
+                  fmaxf(sh.smax[4 * qd + 2], sh.smax[4 * qd + 3]));
+        // [C] Sb = fp16(S 2^-e) with 2^e >= max |S| of the quarter, then S <- gamma^c S
         int e = 0;
         if (m > 0.f) frexpf(m, &e);
         const float s_fwd = ldexpf(1.f, -e);
         s_inv = ldexpf(1.f, e);
-        const float carry = sh.pw[c];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           float t[8];
@@ -518,6 +581,7 @@ __global__ void __launch_bounds__(NT, 1)
           for (int e2 = 0; e2 < 8; ++e2) t[e2] = sv[8 * u + e2] * s_fwd;
           *tile_at(SP, i, 4 * qd + u) = pack8h(t);
         }
+        const float carry = sh.pw[c];
         float lo[16], hi[16];
 #pragma unroll
         for (int e2 = 0; e2 < 16; ++e2) {
@@ -526,128 +590,95 @@ __global__ void __launch_bounds__(NT, 1)
         }
         umma::tmem_st16(myS, lo);
         umma::tmem_st16(myS + 16, hi);
+        umma::tmem_wait_st();
+        warp_arrive(&sh.bar_sb, lane);
       }
-      umma::tmem_wait_st();
-      umma::fence_async_smem();
-      sync_tc();
-      if (tid == 0) {
-        const uint32_t aq = umma::smem_u32(Qt), ak = umma::smem_u32(Kt), as = umma::smem_u32(SP);
+      // [E] epilogue of tile n - 1 (overlaps MMA1 / MMA2 of tile n)
+      if (drain) {
+        float o[32];
+        umma::tmem_ld2x16(oprev + lane_base + col, o);
+        float ss = 0.f;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma::mma_ss(tP, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(ak, kk, ROWS), id_qk,
-                       kk > 0);
+        for (int e = 0; e < 32; ++e) ss = fmaf(o[e], o[e], ss);
+        sh.red_o[qd][i] = ss;
+        named_sync(5 + sub, 128);
+        if (i < prev_c) {
+          const float ro = rsqrtf((sh.red_o[0][i] + sh.red_o[1][i] + sh.red_o[2][i] +
+                                   sh.red_o[3][i]) / (float)D + P.eps);
+          const size_t row = (((size_t)b * P.T + prev_c0 + i) * P.H + h) * D + col;
+          uint4 *y4 = reinterpret_cast<uint4 *>(y + row);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma::mma_ss(oc, umma::desc_kmajor(aq, kk, ROWS), umma::desc_mnmajor(as, kk, ROWS), id_qs,
-                       kk > 0);
-        umma::commit(&sh.bar_mma[0]);
-      }
-    }
-    // [E] epilogue of tile n - 1 (overlaps MMA1 / MMA2 of tile n)
-    if (drain) {
-      float o[32];
-      umma::tmem_ld2x16(op + lane_base + 32 * qd, o);
-      float ss = 0.f;
+          for (int u = 0; u < 4; ++u) {
+            float gf[8], t[8];
+            unpack8(gr[u], gf);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) ss = fmaf(o[e], o[e], ss);
-      sh.red_o[qd][i] = ss;
-      __syncthreads();
-      if (i < prev_c) {
-        const float ro = rsqrtf((sh.red_o[0][i] + sh.red_o[1][i] + sh.red_o[2][i] +
-                                 sh.red_o[3][i]) / (float)D + P.eps);
-        const size_t row = (((size_t)b * P.T + prev_c0 + i) * P.H + h) * D + 32 * qd;
-        uint4 *y4 = reinterpret_cast<uint4 *>(y + row);
+            for (int e = 0; e < 8; ++e) t[e] = o[8 * u + e] * ro * sigmoid_fast(gf[e]);
+            y4[u] = pack8(t);
+          }
+          if (P.o) {
+            float4 *o4 = reinterpret_cast<float4 *>(P.o + row);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          float gf[8], t[8];
-          unpack8(gr[u], gf);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) t[e] = o[8 * u + e] * ro * sigmoid_fast(gf[e]);
-          y4[u] = pack8(t);
-        }
-        if (P.o) {
-          float4 *o4 = reinterpret_cast<float4 *>(P.o + row);
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            o4[u] = make_float4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
-        }
-      }
-    }
-    if (have) {
-      // [F] MMA1 / MMA2 of tile n done
-      if (wait_all(&sh.bar_mma[0], n & 1)) {
-        failed = true;
-        break;
-      }
-      {
-        float pv[32], ov[32];
-        umma::tmem_ld2x16(myP, pv);
-        umma::tmem_ld2x16(oc + lane_base + 32 * qd, ov);
-        // mask: Pm = bf16((Q~ K~^T) (.) D) into SP (Sb is dead)
-        const int jlo = 32 * qd;
-        const int jm = min(i, jlo + 31);
-        float w = (valid && jm >= jlo) ? sh.pw[i - jm] : 0.f;
-#pragma unroll
-        for (int e = 31; e >= 0; --e) {
-          if (jlo + e <= i) {
-            pv[e] *= w;
-            w *= gm;
-          } else {
-            pv[e] = 0.f;
+            for (int u = 0; u < 8; ++u)
+              o4[u] = make_float4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
           }
         }
+      }
+      if (have) {
+        // [F] MMA1 / MMA2 of tile n done
+        wait_or_fail(&sh.bar_mma[0], n & 1, failed);
+        {
+          float pv[32], ov[32];
+          umma::tmem_ld2x16(myP, pv);
+          umma::tmem_ld2x16(ocur + lane_base + col, ov);
+          // mask: Pm = bf16((Q~ K~^T) (.) D) into SP (Sb is dead)
+          const int jlo = (int)col;
+          const int jm = min(i, jlo + 31);
+          float w = (valid && jm >= jlo) ? sh.pw[i - jm] : 0.f;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) *tile_at(SP, i, 4 * qd + u) = pack8(&pv[8 * u]);
-        // O <- gamma^{i+1} 2^e O  (the Q~ S part, before MMA3 adds Pm V)
-        const float f = sh.pw[i + 1] * s_inv;
-        float lo[16], hi[16];
+          for (int e = 31; e >= 0; --e) {
+            if (jlo + e <= i) {
+              pv[e] *= w;
+              w *= gm;
+            } else {
+              pv[e] = 0.f;
+            }
+          }
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          lo[e] = ov[e] * f;
-          hi[e] = ov[16 + e] * f;
+          for (int u = 0; u < 4; ++u) *tile_at(SP, i, 4 * qd + u) = pack8(&pv[8 * u]);
+          // O <- gamma^{i+1} 2^e O  (the Q~ S part, before MMA3 adds Pm V)
+          const float f = sh.pw[i + 1] * s_inv;
+          float lo[16], hi[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            lo[e] = ov[e] * f;
+            hi[e] = ov[16 + e] * f;
+          }
+          umma::tmem_st16(ocur + lane_base + col, lo);
+          umma::tmem_st16(ocur + lane_base + col + 16, hi);
         }
-        umma::tmem_st16(oc + lane_base + 32 * qd, lo);
-        umma::tmem_st16(oc + lane_base + 32 * qd + 16, hi);
-      }
-      // k~dec = gamma^{c-1-i} k~ as bf16, in place (K~ is dead once MMA1 is done)
-      {
-        const float wk = valid ? sh.pw[c - 1 - i] : 0.f;
-        const int ch[4] = {2 * qd, 2 * qd + 1, 8 + 2 * qd, 9 + 2 * qd};
+        // k~dec = gamma^{c-1-i} k~ as bf16, in place (K~ is dead once MMA1 is done)
+        {
+          const float wk = valid ? sh.pw[c - 1 - i] : 0.f;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          uint4 *p = tile_at(Kt, i, ch[u]);
-          float f[8];
-          unpack8h(*p, f);
+          for (int u = 0; u < 4; ++u) {
+            uint4 *p = tile_at(Kt, i, 4 * qd + u);
+            float f[8];
+            unpack8h(*p, f);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] *= wk;
-          *p = pack8(f);
+            for (int e = 0; e < 8; ++e) f[e] *= wk;
+            *p = pack8(f);
+          }
         }
+        umma::tmem_wait_st();
+        warp_arrive(&sh.bar_pm, lane);
+        prev_c0 = c0;
+        prev_c = c;
       }
-      if (wait_all(&sh.bar_v, n & 1)) {  // raw v of tile n is in Vs
-        failed = true;
-        break;
-      }
-      umma::tmem_wait_st();
-      umma::fence_async_smem();
-      sync_tc();
-      if (tid == 0) {
-        const uint32_t ap = umma::smem_u32(SP), av = umma::smem_u32(Vs), ad = umma::smem_u32(Kt);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma::mma_ss(oc, umma::desc_kmajor(ap, kk, ROWS), umma::desc_mnmajor(av, kk, ROWS), id_pv,
-                       1u);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma::mma_ss(tS, umma::desc_mnmajor(ad, kk, ROWS), umma::desc_mnmajor(av, kk, ROWS), id_mn,
-                       1u);
-        umma::commit(&sh.bar_mma[1]);
-      }
-      prev_c0 = c0;
-      prev_c = c;
     }
   }
-  if (failed && tid == 0 && P.err) atomicOr(P.err, 2u);
+  if (failed) atomicOr(&sh.failed, 1u);
   sync_tc();
+  if (sh.failed && tid == 0 && P.err) atomicOr(P.err, 2u);
   if (warp == 0) umma::tmem_dealloc(tm, 512);
 }
 
@@ -716,7 +747,7 @@ cudaError_t launch_tc_seg_output(const MixerParams &P, cudaStream_t st) {
   e = cudaFuncSetAttribute(tc::tc_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)tc::kOutputSmem);
   if (e != cudaSuccess) return e;
-  tc::tc_output_kernel<<<dim3(P.nseg, P.H, P.B), tc::NT, tc::kOutputSmem, st>>>(P, mq, mk, mv);
+  tc::tc_output_kernel<<<dim3(P.nseg, P.H, P.B), tc::NTO, tc::kOutputSmem, st>>>(P, mq, mk, mv);
   return cudaGetLastError();
 }
 
