@@ -353,6 +353,7 @@ struct OutShared {
   float pw[ROWS + 1];
   float smax[NWORK];
   uint64_t bar_mma[2];  // [0]: MMA1 + MMA2 of a tile done, [1]: MMA3 + MMA4 done (commits)
+  uint64_t bar_p;       // MMA1 (P) of a tile done
   uint64_t bar_qk[2];   // TMA of raw q, k into buffer pair 0 / 1
   uint64_t bar_v;       // TMA of raw v
   uint64_t bar_feat;    // workers: q~, k~ of the tile written (one arrive per warp)
@@ -420,6 +421,7 @@ __global__ void __launch_bounds__(NTO, 1)
       umma::mbar_init(&sh.bar_qk[j], 1);
     }
     umma::mbar_init(&sh.bar_v, 1);
+    umma::mbar_init(&sh.bar_p, 1);
     umma::mbar_init(&sh.bar_feat, NWORK);
     umma::mbar_init(&sh.bar_sb, NWORK);
     umma::mbar_init(&sh.bar_pm, NWORK);
@@ -457,11 +459,13 @@ __global__ void __launch_bounds__(NTO, 1)
         const uint32_t as = umma::smem_u32(SP), av = umma::smem_u32(Vs);
         const uint32_t ocur = tm + 128 + 128 * buf;
         wait_or_fail(&sh.bar_feat, n & 1, failed);
-        if (!failed)
+        if (!failed) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma::mma_ss(tP, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(ak, kk, ROWS),
                          id_qk, kk > 0);
+          umma::commit(&sh.bar_p);
+        }
         wait_or_fail(&sh.bar_sb, n & 1, failed);
         if (!failed) {
 #pragma unroll
@@ -624,13 +628,12 @@ __global__ void __launch_bounds__(NTO, 1)
         }
       }
       if (have) {
-        // [F] MMA1 / MMA2 of tile n done
-        wait_or_fail(&sh.bar_mma[0], n & 1, failed);
+        // [F] MMA1 of tile n done: mask P
+        wait_or_fail(&sh.bar_p, n & 1, failed);
         {
-          float pv[32], ov[32];
+          float pv[32];
           umma::tmem_ld2x16(myP, pv);
-          umma::tmem_ld2x16(ocur + lane_base + col, ov);
-          // mask: Pm = bf16((Q~ K~^T) (.) D) into SP (Sb is dead)
+          // mask: Pm = bf16((Q~ K~^T) (.) D) into SP (Sb is dead once MMA2 is done)
           const int jlo = (int)col;
           const int jm = min(i, jlo + 31);
           float w = (valid && jm >= jlo) ? sh.pw[i - jm] : 0.f;
@@ -643,9 +646,13 @@ __global__ void __launch_bounds__(NTO, 1)
               pv[e] = 0.f;
             }
           }
+          // MMA2 of tile n done: Sb is dead and the Q~ S part of O is ready
+          wait_or_fail(&sh.bar_mma[0], n & 1, failed);
 #pragma unroll
           for (int u = 0; u < 4; ++u) *tile_at(SP, i, 4 * qd + u) = pack8(&pv[8 * u]);
           // O <- gamma^{i+1} 2^e O  (the Q~ S part, before MMA3 adds Pm V)
+          float ov[32];
+          umma::tmem_ld2x16(ocur + lane_base + col, ov);
           const float f = sh.pw[i + 1] * s_inv;
           float lo[16], hi[16];
 #pragma unroll
