@@ -533,11 +533,6 @@ __global__ void __launch_bounds__(NTO, 1)
       const uint32_t ocur = tm + 128 + 128 * buf;        // O buffer of tile n
       const uint32_t oprev = tm + 128 + 128 * (buf ^ 1); // O buffer of tile n - 1
       unsigned char *Qt = base + 2 * buf * TILE, *Kt = Qt + TILE;
-      uint4 gr[4];
-      if (drain) {  // gate of tile n - 1, for [E]
-        const bool okp = i < prev_c;
-        load_quarter(gr, row_ptr(P.g, P, b, h, okp ? prev_c0 + i : prev_c0), qd, okp);
-      }
       if (have) {
         // [A] raw q, k of tile n: row fr, pairs [16 fu, 16 fu + 16); norms by shuffles
         wait_or_fail(&sh.bar_qk[buf], (n >> 1) & 1, failed);
@@ -599,6 +594,9 @@ __global__ void __launch_bounds__(NTO, 1)
       }
       // [E] epilogue of tile n - 1 (overlaps MMA1 / MMA2 of tile n)
       if (drain) {
+        uint4 gr[4];  // gate of tile n - 1 (issued late so it does not queue ahead of [A])
+        const bool okp = i < prev_c;
+        load_quarter(gr, row_ptr(P.g, P, b, h, okp ? prev_c0 + i : prev_c0), qd, okp);
         float o[32];
         umma::tmem_ld2x16(oprev + lane_base + col, o);
         float ss = 0.f;
