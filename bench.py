@@ -48,6 +48,27 @@ def parse():
     return p.parse_args()
 
 
+def measured_traffic(token_heads):
+    """DRAM bytes per launch of tc_output_kernel from the committed ncu summary,
+    scaled to `token_heads`; None when the kernel source changed since the capture."""
+    import hashlib
+    import re
+    path = os.path.join(ROOT, "profiles", "traffic_tc_output.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_b = re.search(r"bytes_per_token_head:\s*([0-9.]+)", text)
+    m_s = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    if not (m_b and m_s):
+        return None
+    h = hashlib.sha256()
+    for f in ("tc_prefill.cu", "umma.cuh"):
+        h.update(open(os.path.join(ROOT, "rnn_sequence_mixer_gb300", "csrc", f), "rb").read())
+    if h.hexdigest() != m_s.group(1):
+        return None
+    return float(m_b.group(1)) * token_heads
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -277,8 +298,10 @@ def run_ours(args):
     a_bytes = alg[pass_names[dom]]
     achieved = a_bytes / (pass_ms[dom] / 1e3) / 1e9
     whole = th * 5 * w.d * BF16 / (ms / 1e3) / 1e9
+    traffic = measured_traffic(th) if pass_names[dom] == "seg_output" else None
     roof = {"kernel": pass_names[dom], "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
-            "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
+            "unit": "GB/s", "frac": achieved / hbm_peak,
+            "traffic": traffic / 1e9 if traffic else None, "traffic_unit": "GB per launch",
             "peak_source": f"hbm_gbs of {peak_src}",
             "pass_ms": dict(zip(pass_names, pass_ms)),
             "whole_call": {"alg_bytes": th * 5 * w.d * BF16, "achieved": whole,
