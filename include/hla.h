@@ -200,7 +200,10 @@ size_t hla_backward_workspace_size(const hla_shape *shape);
  *   dstate_out  in:  fp32 [B, H, d, d] gradient of state_out; NULL = zeros
  *   dq, dk, dv, dgate  out: [B, T, H, d], shape->dtype
  *   dstate_in   out: fp32 [B, H, d, d] gradient of state_in; NULL = skip
- *   ws, ws_bytes     device scratch of hla_backward_workspace_size() bytes
+ *   ws, ws_bytes     device scratch of hla_backward_workspace_size() bytes;
+ *                    as for hla_prefill, its last 256 bytes hold the device
+ *                    status word (non-zero after completion: a bounded wait
+ *                    gave up and the gradients are not valid)
  * The forward quantities it needs (o and the per-chunk states) are
  * recomputed, not stored by hla_prefill.
  */

@@ -174,7 +174,7 @@ size_t hla_backward_workspace_size(const hla_shape *s) {
   if (check_shape(s, false) != HLA_OK) return 0;
   Plan p = make_plan(*s);
   size_t rows = (size_t)s->B * s->T * s->H;
-  return 2 * seg_bytes(*s, p) + rows * (size_t)s->dv * sizeof(float);
+  return 2 * seg_bytes(*s, p) + rows * (size_t)s->dv * sizeof(float) + kStatusBytes;
 }
 
 hla_status hla_prefill(const hla_shape *s, const void *q, const void *k, const void *v,
@@ -290,20 +290,26 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
   P.seg = (float *)ws;
   P.seg2 = (float *)((char *)ws + sbytes);
   P.dO = (float *)((char *)ws + 2 * sbytes);
+  // the tensor-core path keeps do in bf16: the second half of its region holds
+  // the per-token diagonal v_t . do_t
+  P.ddiag = (float *)((char *)P.dO + (size_t)s->B * s->T * s->H * s->dv * 2);
+  P.err = (unsigned int *)((char *)ws + need_ws - kStatusBytes);
   cudaStream_t st = (cudaStream_t)stream;
+  const bool tc = tc_supported(P, s->dtype);
   Tracer tr{trace, st};
+  HLA_LAUNCH(cudaMemsetAsync(P.err, 0, sizeof(unsigned int), st));
   HLA_LAUNCH(tr.mark());
-  HLA_LAUNCH(launch_simt_seg_state(P, s->dtype, st));
+  HLA_LAUNCH(tc ? launch_tc_seg_state(P, st) : launch_simt_seg_state(P, s->dtype, st));
   HLA_LAUNCH(tr.mark());
   HLA_LAUNCH(launch_state_scan(P, false, st));
   HLA_LAUNCH(tr.mark());
-  HLA_LAUNCH(launch_simt_bwd_dq(P, s->dtype, st));
+  HLA_LAUNCH(tc ? launch_tc_bwd_dq(P, st) : launch_simt_bwd_dq(P, s->dtype, st));
   HLA_LAUNCH(tr.mark());
-  HLA_LAUNCH(launch_simt_seg_gstate(P, s->dtype, st));
+  HLA_LAUNCH(tc ? launch_tc_seg_gstate(P, st) : launch_simt_seg_gstate(P, s->dtype, st));
   HLA_LAUNCH(tr.mark());
   HLA_LAUNCH(launch_grad_scan(P, dstate_in != nullptr, st));
   HLA_LAUNCH(tr.mark());
-  HLA_LAUNCH(launch_simt_bwd_dkdv(P, s->dtype, st));
+  HLA_LAUNCH(tc ? launch_tc_bwd_dkdv(P, st) : launch_simt_bwd_dkdv(P, s->dtype, st));
   HLA_LAUNCH(tr.mark());
   return HLA_OK;
 }

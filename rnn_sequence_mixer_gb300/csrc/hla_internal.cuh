@@ -32,7 +32,8 @@ struct MixerParams {
   float *o;
   float *seg;              // [B, H, nseg, D, D] per-segment states
   float *seg2;             // backward: [B, H, nseg, D, D] per-segment state gradients
-  float *dO;               // backward: [B, T, H, D] fp32 gradient of o
+  float *dO;               // backward: [B, T, H, D] gradient of o (fp32; bf16 on the tensor-core path)
+  float *ddiag;            // backward, tensor-core path: [B, T, H] fp32 v_t . do_t
   const long long *pos;    // decode: [B] positions or nullptr
   const void *dy;
   const float *dstate_out;
@@ -115,6 +116,9 @@ cudaError_t launch_simt_bwd_dkdv(const MixerParams &P, int dtype, cudaStream_t s
 bool tc_supported(const MixerParams &P, int dtype);
 cudaError_t launch_tc_seg_state(const MixerParams &P, cudaStream_t st);
 cudaError_t launch_tc_seg_output(const MixerParams &P, cudaStream_t st);
+cudaError_t launch_tc_seg_gstate(const MixerParams &P, cudaStream_t st);
+cudaError_t launch_tc_bwd_dq(const MixerParams &P, cudaStream_t st);
+cudaError_t launch_tc_bwd_dkdv(const MixerParams &P, cudaStream_t st);
 
 // Bytes reserved at the end of a workspace for the device status word.
 constexpr size_t kStatusBytes = 256;

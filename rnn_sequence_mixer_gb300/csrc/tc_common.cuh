@@ -1,0 +1,271 @@
+// tc_common.cuh — pieces shared by the tensor-core (tcgen05) kernels of the
+// prefill and of its backward: operand-tile geometry, 16-bit packing, the
+// q/k feature map (RMSNorm, RoPE) applied in place on swizzled tiles,
+// barriers with bounded waits, and the TMA descriptors of [B, T, H, 128]
+// bf16 tensors.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "hla_internal.cuh"
+#include "umma.cuh"
+
+namespace hla {
+namespace tc {
+
+namespace {
+
+constexpr int D = 128;
+constexpr int ROWS = 128;           // rows of every operand tile
+constexpr int NT = 512;             // threads per CTA
+constexpr int TILE = ROWS * D * 2;  // bytes of one 16-bit tile (32 KiB)
+constexpr int HALF_TILE = TILE / 2; // one 64-column block
+
+// ------------------------------------------------------------------ small helpers
+
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+__device__ __forceinline__ void unpack8h(const uint4 &u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint4 pack8(const float *f) {
+  return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
+}
+__device__ __forceinline__ uint32_t pack2h(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ uint4 pack8h(const float *f) {
+  return make_uint4(pack2h(f[0], f[1]), pack2h(f[2], f[3]), pack2h(f[4], f[5]),
+                    pack2h(f[6], f[7]));
+}
+
+__device__ __forceinline__ uint4 *tile_at(unsigned char *tile, int row, int chunk) {
+  return reinterpret_cast<uint4 *>(tile + umma::sw128_off(row, chunk, ROWS));
+}
+
+__device__ __forceinline__ uint4 ldg16(const void *p) {
+  return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+// Row t of a [B, T, H, D] bf16 tensor for (b, h).
+__device__ __forceinline__ const __nv_bfloat16 *row_ptr(const void *X, const MixerParams &P, int b,
+                                                        int h, long long t) {
+  return (const __nv_bfloat16 *)X + (((size_t)b * P.T + t) * P.H + h) * D;
+}
+
+// Elements [32 qd, 32 qd + 32) of a row.
+__device__ __forceinline__ void load_quarter(uint4 (&r)[4], const __nv_bfloat16 *row, int qd,
+                                             bool valid) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) r[u] = valid ? ldg16(row + 32 * qd + 8 * u) : make_uint4(0, 0, 0, 0);
+}
+
+// This thread's 16 RoPE pairs of a row sit in chunks {2qd, 2qd+1} (elements
+// 16qd..16qd+15) and {8+2qd, 9+2qd} (elements 64+16qd..): read them from an
+// operand tile.
+__device__ __forceinline__ void ld_pairs(unsigned char *tile, int row, int qd, uint4 (&r)[4]) {
+  r[0] = *tile_at(tile, row, 2 * qd);
+  r[1] = *tile_at(tile, row, 2 * qd + 1);
+  r[2] = *tile_at(tile, row, 8 + 2 * qd);
+  r[3] = *tile_at(tile, row, 9 + 2 * qd);
+}
+
+__device__ __forceinline__ float sumsq_pairs(const uint4 (&r)[4]) {
+  float s = 0.f;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    float f[8];
+    unpack8(r[u], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s = fmaf(f[e], f[e], s);
+  }
+  return s;
+}
+
+// cos / sin of the RoPE angle of pair u at position p on the special-function
+// unit: the exact fixed-point phase reduced to [-pi, pi), then __sincosf
+// (absolute error ~1e-6, far below the 16-bit rounding of the operands).
+__device__ __forceinline__ void rope_fast(long long p, unsigned long long u, float &c, float &s) {
+  const unsigned long long ph = (unsigned long long)p * u;
+  const float x = (float)(int)(ph >> 32) * 1.4629180792671596e-09f;  // 2 pi / 2^32
+  __sincosf(x, &s, &c);
+}
+
+// sigmoid via the hardware tanh: 1 / (1 + e^-z) = 0.5 + 0.5 tanh(z / 2).
+__device__ __forceinline__ float sigmoid_fast(float z) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * z));
+  return fmaf(0.5f, t, 0.5f);
+}
+
+// Rotate this thread's 16 pairs of raw row `r` (times `scale`) at position p
+// and store them, as fp16 (half) or bf16, into the same chunks of `tile`.
+__device__ __forceinline__ void feature_store(const uint4 (&r)[4], float scale, long long p, int qd,
+                                              const MixerParams &P, unsigned char *tile, int row,
+                                              bool half) {
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    float a[8], bb[8], lo[8], hi[8];
+    unpack8(r[hf], a);
+    unpack8(r[2 + hf], bb);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float c, s;
+      rope_fast(p, P.rope_u[16 * qd + 8 * hf + e], c, s);
+      const float x0 = a[e] * scale, x1 = bb[e] * scale;
+      lo[e] = x0 * c - x1 * s;
+      hi[e] = x0 * s + x1 * c;
+    }
+    *tile_at(tile, row, 2 * qd + hf) = half ? pack8h(lo) : pack8(lo);
+    *tile_at(tile, row, 8 + 2 * qd + hf) = half ? pack8h(hi) : pack8(hi);
+  }
+}
+
+// q~ and k~ of one row at once (shared angles), both fp16, in place.  Returns
+// this thread's part of the fp32 dot product q~ . k~ (before the rounding to
+// fp16), for callers that need the diagonal of Q~ K~^T exactly.
+__device__ __forceinline__ float feature_qk_store(const uint4 (&qr)[4], const uint4 (&kr)[4],
+                                                 float rq, float rk, long long p, int qd,
+                                                 const MixerParams &P, unsigned char *Qt,
+                                                 unsigned char *Kt, int row) {
+  float dot = 0.f;
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    float c[8], s[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) rope_fast(p, P.rope_u[16 * qd + 8 * hf + e], c[e], s[e]);
+    float qlo[8], qhi[8];
+    {
+      float a[8], bb[8];
+      unpack8(qr[hf], a);
+      unpack8(qr[2 + hf], bb);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float x0 = a[e] * rq, x1 = bb[e] * rq;
+        qlo[e] = x0 * c[e] - x1 * s[e];
+        qhi[e] = x0 * s[e] + x1 * c[e];
+      }
+      *tile_at(Qt, row, 2 * qd + hf) = pack8h(qlo);
+      *tile_at(Qt, row, 8 + 2 * qd + hf) = pack8h(qhi);
+    }
+    {
+      float a[8], bb[8], lo[8], hi[8];
+      unpack8(kr[hf], a);
+      unpack8(kr[2 + hf], bb);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float x0 = a[e] * rk, x1 = bb[e] * rk;
+        lo[e] = x0 * c[e] - x1 * s[e];
+        hi[e] = x0 * s[e] + x1 * c[e];
+        dot = fmaf(qlo[e], lo[e], fmaf(qhi[e], hi[e], dot));
+      }
+      *tile_at(Kt, row, 2 * qd + hf) = pack8h(lo);
+      *tile_at(Kt, row, 8 + 2 * qd + hf) = pack8h(hi);
+    }
+  }
+  return dot;
+}
+
+__device__ __forceinline__ void sync_tc() {
+  umma::fence_before();
+  __syncthreads();
+  umma::fence_after();
+}
+
+// Bounded wait on an mbarrier phase, with a CTA-wide vote so that every
+// thread leaves together when any of them gives up.
+__device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
+  const bool late = !umma::mbar_wait(bar, parity);
+  umma::fence_after();
+  return __syncthreads_or(late) != 0;
+}
+
+// TMA of one raw [rows, 128] bf16 tile (rows = chunk) of token rows
+// [c0, c0 + rows) for (b, h): two boxes of 64 columns.
+__device__ __forceinline__ void tma_tile(unsigned char *dst, const CUtensorMap *map, int b, int h,
+                                         int c0, uint64_t *bar) {
+  umma::tma_load_4d(dst, map, 0, h, c0, b, bar);
+  umma::tma_load_4d(dst + HALF_TILE, map, 64, h, c0, b, bar);
+}
+
+// Named barrier among `nthreads` threads (ids 1..15; id 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Bounded wait that becomes a no-op once this thread has seen a timeout, so a
+// failure never strands other warps at a barrier: the loop runs to its end
+// with invalid data and the status word reports it.
+__device__ __forceinline__ void wait_or_fail(uint64_t *bar, uint32_t parity, bool &failed) {
+  if (!failed && !umma::mbar_wait(bar, parity)) failed = true;
+  umma::fence_after();
+}
+
+// One elected arrive per warp on a worker-count barrier, after the warp's
+// shared-memory writes (generic proxy) and TMEM stores are complete.
+__device__ __forceinline__ void warp_arrive(uint64_t *bar, int lane) {
+  umma::fence_async_smem();
+  umma::fence_before();
+  __syncwarp();
+  if (lane == 0) umma::mbar_arrive(bar);
+}
+
+// ------------------------------------------------------------------ host side
+
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                              const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                              const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeFn>(p);
+  }();
+  return fn;
+}
+
+// 4-D map over a [B, T, H, 128] bf16 tensor with a box of 64 columns x 1 head
+// x `rows` tokens x 1 sequence, 128-byte swizzled (the operand tile layout).
+cudaError_t make_map(CUtensorMap *map, const void *ptr, const MixerParams &P, int rows) {
+  EncodeFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)P.H, (cuuint64_t)P.T, (cuuint64_t)P.B};
+  const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)P.H * D * 2,
+                                 (cuuint64_t)P.T * P.H * D * 2};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+}  // namespace tc
+}  // namespace hla

@@ -22,6 +22,9 @@ def dev():
     (1, 260, 2, 128, torch.float32, 128, False, 0),
     (2, 200, 4, 128, torch.bfloat16, 64, True, 1000),
     (1, 1500, 16, 128, torch.bfloat16, 64, False, 0),
+    (1, 1000, 4, 128, torch.bfloat16, 128, True, 77),
+    (3, 333, 5, 128, torch.bfloat16, 128, True, 5),
+    (1, 64, 2, 128, torch.bfloat16, 64, True, 0),
 ])
 def test_backward_small(dev, B, T, H, d, dtype, chunk, with_state, pos):
     g = oracle.gamma(H).astype(np.float32)
@@ -59,3 +62,35 @@ def test_fwd_bwd_workload_sampled(dev):
     for name, got, want in zip(["dq", "dk", "dv", "dgate"], out[:4], ref[:4]):
         err = max_rel_err(sel(got), want)
         assert err <= 2e-2, f"{name}: {err:.3e}"
+
+
+def test_backward_gamma_one_head(dev):
+    """gamma = 1 (no decay: plain linear attention) next to the fastest head of H = 32."""
+    g = oracle.gamma(32)[:2].astype(np.float32).copy()
+    g[1] = 1.0
+    B, T, H, d = 1, 700, 2, 128
+    inp = inputs.mixer_inputs(B, T, H, d, torch.bfloat16, 61, device=dev, with_dy=True)
+    out = api.prefill_backward(inp["q"], inp["k"], inp["v"], inp["gate"], torch.from_numpy(g),
+                               inp["dy"], chunk=128, rope_base=1e6, want_dstate_in=True)
+    torch.cuda.synchronize()
+    ref = oracle.backward(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(inp["gate"]),
+                          g.astype(np.float64), f64(inp["dy"]), base=1e6)
+    for name, got, want in zip(["dq", "dk", "dv", "dgate"], out[:4], ref[:4]):
+        err = max_rel_err(f64(got), want)
+        assert err <= 2e-2, f"{name}: {err:.3e}"
+    assert max_rel_err(f64(out[4]), ref[4], head_axes=(0, 1)) <= 2e-2
+
+
+def test_backward_status_word_is_clear(dev):
+    """The backward workspace ends with the same device status word as the
+    forward's: cleared by the call, 0 when no bounded wait gave up."""
+    B, T, H, d = 1, 2000, 4, 128
+    inp = inputs.mixer_inputs(B, T, H, d, torch.bfloat16, 62, device=dev, with_dy=True)
+    shape = api.make_shape(B, T, H, d, chunk=128, dtype=torch.bfloat16)
+    n = api.backward_workspace_size(shape)
+    ws = torch.full((n,), 0xAB, dtype=torch.uint8, device=dev)
+    api.prefill_backward(inp["q"], inp["k"], inp["v"], inp["gate"],
+                         torch.from_numpy(oracle.gamma(H).astype(np.float32)), inp["dy"],
+                         chunk=128, workspace=ws)
+    torch.cuda.synchronize()
+    assert ws[n - 256:n - 252].view(torch.int32).item() == 0
