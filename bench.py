@@ -392,19 +392,26 @@ def run_ours(args):
 
         def fb_step(i, trace):
             api.prefill(ib["q"], ib["k"], ib["v"], ib["gate"], gb, chunk=wb.chunk,
-                        rope_base=wb.rope_base, eps=wb.eps, y=yb, want_state=False, workspace=wsf)
+                        rope_base=wb.rope_base, eps=wb.eps, y=yb, want_state=False, workspace=wsf,
+                        trace=trace[:4] if trace else None)
             api.prefill_backward(ib["q"], ib["k"], ib["v"], ib["gate"], gb, ib["dy"],
-                                 chunk=wb.chunk, rope_base=wb.rope_base, eps=wb.eps, workspace=wsb)
+                                 chunk=wb.chunk, rope_base=wb.rope_base, eps=wb.eps, workspace=wsb,
+                                 trace=trace[4:] if trace else None)
 
         b_steps = max(1, min(args.steps, 5))
-        b_ms, _ = timed(fb_step, b_steps, 1, stream, D)
+        b_ms, b_passes = timed(fb_step, b_steps, 1, stream, D, trace_count=11)
         launches += 9 * b_steps
         b_ms = D.max(b_ms)
+        b_names = ["fwd.seg_state", "fwd.state_scan", "fwd.seg_output", None, "bwd.seg_state",
+                   "bwd.state_scan", "bwd.dq", "bwd.seg_gstate", "bwd.grad_scan", "bwd.dkdv"]
+        b_pass_ms = {nm: statistics.median(p[j] for p in b_passes)
+                     for j, nm in enumerate(b_names) if nm}
         thb = wb.B * wb.T * wb.H
         alg_b = thb * (5 * wb.d * BF16 + 9 * wb.d * BF16)  # fwd 5 d-rows + bwd 5 in / 4 out
-        out["fwd_bwd"] = {"workload": wb.name, "ms_per_step": b_ms,
+        out["fwd_bwd"] = {"workload": wb.name, "chunk": wb.chunk, "ms_per_step": b_ms,
                           "Mtok_s": D.world * wb.B * wb.T / (b_ms / 1e3) / 1e6,
-                          "alg_bytes": alg_b, "frac_hbm": alg_b / (b_ms / 1e3) / 1e9 / hbm_peak}
+                          "alg_bytes": alg_b, "frac_hbm": alg_b / (b_ms / 1e3) / 1e9 / hbm_peak,
+                          "pass_ms": b_pass_ms}
         del ib, wsb, wsf, yb
         torch.cuda.empty_cache()
 

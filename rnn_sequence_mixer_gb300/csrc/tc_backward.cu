@@ -132,27 +132,32 @@ __device__ __forceinline__ void tmem_ld_pairs(uint32_t taddr, int qd, float (&lo
   umma::tmem_ld16(taddr + 64 + 16 * qd, hi);
 }
 
+// This thread's 16 RoPE pairs of a raw input row (elements 16 qd .. 16 qd + 15
+// and 64 + 16 qd ..), zeros when !valid.
+__device__ __forceinline__ void load_pairs(uint4 (&ra)[4], const __nv_bfloat16 *raw, int qd,
+                                           bool valid) {
+  if (valid) {
+    ra[0] = ldg16(raw + 16 * qd);
+    ra[1] = ldg16(raw + 16 * qd + 8);
+    ra[2] = ldg16(raw + 64 + 16 * qd);
+    ra[3] = ldg16(raw + 64 + 16 * qd + 8);
+  } else {
+    ra[0] = ra[1] = ra[2] = ra[3] = make_uint4(0, 0, 0, 0);
+  }
+}
+
 // Gradient of one feature row through RoPE and RMSNorm: g holds dL/d(rotated
 // normalized row) for this thread's 16 pairs (lo = element m, hi = m + 64,
-// m = 16 qd + e); raw = the input row; r = 1 / RMS(raw).  Writes dL/draw for
-// the pairs to `out` (bf16) when `valid`.  The mean over the row needs the
-// other three threads of the row: red is the [4][ROWS] scratch and the call
-// holds one CTA barrier.
+// m = 16 qd + e); ra = those pairs of the raw input row (load_pairs);
+// r = 1 / RMS(raw).  Writes dL/draw for the pairs to `out` (bf16) when
+// `valid`.  The mean over the row needs the other three threads of the row:
+// red is the [4][ROWS] scratch and the call holds one CTA barrier.
 __device__ __forceinline__ void feature_grad_row(const float (&glo)[16], const float (&ghi)[16],
-                                                 const __nv_bfloat16 *raw, float r, long long p,
+                                                 const uint4 (&ra)[4], float r, long long p,
                                                  int i, int qd, bool valid, const MixerParams &P,
                                                  float (*red)[ROWS], __nv_bfloat16 *out) {
   float n0[16], n1[16], g0[16], g1[16];
   {
-    uint4 ra[4];
-    if (valid) {
-      ra[0] = ldg16(raw + 16 * qd);
-      ra[1] = ldg16(raw + 16 * qd + 8);
-      ra[2] = ldg16(raw + 64 + 16 * qd);
-      ra[3] = ldg16(raw + 64 + 16 * qd + 8);
-    } else {
-      ra[0] = ra[1] = ra[2] = ra[3] = make_uint4(0, 0, 0, 0);
-    }
     float f[8];
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
@@ -321,14 +326,9 @@ __global__ void __launch_bounds__(NT, 1)
         *tile_at(SB, i, 4 * qd + u) = pack8h(t);
       }
       const float carry = sh.pw[c];
-      float lo[16], hi[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        lo[e] = sv[e] * carry;
-        hi[e] = sv[16 + e] * carry;
-      }
-      umma::tmem_st16(tS + col, lo);
-      umma::tmem_st16(tS + col + 16, hi);
+      for (int e = 0; e < 32; ++e) sv[e] *= carry;
+      umma::tmem_st32(tS + col, sv);
       umma::tmem_wait_st();
     }
     umma::fence_async_smem();
@@ -357,19 +357,20 @@ __global__ void __launch_bounds__(NT, 1)
       store_quarter(PM, i, qd, pv);
       rescale_quarter(Kt, i, qd, 1.f, true);
     }
+    uint4 gr[4], dyr[4];  // gate and dy of row i for [3], loaded a phase early
+    {
+      const long long trow = valid ? c0 + i : c0;
+      load_quarter(gr, row_ptr(P.g, P, b, h, trow), qd, valid);
+      load_quarter(dyr, row_ptr(P.dy, P, b, h, trow), qd, valid);
+    }
     BWD_WAIT(&sh.bar_mma[1], ph);
     {
       float ov[32];
       umma::tmem_ld2x16(tO + col, ov);
       const float f = sh.pw[i + 1] * s_inv;
-      float lo[16], hi[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        lo[e] = ov[e] * f;
-        hi[e] = ov[16 + e] * f;
-      }
-      umma::tmem_st16(tO + col, lo);
-      umma::tmem_st16(tO + col + 16, hi);
+      for (int e = 0; e < 32; ++e) ov[e] *= f;
+      umma::tmem_st32(tO + col, ov);
       rescale_quarter(SB, i, qd, s_inv, true);
       umma::tmem_wait_st();
     }
@@ -392,17 +393,13 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
       for (int e = 0; e < 32; ++e) ss = fmaf(ov[e], ov[e], ss);
       sh.red[qd][i] = ss;
-      uint4 gr[4], dyr[4];
-      const long long trow = valid ? c0 + i : c0;
-      load_quarter(gr, row_ptr(P.g, P, b, h, trow), qd, valid);
-      load_quarter(dyr, row_ptr(P.dy, P, b, h, trow), qd, valid);
       __syncthreads();
       const float ro = rsqrtf((sh.red[0][i] + sh.red[1][i] + sh.red[2][i] + sh.red[3][i]) / (float)D + P.eps);
       float mpart = 0.f;
-      float dgv[32];
+      uint4 *d4 = reinterpret_cast<uint4 *>(row_out(P.dg, P, b, h, valid ? c0 + i : c0) + col);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        float gf[8], df[8];
+        float gf[8], df[8], dg8[8];
         unpack8(gr[u], gf);
         unpack8(dyr[u], df);
 #pragma unroll
@@ -410,15 +407,11 @@ __global__ void __launch_bounds__(NT, 1)
           const float nv = ov[8 * u + e] * ro;
           const float z = sigmoid_fast(gf[e]);
           const float dn = df[e] * z;
-          dgv[8 * u + e] = dn * nv * (1.f - z);
+          dg8[e] = dn * nv * (1.f - z);
           mpart = fmaf(dn, nv, mpart);
           ov[8 * u + e] = dn;  // keep dn; n is recomputed below
         }
-      }
-      if (valid) {
-        uint4 *d4 = reinterpret_cast<uint4 *>(row_out(P.dg, P, b, h, c0 + i) + col);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) d4[u] = pack8(&dgv[8 * u]);
+        if (valid) d4[u] = pack8(dg8);
       }
       sh.red2[qd][i] = mpart;
       __syncthreads();
@@ -461,6 +454,7 @@ __global__ void __launch_bounds__(NT, 1)
 
     // [4] dPm = bf16(dP (.) D) into PM (Pm is dead once MMA3 is done)
     BWD_WAIT(&sh.bar_mma[3], ph);
+
     if (tid == 0 && n + 1 < ntile) {  // the Q tile (dO) is free: next q
       umma::mbar_expect_tx(bar_q, tile_bytes);
       tma_tile(Qt, &tmq, b, h, c0 + CV, bar_q);
@@ -476,6 +470,8 @@ __global__ void __launch_bounds__(NT, 1)
       mask_lower(pv, i, (int)col, valid, gm, sh.pw);
       store_quarter(PM, i, qd, pv);
     }
+    uint4 qraw[4];  // raw q pairs of row i for the dq epilogue (in flight during MMA7)
+    load_pairs(qraw, row_ptr(P.q, P, b, h, valid ? c0 + i : c0), qd, valid);
     umma::fence_async_smem();
     sync_tc();
     if (tid == 0) {
@@ -497,16 +493,21 @@ __global__ void __launch_bounds__(NT, 1)
       umma::commit(&sh.bar_mma[5]);
     }
     {
-      float alo[16], ahi[16], blo[16], bhi[16];
-      tmem_ld_pairs(tO, qd, alo, ahi);
-      tmem_ld_pairs(tI, qd, blo, bhi);
+      // dQ~ = intra + gamma^{i+1} inter, for this thread's 16 RoPE pairs
+      float alo[16], ahi[16];
       const float wi = sh.pw[i + 1];
+      {
+        float t[16];
+        umma::tmem_ld16(tO + 16 * qd, alo);
+        umma::tmem_ld16(tI + 16 * qd, t);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        alo[e] = fmaf(wi, blo[e], alo[e]);
-        ahi[e] = fmaf(wi, bhi[e], ahi[e]);
+        for (int e = 0; e < 16; ++e) alo[e] = fmaf(wi, t[e], alo[e]);
+        umma::tmem_ld16(tO + 64 + 16 * qd, ahi);
+        umma::tmem_ld16(tI + 64 + 16 * qd, t);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) ahi[e] = fmaf(wi, t[e], ahi[e]);
       }
-      feature_grad_row(alo, ahi, row_ptr(P.q, P, b, h, valid ? c0 + i : c0), rq, pos, i, qd, valid, P,
+      feature_grad_row(alo, ahi, qraw, rq, pos, i, qd, valid, P,
                        sh.red, row_out(P.dq, P, b, h, valid ? c0 + i : c0));
     }
     BWD_WAIT(&sh.bar_mma[5], ph);
@@ -622,14 +623,9 @@ __global__ void __launch_bounds__(NT, 1)
       umma::tmem_ld2x16(tE + col, ev);
       store_quarter(EB, i, qd, ev);
       const float carry = sh.pw[c];
-      float lo[16], hi[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        lo[e] = ev[e] * carry;
-        hi[e] = ev[16 + e] * carry;
-      }
-      umma::tmem_st16(tE + col, lo);
-      umma::tmem_st16(tE + col + 16, hi);
+      for (int e = 0; e < 32; ++e) ev[e] *= carry;
+      umma::tmem_st32(tE + col, ev);
       __syncthreads();
       const float rq = rsqrtf((sh.red[0][i] + sh.red[1][i] + sh.red[2][i] + sh.red[3][i]) / (float)D + P.eps);
       rk = rsqrtf((sh.red2[0][i] + sh.red2[1][i] + sh.red2[2][i] + sh.red2[3][i]) / (float)D + P.eps);
@@ -675,6 +671,8 @@ __global__ void __launch_bounds__(NT, 1)
 
     // [3] M2 (.) D^T (held in registers until X is free); v -> vdec; q~ -> bf16
     BWD_WAIT(&sh.bar_mma[1], ph);
+    uint4 kraw[4];  // raw k pairs of row i for the dk epilogue
+    load_pairs(kraw, row_ptr(P.k, P, b, h, valid ? c0 + i : c0), qd, valid);
     {
       float v[32];
       umma::tmem_ld2x16(tB + col, v);
@@ -734,7 +732,7 @@ __global__ void __launch_bounds__(NT, 1)
         glo[e] *= P.kscale;
         ghi[e] *= P.kscale;
       }
-      feature_grad_row(glo, ghi, row_ptr(P.k, P, b, h, valid ? c0 + i : c0), rk, pos, i, qd, valid, P,
+      feature_grad_row(glo, ghi, kraw, rk, pos, i, qd, valid, P,
                        sh.red, row_out(P.dk, P, b, h, valid ? c0 + i : c0));
     }
     BWD_WAIT(&sh.bar_mma[4], ph);

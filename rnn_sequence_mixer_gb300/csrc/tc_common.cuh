@@ -208,6 +208,15 @@ __device__ __forceinline__ void tma_tile(unsigned char *dst, const CUtensorMap *
   umma::tma_load_4d(dst + HALF_TILE, map, 64, h, c0, b, bar);
 }
 
+// TMA store of a [rows, 128] bf16 operand-layout tile to token rows
+// [c0, c0 + rows) of (b, h): two boxes of 64 columns.  Rows past T are not
+// written.
+__device__ __forceinline__ void tma_store_tile(const CUtensorMap *map, const unsigned char *src,
+                                               int b, int h, int c0) {
+  umma::tma_store_4d(map, src, 0, h, c0, b);
+  umma::tma_store_4d(map, src + HALF_TILE, 64, h, c0, b);
+}
+
 // Named barrier among `nthreads` threads (ids 1..15; id 0 is __syncthreads).
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -173,11 +173,14 @@ struct OutShared {
   float smax[NWORK];
   uint64_t bar_mma[2];  // [0]: MMA1 + MMA2 of a tile done, [1]: MMA3 + MMA4 done (commits)
   uint64_t bar_p;       // MMA1 (P) of a tile done
-  uint64_t bar_qk[2];   // TMA of raw q, k into buffer pair 0 / 1
+  uint64_t bar_q;       // TMA of raw q
+  uint64_t bar_k[2];    // TMA of raw k into buffer 0 / 1
   uint64_t bar_v;       // TMA of raw v
+  uint64_t bar_g;       // TMA of the gate tile
   uint64_t bar_feat;    // workers: q~, k~ of the tile written (one arrive per warp)
   uint64_t bar_sb;      // workers: Sb written and S rescaled
   uint64_t bar_pm;      // workers: Pm, scaled O and k~dec written
+  uint64_t bar_epi;     // workers: y of the previous tile written over its gate tile
   uint32_t tmem_base;
   uint32_t failed;
 };
@@ -186,7 +189,9 @@ struct OutShared {
 // Output pass over the tiles of one segment, warp-specialized.
 //   Issuer warp (warp 16): per tile n, waits for the workers' barriers and
 //   issues MMA1 (P = Q~ K~^T), MMA2 (O = Q~ Sb), MMA3 (O += Pm V) and MMA4
-//   (S += K~dec^T V), then the TMA copies that refill the freed buffers.
+//   (S += K~dec^T V), the TMA store of y of tile n - 1 (written over its gate
+//   tile by the workers) and the TMA copies that refill the freed buffers.
+//   Every global access of the tile loop is a TMA bulk copy.
 //   Worker warps (0..15), per tile n:
 //     [A]/[D] raw q, k -> row norms (warp shuffles) -> q~, k~ fp16 in place
 //     [B]/[C] after MMA3/MMA4 of tile n - 1: Sb = fp16(S 2^-e) with one power
@@ -197,11 +202,14 @@ struct OutShared {
 // (max |S| per column quarter, the RMS of o per row) use 4-warp named barriers.
 __global__ void __launch_bounds__(NTO, 1)
     tc_output_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmq,
-                     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+                     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                     const __grid_constant__ CUtensorMap tmg, const __grid_constant__ CUtensorMap tmy) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  // buffer pair j: Q at base + 2 j TILE, K at base + (2 j + 1) TILE
-  unsigned char *Vs = base + 4 * TILE, *SP = base + 5 * TILE;
+  // Q: raw q -> q~ (free once MMA2 has read it: the next q lands there).
+  // K buffer j at base + (1 + j) TILE: raw k -> k~ -> k~dec (double-buffered).
+  // G: gate of the tile being drained -> its y, stored from there by TMA.
+  unsigned char *Qs = base, *Vs = base + 3 * TILE, *SP = base + 4 * TILE, *Gs = base + 5 * TILE;
   OutShared &sh = *reinterpret_cast<OutShared *>(base + 6 * TILE);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -216,13 +224,16 @@ __global__ void __launch_bounds__(NTO, 1)
   if (tid == 0) {
     for (int j = 0; j < 2; ++j) {
       umma::mbar_init(&sh.bar_mma[j], 1);
-      umma::mbar_init(&sh.bar_qk[j], 1);
+      umma::mbar_init(&sh.bar_k[j], 1);
     }
+    umma::mbar_init(&sh.bar_q, 1);
     umma::mbar_init(&sh.bar_v, 1);
+    umma::mbar_init(&sh.bar_g, 1);
     umma::mbar_init(&sh.bar_p, 1);
     umma::mbar_init(&sh.bar_feat, NWORK);
     umma::mbar_init(&sh.bar_sb, NWORK);
     umma::mbar_init(&sh.bar_pm, NWORK);
+    umma::mbar_init(&sh.bar_epi, NWORK);
     umma::mbar_fence_init();
     sh.failed = 0;
   }
@@ -243,17 +254,21 @@ __global__ void __launch_bounds__(NTO, 1)
       const uint32_t id_qs = umma::idesc_bf16(128, 128, false, true, true);   // fp16 Q~ S
       const uint32_t id_pv = umma::idesc_bf16(128, 128, false, true);         // bf16 Pm V
       const uint32_t id_mn = umma::idesc_bf16(128, 128, true, true);          // bf16 K~dec^T V
+      umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
+      tma_tile(Qs, &tmq, b, h, t0, &sh.bar_q);
       for (int n = 0; n < 2 && n < ntile; ++n) {
-        umma::mbar_expect_tx(&sh.bar_qk[n], 2 * tile_bytes);
-        tma_tile(base + 2 * n * TILE, &tmq, b, h, t0 + n * CV, &sh.bar_qk[n]);
-        tma_tile(base + (2 * n + 1) * TILE, &tmk, b, h, t0 + n * CV, &sh.bar_qk[n]);
+        umma::mbar_expect_tx(&sh.bar_k[n], tile_bytes);
+        tma_tile(base + (1 + n) * TILE, &tmk, b, h, t0 + n * CV, &sh.bar_k[n]);
       }
       umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
       tma_tile(Vs, &tmv, b, h, t0, &sh.bar_v);
+      umma::mbar_expect_tx(&sh.bar_g, tile_bytes);
+      tma_tile(Gs, &tmg, b, h, t0, &sh.bar_g);
+      const uint32_t aq = umma::smem_u32(Qs);
       for (int n = 0; n < ntile; ++n) {
         const int buf = n & 1;
-        const uint32_t aq = umma::smem_u32(base + 2 * buf * TILE);
-        const uint32_t ak = aq + TILE;
+        const int c0 = t0 + n * CV;
+        const uint32_t ak = umma::smem_u32(base + (1 + buf) * TILE);
         const uint32_t as = umma::smem_u32(SP), av = umma::smem_u32(Vs);
         const uint32_t ocur = tm + 128 + 128 * buf;
         wait_or_fail(&sh.bar_feat, n & 1, failed);
@@ -272,6 +287,23 @@ __global__ void __launch_bounds__(NTO, 1)
                          id_qs, kk > 0);
           umma::commit(&sh.bar_mma[0]);
         }
+        // y of tile n - 1 is in G: store it, then bring in the gate of tile n
+        if (n >= 1) {
+          wait_or_fail(&sh.bar_epi, (n - 1) & 1, failed);
+          if (!failed) {
+            tma_store_tile(&tmy, Gs, b, h, c0 - CV);
+            umma::bulk_commit();
+            umma::bulk_wait_read();
+            umma::mbar_expect_tx(&sh.bar_g, tile_bytes);
+            tma_tile(Gs, &tmg, b, h, c0, &sh.bar_g);
+          }
+        }
+        // MMA2 done: Q is free for the next q
+        wait_or_fail(&sh.bar_mma[0], n & 1, failed);
+        if (!failed && n + 1 < ntile) {
+          umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
+          tma_tile(Qs, &tmq, b, h, c0 + CV, &sh.bar_q);
+        }
         wait_or_fail(&sh.bar_pm, n & 1, failed);
         wait_or_fail(&sh.bar_v, n & 1, failed);
         if (!failed) {
@@ -285,21 +317,26 @@ __global__ void __launch_bounds__(NTO, 1)
                          id_mn, 1u);
           umma::commit(&sh.bar_mma[1]);
         }
-        // MMA3 / MMA4 done: V and buffer pair `buf` are free for the next copies
+        // MMA3 / MMA4 done: V and K buffer `buf` are free for the next copies
         wait_or_fail(&sh.bar_mma[1], n & 1, failed);
         if (!failed) {
-          const int c0 = t0 + n * CV;
           if (n + 1 < ntile) {
             umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
             tma_tile(Vs, &tmv, b, h, c0 + CV, &sh.bar_v);
           }
           if (n + 2 < ntile) {
-            umma::mbar_expect_tx(&sh.bar_qk[buf], 2 * tile_bytes);
-            tma_tile(base + 2 * buf * TILE, &tmq, b, h, c0 + 2 * CV, &sh.bar_qk[buf]);
-            tma_tile(base + (2 * buf + 1) * TILE, &tmk, b, h, c0 + 2 * CV, &sh.bar_qk[buf]);
+            umma::mbar_expect_tx(&sh.bar_k[buf], tile_bytes);
+            tma_tile(base + (1 + buf) * TILE, &tmk, b, h, c0 + 2 * CV, &sh.bar_k[buf]);
           }
         }
       }
+      // y of the last tile
+      wait_or_fail(&sh.bar_epi, (ntile - 1) & 1, failed);
+      if (!failed) {
+        tma_store_tile(&tmy, Gs, b, h, t0 + (ntile - 1) * CV);
+        umma::bulk_commit();
+      }
+      umma::bulk_wait_all();
     }
   } else {
     // ---------------------------------------------------------------- worker warps
@@ -321,7 +358,6 @@ __global__ void __launch_bounds__(NTO, 1)
       umma::tmem_st32(myS, v);
       umma::tmem_wait_st();
     }
-    __nv_bfloat16 *y = (__nv_bfloat16 *)P.y;
     int prev_c0 = 0, prev_c = 0;
     for (int n = 0; n <= ntile; ++n) {
       const bool have = n < ntile, drain = n >= 1;
@@ -330,10 +366,11 @@ __global__ void __launch_bounds__(NTO, 1)
       const bool valid = i < c;
       const uint32_t ocur = tm + 128 + 128 * buf;        // O buffer of tile n
       const uint32_t oprev = tm + 128 + 128 * (buf ^ 1); // O buffer of tile n - 1
-      unsigned char *Qt = base + 2 * buf * TILE, *Kt = Qt + TILE;
+      unsigned char *Qt = Qs, *Kt = base + (1 + buf) * TILE;
       if (have) {
         // [A] raw q, k of tile n: row fr, pairs [16 fu, 16 fu + 16); norms by shuffles
-        wait_or_fail(&sh.bar_qk[buf], (n >> 1) & 1, failed);
+        wait_or_fail(&sh.bar_q, n & 1, failed);
+        wait_or_fail(&sh.bar_k[buf], (n >> 1) & 1, failed);
         uint4 qr[4], kr[4];
         ld_pairs(Qt, fr, fu, qr);
         ld_pairs(Kt, fr, fu, kr);
@@ -392,9 +429,6 @@ __global__ void __launch_bounds__(NTO, 1)
       }
       // [E] epilogue of tile n - 1 (overlaps MMA1 / MMA2 of tile n)
       if (drain) {
-        uint4 gr[4];  // gate of tile n - 1 (issued late so it does not queue ahead of [A])
-        const bool okp = i < prev_c;
-        load_quarter(gr, row_ptr(P.g, P, b, h, okp ? prev_c0 + i : prev_c0), qd, okp);
         float o[32];
         umma::tmem_ld2x16(oprev + lane_base + col, o);
         float ss = 0.f;
@@ -402,19 +436,24 @@ __global__ void __launch_bounds__(NTO, 1)
         for (int e = 0; e < 32; ++e) ss = fmaf(o[e], o[e], ss);
         sh.red_o[qd][i] = ss;
         named_sync(5 + sub, 128);
-        if (i < prev_c) {
+        // gate of tile n - 1 (TMA) -> y, in place; the issuer stores the tile
+        wait_or_fail(&sh.bar_g, (n - 1) & 1, failed);
+        {
           const float ro = rsqrtf((sh.red_o[0][i] + sh.red_o[1][i] + sh.red_o[2][i] +
                                    sh.red_o[3][i]) / (float)D + P.eps);
-          const size_t row = (((size_t)b * P.T + prev_c0 + i) * P.H + h) * D + col;
-          uint4 *y4 = reinterpret_cast<uint4 *>(y + row);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
+            uint4 *p = tile_at(Gs, i, 4 * qd + u);
             float gf[8], t[8];
-            unpack8(gr[u], gf);
+            unpack8(*p, gf);
 #pragma unroll
             for (int e = 0; e < 8; ++e) t[e] = o[8 * u + e] * ro * sigmoid_fast(gf[e]);
-            y4[u] = pack8(t);
+            *p = pack8(t);
           }
+        }
+        warp_arrive(&sh.bar_epi, lane);
+        if (i < prev_c) {
+          const size_t row = (((size_t)b * P.T + prev_c0 + i) * P.H + h) * D + col;
           if (P.o) {
             float4 *o4 = reinterpret_cast<float4 *>(P.o + row);
 #pragma unroll
@@ -518,15 +557,17 @@ cudaError_t launch_tc_seg_gstate(const MixerParams &P, cudaStream_t st) {
 }
 
 cudaError_t launch_tc_seg_output(const MixerParams &P, cudaStream_t st) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mg, my;
   cudaError_t e;
   if ((e = tc::make_map(&mq, P.q, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mk, P.k, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mv, P.v, P, P.chunk)) != cudaSuccess) return e;
+  if ((e = tc::make_map(&mg, P.g, P, P.chunk)) != cudaSuccess) return e;
+  if ((e = tc::make_map(&my, P.y, P, P.chunk)) != cudaSuccess) return e;
   e = cudaFuncSetAttribute(tc::tc_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)tc::kOutputSmem);
   if (e != cudaSuccess) return e;
-  tc::tc_output_kernel<<<dim3(P.nseg, P.H, P.B), tc::NTO, tc::kOutputSmem, st>>>(P, mq, mk, mv);
+  tc::tc_output_kernel<<<dim3(P.nseg, P.H, P.B), tc::NTO, tc::kOutputSmem, st>>>(P, mq, mk, mv, mg, my);
   return cudaGetLastError();
 }
 

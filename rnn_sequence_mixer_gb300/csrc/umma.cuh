@@ -252,5 +252,30 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, int x, 
       : "memory");
 }
 
+// 4-D tiled TMA store of a shared-memory box to global coordinates (x, y, z, w)
+// (never negative).  Rows of the box past the tensor's extent are not written.
+// The writing threads must have made their shared-memory writes visible to the
+// async proxy (fence_async_smem) before the issuing thread got here.
+__device__ __forceinline__ void tma_store_4d(const void *tmap, const void *src, int x, int y, int z,
+                                             int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(src))
+      : "memory");
+}
+
+// Close the group of bulk stores issued by this thread since the last commit.
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until the committed bulk stores of this thread have finished reading
+// shared memory (the source may be overwritten afterwards).
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Wait until the committed bulk stores of this thread are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 }  // namespace umma
 }  // namespace hla
