@@ -149,13 +149,14 @@ __device__ __forceinline__ void load_pairs(uint4 (&ra)[4], const __nv_bfloat16 *
 // Gradient of one feature row through RoPE and RMSNorm: g holds dL/d(rotated
 // normalized row) for this thread's 16 pairs (lo = element m, hi = m + 64,
 // m = 16 qd + e); ra = those pairs of the raw input row (load_pairs);
-// r = 1 / RMS(raw).  Writes dL/draw for the pairs to `out` (bf16) when
-// `valid`.  The mean over the row needs the other three threads of the row:
-// red is the [4][ROWS] scratch and the call holds one CTA barrier.
+// r = 1 / RMS(raw).  Writes dL/draw for the pairs (bf16, zeros when !valid)
+// into row i of the operand-layout tile `out`, for a TMA store.  The mean over
+// the row needs the other three threads of the row: red is the [4][ROWS]
+// scratch and the call holds one CTA barrier.
 __device__ __forceinline__ void feature_grad_row(const float (&glo)[16], const float (&ghi)[16],
                                                  const uint4 (&ra)[4], float r, long long p,
                                                  int i, int qd, bool valid, const MixerParams &P,
-                                                 float (*red)[ROWS], __nv_bfloat16 *out) {
+                                                 float (*red)[ROWS], unsigned char *out) {
   float n0[16], n1[16], g0[16], g1[16];
   {
     float f[8];
@@ -182,24 +183,16 @@ __device__ __forceinline__ void feature_grad_row(const float (&glo)[16], const f
   red[qd][i] = dot;
   __syncthreads();
   const float mean = (red[0][i] + red[1][i] + red[2][i] + red[3][i]) / (float)D;
-  if (valid) {
-    float a[16], bq[16];
+  float a[16], bq[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      a[e] = r * (g0[e] - n0[e] * mean);
-      bq[e] = r * (g1[e] - n1[e] * mean);
-    }
-    uint4 *o4 = reinterpret_cast<uint4 *>(out);
-    o4[2 * qd] = pack8(a);
-    o4[2 * qd + 1] = pack8(a + 8);
-    o4[8 + 2 * qd] = pack8(bq);
-    o4[8 + 2 * qd + 1] = pack8(bq + 8);
+  for (int e = 0; e < 16; ++e) {
+    a[e] = valid ? r * (g0[e] - n0[e] * mean) : 0.f;
+    bq[e] = valid ? r * (g1[e] - n1[e] * mean) : 0.f;
   }
-}
-
-__device__ __forceinline__ __nv_bfloat16 *row_out(void *X, const MixerParams &P, int b, int h,
-                                                  long long t) {
-  return (__nv_bfloat16 *)X + (((size_t)b * P.T + t) * P.H + h) * D;
+  *tile_at(out, i, 2 * qd) = pack8(a);
+  *tile_at(out, i, 2 * qd + 1) = pack8(a + 8);
+  *tile_at(out, i, 8 + 2 * qd) = pack8(bq);
+  *tile_at(out, i, 8 + 2 * qd + 1) = pack8(bq + 8);
 }
 
 // Bounded wait with a CTA-wide vote (every thread calls it); on a timeout
@@ -215,14 +208,19 @@ __device__ __forceinline__ __nv_bfloat16 *row_out(void *X, const MixerParams &P,
 
 __global__ void __launch_bounds__(NT, 1)
     tc_bwd_dq_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmq,
-                     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+                     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                     const __grid_constant__ CUtensorMap tmg, const __grid_constant__ CUtensorMap tmo,
+                     const __grid_constant__ CUtensorMap tmdg, const __grid_constant__ CUtensorMap tmdq) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  // Q: raw q -> q~ (fp16) -> dO (bf16).  K pair j: raw k -> k~ (fp16) -> k~
-  // (bf16) -> k~dec.  SB: Sb (fp16, scaled) -> S (bf16).  PM: P (.) D -> dP (.) D.
+  // Q: raw q -> q~ (fp16); then gate (TMA) -> dO (bf16, in place; TMA-stored).
+  // K pair j: raw k -> k~ (fp16) -> k~ (bf16) -> k~dec.
+  // SB: Sb (fp16, scaled) -> S (bf16); then dq (TMA-stored).
+  // PM: P (.) D; then dgate (TMA-stored); then dP (.) D.
   unsigned char *Qt = base, *Vt = base + 3 * TILE, *SB = base + 4 * TILE, *PM = base + 5 * TILE;
   BwdShared &sh = *reinterpret_cast<BwdShared *>(base + 6 * TILE);
-  uint64_t *bar_q = &sh.bar_tma[0], *bar_k = &sh.bar_tma[1], *bar_v = &sh.bar_tma[3];
+  uint64_t *bar_q = &sh.bar_tma[0], *bar_k = &sh.bar_tma[1], *bar_v = &sh.bar_tma[3],
+           *bar_g = &sh.bar_tma[4];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sub = warp & 3, qd = warp >> 2, i = 32 * sub + lane;
@@ -277,7 +275,6 @@ __global__ void __launch_bounds__(NT, 1)
   const uint32_t id_mnmn = umma::idesc_bf16(128, 128, true, true);
   const uint32_t aQ = umma::smem_u32(Qt), aV = umma::smem_u32(Vt), aSB = umma::smem_u32(SB),
                  aPM = umma::smem_u32(PM);
-  __nv_bfloat16 *dO_ws = (__nv_bfloat16 *)P.dO;
 
   bool failed = false;
   for (int n = 0; n < ntile; ++n) {
@@ -288,6 +285,7 @@ __global__ void __launch_bounds__(NT, 1)
     const int c0 = t0 + n * CV, c = min(CV, t1 - c0);
     const bool valid = i < c;
     const long long pos = P.pos_offset + c0 + i;
+    if (tid == 0) umma::bulk_wait_read();  // the previous dq store has left SB
 
     // [1] q~, k~ (fp16, in place); Sb = fp16(S 2^-e) per column quarter; S <- gamma^c S
     BWD_WAIT(bar_q, ph);
@@ -357,13 +355,13 @@ __global__ void __launch_bounds__(NT, 1)
       store_quarter(PM, i, qd, pv);
       rescale_quarter(Kt, i, qd, 1.f, true);
     }
-    uint4 gr[4], dyr[4];  // gate and dy of row i for [3], loaded a phase early
-    {
-      const long long trow = valid ? c0 + i : c0;
-      load_quarter(gr, row_ptr(P.g, P, b, h, trow), qd, valid);
-      load_quarter(dyr, row_ptr(P.dy, P, b, h, trow), qd, valid);
-    }
+    uint4 dyr[4];  // dy of row i for [3], loaded a phase early
+    load_quarter(dyr, row_ptr(P.dy, P, b, h, valid ? c0 + i : c0), qd, valid);
     BWD_WAIT(&sh.bar_mma[1], ph);
+    if (tid == 0) {  // MMA2 done: Q is free for this tile's gate
+      umma::mbar_expect_tx(bar_g, tile_bytes);
+      tma_tile(Qt, &tmg, b, h, c0, bar_g);
+    }
     {
       float ov[32];
       umma::tmem_ld2x16(tO + col, ov);
@@ -384,8 +382,10 @@ __global__ void __launch_bounds__(NT, 1)
       umma::commit(&sh.bar_mma[2]);
     }
 
-    // [3] dgate and dO from O (output norm and gate backward); dO -> Q tile and workspace
+    // [3] dgate and dO from O (output norm and gate backward): dgate -> PM,
+    // dO -> Q over the gate (each thread rewrites only the chunks it read)
     BWD_WAIT(&sh.bar_mma[2], ph);
+    BWD_WAIT(bar_g, ph);
     {
       float ov[32];
       umma::tmem_ld2x16(tO + col, ov);
@@ -396,11 +396,10 @@ __global__ void __launch_bounds__(NT, 1)
       __syncthreads();
       const float ro = rsqrtf((sh.red[0][i] + sh.red[1][i] + sh.red[2][i] + sh.red[3][i]) / (float)D + P.eps);
       float mpart = 0.f;
-      uint4 *d4 = reinterpret_cast<uint4 *>(row_out(P.dg, P, b, h, valid ? c0 + i : c0) + col);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         float gf[8], df[8], dg8[8];
-        unpack8(gr[u], gf);
+        unpack8(*tile_at(Qt, i, 4 * qd + u), gf);
         unpack8(dyr[u], df);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -411,7 +410,7 @@ __global__ void __launch_bounds__(NT, 1)
           mpart = fmaf(dn, nv, mpart);
           ov[8 * u + e] = dn;  // keep dn; n is recomputed below
         }
-        if (valid) d4[u] = pack8(dg8);
+        *tile_at(PM, i, 4 * qd + u) = pack8(dg8);
       }
       sh.red2[qd][i] = mpart;
       __syncthreads();
@@ -434,15 +433,13 @@ __global__ void __launch_bounds__(NT, 1)
         sh.vd_diag[qd][i] = vd;
       }
       store_quarter(Qt, i, qd, ov);
-      if (valid) {
-        uint4 *o4 = reinterpret_cast<uint4 *>(row_out(dO_ws, P, b, h, c0 + i) + col);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) o4[u] = *tile_at(Qt, i, 4 * qd + u);
-      }
     }
     umma::fence_async_smem();
     sync_tc();
     if (tid == 0) {
+      tma_store_tile(&tmdg, PM, b, h, c0);
+      tma_store_tile(&tmo, Qt, b, h, c0);
+      umma::bulk_commit();
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)  // MMA5: dP = dO V^T
         umma::mma_ss(tm, umma::desc_kmajor(aQ, kk, ROWS), umma::desc_kmajor(aV, kk, ROWS), id_kk, kk > 0);
@@ -450,6 +447,7 @@ __global__ void __launch_bounds__(NT, 1)
       for (int kk = 0; kk < 8; ++kk)  // MMA6: I = dO S^T
         umma::mma_ss(tm + 256, umma::desc_kmajor(aQ, kk, ROWS), umma::desc_kmajor(aSB, kk, ROWS), id_kk, kk > 0);
       umma::commit(&sh.bar_mma[3]);
+      umma::bulk_wait_read();  // dgate and dO have left PM and Q before [4] reuses them
     }
 
     // [4] dPm = bf16(dP (.) D) into PM (Pm is dead once MMA3 is done)
@@ -507,11 +505,13 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) ahi[e] = fmaf(wi, t[e], ahi[e]);
       }
-      feature_grad_row(alo, ahi, qraw, rq, pos, i, qd, valid, P,
-                       sh.red, row_out(P.dq, P, b, h, valid ? c0 + i : c0));
+      feature_grad_row(alo, ahi, qraw, rq, pos, i, qd, valid, P, sh.red, SB);  // S is dead
     }
+    umma::fence_async_smem();
     BWD_WAIT(&sh.bar_mma[5], ph);
-    if (tid == 0) {  // MMA4 done: V and this K buffer are free
+    if (tid == 0) {  // dq out; MMA4 done: V and this K buffer are free
+      tma_store_tile(&tmdq, SB, b, h, c0);
+      umma::bulk_commit();
       if (n + 1 < ntile) {
         umma::mbar_expect_tx(bar_v, tile_bytes);
         tma_tile(Vt, &tmv, b, h, c0 + CV, bar_v);
@@ -522,6 +522,7 @@ __global__ void __launch_bounds__(NT, 1)
       }
     }
   }
+  if (tid == 0) umma::bulk_wait_all();
   if (failed && tid == 0 && P.err) atomicOr(P.err, 4u);
   sync_tc();
   if (warp == 0) umma::tmem_dealloc(tm, 512);
@@ -532,11 +533,13 @@ __global__ void __launch_bounds__(NT, 1)
 __global__ void __launch_bounds__(NT, 1)
     tc_bwd_dkdv_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmq,
                        const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                       const __grid_constant__ CUtensorMap tmo) {
+                       const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmdk,
+                       const __grid_constant__ CUtensorMap tmdv) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  // Q: raw q -> q~ (fp16) -> q~ (bf16) -> q~w.  K: raw k -> k~ (fp16) -> k~dec.
-  // V: v -> vdec.  DO: do.  EB: E (bf16).  X: M1 (.) D^T, then M2 (.) D^T.
+  // Q: raw q -> q~ (fp16) -> q~ (bf16) -> q~w.  K: raw k -> k~ (fp16) -> k~dec,
+  // then dv (TMA-stored).  V: v -> vdec, then dk (TMA-stored).  DO: do.
+  // EB: E (bf16).  X: M1 (.) D^T, then M2 (.) D^T.
   unsigned char *Qt = base, *Kt = base + TILE, *Vt = base + 2 * TILE, *DOt = base + 3 * TILE;
   unsigned char *EB = base + 4 * TILE, *X = base + 5 * TILE;
   BwdShared &sh = *reinterpret_cast<BwdShared *>(base + 6 * TILE);
@@ -684,6 +687,11 @@ __global__ void __launch_bounds__(NT, 1)
       BWD_WAIT(&sh.bar_mma[2], ph);  // dV done: X and K are free
       store_quarter(X, i, qd, v);
     }
+    {  // dv of this tile (dV is complete) -> K, for a TMA store
+      float v[32];
+      umma::tmem_ld2x16(tA + col, v);
+      store_quarter(Kt, i, qd, v);
+    }
     umma::fence_async_smem();
     sync_tc();
     if (tid == 0) {
@@ -694,19 +702,8 @@ __global__ void __launch_bounds__(NT, 1)
       for (int kk = 0; kk < 8; ++kk)  // dK~ += V~dec E^T
         umma::mma_ss(tm + 128, umma::desc_kmajor(aV, kk, ROWS), umma::desc_kmajor(aE, kk, ROWS), id_kk, 1u);
       umma::commit(&sh.bar_mma[3]);
-      if (n > 0) {
-        umma::mbar_expect_tx(bar_k, tile_bytes);
-        tma_tile(Kt, &tmk, b, h, c0 - CV, bar_k);
-      }
-    }
-    {  // dv of this tile (dV is complete)
-      float v[32];
-      umma::tmem_ld2x16(tA + col, v);
-      if (valid) {
-        uint4 *o4 = reinterpret_cast<uint4 *>(row_out(P.dv, P, b, h, c0 + i) + col);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) o4[u] = pack8(&v[8 * u]);
-      }
+      tma_store_tile(&tmdv, Kt, b, h, c0);
+      umma::bulk_commit();
     }
 
     // [4] q~ -> q~w = gamma^{i+1} q~; E += q~w^T dO; dk epilogue overlaps it
@@ -719,9 +716,10 @@ __global__ void __launch_bounds__(NT, 1)
       for (int kk = 0; kk < 8; ++kk)  // E += Q~w^T dO
         umma::mma_ss(tm + 256, umma::desc_mnmajor(aQ, kk, ROWS), umma::desc_mnmajor(aDO, kk, ROWS), id_mnmn, 1u);
       umma::commit(&sh.bar_mma[4]);
+      umma::bulk_wait_read();  // dv has left K
       if (n > 0) {
-        umma::mbar_expect_tx(bar_v, tile_bytes);
-        tma_tile(Vt, &tmv, b, h, c0 - CV, bar_v);
+        umma::mbar_expect_tx(bar_k, tile_bytes);
+        tma_tile(Kt, &tmk, b, h, c0 - CV, bar_k);
       }
     }
     {
@@ -732,17 +730,27 @@ __global__ void __launch_bounds__(NT, 1)
         glo[e] *= P.kscale;
         ghi[e] *= P.kscale;
       }
-      feature_grad_row(glo, ghi, kraw, rk, pos, i, qd, valid, P,
-                       sh.red, row_out(P.dk, P, b, h, valid ? c0 + i : c0));
+      feature_grad_row(glo, ghi, kraw, rk, pos, i, qd, valid, P, sh.red, Vt);  // v~dec is dead
     }
+    umma::fence_async_smem();
     BWD_WAIT(&sh.bar_mma[4], ph);
-    if (tid == 0 && n > 0) {  // E update done: Q and DO are free
-      umma::mbar_expect_tx(bar_q, tile_bytes);
-      tma_tile(Qt, &tmq, b, h, c0 - CV, bar_q);
-      umma::mbar_expect_tx(bar_do, tile_bytes);
-      tma_tile(DOt, &tmo, b, h, c0 - CV, bar_do);
+    if (tid == 0) {  // E update done: Q and DO are free; dk out, then V is free
+      if (n > 0) {
+        umma::mbar_expect_tx(bar_q, tile_bytes);
+        tma_tile(Qt, &tmq, b, h, c0 - CV, bar_q);
+        umma::mbar_expect_tx(bar_do, tile_bytes);
+        tma_tile(DOt, &tmo, b, h, c0 - CV, bar_do);
+      }
+      tma_store_tile(&tmdk, Vt, b, h, c0);
+      umma::bulk_commit();
+      umma::bulk_wait_read();
+      if (n > 0) {
+        umma::mbar_expect_tx(bar_v, tile_bytes);
+        tma_tile(Vt, &tmv, b, h, c0 - CV, bar_v);
+      }
     }
   }
+  if (tid == 0) umma::bulk_wait_all();
   if (failed && tid == 0 && P.err) atomicOr(P.err, 8u);
   sync_tc();
   if (warp == 0) umma::tmem_dealloc(tm, 512);
@@ -756,29 +764,35 @@ constexpr size_t kBwdSmem = 6 * TILE + sizeof(BwdShared) + 1024;
 }  // namespace tc
 
 cudaError_t launch_tc_bwd_dq(const MixerParams &P, cudaStream_t st) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mg, mo, mdg, mdq;
   cudaError_t e;
   if ((e = tc::make_map(&mq, P.q, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mk, P.k, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mv, P.v, P, P.chunk)) != cudaSuccess) return e;
+  if ((e = tc::make_map(&mg, P.g, P, P.chunk)) != cudaSuccess) return e;
+  if ((e = tc::make_map(&mo, P.dO, P, P.chunk)) != cudaSuccess) return e;
+  if ((e = tc::make_map(&mdg, P.dg, P, P.chunk)) != cudaSuccess) return e;
+  if ((e = tc::make_map(&mdq, P.dq, P, P.chunk)) != cudaSuccess) return e;
   e = cudaFuncSetAttribute(tc::tc_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)tc::kBwdSmem);
   if (e != cudaSuccess) return e;
-  tc::tc_bwd_dq_kernel<<<dim3(P.nseg, P.H, P.B), tc::NT, tc::kBwdSmem, st>>>(P, mq, mk, mv);
+  tc::tc_bwd_dq_kernel<<<dim3(P.nseg, P.H, P.B), tc::NT, tc::kBwdSmem, st>>>(P, mq, mk, mv, mg, mo, mdg, mdq);
   return cudaGetLastError();
 }
 
 cudaError_t launch_tc_bwd_dkdv(const MixerParams &P, cudaStream_t st) {
-  CUtensorMap mq, mk, mv, mo;
+  CUtensorMap mq, mk, mv, mo, mdk, mdv;
   cudaError_t e;
   if ((e = tc::make_map(&mq, P.q, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mk, P.k, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mv, P.v, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mo, P.dO, P, P.chunk)) != cudaSuccess) return e;
+  if ((e = tc::make_map(&mdk, P.dk, P, P.chunk)) != cudaSuccess) return e;
+  if ((e = tc::make_map(&mdv, P.dv, P, P.chunk)) != cudaSuccess) return e;
   e = cudaFuncSetAttribute(tc::tc_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)tc::kBwdSmem);
   if (e != cudaSuccess) return e;
-  tc::tc_bwd_dkdv_kernel<<<dim3(P.nseg, P.H, P.B), tc::NT, tc::kBwdSmem, st>>>(P, mq, mk, mv, mo);
+  tc::tc_bwd_dkdv_kernel<<<dim3(P.nseg, P.H, P.B), tc::NT, tc::kBwdSmem, st>>>(P, mq, mk, mv, mo, mdk, mdv);
   return cudaGetLastError();
 }
 
