@@ -17,6 +17,7 @@ prints the line.  ``--impl reference`` times the CPU oracle alone.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -45,6 +46,8 @@ def parse():
                    help="target CPU time of the oracle sample")
     p.add_argument("--prefill-T", type=int, default=0,
                    help="override T of the prefill workload (small cases for ncu captures)")
+    p.add_argument("--backward-B", type=int, default=0,
+                   help="override B of the forward+backward workload (small cases for ncu captures)")
     return p.parse_args()
 
 
@@ -62,7 +65,7 @@ def measured_traffic(token_heads):
     if not (m_b and m_s):
         return None
     h = hashlib.sha256()
-    for f in ("tc_prefill.cu", "umma.cuh"):
+    for f in ("tc_prefill.cu", "tc_common.cuh", "umma.cuh"):
         h.update(open(os.path.join(ROOT, "rnn_sequence_mixer_gb300", "csrc", f), "rb").read())
     if h.hexdigest() != m_s.group(1):
         return None
@@ -265,7 +268,6 @@ def run_ours(args):
     # ---------------------------------------------------------------- prefill @512K
     w = workloads.PREFILL_512K
     if args.prefill_T:
-        import dataclasses
         w = dataclasses.replace(w, T=args.prefill_T, name=f"prefill_B1_T{args.prefill_T}_H16_d128_bf16")
     gam = api.gamma_schedule(w.H)
     inp = inputs.mixer_inputs(w.B, w.T, w.H, w.d, w.dtype, w.seed + 1000 * D.rank, device=dev)
@@ -382,6 +384,8 @@ def run_ours(args):
     # ---------------------------------------------------------------- forward + backward
     if not args.no_backward:
         wb = workloads.FWD_BWD_16K
+        if args.backward_B:
+            wb = dataclasses.replace(wb, B=args.backward_B, name=f"{wb.name}_B{args.backward_B}")
         gb = api.gamma_schedule(wb.H)
         ib = inputs.mixer_inputs(wb.B, wb.T, wb.H, wb.d, wb.dtype, wb.seed + 1000 * D.rank,
                                  device=dev, with_dy=True)
