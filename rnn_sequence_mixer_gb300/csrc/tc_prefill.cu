@@ -41,28 +41,39 @@ namespace {
 
 // ------------------------------------------------------------------ local state pass
 
+constexpr int NWORK = 16;              // worker warps (CUDA-core work), 4 warpgroups
+constexpr int NTO = (NWORK + 4) * 32;  // + one warpgroup: its first warp issues MMAs / TMA copies
+                                       // (registers are granted per warpgroup, so a lone 17th
+                                       // warp would cost as much as four)
+constexpr int kStages = 3;             // (k, v) tile pairs of the local-state pass in flight
+
 struct StateShared {
-  float red_k[4][ROWS];
-  uint64_t bar_mma[2];
-  uint64_t bar_tma[2];
+  uint64_t bar_tma[kStages];   // TMA of the (k, v) pair in stage j
+  uint64_t bar_feat[kStages];  // workers: k~dec of stage j written (one arrive per warp)
+  uint64_t bar_mma[kStages];   // MMA of stage j done (commit)
   uint32_t tmem_base;
+  uint32_t failed;
 };
 
 // kGrad = false: Delta_seg = sum_s gamma^{end-s} k~_s^T v_s   (k~ = RoPE(Norm(k)) / sqrt(d))
 // kGrad = true:  DeltaG_seg = sum_s gamma^{s-start+1} q~_s^T do_s, the backward's
 //                per-segment state gradient (q~ = RoPE(Norm(q)), do a bf16 tensor);
 //                tmk then maps q and tmv maps do.
+// Warp-specialized: 16 worker warps turn raw k rows into decay-weighted k~
+// in place (row norms from the four lanes that share a row); the issuer warp
+// issues one MMA per tile as soon as the workers are done with it and refills
+// the stage once that MMA has read it, three tiles ahead.  Workers never wait
+// for the tensor core.
 template <bool kGrad>
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(NTO, 1)
     tc_state_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  // buffer pair j: K at base + 2 j TILE, V at base + (2 j + 1) TILE
-  StateShared &sh = *reinterpret_cast<StateShared *>(base + 4 * TILE);
+  // stage j: K at base + 2 j TILE, V at base + (2 j + 1) TILE
+  StateShared &sh = *reinterpret_cast<StateShared *>(base + 2 * kStages * TILE);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int sub = warp & 3, qd = warp >> 2, i = 32 * sub + lane;
   const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int t0 = g * P.seg_len, t1 = min(P.T, t0 + P.seg_len);
   const int CV = P.chunk;
@@ -72,100 +83,112 @@ __global__ void __launch_bounds__(NT, 1)
   const uint32_t tile_bytes = (uint32_t)CV * D * 2;
 
   if (tid == 0) {
-    for (int j = 0; j < 2; ++j) {
-      umma::mbar_init(&sh.bar_mma[j], 1);
+    for (int j = 0; j < kStages; ++j) {
       umma::mbar_init(&sh.bar_tma[j], 1);
+      umma::mbar_init(&sh.bar_feat[j], NWORK);
+      umma::mbar_init(&sh.bar_mma[j], 1);
     }
     umma::mbar_fence_init();
+    sh.failed = 0;
   }
   if (warp == 0) umma::tmem_alloc(&sh.tmem_base, 128);
   // rows [CV, 128) of the V buffers are never written by TMA: clear them once
   if (CV < ROWS)
-    for (int e = tid; e < 2 * (ROWS - CV) * 16; e += NT) {
-      const int bufi = e / ((ROWS - CV) * 16), r = e % ((ROWS - CV) * 16);
-      *tile_at(base + (2 * bufi + 1) * TILE, CV + r / 16, r % 16) = make_uint4(0, 0, 0, 0);
+    for (int e = tid; e < kStages * (ROWS - CV) * 16; e += NTO) {
+      const int j = e / ((ROWS - CV) * 16), r = e % ((ROWS - CV) * 16);
+      *tile_at(base + (2 * j + 1) * TILE, CV + r / 16, r % 16) = make_uint4(0, 0, 0, 0);
     }
   sync_tc();
   const uint32_t tm = sh.tmem_base;
-  const uint32_t idesc = umma::idesc_bf16(128, 128, true, true);
-  if (tid == 0) {
-    for (int n = 0; n < 2 && n < ntile; ++n) {
-      umma::mbar_expect_tx(&sh.bar_tma[n], 2 * tile_bytes);
-      tma_tile(base + 2 * n * TILE, &tmk, b, h, t0 + n * CV, &sh.bar_tma[n]);
-      tma_tile(base + (2 * n + 1) * TILE, &tmv, b, h, t0 + n * CV, &sh.bar_tma[n]);
-    }
-  }
-
   bool failed = false;
-  for (int n = 0; n < ntile; ++n) {
-    const int buf = n & 1;
-    unsigned char *Kt = base + 2 * buf * TILE, *Vt = Kt + TILE;
-    const int c0 = t0 + n * CV, c = min(CV, t1 - c0);
-    if (wait_all(&sh.bar_tma[buf], (n >> 1) & 1)) {
-      failed = true;
-      break;
-    }
-    uint4 kr[4];
-    ld_pairs(Kt, i, qd, kr);
-    if (i >= c)  // rows past the tile hold stale bytes: use zeros
-      kr[0] = kr[1] = kr[2] = kr[3] = make_uint4(0, 0, 0, 0);
-    sh.red_k[qd][i] = sumsq_pairs(kr);
-    __syncthreads();
-    const float rk = rsqrtf((sh.red_k[0][i] + sh.red_k[1][i] + sh.red_k[2][i] + sh.red_k[3][i]) /
-                                (float)D + P.eps);
-    // decay weight of this row towards the end (forward) or from the start
-    // (gradient) of the segment; 0 past the tile
-    const int s_rel = c0 - t0 + i;
-    const float wgt = i < c ? exp2f((float)(kGrad ? s_rel + 1 : L - 1 - s_rel) * l2g) : 0.f;
-    feature_store(kr, rk * (kGrad ? 1.f : P.kscale) * wgt, P.pos_offset + c0 + i, qd, P, Kt, i,
-                  false);
-    umma::fence_async_smem();
-    sync_tc();
-    if (tid == 0) {
-      const uint32_t a = umma::smem_u32(Kt), bv = umma::smem_u32(Vt);
+
+  if (warp >= NWORK) {
+    // ---------------------------------------------------------------- issuer
+    if (warp == NWORK && lane == 0) {
+      const uint32_t idesc = umma::idesc_bf16(128, 128, true, true);
+      for (int n = 0; n < kStages && n < ntile; ++n) {
+        umma::mbar_expect_tx(&sh.bar_tma[n], 2 * tile_bytes);
+        tma_tile(base + 2 * n * TILE, &tmk, b, h, t0 + n * CV, &sh.bar_tma[n]);
+        tma_tile(base + (2 * n + 1) * TILE, &tmv, b, h, t0 + n * CV, &sh.bar_tma[n]);
+      }
+      for (int n = 0; n < ntile; ++n) {
+        const int st = n % kStages;
+        const uint32_t par = (n / kStages) & 1;
+        unsigned char *Kt = base + 2 * st * TILE;
+        wait_or_fail(&sh.bar_feat[st], par, failed);
+        if (!failed) {
+          const uint32_t a = umma::smem_u32(Kt), bv = a + TILE;
 #pragma unroll
-      for (int kk = 0; kk < ROWS / 16; ++kk)
-        umma::mma_ss(tm, umma::desc_mnmajor(a, kk, ROWS), umma::desc_mnmajor(bv, kk, ROWS), idesc,
-                     (n > 0 || kk > 0) ? 1u : 0u);
-      umma::commit(&sh.bar_mma[buf]);
+          for (int kk = 0; kk < ROWS / 16; ++kk)
+            umma::mma_ss(tm, umma::desc_mnmajor(a, kk, ROWS), umma::desc_mnmajor(bv, kk, ROWS), idesc,
+                         (n > 0 || kk > 0) ? 1u : 0u);
+          umma::commit(&sh.bar_mma[st]);
+        }
+        if (n + kStages < ntile) {  // the stage takes tile n + 3 once MMA n has read it
+          wait_or_fail(&sh.bar_mma[st], par, failed);
+          if (!failed) {
+            const int cn = t0 + (n + kStages) * CV;
+            umma::mbar_expect_tx(&sh.bar_tma[st], 2 * tile_bytes);
+            tma_tile(Kt, &tmk, b, h, cn, &sh.bar_tma[st]);
+            tma_tile(Kt + TILE, &tmv, b, h, cn, &sh.bar_tma[st]);
+          }
+        }
+      }
     }
-    // refill this buffer pair with tile n + 2 once MMA n has read it
-    if (n + 2 < ntile) {
-      if (wait_all(&sh.bar_mma[buf], (n >> 1) & 1)) {
-        failed = true;
-        break;
-      }
-      if (tid == 0) {
-        umma::mbar_expect_tx(&sh.bar_tma[buf], 2 * tile_bytes);
-        tma_tile(Kt, &tmk, b, h, c0 + 2 * CV, &sh.bar_tma[buf]);
-        tma_tile(Vt, &tmv, b, h, c0 + 2 * CV, &sh.bar_tma[buf]);
-      }
+  } else {
+    // ---------------------------------------------------------------- workers
+    const int fr = 8 * warp + (lane >> 2), fu = lane & 3;  // row, pair quarter
+    const float scale = kGrad ? 1.f : P.kscale;
+    for (int n = 0; n < ntile; ++n) {
+      const int st = n % kStages;
+      unsigned char *Kt = base + 2 * st * TILE;
+      const int c0 = t0 + n * CV, c = min(CV, t1 - c0);
+      wait_or_fail(&sh.bar_tma[st], (n / kStages) & 1, failed);
+      uint4 kr[4];
+      ld_pairs(Kt, fr, fu, kr);
+      const bool valid = fr < c;
+      if (!valid)  // rows past the tile hold stale bytes: use zeros
+        kr[0] = kr[1] = kr[2] = kr[3] = make_uint4(0, 0, 0, 0);
+      float sk = sumsq_pairs(kr);
+      sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+      sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+      const float rk = rsqrtf(sk / (float)D + P.eps);
+      // decay weight of this row towards the end (forward) or from the start
+      // (gradient) of the segment; 0 past the tile
+      const int s_rel = c0 - t0 + fr;
+      const float wgt = valid ? exp2f((float)(kGrad ? s_rel + 1 : L - 1 - s_rel) * l2g) : 0.f;
+      feature_store(kr, rk * scale * wgt, P.pos_offset + c0 + fr, fu, P, Kt, fr, false);
+      warp_arrive(&sh.bar_feat[st], lane);
     }
   }
   // the last MMA's completion covers all earlier ones
-  if (!failed) failed = wait_all(&sh.bar_mma[(ntile - 1) & 1], ((ntile - 1) >> 1) & 1);
+  {
+    const int nl = ntile - 1;
+    if (!failed && !umma::mbar_wait(&sh.bar_mma[nl % kStages], (nl / kStages) & 1)) failed = true;
+    umma::fence_after();
+    if (failed) atomicOr(&sh.failed, 1u);
+  }
+  sync_tc();
   float *out = (kGrad ? P.seg2 : P.seg) + (((size_t)b * P.H + h) * P.nseg + g) * (size_t)D * D;
-  if (!failed) {
-    float v[32];
-    umma::tmem_ld32(tm + ((uint32_t)(32 * sub) << 16) + 32 * qd, v);
-    float4 *o4 = reinterpret_cast<float4 *>(out + (size_t)i * D + 32 * qd);
+  if (warp < NWORK) {
+    const int sub = warp & 3, qd = warp >> 2, i = 32 * sub + lane;
+    if (!sh.failed) {
+      float v[32];
+      umma::tmem_ld32(tm + ((uint32_t)(32 * sub) << 16) + 32 * qd, v);
+      float4 *o4 = reinterpret_cast<float4 *>(out + (size_t)i * D + 32 * qd);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) o4[u] = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-  } else {
-    const float nan = __int_as_float(0x7fc00000);
-    for (int e = tid; e < D * D; e += NT) out[e] = nan;
-    if (tid == 0 && P.err) atomicOr(P.err, 1u);
+      for (int u = 0; u < 8; ++u) o4[u] = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+    } else {
+      const float nan = __int_as_float(0x7fc00000);
+      for (int e = tid; e < D * D; e += NWORK * 32) out[e] = nan;
+      if (tid == 0 && P.err) atomicOr(P.err, 1u);
+    }
   }
   sync_tc();
   if (warp == 0) umma::tmem_dealloc(tm, 128);
 }
 
 // ------------------------------------------------------------------ output pass
-
-constexpr int NWORK = 16;              // worker warps (CUDA-core work), 4 warpgroups
-constexpr int NTO = (NWORK + 4) * 32;  // + one warpgroup: its first warp issues MMAs / TMA copies
-                                       // (registers are granted per warpgroup, so a lone 17th
-                                       // warp would cost as much as four)
 
 struct OutShared {
   float red_o[4][ROWS];
@@ -287,15 +310,13 @@ __global__ void __launch_bounds__(NTO, 1)
                          id_qs, kk > 0);
           umma::commit(&sh.bar_mma[0]);
         }
-        // y of tile n - 1 is in G: store it, then bring in the gate of tile n
+        // y of tile n - 1 is in G: store it (the gate of tile n follows once
+        // the store has read G, after MMA3 / MMA4 are issued)
         if (n >= 1) {
           wait_or_fail(&sh.bar_epi, (n - 1) & 1, failed);
           if (!failed) {
             tma_store_tile(&tmy, Gs, b, h, c0 - CV);
             umma::bulk_commit();
-            umma::bulk_wait_read();
-            umma::mbar_expect_tx(&sh.bar_g, tile_bytes);
-            tma_tile(Gs, &tmg, b, h, c0, &sh.bar_g);
           }
         }
         // MMA2 done: Q is free for the next q
@@ -316,6 +337,11 @@ __global__ void __launch_bounds__(NTO, 1)
             umma::mma_ss(tS, umma::desc_mnmajor(ak, kk, ROWS), umma::desc_mnmajor(av, kk, ROWS),
                          id_mn, 1u);
           umma::commit(&sh.bar_mma[1]);
+        }
+        if (n >= 1 && !failed) {
+          umma::bulk_wait_read();
+          umma::mbar_expect_tx(&sh.bar_g, tile_bytes);
+          tma_tile(Gs, &tmg, b, h, c0, &sh.bar_g);
         }
         // MMA3 / MMA4 done: V and K buffer `buf` are free for the next copies
         wait_or_fail(&sh.bar_mma[1], n & 1, failed);
@@ -524,7 +550,7 @@ __global__ void __launch_bounds__(NTO, 1)
   if (warp == 0) umma::tmem_dealloc(tm, 512);
 }
 
-constexpr size_t kStateSmem = 4 * TILE + sizeof(StateShared) + 1024;
+constexpr size_t kStateSmem = 2 * kStages * TILE + sizeof(StateShared) + 1024;
 constexpr size_t kOutputSmem = 6 * TILE + sizeof(OutShared) + 1024;
 
 }  // namespace
@@ -543,7 +569,7 @@ cudaError_t launch_state_variant(const MixerParams &P, const void *a, const void
   e = cudaFuncSetAttribute(tc::tc_state_kernel<kGrad>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)tc::kStateSmem);
   if (e != cudaSuccess) return e;
-  tc::tc_state_kernel<kGrad><<<dim3(P.nseg, P.H, P.B), tc::NT, tc::kStateSmem, st>>>(P, ma, mb);
+  tc::tc_state_kernel<kGrad><<<dim3(P.nseg, P.H, P.B), tc::NTO, tc::kStateSmem, st>>>(P, ma, mb);
   return cudaGetLastError();
 }
 }  // namespace
