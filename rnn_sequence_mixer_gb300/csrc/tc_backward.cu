@@ -43,6 +43,7 @@ namespace tc {
 namespace {
 
 struct BwdShared {
+  unsigned long long ru[kMaxPairs];  // RoPE phase increments (load_rope_table)
   float red[4][ROWS];
   float red2[4][ROWS];
   float qk_diag[4][ROWS];  // parts of the fp32 q~_i . k~_i
@@ -155,8 +156,9 @@ __device__ __forceinline__ void load_pairs(uint4 (&ra)[4], const __nv_bfloat16 *
 // scratch and the call holds one CTA barrier.
 __device__ __forceinline__ void feature_grad_row(const float (&glo)[16], const float (&ghi)[16],
                                                  const uint4 (&ra)[4], float r, long long p,
-                                                 int i, int qd, bool valid, const MixerParams &P,
-                                                 float (*red)[ROWS], unsigned char *out) {
+                                                 int i, int qd, bool valid,
+                                                 const unsigned long long *ru, float (*red)[ROWS],
+                                                 unsigned char *out) {
   float n0[16], n1[16], g0[16], g1[16];
   {
     float f[8];
@@ -174,7 +176,7 @@ __device__ __forceinline__ void feature_grad_row(const float (&glo)[16], const f
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
     float c, s;
-    rope_fast(p, P.rope_u[16 * qd + e], c, s);
+    rope_fast(p, ru[4 * e + qd], c, s);
     // transpose of (x0, x1) -> (x0 c - x1 s, x0 s + x1 c)
     g0[e] = glo[e] * c + ghi[e] * s;
     g1[e] = ghi[e] * c - glo[e] * s;
@@ -238,6 +240,7 @@ __global__ void __launch_bounds__(NT, 1)
     umma::mbar_fence_init();
   }
   if (tid <= ROWS) sh.pw[tid] = exp2f((float)tid * l2g);
+  load_rope_table(sh.ru, P, tid);
   if (warp == 0) umma::tmem_alloc(&sh.tmem_base, 512);
   if (CV < ROWS)  // rows [CV, 128) of V are never written by TMA: clear them once
     for (int e = tid; e < (ROWS - CV) * 16; e += NT)
@@ -310,7 +313,7 @@ __global__ void __launch_bounds__(NT, 1)
       rq = rsqrtf((sh.red[0][i] + sh.red[1][i] + sh.red[2][i] + sh.red[3][i]) / (float)D + P.eps);
       const float rk = rsqrtf((sh.red2[0][i] + sh.red2[1][i] + sh.red2[2][i] + sh.red2[3][i]) /
                                   (float)D + P.eps) * P.kscale;
-      sh.qk_diag[qd][i] = feature_qk_store(qr, kr, rq, rk, pos, qd, P, Qt, Kt, i);
+      sh.qk_diag[qd][i] = feature_qk_store(qr, kr, rq, rk, pos, qd, sh.ru, Qt, Kt, i);
       m = fmaxf(fmaxf(sh.smax[4 * qd], sh.smax[4 * qd + 1]), fmaxf(sh.smax[4 * qd + 2], sh.smax[4 * qd + 3]));
       int e2 = 0;
       if (m > 0.f) frexpf(m, &e2);
@@ -505,7 +508,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) ahi[e] = fmaf(wi, t[e], ahi[e]);
       }
-      feature_grad_row(alo, ahi, qraw, rq, pos, i, qd, valid, P, sh.red, SB);  // S is dead
+      feature_grad_row(alo, ahi, qraw, rq, pos, i, qd, valid, sh.ru, sh.red, SB);  // S is dead
     }
     umma::fence_async_smem();
     BWD_WAIT(&sh.bar_mma[5], ph);
@@ -562,6 +565,7 @@ __global__ void __launch_bounds__(NT, 1)
     umma::mbar_fence_init();
   }
   if (tid <= ROWS) sh.pw[tid] = exp2f((float)tid * l2g);
+  load_rope_table(sh.ru, P, tid);
   if (warp == 0) umma::tmem_alloc(&sh.tmem_base, 512);
   if (CV < ROWS)  // rows [CV, 128) of V and DO are never written by TMA: clear them once
     for (int e = tid; e < 2 * (ROWS - CV) * 16; e += NT) {
@@ -632,7 +636,7 @@ __global__ void __launch_bounds__(NT, 1)
       __syncthreads();
       const float rq = rsqrtf((sh.red[0][i] + sh.red[1][i] + sh.red[2][i] + sh.red[3][i]) / (float)D + P.eps);
       rk = rsqrtf((sh.red2[0][i] + sh.red2[1][i] + sh.red2[2][i] + sh.red2[3][i]) / (float)D + P.eps);
-      sh.qk_diag[qd][i] = feature_qk_store(qr, kr, rq, rk * P.kscale, pos, qd, P, Qt, Kt, i);
+      sh.qk_diag[qd][i] = feature_qk_store(qr, kr, rq, rk * P.kscale, pos, qd, sh.ru, Qt, Kt, i);
       umma::tmem_wait_st();
     }
     umma::fence_async_smem();
@@ -730,7 +734,7 @@ __global__ void __launch_bounds__(NT, 1)
         glo[e] *= P.kscale;
         ghi[e] *= P.kscale;
       }
-      feature_grad_row(glo, ghi, kraw, rk, pos, i, qd, valid, P, sh.red, Vt);  // v~dec is dead
+      feature_grad_row(glo, ghi, kraw, rk, pos, i, qd, valid, sh.ru, sh.red, Vt);  // v~dec is dead
     }
     umma::fence_async_smem();
     BWD_WAIT(&sh.bar_mma[4], ph);

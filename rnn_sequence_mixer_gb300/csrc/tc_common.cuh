@@ -103,12 +103,26 @@ __device__ __forceinline__ float sumsq_pairs(const uint4 (&r)[4]) {
 }
 
 // cos / sin of the RoPE angle of pair u at position p on the special-function
-// unit: the exact fixed-point phase reduced to [-pi, pi), then __sincosf
-// (absolute error ~1e-6, far below the 16-bit rounding of the operands).
+// unit.  The exact fixed-point phase t (turns, mod 1) becomes a float without a
+// conversion instruction: its top 23 bits under the exponent of 1.0 give
+// f = 1 + t, and x = 2 pi (1.5 - f) = pi - 2 pi t lies in (-pi, pi], where
+// sin x = sin(2 pi t) and cos x = -cos(2 pi t).  Absolute error ~1e-6, far below
+// the 16-bit rounding of the operands.
 __device__ __forceinline__ void rope_fast(long long p, unsigned long long u, float &c, float &s) {
   const unsigned long long ph = (unsigned long long)p * u;
-  const float x = (float)(int)(ph >> 32) * 1.4629180792671596e-09f;  // 2 pi / 2^32
-  __sincosf(x, &s, &c);
+  const float f = __uint_as_float(0x3f800000u | ((uint32_t)(ph >> 32) >> 9));
+  const float x = fmaf(f, -6.2831853071795865f, 9.4247779607693797f);
+  float cx;
+  __sincosf(x, &s, &cx);
+  c = -cx;
+}
+
+// Shared-memory copy of MixerParams::rope_u, transposed so that the four lanes
+// that own pair groups 0..3 of a row read consecutive words:
+// ru[4 m + g] = rope_u[16 g + m] for pair m of group g.
+__device__ __forceinline__ void load_rope_table(unsigned long long *ru, const MixerParams &P,
+                                                int tid) {
+  if (tid < kMaxPairs) ru[4 * (tid & 15) + (tid >> 4)] = P.rope_u[tid];
 }
 
 // sigmoid via the hardware tanh: 1 / (1 + e^-z) = 0.5 + 0.5 tanh(z / 2).
@@ -120,9 +134,10 @@ __device__ __forceinline__ float sigmoid_fast(float z) {
 
 // Rotate this thread's 16 pairs of raw row `r` (times `scale`) at position p
 // and store them, as fp16 (half) or bf16, into the same chunks of `tile`.
+// `ru` is the kernel's table from load_rope_table.
 __device__ __forceinline__ void feature_store(const uint4 (&r)[4], float scale, long long p, int qd,
-                                              const MixerParams &P, unsigned char *tile, int row,
-                                              bool half) {
+                                              const unsigned long long *ru, unsigned char *tile,
+                                              int row, bool half) {
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
     float a[8], bb[8], lo[8], hi[8];
@@ -131,7 +146,7 @@ __device__ __forceinline__ void feature_store(const uint4 (&r)[4], float scale, 
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       float c, s;
-      rope_fast(p, P.rope_u[16 * qd + 8 * hf + e], c, s);
+      rope_fast(p, ru[4 * (8 * hf + e) + qd], c, s);
       const float x0 = a[e] * scale, x1 = bb[e] * scale;
       lo[e] = x0 * c - x1 * s;
       hi[e] = x0 * s + x1 * c;
@@ -146,14 +161,14 @@ __device__ __forceinline__ void feature_store(const uint4 (&r)[4], float scale, 
 // fp16), for callers that need the diagonal of Q~ K~^T exactly.
 __device__ __forceinline__ float feature_qk_store(const uint4 (&qr)[4], const uint4 (&kr)[4],
                                                  float rq, float rk, long long p, int qd,
-                                                 const MixerParams &P, unsigned char *Qt,
+                                                 const unsigned long long *ru, unsigned char *Qt,
                                                  unsigned char *Kt, int row) {
   float dot = 0.f;
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
     float c[8], s[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) rope_fast(p, P.rope_u[16 * qd + 8 * hf + e], c[e], s[e]);
+    for (int e = 0; e < 8; ++e) rope_fast(p, ru[4 * (8 * hf + e) + qd], c[e], s[e]);
     float qlo[8], qhi[8];
     {
       float a[8], bb[8];

@@ -48,6 +48,7 @@ constexpr int NTO = (NWORK + 4) * 32;  // + one warpgroup: its first warp issues
 constexpr int kStages = 3;             // (k, v) tile pairs of the local-state pass in flight
 
 struct StateShared {
+  unsigned long long ru[kMaxPairs];  // RoPE phase increments (load_rope_table)
   uint64_t bar_tma[kStages];   // TMA of the (k, v) pair in stage j
   uint64_t bar_feat[kStages];  // workers: k~dec of stage j written (one arrive per warp)
   uint64_t bar_mma[kStages];   // MMA of stage j done (commit)
@@ -91,6 +92,7 @@ __global__ void __launch_bounds__(NTO, 1)
     umma::mbar_fence_init();
     sh.failed = 0;
   }
+  load_rope_table(sh.ru, P, tid);
   if (warp == 0) umma::tmem_alloc(&sh.tmem_base, 128);
   // rows [CV, 128) of the V buffers are never written by TMA: clear them once
   if (CV < ROWS)
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(NTO, 1)
       // (gradient) of the segment; 0 past the tile
       const int s_rel = c0 - t0 + fr;
       const float wgt = valid ? exp2f((float)(kGrad ? s_rel + 1 : L - 1 - s_rel) * l2g) : 0.f;
-      feature_store(kr, rk * scale * wgt, P.pos_offset + c0 + fr, fu, P, Kt, fr, false);
+      feature_store(kr, rk * scale * wgt, P.pos_offset + c0 + fr, fu, sh.ru, Kt, fr, false);
       warp_arrive(&sh.bar_feat[st], lane);
     }
   }
@@ -191,6 +193,7 @@ __global__ void __launch_bounds__(NTO, 1)
 // ------------------------------------------------------------------ output pass
 
 struct OutShared {
+  unsigned long long ru[kMaxPairs];  // RoPE phase increments (load_rope_table)
   float red_o[4][ROWS];
   float pw[ROWS + 1];
   float smax[NWORK];
@@ -261,6 +264,7 @@ __global__ void __launch_bounds__(NTO, 1)
     sh.failed = 0;
   }
   if (tid <= ROWS) sh.pw[tid] = exp2f((float)tid * l2g);
+  load_rope_table(sh.ru, P, tid);
   if (warp == 0) umma::tmem_alloc(&sh.tmem_base, 512);
   if (CV < ROWS)  // rows [CV, 128) of V are never written by TMA: clear them once
     for (int e = tid; e < (ROWS - CV) * 16; e += NTO)
@@ -411,7 +415,7 @@ __global__ void __launch_bounds__(NTO, 1)
         // [D] q~ = RoPE(Norm(q)), k~ = RoPE(Norm(k)) / sqrt(d), fp16, in place
         const float rq = rsqrtf(sq / (float)D + P.eps);
         const float rk = rsqrtf(sk / (float)D + P.eps) * P.kscale;
-        feature_qk_store(qr, kr, rq, rk, P.pos_offset + c0 + fr, fu, P, Qt, Kt, fr);
+        feature_qk_store(qr, kr, rq, rk, P.pos_offset + c0 + fr, fu, sh.ru, Qt, Kt, fr);
         warp_arrive(&sh.bar_feat, lane);
       }
       if (drain) wait_or_fail(&sh.bar_mma[1], (n - 1) & 1, failed);  // O(n-1), S, SP ready
