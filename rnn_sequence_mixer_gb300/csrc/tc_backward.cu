@@ -55,47 +55,6 @@ struct BwdShared {
   uint32_t tmem_base;
 };
 
-// Upper-left mask of a score row: keep j <= i (weight gamma^{i-j}), zero the
-// rest.  v holds columns [jlo, jlo + 32) of row i; `valid` is i < c.
-__device__ __forceinline__ void mask_lower(float (&v)[32], int i, int jlo, bool valid, float gm,
-                                           const float *pw) {
-  const int jm = min(i, jlo + 31);
-  float w = (valid && jm >= jlo) ? pw[i - jm] : 0.f;
-#pragma unroll
-  for (int e = 31; e >= 0; --e) {
-    if (jlo + e <= i) {
-      v[e] *= w;
-      w *= gm;
-    } else {
-      v[e] = 0.f;
-    }
-  }
-}
-
-// Transposed mask: keep i <= j < c (weight gamma^{j-i}), zero the rest.
-__device__ __forceinline__ void mask_upper(float (&v)[32], int i, int jlo, int c, bool valid,
-                                           float gm, const float *pw) {
-  const int j0 = max(i, jlo);
-  float w = (valid && j0 < jlo + 32) ? pw[j0 - i] : 0.f;
-#pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    const int j = jlo + e;
-    if (j >= i && j < c) {
-      v[e] *= w;
-      w *= gm;
-    } else {
-      v[e] = 0.f;
-    }
-  }
-}
-
-// v[idx] = x for a run-time idx, as predicated moves (a dynamic index would
-// put the array in local memory).
-__device__ __forceinline__ void set_at(float (&v)[32], int idx, float x) {
-#pragma unroll
-  for (int e = 0; e < 32; ++e) v[e] = (e == idx) ? x : v[e];
-}
-
 // Sum of the four quarter parts of row i's diagonal entry.
 __device__ __forceinline__ float diag_sum(const float (*part)[ROWS], int i) {
   return part[0][i] + part[1][i] + part[2][i] + part[3][i];
@@ -350,11 +309,9 @@ __global__ void __launch_bounds__(NT, 1)
     BWD_WAIT(&sh.bar_mma[0], ph);
     {
       float pv[32];
-      umma::tmem_ld2x16(tP + col, pv);
       // the diagonal q~_i . k~_i from fp32 features: where it nearly cancels,
       // o_i and so 1 / RMS(o_i) hinge on it (fp16 operands lose it)
-      if (qd == (i >> 5)) set_at(pv, i & 31, diag_sum(sh.qk_diag, i));
-      mask_lower(pv, i, (int)col, valid, gm, sh.pw);
+      mask_lower_block(tP + col, pv, i, sub, qd, valid, gm, sh.pw, true, diag_sum(sh.qk_diag, i));
       store_quarter(PM, i, qd, pv);
       rescale_quarter(Kt, i, qd, 1.f, true);
     }
@@ -462,13 +419,9 @@ __global__ void __launch_bounds__(NT, 1)
     }
     {
       float pv[32];
-      umma::tmem_ld2x16(tP + col, pv);
-      if (qd == (i >> 5)) {
-        const float vd = diag_sum(sh.vd_diag, i);
-        set_at(pv, i & 31, vd);
-        if (valid) P.ddiag[((size_t)b * P.T + c0 + i) * P.H + h] = vd;
-      }
-      mask_lower(pv, i, (int)col, valid, gm, sh.pw);
+      const float vd = diag_sum(sh.vd_diag, i);
+      if (qd == sub && valid) P.ddiag[((size_t)b * P.T + c0 + i) * P.H + h] = vd;
+      mask_lower_block(tP + col, pv, i, sub, qd, valid, gm, sh.pw, true, vd);
       store_quarter(PM, i, qd, pv);
     }
     uint4 qraw[4];  // raw q pairs of row i for the dq epilogue (in flight during MMA7)
@@ -658,9 +611,8 @@ __global__ void __launch_bounds__(NT, 1)
     BWD_WAIT(&sh.bar_mma[0], ph);
     {
       float v[32];
-      umma::tmem_ld2x16(tA + col, v);
-      if (qd == (i >> 5)) set_at(v, i & 31, diag_sum(sh.qk_diag, i));  // fp32 k~_i . q~_i
-      mask_upper(v, i, (int)col, c, valid, gm, sh.pw);
+      mask_upper_block(tA + col, v, i, sub, qd, c, valid, gm, sh.pw, true,
+                       diag_sum(sh.qk_diag, i));  // fp32 k~_i . q~_i on the diagonal
       store_quarter(X, i, qd, v);
       rescale_quarter(Kt, i, qd, wdec, true);
     }
@@ -682,10 +634,9 @@ __global__ void __launch_bounds__(NT, 1)
     load_pairs(kraw, row_ptr(P.k, P, b, h, valid ? c0 + i : c0), qd, valid);
     {
       float v[32];
-      umma::tmem_ld2x16(tB + col, v);
-      if (qd == (i >> 5))  // fp32 v_i . do_i, kept by the dq pass
-        set_at(v, i & 31, valid ? P.ddiag[((size_t)b * P.T + c0 + i) * P.H + h] : 0.f);
-      mask_upper(v, i, (int)col, c, valid, gm, sh.pw);
+      // fp32 v_i . do_i on the diagonal, kept by the dq pass
+      const float vd = (qd == sub && valid) ? P.ddiag[((size_t)b * P.T + c0 + i) * P.H + h] : 0.f;
+      mask_upper_block(tB + col, v, i, sub, qd, c, valid, gm, sh.pw, true, vd);
       rescale_quarter(Vt, i, qd, wdec, false);
       rescale_quarter(Qt, i, qd, 1.f, true);
       BWD_WAIT(&sh.bar_mma[2], ph);  // dV done: X and K are free

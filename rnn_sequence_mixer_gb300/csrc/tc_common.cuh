@@ -132,6 +132,84 @@ __device__ __forceinline__ float sigmoid_fast(float z) {
   return fmaf(0.5f, t, 0.5f);
 }
 
+// Causal mask of one 32-column block of a score row: v gets columns
+// [32 qd, 32 qd + 32) of row i = 32 sub + lane from TMEM at taddr, keeping
+// j <= i with weight gamma^{i-j} (pw[m] = gamma^m) and zeroing the rest; every
+// entry of an invalid row (!valid) is zeroed.  The warp's block lies wholly
+// above the diagonal (qd > sub: zeros, no TMEM read), wholly below it (qd < sub:
+// no compares) or on it.  If `dset`, the diagonal entry is replaced by `dval`
+// before weighting.  Warp-collective.
+__device__ __forceinline__ void mask_lower_block(uint32_t taddr, float (&v)[32], int i, int sub, int qd,
+                                                 bool valid, float gm, const float *pw, bool dset = false,
+                                                 float dval = 0.f) {
+  if (qd > sub) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = 0.f;
+    return;
+  }
+  umma::tmem_ld2x16(taddr, v);
+  const int jlo = 32 * qd;
+  if (qd < sub) {
+    float w = valid ? pw[i - jlo - 31] : 0.f;
+#pragma unroll
+    for (int e = 31; e >= 0; --e) {
+      v[e] *= w;
+      w *= gm;
+    }
+    return;
+  }
+  const int d = i - jlo;  // lane: the diagonal entry of this row
+  float w = valid ? 1.f : 0.f;
+#pragma unroll
+  for (int e = 31; e >= 0; --e) {
+    if (e <= d) {
+      if (dset && e == d) v[e] = dval;
+      v[e] *= w;
+      w *= gm;
+    } else {
+      v[e] = 0.f;
+    }
+  }
+}
+
+// Transposed mask: keep i <= j < c with weight gamma^{j-i}.  Blocks wholly
+// below the diagonal (qd < sub) are zero without a TMEM read; blocks wholly
+// above it need the j < c test only when the tile is short.  Same conventions
+// as mask_lower_block.
+__device__ __forceinline__ void mask_upper_block(uint32_t taddr, float (&v)[32], int i, int sub, int qd,
+                                                 int c, bool valid, float gm, const float *pw,
+                                                 bool dset = false, float dval = 0.f) {
+  if (qd < sub) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = 0.f;
+    return;
+  }
+  umma::tmem_ld2x16(taddr, v);
+  const int jlo = 32 * qd;
+  if (qd > sub && jlo + 32 <= c) {
+    float w = valid ? pw[jlo - i] : 0.f;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      v[e] *= w;
+      w *= gm;
+    }
+    return;
+  }
+  const int j0 = max(i, jlo);
+  float w = (valid && j0 < jlo + 32) ? pw[j0 - i] : 0.f;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const int j = jlo + e;
+    if (j >= i && j < c) {
+      if (dset && j == i) v[e] = dval;
+      v[e] *= w;
+      w *= gm;
+    } else {
+      v[e] = 0.f;
+    }
+  }
+}
+
 // Rotate this thread's 16 pairs of raw row `r` (times `scale`) at position p
 // and store them, as fp16 (half) or bf16, into the same chunks of `tile`.
 // `ru` is the kernel's table from load_rope_table.
