@@ -200,8 +200,10 @@ def run_reference(args):
 # ----------------------------------------------------------------------------- GPU arms
 
 
-def timed(fn, steps, warmup, stream, dist_ctx, trace_count=0):
-    """Run fn(i, trace) warmup + steps times; returns (ms per step, per-pass ms lists)."""
+def timed(fn, steps, warmup, stream, dist_ctx, trace_count=0, step_events=False):
+    """Run fn(i, trace) warmup + steps times; returns (ms per step, per-pass ms lists).
+    With step_events the harness itself records a trace of two events around
+    each step (fn gets None), so the per-pass lists hold each step's time."""
     import torch
     for i in range(warmup):
         fn(i, None)
@@ -213,7 +215,12 @@ def timed(fn, steps, warmup, stream, dist_ctx, trace_count=0):
     start.record(stream)
     for i in range(steps):
         tr = [torch.cuda.Event(enable_timing=True) for _ in range(trace_count)] or None
-        fn(warmup + i, tr)
+        if step_events:
+            tr[0].record(stream)
+            fn(warmup + i, None)
+            tr[1].record(stream)
+        else:
+            fn(warmup + i, tr)
         traces.append(tr)
     end.record(stream)
     torch.cuda.synchronize()
@@ -313,32 +320,65 @@ def run_ours(args):
               "replicas": D.world}
 
     # ---------------------------------------------------------------- e2e through the API
+    # Inputs start in pinned host memory and y / the final state end there.  The
+    # sequence is streamed through hla_prefill in chunks (state chained from one
+    # call to the next, RoPE positions continued by pos_offset): the host-to-device
+    # copy of chunk j + 1, the prefill of chunk j and the device-to-host copy of y
+    # of chunk j - 1 run on three streams at once.
     e2e = None
     if not args.no_e2e:
+        n_chunk = 16 if w.T % 16 == 0 else 1
+        tc = w.T // n_chunk
         host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in inp.items()}
         for k in host:
             host[k].copy_(inp[k])
         y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
         st_host = torch.empty(st.shape, dtype=st.dtype, pin_memory=True)
         dbuf = {k: torch.empty_like(v) for k, v in inp.items()}
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        shp_c = api.make_shape(w.B, tc, w.H, w.d, chunk=w.chunk)
+        ws_c = torch.empty(api.prefill_workspace_size(shp_c), dtype=torch.uint8, device=dev)
 
         def e2e_step(i, trace):
-            for k in dbuf:
-                dbuf[k].copy_(host[k], non_blocking=True)
-            api.prefill(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["gate"], gam, chunk=w.chunk,
-                        rope_base=w.rope_base, eps=w.eps, y=y, state_out=st, workspace=ws)
-            y_host.copy_(y, non_blocking=True)
-            st_host.copy_(st, non_blocking=True)
+            start = torch.cuda.Event()
+            start.record(stream)
+            s_in.wait_event(start)
+            s_out.wait_event(start)
+            for j in range(n_chunk):
+                sl = slice(j * tc, (j + 1) * tc)
+                with torch.cuda.stream(s_in):
+                    for k in dbuf:
+                        dbuf[k][:, sl].copy_(host[k][:, sl], non_blocking=True)
+                    copied = torch.cuda.Event()
+                    copied.record(s_in)
+                stream.wait_event(copied)
+                api.prefill(dbuf["q"][:, sl], dbuf["k"][:, sl], dbuf["v"][:, sl], dbuf["gate"][:, sl],
+                            gam, st if j else None, chunk=w.chunk, pos_offset=j * tc,
+                            rope_base=w.rope_base, eps=w.eps, y=y[:, sl], state_out=st,
+                            workspace=ws_c)
+                done = torch.cuda.Event()
+                done.record(stream)
+                s_out.wait_event(done)
+                with torch.cuda.stream(s_out):
+                    y_host[:, sl].copy_(y[:, sl], non_blocking=True)
+            with torch.cuda.stream(s_out):
+                st_host.copy_(st, non_blocking=True)
+            stream.wait_stream(s_in)
+            stream.wait_stream(s_out)
 
         e_steps = max(1, min(args.steps, 5))
-        e_ms, _ = timed(e2e_step, e_steps, 1, stream, D)
-        launches += n_pass * e_steps
+        e_ms, e_step_ms = timed(e2e_step, e_steps, 1, stream, D, trace_count=2, step_events=True)
+        launches += n_pass * n_chunk * e_steps
         e_ms = D.max(e_ms)
+        e_step_ms = [p[0] for p in e_step_ms]
+        # The host link is shared with the other GPUs of the machine: a step now
+        # and then takes several times the others.  value uses the mean.
         e2e = {"value": D.world * tokens / (e_ms / 1e3) / 1e6, "unit": "Mtok/s",
-               "ms_per_step": e_ms,
+               "ms_per_step": e_ms, "ms_per_step_median": statistics.median(e_step_ms),
+               "steps_ms": [round(x, 2) for x in e_step_ms], "chunks": n_chunk,
                "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
                "d2h_bytes_per_step": y_host.numel() * 2 + st_host.numel() * 4}
-        del host, y_host, st_host, dbuf
+        del host, y_host, st_host, dbuf, ws_c
     del inp, y, ws
     torch.cuda.empty_cache()
 

@@ -155,3 +155,24 @@ def test_status_word_is_clear(dev, dtype, d):
     torch.cuda.synchronize()
     status = ws[n - 256:n - 252].view(torch.int32).item()
     assert status == 0
+
+
+def test_streamed_prefill_matches_one_shot_oracle(dev):
+    """A sequence fed through hla_prefill in pieces (each piece's final state
+    is the next one's state_in, positions continued by pos_offset) equals the
+    oracle's single pass; the last piece is ragged."""
+    B, T, H, d = 1, 6000, 4, 128
+    inp = inputs.mixer_inputs(B, T, H, d, torch.bfloat16, 41, device=dev)
+    g = gamma32(H)
+    y = torch.empty_like(inp["q"])
+    st = torch.empty((B, H, d, d), dtype=torch.float32, device=dev)
+    for j, (a, b) in enumerate([(0, 2048), (2048, 4096), (4096, T)]):
+        sl = slice(a, b)
+        api.prefill(inp["q"][:, sl], inp["k"][:, sl], inp["v"][:, sl], inp["gate"][:, sl],
+                    torch.from_numpy(g), st if j else None, chunk=128, pos_offset=a,
+                    rope_base=1e6, y=y[:, sl], state_out=st)
+    torch.cuda.synchronize()
+    ry, _, rs = oracle.prefill(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(inp["gate"]),
+                               g.astype(np.float64), None, base=1e6)
+    assert_close(f64(y), ry, 2e-2, "y")
+    assert_state_close(f64(st), rs, 2e-2, "state")
