@@ -38,8 +38,14 @@
  *     runtime; faults during execution surface at the caller's next sync.
  *   - No C++ exception crosses the ABI.  There is no mutable global state:
  *     calls on different streams may run concurrently from several threads.
- *   - Supported: d_k == d_v in {64, 128}; chunk in {64, 128}; T >= 1;
- *     1 <= H <= 256; 0 <= pos_offset and pos_offset + T < 2^62.
+ *   - Supported: d_k == d_v in {64, 128}; chunk in {64, 128}; B >= 0;
+ *     T >= 0 (T == 1 for hla_decode_step); 1 <= H <= 256; 0 <= pos_offset
+ *     and pos_offset + T < 2^62.
+ *   - An empty batch or sequence (B == 0 or T == 0) computes nothing: the
+ *     pointers of tensors with no elements may be NULL, hla_prefill leaves
+ *     state_out = state_in (zeros when state_in is NULL) and
+ *     hla_prefill_backward leaves dstate_in = dstate_out (zeros when
+ *     dstate_out is NULL); the workspace status word is still cleared.
  */
 #ifndef HLA_H_
 #define HLA_H_

@@ -23,7 +23,8 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 hla_status check_shape(const hla_shape *s, bool decode) {
   if (!s) return HLA_ERR_INVALID_ARG;
-  if (s->B < 1 || s->T < 1 || s->H < 1 || s->dk < 1 || s->dv < 1) return HLA_ERR_INVALID_ARG;
+  // B = 0 or T = 0 (an empty batch or sequence) is valid: the call has nothing to compute.
+  if (s->B < 0 || s->T < 0 || s->H < 1 || s->dk < 1 || s->dv < 1) return HLA_ERR_INVALID_ARG;
   if (s->reserved != 0) return HLA_ERR_INVALID_ARG;
   if (!(s->rope_base > 0.0) || !isfinite(s->rope_base)) return HLA_ERR_INVALID_ARG;
   if (!(s->norm_eps >= 0.0f) || !isfinite(s->norm_eps)) return HLA_ERR_INVALID_ARG;
@@ -52,6 +53,18 @@ hla_status check_gamma(const float *gamma, int H) {
 
 hla_status need(const void *p) { return (p && aligned16(p)) ? HLA_OK : HLA_ERR_INVALID_ARG; }
 hla_status maybe(const void *p) { return (!p || aligned16(p)) ? HLA_OK : HLA_ERR_INVALID_ARG; }
+// A tensor with no elements may be NULL.
+hla_status need_unless(bool empty, const void *p) { return empty ? maybe(p) : need(p); }
+
+// The state a call with nothing to compute leaves behind: out = in (copied on
+// the stream unless they alias), or zeros without an input; B * H states.
+cudaError_t pass_state(const hla_shape &s, const float *in, float *out, cudaStream_t st) {
+  if (!out || s.B == 0) return cudaSuccess;
+  const size_t bytes = (size_t)s.B * s.H * s.dk * s.dv * sizeof(float);
+  if (!in) return cudaMemsetAsync(out, 0, bytes, st);
+  if (in == out) return cudaSuccess;
+  return cudaMemcpyAsync(out, in, bytes, cudaMemcpyDeviceToDevice, st);
+}
 
 namespace {
 
@@ -106,6 +119,11 @@ Plan make_plan(const hla_shape &s) {
   Plan p;
   p.nchunk = ceil_div(s.T, s.chunk);
   long long units = (long long)s.B * s.H;
+  if (units == 0 || p.nchunk == 0) {  // empty batch or sequence: no segments
+    p.nseg = 0;
+    p.seg_len = s.chunk;
+    return p;
+  }
   int nseg = (int)((kTargetUnits + units - 1) / units);
   if (nseg < 1) nseg = 1;
   if (nseg > p.nchunk) nseg = p.nchunk;
@@ -183,11 +201,12 @@ hla_status hla_prefill(const hla_shape *s, const void *q, const void *k, const v
                        hla_stream stream, const hla_trace *trace) {
   HLA_TRY(check_shape(s, false));
   HLA_TRY(check_gamma(gamma, s->H));
-  HLA_TRY(need(q));
-  HLA_TRY(need(k));
-  HLA_TRY(need(v));
-  HLA_TRY(need(gate));
-  HLA_TRY(need(y));
+  const bool empty = s->B == 0 || s->T == 0;
+  HLA_TRY(need_unless(empty, q));
+  HLA_TRY(need_unless(empty, k));
+  HLA_TRY(need_unless(empty, v));
+  HLA_TRY(need_unless(empty, gate));
+  HLA_TRY(need_unless(empty, y));
   HLA_TRY(maybe(state_in));
   HLA_TRY(maybe(state_out));
   HLA_TRY(maybe(o));
@@ -195,6 +214,14 @@ hla_status hla_prefill(const hla_shape *s, const void *q, const void *k, const v
   Plan plan = make_plan(*s);
   size_t need_ws = seg_bytes(*s, plan) + kStatusBytes;
   if (!ws || !aligned16(ws) || ws_bytes < need_ws) return HLA_ERR_WORKSPACE;
+  if (empty) {
+    cudaStream_t st = (cudaStream_t)stream;
+    Tracer tr{trace, st};
+    HLA_LAUNCH(cudaMemsetAsync((char *)ws + need_ws - kStatusBytes, 0, sizeof(unsigned int), st));
+    HLA_LAUNCH(pass_state(*s, state_in, state_out, st));
+    for (int i = 0; i < 4; ++i) HLA_LAUNCH(tr.mark());
+    return HLA_OK;
+  }
 
   MixerParams P;
   fill_common(P, *s, gamma);
@@ -227,14 +254,16 @@ hla_status hla_decode_step(const hla_shape *s, const void *q, const void *k, con
                            hla_stream stream) {
   HLA_TRY(check_shape(s, true));
   HLA_TRY(check_gamma(gamma, s->H));
-  HLA_TRY(need(q));
-  HLA_TRY(need(k));
-  HLA_TRY(need(v));
-  HLA_TRY(need(gate));
-  HLA_TRY(need(y));
-  HLA_TRY(need(state_in));
-  HLA_TRY(need(state_out));
+  const bool empty = s->B == 0;
+  HLA_TRY(need_unless(empty, q));
+  HLA_TRY(need_unless(empty, k));
+  HLA_TRY(need_unless(empty, v));
+  HLA_TRY(need_unless(empty, gate));
+  HLA_TRY(need_unless(empty, y));
+  HLA_TRY(need_unless(empty, state_in));
+  HLA_TRY(need_unless(empty, state_out));
   HLA_TRY(maybe(o));
+  if (empty) return HLA_OK;
   if (pos && ((uintptr_t)pos & 7u)) return HLA_ERR_INVALID_ARG;
   // In-place is allowed; any other overlap of the two state buffers is not.
   size_t sb = (size_t)s->B * s->H * s->dk * s->dv * sizeof(float);
@@ -259,15 +288,9 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
                                 size_t ws_bytes, hla_stream stream, const hla_trace *trace) {
   HLA_TRY(check_shape(s, false));
   HLA_TRY(check_gamma(gamma, s->H));
-  HLA_TRY(need(q));
-  HLA_TRY(need(k));
-  HLA_TRY(need(v));
-  HLA_TRY(need(gate));
-  HLA_TRY(need(dy));
-  HLA_TRY(need(dq));
-  HLA_TRY(need(dk));
-  HLA_TRY(need(dv));
-  HLA_TRY(need(dgate));
+  const bool empty = s->B == 0 || s->T == 0;
+  const void *acts[] = {q, k, v, gate, dy, dq, dk, dv, dgate};
+  for (const void *a : acts) HLA_TRY(need_unless(empty, a));
   HLA_TRY(maybe(state_in));
   HLA_TRY(maybe(dstate_out));
   HLA_TRY(maybe(dstate_in));
@@ -276,6 +299,14 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
   size_t sbytes = seg_bytes(*s, plan);
   size_t need_ws = hla_backward_workspace_size(s);
   if (!ws || !aligned16(ws) || ws_bytes < need_ws) return HLA_ERR_WORKSPACE;
+  if (empty) {  // no tokens: the state gradient passes through unchanged
+    cudaStream_t st = (cudaStream_t)stream;
+    Tracer tr{trace, st};
+    HLA_LAUNCH(cudaMemsetAsync((char *)ws + need_ws - kStatusBytes, 0, sizeof(unsigned int), st));
+    HLA_LAUNCH(pass_state(*s, dstate_out, dstate_in, st));
+    for (int i = 0; i < 7; ++i) HLA_LAUNCH(tr.mark());
+    return HLA_OK;
+  }
 
   MixerParams P;
   fill_common(P, *s, gamma);

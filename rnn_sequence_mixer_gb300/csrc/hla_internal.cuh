@@ -100,6 +100,8 @@ hla_status check_shape(const hla_shape *s, bool decode);
 hla_status check_gamma(const float *gamma, int H);
 hla_status need(const void *p);
 hla_status maybe(const void *p);
+hla_status need_unless(bool empty, const void *p);
+cudaError_t pass_state(const hla_shape &s, const float *in, float *out, cudaStream_t st);
 void fill_common(MixerParams &P, const hla_shape &s, const float *gamma);
 size_t seg_bytes(const hla_shape &s, const Plan &p);
 void fill_rope(MixerParams &P, int D, double base);

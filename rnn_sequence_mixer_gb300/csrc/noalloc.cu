@@ -73,12 +73,16 @@ extern "C" hla_status hla_prefill_noalloc(const hla_shape *s, const void *q, con
   hla_status st = check_shape(s, false);
   if (st != HLA_OK) return st;
   if ((st = check_gamma(gamma, s->H)) != HLA_OK) return st;
+  const bool empty = s->B == 0 || s->T == 0;
   const void *required[] = {q, k, v, gate, y};
   for (const void *p : required)
-    if ((st = need(p)) != HLA_OK) return st;
+    if ((st = need_unless(empty, p)) != HLA_OK) return st;
   const void *optional[] = {state_in, state_out, o};
   for (const void *p : optional)
     if ((st = maybe(p)) != HLA_OK) return st;
+  if (empty)
+    return pass_state(*s, state_in, state_out, (cudaStream_t)stream) == cudaSuccess ? HLA_OK
+                                                                                   : HLA_ERR_CUDA;
   Plan plan;
   if ((st = capped_plan(*s, &plan)) != HLA_OK) return st;
   void *scratch = nullptr;

@@ -85,6 +85,10 @@ def test_workspace_sizes():
     # one segment state per (b, h, segment), at least one segment per (b, h)
     tiny = shape(B=1, T=1, H=1, d=64)
     assert api.prefill_workspace_size(tiny) == 64 * 64 * 4 + 256
+    # an empty sequence or batch needs only the status word
+    for empty in (shape(T=0), shape(B=0), shape(B=0, T=0)):
+        assert api.prefill_workspace_size(empty) == 256
+        assert api.backward_workspace_size(empty) == 256
 
 
 def _gamma(H, value=0.9):
@@ -101,8 +105,8 @@ def call_prefill(lib, s, gamma=None, q=FAKE, y=FAKE, ws=FAKE, ws_bytes=1 << 40):
 @pytest.mark.parametrize("kw,code", [
     (dict(d=96), _lib.HLA_ERR_UNSUPPORTED),
     (dict(chunk=32), _lib.HLA_ERR_UNSUPPORTED),
-    (dict(T=0), _lib.HLA_ERR_INVALID_ARG),
-    (dict(B=0), _lib.HLA_ERR_INVALID_ARG),
+    (dict(T=-1), _lib.HLA_ERR_INVALID_ARG),
+    (dict(B=-1), _lib.HLA_ERR_INVALID_ARG),
     (dict(H=257), _lib.HLA_ERR_UNSUPPORTED),
     (dict(pos_offset=-1), _lib.HLA_ERR_INVALID_ARG),
     (dict(rope_base=0.0), _lib.HLA_ERR_INVALID_ARG),

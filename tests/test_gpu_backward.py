@@ -94,3 +94,16 @@ def test_backward_status_word_is_clear(dev):
                          chunk=128, workspace=ws)
     torch.cuda.synchronize()
     assert ws[n - 256:n - 252].view(torch.int32).item() == 0
+
+
+@pytest.mark.parametrize("B,T", [(2, 0), (0, 7)])
+def test_backward_of_an_empty_sequence_passes_the_state_gradient(dev, B, T):
+    H, d = 2, 128
+    inp = inputs.mixer_inputs(B, T, H, d, torch.bfloat16, 8, device=dev, with_dy=True)
+    dso = inputs.state(B, H, d, 9, 0.05, device=dev)
+    out = api.prefill_backward(inp["q"], inp["k"], inp["v"], inp["gate"],
+                               torch.from_numpy(oracle.gamma(H).astype(np.float32)), inp["dy"],
+                               None, dso, chunk=128, want_dstate_in=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out[4], dso)
+    assert all(t.numel() == 0 for t in out[:4])

@@ -78,3 +78,15 @@ def test_decode_workload_sampled(dev):
     assert worst <= 2e-2, worst
     err = max_rel_err(gather_state(state, pairs), rs, head_axes=(0, 1))
     assert err <= 2e-2, err
+
+
+def test_decode_of_an_empty_batch_is_a_no_op():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    dev = torch.device("cuda:0")
+    H, d = 4, 128
+    rows = inputs.decode_inputs(1, 0, H, d, torch.bfloat16, 3, device=dev)
+    state = torch.empty((0, H, d, d), dtype=torch.float32, device=dev)
+    y, _, st = api.decode_step(rows["q"][0], rows["k"][0], rows["v"][0], rows["gate"][0],
+                               api.gamma_schedule(H), state)
+    torch.cuda.synchronize()
+    assert y.numel() == 0 and st.numel() == 0

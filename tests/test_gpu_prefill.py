@@ -176,3 +176,23 @@ def test_streamed_prefill_matches_one_shot_oracle(dev):
                                g.astype(np.float64), None, base=1e6)
     assert_close(f64(y), ry, 2e-2, "y")
     assert_state_close(f64(st), rs, 2e-2, "state")
+
+
+@pytest.mark.parametrize("B,T", [(1, 0), (0, 5), (3, 0)])
+def test_empty_inputs_pass_the_state_through(dev, B, T):
+    """An empty batch or sequence computes nothing: state_out = state_in, or
+    zeros without state_in; the status word is cleared."""
+    H, d = 3, 128
+    inp = inputs.mixer_inputs(B, T, H, d, torch.bfloat16, 5, device=dev)
+    g = torch.from_numpy(gamma32(H))
+    s0 = inputs.state(B, H, d, 6, 0.1, device=dev)
+    _, _, st = api.prefill(inp["q"], inp["k"], inp["v"], inp["gate"], g, s0, chunk=128)
+    torch.cuda.synchronize()
+    assert torch.equal(st, s0)
+    shape = api.make_shape(B, T, H, d, chunk=128, dtype=torch.bfloat16)
+    n = api.prefill_workspace_size(shape)
+    ws = torch.full((n,), 0xAB, dtype=torch.uint8, device=dev)
+    _, _, st0 = api.prefill(inp["q"], inp["k"], inp["v"], inp["gate"], g, chunk=128, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(st0).item() == 0
+    assert ws[n - 256:n - 252].view(torch.int32).item() == 0
