@@ -234,14 +234,22 @@ def timed(fn, steps, warmup, stream, dist_ctx, trace_count=0, step_events=False)
 
 
 class Dist:
-    def __init__(self):
+    """One process per GPU under torchrun (RANK / LOCAL_RANK / WORLD_SIZE /
+    MASTER_* from the environment).  The bench runs an independent replica on
+    every rank: no data moves between ranks, only the barrier around each timed
+    region and the max of the per-rank times.  backend: "nccl" for GPU runs,
+    "gloo" for host-only use (tests)."""
+
+    def __init__(self, backend: str = "nccl"):
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
         self.rank = int(os.environ.get("RANK", "0"))
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.backend = backend
         self.pg = None
         if self.world > 1:
             import torch.distributed as dist
-            dist.init_process_group("nccl")
+            if not dist.is_initialized():
+                dist.init_process_group(backend)
             self.pg = dist
 
     def barrier(self):
@@ -249,12 +257,20 @@ class Dist:
             self.pg.barrier()
 
     def max(self, x: float) -> float:
+        """The largest x over all ranks (every rank gets it)."""
         if not self.pg:
             return x
         import torch
-        t = torch.tensor([x], device=f"cuda:{self.local}")
+        dev = f"cuda:{self.local}" if self.backend == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
         self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
         return float(t.item())
+
+
+def job_rate(units_per_rank: float, max_ms: float, world: int) -> float:
+    """Whole-job throughput of `world` replicas, each processing units_per_rank
+    units, bounded by the slowest rank (units per second)."""
+    return world * units_per_rank / (max_ms / 1e3)
 
 
 def run_ours(args):
@@ -293,7 +309,7 @@ def run_ours(args):
     launches += n_pass * args.steps
     ms = D.max(ms)
     tokens = w.B * w.T
-    value = D.world * tokens / (ms / 1e3) / 1e6
+    value = job_rate(tokens, ms, D.world) / 1e6
     pass_names = ["seg_state", "state_scan", "seg_output"]
     pass_ms = [statistics.mean(p[j] for p in passes) for j in range(n_pass)]
     dom = max(range(n_pass), key=lambda j: pass_ms[j])
@@ -373,7 +389,7 @@ def run_ours(args):
         e_step_ms = [p[0] for p in e_step_ms]
         # The host link is shared with the other GPUs of the machine: a step now
         # and then takes several times the others.  value uses the mean.
-        e2e = {"value": D.world * tokens / (e_ms / 1e3) / 1e6, "unit": "Mtok/s",
+        e2e = {"value": job_rate(tokens, e_ms, D.world) / 1e6, "unit": "Mtok/s",
                "ms_per_step": e_ms, "ms_per_step_median": statistics.median(e_step_ms),
                "steps_ms": [round(x, 2) for x in e_step_ms], "chunks": n_chunk,
                "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
@@ -412,7 +428,7 @@ def run_ours(args):
         us = D.max(1e3 * statistics.mean(per))
         bytes_step = wd.B * wd.H * (2 * wd.d * wd.d * 4 + 5 * wd.d * BF16)
         ach = bytes_step / (us / 1e6) / 1e9
-        out["decode"] = {"workload": wd.name, "tok_s": D.world * wd.B / (us / 1e6),
+        out["decode"] = {"workload": wd.name, "tok_s": job_rate(wd.B, us / 1e3, D.world),
                          "us_per_step": us, "us_per_step_median": 1e3 * statistics.median(per),
                          "steps": wd.steps, "l2": "flushed (512 MiB write) before every step",
                          "roofline": {"kernel": "decode_step", "bound": "hbm", "achieved": ach,
@@ -453,7 +469,7 @@ def run_ours(args):
         thb = wb.B * wb.T * wb.H
         alg_b = thb * (5 * wb.d * BF16 + 9 * wb.d * BF16)  # fwd 5 d-rows + bwd 5 in / 4 out
         out["fwd_bwd"] = {"workload": wb.name, "chunk": wb.chunk, "ms_per_step": b_ms,
-                          "Mtok_s": D.world * wb.B * wb.T / (b_ms / 1e3) / 1e6,
+                          "Mtok_s": job_rate(wb.B * wb.T, b_ms, D.world) / 1e6,
                           "alg_bytes": alg_b, "frac_hbm": alg_b / (b_ms / 1e3) / 1e9 / hbm_peak,
                           "pass_ms": b_pass_ms}
         del ib, wsb, wsf, yb
