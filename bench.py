@@ -51,25 +51,26 @@ def parse():
     return p.parse_args()
 
 
-def measured_traffic(token_heads):
-    """DRAM bytes per launch of tc_output_kernel from the committed ncu summary,
-    scaled to `token_heads`; None when the kernel source changed since the capture."""
+def measured_traffic(record: str, sources, units: float):
+    """DRAM bytes per launch of a kernel from a committed ncu summary
+    (profiles/<record>: `bytes_per_unit` and the sha256 of the listed kernel
+    sources), scaled to `units`; None when a source changed since the capture."""
     import hashlib
     import re
-    path = os.path.join(ROOT, "profiles", "traffic_tc_output.md")
+    path = os.path.join(ROOT, "profiles", record)
     if not os.path.exists(path):
         return None
     text = open(path).read()
-    m_b = re.search(r"bytes_per_token_head:\s*([0-9.]+)", text)
+    m_b = re.search(r"bytes_per_(?:token_head|unit):\s*([0-9.]+)", text)
     m_s = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     if not (m_b and m_s):
         return None
     h = hashlib.sha256()
-    for f in ("tc_prefill.cu", "tc_common.cuh", "umma.cuh"):
+    for f in sources:
         h.update(open(os.path.join(ROOT, "rnn_sequence_mixer_gb300", "csrc", f), "rb").read())
     if h.hexdigest() != m_s.group(1):
         return None
-    return float(m_b.group(1)) * token_heads
+    return float(m_b.group(1)) * units
 
 
 def peaks():
@@ -135,16 +136,39 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- oracle timing
 
 
-def oracle_sample(w, seconds: float):
+def host_cpu_model() -> str:
+    """The host CPU's model name (lscpu), else the machine type."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
+
+
+def oracle_sample(w, seconds: float, threads: int = 0):
     """Time the fp64 oracle on a bounded sample of workload ``w`` (all H heads of
     one sequence, the first n tokens), growing n until the sample takes about
-    ``seconds``.  Returns (tokens/s, n_tokens, threads)."""
+    ``seconds``; on ``threads`` cores (0: all).  Returns (tokens/s, n_tokens,
+    threads, seconds)."""
     import numpy as np
     import torch
 
     import oracle
     from rnn_sequence_mixer_gb300 import inputs
 
+    all_threads = oracle.threads()
+    oracle.set_threads(threads or all_threads)
+    try:
+        return _oracle_sample(w, seconds, oracle, np, torch, inputs)
+    finally:
+        oracle.set_threads(all_threads)
+
+
+def _oracle_sample(w, seconds, oracle, np, torch, inputs):
     gam = oracle.gamma(w.H).astype(np.float32).astype(np.float64)
     n, spent = 256, 0.0
     while True:
@@ -323,7 +347,8 @@ def run_ours(args):
     a_bytes = alg[pass_names[dom]]
     achieved = a_bytes / (pass_ms[dom] / 1e3) / 1e9
     whole = th * 5 * w.d * BF16 / (ms / 1e3) / 1e9
-    traffic = measured_traffic(th) if pass_names[dom] == "seg_output" else None
+    traffic = (measured_traffic("traffic_tc_output.md", ("tc_prefill.cu", "tc_common.cuh", "umma.cuh"),
+                                th) if pass_names[dom] == "seg_output" else None)
     roof = {"kernel": pass_names[dom], "bound": "hbm", "achieved": achieved, "peak": hbm_peak,
             "unit": "GB/s", "frac": achieved / hbm_peak,
             "traffic": traffic / 1e9 if traffic else None, "traffic_unit": "GB per launch",
@@ -426,14 +451,53 @@ def run_ours(args):
         per = [a.elapsed_time(b) for a, b in ev]
         launches += wd.steps
         us = D.max(1e3 * statistics.mean(per))
+        # The same 256 steps (flush, decode, position update) captured once as a
+        # CUDA graph and replayed: the library neither allocates nor synchronizes
+        # inside a call, so a decode step is capturable.  Events inside a graph
+        # cannot be timed, so a second graph without the decode steps is replayed
+        # too and the difference is the decode time.
+        graph_us = None
+        try:
+            def capture(with_decode):
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph):
+                    for s in range(wd.steps):
+                        flush.fill_(float(s))
+                        if with_decode:
+                            api.decode_step(steps["q"][s], steps["k"][s], steps["v"][s],
+                                            steps["gate"][s], gd, state, pos,
+                                            rope_base=wd.rope_base, eps=wd.eps, y=yd)
+                        pos.add_(1)
+                return graph
+
+            def replay_ms(graph):
+                graph.replay()  # warm
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                a.record(stream)
+                graph.replay()
+                b.record(stream)
+                torch.cuda.synchronize()
+                return a.elapsed_time(b)
+
+            g_all, g_flush = capture(True), capture(False)
+            graph_us = 1e3 * (replay_ms(g_all) - replay_ms(g_flush)) / wd.steps
+            launches += 2 * wd.steps
+            del g_all, g_flush
+        except RuntimeError:
+            graph_us = None
         bytes_step = wd.B * wd.H * (2 * wd.d * wd.d * 4 + 5 * wd.d * BF16)
         ach = bytes_step / (us / 1e6) / 1e9
         out["decode"] = {"workload": wd.name, "tok_s": job_rate(wd.B, us / 1e3, D.world),
                          "us_per_step": us, "us_per_step_median": 1e3 * statistics.median(per),
+                         "graph_us_per_step": graph_us,
                          "steps": wd.steps, "l2": "flushed (512 MiB write) before every step",
                          "roofline": {"kernel": "decode_step", "bound": "hbm", "achieved": ach,
                                       "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
-                                      "alg_bytes": bytes_step, "traffic": None}}
+                                      "alg_bytes": bytes_step,
+                                      "traffic": measured_traffic(
+                                          "traffic_decode.md", ("decode.cu", "hla_internal.cuh"),
+                                          wd.B * wd.H)}}
         del steps, state, flush
         torch.cuda.empty_cache()
 
@@ -479,9 +543,13 @@ def run_ours(args):
     cpu = None
     if D.rank == 0 and not args.no_cpu_baseline:
         tok_s, n, cores, dt = oracle_sample(w, args.cpu_seconds)
+        tok_1, n_1, _, dt_1 = oracle_sample(w, max(1.0, args.cpu_seconds / 4), threads=1)
         cpu = {"value": tok_s / 1e6, "unit": "Mtok/s", "cores": cores, "kind": "oracle",
                "sample": f"first {n} tokens of sequence 0 of the 512K workload, all {w.H} heads, "
-                         f"fp64, {dt:.1f} s"}
+                         f"fp64, {dt:.1f} s",
+               "value_1core": tok_1 / 1e6,
+               "sample_1core": f"first {n_1} tokens, all {w.H} heads, one thread, {dt_1:.1f} s",
+               "cpu_model": host_cpu_model()}
 
     if D.rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "Mtok/s", "n_gpus": D.world,

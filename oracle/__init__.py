@@ -52,6 +52,7 @@ def _load():
     lib = ctypes.CDLL(build())
     i, d64, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_double
     lib.hla_oracle_threads.restype = i
+    lib.hla_oracle_set_threads.argtypes = [i]
     lib.hla_oracle_gamma.argtypes = [i, _dp]
     lib.hla_oracle_feature.argtypes = [i, _dp, d64, dbl, dbl, dbl, _dp]
     lib.hla_oracle_prefill.argtypes = [i, i, i, i, _dp, _dp, _dp, _dp, _dp, _dp, d64, dbl, dbl,
@@ -85,6 +86,11 @@ def _ptr(x):
 def threads() -> int:
     """OpenMP threads the oracle uses (all host cores unless OMP_NUM_THREADS)."""
     return int(_load().hla_oracle_threads())
+
+
+def set_threads(n: int) -> None:
+    """Use n OpenMP threads for the following calls (timing on fewer cores)."""
+    _load().hla_oracle_set_threads(int(n))
 
 
 def gamma(H: int) -> np.ndarray:

@@ -51,6 +51,15 @@ int hla_oracle_threads(void) {
 #endif
 }
 
+/* Threads for the following oracle calls (for timing it on fewer cores). */
+void hla_oracle_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 /* Eq. 19: gamma_h = exp(-2^(-8h/H)) for the paper's h = 1..H. */
 void hla_oracle_gamma(int H, double *gamma) {
   for (int h = 0; h < H; ++h) gamma[h] = exp(-pow(2.0, -8.0 * (double)(h + 1) / (double)H));
