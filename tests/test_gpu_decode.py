@@ -21,6 +21,9 @@ def dev():
     (2, 2, 128, torch.float32, False, False),
     (5, 3, 128, torch.bfloat16, True, False),
     (1, 32, 64, torch.bfloat16, False, True),
+    (16, 32, 128, torch.bfloat16, True, True),
+    (9, 40, 64, torch.float32, True, False),
+    (1, 16, 128, torch.bfloat16, False, False),
 ])
 def test_decode_small(dev, B, H, d, dtype, use_pos, inplace):
     g = oracle.gamma(H).astype(np.float32)
