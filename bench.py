@@ -42,6 +42,7 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-decode", action="store_true")
     p.add_argument("--no-backward", action="store_true")
+    p.add_argument("--no-mma-bench", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle sample")
     p.add_argument("--prefill-T", type=int, default=0,
@@ -538,6 +539,36 @@ def run_ours(args):
                           "pass_ms": b_pass_ms}
         del ib, wsb, wsf, yb
         torch.cuda.empty_cache()
+
+    # ---------------------------------------------------------------- MMA ceiling
+    # The output pass's four MMAs per 128-token tile, issued back to back on
+    # shared-memory-resident operands, one CTA per SM: the tensor-core ceiling of
+    # the pass (its own MMAs keep the tensor pipe ~16 % busy; CUDA-core work
+    # bounds it).
+    if not args.no_mma_bench:
+        import ctypes
+        from rnn_sequence_mixer_gb300 import build as libbuild
+        mlib = ctypes.CDLL(libbuild.build_mmabench())
+        mlib.hla_mmabench_run.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_float)]
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        iters = 4000
+        ms_m = ctypes.c_float(0.0)
+        rc = mlib.hla_mmabench_run(sms, iters, ctypes.byref(ms_m))
+        if rc == 0 and ms_m.value > 0:
+            flops = sms * iters * 4 * 2.0 * 128 ** 3
+            tf = flops / (ms_m.value / 1e3) / 1e12
+            # clock-derived dense rate: 8192 bf16/fp16 FLOP per clock per SM (4096 FMA) at the
+            # maximum SM clock; the measured cuBLAS figure ran power-capped at a lower clock
+            clock_mhz = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))).get(
+                "sm_max_mhz", 2070.0)) if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else 2070.0
+            clock_peak = sms * 8192 * clock_mhz * 1e6 / 1e12
+            out["mma_rate"] = {"what": "MMA1-MMA4 of the output pass, 128x128x128 each, operands "
+                                       "in shared memory, one CTA per SM",
+                               "achieved": tf, "peak": tc_peak, "unit": "TFLOP/s",
+                               "frac": tf / tc_peak, "peak_source": f"bf16_tflops of {peak_src}",
+                               "clock_peak": clock_peak, "frac_clock_peak": tf / clock_peak,
+                               "ms": ms_m.value}
+        launches += 1
 
     # ---------------------------------------------------------------- CPU oracle
     cpu = None

@@ -20,6 +20,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libhla.so")
+# Measurement-only companion: the tensor-core rate of the prefill's MMA sequence
+# with shared-memory-resident operands (bench.py); not part of the C ABI.
+MMABENCH_SRC = os.path.join(CSRC, "microbench", "mma_rate.cu")
+MMABENCH_LIB = os.path.join(BUILD, "libhla_mmabench.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
@@ -82,3 +86,19 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True))
+
+
+def build_mmabench(force: bool = False) -> str:
+    """Compile libhla_mmabench.so (one translation unit) next to libhla.so."""
+    deps = [MMABENCH_SRC, os.path.join(CSRC, "umma.cuh"), os.path.join(CSRC, "hla_internal.cuh")]
+    if (not force and os.path.exists(MMABENCH_LIB)
+            and all(os.path.getmtime(p) <= os.path.getmtime(MMABENCH_LIB) for p in deps)):
+        return MMABENCH_LIB
+    os.makedirs(BUILD, exist_ok=True)
+    tmp = MMABENCH_LIB + ".tmp"
+    cmd = [_nvcc(), *NVCC_FLAGS, "-shared", MMABENCH_SRC, "-o", tmp]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError(f"nvcc failed on mma_rate.cu:\n{res.stderr}")
+    os.replace(tmp, MMABENCH_LIB)
+    return MMABENCH_LIB
