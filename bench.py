@@ -533,10 +533,16 @@ def run_ours(args):
                      for j, nm in enumerate(b_names) if nm}
         thb = wb.B * wb.T * wb.H
         alg_b = thb * (5 * wb.d * BF16 + 9 * wb.d * BF16)  # fwd 5 d-rows + bwd 5 in / 4 out
+        # tensor-core work: 21 MMAs of 128 x 128 x 128 per 128-token tile and head
+        # (forward: local state 1 + output 4; backward: local state 1, dq pass 7,
+        # state-gradient sums 1, dk/dv pass 7)
+        flops_b = 21 * 2.0 * 128 ** 3 * thb / 128
+        roof_ms = max(alg_b / (hbm_peak * 1e9), flops_b / (tc_peak * 1e12)) * 1e3
         out["fwd_bwd"] = {"workload": wb.name, "chunk": wb.chunk, "ms_per_step": b_ms,
                           "Mtok_s": job_rate(wb.B * wb.T, b_ms, D.world) / 1e6,
                           "alg_bytes": alg_b, "frac_hbm": alg_b / (b_ms / 1e3) / 1e9 / hbm_peak,
-                          "pass_ms": b_pass_ms}
+                          "tensor_flops": flops_b, "roofline_ms": roof_ms,
+                          "frac_roofline": roof_ms / b_ms, "pass_ms": b_pass_ms}
         del ib, wsb, wsf, yb
         torch.cuda.empty_cache()
 
