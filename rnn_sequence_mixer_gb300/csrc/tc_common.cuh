@@ -102,6 +102,25 @@ __device__ __forceinline__ float sumsq_pairs(const uint4 (&r)[4]) {
   return s;
 }
 
+// one pass over this lane's pairs of a row: sums of a_e^2, b_e^2 and a_e b_e
+// (fp32; the raw q . k gives the fp32 diagonal q~_i . k~_i)
+__device__ __forceinline__ void norms_and_dot(const uint4 (&a)[4], const uint4 (&b)[4],
+                                              float &saa, float &sbb, float &sab) {
+  saa = sbb = sab = 0.f;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    float x[8], y[8];
+    unpack8(a[u], x);
+    unpack8(b[u], y);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      saa = fmaf(x[e], x[e], saa);
+      sbb = fmaf(y[e], y[e], sbb);
+      sab = fmaf(x[e], y[e], sab);
+    }
+  }
+}
+
 // cos / sin of the RoPE angle of pair u at position p on the special-function
 // unit.  The exact fixed-point phase t (turns, mod 1) becomes a float without a
 // conversion instruction: its top 23 bits under the exponent of 1.0 give

@@ -196,6 +196,7 @@ struct OutShared {
   unsigned long long ru[kMaxPairs];  // RoPE phase increments (load_rope_table)
   float red_o[4][ROWS];
   float pw[ROWS + 1];
+  float qk_diag[2][ROWS];  // fp32 q~_i . k~_i of tiles n (n & 1)
   float smax[NWORK];
   uint64_t bar_mma[2];  // [0]: MMA1 + MMA2 of a tile done, [1]: MMA3 + MMA4 done (commits)
   uint64_t bar_p;       // MMA1 (P) of a tile done
@@ -206,6 +207,7 @@ struct OutShared {
   uint64_t bar_feat;    // workers: q~, k~ of the tile written (one arrive per warp)
   uint64_t bar_sb;      // workers: Sb written and S rescaled
   uint64_t bar_pm;      // workers: Pm, scaled O and k~dec written
+  uint64_t bar_diag;    // diagonal warp: fp32 diagonal patched into Pm
   uint64_t bar_epi;     // workers: y of the previous tile written over its gate tile
   uint32_t tmem_base;
   uint32_t failed;
@@ -259,6 +261,7 @@ __global__ void __launch_bounds__(NTO, 1)
     umma::mbar_init(&sh.bar_feat, NWORK);
     umma::mbar_init(&sh.bar_sb, NWORK);
     umma::mbar_init(&sh.bar_pm, NWORK);
+    umma::mbar_init(&sh.bar_diag, 1);
     umma::mbar_init(&sh.bar_epi, NWORK);
     umma::mbar_fence_init();
     sh.failed = 0;
@@ -329,7 +332,7 @@ __global__ void __launch_bounds__(NTO, 1)
           umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
           tma_tile(Qs, &tmq, b, h, c0 + CV, &sh.bar_q);
         }
-        wait_or_fail(&sh.bar_pm, n & 1, failed);
+        wait_or_fail(&sh.bar_diag, n & 1, failed);  // follows bar_pm
         wait_or_fail(&sh.bar_v, n & 1, failed);
         if (!failed) {
 #pragma unroll
@@ -367,6 +370,22 @@ __global__ void __launch_bounds__(NTO, 1)
         umma::bulk_commit();
       }
       umma::bulk_wait_all();
+    } else if (warp == NWORK + 1) {
+      // the diagonal of Pm from fp32 features.  Where q~_i . k~_i nearly cancels
+      // (a row whose output is almost only its own term: t = 0, or gamma near 0)
+      // the fp16 operands of MMA1 lose it; its weight is gamma^0 = 1.
+      for (int n = 0; n < ntile; ++n) {
+        wait_or_fail(&sh.bar_pm, n & 1, failed);
+        if (!failed) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int r = 32 * u + lane;
+            *(reinterpret_cast<__nv_bfloat16 *>(tile_at(SP, r, r >> 3)) + (r & 7)) =
+                __float2bfloat16_rn(sh.qk_diag[n & 1][r]);
+          }
+        }
+        warp_arrive(&sh.bar_diag, lane);
+      }
     }
   } else {
     // ---------------------------------------------------------------- worker warps
@@ -407,14 +426,20 @@ __global__ void __launch_bounds__(NTO, 1)
         const bool fvalid = fr < c;
         if (!fvalid)  // rows past the tile hold stale bytes: use zeros
           qr[0] = qr[1] = qr[2] = qr[3] = kr[0] = kr[1] = kr[2] = kr[3] = make_uint4(0, 0, 0, 0);
-        float sq = sumsq_pairs(qr), sk = sumsq_pairs(kr);
+        float sq, sk, qk;
+        norms_and_dot(qr, kr, sq, sk, qk);
         sq += __shfl_xor_sync(0xffffffffu, sq, 1);
         sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+        qk += __shfl_xor_sync(0xffffffffu, qk, 1);
         sq += __shfl_xor_sync(0xffffffffu, sq, 2);
         sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+        qk += __shfl_xor_sync(0xffffffffu, qk, 2);
         // [D] q~ = RoPE(Norm(q)), k~ = RoPE(Norm(k)) / sqrt(d), fp16, in place
         const float rq = rsqrtf(sq / (float)D + P.eps);
         const float rk = rsqrtf(sk / (float)D + P.eps) * P.kscale;
+        // q~_i . k~_i in fp32 (one rotation acts on both, so RoPE drops out);
+        // zero on rows past the tile.  The diagonal warp reads it after bar_pm.
+        if (fu == 0) sh.qk_diag[buf][fr] = qk * rq * rk;
         feature_qk_store(qr, kr, rq, rk, P.pos_offset + c0 + fr, fu, sh.ru, Qt, Kt, fr);
         warp_arrive(&sh.bar_feat, lane);
       }

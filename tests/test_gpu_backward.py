@@ -107,3 +107,24 @@ def test_backward_of_an_empty_sequence_passes_the_state_gradient(dev, B, T):
     torch.cuda.synchronize()
     assert torch.equal(out[4], dso)
     assert all(t.numel() == 0 for t in out[:4])
+
+
+def test_backward_large_magnitudes(dev):
+    """The tensor-core backward with q, k, v scaled by 1e2 / 1e2 / 1e3, gates of
+    +-20 and a large upstream gradient."""
+    B, T, H, d = 1, 600, 4, 128
+    g = oracle.gamma(H).astype(np.float32)
+    inp = inputs.mixer_inputs(B, T, H, d, torch.float32, 73, device=dev, with_dy=True)
+    for k, sc in (("q", 100.0), ("k", 100.0), ("v", 1000.0), ("gate", 20.0), ("dy", 50.0)):
+        inp[k] *= sc
+    inp = {k: v.to(torch.bfloat16) for k, v in inp.items()}
+    out = api.prefill_backward(inp["q"], inp["k"], inp["v"], inp["gate"], torch.from_numpy(g),
+                               inp["dy"], chunk=128, rope_base=1e6, want_dstate_in=True)
+    torch.cuda.synchronize()
+    ref = oracle.backward(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(inp["gate"]),
+                          g.astype(np.float64), f64(inp["dy"]), base=1e6)
+    for name, got, want in zip(["dq", "dk", "dv", "dgate"], out[:4], ref[:4]):
+        assert torch.isfinite(got.float()).all(), name
+        err = max_rel_err(f64(got), want)
+        assert err <= 2e-2, f"{name}: {err:.3e}"
+    assert max_rel_err(f64(out[4]), ref[4], head_axes=(0, 1)) <= 2e-2

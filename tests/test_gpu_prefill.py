@@ -196,3 +196,34 @@ def test_empty_inputs_pass_the_state_through(dev, B, T):
     torch.cuda.synchronize()
     assert torch.count_nonzero(st0).item() == 0
     assert ws[n - 256:n - 252].view(torch.int32).item() == 0
+
+
+@pytest.mark.parametrize("case", ["large_magnitudes", "single_token", "tiny_gamma"])
+def test_tensor_core_path_edge_inputs(dev, case):
+    """bf16 at d = 128 (the tensor-core kernels) away from N(0, 1) inputs: q, k,
+    v scaled by 1e2 / 1e2 / 1e3 with gates of +-20 (the fp16 state scaling and
+    the norms must absorb them), a single token, and gamma = 1e-6 (every decay
+    power underflows after one step)."""
+    B, T, H, d = 1, 777, 4, 128
+    g = gamma32(H)
+    if case == "single_token":
+        T = 1
+    if case == "tiny_gamma":
+        g = np.full(H, 1e-6, dtype=np.float32)
+    inp = inputs.mixer_inputs(B, T, H, d, torch.float32, 71, device=dev)
+    if case == "large_magnitudes":
+        inp["q"] *= 100.0
+        inp["k"] *= 100.0
+        inp["v"] *= 1000.0
+        inp["gate"] *= 20.0
+    inp = {k: v.to(torch.bfloat16) for k, v in inp.items()}
+    s0 = inputs.state(B, H, d, 72, scale=1.0 if case == "large_magnitudes" else 0.1, device=dev)
+    y, o, st = api.prefill(inp["q"], inp["k"], inp["v"], inp["gate"], torch.from_numpy(g), s0,
+                           chunk=128, rope_base=1e6, want_o=True)
+    torch.cuda.synchronize()
+    ry, ro, rs = oracle.prefill(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(inp["gate"]),
+                                g.astype(np.float64), f64(s0), base=1e6)
+    assert torch.isfinite(y.float()).all() and torch.isfinite(st).all()
+    assert_close(f64(o), ro, 2e-2, "o")
+    assert_close(f64(y), ry, 2e-2, "y")
+    assert_state_close(f64(st), rs, 2e-2, "state")
