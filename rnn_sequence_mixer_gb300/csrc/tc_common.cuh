@@ -59,6 +59,78 @@ __device__ __forceinline__ uint4 pack8h(const float *f) {
                     pack2h(f[6], f[7]));
 }
 
+// ------------------------------------------------------------------ packed fp32
+// sm_100-class SMs run fp32 multiplies and FMAs on register pairs
+// (mul.rn.f32x2, fma.rn.f32x2): one instruction does two lanes of work with the
+// rounding of the scalar forms.  The element-wise phases use them to halve
+// their share of the issue slots.
+typedef unsigned long long f2;  // {lo, hi}
+
+__device__ __forceinline__ f2 mk2(float lo, float hi) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ f2 dup2(float x) { return mk2(x, x); }
+__device__ __forceinline__ void split2(f2 r, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  f2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+  f2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ float hsum2(f2 r) {
+  float lo, hi;
+  split2(r, lo, hi);
+  return lo + hi;
+}
+// bf16x2 / fp16x2 word <-> two fp32 lanes
+__device__ __forceinline__ f2 f2_of_bf(uint32_t w) {
+  return mk2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+__device__ __forceinline__ f2 f2_of_h(uint32_t w) {
+  const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w));
+  return mk2(t.x, t.y);
+}
+__device__ __forceinline__ uint32_t bf_of_f2(f2 r) {
+  float lo, hi;
+  split2(r, lo, hi);
+  return pack2(lo, hi);
+}
+__device__ __forceinline__ uint32_t h_of_f2(f2 r) {
+  float lo, hi;
+  split2(r, lo, hi);
+  return pack2h(lo, hi);
+}
+// the eight bf16 (fp16) of a 16-byte chunk as four fp32 pairs, and back
+__device__ __forceinline__ void unpack4x2(const uint4 &u, f2 (&x)[4]) {
+  x[0] = f2_of_bf(u.x); x[1] = f2_of_bf(u.y); x[2] = f2_of_bf(u.z); x[3] = f2_of_bf(u.w);
+}
+__device__ __forceinline__ void unpack4x2h(const uint4 &u, f2 (&x)[4]) {
+  x[0] = f2_of_h(u.x); x[1] = f2_of_h(u.y); x[2] = f2_of_h(u.z); x[3] = f2_of_h(u.w);
+}
+__device__ __forceinline__ uint4 pack4x2(const f2 *x) {
+  return make_uint4(bf_of_f2(x[0]), bf_of_f2(x[1]), bf_of_f2(x[2]), bf_of_f2(x[3]));
+}
+__device__ __forceinline__ uint4 pack4x2h(const f2 *x) {
+  return make_uint4(h_of_f2(x[0]), h_of_f2(x[1]), h_of_f2(x[2]), h_of_f2(x[3]));
+}
+// 32 fp32 values (a TMEM row slice) as 16 pairs, and back
+__device__ __forceinline__ void pairs_of(const float (&v)[32], f2 (&x)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) x[e] = mk2(v[2 * e], v[2 * e + 1]);
+}
+__device__ __forceinline__ void floats_of(const f2 (&x)[16], float (&v)[32]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) split2(x[e], v[2 * e], v[2 * e + 1]);
+}
+
 __device__ __forceinline__ uint4 *tile_at(unsigned char *tile, int row, int chunk) {
   return reinterpret_cast<uint4 *>(tile + umma::sw128_off(row, chunk, ROWS));
 }
@@ -91,34 +163,37 @@ __device__ __forceinline__ void ld_pairs(unsigned char *tile, int row, int qd, u
 }
 
 __device__ __forceinline__ float sumsq_pairs(const uint4 (&r)[4]) {
-  float s = 0.f;
+  f2 s = 0ull;
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
-    float f[8];
-    unpack8(r[u], f);
+    f2 x[4];
+    unpack4x2(r[u], x);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) s = fmaf(f[e], f[e], s);
+    for (int e = 0; e < 4; ++e) s = fma2(x[e], x[e], s);
   }
-  return s;
+  return hsum2(s);
 }
 
 // one pass over this lane's pairs of a row: sums of a_e^2, b_e^2 and a_e b_e
 // (fp32; the raw q . k gives the fp32 diagonal q~_i . k~_i)
 __device__ __forceinline__ void norms_and_dot(const uint4 (&a)[4], const uint4 (&b)[4],
                                               float &saa, float &sbb, float &sab) {
-  saa = sbb = sab = 0.f;
+  f2 aa = 0ull, bb = 0ull, ab = 0ull;
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
-    float x[8], y[8];
-    unpack8(a[u], x);
-    unpack8(b[u], y);
+    f2 x[4], y[4];
+    unpack4x2(a[u], x);
+    unpack4x2(b[u], y);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      saa = fmaf(x[e], x[e], saa);
-      sbb = fmaf(y[e], y[e], sbb);
-      sab = fmaf(x[e], y[e], sab);
+    for (int e = 0; e < 4; ++e) {
+      aa = fma2(x[e], x[e], aa);
+      bb = fma2(y[e], y[e], bb);
+      ab = fma2(x[e], y[e], ab);
     }
   }
+  saa = hsum2(aa);
+  sbb = hsum2(bb);
+  sab = hsum2(ab);
 }
 
 // cos / sin of the RoPE angle of pair u at position p on the special-function
@@ -144,12 +219,13 @@ __device__ __forceinline__ void load_rope_table(unsigned long long *ru, const Mi
   if (tid < kMaxPairs) ru[4 * (tid & 15) + (tid >> 4)] = P.rope_u[tid];
 }
 
-// sigmoid via the hardware tanh: 1 / (1 + e^-z) = 0.5 + 0.5 tanh(z / 2).
-__device__ __forceinline__ float sigmoid_fast(float z) {
+// the hardware tanh, and sigmoid through it: 1 / (1 + e^-z) = 0.5 + 0.5 tanh(z / 2).
+__device__ __forceinline__ float tanh_fast(float x) {
   float t;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * z));
-  return fmaf(0.5f, t, 0.5f);
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(x));
+  return t;
 }
+__device__ __forceinline__ float sigmoid_fast(float z) { return fmaf(0.5f, tanh_fast(0.5f * z), 0.5f); }
 
 // Causal mask of one 32-column block of a score row: v gets columns
 // [32 qd, 32 qd + 32) of row i = 32 sub + lane from TMEM at taddr, keeping
@@ -229,27 +305,51 @@ __device__ __forceinline__ void mask_upper_block(uint32_t taddr, float (&v)[32],
   }
 }
 
+// RoPE of one 8-element chunk pair, two fp32 lanes at a time: lo = x0 c - x1 s,
+// hi = x0 s + x1 c for x0 = a r, x1 = b r (a: first-half elements, b: their
+// partners d/2 further on).  cs / sn / nsn hold cos, sin and -sin of the 8 angles.
+__device__ __forceinline__ void rotate8(const uint4 &a, const uint4 &b, f2 r, const f2 (&cs)[4],
+                                       const f2 (&sn)[4], const f2 (&nsn)[4], f2 (&lo)[4],
+                                       f2 (&hi)[4]) {
+  f2 xa[4], xb[4];
+  unpack4x2(a, xa);
+  unpack4x2(b, xb);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const f2 x0 = mul2(xa[e], r), x1 = mul2(xb[e], r);
+    lo[e] = fma2(x0, cs[e], mul2(x1, nsn[e]));
+    hi[e] = fma2(x0, sn[e], mul2(x1, cs[e]));
+  }
+}
+
+// cos, sin, -sin of this thread's 8 angles of half `hf` at position p, paired.
+__device__ __forceinline__ void rope8(long long p, const unsigned long long *ru, int hf, int qd,
+                                      f2 (&cs)[4], f2 (&sn)[4], f2 (&nsn)[4]) {
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float c0, s0, c1, s1;
+    rope_fast(p, ru[4 * (8 * hf + 2 * e) + qd], c0, s0);
+    rope_fast(p, ru[4 * (8 * hf + 2 * e + 1) + qd], c1, s1);
+    cs[e] = mk2(c0, c1);
+    sn[e] = mk2(s0, s1);
+    nsn[e] = mk2(-s0, -s1);
+  }
+}
+
 // Rotate this thread's 16 pairs of raw row `r` (times `scale`) at position p
 // and store them, as fp16 (half) or bf16, into the same chunks of `tile`.
 // `ru` is the kernel's table from load_rope_table.
 __device__ __forceinline__ void feature_store(const uint4 (&r)[4], float scale, long long p, int qd,
                                               const unsigned long long *ru, unsigned char *tile,
                                               int row, bool half) {
+  const f2 sc = dup2(scale);
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
-    float a[8], bb[8], lo[8], hi[8];
-    unpack8(r[hf], a);
-    unpack8(r[2 + hf], bb);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float c, s;
-      rope_fast(p, ru[4 * (8 * hf + e) + qd], c, s);
-      const float x0 = a[e] * scale, x1 = bb[e] * scale;
-      lo[e] = x0 * c - x1 * s;
-      hi[e] = x0 * s + x1 * c;
-    }
-    *tile_at(tile, row, 2 * qd + hf) = half ? pack8h(lo) : pack8(lo);
-    *tile_at(tile, row, 8 + 2 * qd + hf) = half ? pack8h(hi) : pack8(hi);
+    f2 cs[4], sn[4], nsn[4], lo[4], hi[4];
+    rope8(p, ru, hf, qd, cs, sn, nsn);
+    rotate8(r[hf], r[2 + hf], sc, cs, sn, nsn, lo, hi);
+    *tile_at(tile, row, 2 * qd + hf) = half ? pack4x2h(lo) : pack4x2(lo);
+    *tile_at(tile, row, 8 + 2 * qd + hf) = half ? pack4x2h(hi) : pack4x2(hi);
   }
 }
 
@@ -260,42 +360,22 @@ __device__ __forceinline__ float feature_qk_store(const uint4 (&qr)[4], const ui
                                                  float rq, float rk, long long p, int qd,
                                                  const unsigned long long *ru, unsigned char *Qt,
                                                  unsigned char *Kt, int row) {
-  float dot = 0.f;
+  f2 dot = 0ull;
+  const f2 sq = dup2(rq), sk = dup2(rk);
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
-    float c[8], s[8];
+    f2 cs[4], sn[4], nsn[4], qlo[4], qhi[4], klo[4], khi[4];
+    rope8(p, ru, hf, qd, cs, sn, nsn);
+    rotate8(qr[hf], qr[2 + hf], sq, cs, sn, nsn, qlo, qhi);
+    *tile_at(Qt, row, 2 * qd + hf) = pack4x2h(qlo);
+    *tile_at(Qt, row, 8 + 2 * qd + hf) = pack4x2h(qhi);
+    rotate8(kr[hf], kr[2 + hf], sk, cs, sn, nsn, klo, khi);
+    *tile_at(Kt, row, 2 * qd + hf) = pack4x2h(klo);
+    *tile_at(Kt, row, 8 + 2 * qd + hf) = pack4x2h(khi);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) rope_fast(p, ru[4 * (8 * hf + e) + qd], c[e], s[e]);
-    float qlo[8], qhi[8];
-    {
-      float a[8], bb[8];
-      unpack8(qr[hf], a);
-      unpack8(qr[2 + hf], bb);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float x0 = a[e] * rq, x1 = bb[e] * rq;
-        qlo[e] = x0 * c[e] - x1 * s[e];
-        qhi[e] = x0 * s[e] + x1 * c[e];
-      }
-      *tile_at(Qt, row, 2 * qd + hf) = pack8h(qlo);
-      *tile_at(Qt, row, 8 + 2 * qd + hf) = pack8h(qhi);
-    }
-    {
-      float a[8], bb[8], lo[8], hi[8];
-      unpack8(kr[hf], a);
-      unpack8(kr[2 + hf], bb);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float x0 = a[e] * rk, x1 = bb[e] * rk;
-        lo[e] = x0 * c[e] - x1 * s[e];
-        hi[e] = x0 * s[e] + x1 * c[e];
-        dot = fmaf(qlo[e], lo[e], fmaf(qhi[e], hi[e], dot));
-      }
-      *tile_at(Kt, row, 2 * qd + hf) = pack8h(lo);
-      *tile_at(Kt, row, 8 + 2 * qd + hf) = pack8h(hi);
-    }
+    for (int e = 0; e < 4; ++e) dot = fma2(qlo[e], klo[e], fma2(qhi[e], khi[e], dot));
   }
-  return dot;
+  return hsum2(dot);
 }
 
 __device__ __forceinline__ void sync_tc() {

@@ -196,6 +196,11 @@ struct OutShared {
   unsigned long long ru[kMaxPairs];  // RoPE phase increments (load_rope_table)
   float red_o[4][ROWS];
   float pw[ROWS + 1];
+  // decay of the causal mask read backwards, in four copies shifted by one
+  // element so that every lane's 32 weights start 16-byte aligned:
+  // dm[c][x] = gamma^(127 - x - c) for x + c <= 127, else 0.  Rows are padded
+  // to 264 floats so that the eight lanes of a quarter-warp hit distinct banks.
+  alignas(16) float dm[4][264];
   float qk_diag[2][ROWS];  // fp32 q~_i . k~_i of tiles n (n & 1)
   float smax[NWORK];
   uint64_t bar_mma[2];  // [0]: MMA1 + MMA2 of a tile done, [1]: MMA3 + MMA4 done (commits)
@@ -267,6 +272,10 @@ __global__ void __launch_bounds__(NTO, 1)
     sh.failed = 0;
   }
   if (tid <= ROWS) sh.pw[tid] = exp2f((float)tid * l2g);
+  for (int e = tid; e < 4 * 264; e += NTO) {
+    const int cp = e / 264, x = e % 264;
+    sh.dm[cp][x] = x + cp <= ROWS - 1 ? exp2f((float)(ROWS - 1 - x - cp) * l2g) : 0.f;
+  }
   load_rope_table(sh.ru, P, tid);
   if (warp == 0) umma::tmem_alloc(&sh.tmem_base, 512);
   if (CV < ROWS)  // rows [CV, 128) of V are never written by TMA: clear them once
@@ -461,24 +470,22 @@ __global__ void __launch_bounds__(NTO, 1)
         // [C] Sb = fp16(S 2^-e) with 2^e >= max |S| of the quarter, then S <- gamma^c S
         int e = 0;
         if (m > 0.f) frexpf(m, &e);
-        const float s_fwd = ldexpf(1.f, -e);
+        const f2 s_fwd = dup2(ldexpf(1.f, -e));
         s_inv = ldexpf(1.f, e);
+        f2 x[16];
+        pairs_of(sv, x);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          float t[8];
+          f2 t[4];
 #pragma unroll
-          for (int e2 = 0; e2 < 8; ++e2) t[e2] = sv[8 * u + e2] * s_fwd;
-          *tile_at(SP, i, 4 * qd + u) = pack8h(t);
+          for (int e2 = 0; e2 < 4; ++e2) t[e2] = mul2(x[4 * u + e2], s_fwd);
+          *tile_at(SP, i, 4 * qd + u) = pack4x2h(t);
         }
-        const float carry = sh.pw[c];
-        float lo[16], hi[16];
+        const f2 carry = dup2(sh.pw[c]);
 #pragma unroll
-        for (int e2 = 0; e2 < 16; ++e2) {
-          lo[e2] = sv[e2] * carry;
-          hi[e2] = sv[16 + e2] * carry;
-        }
-        umma::tmem_st16(myS, lo);
-        umma::tmem_st16(myS + 16, hi);
+        for (int e2 = 0; e2 < 16; ++e2) x[e2] = mul2(x[e2], carry);
+        floats_of(x, sv);
+        umma::tmem_st32(myS, sv);
         umma::tmem_wait_st();
         warp_arrive(&sh.bar_sb, lane);
       }
@@ -486,24 +493,33 @@ __global__ void __launch_bounds__(NTO, 1)
       if (drain) {
         float o[32];
         umma::tmem_ld2x16(oprev + lane_base + col, o);
-        float ss = 0.f;
+        f2 ox[16];
+        pairs_of(o, ox);
+        f2 ss = 0ull;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) ss = fmaf(o[e], o[e], ss);
-        sh.red_o[qd][i] = ss;
+        for (int e = 0; e < 16; ++e) ss = fma2(ox[e], ox[e], ss);
+        sh.red_o[qd][i] = hsum2(ss);
         named_sync(5 + sub, 128);
         // gate of tile n - 1 (TMA) -> y, in place; the issuer stores the tile
         wait_or_fail(&sh.bar_g, (n - 1) & 1, failed);
         {
-          const float ro = rsqrtf((sh.red_o[0][i] + sh.red_o[1][i] + sh.red_o[2][i] +
-                                   sh.red_o[3][i]) / (float)D + P.eps);
+          const f2 ro = dup2(rsqrtf((sh.red_o[0][i] + sh.red_o[1][i] + sh.red_o[2][i] +
+                                     sh.red_o[3][i]) / (float)D + P.eps));
+          const f2 half = dup2(0.5f);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             uint4 *p = tile_at(Gs, i, 4 * qd + u);
-            float gf[8], t[8];
-            unpack8(*p, gf);
+            f2 g[4], t[4];
+            unpack4x2(*p, g);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) t[e] = o[8 * u + e] * ro * sigmoid_fast(gf[e]);
-            *p = pack8(t);
+            for (int e = 0; e < 4; ++e) {
+              // sigmoid(z) = 0.5 + 0.5 tanh(z / 2)
+              float za, zb;
+              split2(mul2(g[e], half), za, zb);
+              const f2 sg = fma2(mk2(tanh_fast(za), tanh_fast(zb)), half, half);
+              t[e] = mul2(mul2(ox[4 * u + e], ro), sg);
+            }
+            *p = pack4x2(t);
           }
         }
         warp_arrive(&sh.bar_epi, lane);
@@ -523,47 +539,46 @@ __global__ void __launch_bounds__(NTO, 1)
         {
           float pv[32];
           umma::tmem_ld2x16(myP, pv);
-          // mask: Pm = bf16((Q~ K~^T) (.) D) into SP (Sb is dead once MMA2 is done)
-          const int jlo = (int)col;
-          const int jm = min(i, jlo + 31);
-          float w = (valid && jm >= jlo) ? sh.pw[i - jm] : 0.f;
+          // mask: Pm = bf16((Q~ K~^T) (.) D) into SP (Sb is dead once MMA2 is done),
+          // D_ij = gamma^(i-j) for j <= i, else 0: weights e = 0..31 of this
+          // lane are dm[.][s0 + e] for s0 = 127 - i + 32 qd.  Rows and columns
+          // past the tile are zero already (their q~, k~ are zero).
+          const int s0 = ROWS - 1 - i + (int)col, cp = s0 & 3;
+          const float4 *wt = reinterpret_cast<const float4 *>(&sh.dm[cp][s0 - cp]);
+          f2 x[16];
+          pairs_of(pv, x);
 #pragma unroll
-          for (int e = 31; e >= 0; --e) {
-            if (jlo + e <= i) {
-              pv[e] *= w;
-              w *= gm;
-            } else {
-              pv[e] = 0.f;
-            }
+          for (int u = 0; u < 8; ++u) {
+            const float4 w = wt[u];
+            x[2 * u] = mul2(x[2 * u], mk2(w.x, w.y));
+            x[2 * u + 1] = mul2(x[2 * u + 1], mk2(w.z, w.w));
           }
           // MMA2 of tile n done: Sb is dead and the Q~ S part of O is ready
           wait_or_fail(&sh.bar_mma[0], n & 1, failed);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) *tile_at(SP, i, 4 * qd + u) = pack8(&pv[8 * u]);
+          for (int u = 0; u < 4; ++u) *tile_at(SP, i, 4 * qd + u) = pack4x2(&x[4 * u]);
           // O <- gamma^{i+1} 2^e O  (the Q~ S part, before MMA3 adds Pm V)
           float ov[32];
           umma::tmem_ld2x16(ocur + lane_base + col, ov);
-          const float f = sh.pw[i + 1] * s_inv;
-          float lo[16], hi[16];
+          const f2 f = dup2(sh.pw[i + 1] * s_inv);
+          f2 y2[16];
+          pairs_of(ov, y2);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            lo[e] = ov[e] * f;
-            hi[e] = ov[16 + e] * f;
-          }
-          umma::tmem_st16(ocur + lane_base + col, lo);
-          umma::tmem_st16(ocur + lane_base + col + 16, hi);
+          for (int e = 0; e < 16; ++e) y2[e] = mul2(y2[e], f);
+          floats_of(y2, ov);
+          umma::tmem_st32(ocur + lane_base + col, ov);
         }
         // k~dec = gamma^{c-1-i} k~ as bf16, in place (K~ is dead once MMA1 is done)
         {
-          const float wk = valid ? sh.pw[c - 1 - i] : 0.f;
+          const f2 wk = dup2(valid ? sh.pw[c - 1 - i] : 0.f);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             uint4 *p = tile_at(Kt, i, 4 * qd + u);
-            float f[8];
-            unpack8h(*p, f);
+            f2 f[4];
+            unpack4x2h(*p, f);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] *= wk;
-            *p = pack8(f);
+            for (int e = 0; e < 4; ++e) f[e] = mul2(f[e], wk);
+            *p = pack4x2(f);
           }
         }
         umma::tmem_wait_st();
