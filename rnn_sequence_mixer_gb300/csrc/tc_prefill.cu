@@ -212,7 +212,6 @@ struct OutShared {
   uint64_t bar_feat;    // workers: q~, k~ of the tile written (one arrive per warp)
   uint64_t bar_sb;      // workers: Sb written and S rescaled
   uint64_t bar_pm;      // workers: Pm, scaled O and k~dec written
-  uint64_t bar_diag;    // diagonal warp: fp32 diagonal patched into Pm
   uint64_t bar_epi;     // workers: y of the previous tile written over its gate tile
   uint32_t tmem_base;
   uint32_t failed;
@@ -266,7 +265,6 @@ __global__ void __launch_bounds__(NTO, 1)
     umma::mbar_init(&sh.bar_feat, NWORK);
     umma::mbar_init(&sh.bar_sb, NWORK);
     umma::mbar_init(&sh.bar_pm, NWORK);
-    umma::mbar_init(&sh.bar_diag, 1);
     umma::mbar_init(&sh.bar_epi, NWORK);
     umma::mbar_fence_init();
     sh.failed = 0;
@@ -326,6 +324,13 @@ __global__ void __launch_bounds__(NTO, 1)
                          id_qs, kk > 0);
           umma::commit(&sh.bar_mma[0]);
         }
+        // MMA2 done: Q is free for the next q (as early as possible: the
+        // workers need it right after this tile's mask)
+        wait_or_fail(&sh.bar_mma[0], n & 1, failed);
+        if (!failed && n + 1 < ntile) {
+          umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
+          tma_tile(Qs, &tmq, b, h, c0 + CV, &sh.bar_q);
+        }
         // y of tile n - 1 is in G: store it (the gate of tile n follows once
         // the store has read G, after MMA3 / MMA4 are issued)
         if (n >= 1) {
@@ -335,13 +340,7 @@ __global__ void __launch_bounds__(NTO, 1)
             umma::bulk_commit();
           }
         }
-        // MMA2 done: Q is free for the next q
-        wait_or_fail(&sh.bar_mma[0], n & 1, failed);
-        if (!failed && n + 1 < ntile) {
-          umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
-          tma_tile(Qs, &tmq, b, h, c0 + CV, &sh.bar_q);
-        }
-        wait_or_fail(&sh.bar_diag, n & 1, failed);  // follows bar_pm
+        wait_or_fail(&sh.bar_pm, n & 1, failed);
         wait_or_fail(&sh.bar_v, n & 1, failed);
         if (!failed) {
 #pragma unroll
@@ -379,22 +378,6 @@ __global__ void __launch_bounds__(NTO, 1)
         umma::bulk_commit();
       }
       umma::bulk_wait_all();
-    } else if (warp == NWORK + 1) {
-      // the diagonal of Pm from fp32 features.  Where q~_i . k~_i nearly cancels
-      // (a row whose output is almost only its own term: t = 0, or gamma near 0)
-      // the fp16 operands of MMA1 lose it; its weight is gamma^0 = 1.
-      for (int n = 0; n < ntile; ++n) {
-        wait_or_fail(&sh.bar_pm, n & 1, failed);
-        if (!failed) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int r = 32 * u + lane;
-            *(reinterpret_cast<__nv_bfloat16 *>(tile_at(SP, r, r >> 3)) + (r & 7)) =
-                __float2bfloat16_rn(sh.qk_diag[n & 1][r]);
-          }
-        }
-        warp_arrive(&sh.bar_diag, lane);
-      }
     }
   } else {
     // ---------------------------------------------------------------- worker warps
@@ -447,7 +430,7 @@ __global__ void __launch_bounds__(NTO, 1)
         const float rq = rsqrtf(sq / (float)D + P.eps);
         const float rk = rsqrtf(sk / (float)D + P.eps) * P.kscale;
         // q~_i . k~_i in fp32 (one rotation acts on both, so RoPE drops out);
-        // zero on rows past the tile.  The diagonal warp reads it after bar_pm.
+        // zero on rows past the tile.  Read in [F] by the diagonal warps.
         if (fu == 0) sh.qk_diag[buf][fr] = qk * rq * rk;
         feature_qk_store(qr, kr, rq, rk, P.pos_offset + c0 + fr, fu, sh.ru, Qt, Kt, fr);
         warp_arrive(&sh.bar_feat, lane);
@@ -493,6 +476,13 @@ __global__ void __launch_bounds__(NTO, 1)
       if (drain) {
         float o[32];
         umma::tmem_ld2x16(oprev + lane_base + col, o);
+        if (P.o && i < prev_c) {
+          const size_t row = (((size_t)b * P.T + prev_c0 + i) * P.H + h) * D + col;
+          float4 *o4 = reinterpret_cast<float4 *>(P.o + row);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            o4[u] = make_float4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+        }
         f2 ox[16];
         pairs_of(o, ox);
         f2 ss = 0ull;
@@ -523,15 +513,6 @@ __global__ void __launch_bounds__(NTO, 1)
           }
         }
         warp_arrive(&sh.bar_epi, lane);
-        if (i < prev_c) {
-          const size_t row = (((size_t)b * P.T + prev_c0 + i) * P.H + h) * D + col;
-          if (P.o) {
-            float4 *o4 = reinterpret_cast<float4 *>(P.o + row);
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              o4[u] = make_float4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
-          }
-        }
       }
       if (have) {
         // [F] MMA1 of tile n done: mask P
@@ -553,10 +534,31 @@ __global__ void __launch_bounds__(NTO, 1)
             x[2 * u] = mul2(x[2 * u], mk2(w.x, w.y));
             x[2 * u + 1] = mul2(x[2 * u + 1], mk2(w.z, w.w));
           }
+          // k~dec = gamma^{c-1-i} k~ as bf16, in place (K~ is dead once MMA1 is done)
+          {
+            const f2 wk = dup2(valid ? sh.pw[c - 1 - i] : 0.f);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint4 *p = tile_at(Kt, i, 4 * qd + u);
+              f2 f[4];
+              unpack4x2h(*p, f);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) f[e] = mul2(f[e], wk);
+              *p = pack4x2(f);
+            }
+          }
           // MMA2 of tile n done: Sb is dead and the Q~ S part of O is ready
           wait_or_fail(&sh.bar_mma[0], n & 1, failed);
 #pragma unroll
           for (int u = 0; u < 4; ++u) *tile_at(SP, i, 4 * qd + u) = pack4x2(&x[4 * u]);
+          // the diagonal of Pm from fp32 features: where q~_i . k~_i nearly
+          // cancels (a row whose output is almost only its own term: t = 0, or
+          // gamma near 0) the fp16 operands of MMA1 lose it; its weight is
+          // gamma^0 = 1.  Rows 32 qd .. 32 qd + 31 of qk_diag were written by
+          // warps 4 qd .. 4 qd + 3, which met this warp at [B]'s barrier.
+          if (qd == sub)
+            *(reinterpret_cast<__nv_bfloat16 *>(tile_at(SP, i, i >> 3)) + (i & 7)) =
+                __float2bfloat16_rn(sh.qk_diag[buf][i]);
           // O <- gamma^{i+1} 2^e O  (the Q~ S part, before MMA3 adds Pm V)
           float ov[32];
           umma::tmem_ld2x16(ocur + lane_base + col, ov);
@@ -567,19 +569,6 @@ __global__ void __launch_bounds__(NTO, 1)
           for (int e = 0; e < 16; ++e) y2[e] = mul2(y2[e], f);
           floats_of(y2, ov);
           umma::tmem_st32(ocur + lane_base + col, ov);
-        }
-        // k~dec = gamma^{c-1-i} k~ as bf16, in place (K~ is dead once MMA1 is done)
-        {
-          const f2 wk = dup2(valid ? sh.pw[c - 1 - i] : 0.f);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint4 *p = tile_at(Kt, i, 4 * qd + u);
-            f2 f[4];
-            unpack4x2h(*p, f);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) f[e] = mul2(f[e], wk);
-            *p = pack4x2(f);
-          }
         }
         umma::tmem_wait_st();
         warp_arrive(&sh.bar_pm, lane);
