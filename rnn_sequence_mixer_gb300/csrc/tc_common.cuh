@@ -400,6 +400,12 @@ __device__ __forceinline__ void tma_tile(unsigned char *dst, const CUtensorMap *
   umma::tma_load_4d(dst + HALF_TILE, map, 64, h, c0, b, bar);
 }
 
+// L2 prefetch of the same tile (no shared-memory destination, no barrier).
+__device__ __forceinline__ void tma_prefetch_tile(const CUtensorMap *map, int b, int h, int c0) {
+  umma::tma_prefetch_4d(map, 0, h, c0, b);
+  umma::tma_prefetch_4d(map, 64, h, c0, b);
+}
+
 // TMA store of a [rows, 128] bf16 operand-layout tile to token rows
 // [c0, c0 + rows) of (b, h): two boxes of 64 columns.  Rows past T are not
 // written.

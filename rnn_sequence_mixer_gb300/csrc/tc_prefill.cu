@@ -331,6 +331,9 @@ __global__ void __launch_bounds__(NTO, 1)
           umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
           tma_tile(Qs, &tmq, b, h, c0 + CV, &sh.bar_q);
         }
+        // the q tile after that into L2, so that its copy (issued one tile
+        // from now, on the workers' critical path) does not wait on HBM
+        if (!failed && n + 2 < ntile) tma_prefetch_tile(&tmq, b, h, c0 + 2 * CV);
         // y of tile n - 1 is in G: store it (the gate of tile n follows once
         // the store has read G, after MMA3 / MMA4 are issued)
         if (n >= 1) {
@@ -584,7 +587,9 @@ __global__ void __launch_bounds__(NTO, 1)
 }
 
 constexpr size_t kStateSmem = 2 * kStages * TILE + sizeof(StateShared) + 1024;
+static_assert(kStateSmem <= 232448, "local-state pass exceeds 227 KiB of shared memory per CTA");
 constexpr size_t kOutputSmem = 6 * TILE + sizeof(OutShared) + 1024;
+static_assert(kOutputSmem <= 232448, "output pass exceeds 227 KiB of shared memory per CTA");
 
 }  // namespace
 }  // namespace tc

@@ -252,6 +252,14 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, int x, 
       : "memory");
 }
 
+// Prefetch of the same box into L2 (x never negative, as for the loads).
+__device__ __forceinline__ void tma_prefetch_4d(const void *tmap, int x, int y, int z, int w) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
+
 // 4-D tiled TMA store of a shared-memory box to global coordinates (x, y, z, w)
 // (never negative).  Rows of the box past the tensor's extent are not written.
 // The writing threads must have made their shared-memory writes visible to the
