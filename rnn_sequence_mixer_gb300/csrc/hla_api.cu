@@ -2,6 +2,7 @@
 // the segment plan, workspace carving and kernel dispatch.  Nothing here
 // allocates, frees or synchronizes.
 #include <math.h>
+#include <algorithm>
 #include <string.h>
 
 #include <new>
@@ -12,10 +13,14 @@ namespace hla {
 
 namespace {
 
-// Target number of (b, h, segment) work units of the prefill passes: four per
-// SM of a 152-SM GB300 (one resident CTA per SM in the tensor-core passes), so
-// a single long sequence with 16 heads still fills every SM in equal waves.
-constexpr int kTargetUnits = 4 * 152;
+// The segment plan sizes its grid for a GB300: 152 SMs, one resident CTA per
+// SM in the tensor-core passes (each holds ~200 KB of shared memory and all
+// 512 TMEM columns).
+constexpr int kSMs = 152;
+// Fixed cost of one segment, in tiles: the CTA's set-up, its entering state
+// read from the workspace, the pipeline filling and draining, and its step in
+// the fp32 scan.
+constexpr int kSegOverhead = 2;
 
 }  // namespace
 
@@ -124,12 +129,25 @@ Plan make_plan(const hla_shape &s) {
     p.seg_len = s.chunk;
     return p;
   }
-  int nseg = (int)((kTargetUnits + units - 1) / units);
-  if (nseg < 1) nseg = 1;
-  if (nseg > p.nchunk) nseg = p.nchunk;
-  int chunks_per_seg = ceil_div(p.nchunk, nseg);
-  p.nseg = ceil_div(p.nchunk, chunks_per_seg);
-  p.seg_len = chunks_per_seg * s.chunk;
+  // Every segment of every (b, h) is one CTA, and CTAs run in waves of kSMs.
+  // Pick the segment count that minimises the time of the slowest SM,
+  // waves x (tiles per segment + kSegOverhead); ties go to fewer segments.
+  // Segment counts past 16 waves of CTAs only add overhead.
+  const long long max_seg = std::min<long long>(p.nchunk, std::max<long long>(1, (16LL * kSMs + units - 1) / units));
+  long long best_cost = -1;
+  int best_cps = p.nchunk;
+  for (long long nseg = 1; nseg <= max_seg; ++nseg) {
+    const int cps = ceil_div(p.nchunk, nseg);
+    if (ceil_div(p.nchunk, cps) != nseg) continue;  // same split as a smaller count
+    const long long waves = (units * nseg + kSMs - 1) / kSMs;
+    const long long cost = waves * (cps + kSegOverhead);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_cps = cps;
+    }
+  }
+  p.nseg = ceil_div(p.nchunk, best_cps);
+  p.seg_len = best_cps * s.chunk;
   return p;
 }
 

@@ -41,7 +41,8 @@ def noalloc(inp, gamma, state_in, *, chunk, base, eps=1e-6):
 
 @pytest.mark.parametrize("B,T,H,d,dtype,chunk,with_state", [
     (1, 4000, 16, 128, torch.bfloat16, 64, False),
-    (3, 300, 100, 128, torch.bfloat16, 64, True),   # 300 heads: the scratch limit caps the segments
+    (3, 300, 100, 128, torch.bfloat16, 64, True),   # 300 heads of d = 128: one segment each
+    (1, 3000, 120, 128, torch.bfloat16, 64, True),  # the plan's 5 segments exceed the scratch: capped to 4
     (2, 517, 4, 64, torch.float32, 128, True),
 ])
 def test_noalloc_matches_prefill_two_calls_in_a_row(B, T, H, d, dtype, chunk, with_state):
