@@ -167,320 +167,544 @@ __device__ __forceinline__ void feature_grad_row(const float (&glo)[16], const f
 
 // ------------------------------------------------------------------ dq pass
 
-__global__ void __launch_bounds__(NT, 1)
+struct DqShared {
+  unsigned long long ru[kMaxPairs];  // RoPE phase increments (load_rope_table)
+  float red_do[2][4][ROWS];  // [W4] quarter parts of sum o^2 and sum dn.o of each row
+  float red_dq[2][4][ROWS];  // [W6] quarter parts of sum q^2 and sum g.q of each row
+  float vd_part[4][ROWS];    // [W4] -> [W5] quarter parts of the fp32 v_i . do_i
+  float qk_diag[2][ROWS];    // [W1] -> [W3] fp32 q~_i . k~_i of tile n (n & 1)
+  float pw[ROWS + 1];
+  alignas(16) float dm[4][DM_STRIDE];  // causal-mask decay table (fill_mask_table)
+  float smax[NWORK];
+  uint64_t bar_q;       // TMA: raw q of tile n into Q
+  uint64_t bar_k[2];    // TMA: raw k into K buffer 0 / 1
+  uint64_t bar_v;       // TMA: v into V
+  uint64_t bar_g;       // TMA: gate of tile n into Q
+  uint64_t bar_qr;      // TMA: raw q of tile n into its (freed) K buffer, for [W6]
+  uint64_t bar_p;       // MMA1 done (P)
+  uint64_t bar_o;       // MMA2 done (O = Q~ Sb)
+  uint64_t bar_m3;      // MMA3 done (O complete)
+  uint64_t bar_m56;     // MMA5 + MMA6 done (dP, I)
+  uint64_t bar_m74;     // MMA7 + MMA4 done (dQ~ complete, S carried)
+  uint64_t bar_rd;      // issuer: the dgate / dO stores have read PM / Q
+  uint64_t bar_feat, bar_sb, bar_pm, bar_do, bar_w5, bar_w6;  // workers, one arrive per warp
+  uint32_t tmem_base;
+  uint32_t failed;
+};
+
+// sigmoid of two lanes: 1 / (1 + e^-z) = 0.5 + 0.5 tanh(z / 2)
+__device__ __forceinline__ f2 sigmoid2(f2 z) {
+  const f2 half = dup2(0.5f);
+  float a, b;
+  split2(mul2(z, half), a, b);
+  return fma2(mk2(tanh_fast(a), tanh_fast(b)), half, half);
+}
+
+// dq pass, warp-specialized: per tile n the forward is recomputed (O), the
+// output norm and gate are differentiated (dgate, dO) and dQ~ is formed, while
+// the state S is carried through TMEM as in the forward output pass.
+//   MMA1  P  = Q~ K~^T               (fp16)      into tP
+//   MMA2  O  = Q~ Sb                 (fp16)      into tA[n & 1]
+//   MMA3  O += Pm V                  (bf16)
+//   MMA5  dP = dO V^T                (bf16)      into tP
+//   MMA6  I  = dO S^T                (bf16)      into tA[n & 1] (O is dead)
+//   MMA7  dQ~ = gamma^{i+1} I + dPm K~           (I scaled in TMEM first)
+//   MMA4  S  += K~^T Vdec,  Vdec_j = gamma^{c-1-j} v_j  (the decay rides on V,
+//         so K~ serves MMA7 and MMA4 unchanged)
+// Worker warps (0..15) run, per loop step n:
+//   [W1] q~, k~ of tile n (fp16, in place)       [W2] Sb = fp16(S 2^-e), S <- gamma^c S
+//   [W3] Pm, O <- gamma^{i+1} 2^e O, K~ -> bf16, Sb -> bf16 S
+//   [W4] dgate -> PM, dO -> Q (over the gate), fp32 v_i . do_i
+//   [W6] dq of tile n - 1 (RoPE^T, RMSNorm backward) in its K buffer, over its raw q
+//   [W5] dPm -> PM (fp32 v_i . do_i on the diagonal), I <- gamma^{i+1} I, V -> Vdec
+// so the dq epilogue of tile n - 1 fills the wait on MMA5 / MMA6 of tile n.
+// The issuer warp (16) waits for each hand-off, issues the MMAs and moves every
+// tile by TMA: q, k (double-buffered), v, the gate (into Q once MMA2 has read
+// it), raw q again for [W6] (into the K buffer that MMA7 / MMA4 freed), and
+// the stores of dgate, dO and dq.  dy is the one operand read by plain loads
+// (tmdy only prefetches it into L2 a tile ahead).
+__global__ void __launch_bounds__(NTO, 1)
     tc_bwd_dq_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmq,
                      const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                      const __grid_constant__ CUtensorMap tmg, const __grid_constant__ CUtensorMap tmo,
-                     const __grid_constant__ CUtensorMap tmdg, const __grid_constant__ CUtensorMap tmdq) {
+                     const __grid_constant__ CUtensorMap tmdg, const __grid_constant__ CUtensorMap tmdq,
+                     const __grid_constant__ CUtensorMap tmdy) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  // Q: raw q -> q~ (fp16); then gate (TMA) -> dO (bf16, in place; TMA-stored).
-  // K pair j: raw k -> k~ (fp16) -> k~ (bf16) -> k~dec.
-  // SB: Sb (fp16, scaled) -> S (bf16); then dq (TMA-stored).
-  // PM: P (.) D; then dgate (TMA-stored); then dP (.) D.
-  unsigned char *Qt = base, *Vt = base + 3 * TILE, *SB = base + 4 * TILE, *PM = base + 5 * TILE;
-  BwdShared &sh = *reinterpret_cast<BwdShared *>(base + 6 * TILE);
-  uint64_t *bar_q = &sh.bar_tma[0], *bar_k = &sh.bar_tma[1], *bar_v = &sh.bar_tma[3],
-           *bar_g = &sh.bar_tma[4];
+  // Q:  raw q -> q~ (fp16) -> gate -> dO (bf16)                 -> next raw q
+  // K j: raw k -> k~ (fp16) -> k~ (bf16) -> raw q -> dq (bf16)  -> k two tiles on
+  // V:  v -> Vdec;  SB: Sb (fp16, scaled) -> S (bf16);  PM: Pm -> dgate -> dPm
+  unsigned char *Qs = base, *Vs = base + 3 * TILE, *SB = base + 4 * TILE, *PM = base + 5 * TILE;
+  DqShared &sh = *reinterpret_cast<DqShared *>(base + 6 * TILE);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int sub = warp & 3, qd = warp >> 2, i = 32 * sub + lane;
   const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int t0 = g * P.seg_len, t1 = min(P.T, t0 + P.seg_len);
   const int CV = P.chunk;
   const int ntile = ceil_div(t1 - t0, CV);
-  const float gm = P.gamma[h];
-  const float l2g = log2f(gm);
+  const float l2g = log2f(P.gamma[h]);
   const uint32_t tile_bytes = (uint32_t)CV * D * 2;
 
   if (tid == 0) {
-    for (int j = 0; j < 5; ++j) umma::mbar_init(&sh.bar_tma[j], 1);
-    for (int j = 0; j < 6; ++j) umma::mbar_init(&sh.bar_mma[j], 1);
+    uint64_t *bars[] = {&sh.bar_q, &sh.bar_k[0], &sh.bar_k[1], &sh.bar_v, &sh.bar_g, &sh.bar_qr,
+                        &sh.bar_p, &sh.bar_o, &sh.bar_m3, &sh.bar_m56, &sh.bar_m74, &sh.bar_rd};
+    for (uint64_t *bar : bars) umma::mbar_init(bar, 1);
+    uint64_t *wbars[] = {&sh.bar_feat, &sh.bar_sb, &sh.bar_pm, &sh.bar_do, &sh.bar_w5, &sh.bar_w6};
+    for (uint64_t *bar : wbars) umma::mbar_init(bar, NWORK);
     umma::mbar_fence_init();
+    sh.failed = 0;
   }
   if (tid <= ROWS) sh.pw[tid] = exp2f((float)tid * l2g);
+  fill_mask_table(sh.dm, l2g, tid, NTO);
   load_rope_table(sh.ru, P, tid);
   if (warp == 0) umma::tmem_alloc(&sh.tmem_base, 512);
   if (CV < ROWS)  // rows [CV, 128) of V are never written by TMA: clear them once
-    for (int e = tid; e < (ROWS - CV) * 16; e += NT)
-      *tile_at(Vt, CV + e / 16, e % 16) = make_uint4(0, 0, 0, 0);
+    for (int e = tid; e < (ROWS - CV) * 16; e += NTO)
+      *tile_at(Vs, CV + e / 16, e % 16) = make_uint4(0, 0, 0, 0);
   sync_tc();
   const uint32_t tm = sh.tmem_base;
-  const uint32_t lb = (uint32_t)(32 * sub) << 16, col = 32 * qd;
-  const uint32_t tP = tm + lb, tO = tm + 128 + lb, tI = tm + 256 + lb, tS = tm + 384 + lb;
-  {  // entering state of the segment -> TMEM
-    const float *sin_ = P.seg + (((size_t)b * P.H + h) * P.nseg + g) * (size_t)D * D;
-    const float4 *s4 = reinterpret_cast<const float4 *>(sin_ + (size_t)i * D + col);
-    float v[32];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float4 x = s4[u];
-      v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
-    }
-    umma::tmem_st32(tS + col, v);
-    umma::tmem_wait_st();
-  }
-  if (tid == 0) {
-    umma::mbar_expect_tx(bar_q, tile_bytes);
-    tma_tile(Qt, &tmq, b, h, t0, bar_q);
-    for (int n = 0; n < 2 && n < ntile; ++n) {
-      umma::mbar_expect_tx(&bar_k[n], tile_bytes);
-      tma_tile(base + (1 + n) * TILE, &tmk, b, h, t0 + n * CV, &bar_k[n]);
-    }
-    umma::mbar_expect_tx(bar_v, tile_bytes);
-    tma_tile(Vt, &tmv, b, h, t0, bar_v);
-  }
-  const uint32_t id_qk16 = umma::idesc_bf16(128, 128, false, false, true);
-  const uint32_t id_qs16 = umma::idesc_bf16(128, 128, false, true, true);
-  const uint32_t id_kmn = umma::idesc_bf16(128, 128, false, true);
-  const uint32_t id_kk = umma::idesc_bf16(128, 128, false, false);
-  const uint32_t id_mnmn = umma::idesc_bf16(128, 128, true, true);
-  const uint32_t aQ = umma::smem_u32(Qt), aV = umma::smem_u32(Vt), aSB = umma::smem_u32(SB),
-                 aPM = umma::smem_u32(PM);
-
+  const uint32_t tP = tm, tS = tm + 384;
   bool failed = false;
-  for (int n = 0; n < ntile; ++n) {
-    const int buf = n & 1;
-    const uint32_t ph = n & 1;
-    unsigned char *Kt = base + (1 + buf) * TILE;
-    const uint32_t aK = aQ + (1 + buf) * TILE;
-    const int c0 = t0 + n * CV, c = min(CV, t1 - c0);
-    const bool valid = i < c;
-    const long long pos = P.pos_offset + c0 + i;
-    if (tid == 0) umma::bulk_wait_read();  // the previous dq store has left SB
 
-    // [1] q~, k~ (fp16, in place); Sb = fp16(S 2^-e) per column quarter; S <- gamma^c S
-    BWD_WAIT(bar_q, ph);
-    BWD_WAIT(&bar_k[buf], (n >> 1) & 1);
-    float rq, s_inv;
-    {
-      uint4 qr[4], kr[4];
-      ld_pairs(Qt, i, qd, qr);
-      ld_pairs(Kt, i, qd, kr);
-      if (!valid) qr[0] = qr[1] = qr[2] = qr[3] = kr[0] = kr[1] = kr[2] = kr[3] = make_uint4(0, 0, 0, 0);
-      sh.red[qd][i] = sumsq_pairs(qr);
-      sh.red2[qd][i] = sumsq_pairs(kr);
-      float sv[32];
-      umma::tmem_ld2x16(tS + col, sv);
-      float m = 0.f;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) m = fmaxf(m, fabsf(sv[e]));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) sh.smax[warp] = m;
-      __syncthreads();
-      rq = rsqrtf((sh.red[0][i] + sh.red[1][i] + sh.red[2][i] + sh.red[3][i]) / (float)D + P.eps);
-      const float rk = rsqrtf((sh.red2[0][i] + sh.red2[1][i] + sh.red2[2][i] + sh.red2[3][i]) /
-                                  (float)D + P.eps) * P.kscale;
-      sh.qk_diag[qd][i] = feature_qk_store(qr, kr, rq, rk, pos, qd, sh.ru, Qt, Kt, i);
-      m = fmaxf(fmaxf(sh.smax[4 * qd], sh.smax[4 * qd + 1]), fmaxf(sh.smax[4 * qd + 2], sh.smax[4 * qd + 3]));
-      int e2 = 0;
-      if (m > 0.f) frexpf(m, &e2);
-      const float s_fwd = ldexpf(1.f, -e2);
-      s_inv = ldexpf(1.f, e2);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        float t[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) t[e] = sv[8 * u + e] * s_fwd;
-        *tile_at(SB, i, 4 * qd + u) = pack8h(t);
+  if (warp >= NWORK) {
+    // ---------------------------------------------------------------- issuer warpgroup
+    if (warp == NWORK && lane == 0) {
+      const uint32_t id_qk = umma::idesc_bf16(128, 128, false, false, true);  // fp16 Q~ K~^T
+      const uint32_t id_qs = umma::idesc_bf16(128, 128, false, true, true);   // fp16 Q~ Sb
+      const uint32_t id_kmn = umma::idesc_bf16(128, 128, false, true);        // Pm V, dPm K~
+      const uint32_t id_kk = umma::idesc_bf16(128, 128, false, false);        // dO V^T, dO S^T
+      const uint32_t id_mnmn = umma::idesc_bf16(128, 128, true, true);        // K~^T Vdec
+      const uint32_t aq = umma::smem_u32(Qs), av = umma::smem_u32(Vs), asb = umma::smem_u32(SB),
+                     apm = umma::smem_u32(PM);
+      umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
+      tma_tile(Qs, &tmq, b, h, t0, &sh.bar_q);
+      for (int n = 0; n < 2 && n < ntile; ++n) {
+        umma::mbar_expect_tx(&sh.bar_k[n], tile_bytes);
+        tma_tile(base + (1 + n) * TILE, &tmk, b, h, t0 + n * CV, &sh.bar_k[n]);
       }
-      const float carry = sh.pw[c];
+      umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
+      tma_tile(Vs, &tmv, b, h, t0, &sh.bar_v);
+      tma_prefetch_tile(&tmg, b, h, t0);
+      tma_prefetch_tile(&tmdy, b, h, t0);
+      for (int n = 0; n < ntile; ++n) {
+        const int buf = n & 1;
+        const uint32_t ph = n & 1;
+        const int c0 = t0 + n * CV;
+        unsigned char *Kt = base + (1 + buf) * TILE;
+        const uint32_t ak = umma::smem_u32(Kt);
+        const uint32_t ta = tm + 128 + 128 * buf;
+        // MMA1 once q~, k~ are written; MMA2 once Sb is
+        wait_or_fail(&sh.bar_feat, ph, failed);
+        if (!failed) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) sv[e] *= carry;
-      umma::tmem_st32(tS + col, sv);
+          for (int kk = 0; kk < 8; ++kk)
+            umma::mma_ss(tP, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(ak, kk, ROWS), id_qk, kk > 0);
+          umma::commit(&sh.bar_p);
+        }
+        wait_or_fail(&sh.bar_sb, ph, failed);
+        if (!failed) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma::mma_ss(ta, umma::desc_kmajor(aq, kk, ROWS), umma::desc_mnmajor(asb, kk, ROWS), id_qs, kk > 0);
+          umma::commit(&sh.bar_o);
+        }
+        // MMA2 done: Q takes this tile's gate
+        wait_or_fail(&sh.bar_o, ph, failed);
+        if (!failed) {
+          umma::mbar_expect_tx(&sh.bar_g, tile_bytes);
+          tma_tile(Qs, &tmg, b, h, c0, &sh.bar_g);
+          if (n + 1 < ntile) {  // next tile's operands into L2 ahead of their copies
+            tma_prefetch_tile(&tmq, b, h, c0 + CV);
+            tma_prefetch_tile(&tmk, b, h, c0 + CV);
+            tma_prefetch_tile(&tmv, b, h, c0 + CV);
+            tma_prefetch_tile(&tmg, b, h, c0 + CV);
+            tma_prefetch_tile(&tmdy, b, h, c0 + CV);
+          }
+        }
+        // MMA3 once Pm, the scaled O and V are in place
+        wait_or_fail(&sh.bar_pm, ph, failed);
+        wait_or_fail(&sh.bar_v, ph, failed);
+        if (!failed) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma::mma_ss(ta, umma::desc_kmajor(apm, kk, ROWS), umma::desc_mnmajor(av, kk, ROWS), id_kmn, 1u);
+          umma::commit(&sh.bar_m3);
+        }
+        // dgate (PM) and dO (Q) out; MMA5, MMA6 from dO
+        wait_or_fail(&sh.bar_do, ph, failed);
+        if (!failed) {
+          tma_store_tile(&tmdg, PM, b, h, c0);
+          tma_store_tile(&tmo, Qs, b, h, c0);
+          umma::bulk_commit();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma::mma_ss(tP, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(av, kk, ROWS), id_kk, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma::mma_ss(ta, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(asb, kk, ROWS), id_kk, kk > 0);
+          umma::commit(&sh.bar_m56);
+          umma::bulk_wait_read();
+        }
+        umma::mbar_arrive(&sh.bar_rd);  // PM may take dPm (also on failure: nobody may wait forever)
+        // MMA5 / MMA6 done and dO stored: Q takes the next q
+        wait_or_fail(&sh.bar_m56, ph, failed);
+        if (!failed && n + 1 < ntile) {
+          umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
+          tma_tile(Qs, &tmq, b, h, c0 + CV, &sh.bar_q);
+        }
+        // dq of tile n - 1 is in its K buffer: store it, then that buffer takes k of tile n + 1
+        if (n >= 1) {
+          wait_or_fail(&sh.bar_w6, (n - 1) & 1, failed);
+          unsigned char *Kp = base + (2 - buf) * TILE;
+          if (!failed) {
+            tma_store_tile(&tmdq, Kp, b, h, c0 - CV);
+            umma::bulk_commit();
+            if (n + 1 < ntile) {
+              umma::bulk_wait_read();
+              umma::mbar_expect_tx(&sh.bar_k[buf ^ 1], tile_bytes);
+              tma_tile(Kp, &tmk, b, h, c0 + CV, &sh.bar_k[buf ^ 1]);
+            }
+          }
+        }
+        // MMA7 and MMA4 once dPm, the scaled I and Vdec are in place
+        wait_or_fail(&sh.bar_w5, ph, failed);
+        if (!failed) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma::mma_ss(ta, umma::desc_kmajor(apm, kk, ROWS), umma::desc_mnmajor(ak, kk, ROWS), id_kmn, 1u);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma::mma_ss(tS, umma::desc_mnmajor(ak, kk, ROWS), umma::desc_mnmajor(av, kk, ROWS), id_mnmn, 1u);
+          umma::commit(&sh.bar_m74);
+        }
+        // both done: V takes the next v, this K buffer takes raw q of tile n for [W6]
+        wait_or_fail(&sh.bar_m74, ph, failed);
+        if (!failed) {
+          if (n + 1 < ntile) {
+            umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
+            tma_tile(Vs, &tmv, b, h, c0 + CV, &sh.bar_v);
+          }
+          umma::mbar_expect_tx(&sh.bar_qr, tile_bytes);
+          tma_tile(Kt, &tmq, b, h, c0, &sh.bar_qr);
+        }
+      }
+      // dq of the last tile
+      wait_or_fail(&sh.bar_w6, (ntile - 1) & 1, failed);
+      if (!failed) {
+        tma_store_tile(&tmdq, base + (1 + ((ntile - 1) & 1)) * TILE, b, h, t0 + (ntile - 1) * CV);
+        umma::bulk_commit();
+      }
+      umma::bulk_wait_all();
+    }
+  } else {
+    // ---------------------------------------------------------------- worker warps
+    const int sub = warp & 3, qd = warp >> 2, i = 32 * sub + lane;  // TMEM phases
+    const int fr = 8 * warp + (lane >> 2), fu = lane & 3;           // feature map: row, quarter
+    const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
+    const uint32_t col = 32 * qd;
+    const uint32_t myS = tS + lane_base + col, myP = tP + lane_base + col;
+    {  // entering state of the segment -> TMEM (fp32)
+      const float *sin_ = P.seg + (((size_t)b * P.H + h) * P.nseg + g) * (size_t)D * D;
+      const float4 *s4 = reinterpret_cast<const float4 *>(sin_ + (size_t)i * D + col);
+      float v[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float4 x = s4[u];
+        v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
+      }
+      umma::tmem_st32(myS, v);
       umma::tmem_wait_st();
     }
-    umma::fence_async_smem();
-    sync_tc();
-    if (tid == 0) {
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // MMA1: P = Q~ K~^T
-        umma::mma_ss(tm, umma::desc_kmajor(aQ, kk, ROWS), umma::desc_kmajor(aK, kk, ROWS), id_qk16, kk > 0);
-      umma::commit(&sh.bar_mma[0]);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // MMA2: O = Q~ Sb
-        umma::mma_ss(tm + 128, umma::desc_kmajor(aQ, kk, ROWS), umma::desc_mnmajor(aSB, kk, ROWS), id_qs16,
-                     kk > 0);
-      umma::commit(&sh.bar_mma[1]);
-    }
-
-    // [2] Pm = bf16(P (.) D); k~ -> bf16; O <- gamma^{i+1} 2^e O; Sb -> S (bf16)
-    BWD_WAIT(&sh.bar_mma[0], ph);
-    {
-      float pv[32];
-      // the diagonal q~_i . k~_i from fp32 features: where it nearly cancels,
-      // o_i and so 1 / RMS(o_i) hinge on it (fp16 operands lose it)
-      mask_lower_block(tP + col, pv, i, sub, qd, valid, gm, sh.pw, true, diag_sum(sh.qk_diag, i));
-      store_quarter(PM, i, qd, pv);
-      rescale_quarter(Kt, i, qd, 1.f, true);
-    }
-    uint4 dyr[4];  // dy of row i for [3], loaded a phase early
-    load_quarter(dyr, row_ptr(P.dy, P, b, h, valid ? c0 + i : c0), qd, valid);
-    BWD_WAIT(&sh.bar_mma[1], ph);
-    if (tid == 0) {  // MMA2 done: Q is free for this tile's gate
-      umma::mbar_expect_tx(bar_g, tile_bytes);
-      tma_tile(Qt, &tmg, b, h, c0, bar_g);
-    }
-    {
-      float ov[32];
-      umma::tmem_ld2x16(tO + col, ov);
-      const float f = sh.pw[i + 1] * s_inv;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) ov[e] *= f;
-      umma::tmem_st32(tO + col, ov);
-      rescale_quarter(SB, i, qd, s_inv, true);
-      umma::tmem_wait_st();
-    }
-    umma::fence_async_smem();
-    umma::fence_before();
-    BWD_WAIT(bar_v, ph);
-    if (tid == 0) {
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // MMA3: O += Pm V
-        umma::mma_ss(tm + 128, umma::desc_kmajor(aPM, kk, ROWS), umma::desc_mnmajor(aV, kk, ROWS), id_kmn, 1u);
-      umma::commit(&sh.bar_mma[2]);
-    }
-
-    // [3] dgate and dO from O (output norm and gate backward): dgate -> PM,
-    // dO -> Q over the gate (each thread rewrites only the chunks it read)
-    BWD_WAIT(&sh.bar_mma[2], ph);
-    BWD_WAIT(bar_g, ph);
-    {
-      float ov[32];
-      umma::tmem_ld2x16(tO + col, ov);
-      float ss = 0.f;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) ss = fmaf(ov[e], ov[e], ss);
-      sh.red[qd][i] = ss;
-      __syncthreads();
-      const float ro = rsqrtf((sh.red[0][i] + sh.red[1][i] + sh.red[2][i] + sh.red[3][i]) / (float)D + P.eps);
-      float mpart = 0.f;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        float gf[8], df[8], dg8[8];
-        unpack8(*tile_at(Qt, i, 4 * qd + u), gf);
-        unpack8(dyr[u], df);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float nv = ov[8 * u + e] * ro;
-          const float z = sigmoid_fast(gf[e]);
-          const float dn = df[e] * z;
-          dg8[e] = dn * nv * (1.f - z);
-          mpart = fmaf(dn, nv, mpart);
-          ov[8 * u + e] = dn;  // keep dn; n is recomputed below
+    int prev_c0 = 0;
+    for (int n = 0; n <= ntile; ++n) {
+      const bool have = n < ntile, drain = n >= 1;
+      const int buf = n & 1;
+      const uint32_t ph = n & 1;
+      const int c0 = t0 + n * CV, c = have ? min(CV, t1 - c0) : 0;
+      const bool valid = i < c;
+      const uint32_t ta = tm + 128 + 128 * buf + lane_base;        // tA of tile n (this lane)
+      const uint32_t tap = tm + 128 + 128 * (buf ^ 1) + lane_base; // tA of tile n - 1
+      unsigned char *Kt = base + (1 + buf) * TILE, *Kp = base + (2 - buf) * TILE;
+      if (have) {
+        // [W1] raw q, k of tile n: row fr, pairs [16 fu, 16 fu + 16); norms by shuffles
+        wait_or_fail(&sh.bar_q, ph, failed);
+        wait_or_fail(&sh.bar_k[buf], (n >> 1) & 1, failed);
+        {
+          uint4 qr[4], kr[4];
+          ld_pairs(Qs, fr, fu, qr);
+          ld_pairs(Kt, fr, fu, kr);
+          if (!(fr < c))  // rows past the tile hold stale bytes: use zeros
+            qr[0] = qr[1] = qr[2] = qr[3] = kr[0] = kr[1] = kr[2] = kr[3] = make_uint4(0, 0, 0, 0);
+          float sq, sk, qk;
+          norms_and_dot(qr, kr, sq, sk, qk);
+          sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+          sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+          qk += __shfl_xor_sync(0xffffffffu, qk, 1);
+          sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+          sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+          qk += __shfl_xor_sync(0xffffffffu, qk, 2);
+          const float rq = rsqrtf(sq / (float)D + P.eps);
+          const float rk = rsqrtf(sk / (float)D + P.eps) * P.kscale;
+          if (fu == 0) sh.qk_diag[buf][fr] = qk * rq * rk;  // q~_i . k~_i in fp32
+          feature_qk_store(qr, kr, rq, rk, P.pos_offset + c0 + fr, fu, sh.ru, Qs, Kt, fr);
         }
-        *tile_at(PM, i, 4 * qd + u) = pack8(dg8);
-      }
-      sh.red2[qd][i] = mpart;
-      __syncthreads();
-      const float mean = (sh.red2[0][i] + sh.red2[1][i] + sh.red2[2][i] + sh.red2[3][i]) / (float)D;
-      // n = o ro again from TMEM (cheaper than holding both o and dn in registers)
-      float o2[32];
-      umma::tmem_ld2x16(tO + col, o2);
+        warp_arrive(&sh.bar_feat, lane);
+
+        // [W2] after MMA7 / MMA4 of tile n - 1: Sb = fp16(S 2^-e) per column quarter, S <- gamma^c S
+        if (n >= 1) wait_or_fail(&sh.bar_m74, (n - 1) & 1, failed);
+        float s_inv;
+        {
+          float sv[32];
+          umma::tmem_ld2x16(myS, sv);
+          float m = 0.f;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) ov[e] = valid ? ro * (ov[e] - o2[e] * ro * mean) : 0.f;
-      {  // v_i . do_i in fp32: do_i is orthogonal to o_i, so this nearly cancels
-         // wherever o_i is close to a multiple of v_i, and bf16 do loses it
-        float vd = 0.f;
+          for (int e = 0; e < 32; ++e) m = fmaxf(m, fabsf(sv[e]));
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          float vf[8];
-          unpack8(*tile_at(Vt, i, 4 * qd + u), vf);
+          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          if (lane == 0) sh.smax[warp] = m;
+          named_sync(1 + qd, 128);
+          m = fmaxf(fmaxf(sh.smax[4 * qd], sh.smax[4 * qd + 1]),
+                    fmaxf(sh.smax[4 * qd + 2], sh.smax[4 * qd + 3]));
+          int e = 0;
+          if (m > 0.f) frexpf(m, &e);
+          const f2 s_fwd = dup2(ldexpf(1.f, -e));
+          s_inv = ldexpf(1.f, e);
+          f2 x[16];
+          pairs_of(sv, x);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) vd = fmaf(vf[e], ov[8 * u + e], vd);
+          for (int u = 0; u < 4; ++u) {
+            f2 t[4];
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) t[e2] = mul2(x[4 * u + e2], s_fwd);
+            *tile_at(SB, i, 4 * qd + u) = pack4x2h(t);
+          }
+          const f2 carry = dup2(sh.pw[c]);
+#pragma unroll
+          for (int e2 = 0; e2 < 16; ++e2) x[e2] = mul2(x[e2], carry);
+          floats_of(x, sv);
+          umma::tmem_st32(myS, sv);
+          umma::tmem_wait_st();
         }
-        sh.vd_diag[qd][i] = vd;
-      }
-      store_quarter(Qt, i, qd, ov);
-    }
-    umma::fence_async_smem();
-    sync_tc();
-    if (tid == 0) {
-      tma_store_tile(&tmdg, PM, b, h, c0);
-      tma_store_tile(&tmo, Qt, b, h, c0);
-      umma::bulk_commit();
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // MMA5: dP = dO V^T
-        umma::mma_ss(tm, umma::desc_kmajor(aQ, kk, ROWS), umma::desc_kmajor(aV, kk, ROWS), id_kk, kk > 0);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // MMA6: I = dO S^T
-        umma::mma_ss(tm + 256, umma::desc_kmajor(aQ, kk, ROWS), umma::desc_kmajor(aSB, kk, ROWS), id_kk, kk > 0);
-      umma::commit(&sh.bar_mma[3]);
-      umma::bulk_wait_read();  // dgate and dO have left PM and Q before [4] reuses them
-    }
+        warp_arrive(&sh.bar_sb, lane);
 
-    // [4] dPm = bf16(dP (.) D) into PM (Pm is dead once MMA3 is done)
-    BWD_WAIT(&sh.bar_mma[3], ph);
+        // [W3] after MMA1: Pm (with the fp32 diagonal), k~ -> bf16; after MMA2:
+        // O <- gamma^{i+1} 2^e O, Sb -> bf16 S
+        uint4 dyr[4];  // dy of row i for [W4], in flight during [W3]
+        load_quarter(dyr, row_ptr(P.dy, P, b, h, valid ? c0 + i : c0), qd, valid);
+        wait_or_fail(&sh.bar_p, ph, failed);
+        {
+          float pv[32];
+          umma::tmem_ld2x16(myP, pv);
+          f2 x[16];
+          pairs_of(pv, x);
+          mask_lower_table(x, sh.dm, i, (int)col);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {  // k~ fp16 -> bf16 for MMA7 / MMA4 (MMA1 has read it)
+            uint4 *p = tile_at(Kt, i, 4 * qd + u);
+            f2 f[4];
+            unpack4x2h(*p, f);
+            *p = pack4x2(f);
+          }
+          wait_or_fail(&sh.bar_o, ph, failed);  // MMA2 done: PM and SB are free to rewrite
+#pragma unroll
+          for (int u = 0; u < 4; ++u) *tile_at(PM, i, 4 * qd + u) = pack4x2(&x[4 * u]);
+          if (qd == sub)  // the diagonal from fp32 features (written in [W1], met at [W2]'s barrier)
+            *(reinterpret_cast<__nv_bfloat16 *>(tile_at(PM, i, i >> 3)) + (i & 7)) =
+                __float2bfloat16_rn(sh.qk_diag[buf][i]);
+          const f2 si = dup2(s_inv);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {  // Sb -> S (bf16, unscaled) for MMA6
+            uint4 *p = tile_at(SB, i, 4 * qd + u);
+            f2 f[4];
+            unpack4x2h(*p, f);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f[e] = mul2(f[e], si);
+            *p = pack4x2(f);
+          }
+          float ov[32];
+          umma::tmem_ld2x16(ta + col, ov);
+          const f2 f = dup2(sh.pw[i + 1] * s_inv);
+          f2 y2[16];
+          pairs_of(ov, y2);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) y2[e] = mul2(y2[e], f);
+          floats_of(y2, ov);
+          umma::tmem_st32(ta + col, ov);
+          umma::tmem_wait_st();
+        }
+        warp_arrive(&sh.bar_pm, lane);
 
-    if (tid == 0 && n + 1 < ntile) {  // the Q tile (dO) is free: next q
-      umma::mbar_expect_tx(bar_q, tile_bytes);
-      tma_tile(Qt, &tmq, b, h, c0 + CV, bar_q);
-    }
-    {
-      float pv[32];
-      const float vd = diag_sum(sh.vd_diag, i);
-      if (qd == sub && valid) P.ddiag[((size_t)b * P.T + c0 + i) * P.H + h] = vd;
-      mask_lower_block(tP + col, pv, i, sub, qd, valid, gm, sh.pw, true, vd);
-      store_quarter(PM, i, qd, pv);
-    }
-    uint4 qraw[4];  // raw q pairs of row i for the dq epilogue (in flight during MMA7)
-    load_pairs(qraw, row_ptr(P.q, P, b, h, valid ? c0 + i : c0), qd, valid);
-    umma::fence_async_smem();
-    sync_tc();
-    if (tid == 0) {
+        // [W4] after MMA3: output norm and gate backward.  n = o r, z = sigmoid(gate),
+        // dn = dy z, dgate = dn n (1 - z), dO = r (dn - n mean(dn n)); rows past the tile get 0
+        wait_or_fail(&sh.bar_m3, ph, failed);
+        wait_or_fail(&sh.bar_g, ph, failed);
+        wait_or_fail(&sh.bar_v, ph, failed);
+        {
+          float o[32];
+          umma::tmem_ld2x16(ta + col, o);
+          f2 ox[16];
+          pairs_of(o, ox);
+          f2 so2 = 0ull, sdo = 0ull;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // MMA7: O-columns <- dPm K~
-        umma::mma_ss(tm + 128, umma::desc_kmajor(aPM, kk, ROWS), umma::desc_mnmajor(aK, kk, ROWS), id_kmn, kk > 0);
-      umma::commit(&sh.bar_mma[4]);
-    }
+          for (int u = 0; u < 4; ++u) {
+            f2 gz[4], dv[4];
+            unpack4x2(*tile_at(Qs, i, 4 * qd + u), gz);
+            unpack4x2(dyr[u], dv);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const f2 dn = mul2(dv[e], sigmoid2(gz[e]));
+              so2 = fma2(ox[4 * u + e], ox[4 * u + e], so2);
+              sdo = fma2(dn, ox[4 * u + e], sdo);
+            }
+          }
+          sh.red_do[0][qd][i] = hsum2(so2);
+          sh.red_do[1][qd][i] = hsum2(sdo);
+          named_sync(5 + sub, 128);
+          const float ro = rsqrtf((sh.red_do[0][0][i] + sh.red_do[0][1][i] + sh.red_do[0][2][i] +
+                                   sh.red_do[0][3][i]) / (float)D + P.eps);
+          const float mean = ro * (sh.red_do[1][0][i] + sh.red_do[1][1][i] + sh.red_do[1][2][i] +
+                                   sh.red_do[1][3][i]) / (float)D;
+          const f2 ro2 = dup2(ro), nmean = dup2(-mean), one = dup2(1.f), keep = dup2(valid ? 1.f : 0.f);
+          f2 vd = 0ull;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 *gp = tile_at(Qs, i, 4 * qd + u);
+            f2 gz[4], dv[4], vv[4], dg[4], dd[4];
+            unpack4x2(*gp, gz);
+            unpack4x2(dyr[u], dv);
+            unpack4x2(*tile_at(Vs, i, 4 * qd + u), vv);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const f2 z = sigmoid2(gz[e]);
+              const f2 dn = mul2(dv[e], z);
+              const f2 nv = mul2(ox[4 * u + e], ro2);
+              dg[e] = mul2(mul2(dn, nv), fma2(z, dup2(-1.f), one));
+              dd[e] = mul2(mul2(ro2, fma2(nv, nmean, dn)), keep);
+              vd = fma2(vv[e], dd[e], vd);
+            }
+            *tile_at(PM, i, 4 * qd + u) = pack4x2(dg);
+            *gp = pack4x2(dd);
+          }
+          sh.vd_part[qd][i] = hsum2(vd);
+        }
+        warp_arrive(&sh.bar_do, lane);
+      }
 
-    // [5] k~dec (in place), MMA4 (state carry); dq epilogue overlaps MMA4
-    BWD_WAIT(&sh.bar_mma[4], ph);
-    rescale_quarter(Kt, i, qd, valid ? sh.pw[c - 1 - i] : 0.f, false);
-    umma::fence_async_smem();
-    sync_tc();
-    if (tid == 0) {
+      if (drain) {
+        // [W6] dq of tile n - 1: dQ~ from TMEM, RoPE^T, RMSNorm backward against raw q
+        // (the K buffer of tile n - 1), in place; pairs m = 16 qd .. 16 qd + 15
+        // (in the last step no [W2] has waited for MMA7 of tile n - 1: wait here)
+        if (!have) wait_or_fail(&sh.bar_m74, (n - 1) & 1, failed);
+        wait_or_fail(&sh.bar_qr, (n - 1) & 1, failed);
+        {
+          float alo[16], ahi[16];
+          {
+            uint32_t ra[16], rb[16];
+            umma::tmem_ld16_nowait(tap + 16 * qd, ra);
+            umma::tmem_ld16_nowait(tap + 64 + 16 * qd, rb);
+            umma::tmem_wait_ld();
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // MMA4: S += K~dec^T V
-        umma::mma_ss(tm + 384, umma::desc_mnmajor(aK, kk, ROWS), umma::desc_mnmajor(aV, kk, ROWS), id_mnmn, 1u);
-      umma::commit(&sh.bar_mma[5]);
-    }
-    {
-      // dQ~ = intra + gamma^{i+1} inter, for this thread's 16 RoPE pairs
-      float alo[16], ahi[16];
-      const float wi = sh.pw[i + 1];
-      {
-        float t[16];
-        umma::tmem_ld16(tO + 16 * qd, alo);
-        umma::tmem_ld16(tI + 16 * qd, t);
+            for (int e = 0; e < 16; ++e) {
+              alo[e] = __uint_as_float(ra[e]);
+              ahi[e] = __uint_as_float(rb[e]);
+            }
+          }
+          uint4 qr[4];
+          ld_pairs(Kp, i, qd, qr);
+          const long long pos = P.pos_offset + prev_c0 + i;
+          f2 g0[8], g1[8];
+          f2 sq = 0ull, sgq = 0ull;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) alo[e] = fmaf(wi, t[e], alo[e]);
-        umma::tmem_ld16(tO + 64 + 16 * qd, ahi);
-        umma::tmem_ld16(tI + 64 + 16 * qd, t);
+          for (int hf = 0; hf < 2; ++hf) {
+            f2 cs[4], sn[4], nsn[4], x0[4], x1[4];
+            rope8(pos, sh.ru, hf, qd, cs, sn, nsn);
+            unpack4x2(qr[hf], x0);
+            unpack4x2(qr[2 + hf], x1);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) ahi[e] = fmaf(wi, t[e], ahi[e]);
+            for (int e = 0; e < 4; ++e) {
+              const f2 a = mk2(alo[8 * hf + 2 * e], alo[8 * hf + 2 * e + 1]);
+              const f2 bq = mk2(ahi[8 * hf + 2 * e], ahi[8 * hf + 2 * e + 1]);
+              // transpose of (x0, x1) -> (x0 c - x1 s, x0 s + x1 c)
+              g0[4 * hf + e] = fma2(a, cs[e], mul2(bq, sn[e]));
+              g1[4 * hf + e] = fma2(bq, cs[e], mul2(a, nsn[e]));
+              sq = fma2(x0[e], x0[e], fma2(x1[e], x1[e], sq));
+              sgq = fma2(g0[4 * hf + e], x0[e], fma2(g1[4 * hf + e], x1[e], sgq));
+            }
+          }
+          sh.red_dq[0][qd][i] = hsum2(sq);
+          sh.red_dq[1][qd][i] = hsum2(sgq);
+          named_sync(5 + sub, 128);
+          const float r = rsqrtf((sh.red_dq[0][0][i] + sh.red_dq[0][1][i] + sh.red_dq[0][2][i] +
+                                  sh.red_dq[0][3][i]) / (float)D + P.eps);
+          const float m = r * (sh.red_dq[1][0][i] + sh.red_dq[1][1][i] + sh.red_dq[1][2][i] +
+                               sh.red_dq[1][3][i]) / (float)D;
+          // dq = r g - r^2 m q
+          const f2 r2 = dup2(r), cq = dup2(-r * r * m);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            f2 x0[4], x1[4], lo[4], hi[4];
+            unpack4x2(qr[hf], x0);
+            unpack4x2(qr[2 + hf], x1);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              lo[e] = fma2(x0[e], cq, mul2(g0[4 * hf + e], r2));
+              hi[e] = fma2(x1[e], cq, mul2(g1[4 * hf + e], r2));
+            }
+            *tile_at(Kp, i, 2 * qd + hf) = pack4x2(lo);
+            *tile_at(Kp, i, 8 + 2 * qd + hf) = pack4x2(hi);
+          }
+        }
+        warp_arrive(&sh.bar_w6, lane);
+      } else if (have) {
+        named_sync(5 + sub, 128);  // orders [W4]'s vd_part before [W5] reads it
       }
-      feature_grad_row(alo, ahi, qraw, rq, pos, i, qd, valid, sh.ru, sh.red, SB);  // S is dead
-    }
-    umma::fence_async_smem();
-    BWD_WAIT(&sh.bar_mma[5], ph);
-    if (tid == 0) {  // dq out; MMA4 done: V and this K buffer are free
-      tma_store_tile(&tmdq, SB, b, h, c0);
-      umma::bulk_commit();
-      if (n + 1 < ntile) {
-        umma::mbar_expect_tx(bar_v, tile_bytes);
-        tma_tile(Vt, &tmv, b, h, c0 + CV, bar_v);
-      }
-      if (n + 2 < ntile) {
-        umma::mbar_expect_tx(&bar_k[buf], tile_bytes);
-        tma_tile(Kt, &tmk, b, h, c0 + 2 * CV, &bar_k[buf]);
+
+      if (have) {
+        // [W5] after MMA5 / MMA6 and the stores' reads: dPm -> PM (diagonal: fp32
+        // v_i . do_i), I <- gamma^{i+1} I, V -> Vdec (in place)
+        wait_or_fail(&sh.bar_m56, ph, failed);
+        wait_or_fail(&sh.bar_rd, ph, failed);
+        {
+          float pv[32];
+          umma::tmem_ld2x16(myP, pv);
+          f2 x[16];
+          pairs_of(pv, x);
+          mask_lower_table(x, sh.dm, i, (int)col);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) *tile_at(PM, i, 4 * qd + u) = pack4x2(&x[4 * u]);
+          if (qd == sub) {
+            const float vd = sh.vd_part[0][i] + sh.vd_part[1][i] + sh.vd_part[2][i] + sh.vd_part[3][i];
+            *(reinterpret_cast<__nv_bfloat16 *>(tile_at(PM, i, i >> 3)) + (i & 7)) = __float2bfloat16_rn(vd);
+            if (valid) P.ddiag[((size_t)b * P.T + c0 + i) * P.H + h] = vd;
+          }
+          float iv[32];
+          umma::tmem_ld2x16(ta + col, iv);
+          const f2 wi = dup2(sh.pw[i + 1]);
+          pairs_of(iv, x);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) x[e] = mul2(x[e], wi);
+          floats_of(x, iv);
+          umma::tmem_st32(ta + col, iv);
+          const f2 wv = dup2(valid ? sh.pw[c - 1 - i] : 0.f);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 *p = tile_at(Vs, i, 4 * qd + u);
+            f2 f[4];
+            unpack4x2(*p, f);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f[e] = mul2(f[e], wv);
+            *p = pack4x2(f);
+          }
+          umma::tmem_wait_st();
+        }
+        warp_arrive(&sh.bar_w5, lane);
+        prev_c0 = c0;
       }
     }
   }
-  if (tid == 0) umma::bulk_wait_all();
-  if (failed && tid == 0 && P.err) atomicOr(P.err, 4u);
+  if (failed) atomicOr(&sh.failed, 1u);
   sync_tc();
+  if (sh.failed && tid == 0 && P.err) atomicOr(P.err, 4u);
   if (warp == 0) umma::tmem_dealloc(tm, 512);
 }
 
@@ -714,12 +938,15 @@ __global__ void __launch_bounds__(NT, 1)
 #undef BWD_WAIT
 
 constexpr size_t kBwdSmem = 6 * TILE + sizeof(BwdShared) + 1024;
+static_assert(kBwdSmem <= 232448, "dk/dv pass exceeds 227 KiB of shared memory per CTA");
+constexpr size_t kDqSmem = 6 * TILE + sizeof(DqShared) + 1024;
+static_assert(kDqSmem <= 232448, "dq pass exceeds 227 KiB of shared memory per CTA");
 
 }  // namespace
 }  // namespace tc
 
 cudaError_t launch_tc_bwd_dq(const MixerParams &P, cudaStream_t st) {
-  CUtensorMap mq, mk, mv, mg, mo, mdg, mdq;
+  CUtensorMap mq, mk, mv, mg, mo, mdg, mdq, mdy;
   cudaError_t e;
   if ((e = tc::make_map(&mq, P.q, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mk, P.k, P, P.chunk)) != cudaSuccess) return e;
@@ -728,10 +955,11 @@ cudaError_t launch_tc_bwd_dq(const MixerParams &P, cudaStream_t st) {
   if ((e = tc::make_map(&mo, P.dO, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mdg, P.dg, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mdq, P.dq, P, P.chunk)) != cudaSuccess) return e;
+  if ((e = tc::make_map(&mdy, P.dy, P, P.chunk)) != cudaSuccess) return e;
   e = cudaFuncSetAttribute(tc::tc_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)tc::kBwdSmem);
+                           (int)tc::kDqSmem);
   if (e != cudaSuccess) return e;
-  tc::tc_bwd_dq_kernel<<<dim3(P.nseg, P.H, P.B), tc::NT, tc::kBwdSmem, st>>>(P, mq, mk, mv, mg, mo, mdg, mdq);
+  tc::tc_bwd_dq_kernel<<<dim3(P.nseg, P.H, P.B), tc::NTO, tc::kDqSmem, st>>>(P, mq, mk, mv, mg, mo, mdg, mdq, mdy);
   return cudaGetLastError();
 }
 

@@ -18,7 +18,13 @@ namespace {
 
 constexpr int D = 128;
 constexpr int ROWS = 128;           // rows of every operand tile
-constexpr int NT = 512;             // threads per CTA
+constexpr int NT = 512;             // threads per CTA of the lockstep kernels
+constexpr int NWORK = 16;              // worker warps (CUDA-core work) of the warp-specialized
+                                       // kernels, 4 warpgroups
+constexpr int NTO = (NWORK + 4) * 32;  // + one warpgroup: its first warp issues MMAs / TMA copies
+                                       // (registers are granted per warpgroup, so a lone 17th
+                                       // warp would cost as much as four)
+constexpr int DM_STRIDE = 264;      // row pitch (floats) of the causal-mask decay table
 constexpr int TILE = ROWS * D * 2;  // bytes of one 16-bit tile (32 KiB)
 constexpr int HALF_TILE = TILE / 2; // one 64-column block
 
@@ -302,6 +308,34 @@ __device__ __forceinline__ void mask_upper_block(uint32_t taddr, float (&v)[32],
     } else {
       v[e] = 0.f;
     }
+  }
+}
+
+// Decay table of the causal mask, read backwards, in four copies shifted by
+// one element so that every lane's 32 weights start 16-byte aligned:
+// dm[cp][x] = gamma^(127 - x - cp) for x + cp <= 127, else 0.  Rows are padded
+// to DM_STRIDE floats so that the eight lanes of a quarter-warp hit distinct
+// banks.  Filled by all `nthreads` threads of the CTA.
+__device__ __forceinline__ void fill_mask_table(float (*dm)[DM_STRIDE], float log2g, int tid,
+                                                int nthreads) {
+  for (int e = tid; e < 4 * DM_STRIDE; e += nthreads) {
+    const int cp = e / DM_STRIDE, x = e % DM_STRIDE;
+    dm[cp][x] = x + cp <= ROWS - 1 ? exp2f((float)(ROWS - 1 - x - cp) * log2g) : 0.f;
+  }
+}
+
+// Causal decay of columns [col, col + 32) of score row i, in place on 16
+// pairs: x_j *= gamma^(i - j) for j <= i, 0 for j > i.  The weight of column
+// col + e is dm[cp][s0 - cp + e] with s0 = 127 - i + col, cp = s0 & 3.
+__device__ __forceinline__ void mask_lower_table(f2 (&x)[16], const float (*dm)[DM_STRIDE], int i,
+                                                 int col) {
+  const int s0 = ROWS - 1 - i + col, cp = s0 & 3;
+  const float4 *wt = reinterpret_cast<const float4 *>(&dm[cp][s0 - cp]);
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const float4 w = wt[u];
+    x[2 * u] = mul2(x[2 * u], mk2(w.x, w.y));
+    x[2 * u + 1] = mul2(x[2 * u + 1], mk2(w.z, w.w));
   }
 }
 

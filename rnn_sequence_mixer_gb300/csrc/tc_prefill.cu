@@ -41,10 +41,6 @@ namespace {
 
 // ------------------------------------------------------------------ local state pass
 
-constexpr int NWORK = 16;              // worker warps (CUDA-core work), 4 warpgroups
-constexpr int NTO = (NWORK + 4) * 32;  // + one warpgroup: its first warp issues MMAs / TMA copies
-                                       // (registers are granted per warpgroup, so a lone 17th
-                                       // warp would cost as much as four)
 constexpr int kStages = 3;             // (k, v) tile pairs of the local-state pass in flight
 
 struct StateShared {
@@ -196,11 +192,7 @@ struct OutShared {
   unsigned long long ru[kMaxPairs];  // RoPE phase increments (load_rope_table)
   float red_o[4][ROWS];
   float pw[ROWS + 1];
-  // decay of the causal mask read backwards, in four copies shifted by one
-  // element so that every lane's 32 weights start 16-byte aligned:
-  // dm[c][x] = gamma^(127 - x - c) for x + c <= 127, else 0.  Rows are padded
-  // to 264 floats so that the eight lanes of a quarter-warp hit distinct banks.
-  alignas(16) float dm[4][264];
+  alignas(16) float dm[4][DM_STRIDE];  // causal-mask decay table (fill_mask_table)
   float qk_diag[2][ROWS];  // fp32 q~_i . k~_i of tiles n (n & 1)
   float smax[NWORK];
   uint64_t bar_mma[2];  // [0]: MMA1 + MMA2 of a tile done, [1]: MMA3 + MMA4 done (commits)
@@ -270,10 +262,7 @@ __global__ void __launch_bounds__(NTO, 1)
     sh.failed = 0;
   }
   if (tid <= ROWS) sh.pw[tid] = exp2f((float)tid * l2g);
-  for (int e = tid; e < 4 * 264; e += NTO) {
-    const int cp = e / 264, x = e % 264;
-    sh.dm[cp][x] = x + cp <= ROWS - 1 ? exp2f((float)(ROWS - 1 - x - cp) * l2g) : 0.f;
-  }
+  fill_mask_table(sh.dm, l2g, tid, NTO);
   load_rope_table(sh.ru, P, tid);
   if (warp == 0) umma::tmem_alloc(&sh.tmem_base, 512);
   if (CV < ROWS)  // rows [CV, 128) of V are never written by TMA: clear them once
@@ -524,19 +513,11 @@ __global__ void __launch_bounds__(NTO, 1)
           float pv[32];
           umma::tmem_ld2x16(myP, pv);
           // mask: Pm = bf16((Q~ K~^T) (.) D) into SP (Sb is dead once MMA2 is done),
-          // D_ij = gamma^(i-j) for j <= i, else 0: weights e = 0..31 of this
-          // lane are dm[.][s0 + e] for s0 = 127 - i + 32 qd.  Rows and columns
-          // past the tile are zero already (their q~, k~ are zero).
-          const int s0 = ROWS - 1 - i + (int)col, cp = s0 & 3;
-          const float4 *wt = reinterpret_cast<const float4 *>(&sh.dm[cp][s0 - cp]);
+          // D_ij = gamma^(i-j) for j <= i, else 0.  Rows and columns past the
+          // tile are zero already (their q~, k~ are zero).
           f2 x[16];
           pairs_of(pv, x);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const float4 w = wt[u];
-            x[2 * u] = mul2(x[2 * u], mk2(w.x, w.y));
-            x[2 * u + 1] = mul2(x[2 * u + 1], mk2(w.z, w.w));
-          }
+          mask_lower_table(x, sh.dm, i, (int)col);
           // k~dec = gamma^{c-1-i} k~ as bf16, in place (K~ is dead once MMA1 is done)
           {
             const f2 wk = dup2(valid ? sh.pw[c - 1 - i] : 0.f);
