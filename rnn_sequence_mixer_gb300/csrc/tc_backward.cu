@@ -7,12 +7,12 @@
 // gamma^{i-j} for i >= j:
 //
 //   tc_bwd_dq_kernel (tiles in order, S carried in TMEM as in the forward)
-//     O     = diag(gamma^{i+1}) Q~ S + (Q~ K~^T (.) D) V          MMA1-3 (recompute)
+//     O     = diag(gamma^{i+1}) Q~ S + (Q~ K~^T (.) D) V          (recompute)
 //     dgate = dy n sigma(g) (1 - sigma(g)),  n = O r,  r = 1/RMS(O)
 //     dO    = r (dn - n mean(dn n)),  dn = dy sigma(g)              (to the workspace, bf16)
-//     dQ~   = diag(gamma^{i+1}) dO S^T + ((dO V^T) (.) D) K~       MMA5-7
+//     dQ~   = diag(gamma^{i+1}) dO S^T + ((dO V^T) (.) D) K~
 //     dq    = Norm^T RoPE^T dQ~
-//     S    <- gamma^c S + (diag(gamma^{c-1-j}) K~)^T V              MMA4
+//     S    <- gamma^c S + K~^T diag(gamma^{c-1-j}) V
 //   tc_state_kernel<true> (tc_prefill.cu) then sums q~^T do per segment and
 //   the fp32 scan (scan.cu) turns those sums into E, the gradient reaching the
 //   state at each segment's last token from later tokens.
@@ -28,69 +28,22 @@
 // accumulation.  Two diagonal entries are taken in fp32 on the CUDA cores
 // instead: q~_i . k~_i (where it nearly cancels, o_i is small and dO_i ~ 1/|o_i|
 // magnifies its error) and v_i . do_i (do_i is orthogonal to o_i, so this
-// cancels wherever o_i is close to a multiple of v_i, e.g. at t = 0).  Decay weights that multiply a whole operand row are folded
-// into that operand (K~dec, Vdec, Q~w); the one that multiplies a product row
-// after the fact (gamma^{i+1} on dO S^T) gets its own TMEM accumulator.
+// cancels wherever o_i is close to a multiple of v_i, e.g. at t = 0).  Decay
+// weights that multiply a whole operand row are folded into that operand
+// (K~dec, Vdec, Q~w); gamma^{i+1} on the rows of dO S^T is applied to that
+// product in TMEM before the intra-chunk term accumulates onto it.
 //
-// Threads: 512 per (b, h, segment), all in lockstep.  Thread (warp w, lane l)
-// owns tile row i = 32 (w % 4) + l (its TMEM lane) and column quarter
-// qd = w / 4; thread 0 issues the TMA copies and MMAs between CTA barriers.
+// Threads: both kernels are warp-specialized like the forward output pass:
+// 16 worker warps own the CUDA-core phases (thread (warp w, lane l) owns tile
+// row i = 32 (w % 4) + l, its TMEM lane, and column quarter qd = w / 4; the
+// feature map uses row 8 w + l / 4 and pair quarter l % 4) and one issuer
+// thread issues the MMAs and TMA copies; they hand off through mbarriers.
 #include "tc_common.cuh"
 
 namespace hla {
 namespace tc {
 
 namespace {
-
-struct BwdShared {
-  unsigned long long ru[kMaxPairs];  // RoPE phase increments (load_rope_table)
-  float red[4][ROWS];
-  float red2[4][ROWS];
-  float qk_diag[4][ROWS];  // parts of the fp32 q~_i . k~_i
-  float vd_diag[4][ROWS];  // parts of the fp32 v_i . do_i
-  float pw[ROWS + 1];
-  float smax[NT / 32];
-  uint64_t bar_tma[5];
-  uint64_t bar_mma[6];
-  uint32_t tmem_base;
-};
-
-// Sum of the four quarter parts of row i's diagonal entry.
-__device__ __forceinline__ float diag_sum(const float (*part)[ROWS], int i) {
-  return part[0][i] + part[1][i] + part[2][i] + part[3][i];
-}
-
-// Store 32 values of row i, columns [32 qd, 32 qd + 32), as bf16 into a tile.
-__device__ __forceinline__ void store_quarter(unsigned char *tile, int i, int qd, const float (&v)[32]) {
-#pragma unroll
-  for (int u = 0; u < 4; ++u) *tile_at(tile, i, 4 * qd + u) = pack8(&v[8 * u]);
-}
-
-// Scale row i, columns [32 qd, 32 qd + 32) of a tile by w, converting fp16 ->
-// bf16 (from_half) or bf16 -> bf16.
-__device__ __forceinline__ void rescale_quarter(unsigned char *tile, int i, int qd, float w,
-                                                bool from_half) {
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    uint4 *p = tile_at(tile, i, 4 * qd + u);
-    float f[8];
-    if (from_half)
-      unpack8h(*p, f);
-    else
-      unpack8(*p, f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) f[e] *= w;
-    *p = pack8(f);
-  }
-}
-
-// TMEM columns {16 qd .. 16 qd + 15} and {64 + 16 qd .. 64 + 16 qd + 15} of this
-// thread's lane: the 16 RoPE pairs this thread owns.
-__device__ __forceinline__ void tmem_ld_pairs(uint32_t taddr, int qd, float (&lo)[16],
-                                              float (&hi)[16]) {
-  umma::tmem_ld16(taddr + 16 * qd, lo);
-  umma::tmem_ld16(taddr + 64 + 16 * qd, hi);
-}
 
 // This thread's 16 RoPE pairs of a raw input row (elements 16 qd .. 16 qd + 15
 // and 64 + 16 qd ..), zeros when !valid.
@@ -106,64 +59,71 @@ __device__ __forceinline__ void load_pairs(uint4 (&ra)[4], const __nv_bfloat16 *
   }
 }
 
-// Gradient of one feature row through RoPE and RMSNorm: g holds dL/d(rotated
-// normalized row) for this thread's 16 pairs (lo = element m, hi = m + 64,
-// m = 16 qd + e); ra = those pairs of the raw input row (load_pairs);
-// r = 1 / RMS(raw).  Writes dL/draw for the pairs (bf16, zeros when !valid)
-// into row i of the operand-layout tile `out`, for a TMA store.  The mean over
-// the row needs the other three threads of the row: red is the [4][ROWS]
-// scratch and the call holds one CTA barrier.
-__device__ __forceinline__ void feature_grad_row(const float (&glo)[16], const float (&ghi)[16],
-                                                 const uint4 (&ra)[4], float r, long long p,
-                                                 int i, int qd, bool valid,
-                                                 const unsigned long long *ru, float (*red)[ROWS],
-                                                 unsigned char *out) {
-  float n0[16], n1[16], g0[16], g1[16];
+// Gradient with respect to a raw q or k row, through RoPE and RMSNorm, for this
+// thread's 16 RoPE pairs of row i (elements 16 qd .. 16 qd + 15 and their
+// partners 64 further on).  g~ = gscale * (the gradient of the rotated,
+// normalized row) is read from TMEM at tmem_row (the lane's base address,
+// column 0); raw holds the raw row's pairs (ld_pairs / load_pairs layout).
+// With g = RoPE^T g~, x the raw row and r = 1 / RMS(x):
+//   dL/dx = r g - r^3 x (g . x) / d.
+// Writes it as bf16 into the same chunks of `out`.  The two row sums need the
+// other three threads of the row (warps sub, sub + 4, sub + 8, sub + 12): red
+// is a [2][4][ROWS] scratch and the call holds named barrier 5 + sub.
+__device__ __forceinline__ void feature_grad_pairs(uint32_t tmem_row, const uint4 (&raw)[4],
+                                                   float gscale, long long pos, int i, int qd,
+                                                   int sub, float eps, const unsigned long long *ru,
+                                                   float (*red)[4][ROWS], unsigned char *out) {
+  float alo[16], ahi[16];
   {
-    float f[8];
+    uint32_t ra[16], rb[16];
+    umma::tmem_ld16_nowait(tmem_row + 16 * qd, ra);
+    umma::tmem_ld16_nowait(tmem_row + 64 + 16 * qd, rb);
+    umma::tmem_wait_ld();
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      unpack8(ra[hf], f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) n0[8 * hf + e] = f[e] * r;
-      unpack8(ra[2 + hf], f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) n1[8 * hf + e] = f[e] * r;
+    for (int e = 0; e < 16; ++e) {
+      alo[e] = __uint_as_float(ra[e]) * gscale;
+      ahi[e] = __uint_as_float(rb[e]) * gscale;
     }
   }
-  float dot = 0.f;
+  f2 g0[8], g1[8];
+  f2 sx = 0ull, sgx = 0ull;
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    float c, s;
-    rope_fast(p, ru[4 * e + qd], c, s);
-    // transpose of (x0, x1) -> (x0 c - x1 s, x0 s + x1 c)
-    g0[e] = glo[e] * c + ghi[e] * s;
-    g1[e] = ghi[e] * c - glo[e] * s;
-    dot = fmaf(g0[e], n0[e], fmaf(g1[e], n1[e], dot));
-  }
-  red[qd][i] = dot;
-  __syncthreads();
-  const float mean = (red[0][i] + red[1][i] + red[2][i] + red[3][i]) / (float)D;
-  float a[16], bq[16];
+  for (int hf = 0; hf < 2; ++hf) {
+    f2 cs[4], sn[4], nsn[4], x0[4], x1[4];
+    rope8(pos, ru, hf, qd, cs, sn, nsn);
+    unpack4x2(raw[hf], x0);
+    unpack4x2(raw[2 + hf], x1);
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    a[e] = valid ? r * (g0[e] - n0[e] * mean) : 0.f;
-    bq[e] = valid ? r * (g1[e] - n1[e] * mean) : 0.f;
+    for (int e = 0; e < 4; ++e) {
+      const f2 a = mk2(alo[8 * hf + 2 * e], alo[8 * hf + 2 * e + 1]);
+      const f2 bq = mk2(ahi[8 * hf + 2 * e], ahi[8 * hf + 2 * e + 1]);
+      // transpose of (x0, x1) -> (x0 c - x1 s, x0 s + x1 c)
+      g0[4 * hf + e] = fma2(a, cs[e], mul2(bq, sn[e]));
+      g1[4 * hf + e] = fma2(bq, cs[e], mul2(a, nsn[e]));
+      sx = fma2(x0[e], x0[e], fma2(x1[e], x1[e], sx));
+      sgx = fma2(g0[4 * hf + e], x0[e], fma2(g1[4 * hf + e], x1[e], sgx));
+    }
   }
-  *tile_at(out, i, 2 * qd) = pack8(a);
-  *tile_at(out, i, 2 * qd + 1) = pack8(a + 8);
-  *tile_at(out, i, 8 + 2 * qd) = pack8(bq);
-  *tile_at(out, i, 8 + 2 * qd + 1) = pack8(bq + 8);
+  red[0][qd][i] = hsum2(sx);
+  red[1][qd][i] = hsum2(sgx);
+  named_sync(5 + sub, 128);
+  const float r = rsqrtf((red[0][0][i] + red[0][1][i] + red[0][2][i] + red[0][3][i]) / (float)D + eps);
+  const float m = r * (red[1][0][i] + red[1][1][i] + red[1][2][i] + red[1][3][i]) / (float)D;
+  const f2 r2 = dup2(r), cx = dup2(-r * r * m);  // dL/dx = r g - r^2 m x
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    f2 x0[4], x1[4], lo[4], hi[4];
+    unpack4x2(raw[hf], x0);
+    unpack4x2(raw[2 + hf], x1);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      lo[e] = fma2(x0[e], cx, mul2(g0[4 * hf + e], r2));
+      hi[e] = fma2(x1[e], cx, mul2(g1[4 * hf + e], r2));
+    }
+    *tile_at(out, i, 2 * qd + hf) = pack4x2(lo);
+    *tile_at(out, i, 8 + 2 * qd + hf) = pack4x2(hi);
+  }
 }
-
-// Bounded wait with a CTA-wide vote (every thread calls it); on a timeout
-// every thread leaves the tile loop together.  A statement, not an expression:
-// its `break` must reach the tile loop.
-#define BWD_WAIT(bar, parity)          \
-  if (wait_all((bar), (parity))) {     \
-    failed = true;                     \
-    break;                             \
-  }
 
 // ------------------------------------------------------------------ dq pass
 
@@ -597,62 +557,10 @@ __global__ void __launch_bounds__(NTO, 1)
         if (!have) wait_or_fail(&sh.bar_m74, (n - 1) & 1, failed);
         wait_or_fail(&sh.bar_qr, (n - 1) & 1, failed);
         {
-          float alo[16], ahi[16];
-          {
-            uint32_t ra[16], rb[16];
-            umma::tmem_ld16_nowait(tap + 16 * qd, ra);
-            umma::tmem_ld16_nowait(tap + 64 + 16 * qd, rb);
-            umma::tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              alo[e] = __uint_as_float(ra[e]);
-              ahi[e] = __uint_as_float(rb[e]);
-            }
-          }
           uint4 qr[4];
           ld_pairs(Kp, i, qd, qr);
-          const long long pos = P.pos_offset + prev_c0 + i;
-          f2 g0[8], g1[8];
-          f2 sq = 0ull, sgq = 0ull;
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            f2 cs[4], sn[4], nsn[4], x0[4], x1[4];
-            rope8(pos, sh.ru, hf, qd, cs, sn, nsn);
-            unpack4x2(qr[hf], x0);
-            unpack4x2(qr[2 + hf], x1);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const f2 a = mk2(alo[8 * hf + 2 * e], alo[8 * hf + 2 * e + 1]);
-              const f2 bq = mk2(ahi[8 * hf + 2 * e], ahi[8 * hf + 2 * e + 1]);
-              // transpose of (x0, x1) -> (x0 c - x1 s, x0 s + x1 c)
-              g0[4 * hf + e] = fma2(a, cs[e], mul2(bq, sn[e]));
-              g1[4 * hf + e] = fma2(bq, cs[e], mul2(a, nsn[e]));
-              sq = fma2(x0[e], x0[e], fma2(x1[e], x1[e], sq));
-              sgq = fma2(g0[4 * hf + e], x0[e], fma2(g1[4 * hf + e], x1[e], sgq));
-            }
-          }
-          sh.red_dq[0][qd][i] = hsum2(sq);
-          sh.red_dq[1][qd][i] = hsum2(sgq);
-          named_sync(5 + sub, 128);
-          const float r = rsqrtf((sh.red_dq[0][0][i] + sh.red_dq[0][1][i] + sh.red_dq[0][2][i] +
-                                  sh.red_dq[0][3][i]) / (float)D + P.eps);
-          const float m = r * (sh.red_dq[1][0][i] + sh.red_dq[1][1][i] + sh.red_dq[1][2][i] +
-                               sh.red_dq[1][3][i]) / (float)D;
-          // dq = r g - r^2 m q
-          const f2 r2 = dup2(r), cq = dup2(-r * r * m);
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            f2 x0[4], x1[4], lo[4], hi[4];
-            unpack4x2(qr[hf], x0);
-            unpack4x2(qr[2 + hf], x1);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              lo[e] = fma2(x0[e], cq, mul2(g0[4 * hf + e], r2));
-              hi[e] = fma2(x1[e], cq, mul2(g1[4 * hf + e], r2));
-            }
-            *tile_at(Kp, i, 2 * qd + hf) = pack4x2(lo);
-            *tile_at(Kp, i, 8 + 2 * qd + hf) = pack4x2(hi);
-          }
+          feature_grad_pairs(tap, qr, 1.f, P.pos_offset + prev_c0 + i, i, qd, sub, P.eps, sh.ru,
+                             sh.red_dq, Kp);
         }
         warp_arrive(&sh.bar_w6, lane);
       } else if (have) {
@@ -710,234 +618,349 @@ __global__ void __launch_bounds__(NTO, 1)
 
 // ------------------------------------------------------------------ dk / dv pass
 
-__global__ void __launch_bounds__(NT, 1)
+struct DkdvShared {
+  unsigned long long ru[kMaxPairs];  // RoPE phase increments (load_rope_table)
+  float red_dk[2][4][ROWS];  // [V6b] quarter parts of sum k^2 and sum g.k of each row
+  float qk_diag[ROWS];       // [V1] -> [V3] fp32 k~_i . q~_i of the tile
+  float pw[ROWS + 1];
+  alignas(16) float du[4][DM_STRIDE];  // transposed causal-mask table (fill_mask_table_upper)
+  uint64_t bar_q, bar_k, bar_v, bar_dot;                    // TMA loads of q, k, v, dO
+  uint64_t bar_m1, bar_m2, bar_dv, bar_dk, bar_eupd;        // MMA commits
+  uint64_t bar_feat, bar_eb, bar_x, bar_xp, bar_dvout, bar_qw, bar_dkout;  // workers
+  uint32_t tmem_base;
+  uint32_t failed;
+};
+
+// dk / dv pass, warp-specialized, over the tiles of a segment in reverse, with
+// E (the gradient reaching the state from later tokens) carried in TMEM:
+//   M1   = K~ Q~^T (fp16)                       into tA
+//   M2   = V dO^T                               into tB
+//   dV   = X dO + K~dec Eb,    X  = M1 (.) D^T  (fp32 k~_i . q~_i on the diagonal)
+//   dK~  = X' Q~ + Vdec Eb^T,  X' = M2 (.) D^T  (fp32 v_i . do_i on the diagonal)
+//   E   <- gamma^c E + Q~w^T dO,  Q~w = diag(gamma^{i+1}) Q~
+// with D^T_ij = gamma^{j-i} for j >= i, K~dec / Vdec rows scaled by gamma^{c-1-i}
+// and Eb = bf16(E) at the tile's end.  Worker warps, per tile:
+//   [V1] q~, k~ (fp16, in place)             [V2] Eb, E <- gamma^c E
+//   [V3] X -> X, k~ -> K~dec                  [V4] Vdec, q~ -> bf16, X' -> X once dV is done
+//   [V5] dv -> K (over K~dec)                 [V6] q~ -> Q~w, then dk (RoPE^T, RMSNorm
+//                                                  backward against raw k) -> V (over Vdec)
+// The issuer warp issues the MMAs as their operands are ready, stores dv and dk
+// by TMA and refills Q, K, V and dO for the tile before as each is freed.  Raw
+// k for the RMSNorm backward and the v . do diagonal are plain loads.
+__global__ void __launch_bounds__(NTO, 1)
     tc_bwd_dkdv_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmq,
                        const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                        const __grid_constant__ CUtensorMap tmo, const __grid_constant__ CUtensorMap tmdk,
                        const __grid_constant__ CUtensorMap tmdv) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  // Q: raw q -> q~ (fp16) -> q~ (bf16) -> q~w.  K: raw k -> k~ (fp16) -> k~dec,
-  // then dv (TMA-stored).  V: v -> vdec, then dk (TMA-stored).  DO: do.
-  // EB: E (bf16).  X: M1 (.) D^T, then M2 (.) D^T.
+  // Q: raw q -> q~ (fp16) -> q~ (bf16) -> Q~w.  K: raw k -> k~ (fp16) -> K~dec -> dv.
+  // V: v -> Vdec -> dk.  DO: dO.  EB: Eb.  X: X, then X'.
   unsigned char *Qt = base, *Kt = base + TILE, *Vt = base + 2 * TILE, *DOt = base + 3 * TILE;
   unsigned char *EB = base + 4 * TILE, *X = base + 5 * TILE;
-  BwdShared &sh = *reinterpret_cast<BwdShared *>(base + 6 * TILE);
-  uint64_t *bar_q = &sh.bar_tma[0], *bar_k = &sh.bar_tma[1], *bar_v = &sh.bar_tma[2],
-           *bar_do = &sh.bar_tma[3];
+  DkdvShared &sh = *reinterpret_cast<DkdvShared *>(base + 6 * TILE);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int sub = warp & 3, qd = warp >> 2, i = 32 * sub + lane;
   const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int t0 = g * P.seg_len, t1 = min(P.T, t0 + P.seg_len);
   const int CV = P.chunk;
   const int ntile = ceil_div(t1 - t0, CV);
-  const float gm = P.gamma[h];
-  const float l2g = log2f(gm);
+  const float l2g = log2f(P.gamma[h]);
   const uint32_t tile_bytes = (uint32_t)CV * D * 2;
 
   if (tid == 0) {
-    for (int j = 0; j < 5; ++j) umma::mbar_init(&sh.bar_tma[j], 1);
-    for (int j = 0; j < 6; ++j) umma::mbar_init(&sh.bar_mma[j], 1);
+    uint64_t *bars[] = {&sh.bar_q, &sh.bar_k, &sh.bar_v, &sh.bar_dot, &sh.bar_m1,
+                        &sh.bar_m2, &sh.bar_dv, &sh.bar_dk, &sh.bar_eupd};
+    for (uint64_t *bar : bars) umma::mbar_init(bar, 1);
+    uint64_t *wbars[] = {&sh.bar_feat, &sh.bar_eb, &sh.bar_x, &sh.bar_xp,
+                         &sh.bar_dvout, &sh.bar_qw, &sh.bar_dkout};
+    for (uint64_t *bar : wbars) umma::mbar_init(bar, NWORK);
     umma::mbar_fence_init();
+    sh.failed = 0;
   }
   if (tid <= ROWS) sh.pw[tid] = exp2f((float)tid * l2g);
+  fill_mask_table_upper(sh.du, l2g, tid, NTO);
   load_rope_table(sh.ru, P, tid);
   if (warp == 0) umma::tmem_alloc(&sh.tmem_base, 512);
   if (CV < ROWS)  // rows [CV, 128) of V and DO are never written by TMA: clear them once
-    for (int e = tid; e < 2 * (ROWS - CV) * 16; e += NT) {
+    for (int e = tid; e < 2 * (ROWS - CV) * 16; e += NTO) {
       const int r = e % ((ROWS - CV) * 16);
       *tile_at(e < (ROWS - CV) * 16 ? Vt : DOt, CV + r / 16, r % 16) = make_uint4(0, 0, 0, 0);
     }
   sync_tc();
   const uint32_t tm = sh.tmem_base;
-  const uint32_t lb = (uint32_t)(32 * sub) << 16, col = 32 * qd;
-  const uint32_t tA = tm + lb, tB = tm + 128 + lb, tE = tm + 256 + lb;
-  {  // gradient reaching the segment's last state from later tokens -> TMEM
-    const float *ein = P.seg2 + (((size_t)b * P.H + h) * P.nseg + g) * (size_t)D * D;
-    const float4 *s4 = reinterpret_cast<const float4 *>(ein + (size_t)i * D + col);
-    float v[32];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float4 x = s4[u];
-      v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
-    }
-    umma::tmem_st32(tE + col, v);
-    umma::tmem_wait_st();
-  }
-  if (tid == 0) {
-    const int cl = t0 + (ntile - 1) * CV;
-    umma::mbar_expect_tx(bar_q, tile_bytes);
-    tma_tile(Qt, &tmq, b, h, cl, bar_q);
-    umma::mbar_expect_tx(bar_k, tile_bytes);
-    tma_tile(Kt, &tmk, b, h, cl, bar_k);
-    umma::mbar_expect_tx(bar_v, tile_bytes);
-    tma_tile(Vt, &tmv, b, h, cl, bar_v);
-    umma::mbar_expect_tx(bar_do, tile_bytes);
-    tma_tile(DOt, &tmo, b, h, cl, bar_do);
-  }
-  const uint32_t id_kq16 = umma::idesc_bf16(128, 128, false, false, true);
-  const uint32_t id_kmn = umma::idesc_bf16(128, 128, false, true);
-  const uint32_t id_kk = umma::idesc_bf16(128, 128, false, false);
-  const uint32_t id_mnmn = umma::idesc_bf16(128, 128, true, true);
-  const uint32_t aQ = umma::smem_u32(Qt), aK = umma::smem_u32(Kt), aV = umma::smem_u32(Vt),
-                 aDO = umma::smem_u32(DOt), aE = umma::smem_u32(EB), aX = umma::smem_u32(X);
-
+  const uint32_t tA = tm, tB = tm + 128, tE = tm + 256;
   bool failed = false;
-  for (int it = 0; it < ntile; ++it) {
-    const int n = ntile - 1 - it;
-    const uint32_t ph = it & 1;
-    const int c0 = t0 + n * CV, c = min(CV, t1 - c0);
-    const bool valid = i < c;
-    const long long pos = P.pos_offset + c0 + i;
-    const float wdec = valid ? sh.pw[c - 1 - i] : 0.f;
 
-    // [1] q~, k~ (fp16, in place); EB = bf16(E); E <- gamma^c E
-    BWD_WAIT(bar_q, ph);
-    BWD_WAIT(bar_k, ph);
-    float rk;
-    {
-      uint4 qr[4], kr[4];
-      ld_pairs(Qt, i, qd, qr);
-      ld_pairs(Kt, i, qd, kr);
-      if (!valid) qr[0] = qr[1] = qr[2] = qr[3] = kr[0] = kr[1] = kr[2] = kr[3] = make_uint4(0, 0, 0, 0);
-      sh.red[qd][i] = sumsq_pairs(qr);
-      sh.red2[qd][i] = sumsq_pairs(kr);
-      float ev[32];
-      umma::tmem_ld2x16(tE + col, ev);
-      store_quarter(EB, i, qd, ev);
-      const float carry = sh.pw[c];
+  if (warp >= NWORK) {
+    // ---------------------------------------------------------------- issuer warpgroup
+    if (warp == NWORK && lane == 0) {
+      const uint32_t id_kq16 = umma::idesc_bf16(128, 128, false, false, true);  // fp16 K~ Q~^T
+      const uint32_t id_kmn = umma::idesc_bf16(128, 128, false, true);
+      const uint32_t id_kk = umma::idesc_bf16(128, 128, false, false);
+      const uint32_t id_mnmn = umma::idesc_bf16(128, 128, true, true);
+      const uint32_t aQ = umma::smem_u32(Qt), aK = umma::smem_u32(Kt), aV = umma::smem_u32(Vt),
+                     aDO = umma::smem_u32(DOt), aE = umma::smem_u32(EB), aX = umma::smem_u32(X);
+      {
+        const int cl = t0 + (ntile - 1) * CV;
+        umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
+        tma_tile(Qt, &tmq, b, h, cl, &sh.bar_q);
+        umma::mbar_expect_tx(&sh.bar_k, tile_bytes);
+        tma_tile(Kt, &tmk, b, h, cl, &sh.bar_k);
+        umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
+        tma_tile(Vt, &tmv, b, h, cl, &sh.bar_v);
+        umma::mbar_expect_tx(&sh.bar_dot, tile_bytes);
+        tma_tile(DOt, &tmo, b, h, cl, &sh.bar_dot);
+      }
+      for (int it = 0; it < ntile; ++it) {
+        const int n = ntile - 1 - it;
+        const uint32_t ph = it & 1;
+        const int c0 = t0 + n * CV;
+        wait_or_fail(&sh.bar_feat, ph, failed);
+        if (!failed) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) ev[e] *= carry;
-      umma::tmem_st32(tE + col, ev);
-      __syncthreads();
-      const float rq = rsqrtf((sh.red[0][i] + sh.red[1][i] + sh.red[2][i] + sh.red[3][i]) / (float)D + P.eps);
-      rk = rsqrtf((sh.red2[0][i] + sh.red2[1][i] + sh.red2[2][i] + sh.red2[3][i]) / (float)D + P.eps);
-      sh.qk_diag[qd][i] = feature_qk_store(qr, kr, rq, rk * P.kscale, pos, qd, sh.ru, Qt, Kt, i);
+          for (int kk = 0; kk < 8; ++kk)  // M1 = K~ Q~^T
+            umma::mma_ss(tA, umma::desc_kmajor(aK, kk, ROWS), umma::desc_kmajor(aQ, kk, ROWS), id_kq16, kk > 0);
+          umma::commit(&sh.bar_m1);
+        }
+        wait_or_fail(&sh.bar_v, ph, failed);
+        wait_or_fail(&sh.bar_dot, ph, failed);
+        if (!failed) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // M2 = V dO^T
+            umma::mma_ss(tB, umma::desc_kmajor(aV, kk, ROWS), umma::desc_kmajor(aDO, kk, ROWS), id_kk, kk > 0);
+          umma::commit(&sh.bar_m2);
+          if (n > 0) {  // the tile before into L2 ahead of its copies
+            tma_prefetch_tile(&tmq, b, h, c0 - CV);
+            tma_prefetch_tile(&tmk, b, h, c0 - CV);
+            tma_prefetch_tile(&tmv, b, h, c0 - CV);
+            tma_prefetch_tile(&tmo, b, h, c0 - CV);
+          }
+        }
+        wait_or_fail(&sh.bar_x, ph, failed);
+        wait_or_fail(&sh.bar_eb, ph, failed);
+        if (!failed) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dV = X dO
+            umma::mma_ss(tA, umma::desc_kmajor(aX, kk, ROWS), umma::desc_mnmajor(aDO, kk, ROWS), id_kmn, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dV += K~dec Eb
+            umma::mma_ss(tA, umma::desc_kmajor(aK, kk, ROWS), umma::desc_mnmajor(aE, kk, ROWS), id_kmn, 1u);
+          umma::commit(&sh.bar_dv);
+        }
+        wait_or_fail(&sh.bar_xp, ph, failed);
+        if (!failed) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dK~ = X' Q~
+            umma::mma_ss(tB, umma::desc_kmajor(aX, kk, ROWS), umma::desc_mnmajor(aQ, kk, ROWS), id_kmn, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dK~ += Vdec Eb^T
+            umma::mma_ss(tB, umma::desc_kmajor(aV, kk, ROWS), umma::desc_kmajor(aE, kk, ROWS), id_kk, 1u);
+          umma::commit(&sh.bar_dk);
+        }
+        wait_or_fail(&sh.bar_dvout, ph, failed);
+        if (!failed) {
+          tma_store_tile(&tmdv, Kt, b, h, c0);
+          umma::bulk_commit();
+        }
+        wait_or_fail(&sh.bar_qw, ph, failed);
+        if (!failed) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // E += Q~w^T dO
+            umma::mma_ss(tE, umma::desc_mnmajor(aQ, kk, ROWS), umma::desc_mnmajor(aDO, kk, ROWS), id_mnmn, 1u);
+          umma::commit(&sh.bar_eupd);
+        }
+        // E update done (on the last tile too: TMEM is freed at the end): Q and DO
+        // take the tile before; once the dv store has left K, so does K
+        wait_or_fail(&sh.bar_eupd, ph, failed);
+        if (n > 0) {
+          if (!failed) {
+            umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
+            tma_tile(Qt, &tmq, b, h, c0 - CV, &sh.bar_q);
+            umma::mbar_expect_tx(&sh.bar_dot, tile_bytes);
+            tma_tile(DOt, &tmo, b, h, c0 - CV, &sh.bar_dot);
+            umma::bulk_wait_read();
+            umma::mbar_expect_tx(&sh.bar_k, tile_bytes);
+            tma_tile(Kt, &tmk, b, h, c0 - CV, &sh.bar_k);
+          }
+        }
+        // dk out of V, then V takes the tile before
+        wait_or_fail(&sh.bar_dkout, ph, failed);
+        if (!failed) {
+          tma_store_tile(&tmdk, Vt, b, h, c0);
+          umma::bulk_commit();
+          if (n > 0) {
+            umma::bulk_wait_read();
+            umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
+            tma_tile(Vt, &tmv, b, h, c0 - CV, &sh.bar_v);
+          }
+        }
+      }
+      umma::bulk_wait_all();
+    }
+  } else {
+    // ---------------------------------------------------------------- worker warps
+    const int sub = warp & 3, qd = warp >> 2, i = 32 * sub + lane;  // TMEM phases
+    const int fr = 8 * warp + (lane >> 2), fu = lane & 3;           // feature map: row, quarter
+    const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
+    const uint32_t col = 32 * qd;
+    {  // gradient reaching the segment's last state from later tokens -> TMEM
+      const float *ein = P.seg2 + (((size_t)b * P.H + h) * P.nseg + g) * (size_t)D * D;
+      const float4 *s4 = reinterpret_cast<const float4 *>(ein + (size_t)i * D + col);
+      float v[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float4 x = s4[u];
+        v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
+      }
+      umma::tmem_st32(tE + lane_base + col, v);
       umma::tmem_wait_st();
     }
-    umma::fence_async_smem();
-    umma::fence_before();
-    BWD_WAIT(bar_v, ph);
-    BWD_WAIT(bar_do, ph);
-    if (tid == 0) {
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // M1 = K~ Q~^T (fp16)
-        umma::mma_ss(tm, umma::desc_kmajor(aK, kk, ROWS), umma::desc_kmajor(aQ, kk, ROWS), id_kq16, kk > 0);
-      umma::commit(&sh.bar_mma[0]);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // M2 = V dO^T
-        umma::mma_ss(tm + 128, umma::desc_kmajor(aV, kk, ROWS), umma::desc_kmajor(aDO, kk, ROWS), id_kk, kk > 0);
-      umma::commit(&sh.bar_mma[1]);
-    }
+    for (int it = 0; it < ntile; ++it) {
+      const int n = ntile - 1 - it;
+      const uint32_t ph = it & 1;
+      const int c0 = t0 + n * CV, c = min(CV, t1 - c0);
+      const bool valid = i < c;
+      const long long pos = P.pos_offset + c0 + i;
+      const float wdec = valid ? sh.pw[c - 1 - i] : 0.f;
 
-    // [2] X = bf16(M1 (.) D^T); k~ -> k~dec
-    BWD_WAIT(&sh.bar_mma[0], ph);
-    {
-      float v[32];
-      mask_upper_block(tA + col, v, i, sub, qd, c, valid, gm, sh.pw, true,
-                       diag_sum(sh.qk_diag, i));  // fp32 k~_i . q~_i on the diagonal
-      store_quarter(X, i, qd, v);
-      rescale_quarter(Kt, i, qd, wdec, true);
-    }
-    umma::fence_async_smem();
-    sync_tc();
-    if (tid == 0) {
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // dV = X dO
-        umma::mma_ss(tm, umma::desc_kmajor(aX, kk, ROWS), umma::desc_mnmajor(aDO, kk, ROWS), id_kmn, kk > 0);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // dV += K~dec E
-        umma::mma_ss(tm, umma::desc_kmajor(aK, kk, ROWS), umma::desc_mnmajor(aE, kk, ROWS), id_kmn, 1u);
-      umma::commit(&sh.bar_mma[2]);
-    }
+      // [V1] q~, k~ (fp16, in place): row fr, pairs [16 fu, 16 fu + 16)
+      wait_or_fail(&sh.bar_q, ph, failed);
+      wait_or_fail(&sh.bar_k, ph, failed);
+      {
+        uint4 qr[4], kr[4];
+        ld_pairs(Qt, fr, fu, qr);
+        ld_pairs(Kt, fr, fu, kr);
+        if (!(fr < c))
+          qr[0] = qr[1] = qr[2] = qr[3] = kr[0] = kr[1] = kr[2] = kr[3] = make_uint4(0, 0, 0, 0);
+        float sq, sk, qk;
+        norms_and_dot(qr, kr, sq, sk, qk);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+        sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+        qk += __shfl_xor_sync(0xffffffffu, qk, 1);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+        sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+        qk += __shfl_xor_sync(0xffffffffu, qk, 2);
+        const float rq = rsqrtf(sq / (float)D + P.eps);
+        const float rk = rsqrtf(sk / (float)D + P.eps) * P.kscale;
+        if (fu == 0) sh.qk_diag[fr] = qk * rq * rk;
+        feature_qk_store(qr, kr, rq, rk, P.pos_offset + c0 + fr, fu, sh.ru, Qt, Kt, fr);
+      }
+      warp_arrive(&sh.bar_feat, lane);
 
-    // [3] M2 (.) D^T (held in registers until X is free); v -> vdec; q~ -> bf16
-    BWD_WAIT(&sh.bar_mma[1], ph);
-    uint4 kraw[4];  // raw k pairs of row i for the dk epilogue
-    load_pairs(kraw, row_ptr(P.k, P, b, h, valid ? c0 + i : c0), qd, valid);
-    {
-      float v[32];
-      // fp32 v_i . do_i on the diagonal, kept by the dq pass
-      const float vd = (qd == sub && valid) ? P.ddiag[((size_t)b * P.T + c0 + i) * P.H + h] : 0.f;
-      mask_upper_block(tB + col, v, i, sub, qd, c, valid, gm, sh.pw, true, vd);
-      rescale_quarter(Vt, i, qd, wdec, false);
-      rescale_quarter(Qt, i, qd, 1.f, true);
-      BWD_WAIT(&sh.bar_mma[2], ph);  // dV done: X and K are free
-      store_quarter(X, i, qd, v);
-    }
-    {  // dv of this tile (dV is complete) -> K, for a TMA store
-      float v[32];
-      umma::tmem_ld2x16(tA + col, v);
-      store_quarter(Kt, i, qd, v);
-    }
-    umma::fence_async_smem();
-    sync_tc();
-    if (tid == 0) {
+      // [V2] after the E update of the tile after: Eb = bf16(E), E <- gamma^c E
+      if (it > 0) wait_or_fail(&sh.bar_eupd, (it - 1) & 1, failed);
+      {
+        float ev[32];
+        umma::tmem_ld2x16(tE + lane_base + col, ev);
+        f2 x[16];
+        pairs_of(ev, x);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // dK~ = X Q~
-        umma::mma_ss(tm + 128, umma::desc_kmajor(aX, kk, ROWS), umma::desc_mnmajor(aQ, kk, ROWS), id_kmn, kk > 0);
+        for (int u = 0; u < 4; ++u) *tile_at(EB, i, 4 * qd + u) = pack4x2(&x[4 * u]);
+        const f2 carry = dup2(sh.pw[c]);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // dK~ += V~dec E^T
-        umma::mma_ss(tm + 128, umma::desc_kmajor(aV, kk, ROWS), umma::desc_kmajor(aE, kk, ROWS), id_kk, 1u);
-      umma::commit(&sh.bar_mma[3]);
-      tma_store_tile(&tmdv, Kt, b, h, c0);
-      umma::bulk_commit();
-    }
+        for (int e = 0; e < 16; ++e) x[e] = mul2(x[e], carry);
+        floats_of(x, ev);
+        umma::tmem_st32(tE + lane_base + col, ev);
+        umma::tmem_wait_st();
+      }
+      warp_arrive(&sh.bar_eb, lane);
 
-    // [4] q~ -> q~w = gamma^{i+1} q~; E += q~w^T dO; dk epilogue overlaps it
-    BWD_WAIT(&sh.bar_mma[3], ph);
-    rescale_quarter(Qt, i, qd, sh.pw[i + 1], false);
-    umma::fence_async_smem();
-    sync_tc();
-    if (tid == 0) {
+      // [V3] after M1: X = bf16(M1 (.) D^T) with the fp32 diagonal; k~ -> K~dec
+      wait_or_fail(&sh.bar_m1, ph, failed);
+      {
+        float v[32];
+        umma::tmem_ld2x16(tA + lane_base + col, v);
+        f2 x[16];
+        pairs_of(v, x);
+        mask_upper_table(x, sh.du, i, (int)col);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // E += Q~w^T dO
-        umma::mma_ss(tm + 256, umma::desc_mnmajor(aQ, kk, ROWS), umma::desc_mnmajor(aDO, kk, ROWS), id_mnmn, 1u);
-      umma::commit(&sh.bar_mma[4]);
-      umma::bulk_wait_read();  // dv has left K
-      if (n > 0) {
-        umma::mbar_expect_tx(bar_k, tile_bytes);
-        tma_tile(Kt, &tmk, b, h, c0 - CV, bar_k);
-      }
-    }
-    {
-      float glo[16], ghi[16];
-      tmem_ld_pairs(tB, qd, glo, ghi);
+        for (int u = 0; u < 4; ++u) *tile_at(X, i, 4 * qd + u) = pack4x2(&x[4 * u]);
+        if (qd == sub)  // written in [V1] by warps 4 sub .. 4 sub + 3, ordered by bar_feat -> M1
+          *(reinterpret_cast<__nv_bfloat16 *>(tile_at(X, i, i >> 3)) + (i & 7)) =
+              __float2bfloat16_rn(sh.qk_diag[i]);
+        const f2 w = dup2(wdec);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        glo[e] *= P.kscale;
-        ghi[e] *= P.kscale;
+        for (int u = 0; u < 4; ++u) {
+          uint4 *p = tile_at(Kt, i, 4 * qd + u);
+          f2 f[4];
+          unpack4x2h(*p, f);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) f[e] = mul2(f[e], w);
+          *p = pack4x2(f);
+        }
       }
-      feature_grad_row(glo, ghi, kraw, rk, pos, i, qd, valid, sh.ru, sh.red, Vt);  // v~dec is dead
-    }
-    umma::fence_async_smem();
-    BWD_WAIT(&sh.bar_mma[4], ph);
-    if (tid == 0) {  // E update done: Q and DO are free; dk out, then V is free
-      if (n > 0) {
-        umma::mbar_expect_tx(bar_q, tile_bytes);
-        tma_tile(Qt, &tmq, b, h, c0 - CV, bar_q);
-        umma::mbar_expect_tx(bar_do, tile_bytes);
-        tma_tile(DOt, &tmo, b, h, c0 - CV, bar_do);
+      warp_arrive(&sh.bar_x, lane);
+
+      // [V4] after M2: Vdec, q~ -> bf16; X' = M2 (.) D^T (fp32 v_i . do_i on the
+      // diagonal, from the dq pass) into X once dV has read X
+      {
+        const float vdiag = (qd == sub && valid) ? P.ddiag[((size_t)b * P.T + c0 + i) * P.H + h] : 0.f;
+        wait_or_fail(&sh.bar_m2, ph, failed);
+        const f2 w = dup2(wdec);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint4 *p = tile_at(Vt, i, 4 * qd + u);
+          f2 f[4];
+          unpack4x2(*p, f);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) f[e] = mul2(f[e], w);
+          *p = pack4x2(f);
+          uint4 *pq = tile_at(Qt, i, 4 * qd + u);
+          unpack4x2h(*pq, f);
+          *pq = pack4x2(f);
+        }
+        float v[32];
+        umma::tmem_ld2x16(tB + lane_base + col, v);
+        f2 x[16];
+        pairs_of(v, x);
+        mask_upper_table(x, sh.du, i, (int)col);
+        wait_or_fail(&sh.bar_dv, ph, failed);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) *tile_at(X, i, 4 * qd + u) = pack4x2(&x[4 * u]);
+        if (qd == sub) *(reinterpret_cast<__nv_bfloat16 *>(tile_at(X, i, i >> 3)) + (i & 7)) = __float2bfloat16_rn(vdiag);
       }
-      tma_store_tile(&tmdk, Vt, b, h, c0);
-      umma::bulk_commit();
-      umma::bulk_wait_read();
-      if (n > 0) {
-        umma::mbar_expect_tx(bar_v, tile_bytes);
-        tma_tile(Vt, &tmv, b, h, c0 - CV, bar_v);
+      warp_arrive(&sh.bar_xp, lane);
+
+      // [V5] dv (dV is complete) -> K over K~dec, for a TMA store
+      uint4 kraw[4];  // raw k pairs of row i for [V6], in flight meanwhile
+      load_pairs(kraw, row_ptr(P.k, P, b, h, valid ? c0 + i : c0), qd, valid);
+      {
+        float v[32];
+        umma::tmem_ld2x16(tA + lane_base + col, v);
+        f2 x[16];
+        pairs_of(v, x);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) *tile_at(Kt, i, 4 * qd + u) = pack4x2(&x[4 * u]);
       }
+      warp_arrive(&sh.bar_dvout, lane);
+
+      // [V6] after dK~: q~ -> Q~w = gamma^{i+1} q~ for the E update, then dk
+      wait_or_fail(&sh.bar_dk, ph, failed);
+      {
+        const f2 w = dup2(sh.pw[i + 1]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint4 *p = tile_at(Qt, i, 4 * qd + u);
+          f2 f[4];
+          unpack4x2(*p, f);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) f[e] = mul2(f[e], w);
+          *p = pack4x2(f);
+        }
+      }
+      warp_arrive(&sh.bar_qw, lane);
+      feature_grad_pairs(tB + lane_base, kraw, P.kscale, pos, i, qd, sub, P.eps, sh.ru, sh.red_dk, Vt);
+      warp_arrive(&sh.bar_dkout, lane);
     }
   }
-  if (tid == 0) umma::bulk_wait_all();
-  if (failed && tid == 0 && P.err) atomicOr(P.err, 8u);
+  if (failed) atomicOr(&sh.failed, 1u);
   sync_tc();
+  if (sh.failed && tid == 0 && P.err) atomicOr(P.err, 8u);
   if (warp == 0) umma::tmem_dealloc(tm, 512);
 }
 
-#undef BWD_WAIT
-
-constexpr size_t kBwdSmem = 6 * TILE + sizeof(BwdShared) + 1024;
+constexpr size_t kBwdSmem = 6 * TILE + sizeof(DkdvShared) + 1024;
 static_assert(kBwdSmem <= 232448, "dk/dv pass exceeds 227 KiB of shared memory per CTA");
 constexpr size_t kDqSmem = 6 * TILE + sizeof(DqShared) + 1024;
 static_assert(kDqSmem <= 232448, "dq pass exceeds 227 KiB of shared memory per CTA");
@@ -975,7 +998,7 @@ cudaError_t launch_tc_bwd_dkdv(const MixerParams &P, cudaStream_t st) {
   e = cudaFuncSetAttribute(tc::tc_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)tc::kBwdSmem);
   if (e != cudaSuccess) return e;
-  tc::tc_bwd_dkdv_kernel<<<dim3(P.nseg, P.H, P.B), tc::NT, tc::kBwdSmem, st>>>(P, mq, mk, mv, mo, mdk, mdv);
+  tc::tc_bwd_dkdv_kernel<<<dim3(P.nseg, P.H, P.B), tc::NTO, tc::kBwdSmem, st>>>(P, mq, mk, mv, mo, mdk, mdv);
   return cudaGetLastError();
 }
 

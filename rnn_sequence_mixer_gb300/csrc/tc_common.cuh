@@ -339,6 +339,31 @@ __device__ __forceinline__ void mask_lower_table(f2 (&x)[16], const float (*dm)[
   }
 }
 
+// The transposed mask's table: du[cp][y] = gamma^(y + cp - 127) for
+// y + cp >= 127, else 0 (same layout and padding as fill_mask_table).
+__device__ __forceinline__ void fill_mask_table_upper(float (*du)[DM_STRIDE], float log2g, int tid,
+                                                      int nthreads) {
+  for (int e = tid; e < 4 * DM_STRIDE; e += nthreads) {
+    const int cp = e / DM_STRIDE, x = e % DM_STRIDE + cp;
+    du[cp][e % DM_STRIDE] = x >= ROWS - 1 ? exp2f((float)(x - (ROWS - 1)) * log2g) : 0.f;
+  }
+}
+
+// Transposed causal decay of columns [col, col + 32) of row i, in place:
+// x_j *= gamma^(j - i) for j >= i, 0 for j < i.  The weight of column col + e
+// is du[cp][s - cp + e] with s = 127 + col - i, cp = s & 3.
+__device__ __forceinline__ void mask_upper_table(f2 (&x)[16], const float (*du)[DM_STRIDE], int i,
+                                                 int col) {
+  const int s = ROWS - 1 + col - i, cp = s & 3;
+  const float4 *wt = reinterpret_cast<const float4 *>(&du[cp][s - cp]);
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const float4 w = wt[u];
+    x[2 * u] = mul2(x[2 * u], mk2(w.x, w.y));
+    x[2 * u + 1] = mul2(x[2 * u + 1], mk2(w.z, w.w));
+  }
+}
+
 // RoPE of one 8-element chunk pair, two fp32 lanes at a time: lo = x0 c - x1 s,
 // hi = x0 s + x1 c for x0 = a r, x1 = b r (a: first-half elements, b: their
 // partners d/2 further on).  cs / sn / nsn hold cos, sin and -sin of the 8 angles.
