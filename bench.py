@@ -519,24 +519,26 @@ def run_ours(args):
             api.prefill(ib["q"], ib["k"], ib["v"], ib["gate"], gb, chunk=wb.chunk,
                         rope_base=wb.rope_base, eps=wb.eps, y=yb, want_state=False, workspace=wsf,
                         trace=trace[:4] if trace else None)
+            # the backward reads the segment states the forward left in its
+            # workspace (saved for backward) instead of recomputing them
             api.prefill_backward(ib["q"], ib["k"], ib["v"], ib["gate"], gb, ib["dy"],
                                  chunk=wb.chunk, rope_base=wb.rope_base, eps=wb.eps, workspace=wsb,
-                                 trace=trace[4:] if trace else None)
+                                 trace=trace[4:] if trace else None, fwd_workspace=wsf)
 
         b_steps = max(1, min(args.steps, 5))
         b_ms, b_passes = timed(fb_step, b_steps, 1, stream, D, trace_count=11)
-        launches += 9 * b_steps
+        launches += 7 * b_steps  # forward 3, backward 4 (its state pass and scan are skipped)
         b_ms = D.max(b_ms)
-        b_names = ["fwd.seg_state", "fwd.state_scan", "fwd.seg_output", None, "bwd.seg_state",
-                   "bwd.state_scan", "bwd.dq", "bwd.seg_gstate", "bwd.grad_scan", "bwd.dkdv"]
+        b_names = ["fwd.seg_state", "fwd.state_scan", "fwd.seg_output", None, None, None,
+                   "bwd.dq", "bwd.seg_gstate", "bwd.grad_scan", "bwd.dkdv"]
         b_pass_ms = {nm: statistics.median(p[j] for p in b_passes)
                      for j, nm in enumerate(b_names) if nm}
         thb = wb.B * wb.T * wb.H
         alg_b = thb * (5 * wb.d * BF16 + 9 * wb.d * BF16)  # fwd 5 d-rows + bwd 5 in / 4 out
-        # tensor-core work: 21 MMAs of 128 x 128 x 128 per 128-token tile and head
-        # (forward: local state 1 + output 4; backward: local state 1, dq pass 7,
-        # state-gradient sums 1, dk/dv pass 7)
-        flops_b = 21 * 2.0 * 128 ** 3 * thb / 128
+        # tensor-core work: 20 MMAs of 128 x 128 x 128 per 128-token tile and head
+        # (forward: local state 1 + output 4; backward: dq pass 7, state-gradient
+        # sums 1, dk/dv pass 7)
+        flops_b = 20 * 2.0 * 128 ** 3 * thb / 128
         roof_ms = max(alg_b / (hbm_peak * 1e9), flops_b / (tc_peak * 1e12)) * 1e3
         out["fwd_bwd"] = {"workload": wb.name, "chunk": wb.chunk, "ms_per_step": b_ms,
                           "Mtok_s": job_rate(wb.B * wb.T, b_ms, D.world) / 1e6,

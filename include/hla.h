@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define HLA_ABI_VERSION 1
+#define HLA_ABI_VERSION 2
 
 typedef enum {
   HLA_OK = 0,
@@ -210,15 +210,25 @@ size_t hla_backward_workspace_size(const hla_shape *shape);
  *                    as for hla_prefill, its last 256 bytes hold the device
  *                    status word (non-zero after completion: a bounded wait
  *                    gave up and the gradients are not valid)
- * The forward quantities it needs (o and the per-chunk states) are
- * recomputed, not stored by hla_prefill.
+ *   trace            optional pass events (see hla_trace); NULL = none
+ *   fwd_ws           optional: the workspace of an hla_prefill call with the
+ *                    same shape, q, k, v, gamma and state_in, already enqueued
+ *                    before this call (same stream, or ordered by the caller)
+ *                    and not reused since.  That call left the state entering
+ *                    every segment in it, and the backward reads them instead
+ *                    of recomputing them (it skips two of its passes).  Read
+ *                    only.  NULL = recompute.  Passing a workspace that does
+ *                    not hold those states gives wrong gradients; nothing can
+ *                    check it.
+ * o and the per-chunk states inside a segment are always recomputed; hla_prefill
+ * stores neither.
  */
 hla_status hla_prefill_backward(const hla_shape *shape, const void *q, const void *k,
                                 const void *v, const void *gate, const float *gamma,
                                 const float *state_in, const void *dy, const float *dstate_out,
                                 void *dq, void *dk, void *dv, void *dgate, float *dstate_in,
                                 void *ws, size_t ws_bytes, hla_stream stream,
-                                const hla_trace *trace);
+                                const hla_trace *trace, const void *fwd_ws);
 
 #ifdef __cplusplus
 }

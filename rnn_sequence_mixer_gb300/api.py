@@ -157,8 +157,12 @@ def decode_step(q, k, v, gate, gamma, state, pos=None, *, pos_offset=0, rope_bas
 
 def prefill_backward(q, k, v, gate, gamma, dy, state_in=None, dstate_out=None, *, chunk=64,
                      pos_offset=0, rope_base=1e4, eps=1e-6, want_dstate_in=False,
-                     workspace=None, trace=None):
-    """hla_prefill_backward.  Returns (dq, dk, dv, dgate, dstate_in or None)."""
+                     workspace=None, trace=None, fwd_workspace=None):
+    """hla_prefill_backward.  Returns (dq, dk, dv, dgate, dstate_in or None).
+    ``fwd_workspace``: the ``workspace`` of a ``prefill`` call on the same
+    shape, inputs, gamma and state_in, enqueued earlier on this stream; the
+    backward then reads the forward's segment states instead of recomputing
+    them."""
     _check_acts(q, k, v, gate, dy)
     B, T, H, d = q.shape
     _check_state(state_in, B, H, d, q.device)
@@ -176,7 +180,7 @@ def prefill_backward(q, k, v, gate, gamma, dy, state_in=None, dstate_out=None, *
     st = lib.hla_prefill_backward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(gate), g_ptr,
                                   _ptr(state_in), _ptr(dy), _ptr(dstate_out), _ptr(dq), _ptr(dk),
                                   _ptr(dv), _ptr(dg), _ptr(dsi), _ptr(workspace), workspace.numel(),
-                                  _stream(q.device), tr[0] if tr else None)
+                                  _stream(q.device), tr[0] if tr else None, _ptr(fwd_workspace))
     _lib.check(st, "hla_prefill_backward")
     del g_host
     return dq, dk, dv, dg, dsi

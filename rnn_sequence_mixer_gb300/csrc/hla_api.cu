@@ -303,7 +303,8 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
                                 const void *gate, const float *gamma, const float *state_in,
                                 const void *dy, const float *dstate_out, void *dq, void *dk,
                                 void *dv, void *dgate, float *dstate_in, void *ws,
-                                size_t ws_bytes, hla_stream stream, const hla_trace *trace) {
+                                size_t ws_bytes, hla_stream stream, const hla_trace *trace,
+                                const void *fwd_ws) {
   HLA_TRY(check_shape(s, false));
   HLA_TRY(check_gamma(gamma, s->H));
   const bool empty = s->B == 0 || s->T == 0;
@@ -313,6 +314,7 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
   HLA_TRY(maybe(dstate_out));
   HLA_TRY(maybe(dstate_in));
   HLA_TRY(check_trace(trace));
+  HLA_TRY(maybe(fwd_ws));
   Plan plan = make_plan(*s);
   size_t sbytes = seg_bytes(*s, plan);
   size_t need_ws = hla_backward_workspace_size(s);
@@ -336,7 +338,9 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
   P.dstate_out = dstate_out;
   P.dq = dq; P.dk = dk; P.dv = dv; P.dg = dgate;
   P.dstate_in = dstate_in;
-  P.seg = (float *)ws;
+  // the state entering each segment: from the forward's workspace (written
+  // by its scan, read only here) or recomputed into this workspace
+  P.seg = fwd_ws ? (float *)const_cast<void *>(fwd_ws) : (float *)ws;
   P.seg2 = (float *)((char *)ws + sbytes);
   P.dO = (float *)((char *)ws + 2 * sbytes);
   // the tensor-core path keeps do in bf16: the second half of its region holds
@@ -348,9 +352,9 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
   Tracer tr{trace, st};
   HLA_LAUNCH(cudaMemsetAsync(P.err, 0, sizeof(unsigned int), st));
   HLA_LAUNCH(tr.mark());
-  HLA_LAUNCH(tc ? launch_tc_seg_state(P, st) : launch_simt_seg_state(P, s->dtype, st));
+  if (!fwd_ws) HLA_LAUNCH(tc ? launch_tc_seg_state(P, st) : launch_simt_seg_state(P, s->dtype, st));
   HLA_LAUNCH(tr.mark());
-  HLA_LAUNCH(launch_state_scan(P, false, st));
+  if (!fwd_ws) HLA_LAUNCH(launch_state_scan(P, false, st));
   HLA_LAUNCH(tr.mark());
   HLA_LAUNCH(tc ? launch_tc_bwd_dq(P, st) : launch_simt_bwd_dq(P, s->dtype, st));
   HLA_LAUNCH(tr.mark());

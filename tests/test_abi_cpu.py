@@ -48,7 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.hla_abi_version() == 1
+    assert lib.hla_abi_version() == 2
     for code in range(6):
         assert _lib.status_string(code).startswith("HLA_")
     assert "UNKNOWN" in _lib.status_string(99)
@@ -163,13 +163,17 @@ def test_backward_rejects_bad_arguments(lib):
     args = lambda **kw: [kw.get(n, FAKE) for n in ("q", "k", "v", "g")]
     assert lib.hla_prefill_backward(ctypes.byref(s), *args(), gp, None, FAKE, None, FAKE, FAKE,
                                     FAKE, FAKE, None, FAKE, need - 16,
-                                    None, None) == _lib.HLA_ERR_WORKSPACE
+                                    None, None, None) == _lib.HLA_ERR_WORKSPACE
     assert lib.hla_prefill_backward(ctypes.byref(s), *args(), gp, None, None, None, FAKE, FAKE,
                                     FAKE, FAKE, None, FAKE, need, None,
-                                    None) == _lib.HLA_ERR_INVALID_ARG
+                                    None, None) == _lib.HLA_ERR_INVALID_ARG
     assert lib.hla_prefill_backward(ctypes.byref(s), *args(), gp, None, FAKE, None, FAKE, FAKE,
                                     FAKE, FAKE + 1, None, FAKE, need,
-                                    None, None) == _lib.HLA_ERR_INVALID_ARG
+                                    None, None, None) == _lib.HLA_ERR_INVALID_ARG
+    # a misaligned forward workspace
+    assert lib.hla_prefill_backward(ctypes.byref(s), *args(), gp, None, FAKE, None, FAKE, FAKE,
+                                    FAKE, FAKE, None, FAKE, need, None, None,
+                                    FAKE + 4) == _lib.HLA_ERR_INVALID_ARG
 
 
 def test_python_api_has_no_cpu_path():

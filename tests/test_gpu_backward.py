@@ -128,3 +128,36 @@ def test_backward_large_magnitudes(dev):
         err = max_rel_err(f64(got), want)
         assert err <= 2e-2, f"{name}: {err:.3e}"
     assert max_rel_err(f64(out[4]), ref[4], head_axes=(0, 1)) <= 2e-2
+
+
+@pytest.mark.parametrize("B,T,H,d,dtype,chunk", [
+    (2, 90, 3, 64, torch.float32, 64),       # CUDA-core passes
+    (3, 1000, 8, 128, torch.bfloat16, 128),  # tensor-core passes, several segments, ragged tail
+])
+def test_backward_reads_forward_states(dev, B, T, H, d, dtype, chunk):
+    """The backward given the forward's workspace skips recomputing the segment
+    states and must give the same gradients, bit for bit, as the one that
+    recomputes them (the same kernels produced both), and match the oracle."""
+    g = oracle.gamma(H).astype(np.float32)
+    gt = torch.from_numpy(g)
+    inp = inputs.mixer_inputs(B, T, H, d, dtype, 70 + T, device=dev, with_dy=True)
+    s0 = inputs.state(B, H, d, 71, 0.1, device=dev)
+    dso = inputs.state(B, H, d, 72, 0.05, device=dev)
+    kw = dict(chunk=chunk, pos_offset=3, rope_base=1e6)
+    shape = api.make_shape(B, T, H, d, dtype=dtype, **kw)
+    wsf = torch.empty(api.prefill_workspace_size(shape), dtype=torch.uint8, device=dev)
+    api.prefill(inp["q"], inp["k"], inp["v"], inp["gate"], gt, s0, workspace=wsf, **kw)
+    saved = api.prefill_backward(inp["q"], inp["k"], inp["v"], inp["gate"], gt, inp["dy"], s0, dso,
+                                 want_dstate_in=True, fwd_workspace=wsf, **kw)
+    fresh = api.prefill_backward(inp["q"], inp["k"], inp["v"], inp["gate"], gt, inp["dy"], s0, dso,
+                                 want_dstate_in=True, **kw)
+    torch.cuda.synchronize()
+    for name, a, b in zip(["dq", "dk", "dv", "dgate", "dstate_in"], saved, fresh):
+        assert torch.equal(a, b), name
+    ref = oracle.backward(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(inp["gate"]),
+                          g.astype(np.float64), f64(inp["dy"]), f64(s0), f64(dso), pos_offset=3,
+                          base=1e6)
+    tol = tol_for(dtype)
+    for name, got, want in zip(["dq", "dk", "dv", "dgate"], saved[:4], ref[:4]):
+        err = max_rel_err(f64(got), want)
+        assert err <= tol, f"{name}: {err:.3e}"
