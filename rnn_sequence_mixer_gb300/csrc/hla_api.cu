@@ -155,6 +155,20 @@ size_t seg_bytes(const hla_shape &s, const Plan &p) {
   return (size_t)s.B * s.H * p.nseg * (size_t)s.dk * s.dv * sizeof(float);
 }
 
+// Pieces per segment the tensor-core local-state passes can write: every tile
+// of a full segment (gamma = 1), an upper bound for any gamma.  0 on the
+// CUDA-core path, whose local-state pass writes the segment states directly.
+int part_count(const hla_shape &s, const Plan &p) {
+  if (!(s.dtype == HLA_BF16 && s.dk == 128) || p.nseg == 0) return 0;
+  return ceil_div(ceil_div(p.seg_len, s.chunk), kPieceTiles);
+}
+
+// The partial-sum buffer (only when a segment can have more than one piece).
+size_t part_bytes(const hla_shape &s, const Plan &p) {
+  const int n = part_count(s, p);
+  return n > 1 ? (size_t)s.B * s.H * p.nseg * (size_t)n * s.dk * s.dv * sizeof(float) : 0;
+}
+
 void fill_rope(MixerParams &P, int D, double base) {
   // One-entry per-thread cache: the table depends only on (base, D).
   thread_local double cached_base = -1.0;
@@ -203,14 +217,16 @@ hla_status hla_gamma_schedule(int32_t H, float *gamma_out) {
 
 size_t hla_prefill_workspace_size(const hla_shape *s) {
   if (check_shape(s, false) != HLA_OK) return 0;
-  return seg_bytes(*s, make_plan(*s)) + kStatusBytes;
+  Plan p = make_plan(*s);
+  return seg_bytes(*s, p) + part_bytes(*s, p) + kStatusBytes;
 }
 
 size_t hla_backward_workspace_size(const hla_shape *s) {
   if (check_shape(s, false) != HLA_OK) return 0;
   Plan p = make_plan(*s);
   size_t rows = (size_t)s->B * s->T * s->H;
-  return 2 * seg_bytes(*s, p) + rows * (size_t)s->dv * sizeof(float) + kStatusBytes;
+  return 2 * seg_bytes(*s, p) + part_bytes(*s, p) + rows * (size_t)s->dv * sizeof(float) +
+         kStatusBytes;
 }
 
 hla_status hla_prefill(const hla_shape *s, const void *q, const void *k, const void *v,
@@ -230,7 +246,7 @@ hla_status hla_prefill(const hla_shape *s, const void *q, const void *k, const v
   HLA_TRY(maybe(o));
   HLA_TRY(check_trace(trace));
   Plan plan = make_plan(*s);
-  size_t need_ws = seg_bytes(*s, plan) + kStatusBytes;
+  size_t need_ws = seg_bytes(*s, plan) + part_bytes(*s, plan) + kStatusBytes;
   if (!ws || !aligned16(ws) || ws_bytes < need_ws) return HLA_ERR_WORKSPACE;
   if (empty) {
     cudaStream_t st = (cudaStream_t)stream;
@@ -251,7 +267,9 @@ hla_status hla_prefill(const hla_shape *s, const void *q, const void *k, const v
   P.y = y;
   P.o = o;
   P.seg = (float *)ws;
-  P.err = (unsigned int *)((char *)ws + seg_bytes(*s, plan));
+  P.npart = part_count(*s, plan);
+  P.part = P.npart > 1 ? (float *)((char *)ws + seg_bytes(*s, plan)) : nullptr;
+  P.err = (unsigned int *)((char *)ws + need_ws - kStatusBytes);
   cudaStream_t st = (cudaStream_t)stream;
   const bool tc = tc_supported(P, s->dtype);
   Tracer tr{trace, st};
@@ -342,7 +360,9 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
   // by its scan, read only here) or recomputed into this workspace
   P.seg = fwd_ws ? (float *)const_cast<void *>(fwd_ws) : (float *)ws;
   P.seg2 = (float *)((char *)ws + sbytes);
-  P.dO = (float *)((char *)ws + 2 * sbytes);
+  P.npart = part_count(*s, plan);
+  P.part = P.npart > 1 ? (float *)((char *)ws + 2 * sbytes) : nullptr;
+  P.dO = (float *)((char *)ws + 2 * sbytes + part_bytes(*s, plan));
   // the tensor-core path keeps do in bf16: the second half of its region holds
   // the per-token diagonal v_t . do_t
   P.ddiag = (float *)((char *)P.dO + (size_t)s->B * s->T * s->H * s->dv * 2);

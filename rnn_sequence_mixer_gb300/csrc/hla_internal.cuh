@@ -32,6 +32,13 @@ struct MixerParams {
   float *o;
   float *seg;              // [B, H, nseg, D, D] per-segment states
   float *seg2;             // backward: [B, H, nseg, D, D] per-segment state gradients
+  // Tensor-core local-state passes: each CTA covers one piece of a segment (see
+  // piece_tiles; npart pieces per segment at most, 0 on the CUDA-core path).
+  // With npart > 1, part holds [B, H, nseg, npart, D, D] partial sums that
+  // part_sum adds into seg / seg2; with npart = 1 the pass writes seg / seg2
+  // directly and part is nullptr.
+  float *part;
+  int npart;
   float *dO;               // backward: [B, T, H, D] gradient of o (fp32; bf16 on the tensor-core path)
   float *ddiag;            // backward, tensor-core path: [B, T, H] fp32 v_t . do_t
   const long long *pos;    // decode: [B] positions or nullptr
@@ -92,6 +99,52 @@ __device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __ex
 // gamma^m in fp32 for small non-negative m (exp2 of m log2 gamma).
 __device__ __forceinline__ float gpow(float log2g, float m) { return exp2f(m * log2g); }
 
+// ------------------------------------------------------------------ pieces of the local-state passes
+// The local state of a segment weights token s by gamma^m, m = L - 1 - s from
+// the segment's end (forward) or m = s + 1 from its start (state gradient).
+// For m >= decay_rows(log2 gamma), m |log2 gamma| > 160, so gamma^m computed
+// in fp32 is exactly 0 and those tokens add nothing: the pass skips their
+// tiles.  The tiles that remain are cut into pieces of kPieceTiles, each one
+// CTA writing its own partial sum, which the scan adds in a fixed order.
+constexpr int kPieceTiles = 32;
+
+// fp32 throughout: its rounding (~1e-7 relative) is far inside the margin
+// between 160 and the 150 below which exp2f stops flushing to 0.
+__host__ __device__ inline long long decay_rows(float log2g) {
+  if (!(log2g < 0.f)) return 1LL << 40;  // gamma = 1: nothing decays
+  const float w = 160.f / -log2g;
+  return w >= 1.0995116e12f ? (1LL << 40) : (long long)w + 1;
+}
+
+// Tiles [lo, hi) of a segment of L tokens (ntile tiles of CV) that piece p
+// covers; lo >= hi when the piece is empty.  grad: weights from the start.
+__host__ __device__ inline void piece_tiles(long long W, int L, int CV, int p, bool grad, int &lo,
+                                            int &hi) {
+  const int ntile = (L + CV - 1) / CV;
+  if (!grad) {  // rows s >= L - W carry weight
+    const int first = (long long)L > W ? (int)(((long long)L - W) / CV) : 0;
+    hi = ntile - p * kPieceTiles;
+    lo = hi - kPieceTiles > first ? hi - kPieceTiles : first;
+  } else {      // rows s <= W - 2 carry weight
+    const int last = W >= 2 ? (int)((W - 2) / CV + 1 < ntile ? (W - 2) / CV + 1 : ntile) : 0;
+    lo = p * kPieceTiles;
+    hi = lo + kPieceTiles < last ? lo + kPieceTiles : last;
+  }
+}
+
+// Number of non-empty pieces of that segment (pieces 0 .. n-1).
+__host__ __device__ inline int piece_count(long long W, int L, int CV, bool grad) {
+  const int ntile = (L + CV - 1) / CV;
+  int nt;
+  if (!grad) {
+    const int first = (long long)L > W ? (int)(((long long)L - W) / CV) : 0;
+    nt = ntile - first;
+  } else {
+    nt = W >= 2 ? (int)((W - 2) / CV + 1 < ntile ? (W - 2) / CV + 1 : ntile) : 0;
+  }
+  return (nt + kPieceTiles - 1) / kPieceTiles;
+}
+
 // ------------------------------------------------------------------ host side
 
 Plan make_plan(const hla_shape &s);
@@ -104,12 +157,15 @@ hla_status need_unless(bool empty, const void *p);
 cudaError_t pass_state(const hla_shape &s, const float *in, float *out, cudaStream_t st);
 void fill_common(MixerParams &P, const hla_shape &s, const float *gamma);
 size_t seg_bytes(const hla_shape &s, const Plan &p);
+size_t part_bytes(const hla_shape &s, const Plan &p);
+int part_count(const hla_shape &s, const Plan &p);
 void fill_rope(MixerParams &P, int D, double base);
 
 // Kernel launchers (return the cudaError_t of the launch).
 cudaError_t launch_decode(const MixerParams &P, int dtype, cudaStream_t st);
 cudaError_t launch_state_scan(const MixerParams &P, bool write_state_out, cudaStream_t st);
 cudaError_t launch_grad_scan(const MixerParams &P, bool write_dstate_in, cudaStream_t st);
+cudaError_t launch_part_sum(const MixerParams &P, bool grad, cudaStream_t st);
 cudaError_t launch_simt_seg_state(const MixerParams &P, int dtype, cudaStream_t st);
 cudaError_t launch_simt_seg_output(const MixerParams &P, int dtype, cudaStream_t st);
 cudaError_t launch_simt_bwd_dq(const MixerParams &P, int dtype, cudaStream_t st);

@@ -16,6 +16,10 @@
 // later tokens (dstate_out for the last segment):
 //   E_{nseg-1} = dstate_out,   E_{g-1} = gamma^{L_g} E_g + DeltaG_g,
 // and dstate_in = E_{-1}.
+//
+// The tensor-core local-state passes write one partial sum per piece of a
+// segment (piece_tiles in hla_internal.cuh); part_sum adds a segment's pieces
+// in order into its seg / seg2 slot before the scan.
 #include "hla_internal.cuh"
 
 namespace hla {
@@ -86,7 +90,34 @@ __global__ void __launch_bounds__(kScanThreads) grad_scan_kernel(const MixerPara
   if (write_out) P.dstate_in[(size_t)bh * DD + e] = E;
 }
 
+// Delta_g (or DeltaG_g) = sum of the segment's non-empty pieces, p = 0, 1, ...
+// One thread per state element of one (b, h, segment).
+__global__ void __launch_bounds__(kScanThreads) part_sum_kernel(const MixerParams P, int grad) {
+  const size_t DD = (size_t)P.D * P.D;
+  const size_t e = (size_t)blockIdx.x * kScanThreads + threadIdx.x;
+  if (e >= DD) return;
+  const int g = blockIdx.y, bh = blockIdx.z;
+  const int h = bh % P.H;
+  const int L = g == P.nseg - 1 ? P.T - (P.nseg - 1) * P.seg_len : P.seg_len;
+  const int np = piece_count(decay_rows(log2f(P.gamma[h])), L, P.chunk, grad != 0);
+  const float *part = P.part + ((size_t)bh * P.nseg + g) * P.npart * DD + e;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int p0 = 0; p0 < np; p0 += 4) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (p0 + j < np) acc[j] += part[(size_t)(p0 + j) * DD];
+  }
+  float *dst = (grad ? P.seg2 : P.seg) + ((size_t)bh * P.nseg + g) * DD + e;
+  *dst = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
 }  // namespace
+
+cudaError_t launch_part_sum(const MixerParams &P, bool grad, cudaStream_t st) {
+  dim3 grid(ceil_div((long long)P.D * P.D, kScanThreads), P.nseg, P.B * P.H);
+  part_sum_kernel<<<grid, kScanThreads, 0, st>>>(P, grad ? 1 : 0);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_state_scan(const MixerParams &P, bool write_state_out, cudaStream_t st) {
   dim3 grid(P.B * P.H, ceil_div((long long)P.D * P.D, kScanThreads));

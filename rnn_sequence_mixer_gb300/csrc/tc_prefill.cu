@@ -56,6 +56,9 @@ struct StateShared {
 // kGrad = true:  DeltaG_seg = sum_s gamma^{s-start+1} q~_s^T do_s, the backward's
 //                per-segment state gradient (q~ = RoPE(Norm(q)), do a bf16 tensor);
 //                tmk then maps q and tmv maps do.
+// One CTA per piece of a segment (piece_tiles): only the tiles whose decay
+// weights can be non-zero in fp32 are read, cut into pieces of at most
+// kPieceTiles, and each piece's sum goes to its own slot of P.part.
 // Warp-specialized: 16 worker warps turn raw k rows into decay-weighted k~
 // in place (row norms from the four lanes that share a row); the issuer warp
 // issues one MMA per tile as soon as the workers are done with it and refills
@@ -71,12 +74,23 @@ __global__ void __launch_bounds__(NTO, 1)
   StateShared &sh = *reinterpret_cast<StateShared *>(base + 2 * kStages * TILE);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int np = P.npart > 1 ? P.npart : 1;
+  const int g = blockIdx.x / np, piece = blockIdx.x % np, h = blockIdx.y, b = blockIdx.z;
   const int t0 = g * P.seg_len, t1 = min(P.T, t0 + P.seg_len);
   const int CV = P.chunk;
   const int L = t1 - t0;
-  const int ntile = ceil_div(L, CV);
   const float l2g = log2f(P.gamma[h]);
+  int lo, hi;
+  piece_tiles(decay_rows(l2g), L, CV, piece, kGrad, lo, hi);
+  float *out = P.part ? P.part + ((((size_t)b * P.H + h) * P.nseg + g) * P.npart + piece) * (size_t)D * D
+                      : (kGrad ? P.seg2 : P.seg) + (((size_t)b * P.H + h) * P.nseg + g) * (size_t)D * D;
+  if (lo >= hi) {  // nothing with a non-zero weight (uniform: the CTA leaves before any barrier)
+    if (!P.part)   // the segment's only piece: its sum is zero
+      for (int e = threadIdx.x; e < D * D; e += NTO) out[e] = 0.f;
+    return;
+  }
+  const int ntile = hi - lo;       // tiles of this piece
+  const int tb = t0 + lo * CV;     // its first token
   const uint32_t tile_bytes = (uint32_t)CV * D * 2;
 
   if (tid == 0) {
@@ -106,8 +120,8 @@ __global__ void __launch_bounds__(NTO, 1)
       const uint32_t idesc = umma::idesc_bf16(128, 128, true, true);
       for (int n = 0; n < kStages && n < ntile; ++n) {
         umma::mbar_expect_tx(&sh.bar_tma[n], 2 * tile_bytes);
-        tma_tile(base + 2 * n * TILE, &tmk, b, h, t0 + n * CV, &sh.bar_tma[n]);
-        tma_tile(base + (2 * n + 1) * TILE, &tmv, b, h, t0 + n * CV, &sh.bar_tma[n]);
+        tma_tile(base + 2 * n * TILE, &tmk, b, h, tb + n * CV, &sh.bar_tma[n]);
+        tma_tile(base + (2 * n + 1) * TILE, &tmv, b, h, tb + n * CV, &sh.bar_tma[n]);
       }
       for (int n = 0; n < ntile; ++n) {
         const int st = n % kStages;
@@ -125,7 +139,7 @@ __global__ void __launch_bounds__(NTO, 1)
         if (n + kStages < ntile) {  // the stage takes tile n + 3 once MMA n has read it
           wait_or_fail(&sh.bar_mma[st], par, failed);
           if (!failed) {
-            const int cn = t0 + (n + kStages) * CV;
+            const int cn = tb + (n + kStages) * CV;
             umma::mbar_expect_tx(&sh.bar_tma[st], 2 * tile_bytes);
             tma_tile(Kt, &tmk, b, h, cn, &sh.bar_tma[st]);
             tma_tile(Kt + TILE, &tmv, b, h, cn, &sh.bar_tma[st]);
@@ -140,7 +154,7 @@ __global__ void __launch_bounds__(NTO, 1)
     for (int n = 0; n < ntile; ++n) {
       const int st = n % kStages;
       unsigned char *Kt = base + 2 * st * TILE;
-      const int c0 = t0 + n * CV, c = min(CV, t1 - c0);
+      const int c0 = tb + n * CV, c = min(CV, t1 - c0);
       wait_or_fail(&sh.bar_tma[st], (n / kStages) & 1, failed);
       uint4 kr[4];
       ld_pairs(Kt, fr, fu, kr);
@@ -167,7 +181,6 @@ __global__ void __launch_bounds__(NTO, 1)
     if (failed) atomicOr(&sh.failed, 1u);
   }
   sync_tc();
-  float *out = (kGrad ? P.seg2 : P.seg) + (((size_t)b * P.H + h) * P.nseg + g) * (size_t)D * D;
   if (warp < NWORK) {
     const int sub = warp & 3, qd = warp >> 2, i = 32 * sub + lane;
     if (!sh.failed) {
@@ -588,8 +601,10 @@ cudaError_t launch_state_variant(const MixerParams &P, const void *a, const void
   e = cudaFuncSetAttribute(tc::tc_state_kernel<kGrad>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)tc::kStateSmem);
   if (e != cudaSuccess) return e;
-  tc::tc_state_kernel<kGrad><<<dim3(P.nseg, P.H, P.B), tc::NTO, tc::kStateSmem, st>>>(P, ma, mb);
-  return cudaGetLastError();
+  const int np = P.npart > 1 ? P.npart : 1;
+  tc::tc_state_kernel<kGrad><<<dim3(P.nseg * np, P.H, P.B), tc::NTO, tc::kStateSmem, st>>>(P, ma, mb);
+  if (cudaGetLastError() != cudaSuccess) return cudaErrorLaunchFailure;
+  return P.part ? launch_part_sum(P, kGrad, st) : cudaSuccess;
 }
 }  // namespace
 

@@ -78,7 +78,9 @@ def test_workspace_sizes():
     n = api.prefill_workspace_size(s)
     assert n > 256 and (n - 256) % (128 * 128 * 4) == 0
     bw = api.backward_workspace_size(s)
-    assert bw >= 2 * (n - 256) + 524288 * 16 * 128 * 4
+    # the backward holds what the forward does (segment states and the local-state
+    # pass's partial sums), a second set of segment states and an fp32-sized dO region
+    assert bw >= (n - 256) + 16 * 128 * 128 * 4 + 524288 * 16 * 128 * 4
     bad = shape(d=96)
     assert api.prefill_workspace_size(bad) == 0
     assert api.backward_workspace_size(bad) == 0
