@@ -233,8 +233,9 @@ struct OutShared {
 //     [A]/[D] raw q, k -> row norms (warp shuffles) -> q~, k~ fp16 in place
 //     [B]/[C] after MMA3/MMA4 of tile n - 1: Sb = fp16(S 2^-e) with one power
 //             of two per column quarter, S <- gamma^c S
-//     [E]     epilogue of tile n - 1 (overlaps MMA1/MMA2 of tile n)
 //     [F]     after MMA1/MMA2: mask P -> Pm, O <- gamma^{i+1} 2^e O, k~ -> k~dec
+//     [E]     epilogue of tile n - 1, while MMA3/MMA4 of tile n run and q of
+//             tile n + 1 is copied into the Q buffer MMA2 has just freed
 // The only CTA-wide barriers are outside the tile loop; the two reductions
 // (max |S| per column quarter, the RMS of o per row) use 4-warp named barriers.
 __global__ void __launch_bounds__(NTO, 1)
@@ -336,15 +337,6 @@ __global__ void __launch_bounds__(NTO, 1)
         // the q tile after that into L2, so that its copy (issued one tile
         // from now, on the workers' critical path) does not wait on HBM
         if (!failed && n + 2 < ntile) tma_prefetch_tile(&tmq, b, h, c0 + 2 * CV);
-        // y of tile n - 1 is in G: store it (the gate of tile n follows once
-        // the store has read G, after MMA3 / MMA4 are issued)
-        if (n >= 1) {
-          wait_or_fail(&sh.bar_epi, (n - 1) & 1, failed);
-          if (!failed) {
-            tma_store_tile(&tmy, Gs, b, h, c0 - CV);
-            umma::bulk_commit();
-          }
-        }
         wait_or_fail(&sh.bar_pm, n & 1, failed);
         wait_or_fail(&sh.bar_v, n & 1, failed);
         if (!failed) {
@@ -358,11 +350,6 @@ __global__ void __launch_bounds__(NTO, 1)
                          id_mn, 1u);
           umma::commit(&sh.bar_mma[1]);
         }
-        if (n >= 1 && !failed) {
-          umma::bulk_wait_read();
-          umma::mbar_expect_tx(&sh.bar_g, tile_bytes);
-          tma_tile(Gs, &tmg, b, h, c0, &sh.bar_g);
-        }
         // MMA3 / MMA4 done: V and K buffer `buf` are free for the next copies
         wait_or_fail(&sh.bar_mma[1], n & 1, failed);
         if (!failed) {
@@ -373,6 +360,18 @@ __global__ void __launch_bounds__(NTO, 1)
           if (n + 2 < ntile) {
             umma::mbar_expect_tx(&sh.bar_k[buf], tile_bytes);
             tma_tile(base + (1 + buf) * TILE, &tmk, b, h, c0 + 2 * CV, &sh.bar_k[buf]);
+          }
+        }
+        // y of tile n - 1 is in G once the workers' epilogue (after this
+        // tile's mask) is done: store it, then G takes the gate of tile n
+        if (n >= 1) {
+          wait_or_fail(&sh.bar_epi, (n - 1) & 1, failed);
+          if (!failed) {
+            tma_store_tile(&tmy, Gs, b, h, c0 - CV);
+            umma::bulk_commit();
+            umma::bulk_wait_read();
+            umma::mbar_expect_tx(&sh.bar_g, tile_bytes);
+            tma_tile(Gs, &tmg, b, h, c0, &sh.bar_g);
           }
         }
       }
@@ -477,48 +476,6 @@ __global__ void __launch_bounds__(NTO, 1)
         umma::tmem_wait_st();
         warp_arrive(&sh.bar_sb, lane);
       }
-      // [E] epilogue of tile n - 1 (overlaps MMA1 / MMA2 of tile n)
-      if (drain) {
-        float o[32];
-        umma::tmem_ld2x16(oprev + lane_base + col, o);
-        if (P.o && i < prev_c) {
-          const size_t row = (((size_t)b * P.T + prev_c0 + i) * P.H + h) * D + col;
-          float4 *o4 = reinterpret_cast<float4 *>(P.o + row);
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            o4[u] = make_float4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
-        }
-        f2 ox[16];
-        pairs_of(o, ox);
-        f2 ss = 0ull;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) ss = fma2(ox[e], ox[e], ss);
-        sh.red_o[qd][i] = hsum2(ss);
-        named_sync(5 + sub, 128);
-        // gate of tile n - 1 (TMA) -> y, in place; the issuer stores the tile
-        wait_or_fail(&sh.bar_g, (n - 1) & 1, failed);
-        {
-          const f2 ro = dup2(rsqrtf((sh.red_o[0][i] + sh.red_o[1][i] + sh.red_o[2][i] +
-                                     sh.red_o[3][i]) / (float)D + P.eps));
-          const f2 half = dup2(0.5f);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint4 *p = tile_at(Gs, i, 4 * qd + u);
-            f2 g[4], t[4];
-            unpack4x2(*p, g);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              // sigmoid(z) = 0.5 + 0.5 tanh(z / 2)
-              float za, zb;
-              split2(mul2(g[e], half), za, zb);
-              const f2 sg = fma2(mk2(tanh_fast(za), tanh_fast(zb)), half, half);
-              t[e] = mul2(mul2(ox[4 * u + e], ro), sg);
-            }
-            *p = pack4x2(t);
-          }
-        }
-        warp_arrive(&sh.bar_epi, lane);
-      }
       if (have) {
         // [F] MMA1 of tile n done: mask P
         wait_or_fail(&sh.bar_p, n & 1, failed);
@@ -569,9 +526,52 @@ __global__ void __launch_bounds__(NTO, 1)
         }
         umma::tmem_wait_st();
         warp_arrive(&sh.bar_pm, lane);
-        prev_c0 = c0;
-        prev_c = c;
       }
+      // [E] epilogue of tile n - 1 (overlaps MMA3 / MMA4 of tile n and the copy of
+      // q of tile n + 1)
+      if (drain) {
+        float o[32];
+        umma::tmem_ld2x16(oprev + lane_base + col, o);
+        if (P.o && i < prev_c) {
+          const size_t row = (((size_t)b * P.T + prev_c0 + i) * P.H + h) * D + col;
+          float4 *o4 = reinterpret_cast<float4 *>(P.o + row);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            o4[u] = make_float4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+        }
+        f2 ox[16];
+        pairs_of(o, ox);
+        f2 ss = 0ull;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) ss = fma2(ox[e], ox[e], ss);
+        sh.red_o[qd][i] = hsum2(ss);
+        named_sync(5 + sub, 128);
+        // gate of tile n - 1 (TMA) -> y, in place; the issuer stores the tile
+        wait_or_fail(&sh.bar_g, (n - 1) & 1, failed);
+        {
+          const f2 ro = dup2(rsqrtf((sh.red_o[0][i] + sh.red_o[1][i] + sh.red_o[2][i] +
+                                     sh.red_o[3][i]) / (float)D + P.eps));
+          const f2 half = dup2(0.5f);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 *p = tile_at(Gs, i, 4 * qd + u);
+            f2 g[4], t[4];
+            unpack4x2(*p, g);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              // sigmoid(z) = 0.5 + 0.5 tanh(z / 2)
+              float za, zb;
+              split2(mul2(g[e], half), za, zb);
+              const f2 sg = fma2(mk2(tanh_fast(za), tanh_fast(zb)), half, half);
+              t[e] = mul2(mul2(ox[4 * u + e], ro), sg);
+            }
+            *p = pack4x2(t);
+          }
+        }
+        warp_arrive(&sh.bar_epi, lane);
+      }
+      prev_c0 = c0;
+      prev_c = c;
     }
   }
   if (failed) atomicOr(&sh.failed, 1u);
