@@ -141,6 +141,7 @@ struct DqShared {
   uint64_t bar_v;       // TMA: v into V
   uint64_t bar_g;       // TMA: gate of tile n into Q
   uint64_t bar_qr;      // TMA: raw q of tile n into its (freed) K buffer, for [W6]
+  uint64_t bar_dy;      // TMA: dy of tile n into PM (once MMA7 of tile n - 1 has read dPm)
   uint64_t bar_p;       // MMA1 done (P)
   uint64_t bar_o;       // MMA2 done (O = Q~ Sb)
   uint64_t bar_m3;      // MMA3 done (O complete)
@@ -173,16 +174,19 @@ __device__ __forceinline__ f2 sigmoid2(f2 z) {
 //         so K~ serves MMA7 and MMA4 unchanged)
 // Worker warps (0..15) run, per loop step n:
 //   [W1] q~, k~ of tile n (fp16, in place)       [W2] Sb = fp16(S 2^-e), S <- gamma^c S
-//   [W3] Pm, O <- gamma^{i+1} 2^e O, K~ -> bf16, Sb -> bf16 S
-//   [W4] dgate -> PM, dO -> Q (over the gate), fp32 v_i . do_i
+//   [W3] Pm (into the P columns of TMEM), O <- gamma^{i+1} 2^e O, K~ -> bf16,
+//        Sb -> bf16 S
+//   [W4] dgate -> PM (over dy), dO -> Q (over the gate), fp32 v_i . do_i
 //   [W6] dq of tile n - 1 (RoPE^T, RMSNorm backward) in its K buffer, over its raw q
 //   [W5] dPm -> PM (fp32 v_i . do_i on the diagonal), I <- gamma^{i+1} I, V -> Vdec
-// so the dq epilogue of tile n - 1 fills the wait on MMA5 / MMA6 of tile n.
-// The issuer warp (16) waits for each hand-off, issues the MMAs and moves every
-// tile by TMA: q, k (double-buffered), v, the gate (into Q once MMA2 has read
-// it), raw q again for [W6] (into the K buffer that MMA7 / MMA4 freed), and
-// the stores of dgate, dO and dq.  dy is the one operand read by plain loads
-// (tmdy only prefetches it into L2 a tile ahead).
+// so the dq epilogue of tile n - 1 runs while MMA5 / MMA6 of tile n are in
+// flight.  The issuer warp (16) waits for each hand-off, issues the MMAs and
+// moves every tile by TMA: q, k (double-buffered), v, the gate (into Q once
+// MMA2 has read it), dy (into PM once MMA7 of the tile before has read dPm: a
+// tile ahead), raw q again for [W6] (into the K buffer that MMA7 / MMA4 freed),
+// and the stores of dgate, dO and dq.  No operand is read by plain loads: 16-byte loads of dy
+// from 32 rows per warp instruction crowded the load pipeline and stalled every
+// later shared-memory access of the warps (~20 % of a tile).
 __global__ void __launch_bounds__(NTO, 1)
     tc_bwd_dq_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmq,
                      const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -193,7 +197,7 @@ __global__ void __launch_bounds__(NTO, 1)
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   // Q:  raw q -> q~ (fp16) -> gate -> dO (bf16)                 -> next raw q
   // K j: raw k -> k~ (fp16) -> k~ (bf16) -> raw q -> dq (bf16)  -> k two tiles on
-  // V:  v -> Vdec;  SB: Sb (fp16, scaled) -> S (bf16);  PM: Pm -> dgate -> dPm
+  // V:  v -> Vdec;  SB: Sb (fp16, scaled) -> S (bf16);  PM: dy -> dgate -> dPm
   unsigned char *Qs = base, *Vs = base + 3 * TILE, *SB = base + 4 * TILE, *PM = base + 5 * TILE;
   DqShared &sh = *reinterpret_cast<DqShared *>(base + 6 * TILE);
 
@@ -206,7 +210,7 @@ __global__ void __launch_bounds__(NTO, 1)
   const uint32_t tile_bytes = (uint32_t)CV * D * 2;
 
   if (tid == 0) {
-    uint64_t *bars[] = {&sh.bar_q, &sh.bar_k[0], &sh.bar_k[1], &sh.bar_v, &sh.bar_g, &sh.bar_qr,
+    uint64_t *bars[] = {&sh.bar_q, &sh.bar_k[0], &sh.bar_k[1], &sh.bar_v, &sh.bar_g, &sh.bar_qr, &sh.bar_dy,
                         &sh.bar_p, &sh.bar_o, &sh.bar_m3, &sh.bar_m56, &sh.bar_m74, &sh.bar_rd};
     for (uint64_t *bar : bars) umma::mbar_init(bar, 1);
     uint64_t *wbars[] = {&sh.bar_feat, &sh.bar_sb, &sh.bar_pm, &sh.bar_do, &sh.bar_w5, &sh.bar_w6};
@@ -244,8 +248,9 @@ __global__ void __launch_bounds__(NTO, 1)
       }
       umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
       tma_tile(Vs, &tmv, b, h, t0, &sh.bar_v);
+      umma::mbar_expect_tx(&sh.bar_dy, tile_bytes);
+      tma_tile(PM, &tmdy, b, h, t0, &sh.bar_dy);
       tma_prefetch_tile(&tmg, b, h, t0);
-      tma_prefetch_tile(&tmdy, b, h, t0);
       for (int n = 0; n < ntile; ++n) {
         const int buf = n & 1;
         const uint32_t ph = n & 1;
@@ -286,8 +291,9 @@ __global__ void __launch_bounds__(NTO, 1)
         wait_or_fail(&sh.bar_v, ph, failed);
         if (!failed) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma::mma_ss(ta, umma::desc_kmajor(apm, kk, ROWS), umma::desc_mnmajor(av, kk, ROWS), id_kmn, 1u);
+          for (int kk = 0; kk < 8; ++kk)  // A = Pm from the P columns of TMEM
+            umma::mma_ts(ta, tP + 32 * (kk >> 1) + 8 * (kk & 1), umma::desc_mnmajor(av, kk, ROWS),
+                         id_kmn, 1u);
           umma::commit(&sh.bar_m3);
         }
         // dgate (PM) and dO (Q) out; MMA5, MMA6 from dO
@@ -346,6 +352,10 @@ __global__ void __launch_bounds__(NTO, 1)
           }
           umma::mbar_expect_tx(&sh.bar_qr, tile_bytes);
           tma_tile(Kt, &tmq, b, h, c0, &sh.bar_qr);
+          if (n + 1 < ntile) {  // MMA7 has read dPm: PM takes dy of the next tile
+            umma::mbar_expect_tx(&sh.bar_dy, tile_bytes);
+            tma_tile(PM, &tmdy, b, h, c0 + CV, &sh.bar_dy);
+          }
         }
       }
       // dq of the last tile
@@ -449,8 +459,6 @@ __global__ void __launch_bounds__(NTO, 1)
 
         // [W3] after MMA1: Pm (with the fp32 diagonal), k~ -> bf16; after MMA2:
         // O <- gamma^{i+1} 2^e O, Sb -> bf16 S
-        uint4 dyr[4];  // dy of row i for [W4], in flight during [W3]
-        load_quarter(dyr, row_ptr(P.dy, P, b, h, valid ? c0 + i : c0), qd, valid);
         wait_or_fail(&sh.bar_p, ph, failed);
         {
           float pv[32];
@@ -465,12 +473,26 @@ __global__ void __launch_bounds__(NTO, 1)
             unpack4x2h(*p, f);
             *p = pack4x2(f);
           }
-          wait_or_fail(&sh.bar_o, ph, failed);  // MMA2 done: PM and SB are free to rewrite
+          // Pm as packed bf16 over the first 16 of the 32 P columns this thread has
+          // read: MMA3 takes its A operand from there (K-step kk at column
+          // 32 (kk / 2) + 8 (kk % 2)), which leaves PM free for dy.  The diagonal
+          // entry (element i - 32 qd on the warps with qd == sub) comes from fp32
+          // features (written in [W1], met at [W2]'s barrier).
+          {
+            const int e = qd == sub ? i - (int)col : -1;
+            const float dval = qd == sub ? sh.qk_diag[buf][i] : 0.f;
+            uint32_t pm[16];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) *tile_at(PM, i, 4 * qd + u) = pack4x2(&x[4 * u]);
-          if (qd == sub)  // the diagonal from fp32 features (written in [W1], met at [W2]'s barrier)
-            *(reinterpret_cast<__nv_bfloat16 *>(tile_at(PM, i, i >> 3)) + (i & 7)) =
-                __float2bfloat16_rn(sh.qk_diag[buf][i]);
+            for (int e2 = 0; e2 < 16; ++e2) {
+              float lo, hi;
+              split2(x[e2], lo, hi);
+              lo = e == 2 * e2 ? dval : lo;
+              hi = e == 2 * e2 + 1 ? dval : hi;
+              pm[e2] = pack2(lo, hi);
+            }
+            umma::tmem_st16u(myP, pm);
+          }
+          wait_or_fail(&sh.bar_o, ph, failed);  // MMA2 done: SB is free to rewrite
           const f2 si = dup2(s_inv);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {  // Sb -> S (bf16, unscaled) for MMA6
@@ -493,12 +515,15 @@ __global__ void __launch_bounds__(NTO, 1)
           umma::tmem_wait_st();
         }
         warp_arrive(&sh.bar_pm, lane);
+      }
 
+      if (have) {
         // [W4] after MMA3: output norm and gate backward.  n = o r, z = sigmoid(gate),
         // dn = dy z, dgate = dn n (1 - z), dO = r (dn - n mean(dn n)); rows past the tile get 0
         wait_or_fail(&sh.bar_m3, ph, failed);
         wait_or_fail(&sh.bar_g, ph, failed);
         wait_or_fail(&sh.bar_v, ph, failed);
+        wait_or_fail(&sh.bar_dy, ph, failed);
         {
           float o[32];
           umma::tmem_ld2x16(ta + col, o);
@@ -509,7 +534,7 @@ __global__ void __launch_bounds__(NTO, 1)
           for (int u = 0; u < 4; ++u) {
             f2 gz[4], dv[4];
             unpack4x2(*tile_at(Qs, i, 4 * qd + u), gz);
-            unpack4x2(dyr[u], dv);
+            unpack4x2(*tile_at(PM, i, 4 * qd + u), dv);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const f2 dn = mul2(dv[e], sigmoid2(gz[e]));
@@ -531,7 +556,7 @@ __global__ void __launch_bounds__(NTO, 1)
             uint4 *gp = tile_at(Qs, i, 4 * qd + u);
             f2 gz[4], dv[4], vv[4], dg[4], dd[4];
             unpack4x2(*gp, gz);
-            unpack4x2(dyr[u], dv);
+            unpack4x2(*tile_at(PM, i, 4 * qd + u), dv);
             unpack4x2(*tile_at(Vs, i, 4 * qd + u), vv);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -552,7 +577,8 @@ __global__ void __launch_bounds__(NTO, 1)
 
       if (drain) {
         // [W6] dq of tile n - 1: dQ~ from TMEM, RoPE^T, RMSNorm backward against raw q
-        // (the K buffer of tile n - 1), in place; pairs m = 16 qd .. 16 qd + 15
+        // (the K buffer of tile n - 1), in place; pairs m = 16 qd .. 16 qd + 15.  Runs
+        // while MMA5 / MMA6 of tile n are in flight.
         // (in the last step no [W2] has waited for MMA7 of tile n - 1: wait here)
         if (!have) wait_or_fail(&sh.bar_m74, (n - 1) & 1, failed);
         wait_or_fail(&sh.bar_qr, (n - 1) & 1, failed);
@@ -563,7 +589,9 @@ __global__ void __launch_bounds__(NTO, 1)
                              sh.red_dq, Kp);
         }
         warp_arrive(&sh.bar_w6, lane);
-      } else if (have) {
+      }
+
+      else if (have) {
         named_sync(5 + sub, 128);  // orders [W4]'s vd_part before [W5] reads it
       }
 
