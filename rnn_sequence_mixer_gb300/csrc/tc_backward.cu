@@ -45,25 +45,27 @@ namespace tc {
 
 namespace {
 
-// This thread's 16 RoPE pairs of a raw input row (elements 16 qd .. 16 qd + 15
-// and 64 + 16 qd ..), zeros when !valid.
-__device__ __forceinline__ void load_pairs(uint4 (&ra)[4], const __nv_bfloat16 *raw, int qd,
-                                           bool valid) {
-  if (valid) {
-    ra[0] = ldg16(raw + 16 * qd);
-    ra[1] = ldg16(raw + 16 * qd + 8);
-    ra[2] = ldg16(raw + 64 + 16 * qd);
-    ra[3] = ldg16(raw + 64 + 16 * qd + 8);
-  } else {
-    ra[0] = ra[1] = ra[2] = ra[3] = make_uint4(0, 0, 0, 0);
+// 32 fp32 values of a row (16 pairs) as packed bf16 into 16 TMEM columns at
+// taddr (an MMA A operand in tensor memory).  Element e (0..31, none when e < 0)
+// is replaced by dval first.  Selects in registers: no dynamic indexing.
+__device__ __forceinline__ void store_tmem_bf16(uint32_t taddr, const f2 (&x)[16], int e, float dval) {
+  uint32_t w[16];
+#pragma unroll
+  for (int e2 = 0; e2 < 16; ++e2) {
+    float lo, hi;
+    split2(x[e2], lo, hi);
+    lo = e == 2 * e2 ? dval : lo;
+    hi = e == 2 * e2 + 1 ? dval : hi;
+    w[e2] = pack2(lo, hi);
   }
+  umma::tmem_st16u(taddr, w);
 }
 
 // Gradient with respect to a raw q or k row, through RoPE and RMSNorm, for this
 // thread's 16 RoPE pairs of row i (elements 16 qd .. 16 qd + 15 and their
 // partners 64 further on).  g~ = gscale * (the gradient of the rotated,
 // normalized row) is read from TMEM at tmem_row (the lane's base address,
-// column 0); raw holds the raw row's pairs (ld_pairs / load_pairs layout).
+// column 0); raw holds the raw row's pairs (ld_pairs layout).
 // With g = RoPE^T g~, x the raw row and r = 1 / RMS(x):
 //   dL/dx = r g - r^3 x (g . x) / d.
 // Writes it as bf16 into the same chunks of `out`.  The two row sums need the
@@ -478,20 +480,7 @@ __global__ void __launch_bounds__(NTO, 1)
           // 32 (kk / 2) + 8 (kk % 2)), which leaves PM free for dy.  The diagonal
           // entry (element i - 32 qd on the warps with qd == sub) comes from fp32
           // features (written in [W1], met at [W2]'s barrier).
-          {
-            const int e = qd == sub ? i - (int)col : -1;
-            const float dval = qd == sub ? sh.qk_diag[buf][i] : 0.f;
-            uint32_t pm[16];
-#pragma unroll
-            for (int e2 = 0; e2 < 16; ++e2) {
-              float lo, hi;
-              split2(x[e2], lo, hi);
-              lo = e == 2 * e2 ? dval : lo;
-              hi = e == 2 * e2 + 1 ? dval : hi;
-              pm[e2] = pack2(lo, hi);
-            }
-            umma::tmem_st16u(myP, pm);
-          }
+          store_tmem_bf16(myP, x, qd == sub ? i - (int)col : -1, qd == sub ? sh.qk_diag[buf][i] : 0.f);
           wait_or_fail(&sh.bar_o, ph, failed);  // MMA2 done: SB is free to rewrite
           const f2 si = dup2(s_inv);
 #pragma unroll
@@ -653,6 +642,7 @@ struct DkdvShared {
   float pw[ROWS + 1];
   alignas(16) float du[4][DM_STRIDE];  // transposed causal-mask table (fill_mask_table_upper)
   uint64_t bar_q, bar_k, bar_v, bar_dot;                    // TMA loads of q, k, v, dO
+  uint64_t bar_kr;                                          // TMA: raw k again, into X, for [V6]
   uint64_t bar_m1, bar_m2, bar_dv, bar_dk, bar_eupd;        // MMA commits
   uint64_t bar_feat, bar_eb, bar_x, bar_xp, bar_dvout, bar_qw, bar_dkout;  // workers
   uint32_t tmem_base;
@@ -667,14 +657,16 @@ struct DkdvShared {
 //   dK~  = X' Q~ + Vdec Eb^T,  X' = M2 (.) D^T  (fp32 v_i . do_i on the diagonal)
 //   E   <- gamma^c E + Q~w^T dO,  Q~w = diag(gamma^{i+1}) Q~
 // with D^T_ij = gamma^{j-i} for j >= i, K~dec / Vdec rows scaled by gamma^{c-1-i}
-// and Eb = bf16(E) at the tile's end.  Worker warps, per tile:
+// and Eb = bf16(E) at the tile's end.  X and X' are MMA A operands in tensor
+// memory (packed bf16, 64 columns each next to E).  Worker warps, per tile:
 //   [V1] q~, k~ (fp16, in place)             [V2] Eb, E <- gamma^c E
-//   [V3] X -> X, k~ -> K~dec                  [V4] Vdec, q~ -> bf16, X' -> X once dV is done
+//   [V3] X -> TMEM, k~ -> K~dec               [V4] Vdec, q~ -> bf16, X' -> TMEM
 //   [V5] dv -> K (over K~dec)                 [V6] q~ -> Q~w, then dk (RoPE^T, RMSNorm
 //                                                  backward against raw k) -> V (over Vdec)
 // The issuer warp issues the MMAs as their operands are ready, stores dv and dk
 // by TMA and refills Q, K, V and dO for the tile before as each is freed.  Raw
-// k for the RMSNorm backward and the v . do diagonal are plain loads.
+// k for the RMSNorm backward arrives by TMA in the X buffer a tile ahead; the
+// v . do diagonal (one word per row) is the only plain load.
 __global__ void __launch_bounds__(NTO, 1)
     tc_bwd_dkdv_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmq,
                        const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -683,7 +675,7 @@ __global__ void __launch_bounds__(NTO, 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   // Q: raw q -> q~ (fp16) -> q~ (bf16) -> Q~w.  K: raw k -> k~ (fp16) -> K~dec -> dv.
-  // V: v -> Vdec -> dk.  DO: dO.  EB: Eb.  X: X, then X'.
+  // V: v -> Vdec -> dk.  DO: dO.  EB: Eb.  X: raw k of the tile, for [V6].
   unsigned char *Qt = base, *Kt = base + TILE, *Vt = base + 2 * TILE, *DOt = base + 3 * TILE;
   unsigned char *EB = base + 4 * TILE, *X = base + 5 * TILE;
   DkdvShared &sh = *reinterpret_cast<DkdvShared *>(base + 6 * TILE);
@@ -697,7 +689,7 @@ __global__ void __launch_bounds__(NTO, 1)
   const uint32_t tile_bytes = (uint32_t)CV * D * 2;
 
   if (tid == 0) {
-    uint64_t *bars[] = {&sh.bar_q, &sh.bar_k, &sh.bar_v, &sh.bar_dot, &sh.bar_m1,
+    uint64_t *bars[] = {&sh.bar_q, &sh.bar_k, &sh.bar_v, &sh.bar_dot, &sh.bar_kr, &sh.bar_m1,
                         &sh.bar_m2, &sh.bar_dv, &sh.bar_dk, &sh.bar_eupd};
     for (uint64_t *bar : bars) umma::mbar_init(bar, 1);
     uint64_t *wbars[] = {&sh.bar_feat, &sh.bar_eb, &sh.bar_x, &sh.bar_xp,
@@ -717,7 +709,7 @@ __global__ void __launch_bounds__(NTO, 1)
     }
   sync_tc();
   const uint32_t tm = sh.tmem_base;
-  const uint32_t tA = tm, tB = tm + 128, tE = tm + 256;
+  const uint32_t tA = tm, tB = tm + 128, tE = tm + 256, tX = tm + 384;  // tX: X, then X' at + 64
   bool failed = false;
 
   if (warp >= NWORK) {
@@ -728,7 +720,7 @@ __global__ void __launch_bounds__(NTO, 1)
       const uint32_t id_kk = umma::idesc_bf16(128, 128, false, false);
       const uint32_t id_mnmn = umma::idesc_bf16(128, 128, true, true);
       const uint32_t aQ = umma::smem_u32(Qt), aK = umma::smem_u32(Kt), aV = umma::smem_u32(Vt),
-                     aDO = umma::smem_u32(DOt), aE = umma::smem_u32(EB), aX = umma::smem_u32(X);
+                     aDO = umma::smem_u32(DOt), aE = umma::smem_u32(EB);
       {
         const int cl = t0 + (ntile - 1) * CV;
         umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
@@ -739,6 +731,8 @@ __global__ void __launch_bounds__(NTO, 1)
         tma_tile(Vt, &tmv, b, h, cl, &sh.bar_v);
         umma::mbar_expect_tx(&sh.bar_dot, tile_bytes);
         tma_tile(DOt, &tmo, b, h, cl, &sh.bar_dot);
+        umma::mbar_expect_tx(&sh.bar_kr, tile_bytes);
+        tma_tile(X, &tmk, b, h, cl, &sh.bar_kr);
       }
       for (int it = 0; it < ntile; ++it) {
         const int n = ntile - 1 - it;
@@ -769,8 +763,8 @@ __global__ void __launch_bounds__(NTO, 1)
         wait_or_fail(&sh.bar_eb, ph, failed);
         if (!failed) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dV = X dO
-            umma::mma_ss(tA, umma::desc_kmajor(aX, kk, ROWS), umma::desc_mnmajor(aDO, kk, ROWS), id_kmn, kk > 0);
+          for (int kk = 0; kk < 8; ++kk)  // dV = X dO (X in TMEM)
+            umma::mma_ts(tA, tX + 8 * kk, umma::desc_mnmajor(aDO, kk, ROWS), id_kmn, kk > 0);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dV += K~dec Eb
             umma::mma_ss(tA, umma::desc_kmajor(aK, kk, ROWS), umma::desc_mnmajor(aE, kk, ROWS), id_kmn, 1u);
@@ -779,8 +773,8 @@ __global__ void __launch_bounds__(NTO, 1)
         wait_or_fail(&sh.bar_xp, ph, failed);
         if (!failed) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dK~ = X' Q~
-            umma::mma_ss(tB, umma::desc_kmajor(aX, kk, ROWS), umma::desc_mnmajor(aQ, kk, ROWS), id_kmn, kk > 0);
+          for (int kk = 0; kk < 8; ++kk)  // dK~ = X' Q~ (X' in TMEM)
+            umma::mma_ts(tB, tX + 64 + 8 * kk, umma::desc_mnmajor(aQ, kk, ROWS), id_kmn, kk > 0);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dK~ += Vdec Eb^T
             umma::mma_ss(tB, umma::desc_kmajor(aV, kk, ROWS), umma::desc_kmajor(aE, kk, ROWS), id_kk, 1u);
@@ -812,9 +806,14 @@ __global__ void __launch_bounds__(NTO, 1)
             tma_tile(Kt, &tmk, b, h, c0 - CV, &sh.bar_k);
           }
         }
-        // dk out of V, then V takes the tile before
+        // dk out of V, then V takes the tile before; [V6] is done with raw k: X
+        // takes raw k of the tile before
         wait_or_fail(&sh.bar_dkout, ph, failed);
         if (!failed) {
+          if (n > 0) {
+            umma::mbar_expect_tx(&sh.bar_kr, tile_bytes);
+            tma_tile(X, &tmk, b, h, c0 - CV, &sh.bar_kr);
+          }
           tma_store_tile(&tmdk, Vt, b, h, c0);
           umma::bulk_commit();
           if (n > 0) {
@@ -902,11 +901,12 @@ __global__ void __launch_bounds__(NTO, 1)
         f2 x[16];
         pairs_of(v, x);
         mask_upper_table(x, sh.du, i, (int)col);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) *tile_at(X, i, 4 * qd + u) = pack4x2(&x[4 * u]);
-        if (qd == sub)  // written in [V1] by warps 4 sub .. 4 sub + 3, ordered by bar_feat -> M1
-          *(reinterpret_cast<__nv_bfloat16 *>(tile_at(X, i, i >> 3)) + (i & 7)) =
-              __float2bfloat16_rn(sh.qk_diag[i]);
+        // X as packed bf16 into TMEM (row i, K = 32 qd .. 32 qd + 31 at columns
+        // 16 qd ..); the diagonal entry (element i - 32 qd on the warps with
+        // qd == sub) is k~_i . q~_i in fp32, written in [V1] by warps
+        // 4 sub .. 4 sub + 3 and ordered by bar_feat -> M1
+        store_tmem_bf16(tX + lane_base + 16 * qd, x, qd == sub ? i - (int)col : -1,
+                        qd == sub ? sh.qk_diag[i] : 0.f);
         const f2 w = dup2(wdec);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -917,6 +917,7 @@ __global__ void __launch_bounds__(NTO, 1)
           for (int e = 0; e < 4; ++e) f[e] = mul2(f[e], w);
           *p = pack4x2(f);
         }
+        umma::tmem_wait_st();
       }
       warp_arrive(&sh.bar_x, lane);
 
@@ -943,16 +944,13 @@ __global__ void __launch_bounds__(NTO, 1)
         f2 x[16];
         pairs_of(v, x);
         mask_upper_table(x, sh.du, i, (int)col);
-        wait_or_fail(&sh.bar_dv, ph, failed);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) *tile_at(X, i, 4 * qd + u) = pack4x2(&x[4 * u]);
-        if (qd == sub) *(reinterpret_cast<__nv_bfloat16 *>(tile_at(X, i, i >> 3)) + (i & 7)) = __float2bfloat16_rn(vdiag);
+        store_tmem_bf16(tX + 64 + lane_base + 16 * qd, x, qd == sub ? i - (int)col : -1, vdiag);
+        umma::tmem_wait_st();
       }
       warp_arrive(&sh.bar_xp, lane);
 
-      // [V5] dv (dV is complete) -> K over K~dec, for a TMA store
-      uint4 kraw[4];  // raw k pairs of row i for [V6], in flight meanwhile
-      load_pairs(kraw, row_ptr(P.k, P, b, h, valid ? c0 + i : c0), qd, valid);
+      // [V5] after dV: dv -> K over K~dec, for a TMA store
+      wait_or_fail(&sh.bar_dv, ph, failed);
       {
         float v[32];
         umma::tmem_ld2x16(tA + lane_base + col, v);
@@ -978,7 +976,12 @@ __global__ void __launch_bounds__(NTO, 1)
         }
       }
       warp_arrive(&sh.bar_qw, lane);
-      feature_grad_pairs(tB + lane_base, kraw, P.kscale, pos, i, qd, sub, P.eps, sh.ru, sh.red_dk, Vt);
+      wait_or_fail(&sh.bar_kr, ph, failed);
+      {
+        uint4 kraw[4];  // raw k pairs of row i
+        ld_pairs(X, i, qd, kraw);
+        feature_grad_pairs(tB + lane_base, kraw, P.kscale, pos, i, qd, sub, P.eps, sh.ru, sh.red_dk, Vt);
+      }
       warp_arrive(&sh.bar_dkout, lane);
     }
   }
