@@ -143,13 +143,12 @@ struct DqShared {
   uint64_t bar_v;       // TMA: v into V
   uint64_t bar_g;       // TMA: gate of tile n into Q
   uint64_t bar_qr;      // TMA: raw q of tile n into its (freed) K buffer, for [W6]
-  uint64_t bar_dy;      // TMA: dy of tile n into PM (once MMA7 of tile n - 1 has read dPm)
+  uint64_t bar_dy;      // TMA: dy of tile n into PM (once the dgate store of tile n - 1 has read it)
   uint64_t bar_p;       // MMA1 done (P)
   uint64_t bar_o;       // MMA2 done (O = Q~ Sb)
   uint64_t bar_m3;      // MMA3 done (O complete)
   uint64_t bar_m56;     // MMA5 + MMA6 done (dP, I)
   uint64_t bar_m74;     // MMA7 + MMA4 done (dQ~ complete, S carried)
-  uint64_t bar_rd;      // issuer: the dgate / dO stores have read PM / Q
   uint64_t bar_feat, bar_sb, bar_pm, bar_do, bar_w5, bar_w6;  // workers, one arrive per warp
   uint32_t tmem_base;
   uint32_t failed;
@@ -180,15 +179,18 @@ __device__ __forceinline__ f2 sigmoid2(f2 z) {
 //        Sb -> bf16 S
 //   [W4] dgate -> PM (over dy), dO -> Q (over the gate), fp32 v_i . do_i
 //   [W6] dq of tile n - 1 (RoPE^T, RMSNorm backward) in its K buffer, over its raw q
-//   [W5] dPm -> PM (fp32 v_i . do_i on the diagonal), I <- gamma^{i+1} I, V -> Vdec
+//   [W5] dPm (fp32 v_i . do_i on the diagonal) into the dP columns of TMEM,
+//        I <- gamma^{i+1} I, V -> Vdec
 // so the dq epilogue of tile n - 1 runs while MMA5 / MMA6 of tile n are in
 // flight.  The issuer warp (16) waits for each hand-off, issues the MMAs and
 // moves every tile by TMA: q, k (double-buffered), v, the gate (into Q once
-// MMA2 has read it), dy (into PM once MMA7 of the tile before has read dPm: a
-// tile ahead), raw q again for [W6] (into the K buffer that MMA7 / MMA4 freed),
-// and the stores of dgate, dO and dq.  No operand is read by plain loads: 16-byte loads of dy
-// from 32 rows per warp instruction crowded the load pipeline and stalled every
-// later shared-memory access of the warps (~20 % of a tile).
+// MMA2 has read it), dy (into PM once the dgate store of the tile before has
+// read it: a tile ahead), raw q again for [W6] (into the K buffer that MMA7 /
+// MMA4 freed), and the stores of dgate, dO and dq.  MMA3 and MMA7 take their A
+// operands (Pm, dPm) from tensor memory.  No operand is read by plain loads:
+// 16-byte loads of dy from 32 rows per warp instruction crowded the load
+// pipeline and stalled every later shared-memory access of the warps (~20 % of
+// a tile).
 __global__ void __launch_bounds__(NTO, 1)
     tc_bwd_dq_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmq,
                      const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(NTO, 1)
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   // Q:  raw q -> q~ (fp16) -> gate -> dO (bf16)                 -> next raw q
   // K j: raw k -> k~ (fp16) -> k~ (bf16) -> raw q -> dq (bf16)  -> k two tiles on
-  // V:  v -> Vdec;  SB: Sb (fp16, scaled) -> S (bf16);  PM: dy -> dgate -> dPm
+  // V:  v -> Vdec;  SB: Sb (fp16, scaled) -> S (bf16);  PM: dy -> dgate
   unsigned char *Qs = base, *Vs = base + 3 * TILE, *SB = base + 4 * TILE, *PM = base + 5 * TILE;
   DqShared &sh = *reinterpret_cast<DqShared *>(base + 6 * TILE);
 
@@ -213,7 +215,7 @@ __global__ void __launch_bounds__(NTO, 1)
 
   if (tid == 0) {
     uint64_t *bars[] = {&sh.bar_q, &sh.bar_k[0], &sh.bar_k[1], &sh.bar_v, &sh.bar_g, &sh.bar_qr, &sh.bar_dy,
-                        &sh.bar_p, &sh.bar_o, &sh.bar_m3, &sh.bar_m56, &sh.bar_m74, &sh.bar_rd};
+                        &sh.bar_p, &sh.bar_o, &sh.bar_m3, &sh.bar_m56, &sh.bar_m74};
     for (uint64_t *bar : bars) umma::mbar_init(bar, 1);
     uint64_t *wbars[] = {&sh.bar_feat, &sh.bar_sb, &sh.bar_pm, &sh.bar_do, &sh.bar_w5, &sh.bar_w6};
     for (uint64_t *bar : wbars) umma::mbar_init(bar, NWORK);
@@ -240,8 +242,7 @@ __global__ void __launch_bounds__(NTO, 1)
       const uint32_t id_kmn = umma::idesc_bf16(128, 128, false, true);        // Pm V, dPm K~
       const uint32_t id_kk = umma::idesc_bf16(128, 128, false, false);        // dO V^T, dO S^T
       const uint32_t id_mnmn = umma::idesc_bf16(128, 128, true, true);        // K~^T Vdec
-      const uint32_t aq = umma::smem_u32(Qs), av = umma::smem_u32(Vs), asb = umma::smem_u32(SB),
-                     apm = umma::smem_u32(PM);
+      const uint32_t aq = umma::smem_u32(Qs), av = umma::smem_u32(Vs), asb = umma::smem_u32(SB);
       umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
       tma_tile(Qs, &tmq, b, h, t0, &sh.bar_q);
       for (int n = 0; n < 2 && n < ntile; ++n) {
@@ -312,8 +313,11 @@ __global__ void __launch_bounds__(NTO, 1)
             umma::mma_ss(ta, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(asb, kk, ROWS), id_kk, kk > 0);
           umma::commit(&sh.bar_m56);
           umma::bulk_wait_read();
+          if (n + 1 < ntile) {  // the dgate store has read PM: it takes dy of the next tile
+            umma::mbar_expect_tx(&sh.bar_dy, tile_bytes);
+            tma_tile(PM, &tmdy, b, h, c0 + CV, &sh.bar_dy);
+          }
         }
-        umma::mbar_arrive(&sh.bar_rd);  // PM may take dPm (also on failure: nobody may wait forever)
         // MMA5 / MMA6 done and dO stored: Q takes the next q
         wait_or_fail(&sh.bar_m56, ph, failed);
         if (!failed && n + 1 < ntile) {
@@ -338,8 +342,9 @@ __global__ void __launch_bounds__(NTO, 1)
         wait_or_fail(&sh.bar_w5, ph, failed);
         if (!failed) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma::mma_ss(ta, umma::desc_kmajor(apm, kk, ROWS), umma::desc_mnmajor(ak, kk, ROWS), id_kmn, 1u);
+          for (int kk = 0; kk < 8; ++kk)  // A = dPm from the dP columns of TMEM
+            umma::mma_ts(ta, tP + 32 * (kk >> 1) + 8 * (kk & 1), umma::desc_mnmajor(ak, kk, ROWS),
+                         id_kmn, 1u);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma::mma_ss(tS, umma::desc_mnmajor(ak, kk, ROWS), umma::desc_mnmajor(av, kk, ROWS), id_mnmn, 1u);
@@ -354,10 +359,7 @@ __global__ void __launch_bounds__(NTO, 1)
           }
           umma::mbar_expect_tx(&sh.bar_qr, tile_bytes);
           tma_tile(Kt, &tmq, b, h, c0, &sh.bar_qr);
-          if (n + 1 < ntile) {  // MMA7 has read dPm: PM takes dy of the next tile
-            umma::mbar_expect_tx(&sh.bar_dy, tile_bytes);
-            tma_tile(PM, &tmdy, b, h, c0 + CV, &sh.bar_dy);
-          }
+
         }
       }
       // dq of the last tile
@@ -585,23 +587,21 @@ __global__ void __launch_bounds__(NTO, 1)
       }
 
       if (have) {
-        // [W5] after MMA5 / MMA6 and the stores' reads: dPm -> PM (diagonal: fp32
-        // v_i . do_i), I <- gamma^{i+1} I, V -> Vdec (in place)
+        // [W5] after MMA5 / MMA6: dPm (diagonal: fp32 v_i . do_i) over the dP
+        // columns of TMEM (MMA7's A operand, laid out as Pm in [W3]),
+        // I <- gamma^{i+1} I, V -> Vdec (in place)
         wait_or_fail(&sh.bar_m56, ph, failed);
-        wait_or_fail(&sh.bar_rd, ph, failed);
         {
           float pv[32];
           umma::tmem_ld2x16(myP, pv);
           f2 x[16];
           pairs_of(pv, x);
           mask_lower_table(x, sh.dm, i, (int)col);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) *tile_at(PM, i, 4 * qd + u) = pack4x2(&x[4 * u]);
-          if (qd == sub) {
-            const float vd = sh.vd_part[0][i] + sh.vd_part[1][i] + sh.vd_part[2][i] + sh.vd_part[3][i];
-            *(reinterpret_cast<__nv_bfloat16 *>(tile_at(PM, i, i >> 3)) + (i & 7)) = __float2bfloat16_rn(vd);
-            if (valid) P.ddiag[((size_t)b * P.T + c0 + i) * P.H + h] = vd;
-          }
+          const float vd = qd == sub ? sh.vd_part[0][i] + sh.vd_part[1][i] + sh.vd_part[2][i] +
+                                           sh.vd_part[3][i]
+                                     : 0.f;
+          store_tmem_bf16(myP, x, qd == sub ? i - (int)col : -1, vd);
+          if (qd == sub && valid) P.ddiag[((size_t)b * P.T + c0 + i) * P.H + h] = vd;
           float iv[32];
           umma::tmem_ld2x16(ta + col, iv);
           const f2 wi = dup2(sh.pw[i + 1]);
