@@ -75,7 +75,9 @@ __global__ void __launch_bounds__(NTO, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int np = P.npart > 1 ? P.npart : 1;
-  const int g = blockIdx.x / np, piece = blockIdx.x % np, h = blockIdx.y, b = blockIdx.z;
+  // heads in reverse launch order: under the paper's schedule gamma_h grows with
+  // h, so the slowest-decaying heads, whose pieces are the longest, start first
+  const int g = blockIdx.x / np, piece = blockIdx.x % np, h = P.H - 1 - blockIdx.y, b = blockIdx.z;
   const int t0 = g * P.seg_len, t1 = min(P.T, t0 + P.seg_len);
   const int CV = P.chunk;
   const int L = t1 - t0;
