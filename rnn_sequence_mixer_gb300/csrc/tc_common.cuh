@@ -18,9 +18,7 @@ namespace {
 
 constexpr int D = 128;
 constexpr int ROWS = 128;           // rows of every operand tile
-constexpr int NT = 512;             // threads per CTA of the lockstep kernels
-constexpr int NWORK = 16;              // worker warps (CUDA-core work) of the warp-specialized
-                                       // kernels, 4 warpgroups
+constexpr int NWORK = 16;              // worker warps (CUDA-core work), 4 warpgroups
 constexpr int NTO = (NWORK + 4) * 32;  // + one warpgroup: its first warp issues MMAs / TMA copies
                                        // (registers are granted per warpgroup, so a lone 17th
                                        // warp would cost as much as four)
@@ -30,39 +28,13 @@ constexpr int HALF_TILE = TILE / 2; // one 64-column block
 
 // ------------------------------------------------------------------ small helpers
 
-__device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
-}
-
-__device__ __forceinline__ void unpack8h(const uint4 &u, float (&f)[8]) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
-    f[2 * i] = t.x;
-    f[2 * i + 1] = t.y;
-  }
-}
-
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t *>(&h);
 }
-__device__ __forceinline__ uint4 pack8(const float *f) {
-  return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
-}
 __device__ __forceinline__ uint32_t pack2h(float a, float b) {
   __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t *>(&h);
-}
-__device__ __forceinline__ uint4 pack8h(const float *f) {
-  return make_uint4(pack2h(f[0], f[1]), pack2h(f[2], f[3]), pack2h(f[4], f[5]),
-                    pack2h(f[6], f[7]));
 }
 
 // ------------------------------------------------------------------ packed fp32
@@ -141,23 +113,6 @@ __device__ __forceinline__ uint4 *tile_at(unsigned char *tile, int row, int chun
   return reinterpret_cast<uint4 *>(tile + umma::sw128_off(row, chunk, ROWS));
 }
 
-__device__ __forceinline__ uint4 ldg16(const void *p) {
-  return __ldg(reinterpret_cast<const uint4 *>(p));
-}
-
-// Row t of a [B, T, H, D] bf16 tensor for (b, h).
-__device__ __forceinline__ const __nv_bfloat16 *row_ptr(const void *X, const MixerParams &P, int b,
-                                                        int h, long long t) {
-  return (const __nv_bfloat16 *)X + (((size_t)b * P.T + t) * P.H + h) * D;
-}
-
-// Elements [32 qd, 32 qd + 32) of a row.
-__device__ __forceinline__ void load_quarter(uint4 (&r)[4], const __nv_bfloat16 *row, int qd,
-                                             bool valid) {
-#pragma unroll
-  for (int u = 0; u < 4; ++u) r[u] = valid ? ldg16(row + 32 * qd + 8 * u) : make_uint4(0, 0, 0, 0);
-}
-
 // This thread's 16 RoPE pairs of a row sit in chunks {2qd, 2qd+1} (elements
 // 16qd..16qd+15) and {8+2qd, 9+2qd} (elements 64+16qd..): read them from an
 // operand tile.
@@ -225,90 +180,11 @@ __device__ __forceinline__ void load_rope_table(unsigned long long *ru, const Mi
   if (tid < kMaxPairs) ru[4 * (tid & 15) + (tid >> 4)] = P.rope_u[tid];
 }
 
-// the hardware tanh, and sigmoid through it: 1 / (1 + e^-z) = 0.5 + 0.5 tanh(z / 2).
+// the hardware tanh (sigmoid through it: 1 / (1 + e^-z) = 0.5 + 0.5 tanh(z / 2)).
 __device__ __forceinline__ float tanh_fast(float x) {
   float t;
   asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(x));
   return t;
-}
-__device__ __forceinline__ float sigmoid_fast(float z) { return fmaf(0.5f, tanh_fast(0.5f * z), 0.5f); }
-
-// Causal mask of one 32-column block of a score row: v gets columns
-// [32 qd, 32 qd + 32) of row i = 32 sub + lane from TMEM at taddr, keeping
-// j <= i with weight gamma^{i-j} (pw[m] = gamma^m) and zeroing the rest; every
-// entry of an invalid row (!valid) is zeroed.  The warp's block lies wholly
-// above the diagonal (qd > sub: zeros, no TMEM read), wholly below it (qd < sub:
-// no compares) or on it.  If `dset`, the diagonal entry is replaced by `dval`
-// before weighting.  Warp-collective.
-__device__ __forceinline__ void mask_lower_block(uint32_t taddr, float (&v)[32], int i, int sub, int qd,
-                                                 bool valid, float gm, const float *pw, bool dset = false,
-                                                 float dval = 0.f) {
-  if (qd > sub) {
-#pragma unroll
-    for (int e = 0; e < 32; ++e) v[e] = 0.f;
-    return;
-  }
-  umma::tmem_ld2x16(taddr, v);
-  const int jlo = 32 * qd;
-  if (qd < sub) {
-    float w = valid ? pw[i - jlo - 31] : 0.f;
-#pragma unroll
-    for (int e = 31; e >= 0; --e) {
-      v[e] *= w;
-      w *= gm;
-    }
-    return;
-  }
-  const int d = i - jlo;  // lane: the diagonal entry of this row
-  float w = valid ? 1.f : 0.f;
-#pragma unroll
-  for (int e = 31; e >= 0; --e) {
-    if (e <= d) {
-      if (dset && e == d) v[e] = dval;
-      v[e] *= w;
-      w *= gm;
-    } else {
-      v[e] = 0.f;
-    }
-  }
-}
-
-// Transposed mask: keep i <= j < c with weight gamma^{j-i}.  Blocks wholly
-// below the diagonal (qd < sub) are zero without a TMEM read; blocks wholly
-// above it need the j < c test only when the tile is short.  Same conventions
-// as mask_lower_block.
-__device__ __forceinline__ void mask_upper_block(uint32_t taddr, float (&v)[32], int i, int sub, int qd,
-                                                 int c, bool valid, float gm, const float *pw,
-                                                 bool dset = false, float dval = 0.f) {
-  if (qd < sub) {
-#pragma unroll
-    for (int e = 0; e < 32; ++e) v[e] = 0.f;
-    return;
-  }
-  umma::tmem_ld2x16(taddr, v);
-  const int jlo = 32 * qd;
-  if (qd > sub && jlo + 32 <= c) {
-    float w = valid ? pw[jlo - i] : 0.f;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      v[e] *= w;
-      w *= gm;
-    }
-    return;
-  }
-  const int j0 = max(i, jlo);
-  float w = (valid && j0 < jlo + 32) ? pw[j0 - i] : 0.f;
-#pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    const int j = jlo + e;
-    if (j >= i && j < c) {
-      if (dset && j == i) v[e] = dval;
-      v[e] *= w;
-      w *= gm;
-    } else {
-      v[e] = 0.f;
-    }
-  }
 }
 
 // Decay table of the causal mask, read backwards, in four copies shifted by
@@ -441,14 +317,6 @@ __device__ __forceinline__ void sync_tc() {
   umma::fence_before();
   __syncthreads();
   umma::fence_after();
-}
-
-// Bounded wait on an mbarrier phase, with a CTA-wide vote so that every
-// thread leaves together when any of them gives up.
-__device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity) {
-  const bool late = !umma::mbar_wait(bar, parity);
-  umma::fence_after();
-  return __syncthreads_or(late) != 0;
 }
 
 // TMA of one raw [rows, 128] bf16 tile (rows = chunk) of token rows
