@@ -63,3 +63,39 @@ def test_backward_with_pieces(case):
         assert err <= 2e-2, f"{name}: {err:.3e}"
     dsi = f64(torch.stack([out[4][0, h] for h in HEADS]).unsqueeze(0))
     assert max_rel_err(dsi, ref[4], head_axes=(0, 1)) <= 2e-2
+
+
+def test_arbitrary_gammas_forward_and_backward():
+    """Per-head gamma drawn over (0, 1] (not the paper's schedule): each head
+    keeps a different number of non-zero-weight tiles and pieces.  152 heads of
+    5000 tokens are one segment each; sampled heads against the oracle."""
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    dev = torch.device("cuda:0")
+    B_, T_, H_ = 1, 5000, 152
+    rng = np.random.default_rng(7)
+    g = np.exp(-10.0 ** rng.uniform(-4.5, 1.0, size=H_)).astype(np.float32)  # 0.99997 .. 4.5e-5
+    g[3] = 0.99999
+    heads = [0, 3, 50, 100, 151]
+    inp = inputs.mixer_inputs(B_, T_, H_, D, torch.bfloat16, 93, device=dev, with_dy=True)
+    s0 = inputs.state(B_, H_, D, 94, 0.1, device=dev)
+    dso = inputs.state(B_, H_, D, 95, 0.05, device=dev)
+    gt = torch.from_numpy(g)
+    y, o, st = api.prefill(inp["q"], inp["k"], inp["v"], inp["gate"], gt, s0, chunk=128,
+                           rope_base=1e6, want_o=True)
+    grads = api.prefill_backward(inp["q"], inp["k"], inp["v"], inp["gate"], gt, inp["dy"], s0, dso,
+                                 chunk=128, rope_base=1e6, want_dstate_in=True)
+    torch.cuda.synchronize()
+    sel = lambda t: f64(torch.stack([t[0, :, h, :] for h in heads], dim=1).unsqueeze(0))
+    selst = lambda t: f64(torch.stack([t[0, h] for h in heads]).unsqueeze(0))
+    gg = g[heads].astype(np.float64)
+    ry, ro, rs = oracle.prefill(sel(inp["q"]), sel(inp["k"]), sel(inp["v"]), sel(inp["gate"]), gg,
+                                selst(s0), base=1e6)
+    assert max_rel_err(sel(y), ry) <= 2e-2
+    assert max_rel_err(sel(o), ro) <= 2e-2
+    assert max_rel_err(selst(st), rs, head_axes=(0, 1)) <= 2e-2
+    ref = oracle.backward(sel(inp["q"]), sel(inp["k"]), sel(inp["v"]), sel(inp["gate"]), gg,
+                          sel(inp["dy"]), selst(s0), selst(dso), base=1e6)
+    for name, got, want in zip(["dq", "dk", "dv", "dgate"], grads[:4], ref[:4]):
+        err = max_rel_err(sel(got), want)
+        assert err <= 2e-2, f"{name}: {err:.3e}"
+    assert max_rel_err(selst(grads[4]), ref[4], head_axes=(0, 1)) <= 2e-2
