@@ -47,6 +47,9 @@ def parse():
                    help="target CPU time of the oracle sample")
     p.add_argument("--prefill-T", type=int, default=0,
                    help="override T of the prefill workload (small cases for ncu captures)")
+    p.add_argument("--fb-recompute", action="store_true",
+                   help="forward + backward without saved features (the backward "
+                        "recomputes the q / k feature map)")
     p.add_argument("--backward-B", type=int, default=0,
                    help="override B of the forward+backward workload (small cases for ncu captures)")
     return p.parse_args()
@@ -516,16 +519,19 @@ def run_ours(args):
         wsb = torch.empty(api.backward_workspace_size(shp), dtype=torch.uint8, device=dev)
         wsf = torch.empty(api.prefill_workspace_size(shp), dtype=torch.uint8, device=dev)
         yb = torch.empty_like(ib["q"])
+        # the features the forward saves for the backward (fp16 q~, k~ and the norms)
+        svb = (None if args.fb_recompute else
+               torch.empty(api.saved_bytes(shp), dtype=torch.uint8, device=dev))
 
         def fb_step(i, trace):
             api.prefill(ib["q"], ib["k"], ib["v"], ib["gate"], gb, chunk=wb.chunk,
                         rope_base=wb.rope_base, eps=wb.eps, y=yb, want_state=False, workspace=wsf,
-                        trace=trace[:4] if trace else None)
+                        trace=trace[:4] if trace else None, saved=svb)
             # the backward reads the segment states the forward left in its
-            # workspace (saved for backward) instead of recomputing them
+            # workspace and the features it saved instead of recomputing them
             api.prefill_backward(ib["q"], ib["k"], ib["v"], ib["gate"], gb, ib["dy"],
                                  chunk=wb.chunk, rope_base=wb.rope_base, eps=wb.eps, workspace=wsb,
-                                 trace=trace[4:] if trace else None, fwd_workspace=wsf)
+                                 trace=trace[4:] if trace else None, fwd_workspace=wsf, saved=svb)
 
         b_steps = max(1, min(args.steps, 5))
         b_ms, b_passes = timed(fb_step, b_steps, 1, stream, D, trace_count=11)
@@ -546,8 +552,10 @@ def run_ours(args):
                           "Mtok_s": job_rate(wb.B * wb.T, b_ms, D.world) / 1e6,
                           "alg_bytes": alg_b, "frac_hbm": alg_b / (b_ms / 1e3) / 1e9 / hbm_peak,
                           "tensor_flops": flops_b, "roofline_ms": roof_ms,
-                          "frac_roofline": roof_ms / b_ms, "pass_ms": b_pass_ms}
-        del ib, wsb, wsf, yb
+                          "frac_roofline": roof_ms / b_ms, "pass_ms": b_pass_ms,
+                          "saved_features": svb is not None,
+                          "saved_bytes": 0 if svb is None else svb.numel()}
+        del ib, wsb, wsf, yb, svb
         torch.cuda.empty_cache()
 
     # ---------------------------------------------------------------- MMA ceiling

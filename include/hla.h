@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define HLA_ABI_VERSION 2
+#define HLA_ABI_VERSION 3
 
 typedef enum {
   HLA_OK = 0,
@@ -119,6 +119,20 @@ hla_status hla_gamma_schedule(int32_t H, float *gamma_out);
 size_t hla_prefill_workspace_size(const hla_shape *shape);
 
 /*
+ * Bytes of the features hla_prefill can save for hla_prefill_backward (its
+ * `saved` argument).  Non-zero only for bf16 at d = 128 (the tensor-core
+ * path); 0 on a bad shape or where saving is not supported.  Layout, all
+ * device memory, B, T, H of the shape, d = 128:
+ *   q~   fp16 [B, T, H, d]   RoPE(Norm(q))            at byte 0
+ *   k~   fp16 [B, T, H, d]   RoPE(Norm(k)) / sqrt(d)  at byte 2 B T H d
+ *   fp32 [3, B, H, T]                                  at byte 4 B T H d:
+ *        [0] 1 / RMS(q_t), [1] 1 / RMS(k_t)   (RMS(x) = sqrt(mean(x^2) + eps))
+ *        [2] q~_t . k~_t, accumulated in fp32 before the fp16 rounding
+ * Total B T H (4 d + 12) bytes.
+ */
+size_t hla_saved_bytes(const hla_shape *shape);
+
+/*
  * Forward over T tokens (prefill), Eq. 18 for every (b, h, t).
  *   q, k, v, gate  in:  [B, T, H, d], shape->dtype, raw (pre-norm, pre-RoPE,
  *                       pre-sigmoid)
@@ -136,13 +150,21 @@ size_t hla_prefill_workspace_size(const hla_shape *shape);
  *                  device-side wait gave up (HLA_ERR_TIMEOUT) and the outputs
  *                  of the affected segments are not valid
  *   trace          optional pass events (see hla_trace); NULL = none
+ *   saved          out: optional, hla_saved_bytes() bytes of device memory;
+ *                  the call also writes the features the backward needs
+ *                  there (layout at hla_saved_bytes), so that
+ *                  hla_prefill_backward can read them instead of recomputing
+ *                  the q/k feature map.  NULL = skip.  On a shape whose
+ *                  hla_saved_bytes() is 0 a non-NULL pointer returns
+ *                  HLA_ERR_UNSUPPORTED.  y, o and the state are the same with
+ *                  and without it.
  * The output of token t depends on all tokens <= t of its sequence and on
  * state_in; sequences and heads are independent.
  */
 hla_status hla_prefill(const hla_shape *shape, const void *q, const void *k, const void *v,
                        const void *gate, const float *gamma, const float *state_in,
                        float *state_out, void *y, float *o, void *ws, size_t ws_bytes,
-                       hla_stream stream, const hla_trace *trace);
+                       hla_stream stream, const hla_trace *trace, void *saved);
 
 /*
  * hla_prefill for callers that cannot allocate device memory.  The paper has
@@ -220,6 +242,15 @@ size_t hla_backward_workspace_size(const hla_shape *shape);
  *                    only.  NULL = recompute.  Passing a workspace that does
  *                    not hold those states gives wrong gradients; nothing can
  *                    check it.
+ *   saved            optional: the `saved` buffer of an hla_prefill call with
+ *                    the same shape, q and k, enqueued before this call and
+ *                    not reused since.  The dq and dk/dv passes read q~, k~
+ *                    and the norms from it instead of recomputing them.  Read
+ *                    only.  NULL = recompute.  HLA_ERR_UNSUPPORTED where
+ *                    hla_saved_bytes() is 0.  Gradients agree with the
+ *                    recomputing path up to the fp16 rounding of q~ and k~
+ *                    (the RMSNorm backward then starts from the rounded
+ *                    features).
  * o and the per-chunk states inside a segment are always recomputed; hla_prefill
  * stores neither.
  */
@@ -228,7 +259,7 @@ hla_status hla_prefill_backward(const hla_shape *shape, const void *q, const voi
                                 const float *state_in, const void *dy, const float *dstate_out,
                                 void *dq, void *dk, void *dv, void *dgate, float *dstate_in,
                                 void *ws, size_t ws_bytes, hla_stream stream,
-                                const hla_trace *trace, const void *fwd_ws);
+                                const hla_trace *trace, const void *fwd_ws, const void *saved);
 
 #ifdef __cplusplus
 }

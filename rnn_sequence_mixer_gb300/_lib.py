@@ -24,6 +24,7 @@ EXPORTS = (
     "hla_status_string",
     "hla_gamma_schedule",
     "hla_prefill_workspace_size",
+    "hla_saved_bytes",
     "hla_prefill",
     "hla_decode_step",
     "hla_backward_workspace_size",
@@ -87,18 +88,20 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.hla_gamma_schedule.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_float)]
     lib.hla_prefill_workspace_size.restype = sz
     lib.hla_prefill_workspace_size.argtypes = [shp]
+    lib.hla_saved_bytes.restype = sz
+    lib.hla_saved_bytes.argtypes = [shp]
     lib.hla_backward_workspace_size.restype = sz
     lib.hla_backward_workspace_size.argtypes = [shp]
     lib.hla_prefill.restype = ctypes.c_int
     trp = ctypes.POINTER(HlaTrace)
     lib.hla_prefill.argtypes = [shp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_float), f32p, f32p, vp,
-                                f32p, vp, sz, vp, trp]
+                                f32p, vp, sz, vp, trp, vp]
     lib.hla_decode_step.restype = ctypes.c_int
     lib.hla_decode_step.argtypes = [shp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_float), i64p,
                                     f32p, f32p, vp, f32p, vp]
     lib.hla_prefill_backward.restype = ctypes.c_int
     lib.hla_prefill_backward.argtypes = [shp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_float), f32p,
-                                         vp, f32p, vp, vp, vp, vp, f32p, vp, sz, vp, trp, vp]
+                                         vp, f32p, vp, vp, vp, vp, f32p, vp, sz, vp, trp, vp, vp]
     lib.hla_prefill_noalloc.restype = ctypes.c_int
     lib.hla_prefill_noalloc.argtypes = [shp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_float), f32p,
                                         f32p, vp, f32p, vp]

@@ -73,8 +73,24 @@ def prefill_workspace_size(shape: _lib.HlaShape) -> int:
     return int(_lib.load().hla_prefill_workspace_size(ctypes.byref(shape)))
 
 
+def saved_bytes(shape: _lib.HlaShape) -> int:
+    """hla_saved_bytes: size of the ``saved`` buffer of prefill / prefill_backward
+    (0 where the shape cannot save its features)."""
+    return int(_lib.load().hla_saved_bytes(ctypes.byref(shape)))
+
+
 def backward_workspace_size(shape: _lib.HlaShape) -> int:
     return int(_lib.load().hla_backward_workspace_size(ctypes.byref(shape)))
+
+
+def _check_saved(saved, shape):
+    if saved is None:
+        return
+    need = saved_bytes(shape)
+    if saved.dtype != torch.uint8 or not saved.is_cuda or not saved.is_contiguous():
+        raise ValueError("saved must be a contiguous uint8 CUDA tensor")
+    if need and saved.numel() < need:
+        raise ValueError(f"saved holds {saved.numel()} bytes, the shape needs {need}")
 
 
 def _stream(device) -> ctypes.c_void_p:
@@ -99,9 +115,11 @@ def _trace(events, device):
 
 def prefill(q, k, v, gate, gamma: Sequence[float] | torch.Tensor, state_in=None, *, chunk=64,
             pos_offset=0, rope_base=1e4, eps=1e-6, want_o=False, want_state=True, y=None,
-            state_out=None, workspace=None, trace=None):
+            state_out=None, workspace=None, trace=None, saved=None):
     """hla_prefill.  Returns (y, o or None, state_out or None).  ``trace``: optional
-    list of torch.cuda.Event recorded before each pass and after the last."""
+    list of torch.cuda.Event recorded before each pass and after the last.
+    ``saved``: optional uint8 CUDA tensor of ``saved_bytes(shape)`` bytes that
+    receives the features for ``prefill_backward(..., saved=...)``."""
     _check_acts(q, k, v, gate)
     B, T, H, d = q.shape
     _check_state(state_in, B, H, d, q.device)
@@ -119,10 +137,12 @@ def prefill(q, k, v, gate, gamma: Sequence[float] | torch.Tensor, state_in=None,
     ws_bytes = prefill_workspace_size(shape)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    _check_saved(saved, shape)
     tr = _trace(trace, q.device)
     st = lib.hla_prefill(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(gate), g_ptr,
                          _ptr(state_in), _ptr(state_out), _ptr(y), _ptr(o), _ptr(workspace),
-                         workspace.numel(), _stream(q.device), tr[0] if tr else None)
+                         workspace.numel(), _stream(q.device), tr[0] if tr else None,
+                         _ptr(saved))
     _lib.check(st, "hla_prefill")
     del g_host
     return y, o, state_out
@@ -157,12 +177,13 @@ def decode_step(q, k, v, gate, gamma, state, pos=None, *, pos_offset=0, rope_bas
 
 def prefill_backward(q, k, v, gate, gamma, dy, state_in=None, dstate_out=None, *, chunk=64,
                      pos_offset=0, rope_base=1e4, eps=1e-6, want_dstate_in=False,
-                     workspace=None, trace=None, fwd_workspace=None):
+                     workspace=None, trace=None, fwd_workspace=None, saved=None):
     """hla_prefill_backward.  Returns (dq, dk, dv, dgate, dstate_in or None).
     ``fwd_workspace``: the ``workspace`` of a ``prefill`` call on the same
     shape, inputs, gamma and state_in, enqueued earlier on this stream; the
     backward then reads the forward's segment states instead of recomputing
-    them."""
+    them.  ``saved``: the ``saved`` buffer of such a call; the backward reads
+    the q / k features from it."""
     _check_acts(q, k, v, gate, dy)
     B, T, H, d = q.shape
     _check_state(state_in, B, H, d, q.device)
@@ -176,11 +197,13 @@ def prefill_backward(q, k, v, gate, gamma, dy, state_in=None, dstate_out=None, *
     ws_bytes = backward_workspace_size(shape)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    _check_saved(saved, shape)
     tr = _trace(trace, q.device)
     st = lib.hla_prefill_backward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(gate), g_ptr,
                                   _ptr(state_in), _ptr(dy), _ptr(dstate_out), _ptr(dq), _ptr(dk),
                                   _ptr(dv), _ptr(dg), _ptr(dsi), _ptr(workspace), workspace.numel(),
-                                  _stream(q.device), tr[0] if tr else None, _ptr(fwd_workspace))
+                                  _stream(q.device), tr[0] if tr else None, _ptr(fwd_workspace),
+                                  _ptr(saved))
     _lib.check(st, "hla_prefill_backward")
     del g_host
     return dq, dk, dv, dg, dsi

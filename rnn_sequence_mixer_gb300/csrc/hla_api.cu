@@ -169,6 +169,14 @@ size_t part_bytes(const hla_shape &s, const Plan &p) {
   return n > 1 ? (size_t)s.B * s.H * p.nseg * (size_t)n * s.dk * s.dv * sizeof(float) : 0;
 }
 
+// Bytes of the saved features of a shape: fp16 q~ and k~, and three fp32
+// scalars per row.  0 where the shape runs on the CUDA-core path, which
+// saves nothing.
+size_t saved_bytes(const hla_shape &s) {
+  if (!(s.dtype == HLA_BF16 && s.dk == 128)) return 0;
+  return saved_scalar_offset(s.B, s.T, s.H, s.dk) + 3 * (size_t)s.B * s.T * s.H * sizeof(float);
+}
+
 void fill_rope(MixerParams &P, int D, double base) {
   // One-entry per-thread cache: the table depends only on (base, D).
   thread_local double cached_base = -1.0;
@@ -221,6 +229,11 @@ size_t hla_prefill_workspace_size(const hla_shape *s) {
   return seg_bytes(*s, p) + part_bytes(*s, p) + kStatusBytes;
 }
 
+size_t hla_saved_bytes(const hla_shape *s) {
+  if (check_shape(s, false) != HLA_OK) return 0;
+  return saved_bytes(*s);
+}
+
 size_t hla_backward_workspace_size(const hla_shape *s) {
   if (check_shape(s, false) != HLA_OK) return 0;
   Plan p = make_plan(*s);
@@ -232,7 +245,7 @@ size_t hla_backward_workspace_size(const hla_shape *s) {
 hla_status hla_prefill(const hla_shape *s, const void *q, const void *k, const void *v,
                        const void *gate, const float *gamma, const float *state_in,
                        float *state_out, void *y, float *o, void *ws, size_t ws_bytes,
-                       hla_stream stream, const hla_trace *trace) {
+                       hla_stream stream, const hla_trace *trace, void *saved) {
   HLA_TRY(check_shape(s, false));
   HLA_TRY(check_gamma(gamma, s->H));
   const bool empty = s->B == 0 || s->T == 0;
@@ -245,6 +258,8 @@ hla_status hla_prefill(const hla_shape *s, const void *q, const void *k, const v
   HLA_TRY(maybe(state_out));
   HLA_TRY(maybe(o));
   HLA_TRY(check_trace(trace));
+  HLA_TRY(maybe(saved));
+  if (saved && saved_bytes(*s) == 0) return HLA_ERR_UNSUPPORTED;
   Plan plan = make_plan(*s);
   size_t need_ws = seg_bytes(*s, plan) + part_bytes(*s, plan) + kStatusBytes;
   if (!ws || !aligned16(ws) || ws_bytes < need_ws) return HLA_ERR_WORKSPACE;
@@ -276,6 +291,7 @@ hla_status hla_prefill(const hla_shape *s, const void *q, const void *k, const v
   HLA_LAUNCH(cudaMemsetAsync(P.err, 0, sizeof(unsigned int), st));
   HLA_LAUNCH(tr.mark());
   HLA_LAUNCH(tc ? launch_tc_seg_state(P, st) : launch_simt_seg_state(P, s->dtype, st));
+  P.saved = (unsigned char *)saved;  // written by the output pass only
   HLA_LAUNCH(tr.mark());
   HLA_LAUNCH(launch_state_scan(P, state_out != nullptr, st));
   HLA_LAUNCH(tr.mark());
@@ -322,7 +338,7 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
                                 const void *dy, const float *dstate_out, void *dq, void *dk,
                                 void *dv, void *dgate, float *dstate_in, void *ws,
                                 size_t ws_bytes, hla_stream stream, const hla_trace *trace,
-                                const void *fwd_ws) {
+                                const void *fwd_ws, const void *saved) {
   HLA_TRY(check_shape(s, false));
   HLA_TRY(check_gamma(gamma, s->H));
   const bool empty = s->B == 0 || s->T == 0;
@@ -333,6 +349,8 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
   HLA_TRY(maybe(dstate_in));
   HLA_TRY(check_trace(trace));
   HLA_TRY(maybe(fwd_ws));
+  HLA_TRY(maybe(saved));
+  if (saved && saved_bytes(*s) == 0) return HLA_ERR_UNSUPPORTED;
   Plan plan = make_plan(*s);
   size_t sbytes = seg_bytes(*s, plan);
   size_t need_ws = hla_backward_workspace_size(s);
@@ -376,9 +394,14 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
   HLA_LAUNCH(tr.mark());
   if (!fwd_ws) HLA_LAUNCH(launch_state_scan(P, false, st));
   HLA_LAUNCH(tr.mark());
+  P.saved = (unsigned char *)const_cast<void *>(saved);  // read by the dq and dk/dv passes
   HLA_LAUNCH(tc ? launch_tc_bwd_dq(P, st) : launch_simt_bwd_dq(P, s->dtype, st));
   HLA_LAUNCH(tr.mark());
-  HLA_LAUNCH(tc ? launch_tc_seg_gstate(P, st) : launch_simt_seg_gstate(P, s->dtype, st));
+  {
+    MixerParams Pg = P;  // the state-gradient pass recomputes q~ from raw q
+    Pg.saved = nullptr;
+    HLA_LAUNCH(tc ? launch_tc_seg_gstate(Pg, st) : launch_simt_seg_gstate(Pg, s->dtype, st));
+  }
   HLA_LAUNCH(tr.mark());
   HLA_LAUNCH(launch_grad_scan(P, dstate_in != nullptr, st));
   HLA_LAUNCH(tr.mark());

@@ -47,6 +47,12 @@ struct MixerParams {
   void *dq, *dk, *dv, *dg;
   float *dstate_in;
   unsigned int *err;       // device status word: bits set when a bounded wait gave up
+  // Features saved by the forward for the backward (tensor-core path only;
+  // nullptr = none): q~ and k~ as fp16 [B, T, H, D] (k~ includes 1/sqrt(d)),
+  // then fp32 [3][B, H, T]: 1/RMS(q), 1/RMS(k) and the fp32 q~_t . k~_t.
+  // Written by the output pass when the forward is given one, read by the
+  // backward passes instead of recomputing the feature map.
+  unsigned char *saved;
   float gamma[kMaxHeads];
   // RoPE phase increment of pair i, in units of 2^-64 turns:
   // round(frac(rope_base^(-2i/D) / (2 pi)) * 2^64).  The angle of position p is
@@ -145,6 +151,21 @@ __host__ __device__ inline int piece_count(long long W, int L, int CV, bool grad
   return (nt + kPieceTiles - 1) / kPieceTiles;
 }
 
+// ------------------------------------------------------------------ saved features
+// Byte offset of k~ in the saved buffer, and of the fp32 per-row scalars.
+__host__ __device__ inline size_t saved_k_offset(int B, int T, int H, int D) {
+  return (size_t)B * T * H * D * 2;
+}
+__host__ __device__ inline size_t saved_scalar_offset(int B, int T, int H, int D) {
+  return 2 * saved_k_offset(B, T, H, D);
+}
+enum { kSavedRq = 0, kSavedRk = 1, kSavedDiag = 2 };
+// Scalar f of row (b, h, t).
+__device__ __forceinline__ float *saved_scalar(const MixerParams &P, int f, int b, int h, int t) {
+  float *base = reinterpret_cast<float *>(P.saved + saved_scalar_offset(P.B, P.T, P.H, P.D));
+  return base + (((size_t)f * P.B + b) * P.H + h) * (size_t)P.T + t;
+}
+
 // ------------------------------------------------------------------ host side
 
 Plan make_plan(const hla_shape &s);
@@ -158,6 +179,7 @@ cudaError_t pass_state(const hla_shape &s, const float *in, float *out, cudaStre
 void fill_common(MixerParams &P, const hla_shape &s, const float *gamma);
 size_t seg_bytes(const hla_shape &s, const Plan &p);
 size_t part_bytes(const hla_shape &s, const Plan &p);
+size_t saved_bytes(const hla_shape &s);
 int part_count(const hla_shape &s, const Plan &p);
 void fill_rope(MixerParams &P, int D, double base);
 

@@ -127,6 +127,63 @@ __device__ __forceinline__ void feature_grad_pairs(uint32_t tmem_row, const uint
   }
 }
 
+// The same gradient from the saved features instead of the raw row.  With
+// x^ = Norm(x) rotated (x^ = xscale * xt, xt the saved fp16 row in ld_pairs
+// layout), r = 1 / RMS(x) saved by the forward and g~ = gscale * (the TMEM
+// row): RoPE is orthogonal, so g . Norm(x) = g~ . x^ and
+//   dL/dx = r RoPE^T (g~ - x^ (g~ . x^) / d),
+// one row sum instead of two and no raw row (gscale rides on r: the bracket
+// is linear in g~).  red is [4][ROWS]; the call holds named barrier 5 + sub.
+__device__ __forceinline__ void feature_grad_saved(uint32_t tmem_row, const uint4 (&xt)[4],
+                                                   float gscale, float xscale, float r,
+                                                   long long pos, int i, int qd, int sub,
+                                                   const unsigned long long *ru,
+                                                   float (*red)[ROWS], unsigned char *out) {
+  f2 a[8], bq[8];
+  {
+    uint32_t ra[16], rb[16];
+    umma::tmem_ld16_nowait(tmem_row + 16 * qd, ra);
+    umma::tmem_ld16_nowait(tmem_row + 64 + 16 * qd, rb);
+    umma::tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      a[e] = mk2(__uint_as_float(ra[2 * e]), __uint_as_float(ra[2 * e + 1]));
+      bq[e] = mk2(__uint_as_float(rb[2 * e]), __uint_as_float(rb[2 * e + 1]));
+    }
+  }
+  f2 sgx = 0ull;
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {  // the fp16 row stays packed until it is used
+    f2 x0[4], x1[4];
+    unpack4x2h(xt[hf], x0);
+    unpack4x2h(xt[2 + hf], x1);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sgx = fma2(a[4 * hf + e], x0[e], fma2(bq[4 * hf + e], x1[e], sgx));
+  }
+  red[qd][i] = hsum2(sgx);
+  named_sync(5 + sub, 128);
+  // g~ - x^ (g~ . x^) / d = gscale (a + cx * xt), a the TMEM row
+  const f2 cx = dup2(-xscale * xscale * (red[0][i] + red[1][i] + red[2][i] + red[3][i]) / (float)D);
+  const f2 r2 = dup2(r * gscale);
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    f2 cs[4], sn[4], nsn[4], lo[4], hi[4], x0[4], x1[4];
+    rope8(pos, ru, hf, qd, cs, sn, nsn);
+    unpack4x2h(xt[hf], x0);
+    unpack4x2h(xt[2 + hf], x1);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const f2 u0 = fma2(x0[e], cx, a[4 * hf + e]);
+      const f2 u1 = fma2(x1[e], cx, bq[4 * hf + e]);
+      // transpose of (x0, x1) -> (x0 c - x1 s, x0 s + x1 c), then times r
+      lo[e] = mul2(fma2(u0, cs[e], mul2(u1, sn[e])), r2);
+      hi[e] = mul2(fma2(u1, cs[e], mul2(u0, nsn[e])), r2);
+    }
+    *tile_at(out, i, 2 * qd + hf) = pack4x2(lo);
+    *tile_at(out, i, 8 + 2 * qd + hf) = pack4x2(hi);
+  }
+}
+
 // ------------------------------------------------------------------ dq pass
 
 struct DqShared {
@@ -135,6 +192,8 @@ struct DqShared {
   float red_dq[2][4][ROWS];  // [W6] quarter parts of sum q^2 and sum g.q of each row
   float vd_part[4][ROWS];    // [W4] -> [W5] quarter parts of the fp32 v_i . do_i
   float qk_diag[2][ROWS];    // [W1] -> [W3] fp32 q~_i . k~_i of tile n (n & 1)
+  float r_saved[2][4][ROWS]; // saved features: 1 / RMS(q) of row i of tile n (n & 1), for
+                             // [W6] of thread (qd, i)
   float pw[ROWS + 1];
   alignas(16) float dm[4][DM_STRIDE];  // causal-mask decay table (fill_mask_table)
   float smax[NWORK];
@@ -191,6 +250,10 @@ __device__ __forceinline__ f2 sigmoid2(f2 z) {
 // 16-byte loads of dy from 32 rows per warp instruction crowded the load
 // pipeline and stalled every later shared-memory access of the warps (~20 % of
 // a tile).
+// kSaved: tmq / tmk map the forward's saved fp16 q~, k~.  [W1] is skipped
+// (MMA1 waits for the copies instead), the q~ . k~ diagonal and 1/RMS(q) come
+// from the saved scalars, and [W6] works on q~ (feature_grad_saved).
+template <bool kSaved>
 __global__ void __launch_bounds__(NTO, 1)
     tc_bwd_dq_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmq,
                      const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -226,9 +289,12 @@ __global__ void __launch_bounds__(NTO, 1)
   fill_mask_table(sh.dm, l2g, tid, NTO);
   load_rope_table(sh.ru, P, tid);
   if (warp == 0) umma::tmem_alloc(&sh.tmem_base, 512);
-  if (CV < ROWS)  // rows [CV, 128) of V are never written by TMA: clear them once
-    for (int e = tid; e < (ROWS - CV) * 16; e += NTO)
-      *tile_at(Vs, CV + e / 16, e % 16) = make_uint4(0, 0, 0, 0);
+  if (CV < ROWS)  // rows [CV, 128) of V (and, with saved features, of Q and both
+                  // K buffers, which [W1] would have zeroed) are never written by TMA
+    for (int e = tid; e < (kSaved ? 4 : 1) * (ROWS - CV) * 16; e += NTO) {
+      const int t = e / ((ROWS - CV) * 16), r = e % ((ROWS - CV) * 16);
+      *tile_at(t == 0 ? Vs : base + (t - 1) * TILE, CV + r / 16, r % 16) = make_uint4(0, 0, 0, 0);
+    }
   sync_tc();
   const uint32_t tm = sh.tmem_base;
   const uint32_t tP = tm, tS = tm + 384;
@@ -261,8 +327,13 @@ __global__ void __launch_bounds__(NTO, 1)
         unsigned char *Kt = base + (1 + buf) * TILE;
         const uint32_t ak = umma::smem_u32(Kt);
         const uint32_t ta = tm + 128 + 128 * buf;
-        // MMA1 once q~, k~ are written; MMA2 once Sb is
-        wait_or_fail(&sh.bar_feat, ph, failed);
+        // MMA1 once q~, k~ are written (copied, when saved); MMA2 once Sb is
+        if (kSaved) {
+          wait_or_fail(&sh.bar_q, ph, failed);
+          wait_or_fail(&sh.bar_k[buf], (n >> 1) & 1, failed);
+        } else {
+          wait_or_fail(&sh.bar_feat, ph, failed);
+        }
         if (!failed) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
@@ -403,7 +474,7 @@ __global__ void __launch_bounds__(NTO, 1)
         // [W1] raw q, k of tile n: row fr, pairs [16 fu, 16 fu + 16); norms by shuffles
         wait_or_fail(&sh.bar_q, ph, failed);
         wait_or_fail(&sh.bar_k[buf], (n >> 1) & 1, failed);
-        {
+        if (!kSaved) {
           uint4 qr[4], kr[4];
           ld_pairs(Qs, fr, fu, qr);
           ld_pairs(Kt, fr, fu, kr);
@@ -421,8 +492,17 @@ __global__ void __launch_bounds__(NTO, 1)
           const float rk = rsqrtf(sk / (float)D + P.eps) * P.kscale;
           if (fu == 0) sh.qk_diag[buf][fr] = qk * rq * rk;  // q~_i . k~_i in fp32
           feature_qk_store(qr, kr, rq, rk, P.pos_offset + c0 + fr, fu, sh.ru, Qs, Kt, fr);
+          warp_arrive(&sh.bar_feat, lane);
+        } else {  // saved scalars of row i into slots only this thread reads: 1 / RMS(q_i)
+                  // for [W6] one step later and, on the diagonal warps, q~_i . k~_i for [W3]
+          if (valid) {
+            cp_async4(&sh.r_saved[buf][qd][i], saved_scalar(P, kSavedRq, b, h, c0 + i));
+            if (qd == sub) cp_async4(&sh.qk_diag[buf][i], saved_scalar(P, kSavedDiag, b, h, c0 + i));
+          } else {
+            sh.r_saved[buf][qd][i] = 0.f;
+            if (qd == sub) sh.qk_diag[buf][i] = 0.f;
+          }
         }
-        warp_arrive(&sh.bar_feat, lane);
 
         // [W2] after MMA7 / MMA4 of tile n - 1: Sb = fp16(S 2^-e) per column quarter, S <- gamma^c S
         if (n >= 1) wait_or_fail(&sh.bar_m74, (n - 1) & 1, failed);
@@ -482,6 +562,7 @@ __global__ void __launch_bounds__(NTO, 1)
           // 32 (kk / 2) + 8 (kk % 2)), which leaves PM free for dy.  The diagonal
           // entry (element i - 32 qd on the warps with qd == sub) comes from fp32
           // features (written in [W1], met at [W2]'s barrier).
+          if (kSaved) cp_async_wait();
           store_tmem_bf16(myP, x, qd == sub ? i - (int)col : -1, qd == sub ? sh.qk_diag[buf][i] : 0.f);
           wait_or_fail(&sh.bar_o, ph, failed);  // MMA2 done: SB is free to rewrite
           const f2 si = dup2(s_inv);
@@ -576,8 +657,12 @@ __global__ void __launch_bounds__(NTO, 1)
         {
           uint4 qr[4];
           ld_pairs(Kp, i, qd, qr);
-          feature_grad_pairs(tap, qr, 1.f, P.pos_offset + prev_c0 + i, i, qd, sub, P.eps, sh.ru,
-                             sh.red_dq, Kp);
+          if (kSaved)
+            feature_grad_saved(tap, qr, 1.f, 1.f, sh.r_saved[buf ^ 1][qd][i], P.pos_offset + prev_c0 + i,
+                               i, qd, sub, sh.ru, sh.red_dq[0], Kp);
+          else
+            feature_grad_pairs(tap, qr, 1.f, P.pos_offset + prev_c0 + i, i, qd, sub, P.eps, sh.ru,
+                               sh.red_dq, Kp);
         }
         warp_arrive(&sh.bar_w6, lane);
       }
@@ -639,6 +724,7 @@ struct DkdvShared {
   unsigned long long ru[kMaxPairs];  // RoPE phase increments (load_rope_table)
   float red_dk[2][4][ROWS];  // [V6b] quarter parts of sum k^2 and sum g.k of each row
   float qk_diag[ROWS];       // [V1] -> [V3] fp32 k~_i . q~_i of the tile
+  float r_saved[4][ROWS];    // saved features: 1 / RMS(k) of row i for [V6] of thread (qd, i)
   float pw[ROWS + 1];
   alignas(16) float du[4][DM_STRIDE];  // transposed causal-mask table (fill_mask_table_upper)
   uint64_t bar_q, bar_k, bar_v, bar_dot;                    // TMA loads of q, k, v, dO
@@ -667,6 +753,10 @@ struct DkdvShared {
 // by TMA and refills Q, K, V and dO for the tile before as each is freed.  Raw
 // k for the RMSNorm backward arrives by TMA in the X buffer a tile ahead; the
 // v . do diagonal (one word per row) is the only plain load.
+// kSaved: tmq / tmk map the forward's saved fp16 q~, k~.  [V1] is skipped (M1
+// waits for the copies instead), the k~ . q~ diagonal and 1/RMS(k) are read
+// from the saved scalars, X receives k~ and [V6] uses feature_grad_saved.
+template <bool kSaved>
 __global__ void __launch_bounds__(NTO, 1)
     tc_bwd_dkdv_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmq,
                        const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -702,11 +792,17 @@ __global__ void __launch_bounds__(NTO, 1)
   fill_mask_table_upper(sh.du, l2g, tid, NTO);
   load_rope_table(sh.ru, P, tid);
   if (warp == 0) umma::tmem_alloc(&sh.tmem_base, 512);
-  if (CV < ROWS)  // rows [CV, 128) of V and DO are never written by TMA: clear them once
+  if (CV < ROWS) {  // rows [CV, 128) of V and DO are never written by TMA: clear them once
     for (int e = tid; e < 2 * (ROWS - CV) * 16; e += NTO) {
       const int r = e % ((ROWS - CV) * 16);
       *tile_at(e < (ROWS - CV) * 16 ? Vt : DOt, CV + r / 16, r % 16) = make_uint4(0, 0, 0, 0);
     }
+    if (kSaved)  // nor those of Q and K, which [V1] would have zeroed
+      for (int e = tid; e < 2 * (ROWS - CV) * 16; e += NTO) {
+        const int r = e % ((ROWS - CV) * 16);
+        *tile_at(e < (ROWS - CV) * 16 ? Qt : Kt, CV + r / 16, r % 16) = make_uint4(0, 0, 0, 0);
+      }
+  }
   sync_tc();
   const uint32_t tm = sh.tmem_base;
   const uint32_t tA = tm, tB = tm + 128, tE = tm + 256, tX = tm + 384;  // tX: X, then X' at + 64
@@ -738,7 +834,12 @@ __global__ void __launch_bounds__(NTO, 1)
         const int n = ntile - 1 - it;
         const uint32_t ph = it & 1;
         const int c0 = t0 + n * CV;
-        wait_or_fail(&sh.bar_feat, ph, failed);
+        if (kSaved) {
+          wait_or_fail(&sh.bar_q, ph, failed);
+          wait_or_fail(&sh.bar_k, ph, failed);
+        } else {
+          wait_or_fail(&sh.bar_feat, ph, failed);
+        }
         if (!failed) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // M1 = K~ Q~^T
@@ -854,7 +955,7 @@ __global__ void __launch_bounds__(NTO, 1)
       // [V1] q~, k~ (fp16, in place): row fr, pairs [16 fu, 16 fu + 16)
       wait_or_fail(&sh.bar_q, ph, failed);
       wait_or_fail(&sh.bar_k, ph, failed);
-      {
+      if (!kSaved) {
         uint4 qr[4], kr[4];
         ld_pairs(Qt, fr, fu, qr);
         ld_pairs(Kt, fr, fu, kr);
@@ -872,9 +973,18 @@ __global__ void __launch_bounds__(NTO, 1)
         const float rk = rsqrtf(sk / (float)D + P.eps) * P.kscale;
         if (fu == 0) sh.qk_diag[fr] = qk * rq * rk;
         feature_qk_store(qr, kr, rq, rk, P.pos_offset + c0 + fr, fu, sh.ru, Qt, Kt, fr);
+        warp_arrive(&sh.bar_feat, lane);
+      } else {  // saved scalars of row i into slots only this thread reads (no
+                // register held across the phases): 1 / RMS(k_i) for [V6] and, on
+                // the diagonal warps, k~_i . q~_i for [V3]
+        if (valid) {
+          cp_async4(&sh.r_saved[qd][i], saved_scalar(P, kSavedRk, b, h, c0 + i));
+          if (qd == sub) cp_async4(&sh.qk_diag[i], saved_scalar(P, kSavedDiag, b, h, c0 + i));
+        } else {
+          sh.r_saved[qd][i] = 0.f;
+          if (qd == sub) sh.qk_diag[i] = 0.f;
+        }
       }
-      warp_arrive(&sh.bar_feat, lane);
-
       // [V2] after the E update of the tile after: Eb = bf16(E), E <- gamma^c E
       if (it > 0) wait_or_fail(&sh.bar_eupd, (it - 1) & 1, failed);
       {
@@ -905,6 +1015,7 @@ __global__ void __launch_bounds__(NTO, 1)
         // 16 qd ..); the diagonal entry (element i - 32 qd on the warps with
         // qd == sub) is k~_i . q~_i in fp32, written in [V1] by warps
         // 4 sub .. 4 sub + 3 and ordered by bar_feat -> M1
+        if (kSaved) cp_async_wait();
         store_tmem_bf16(tX + lane_base + 16 * qd, x, qd == sub ? i - (int)col : -1,
                         qd == sub ? sh.qk_diag[i] : 0.f);
         const f2 w = dup2(wdec);
@@ -978,9 +1089,13 @@ __global__ void __launch_bounds__(NTO, 1)
       warp_arrive(&sh.bar_qw, lane);
       wait_or_fail(&sh.bar_kr, ph, failed);
       {
-        uint4 kraw[4];  // raw k pairs of row i
+        uint4 kraw[4];  // raw k (saved k~) pairs of row i
         ld_pairs(X, i, qd, kraw);
-        feature_grad_pairs(tB + lane_base, kraw, P.kscale, pos, i, qd, sub, P.eps, sh.ru, sh.red_dk, Vt);
+        if (kSaved)
+          feature_grad_saved(tB + lane_base, kraw, P.kscale, 1.f / P.kscale, sh.r_saved[qd][i], pos,
+                             i, qd, sub, sh.ru, sh.red_dk[0], Vt);
+        else
+          feature_grad_pairs(tB + lane_base, kraw, P.kscale, pos, i, qd, sub, P.eps, sh.ru, sh.red_dk, Vt);
       }
       warp_arrive(&sh.bar_dkout, lane);
     }
@@ -999,38 +1114,67 @@ static_assert(kDqSmem <= 232448, "dq pass exceeds 227 KiB of shared memory per C
 }  // namespace
 }  // namespace tc
 
-cudaError_t launch_tc_bwd_dq(const MixerParams &P, cudaStream_t st) {
+namespace {
+cudaError_t qk_maps(const MixerParams &P, CUtensorMap *mq, CUtensorMap *mk);
+
+template <bool kSaved>
+cudaError_t launch_dq_variant(const MixerParams &P, cudaStream_t st) {
   CUtensorMap mq, mk, mv, mg, mo, mdg, mdq, mdy;
   cudaError_t e;
-  if ((e = tc::make_map(&mq, P.q, P, P.chunk)) != cudaSuccess) return e;
-  if ((e = tc::make_map(&mk, P.k, P, P.chunk)) != cudaSuccess) return e;
+  if ((e = qk_maps(P, &mq, &mk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mv, P.v, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mg, P.g, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mo, P.dO, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mdg, P.dg, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mdq, P.dq, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mdy, P.dy, P, P.chunk)) != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc::tc_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(tc::tc_bwd_dq_kernel<kSaved>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)tc::kDqSmem);
   if (e != cudaSuccess) return e;
-  tc::tc_bwd_dq_kernel<<<dim3(P.nseg, P.H, P.B), tc::NTO, tc::kDqSmem, st>>>(P, mq, mk, mv, mg, mo, mdg, mdq, mdy);
+  tc::tc_bwd_dq_kernel<kSaved><<<dim3(P.nseg, P.H, P.B), tc::NTO, tc::kDqSmem, st>>>(
+      P, mq, mk, mv, mg, mo, mdg, mdq, mdy);
   return cudaGetLastError();
 }
+}  // namespace
 
-cudaError_t launch_tc_bwd_dkdv(const MixerParams &P, cudaStream_t st) {
+cudaError_t launch_tc_bwd_dq(const MixerParams &P, cudaStream_t st) {
+  return P.saved ? launch_dq_variant<true>(P, st) : launch_dq_variant<false>(P, st);
+}
+
+namespace {
+// q and k operand maps: the raw inputs, or the forward's saved fp16 q~, k~.
+cudaError_t qk_maps(const MixerParams &P, CUtensorMap *mq, CUtensorMap *mk) {
+  cudaError_t e;
+  if (P.saved) {
+    if ((e = tc::make_map(mq, P.saved, P, P.chunk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != cudaSuccess)
+      return e;
+    return tc::make_map(mk, P.saved + saved_k_offset(P.B, P.T, P.H, P.D), P, P.chunk,
+                        CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+  }
+  if ((e = tc::make_map(mq, P.q, P, P.chunk)) != cudaSuccess) return e;
+  return tc::make_map(mk, P.k, P, P.chunk);
+}
+
+template <bool kSaved>
+cudaError_t launch_dkdv_variant(const MixerParams &P, cudaStream_t st) {
   CUtensorMap mq, mk, mv, mo, mdk, mdv;
   cudaError_t e;
-  if ((e = tc::make_map(&mq, P.q, P, P.chunk)) != cudaSuccess) return e;
-  if ((e = tc::make_map(&mk, P.k, P, P.chunk)) != cudaSuccess) return e;
+  if ((e = qk_maps(P, &mq, &mk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mv, P.v, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mo, P.dO, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mdk, P.dk, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mdv, P.dv, P, P.chunk)) != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc::tc_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(tc::tc_bwd_dkdv_kernel<kSaved>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)tc::kBwdSmem);
   if (e != cudaSuccess) return e;
-  tc::tc_bwd_dkdv_kernel<<<dim3(P.nseg, P.H, P.B), tc::NTO, tc::kBwdSmem, st>>>(P, mq, mk, mv, mo, mdk, mdv);
+  tc::tc_bwd_dkdv_kernel<kSaved><<<dim3(P.nseg, P.H, P.B), tc::NTO, tc::kBwdSmem, st>>>(
+      P, mq, mk, mv, mo, mdk, mdv);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_tc_bwd_dkdv(const MixerParams &P, cudaStream_t st) {
+  return P.saved ? launch_dkdv_variant<true>(P, st) : launch_dkdv_variant<false>(P, st);
 }
 
 }  // namespace hla

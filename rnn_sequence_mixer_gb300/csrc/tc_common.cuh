@@ -2,7 +2,7 @@
 // prefill and of its backward: operand-tile geometry, 16-bit packing, the
 // q/k feature map (RMSNorm, RoPE) applied in place on swizzled tiles,
 // barriers with bounded waits, and the TMA descriptors of [B, T, H, 128]
-// bf16 tensors.
+// 16-bit tensors.
 #pragma once
 
 #include <cuda.h>
@@ -357,6 +357,15 @@ __device__ __forceinline__ void wait_or_fail(uint64_t *bar, uint32_t parity, boo
 
 // One elected arrive per warp on a worker-count barrier, after the warp's
 // shared-memory writes (generic proxy) and TMEM stores are complete.
+// A 4-byte global -> shared copy that holds no register while it is in flight
+// (cp.async); its data is there for this thread after cp_async_wait().
+__device__ __forceinline__ void cp_async4(void *dst_smem, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(umma::smem_u32(dst_smem)),
+               "l"(__cvta_generic_to_global(src))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ void warp_arrive(uint64_t *bar, int lane) {
   umma::fence_async_smem();
   umma::fence_before();
@@ -384,9 +393,11 @@ EncodeFn encode_fn() {
   return fn;
 }
 
-// 4-D map over a [B, T, H, 128] bf16 tensor with a box of 64 columns x 1 head
-// x `rows` tokens x 1 sequence, 128-byte swizzled (the operand tile layout).
-cudaError_t make_map(CUtensorMap *map, const void *ptr, const MixerParams &P, int rows) {
+// 4-D map over a [B, T, H, 128] 16-bit tensor (bf16 unless `dt` says fp16)
+// with a box of 64 columns x 1 head x `rows` tokens x 1 sequence, 128-byte
+// swizzled (the operand tile layout).
+cudaError_t make_map(CUtensorMap *map, const void *ptr, const MixerParams &P, int rows,
+                     CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   EncodeFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)P.H, (cuuint64_t)P.T, (cuuint64_t)P.B};
@@ -394,7 +405,7 @@ cudaError_t make_map(CUtensorMap *map, const void *ptr, const MixerParams &P, in
                                  (cuuint64_t)P.T * P.H * D * 2};
   const cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides,
+  CUresult r = enc(map, dt, 4, const_cast<void *>(ptr), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;

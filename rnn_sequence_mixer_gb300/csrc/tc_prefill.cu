@@ -220,6 +220,7 @@ struct OutShared {
   uint64_t bar_sb;      // workers: Sb written and S rescaled
   uint64_t bar_pm;      // workers: Pm, scaled O and k~dec written
   uint64_t bar_epi;     // workers: y of the previous tile written over its gate tile
+  uint64_t bar_sv;      // saving: the TMA stores of q~, k~ have read Q and K (issuer)
   uint32_t tmem_base;
   uint32_t failed;
 };
@@ -240,10 +241,16 @@ struct OutShared {
 //             tile n + 1 is copied into the Q buffer MMA2 has just freed
 // The only CTA-wide barriers are outside the tile loop; the two reductions
 // (max |S| per column quarter, the RMS of o per row) use 4-warp named barriers.
+// kSave: the features are also saved for the backward.  Once q~, k~ of a tile
+// are in place the issuer stores both tiles by TMA (fp16 maps tmsq / tmsk)
+// and, when the stores have read them, lets the workers turn k~ into k~dec
+// (bar_sv); the [A]/[D] warps write 1/RMS(q), 1/RMS(k) and q~_i . k~_i.
+template <bool kSave>
 __global__ void __launch_bounds__(NTO, 1)
     tc_output_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmq,
                      const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                     const __grid_constant__ CUtensorMap tmg, const __grid_constant__ CUtensorMap tmy) {
+                     const __grid_constant__ CUtensorMap tmg, const __grid_constant__ CUtensorMap tmy,
+                     const __grid_constant__ CUtensorMap tmsq, const __grid_constant__ CUtensorMap tmsk) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   // Q: raw q -> q~ (free once MMA2 has read it: the next q lands there).
@@ -270,6 +277,7 @@ __global__ void __launch_bounds__(NTO, 1)
     umma::mbar_init(&sh.bar_v, 1);
     umma::mbar_init(&sh.bar_g, 1);
     umma::mbar_init(&sh.bar_p, 1);
+    umma::mbar_init(&sh.bar_sv, 1);
     umma::mbar_init(&sh.bar_feat, NWORK);
     umma::mbar_init(&sh.bar_sb, NWORK);
     umma::mbar_init(&sh.bar_pm, NWORK);
@@ -315,6 +323,11 @@ __global__ void __launch_bounds__(NTO, 1)
         const uint32_t ocur = tm + 128 + 128 * buf;
         wait_or_fail(&sh.bar_feat, n & 1, failed);
         if (!failed) {
+          if (kSave) {  // q~, k~ of the tile out for the backward
+            tma_store_tile(&tmsq, Qs, b, h, c0);
+            tma_store_tile(&tmsk, base + (1 + buf) * TILE, b, h, c0);
+            umma::bulk_commit();
+          }
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma::mma_ss(tP, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(ak, kk, ROWS),
@@ -328,6 +341,10 @@ __global__ void __launch_bounds__(NTO, 1)
             umma::mma_ss(ocur, umma::desc_kmajor(aq, kk, ROWS), umma::desc_mnmajor(as, kk, ROWS),
                          id_qs, kk > 0);
           umma::commit(&sh.bar_mma[0]);
+        }
+        if (kSave) {  // the saving stores have read Q and K: K may become k~dec
+          if (!failed) umma::bulk_wait_read();
+          umma::mbar_arrive(&sh.bar_sv);
         }
         // MMA2 done: Q is free for the next q (as early as possible: the
         // workers need it right after this tile's mask)
@@ -434,10 +451,15 @@ __global__ void __launch_bounds__(NTO, 1)
         qk += __shfl_xor_sync(0xffffffffu, qk, 2);
         // [D] q~ = RoPE(Norm(q)), k~ = RoPE(Norm(k)) / sqrt(d), fp16, in place
         const float rq = rsqrtf(sq / (float)D + P.eps);
-        const float rk = rsqrtf(sk / (float)D + P.eps) * P.kscale;
+        const float rk0 = rsqrtf(sk / (float)D + P.eps), rk = rk0 * P.kscale;
         // q~_i . k~_i in fp32 (one rotation acts on both, so RoPE drops out);
         // zero on rows past the tile.  Read in [F] by the diagonal warps.
         if (fu == 0) sh.qk_diag[buf][fr] = qk * rq * rk;
+        if (kSave && fu == 0 && fvalid) {
+          *saved_scalar(P, kSavedRq, b, h, c0 + fr) = rq;
+          *saved_scalar(P, kSavedRk, b, h, c0 + fr) = rk0;
+          *saved_scalar(P, kSavedDiag, b, h, c0 + fr) = qk * rq * rk;
+        }
         feature_qk_store(qr, kr, rq, rk, P.pos_offset + c0 + fr, fu, sh.ru, Qt, Kt, fr);
         warp_arrive(&sh.bar_feat, lane);
       }
@@ -490,7 +512,9 @@ __global__ void __launch_bounds__(NTO, 1)
           f2 x[16];
           pairs_of(pv, x);
           mask_lower_table(x, sh.dm, i, (int)col);
-          // k~dec = gamma^{c-1-i} k~ as bf16, in place (K~ is dead once MMA1 is done)
+          // k~dec = gamma^{c-1-i} k~ as bf16, in place (K~ is dead once MMA1 is done,
+          // and, when saving, once its store has read it)
+          if (kSave) wait_or_fail(&sh.bar_sv, n & 1, failed);
           {
             const f2 wk = dup2(valid ? sh.pw[c - 1 - i] : 0.f);
 #pragma unroll
@@ -618,19 +642,37 @@ cudaError_t launch_tc_seg_gstate(const MixerParams &P, cudaStream_t st) {
   return launch_state_variant<true>(P, P.q, P.dO, st);
 }
 
-cudaError_t launch_tc_seg_output(const MixerParams &P, cudaStream_t st) {
-  CUtensorMap mq, mk, mv, mg, my;
+namespace {
+template <bool kSave>
+cudaError_t launch_output_variant(const MixerParams &P, cudaStream_t st) {
+  CUtensorMap mq, mk, mv, mg, my, msq, msk;
   cudaError_t e;
   if ((e = tc::make_map(&mq, P.q, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mk, P.k, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mv, P.v, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mg, P.g, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&my, P.y, P, P.chunk)) != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc::tc_output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (kSave) {
+    if ((e = tc::make_map(&msq, P.saved, P, P.chunk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != cudaSuccess)
+      return e;
+    if ((e = tc::make_map(&msk, P.saved + saved_k_offset(P.B, P.T, P.H, P.D), P, P.chunk,
+                          CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != cudaSuccess)
+      return e;
+  } else {
+    msq = mq;  // not read
+    msk = mk;
+  }
+  e = cudaFuncSetAttribute(tc::tc_output_kernel<kSave>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)tc::kOutputSmem);
   if (e != cudaSuccess) return e;
-  tc::tc_output_kernel<<<dim3(P.nseg, P.H, P.B), tc::NTO, tc::kOutputSmem, st>>>(P, mq, mk, mv, mg, my);
+  tc::tc_output_kernel<kSave><<<dim3(P.nseg, P.H, P.B), tc::NTO, tc::kOutputSmem, st>>>(
+      P, mq, mk, mv, mg, my, msq, msk);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_tc_seg_output(const MixerParams &P, cudaStream_t st) {
+  return P.saved ? launch_output_variant<true>(P, st) : launch_output_variant<false>(P, st);
 }
 
 }  // namespace hla

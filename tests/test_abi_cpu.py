@@ -48,7 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.hla_abi_version() == 2
+    assert lib.hla_abi_version() == 3
     for code in range(6):
         assert _lib.status_string(code).startswith("HLA_")
     assert "UNKNOWN" in _lib.status_string(99)
@@ -98,10 +98,10 @@ def _gamma(H, value=0.9):
     return ctypes.cast(arr, ctypes.POINTER(ctypes.c_float)), arr
 
 
-def call_prefill(lib, s, gamma=None, q=FAKE, y=FAKE, ws=FAKE, ws_bytes=1 << 40):
+def call_prefill(lib, s, gamma=None, q=FAKE, y=FAKE, ws=FAKE, ws_bytes=1 << 40, saved=None):
     gp, keep = _gamma(s.H) if gamma is None else gamma
     return lib.hla_prefill(ctypes.byref(s), q, FAKE, FAKE, FAKE, gp, None, None, y, None, ws,
-                           ws_bytes, None, None)
+                           ws_bytes, None, None, saved)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -121,12 +121,12 @@ def test_prefill_rejects_bad_shapes(lib, kw, code):
 def test_prefill_rejects_bad_pointers_gamma_and_workspace(lib):
     s = shape()
     assert lib.hla_prefill(None, FAKE, FAKE, FAKE, FAKE, _gamma(2)[0], None, None, FAKE, None,
-                           FAKE, 1 << 40, None, None) == _lib.HLA_ERR_INVALID_ARG
+                           FAKE, 1 << 40, None, None, None) == _lib.HLA_ERR_INVALID_ARG
     bad_trace = _lib.HlaTrace()
     bad_trace.count = _lib.HLA_TRACE_MAX + 1
     assert lib.hla_prefill(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, _gamma(2)[0], None, None, FAKE,
                            None, FAKE, 1 << 40, None,
-                           ctypes.byref(bad_trace)) == _lib.HLA_ERR_INVALID_ARG
+                           ctypes.byref(bad_trace), None) == _lib.HLA_ERR_INVALID_ARG
     assert call_prefill(lib, s, q=None) == _lib.HLA_ERR_INVALID_ARG
     assert call_prefill(lib, s, q=FAKE + 8) == _lib.HLA_ERR_INVALID_ARG
     assert call_prefill(lib, s, y=FAKE + 2) == _lib.HLA_ERR_INVALID_ARG
@@ -165,17 +165,38 @@ def test_backward_rejects_bad_arguments(lib):
     args = lambda **kw: [kw.get(n, FAKE) for n in ("q", "k", "v", "g")]
     assert lib.hla_prefill_backward(ctypes.byref(s), *args(), gp, None, FAKE, None, FAKE, FAKE,
                                     FAKE, FAKE, None, FAKE, need - 16,
-                                    None, None, None) == _lib.HLA_ERR_WORKSPACE
+                                    None, None, None, None) == _lib.HLA_ERR_WORKSPACE
     assert lib.hla_prefill_backward(ctypes.byref(s), *args(), gp, None, None, None, FAKE, FAKE,
                                     FAKE, FAKE, None, FAKE, need, None,
-                                    None, None) == _lib.HLA_ERR_INVALID_ARG
+                                    None, None, None) == _lib.HLA_ERR_INVALID_ARG
     assert lib.hla_prefill_backward(ctypes.byref(s), *args(), gp, None, FAKE, None, FAKE, FAKE,
                                     FAKE, FAKE + 1, None, FAKE, need,
-                                    None, None, None) == _lib.HLA_ERR_INVALID_ARG
+                                    None, None, None, None) == _lib.HLA_ERR_INVALID_ARG
     # a misaligned forward workspace
     assert lib.hla_prefill_backward(ctypes.byref(s), *args(), gp, None, FAKE, None, FAKE, FAKE,
                                     FAKE, FAKE, None, FAKE, need, None, None,
+                                    FAKE + 4, None) == _lib.HLA_ERR_INVALID_ARG
+    # saved features: misaligned, and on a shape that cannot save them
+    assert lib.hla_prefill_backward(ctypes.byref(s), *args(), gp, None, FAKE, None, FAKE, FAKE,
+                                    FAKE, FAKE, None, FAKE, need, None, None, None,
                                     FAKE + 4) == _lib.HLA_ERR_INVALID_ARG
+    s64 = shape(d=64)
+    assert lib.hla_prefill_backward(ctypes.byref(s64), *args(), gp, None, FAKE, None, FAKE, FAKE,
+                                    FAKE, FAKE, None, FAKE, 1 << 40, None, None, None,
+                                    FAKE) == _lib.HLA_ERR_UNSUPPORTED
+
+
+def test_saved_feature_bytes_and_checks(lib):
+    # fp16 q~ and k~ plus three fp32 scalars per row, on the tensor-core path only
+    s = shape(B=2, T=1000, H=3, d=128)
+    assert api.saved_bytes(s) == 2 * 1000 * 3 * (4 * 128 + 12)
+    assert api.saved_bytes(shape(B=2, T=1000, H=3, d=64)) == 0
+    assert api.saved_bytes(shape(B=2, T=1000, H=3, d=128, dtype=torch.float32)) == 0
+    assert api.saved_bytes(shape(d=96)) == 0
+    assert api.saved_bytes(shape(B=0, d=128)) == 0
+    assert call_prefill(lib, s, saved=FAKE + 8) == _lib.HLA_ERR_INVALID_ARG
+    assert call_prefill(lib, shape(d=64), saved=FAKE) == _lib.HLA_ERR_UNSUPPORTED
+    assert call_prefill(lib, shape(d=128, dtype=torch.float32), saved=FAKE) == _lib.HLA_ERR_UNSUPPORTED
 
 
 def test_python_api_has_no_cpu_path():
