@@ -244,8 +244,8 @@ size_t hla_backward_workspace_size(const hla_shape *shape);
  *                    check it.
  *   saved            optional: the `saved` buffer of an hla_prefill call with
  *                    the same shape, q and k, enqueued before this call and
- *                    not reused since.  The dq and dk/dv passes read q~, k~
- *                    and the norms from it instead of recomputing them.  Read
+ *                    not reused since.  The backward passes read q~, k~ and
+ *                    the norms from it instead of recomputing them.  Read
  *                    only.  NULL = recompute.  HLA_ERR_UNSUPPORTED where
  *                    hla_saved_bytes() is 0.  Gradients agree with the
  *                    recomputing path up to the fp16 rounding of q~ and k~

@@ -394,14 +394,10 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
   HLA_LAUNCH(tr.mark());
   if (!fwd_ws) HLA_LAUNCH(launch_state_scan(P, false, st));
   HLA_LAUNCH(tr.mark());
-  P.saved = (unsigned char *)const_cast<void *>(saved);  // read by the dq and dk/dv passes
+  P.saved = (unsigned char *)const_cast<void *>(saved);  // read by the three passes below
   HLA_LAUNCH(tc ? launch_tc_bwd_dq(P, st) : launch_simt_bwd_dq(P, s->dtype, st));
   HLA_LAUNCH(tr.mark());
-  {
-    MixerParams Pg = P;  // the state-gradient pass recomputes q~ from raw q
-    Pg.saved = nullptr;
-    HLA_LAUNCH(tc ? launch_tc_seg_gstate(Pg, st) : launch_simt_seg_gstate(Pg, s->dtype, st));
-  }
+  HLA_LAUNCH(tc ? launch_tc_seg_gstate(P, st) : launch_simt_seg_gstate(P, s->dtype, st));
   HLA_LAUNCH(tr.mark());
   HLA_LAUNCH(launch_grad_scan(P, dstate_in != nullptr, st));
   HLA_LAUNCH(tr.mark());

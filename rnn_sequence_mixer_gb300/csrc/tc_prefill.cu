@@ -64,7 +64,9 @@ struct StateShared {
 // issues one MMA per tile as soon as the workers are done with it and refills
 // the stage once that MMA has read it, three tiles ahead.  Workers never wait
 // for the tensor core.
-template <bool kGrad>
+// kSaved (with kGrad): tmk maps the forward's saved fp16 q~, so the workers
+// only weight it and convert it to bf16 (the MMA's type, that of do).
+template <bool kGrad, bool kSaved = false>
 __global__ void __launch_bounds__(NTO, 1)
     tc_state_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv) {
@@ -158,9 +160,23 @@ __global__ void __launch_bounds__(NTO, 1)
       unsigned char *Kt = base + 2 * st * TILE;
       const int c0 = tb + n * CV, c = min(CV, t1 - c0);
       wait_or_fail(&sh.bar_tma[st], (n / kStages) & 1, failed);
+      const bool valid = fr < c;
+      if (kSaved) {  // q~ (fp16) -> gamma^{s+1} q~ (bf16) in place; zeros past the tile
+        const f2 w = dup2(exp2f((float)(c0 - t0 + fr + 1) * l2g));
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint4 *p = tile_at(Kt, fr, (u < 2 ? 0 : 8) + 2 * fu + (u & 1));
+          f2 f[4];
+          unpack4x2h(*p, f);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) f[e] = mul2(f[e], w);
+          *p = valid ? pack4x2(f) : make_uint4(0, 0, 0, 0);
+        }
+        warp_arrive(&sh.bar_feat[st], lane);
+        continue;
+      }
       uint4 kr[4];
       ld_pairs(Kt, fr, fu, kr);
-      const bool valid = fr < c;
       if (!valid)  // rows past the tile hold stale bytes: use zeros
         kr[0] = kr[1] = kr[2] = kr[3] = make_uint4(0, 0, 0, 0);
       float sk = sumsq_pairs(kr);
@@ -617,18 +633,22 @@ static_assert(kOutputSmem <= 232448, "output pass exceeds 227 KiB of shared memo
 bool tc_supported(const MixerParams &P, int dtype) { return dtype == HLA_BF16 && P.D == 128; }
 
 namespace {
-template <bool kGrad>
+template <bool kGrad, bool kSaved = false>
 cudaError_t launch_state_variant(const MixerParams &P, const void *a, const void *bsrc,
                                  cudaStream_t st) {
   CUtensorMap ma, mb;
   cudaError_t e;
-  if ((e = tc::make_map(&ma, a, P, P.chunk)) != cudaSuccess) return e;
+  if ((e = tc::make_map(&ma, a, P, P.chunk,
+                        kSaved ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16)) !=
+      cudaSuccess)
+    return e;
   if ((e = tc::make_map(&mb, bsrc, P, P.chunk)) != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc::tc_state_kernel<kGrad>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)tc::kStateSmem);
+  e = cudaFuncSetAttribute(tc::tc_state_kernel<kGrad, kSaved>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::kStateSmem);
   if (e != cudaSuccess) return e;
   const int np = P.npart > 1 ? P.npart : 1;
-  tc::tc_state_kernel<kGrad><<<dim3(P.nseg * np, P.H, P.B), tc::NTO, tc::kStateSmem, st>>>(P, ma, mb);
+  tc::tc_state_kernel<kGrad, kSaved><<<dim3(P.nseg * np, P.H, P.B), tc::NTO, tc::kStateSmem, st>>>(
+      P, ma, mb);
   if (cudaGetLastError() != cudaSuccess) return cudaErrorLaunchFailure;
   return P.part ? launch_part_sum(P, kGrad, st) : cudaSuccess;
 }
@@ -639,7 +659,9 @@ cudaError_t launch_tc_seg_state(const MixerParams &P, cudaStream_t st) {
 }
 
 cudaError_t launch_tc_seg_gstate(const MixerParams &P, cudaStream_t st) {
-  return launch_state_variant<true>(P, P.q, P.dO, st);
+  // q~ from the forward's saved features when there are some
+  return P.saved ? launch_state_variant<true, true>(P, P.saved, P.dO, st)
+                 : launch_state_variant<true>(P, P.q, P.dO, st);
 }
 
 namespace {
