@@ -19,7 +19,7 @@
 //   tc_bwd_dkdv_kernel (tiles in reverse, E carried in TMEM)
 //     dV  = ((K~ Q~^T) (.) D^T) dO + diag(gamma^{c-1-i}) K~ E
 //     dK~ = ((V dO^T) (.) D^T) Q~ + diag(gamma^{c-1-i}) V E^T
-//     E  <- gamma^c E + (diag(gamma^{i+1}) Q~)^T dO
+//     E  <- gamma^c E + Q~^T diag(gamma^{i+1}) dO
 //     dk  = Norm^T RoPE^T dK~ / sqrt(d)
 //
 // Precision: K~ Q~^T runs on fp16 operands (its rounding would dominate dv
@@ -30,7 +30,7 @@
 // magnifies its error) and v_i . do_i (do_i is orthogonal to o_i, so this
 // cancels wherever o_i is close to a multiple of v_i, e.g. at t = 0).  Decay
 // weights that multiply a whole operand row are folded into that operand
-// (K~dec, Vdec, Q~w); gamma^{i+1} on the rows of dO S^T is applied to that
+// (K~dec, Vdec, dOw); gamma^{i+1} on the rows of dO S^T is applied to that
 // product in TMEM before the intra-chunk term accumulates onto it.
 //
 // Threads: both kernels are warp-specialized like the forward output pass:
@@ -730,7 +730,7 @@ struct DkdvShared {
   uint64_t bar_q, bar_k, bar_v, bar_dot;                    // TMA loads of q, k, v, dO
   uint64_t bar_kr;                                          // TMA: raw k again, into X, for [V6]
   uint64_t bar_m1, bar_m2, bar_dv, bar_dk, bar_eupd;        // MMA commits
-  uint64_t bar_feat, bar_eb, bar_x, bar_xp, bar_dvout, bar_qw, bar_dkout;  // workers
+  uint64_t bar_feat, bar_eb, bar_x, bar_xp, bar_dvout, bar_dkout;  // workers
   uint32_t tmem_base;
   uint32_t failed;
 };
@@ -741,16 +741,17 @@ struct DkdvShared {
 //   M2   = V dO^T                               into tB
 //   dV   = X dO + K~dec Eb,    X  = M1 (.) D^T  (fp32 k~_i . q~_i on the diagonal)
 //   dK~  = X' Q~ + Vdec Eb^T,  X' = M2 (.) D^T  (fp32 v_i . do_i on the diagonal)
-//   E   <- gamma^c E + Q~w^T dO,  Q~w = diag(gamma^{i+1}) Q~
+//   E   <- gamma^c E + Q~^T dOw,  dOw = diag(gamma^{i+1}) dO
 // with D^T_ij = gamma^{j-i} for j >= i, K~dec / Vdec rows scaled by gamma^{c-1-i}
 // and Eb = bf16(E) at the tile's end.  X and X' are MMA A operands in tensor
 // memory (packed bf16, 64 columns each next to E).  Worker warps, per tile:
 //   [V1] q~, k~ (fp16, in place)             [V2] Eb, E <- gamma^c E
 //   [V3] X -> TMEM, k~ -> K~dec               [V4] Vdec, q~ -> bf16, X' -> TMEM
-//   [V5] dv -> K (over K~dec)                 [V6] q~ -> Q~w, then dk (RoPE^T, RMSNorm
-//                                                  backward against raw k) -> V (over Vdec)
-// The issuer warp issues the MMAs as their operands are ready, stores dv and dk
-// by TMA and refills Q, K, V and dO for the tile before as each is freed.  Raw
+//   [V5] dv -> K (over K~dec), dO -> dOw      [V6] dk (RoPE^T, RMSNorm backward
+//                                                  against raw k) -> V (over Vdec)
+// The issuer warp issues the MMAs as their operands are ready (the E update
+// right behind dK~: both only read Q~), stores dv and dk by TMA and refills Q,
+// K, V and dO for the tile before as each is freed.  Raw
 // k for the RMSNorm backward arrives by TMA in the X buffer a tile ahead; the
 // v . do diagonal (one word per row) is the only plain load.
 // kSaved: tmq / tmk map the forward's saved fp16 q~, k~.  [V1] is skipped (M1
@@ -764,8 +765,8 @@ __global__ void __launch_bounds__(NTO, 1)
                        const __grid_constant__ CUtensorMap tmdv) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  // Q: raw q -> q~ (fp16) -> q~ (bf16) -> Q~w.  K: raw k -> k~ (fp16) -> K~dec -> dv.
-  // V: v -> Vdec -> dk.  DO: dO.  EB: Eb.  X: raw k of the tile, for [V6].
+  // Q: raw q -> q~ (fp16) -> q~ (bf16).  K: raw k -> k~ (fp16) -> K~dec -> dv.
+  // V: v -> Vdec -> dk.  DO: dO -> dOw.  EB: Eb.  X: raw k (saved k~) of the tile, for [V6].
   unsigned char *Qt = base, *Kt = base + TILE, *Vt = base + 2 * TILE, *DOt = base + 3 * TILE;
   unsigned char *EB = base + 4 * TILE, *X = base + 5 * TILE;
   DkdvShared &sh = *reinterpret_cast<DkdvShared *>(base + 6 * TILE);
@@ -782,8 +783,8 @@ __global__ void __launch_bounds__(NTO, 1)
     uint64_t *bars[] = {&sh.bar_q, &sh.bar_k, &sh.bar_v, &sh.bar_dot, &sh.bar_kr, &sh.bar_m1,
                         &sh.bar_m2, &sh.bar_dv, &sh.bar_dk, &sh.bar_eupd};
     for (uint64_t *bar : bars) umma::mbar_init(bar, 1);
-    uint64_t *wbars[] = {&sh.bar_feat, &sh.bar_eb, &sh.bar_x, &sh.bar_xp,
-                         &sh.bar_dvout, &sh.bar_qw, &sh.bar_dkout};
+    uint64_t *wbars[] = {&sh.bar_feat, &sh.bar_eb, &sh.bar_x, &sh.bar_xp, &sh.bar_dvout,
+                         &sh.bar_dkout};
     for (uint64_t *bar : wbars) umma::mbar_init(bar, NWORK);
     umma::mbar_fence_init();
     sh.failed = 0;
@@ -885,11 +886,8 @@ __global__ void __launch_bounds__(NTO, 1)
         if (!failed) {
           tma_store_tile(&tmdv, Kt, b, h, c0);
           umma::bulk_commit();
-        }
-        wait_or_fail(&sh.bar_qw, ph, failed);
-        if (!failed) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // E += Q~w^T dO
+          for (int kk = 0; kk < 8; ++kk)  // E += Q~^T dOw
             umma::mma_ss(tE, umma::desc_mnmajor(aQ, kk, ROWS), umma::desc_mnmajor(aDO, kk, ROWS), id_mnmn, 1u);
           umma::commit(&sh.bar_eupd);
         }
@@ -1060,7 +1058,8 @@ __global__ void __launch_bounds__(NTO, 1)
       }
       warp_arrive(&sh.bar_xp, lane);
 
-      // [V5] after dV: dv -> K over K~dec, for a TMA store
+      // [V5] after dV: dv -> K over K~dec, for a TMA store; dO has been read by
+      // M2 and dV: dO -> dOw = gamma^{i+1} dO in place, for the E update
       wait_or_fail(&sh.bar_dv, ph, failed);
       {
         float v[32];
@@ -1069,16 +1068,10 @@ __global__ void __launch_bounds__(NTO, 1)
         pairs_of(v, x);
 #pragma unroll
         for (int u = 0; u < 4; ++u) *tile_at(Kt, i, 4 * qd + u) = pack4x2(&x[4 * u]);
-      }
-      warp_arrive(&sh.bar_dvout, lane);
-
-      // [V6] after dK~: q~ -> Q~w = gamma^{i+1} q~ for the E update, then dk
-      wait_or_fail(&sh.bar_dk, ph, failed);
-      {
         const f2 w = dup2(sh.pw[i + 1]);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          uint4 *p = tile_at(Qt, i, 4 * qd + u);
+          uint4 *p = tile_at(DOt, i, 4 * qd + u);
           f2 f[4];
           unpack4x2(*p, f);
 #pragma unroll
@@ -1086,7 +1079,10 @@ __global__ void __launch_bounds__(NTO, 1)
           *p = pack4x2(f);
         }
       }
-      warp_arrive(&sh.bar_qw, lane);
+      warp_arrive(&sh.bar_dvout, lane);
+
+      // [V6] after dK~: dk
+      wait_or_fail(&sh.bar_dk, ph, failed);
       wait_or_fail(&sh.bar_kr, ph, failed);
       {
         uint4 kraw[4];  // raw k (saved k~) pairs of row i
