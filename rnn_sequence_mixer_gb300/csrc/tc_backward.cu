@@ -601,19 +601,31 @@ __global__ void __launch_bounds__(NTO, 1)
           umma::tmem_ld2x16(ta + col, o);
           f2 ox[16];
           pairs_of(o, ox);
+          // z = sigmoid(gate) once per element, kept in fp32 in this thread's P
+          // columns of TMEM until the second loop (MMA3 has read Pm from them
+          // and MMA5 writes dP there only after this phase)
           f2 so2 = 0ull, sdo = 0ull;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            f2 gz[4], dv[4];
-            unpack4x2(*tile_at(Qs, i, 4 * qd + u), gz);
-            unpack4x2(*tile_at(PM, i, 4 * qd + u), dv);
+          for (int hf = 0; hf < 2; ++hf) {
+            float zs[16];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const f2 dn = mul2(dv[e], sigmoid2(gz[e]));
-              so2 = fma2(ox[4 * u + e], ox[4 * u + e], so2);
-              sdo = fma2(dn, ox[4 * u + e], sdo);
+            for (int uu = 0; uu < 2; ++uu) {
+              const int u = 2 * hf + uu;
+              f2 gz[4], dv[4];
+              unpack4x2(*tile_at(Qs, i, 4 * qd + u), gz);
+              unpack4x2(*tile_at(PM, i, 4 * qd + u), dv);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const f2 z = sigmoid2(gz[e]);
+                const f2 dn = mul2(dv[e], z);
+                so2 = fma2(ox[4 * u + e], ox[4 * u + e], so2);
+                sdo = fma2(dn, ox[4 * u + e], sdo);
+                split2(z, zs[8 * uu + 2 * e], zs[8 * uu + 2 * e + 1]);
+              }
             }
+            umma::tmem_st16(myP + 16 * hf, zs);
           }
+          umma::tmem_wait_st();
           sh.red_do[0][qd][i] = hsum2(so2);
           sh.red_do[1][qd][i] = hsum2(sdo);
           named_sync(5 + sub, 128);
@@ -625,14 +637,15 @@ __global__ void __launch_bounds__(NTO, 1)
           f2 vd = 0ull;
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
+            float zs[8];
+            umma::tmem_ld8(myP + 8 * u, zs);
             uint4 *gp = tile_at(Qs, i, 4 * qd + u);
-            f2 gz[4], dv[4], vv[4], dg[4], dd[4];
-            unpack4x2(*gp, gz);
+            f2 dv[4], vv[4], dg[4], dd[4];
             unpack4x2(*tile_at(PM, i, 4 * qd + u), dv);
             unpack4x2(*tile_at(Vs, i, 4 * qd + u), vv);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const f2 z = sigmoid2(gz[e]);
+              const f2 z = mk2(zs[2 * e], zs[2 * e + 1]);
               const f2 dn = mul2(dv[e], z);
               const f2 nv = mul2(ox[4 * u + e], ro2);
               dg[e] = mul2(mul2(dn, nv), fma2(z, dup2(-1.f), one));
