@@ -271,6 +271,54 @@ __device__ __forceinline__ void rope8(long long p, const unsigned long long *ru,
   }
 }
 
+// ------------------------------------------------------------------ RoPE angles by angle addition
+// The angle of pair m at position p0 + b is the sum of its angles at p0 and at
+// b, so cos / sin at p0 + b follow from those at p0 (computed once per group
+// of 8 rows) and at b = 0..7 (a per-CTA table) with one complex product:
+// four packed FMAs for two angles instead of the fixed-point phase and the
+// special-function unit for each.  A RopeTab holds one position's 64 angles
+// as float4 {cos m, cos m+1, sin m, sin m+1} for m = 16 qd + 2 jj at [qd][jj];
+// the padding entry staggers the four quarters across the banks.
+struct RopeTab {
+  float4 v[4][9];
+};
+
+// Entry (qd, jj) of the table of position p, from the exact phase (rope_fast);
+// `ru` is the kernel's load_rope_table copy.
+__device__ __forceinline__ float4 rope_entry(long long p, const unsigned long long *ru, int qd, int jj) {
+  float c0, s0, c1, s1;
+  rope_fast(p, ru[4 * (2 * jj) + qd], c0, s0);
+  rope_fast(p, ru[4 * (2 * jj + 1) + qd], c1, s1);
+  return make_float4(c0, c1, s0, s1);
+}
+
+// The eight small-offset tables, b = 0..7 (the whole CTA, before its first barrier).
+__device__ __forceinline__ void fill_rope_small(RopeTab *small, const unsigned long long *ru_global,
+                                                int tid, int nthreads) {
+  for (int e = tid; e < 8 * 32; e += nthreads) {
+    const int b = e >> 5, qd = (e >> 3) & 3, jj = e & 7;
+    float c0, s0, c1, s1;
+    rope_fast(b, ru_global[16 * qd + 2 * jj], c0, s0);
+    rope_fast(b, ru_global[16 * qd + 2 * jj + 1], c1, s1);
+    small[b].v[qd][jj] = make_float4(c0, c1, s0, s1);
+  }
+}
+
+// cos, sin, -sin of a thread's 8 angles of half `hf` (pairs 16 qd + 8 hf ..),
+// from the rows' base table `bt` and offset table `st` (both at [qd][0]).
+__device__ __forceinline__ void rope8_tab(const float4 *bt, const float4 *st, int hf, f2 (&cs)[4],
+                                          f2 (&sn)[4], f2 (&nsn)[4]) {
+  const f2 m1 = dup2(-1.f);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float4 B = bt[4 * hf + e], S = st[4 * hf + e];
+    const f2 cb = mk2(B.x, B.y), sb = mk2(B.z, B.w), co = mk2(S.x, S.y), so = mk2(S.z, S.w);
+    cs[e] = fma2(cb, co, mul2(sb, mul2(so, m1)));  // cos(a + b) = ca cb - sa sb
+    sn[e] = fma2(sb, co, mul2(cb, so));            // sin(a + b) = sa cb + ca sb
+    nsn[e] = mul2(sn[e], m1);
+  }
+}
+
 // Rotate this thread's 16 pairs of raw row `r` (times `scale`) at position p
 // and store them, as fp16 (half) or bf16, into the same chunks of `tile`.
 // `ru` is the kernel's table from load_rope_table.
@@ -301,6 +349,30 @@ __device__ __forceinline__ float feature_qk_store(const uint4 (&qr)[4], const ui
   for (int hf = 0; hf < 2; ++hf) {
     f2 cs[4], sn[4], nsn[4], qlo[4], qhi[4], klo[4], khi[4];
     rope8(p, ru, hf, qd, cs, sn, nsn);
+    rotate8(qr[hf], qr[2 + hf], sq, cs, sn, nsn, qlo, qhi);
+    *tile_at(Qt, row, 2 * qd + hf) = pack4x2h(qlo);
+    *tile_at(Qt, row, 8 + 2 * qd + hf) = pack4x2h(qhi);
+    rotate8(kr[hf], kr[2 + hf], sk, cs, sn, nsn, klo, khi);
+    *tile_at(Kt, row, 2 * qd + hf) = pack4x2h(klo);
+    *tile_at(Kt, row, 8 + 2 * qd + hf) = pack4x2h(khi);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dot = fma2(qlo[e], klo[e], fma2(qhi[e], khi[e], dot));
+  }
+  return hsum2(dot);
+}
+
+// feature_qk_store with the angles from a base and an offset RopeTab row
+// (rope8_tab) instead of the phase of each angle.
+__device__ __forceinline__ float feature_qk_store_tab(const uint4 (&qr)[4], const uint4 (&kr)[4],
+                                                     float rq, float rk, const float4 *bt,
+                                                     const float4 *st, int qd, unsigned char *Qt,
+                                                     unsigned char *Kt, int row) {
+  f2 dot = 0ull;
+  const f2 sq = dup2(rq), sk = dup2(rk);
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    f2 cs[4], sn[4], nsn[4], qlo[4], qhi[4], klo[4], khi[4];
+    rope8_tab(bt, st, hf, cs, sn, nsn);
     rotate8(qr[hf], qr[2 + hf], sq, cs, sn, nsn, qlo, qhi);
     *tile_at(Qt, row, 2 * qd + hf) = pack4x2h(qlo);
     *tile_at(Qt, row, 8 + 2 * qd + hf) = pack4x2h(qhi);

@@ -220,6 +220,8 @@ __global__ void __launch_bounds__(NTO, 1)
 // ------------------------------------------------------------------ output pass
 
 struct OutShared {
+  RopeTab rope_small[8];             // RoPE angles of the offsets 0..7 (fill_rope_small)
+  RopeTab rope_base[NWORK];          // per worker warp: angles at its first feature row
   unsigned long long ru[kMaxPairs];  // RoPE phase increments (load_rope_table)
   float red_o[4][ROWS];
   float pw[ROWS + 1];
@@ -304,6 +306,7 @@ __global__ void __launch_bounds__(NTO, 1)
   if (tid <= ROWS) sh.pw[tid] = exp2f((float)tid * l2g);
   fill_mask_table(sh.dm, l2g, tid, NTO);
   load_rope_table(sh.ru, P, tid);
+  fill_rope_small(sh.rope_small, P.rope_u, tid, NTO);
   if (warp == 0) umma::tmem_alloc(&sh.tmem_base, 512);
   if (CV < ROWS)  // rows [CV, 128) of V are never written by TMA: clear them once
     for (int e = tid; e < (ROWS - CV) * 16; e += NTO)
@@ -448,6 +451,12 @@ __global__ void __launch_bounds__(NTO, 1)
       const uint32_t oprev = tm + 128 + 128 * (buf ^ 1); // O buffer of tile n - 1
       unsigned char *Qt = Qs, *Kt = base + (1 + buf) * TILE;
       if (have) {
+        // this warp's RoPE angles at row 8 warp of the tile (its rows are 8 warp + 0..7),
+        // two per lane, into its own table (rope8_tab)
+        __syncwarp();
+        sh.rope_base[warp].v[lane >> 3][lane & 7] =
+            rope_entry(P.pos_offset + c0 + 8 * warp, sh.ru, lane >> 3, lane & 7);
+        __syncwarp();
         // [A] raw q, k of tile n: row fr, pairs [16 fu, 16 fu + 16); norms by shuffles
         wait_or_fail(&sh.bar_q, n & 1, failed);
         wait_or_fail(&sh.bar_k[buf], (n >> 1) & 1, failed);
@@ -476,7 +485,8 @@ __global__ void __launch_bounds__(NTO, 1)
           *saved_scalar(P, kSavedRk, b, h, c0 + fr) = rk0;
           *saved_scalar(P, kSavedDiag, b, h, c0 + fr) = qk * rq * rk;
         }
-        feature_qk_store(qr, kr, rq, rk, P.pos_offset + c0 + fr, fu, sh.ru, Qt, Kt, fr);
+        feature_qk_store_tab(qr, kr, rq, rk, &sh.rope_base[warp].v[fu][0],
+                             &sh.rope_small[lane >> 2].v[fu][0], fu, Qt, Kt, fr);
         warp_arrive(&sh.bar_feat, lane);
       }
       if (drain) wait_or_fail(&sh.bar_mma[1], (n - 1) & 1, failed);  // O(n-1), S, SP ready
