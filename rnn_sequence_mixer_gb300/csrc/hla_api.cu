@@ -290,10 +290,14 @@ hla_status hla_prefill(const hla_shape *s, const void *q, const void *k, const v
   Tracer tr{trace, st};
   HLA_LAUNCH(cudaMemsetAsync(P.err, 0, sizeof(unsigned int), st));
   HLA_LAUNCH(tr.mark());
+  // tensor cores: the last segment's local state is not summed; its output
+  // pass writes state_out from the state it carries
+  P.state_seg0 = 0;
+  P.state_nseg = P.nseg - 1;
   HLA_LAUNCH(tc ? launch_tc_seg_state(P, st) : launch_simt_seg_state(P, s->dtype, st));
   P.saved = (unsigned char *)saved;  // written by the output pass only
   HLA_LAUNCH(tr.mark());
-  HLA_LAUNCH(launch_state_scan(P, state_out != nullptr, st));
+  HLA_LAUNCH(launch_state_scan(P, !tc && state_out != nullptr, st));
   HLA_LAUNCH(tr.mark());
   HLA_LAUNCH(tc ? launch_tc_seg_output(P, st) : launch_simt_seg_output(P, s->dtype, st));
   HLA_LAUNCH(tr.mark());
@@ -390,6 +394,8 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
   Tracer tr{trace, st};
   HLA_LAUNCH(cudaMemsetAsync(P.err, 0, sizeof(unsigned int), st));
   HLA_LAUNCH(tr.mark());
+  P.state_seg0 = 0;  // entering states only: the last segment's sum is not needed
+  P.state_nseg = P.nseg - 1;
   if (!fwd_ws) HLA_LAUNCH(tc ? launch_tc_seg_state(P, st) : launch_simt_seg_state(P, s->dtype, st));
   HLA_LAUNCH(tr.mark());
   if (!fwd_ws) HLA_LAUNCH(launch_state_scan(P, false, st));
@@ -397,9 +403,13 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
   P.saved = (unsigned char *)const_cast<void *>(saved);  // read by the three passes below
   HLA_LAUNCH(tc ? launch_tc_bwd_dq(P, st) : launch_simt_bwd_dq(P, s->dtype, st));
   HLA_LAUNCH(tr.mark());
+  // tensor cores: the first segment's state-gradient sum is not formed; its
+  // dk/dv pass writes dstate_in from the gradient it carries
+  P.state_seg0 = 1;
+  P.state_nseg = P.nseg - 1;
   HLA_LAUNCH(tc ? launch_tc_seg_gstate(P, st) : launch_simt_seg_gstate(P, s->dtype, st));
   HLA_LAUNCH(tr.mark());
-  HLA_LAUNCH(launch_grad_scan(P, dstate_in != nullptr, st));
+  HLA_LAUNCH(launch_grad_scan(P, !tc && dstate_in != nullptr, st));
   HLA_LAUNCH(tr.mark());
   HLA_LAUNCH(tc ? launch_tc_bwd_dkdv(P, st) : launch_simt_bwd_dkdv(P, s->dtype, st));
   HLA_LAUNCH(tr.mark());

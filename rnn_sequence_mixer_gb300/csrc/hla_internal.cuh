@@ -39,6 +39,11 @@ struct MixerParams {
   // directly and part is nullptr.
   float *part;
   int npart;
+  // Segments [state_seg0, state_seg0 + state_nseg) that a tensor-core local-state
+  // pass covers: the forward's sums of the last segment feed only the final
+  // state, and the state gradient's of the first only dstate_in, which the
+  // output and dk/dv passes write from the state they carry instead.
+  int state_seg0, state_nseg;
   float *dO;               // backward: [B, T, H, D] gradient of o (fp32; bf16 on the tensor-core path)
   float *ddiag;            // backward, tensor-core path: [B, T, H] fp32 v_t . do_t
   const long long *pos;    // decode: [B] positions or nullptr

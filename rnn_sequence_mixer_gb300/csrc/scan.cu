@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kScanThreads) part_sum_kernel(const MixerParam
   const size_t DD = (size_t)P.D * P.D;
   const size_t e = (size_t)blockIdx.x * kScanThreads + threadIdx.x;
   if (e >= DD) return;
-  const int g = blockIdx.y, bh = blockIdx.z;
+  const int g = P.state_seg0 + blockIdx.y, bh = blockIdx.z;
   const int h = bh % P.H;
   const int L = g == P.nseg - 1 ? P.T - (P.nseg - 1) * P.seg_len : P.seg_len;
   const int np = piece_count(decay_rows(log2f(P.gamma[h])), L, P.chunk, grad != 0);
@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(kScanThreads) part_sum_kernel(const MixerParam
 }  // namespace
 
 cudaError_t launch_part_sum(const MixerParams &P, bool grad, cudaStream_t st) {
-  dim3 grid(ceil_div((long long)P.D * P.D, kScanThreads), P.nseg, P.B * P.H);
+  dim3 grid(ceil_div((long long)P.D * P.D, kScanThreads), P.state_nseg, P.B * P.H);
   part_sum_kernel<<<grid, kScanThreads, 0, st>>>(P, grad ? 1 : 0);
   return cudaGetLastError();
 }

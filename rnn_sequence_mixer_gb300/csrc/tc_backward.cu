@@ -1108,6 +1108,16 @@ __global__ void __launch_bounds__(NTO, 1)
       }
       warp_arrive(&sh.bar_dkout, lane);
     }
+    // the first segment's E after its first tile's update is the gradient of
+    // the state entering the sequence
+    if (P.dstate_in && g == 0) {
+      wait_or_fail(&sh.bar_eupd, (ntile - 1) & 1, failed);
+      float ev[32];
+      umma::tmem_ld2x16(tE + lane_base + col, ev);
+      float4 *o4 = reinterpret_cast<float4 *>(P.dstate_in + (((size_t)b * P.H + h) * D + i) * D + col);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) o4[u] = make_float4(ev[4 * u], ev[4 * u + 1], ev[4 * u + 2], ev[4 * u + 3]);
+    }
   }
   if (failed) atomicOr(&sh.failed, 1u);
   sync_tc();

@@ -427,8 +427,6 @@ __device__ __forceinline__ void wait_or_fail(uint64_t *bar, uint32_t parity, boo
   umma::fence_after();
 }
 
-// One elected arrive per warp on a worker-count barrier, after the warp's
-// shared-memory writes (generic proxy) and TMEM stores are complete.
 // A 4-byte global -> shared copy that holds no register while it is in flight
 // (cp.async); its data is there for this thread after cp_async_wait().
 __device__ __forceinline__ void cp_async4(void *dst_smem, const void *src) {
@@ -438,6 +436,8 @@ __device__ __forceinline__ void cp_async4(void *dst_smem, const void *src) {
 }
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// One elected arrive per warp on a worker-count barrier, after the warp's
+// shared-memory writes (generic proxy) and TMEM stores are complete.
 __device__ __forceinline__ void warp_arrive(uint64_t *bar, int lane) {
   umma::fence_async_smem();
   umma::fence_before();

@@ -79,7 +79,8 @@ __global__ void __launch_bounds__(NTO, 1)
   const int np = P.npart > 1 ? P.npart : 1;
   // heads in reverse launch order: under the paper's schedule gamma_h grows with
   // h, so the slowest-decaying heads, whose pieces are the longest, start first
-  const int g = blockIdx.x / np, piece = blockIdx.x % np, h = P.H - 1 - blockIdx.y, b = blockIdx.z;
+  const int g = P.state_seg0 + blockIdx.x / np, piece = blockIdx.x % np;
+  const int h = P.H - 1 - blockIdx.y, b = blockIdx.z;
   const int t0 = g * P.seg_len, t1 = min(P.T, t0 + P.seg_len);
   const int CV = P.chunk;
   const int L = t1 - t0;
@@ -629,6 +630,21 @@ __global__ void __launch_bounds__(NTO, 1)
   if (failed) atomicOr(&sh.failed, 1u);
   sync_tc();
   if (sh.failed && tid == 0 && P.err) atomicOr(P.err, 2u);
+  // the last segment's S after its last tile (its MMA4 was waited for in the
+  // workers' drain step) is the sequence's final state
+  // (by the issuer warpgroup, idle by now: row i = its TMEM lane, all columns)
+  if (P.state_out && g == P.nseg - 1 && warp >= NWORK) {
+    const int i = 32 * (warp & 3) + lane;
+    float *row = P.state_out + (((size_t)b * P.H + h) * D + i) * D;
+#pragma unroll 1
+    for (int qd = 0; qd < 4; ++qd) {
+      float sv[32];
+      umma::tmem_ld2x16(tS + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * qd, sv);
+      float4 *o4 = reinterpret_cast<float4 *>(row + 32 * qd);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) o4[u] = make_float4(sv[4 * u], sv[4 * u + 1], sv[4 * u + 2], sv[4 * u + 3]);
+    }
+  }
   if (warp == 0) umma::tmem_dealloc(tm, 512);
 }
 
@@ -657,8 +673,9 @@ cudaError_t launch_state_variant(const MixerParams &P, const void *a, const void
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::kStateSmem);
   if (e != cudaSuccess) return e;
   const int np = P.npart > 1 ? P.npart : 1;
-  tc::tc_state_kernel<kGrad, kSaved><<<dim3(P.nseg * np, P.H, P.B), tc::NTO, tc::kStateSmem, st>>>(
-      P, ma, mb);
+  if (P.state_nseg == 0) return cudaSuccess;  // one segment: its sums feed no other
+  tc::tc_state_kernel<kGrad, kSaved><<<dim3(P.state_nseg * np, P.H, P.B), tc::NTO, tc::kStateSmem,
+                                       st>>>(P, ma, mb);
   if (cudaGetLastError() != cudaSuccess) return cudaErrorLaunchFailure;
   return P.part ? launch_part_sum(P, kGrad, st) : cudaSuccess;
 }
