@@ -77,6 +77,27 @@ def measured_traffic(record: str, sources, units: float):
     return float(m_b.group(1)) * units
 
 
+def tc_launches(B: int, T: int, H: int, chunk: int, grad: bool = False) -> int:
+    """Kernels one tensor-core prefill (or backward) call launches: the library's
+    segment plan (waves x (tiles per segment + 2) over 152 SMs) decides whether
+    the local-state pass runs (more than one segment) and whether its pieces
+    of at most 32 tiles need the extra sum kernel."""
+    nchunk, units = -(-T // chunk), B * H
+    max_seg = min(nchunk, max(1, -(-16 * 152 // units)))
+    best = None
+    for nseg in range(1, max_seg + 1):
+        cps = -(-nchunk // nseg)
+        if -(-nchunk // cps) != nseg:
+            continue
+        cost = -(-(units * nseg) // 152) * (cps + 2)
+        if best is None or cost < best[0]:
+            best = (cost, cps)
+    cps = best[1]
+    nseg = -(-nchunk // cps)
+    state = 0 if nseg == 1 else (1 + (1 if -(-cps // 32) > 1 else 0))
+    return state + 3 if grad else state + 2  # + scan + output (+ dq, dk/dv)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -327,6 +348,7 @@ def run_ours(args):
     ws = torch.empty(api.prefill_workspace_size(api.make_shape(w.B, w.T, w.H, w.d, chunk=w.chunk)),
                      dtype=torch.uint8, device=dev)
     n_pass = 3
+    n_launch = tc_launches(w.B, w.T, w.H, w.chunk)
 
     def prefill_step(i, trace):
         api.prefill(inp["q"], inp["k"], inp["v"], inp["gate"], gam, chunk=w.chunk,
@@ -334,7 +356,7 @@ def run_ours(args):
 
     with ClockSampler(D.local) as clk:
         ms, passes = timed(prefill_step, args.steps, args.warmup, stream, D, n_pass + 1)
-    launches += n_pass * args.steps
+    launches += n_launch * args.steps
     ms = D.max(ms)
     tokens = w.B * w.T
     value = job_rate(tokens, ms, D.world) / 1e6
@@ -415,7 +437,7 @@ def run_ours(args):
         # shared host link) from dominating the mean
         e_steps = max(3, min(2 * args.steps, 20))
         e_ms, e_step_ms = timed(e2e_step, e_steps, 1, stream, D, trace_count=2, step_events=True)
-        launches += n_pass * n_chunk * e_steps
+        launches += tc_launches(w.B, tc, w.H, w.chunk) * n_chunk * e_steps
         e_ms = D.max(e_ms)
         e_step_ms = [p[0] for p in e_step_ms]
         # The host link is shared with the other GPUs of the machine: a step now
@@ -535,7 +557,9 @@ def run_ours(args):
 
         b_steps = max(1, min(args.steps, 5))
         b_ms, b_passes = timed(fb_step, b_steps, 1, stream, D, trace_count=11)
-        launches += 7 * b_steps  # forward 3, backward 4 (its state pass and scan are skipped)
+        # forward, then the backward without its own local-state pass and scan (fwd_ws)
+        launches += (tc_launches(wb.B, wb.T, wb.H, wb.chunk) +
+                     tc_launches(wb.B, wb.T, wb.H, wb.chunk, grad=True)) * b_steps
         b_ms = D.max(b_ms)
         b_names = ["fwd.seg_state", "fwd.state_scan", "fwd.seg_output", None, None, None,
                    "bwd.dq", "bwd.seg_gstate", "bwd.grad_scan", "bwd.dkdv"]
