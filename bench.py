@@ -81,7 +81,7 @@ def tc_launches(B: int, T: int, H: int, chunk: int, grad: bool = False) -> int:
     """Kernels one tensor-core prefill (or backward) call launches: the library's
     segment plan (waves x (tiles per segment + 2) over 152 SMs) decides whether
     the local-state pass runs (more than one segment) and whether its pieces
-    of at most 32 tiles need the extra sum kernel."""
+    of at most 48 tiles need the extra sum kernel."""
     nchunk, units = -(-T // chunk), B * H
     max_seg = min(nchunk, max(1, -(-16 * 152 // units)))
     best = None
@@ -94,7 +94,7 @@ def tc_launches(B: int, T: int, H: int, chunk: int, grad: bool = False) -> int:
             best = (cost, cps)
     cps = best[1]
     nseg = -(-nchunk // cps)
-    state = 0 if nseg == 1 else (1 + (1 if -(-cps // 32) > 1 else 0))
+    state = 0 if nseg == 1 else (1 + (1 if -(-cps // 48) > 1 else 0))
     return state + 3 if grad else state + 2  # + scan + output (+ dq, dk/dv)
 
 

@@ -117,7 +117,7 @@ __device__ __forceinline__ float gpow(float log2g, float m) { return exp2f(m * l
 // in fp32 is exactly 0 and those tokens add nothing: the pass skips their
 // tiles.  The tiles that remain are cut into pieces of kPieceTiles, each one
 // CTA writing its own partial sum, which the scan adds in a fixed order.
-constexpr int kPieceTiles = 32;
+constexpr int kPieceTiles = 48;
 
 // fp32 throughout: its rounding (~1e-7 relative) is far inside the margin
 // between 160 and the 150 below which exp2f stops flushing to 0.
