@@ -45,7 +45,7 @@ struct MixerParams {
   // output and dk/dv passes write from the state they carry instead.
   int state_seg0, state_nseg;
   float *dO;               // backward: [B, T, H, D] gradient of o (fp32; bf16 on the tensor-core path)
-  float *ddiag;            // backward, tensor-core path: [B, T, H] fp32 v_t . do_t
+  float *ddiag;            // backward, tensor-core path: [B, H, T] fp32 v_t . do_t (token-contiguous)
   const long long *pos;    // decode: [B] positions or nullptr
   const void *dy;
   const float *dstate_out;

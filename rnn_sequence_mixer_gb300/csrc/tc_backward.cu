@@ -699,7 +699,7 @@ __global__ void __launch_bounds__(NTO, 1)
                                            sh.vd_part[3][i]
                                      : 0.f;
           store_tmem_bf16(myP, x, qd == sub ? i - (int)col : -1, vd);
-          if (qd == sub && valid) P.ddiag[((size_t)b * P.T + c0 + i) * P.H + h] = vd;
+          if (qd == sub && valid) P.ddiag[((size_t)b * P.H + h) * P.T + c0 + i] = vd;
           float iv[32];
           umma::tmem_ld2x16(ta + col, iv);
           const f2 wi = dup2(sh.pw[i + 1]);
@@ -1046,7 +1046,7 @@ __global__ void __launch_bounds__(NTO, 1)
       // [V4] after M2: Vdec, q~ -> bf16; X' = M2 (.) D^T (fp32 v_i . do_i on the
       // diagonal, from the dq pass) into X once dV has read X
       {
-        const float vdiag = (qd == sub && valid) ? P.ddiag[((size_t)b * P.T + c0 + i) * P.H + h] : 0.f;
+        const float vdiag = (qd == sub && valid) ? P.ddiag[((size_t)b * P.H + h) * P.T + c0 + i] : 0.f;
         wait_or_fail(&sh.bar_m2, ph, failed);
         const f2 w = dup2(wdec);
 #pragma unroll
