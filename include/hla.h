@@ -154,9 +154,10 @@ size_t hla_saved_bytes(const hla_shape *shape);
  *                  the call also writes the features the backward needs
  *                  there (layout at hla_saved_bytes), so that
  *                  hla_prefill_backward can read them instead of recomputing
- *                  the q/k feature map.  NULL = skip.  On a shape whose
- *                  hla_saved_bytes() is 0 a non-NULL pointer returns
- *                  HLA_ERR_UNSUPPORTED.  y, o and the state are the same with
+ *                  the q/k feature map.  NULL = skip.  Only bf16 at d = 128
+ *                  can save: elsewhere a non-NULL pointer returns
+ *                  HLA_ERR_UNSUPPORTED.  With no rows (B == 0 or T == 0)
+ *                  nothing is written.  y, o and the state are the same with
  *                  and without it.
  * The output of token t depends on all tokens <= t of its sequence and on
  * state_in; sequences and heads are independent.
@@ -246,8 +247,8 @@ size_t hla_backward_workspace_size(const hla_shape *shape);
  *                    the same shape, q and k, enqueued before this call and
  *                    not reused since.  The backward passes read q~, k~ and
  *                    the norms from it instead of recomputing them.  Read
- *                    only.  NULL = recompute.  HLA_ERR_UNSUPPORTED where
- *                    hla_saved_bytes() is 0.  Gradients agree with the
+ *                    only.  NULL = recompute.  HLA_ERR_UNSUPPORTED unless bf16
+ *                    at d = 128.  Gradients agree with the
  *                    recomputing path up to the fp16 rounding of q~ and k~
  *                    (the RMSNorm backward then starts from the rounded
  *                    features).

@@ -169,11 +169,13 @@ size_t part_bytes(const hla_shape &s, const Plan &p) {
   return n > 1 ? (size_t)s.B * s.H * p.nseg * (size_t)n * s.dk * s.dv * sizeof(float) : 0;
 }
 
+// Whether a shape can save its features: the tensor-core path (bf16, d = 128).
+bool can_save(const hla_shape &s) { return s.dtype == HLA_BF16 && s.dk == 128; }
+
 // Bytes of the saved features of a shape: fp16 q~ and k~, and three fp32
-// scalars per row.  0 where the shape runs on the CUDA-core path, which
-// saves nothing.
+// scalars per row.  0 where the shape cannot save them (or has no rows).
 size_t saved_bytes(const hla_shape &s) {
-  if (!(s.dtype == HLA_BF16 && s.dk == 128)) return 0;
+  if (!can_save(s)) return 0;
   return saved_scalar_offset(s.B, s.T, s.H, s.dk) + 3 * (size_t)s.B * s.T * s.H * sizeof(float);
 }
 
@@ -259,7 +261,7 @@ hla_status hla_prefill(const hla_shape *s, const void *q, const void *k, const v
   HLA_TRY(maybe(o));
   HLA_TRY(check_trace(trace));
   HLA_TRY(maybe(saved));
-  if (saved && saved_bytes(*s) == 0) return HLA_ERR_UNSUPPORTED;
+  if (saved && !can_save(*s)) return HLA_ERR_UNSUPPORTED;
   Plan plan = make_plan(*s);
   size_t need_ws = seg_bytes(*s, plan) + part_bytes(*s, plan) + kStatusBytes;
   if (!ws || !aligned16(ws) || ws_bytes < need_ws) return HLA_ERR_WORKSPACE;
@@ -354,7 +356,7 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
   HLA_TRY(check_trace(trace));
   HLA_TRY(maybe(fwd_ws));
   HLA_TRY(maybe(saved));
-  if (saved && saved_bytes(*s) == 0) return HLA_ERR_UNSUPPORTED;
+  if (saved && !can_save(*s)) return HLA_ERR_UNSUPPORTED;
   Plan plan = make_plan(*s);
   size_t sbytes = seg_bytes(*s, plan);
   size_t need_ws = hla_backward_workspace_size(s);

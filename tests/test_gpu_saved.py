@@ -144,3 +144,22 @@ def test_fwd_bwd_workload_saved_features_sampled(dev):
     for name, got, want in zip(["dq", "dk", "dv", "dgate"], out[:4], ref[:4]):
         err = max_rel_err(sel(got), want)
         assert err <= 2e-2, f"{name}: {err:.3e}"
+
+
+@pytest.mark.parametrize("B,T", [(2, 0), (0, 7)])
+def test_saved_features_of_an_empty_batch_or_sequence(dev, B, T):
+    """No rows: a saved buffer is accepted and nothing is written; the states
+    pass through as without one."""
+    H, d = 2, 128
+    g = torch.from_numpy(oracle.gamma(H).astype(np.float32))
+    inp = inputs.mixer_inputs(B, T, H, d, torch.bfloat16, 8, device=dev, with_dy=True)
+    s0 = inputs.state(B, H, d, 9, 0.1, device=dev)
+    dso = inputs.state(B, H, d, 10, 0.05, device=dev)
+    sv = torch.full((16,), 0x5A, dtype=torch.uint8, device=dev)
+    _, _, st = api.prefill(inp["q"], inp["k"], inp["v"], inp["gate"], g, s0, chunk=128, saved=sv)
+    out = api.prefill_backward(inp["q"], inp["k"], inp["v"], inp["gate"], g, inp["dy"], s0, dso,
+                               chunk=128, want_dstate_in=True, saved=sv)
+    torch.cuda.synchronize()
+    assert torch.equal(st, s0)
+    assert torch.equal(out[4], dso)
+    assert bool((sv == 0x5A).all())
