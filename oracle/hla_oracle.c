@@ -20,7 +20,7 @@
  * outside the mixer: q, k, v are the projected rows and g is the pre-sigmoid
  * gate logit x W_z.
  *
- * Readings where the paper leaves a step open (all restated in the design doc):
+ * Readings where the paper leaves a step open:
  *   - Norm is RMSNorm x / sqrt(mean(x^2) + eps) with unit weight, eps a
  *     parameter (1e-6 in every workload).
  *   - RoPE is the rotate-half form: for i < d/2 the pair (x_i, x_{i+d/2}) is
