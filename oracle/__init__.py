@@ -67,6 +67,9 @@ def _load():
     lib.hla_oracle_backward.argtypes = [i, i, i, i, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, d64,
                                         dbl, dbl, _dp, _dp, _dp, _dp, _dp]
     lib.hla_oracle_backward.restype = i
+    lib.hla_oracle_attention.argtypes = [i, i, i, i, i, _dp, _dp, _dp, _dp, dbl, d64, dbl, _dp,
+                                         _dp]
+    lib.hla_oracle_attention.restype = i
     _lib = lib
     return lib
 
@@ -175,3 +178,20 @@ def backward(q, k, v, g, gam, dy, state_in=None, dstate_out=None, pos_offset=0, 
     if rc:
         raise RuntimeError(f"oracle backward failed ({rc})")
     return dq, dk, dv, dg, dst
+
+
+def attention(q, k, v, g, a, pos_offset=0, eps=1e-6):
+    """Causal NoPE softmax attention with logit scaling s = log_a(p + 1 + a)
+    (Section 5.1, Eq. 11; Appendix A, Eq. 17), output norm and gate.
+    q, g [B, T, Hq, d]; k, v [B, T, Hkv, d].  Returns (y, o)."""
+    q, k, v, g = map(_f64, (q, k, v, g))
+    B, T, Hq, d = _dims(q)
+    Hkv = k.shape[2]
+    if k.shape != (B, T, Hkv, d) or v.shape != k.shape or g.shape != q.shape:
+        raise ValueError("q, g [B, T, Hq, d] and k, v [B, T, Hkv, d]")
+    y, o = np.zeros_like(q), np.zeros_like(q)
+    rc = _load().hla_oracle_attention(B, T, Hq, Hkv, d, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                      float(a), int(pos_offset), float(eps), _ptr(y), _ptr(o))
+    if rc:
+        raise RuntimeError(f"oracle attention failed ({rc})")
+    return y, o

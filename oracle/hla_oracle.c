@@ -1,5 +1,6 @@
 /*
- * hla_oracle.c — plain, slow, fp64 CPU oracle of the Lightning Attention RNN mixer.
+ * hla_oracle.c — plain, slow, fp64 CPU oracle of the Lightning Attention RNN mixer
+ * (and, at the end of the file, of the hybrid's softmax attention layer).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls
  * this file.  The only legitimate users are the test suite, the smoke check in
@@ -421,4 +422,74 @@ int hla_oracle_backward(int B, int T, int H, int d, const double *q, const doubl
     free(S); free(Sb); free(dO); free(w);
   }
   return fail ? 3 : 0;
+}
+
+/*
+ * NoPE softmax attention of the hybrid's attention layers (arXiv 2601.22156,
+ * Section 5.1 "Attention Logits Scaling", Eq. 11, and Appendix A "Attention
+ * Layers", Eq. 17), per query head h, whose keys and values are those of
+ * key/value head h / (Hq / Hkv) (grouped-query attention):
+ *
+ *   s_t  = log_a(t + a)          t the paper's 1-based query position
+ *   q~_t = s_t q_t / sqrt(d)
+ *   o_t  = sum_{i <= t} exp(q~_t . k_i) v_i / sum_{j <= t} exp(q~_t . k_j)
+ *   y_t  = Norm(o_t) * sigmoid(g_t)
+ *
+ * Readings: the printed denominator's exp(q~_j k_j) is the softmax's own
+ * normalisation over the same keys, exp(q~_t k_j); token t of a call sits at
+ * the 0-based position p = pos_offset + t, so s = ln(p + 1 + a) / ln(a); the
+ * keys are this call's tokens 0..t; no positional encoding and no QK-norm.
+ * The softmax subtracts the row's largest logit before exp (the same value in
+ * exact arithmetic, and no overflow in fp64).
+ * Layouts: q, g, y, o [B, T, Hq, d]; k, v [B, T, Hkv, d].  o may be NULL.
+ * Returns 0, or non-zero on a bad shape or an allocation failure.
+ */
+int hla_oracle_attention(int B, int T, int Hq, int Hkv, int d, const double *q, const double *k,
+                         const double *v, const double *g, double a, int64_t pos_offset,
+                         double eps, double *y, double *o) {
+  if (B < 0 || T < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv || d < 1 || !(a > 1.0)) return 1;
+  const int group = Hq / Hkv;
+  const double la = log(a);
+  int fail = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+  for (int b = 0; b < B; ++b)
+    for (int h = 0; h < Hq; ++h) {
+      double *w = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+      double *ot = (double *)malloc(sizeof(double) * (size_t)d);
+      if (!w || !ot) {
+#pragma omp atomic write
+        fail = 1;
+        free(w); free(ot);
+        continue;
+      }
+      const int hk = h / group;
+      for (int t = 0; t < T; ++t) {
+        const size_t qi = (((size_t)b * T + t) * Hq + h) * d;
+        const double s = log((double)(pos_offset + t) + 1.0 + a) / la;
+        const double qs = s / sqrt((double)d);
+        double m = -HUGE_VAL;
+        for (int i = 0; i <= t; ++i) {
+          const size_t ki = (((size_t)b * T + i) * Hkv + hk) * d;
+          double dot = 0.0;
+          for (int e = 0; e < d; ++e) dot += q[qi + e] * k[ki + e];
+          w[i] = qs * dot;
+          if (w[i] > m) m = w[i];
+        }
+        double z = 0.0;
+        for (int i = 0; i <= t; ++i) {
+          w[i] = exp(w[i] - m);
+          z += w[i];
+        }
+        for (int e = 0; e < d; ++e) ot[e] = 0.0;
+        for (int i = 0; i <= t; ++i) {
+          const size_t vi = (((size_t)b * T + i) * Hkv + hk) * d;
+          for (int e = 0; e < d; ++e) ot[e] += w[i] * v[vi + e];
+        }
+        for (int e = 0; e < d; ++e) ot[e] /= z;
+        if (o) memcpy(o + qi, ot, sizeof(double) * (size_t)d);
+        gate_output(ot, g + qi, d, eps, y + qi);
+      }
+      free(w); free(ot);
+    }
+  return fail ? 2 : 0;
 }
