@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define HLA_ABI_VERSION 3
+#define HLA_ABI_VERSION 4
 
 typedef enum {
   HLA_OK = 0,
@@ -261,6 +261,52 @@ hla_status hla_prefill_backward(const hla_shape *shape, const void *q, const voi
                                 void *dq, void *dk, void *dv, void *dgate, float *dstate_in,
                                 void *ws, size_t ws_bytes, hla_stream stream,
                                 const hla_trace *trace, const void *fwd_ws, const void *saved);
+
+/*
+ * The hybrid's other mixer: causal softmax attention without positional
+ * encoding, with the position-dependent logit scale of arXiv 2601.22156,
+ * Section 5.1 "Attention Logits Scaling" (Eq. 11) and Appendix A "Attention
+ * Layers" (Eq. 17), followed by the same output norm and gate:
+ *
+ *   s_t  = log_a(t + a)   (t the paper's 1-based position: here p + 1, p = pos_offset + t)
+ *   q~_t = s_t q_t / sqrt(d)
+ *   o_t  = sum_{i <= t} softmax_i(q~_t . k_i) v_i     (keys: this call's tokens 0..t)
+ *   y_t  = Norm(o_t) * sigmoid(gate_t)
+ *
+ * Query head h reads key/value head h / (Hq / Hkv) (grouped-query attention).
+ * No QK-norm is applied (a base model's QK-norm is the caller's).
+ */
+typedef struct {
+  int32_t B;          /* sequences                                               */
+  int32_t T;          /* tokens per sequence                                     */
+  int32_t Hq;         /* query heads                                             */
+  int32_t Hkv;        /* key/value heads; must divide Hq                         */
+  int32_t d;          /* head dim (128)                                          */
+  int32_t dtype;      /* hla_dtype of q, k, v, gate and y (HLA_BF16)             */
+  int64_t pos_offset; /* position of token 0                                     */
+  double a;           /* the logit-scale base a > 1 (500 / 600 / 900, Table 6)   */
+  float norm_eps;     /* RMSNorm epsilon of the output norm                      */
+} hla_attn_shape;
+
+/* Device workspace bytes hla_attention_prefill needs (its status word); 0 on a
+ * bad shape. */
+size_t hla_attention_workspace_size(const hla_attn_shape *shape);
+
+/*
+ * Causal attention over T tokens.  Tensor cores only: bf16 at d = 128 (other
+ * shapes return HLA_ERR_UNSUPPORTED); 1 <= Hkv, Hkv divides Hq, Hq <= 256.
+ *   q, gate   in:  [B, T, Hq, d] bf16
+ *   k, v      in:  [B, T, Hkv, d] bf16
+ *   y         out: [B, T, Hq, d] bf16
+ *   o         out: fp32 [B, T, Hq, d] attention output before the norm; NULL = skip
+ *   ws, ws_bytes   device scratch of hla_attention_workspace_size() bytes: a
+ *                  uint32 status word, cleared by the call, non-zero after it
+ *                  completes when a bounded device-side wait gave up
+ * Pointer, stream and error conventions as above.
+ */
+hla_status hla_attention_prefill(const hla_attn_shape *shape, const void *q, const void *k,
+                                 const void *v, const void *gate, void *y, float *o, void *ws,
+                                 size_t ws_bytes, hla_stream stream);
 
 #ifdef __cplusplus
 }

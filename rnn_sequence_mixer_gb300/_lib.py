@@ -30,6 +30,8 @@ EXPORTS = (
     "hla_backward_workspace_size",
     "hla_prefill_backward",
     "hla_prefill_noalloc",
+    "hla_attention_workspace_size",
+    "hla_attention_prefill",
 )
 
 
@@ -45,6 +47,20 @@ class HlaShape(ctypes.Structure):
         ("reserved", ctypes.c_int32),
         ("pos_offset", ctypes.c_int64),
         ("rope_base", ctypes.c_double),
+        ("norm_eps", ctypes.c_float),
+    ]
+
+
+class HlaAttnShape(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32),
+        ("T", ctypes.c_int32),
+        ("Hq", ctypes.c_int32),
+        ("Hkv", ctypes.c_int32),
+        ("d", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("pos_offset", ctypes.c_int64),
+        ("a", ctypes.c_double),
         ("norm_eps", ctypes.c_float),
     ]
 
@@ -105,6 +121,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.hla_prefill_noalloc.restype = ctypes.c_int
     lib.hla_prefill_noalloc.argtypes = [shp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_float), f32p,
                                         f32p, vp, f32p, vp]
+    ashp = ctypes.POINTER(HlaAttnShape)
+    lib.hla_attention_workspace_size.restype = sz
+    lib.hla_attention_workspace_size.argtypes = [ashp]
+    lib.hla_attention_prefill.restype = ctypes.c_int
+    lib.hla_attention_prefill.argtypes = [ashp, vp, vp, vp, vp, vp, f32p, vp, sz, vp]
     _lib = lib
     return lib
 

@@ -207,3 +207,39 @@ def prefill_backward(q, k, v, gate, gamma, dy, state_in=None, dstate_out=None, *
     _lib.check(st, "hla_prefill_backward")
     del g_host
     return dq, dk, dv, dg, dsi
+
+
+def make_attn_shape(B, T, Hq, Hkv, d, *, a, dtype=torch.bfloat16, pos_offset=0,
+                    eps=1e-6) -> _lib.HlaAttnShape:
+    return _lib.HlaAttnShape(B=B, T=T, Hq=Hq, Hkv=Hkv, d=d, dtype=_DTYPES[dtype],
+                             pos_offset=int(pos_offset), a=float(a), norm_eps=float(eps))
+
+
+def attention_workspace_size(shape: _lib.HlaAttnShape) -> int:
+    return int(_lib.load().hla_attention_workspace_size(ctypes.byref(shape)))
+
+
+def attention_prefill(q, k, v, gate, a: float, *, pos_offset=0, eps=1e-6, want_o=False, y=None,
+                      workspace=None):
+    """hla_attention_prefill: causal softmax attention with the logit scale
+    log_a(p + 1 + a), output norm and gate.  q, gate [B, T, Hq, d]; k, v
+    [B, T, Hkv, d] (Hkv divides Hq).  Returns (y, o or None)."""
+    _check_acts(q, gate)
+    _check_acts(k, v)
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape[:2] != (B, T) or k.shape[3] != d or k.dtype != q.dtype or k.device != q.device:
+        raise ValueError("k, v must be [B, T, Hkv, d] with q's B, T, d, dtype and device")
+    shape = make_attn_shape(B, T, Hq, Hkv, d, a=a, dtype=q.dtype, pos_offset=pos_offset, eps=eps)
+    lib = _lib.load()
+    if y is None:
+        y = torch.empty_like(q)
+    o = torch.empty(q.shape, dtype=torch.float32, device=q.device) if want_o else None
+    if workspace is None:
+        workspace = torch.empty(max(attention_workspace_size(shape), 16), dtype=torch.uint8,
+                                device=q.device)
+    st = lib.hla_attention_prefill(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(gate),
+                                   _ptr(y), _ptr(o), _ptr(workspace), workspace.numel(),
+                                   _stream(q.device))
+    _lib.check(st, "hla_attention_prefill")
+    return y, o

@@ -45,3 +45,23 @@ FWD_BWD_16K = Workload("fwd_bwd_B8_T16384_H32_d128_bf16", "fwd_bwd", 8, 16384, 3
                        torch.bfloat16, 128, 1e6, 5)
 
 ALL = (TINY_FP32, PREFILL_16K, PREFILL_512K, DECODE_B64, FWD_BWD_16K)
+
+
+@dataclass(frozen=True)
+class AttentionWorkload:
+    """The hybrid's softmax attention layer (Section 5.1, Eq. 11; Appendix A,
+    Eq. 17).  HypeNet-2B is Qwen3-1.7B-sized: 16 query heads over 8 key/value
+    heads of dim 128, logit-scale base a = 500 (Table 6)."""
+    name: str
+    B: int
+    T: int
+    Hq: int
+    Hkv: int
+    d: int
+    a: float
+    seed: int
+    eps: float = 1e-6
+
+
+ATTENTION_16K = AttentionWorkload("attention_B1_T16384_Hq16_Hkv8_d128_bf16_a500", 1, 16384, 16, 8,
+                                  128, 500.0, 6)

@@ -48,7 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.hla_abi_version() == 3
+    assert lib.hla_abi_version() == 4
     for code in range(6):
         assert _lib.status_string(code).startswith("HLA_")
     assert "UNKNOWN" in _lib.status_string(99)
@@ -206,3 +206,37 @@ def test_python_api_has_no_cpu_path():
     with pytest.raises(ValueError):
         api.decode_step(x[:, :1], x[:, :1], x[:, :1], x[:, :1], [0.5, 0.5],
                         torch.zeros(1, 2, 64, 64))
+
+
+def attn_shape(**kw):
+    base = dict(B=1, T=256, Hq=4, Hkv=2, d=128, a=500.0, dtype=torch.bfloat16, pos_offset=0,
+                eps=1e-6)
+    base.update(kw)
+    return api.make_attn_shape(base.pop("B"), base.pop("T"), base.pop("Hq"), base.pop("Hkv"),
+                               base.pop("d"), **base)
+
+
+def call_attention(lib, s, q=FAKE, y=FAKE, o=None, ws=FAKE, ws_bytes=256):
+    return lib.hla_attention_prefill(ctypes.byref(s), q, FAKE, FAKE, FAKE, y, o, ws, ws_bytes, None)
+
+
+def test_attention_workspace_and_argument_checks(lib):
+    assert api.attention_workspace_size(attn_shape()) == 256
+    assert api.attention_workspace_size(attn_shape(Hkv=3)) == 0
+    for kw, code in [(dict(Hkv=3), _lib.HLA_ERR_INVALID_ARG),     # Hkv must divide Hq
+                     (dict(a=1.0), _lib.HLA_ERR_INVALID_ARG),     # log base a > 1
+                     (dict(a=float("nan")), _lib.HLA_ERR_INVALID_ARG),
+                     (dict(T=-1), _lib.HLA_ERR_INVALID_ARG),
+                     (dict(pos_offset=-5), _lib.HLA_ERR_INVALID_ARG),
+                     (dict(d=64), _lib.HLA_ERR_UNSUPPORTED),
+                     (dict(dtype=torch.float32), _lib.HLA_ERR_UNSUPPORTED),
+                     (dict(Hq=512, Hkv=2), _lib.HLA_ERR_UNSUPPORTED)]:
+        assert call_attention(lib, attn_shape(**kw)) == code, kw
+    s = attn_shape()
+    assert lib.hla_attention_prefill(None, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 256,
+                                     None) == _lib.HLA_ERR_INVALID_ARG
+    assert call_attention(lib, s, q=None) == _lib.HLA_ERR_INVALID_ARG
+    assert call_attention(lib, s, y=FAKE + 2) == _lib.HLA_ERR_INVALID_ARG
+    assert call_attention(lib, s, o=FAKE + 4) == _lib.HLA_ERR_INVALID_ARG
+    assert call_attention(lib, s, ws=None) == _lib.HLA_ERR_WORKSPACE
+    assert call_attention(lib, s, ws_bytes=255) == _lib.HLA_ERR_WORKSPACE
