@@ -43,6 +43,7 @@ def parse():
     p.add_argument("--no-decode", action="store_true")
     p.add_argument("--no-backward", action="store_true")
     p.add_argument("--no-mma-bench", action="store_true")
+    p.add_argument("--no-attention", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle sample")
     p.add_argument("--prefill-T", type=int, default=0,
@@ -580,6 +581,40 @@ def run_ours(args):
                           "saved_features": svb is not None,
                           "saved_bytes": 0 if svb is None else svb.numel()}
         del ib, wsb, wsf, yb, svb
+        torch.cuda.empty_cache()
+
+    # ---------------------------------------------------------------- softmax attention
+    # The hybrid's other mixer (hla_attention_prefill) on the HypeNet-2B
+    # attention shape: 16 query heads over 8 key/value heads, 16K tokens.
+    # Tensor-bound: the causal QK^T and PV products are 4 d T (T + 1) / 2 FLOPs
+    # per query head; q, k, v, gate and y (256 MiB) exceed L2.
+    if not args.no_attention:
+        wa = workloads.ATTENTION_16K
+        xa = inputs.mixer_inputs(wa.B, wa.T, wa.Hq, wa.d, torch.bfloat16, wa.seed + 1000 * D.rank,
+                                 device=dev)
+        kva = inputs.mixer_inputs(wa.B, wa.T, wa.Hkv, wa.d, torch.bfloat16,
+                                  wa.seed + 1 + 1000 * D.rank, device=dev)
+        ya = torch.empty_like(xa["q"])
+        wsa = torch.empty(api.attention_workspace_size(
+            api.make_attn_shape(wa.B, wa.T, wa.Hq, wa.Hkv, wa.d, a=wa.a)), dtype=torch.uint8,
+            device=dev)
+
+        def attn_step(i, trace):
+            api.attention_prefill(xa["q"], kva["k"], kva["v"], xa["gate"], wa.a, eps=wa.eps, y=ya,
+                                  workspace=wsa)
+
+        a_ms, _ = timed(attn_step, args.steps, args.warmup, stream, D)
+        launches += args.steps
+        a_ms = D.max(a_ms)
+        flops_a = 4.0 * wa.d * wa.T * (wa.T + 1) / 2 * wa.Hq * wa.B
+        tf = flops_a / (a_ms / 1e3) / 1e12
+        out["attention"] = {"workload": wa.name, "ms_per_step": a_ms,
+                            "Mtok_s": job_rate(wa.B * wa.T, a_ms, D.world) / 1e6,
+                            "roofline": {"kernel": "attention", "bound": "tensor",
+                                         "achieved": tf, "peak": tc_peak, "unit": "TFLOP/s",
+                                         "frac": tf / tc_peak, "alg_flops": flops_a,
+                                         "peak_source": f"bf16_tflops of {peak_src}"}}
+        del xa, kva, ya, wsa
         torch.cuda.empty_cache()
 
     # ---------------------------------------------------------------- MMA ceiling

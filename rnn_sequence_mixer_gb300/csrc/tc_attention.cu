@@ -21,7 +21,8 @@
 //   MMA2  O += P V_j               (A = P from tensor memory)
 // The issuer issues MMA1 of tile j + 1 before waiting for the workers' P of
 // tile j, so the QK^T product of the next tile runs under this tile's
-// softmax; k and v are double-buffered by TMA.  The epilogue divides by the
+// softmax; k and v are double-buffered by TMA, k refilled as soon as MMA1 of
+// the tile before has read it and v once MMA2 has.  The epilogue divides by the
 // row sum, takes the output RMSNorm and the gate (tile loaded at the start)
 // and writes y over the gate tile for a TMA store.
 #include "tc_common.cuh"
@@ -45,7 +46,8 @@ struct AttnShared {
   float red_m[2][4][ROWS];  // quarter maxima of each row, by key-tile parity
   float red_e[2][4][ROWS];  // epilogue: quarter parts of the row sum and of sum O^2
   uint64_t bar_q, bar_g;    // TMA: q tile, gate tile
-  uint64_t bar_kv[2];       // TMA: k and v tiles into buffer 0 / 1
+  uint64_t bar_k[2];        // TMA: k tile into buffer 0 / 1
+  uint64_t bar_v[2];        // TMA: v tile into buffer 0 / 1
   uint64_t bar_s[2];        // MMA1 done (S buffer 0 / 1)
   uint64_t bar_o;           // MMA2 done
   uint64_t bar_p;           // workers: P written, O rescaled (one arrive per warp)
@@ -86,8 +88,8 @@ __global__ void __launch_bounds__(NTO, 1)
   const uint32_t tile_bytes = (uint32_t)ROWS * D * 2;
 
   if (tid == 0) {
-    uint64_t *bars[] = {&sh.bar_q, &sh.bar_g, &sh.bar_kv[0], &sh.bar_kv[1],
-                        &sh.bar_s[0], &sh.bar_s[1], &sh.bar_o};
+    uint64_t *bars[] = {&sh.bar_q,    &sh.bar_g,    &sh.bar_k[0], &sh.bar_k[1], &sh.bar_v[0],
+                        &sh.bar_v[1], &sh.bar_s[0], &sh.bar_s[1], &sh.bar_o};
     for (uint64_t *bar : bars) umma::mbar_init(bar, 1);
     umma::mbar_init(&sh.bar_p, NWORK);
     umma::mbar_init(&sh.bar_epi, NWORK);
@@ -111,15 +113,16 @@ __global__ void __launch_bounds__(NTO, 1)
       umma::mbar_expect_tx(&sh.bar_g, tile_bytes);
       tma_tile(Gs, &tmg, b, h, q0, &sh.bar_g);
       for (int n = 0; n < 2 && n < nkt; ++n) {
-        umma::mbar_expect_tx(&sh.bar_kv[n], 2 * tile_bytes);
-        tma_tile(base + (1 + n) * TILE, &tmk, b, hk, n * ROWS, &sh.bar_kv[n]);
-        tma_tile(base + (3 + n) * TILE, &tmv, b, hk, n * ROWS, &sh.bar_kv[n]);
+        umma::mbar_expect_tx(&sh.bar_k[n], tile_bytes);
+        tma_tile(base + (1 + n) * TILE, &tmk, b, hk, n * ROWS, &sh.bar_k[n]);
+        umma::mbar_expect_tx(&sh.bar_v[n], tile_bytes);
+        tma_tile(base + (3 + n) * TILE, &tmv, b, hk, n * ROWS, &sh.bar_v[n]);
       }
       wait_or_fail(&sh.bar_q, 0, failed);
       for (int j = 0; j <= nkt; ++j) {
         if (j < nkt) {  // MMA1 of tile j as soon as its k has landed
           const int buf = j & 1;
-          wait_or_fail(&sh.bar_kv[buf], (j >> 1) & 1, failed);
+          wait_or_fail(&sh.bar_k[buf], (j >> 1) & 1, failed);
           if (!failed) {
             const uint32_t ak = umma::smem_u32(base + (1 + buf) * TILE);
 #pragma unroll
@@ -129,9 +132,20 @@ __global__ void __launch_bounds__(NTO, 1)
             umma::commit(&sh.bar_s[buf]);
           }
         }
+        // MMA1 of tile j - 1 is done (its softmax has started or finished): that
+        // k buffer takes tile j + 1, a whole tile before MMA1 needs it
+        if (j >= 1 && j + 1 < nkt) {
+          const int pb = (j - 1) & 1;
+          wait_or_fail(&sh.bar_s[pb], ((j - 1) >> 1) & 1, failed);
+          if (!failed) {
+            umma::mbar_expect_tx(&sh.bar_k[pb], tile_bytes);
+            tma_tile(base + (1 + pb) * TILE, &tmk, b, hk, (j + 1) * ROWS, &sh.bar_k[pb]);
+          }
+        }
         if (j >= 1) {  // MMA2 of tile j - 1 once its P is in place
           const int jp = j - 1, pb = jp & 1;
           wait_or_fail(&sh.bar_p, jp & 1, failed);
+          wait_or_fail(&sh.bar_v[pb], (jp >> 1) & 1, failed);
           if (!failed) {
             const uint32_t av = umma::smem_u32(base + (3 + pb) * TILE);
 #pragma unroll
@@ -140,12 +154,11 @@ __global__ void __launch_bounds__(NTO, 1)
                            umma::desc_mnmajor(av, kk, ROWS), id_pv, (jp > 0 || kk > 0) ? 1u : 0u);
             umma::commit(&sh.bar_o);
           }
-          // MMA1 and MMA2 of tile j - 1 done: its buffers take tile j + 1
+          // MMA2 of tile j - 1 done: its v buffer takes tile j + 1
           wait_or_fail(&sh.bar_o, jp & 1, failed);
           if (!failed && j + 1 < nkt) {
-            umma::mbar_expect_tx(&sh.bar_kv[pb], 2 * tile_bytes);
-            tma_tile(base + (1 + pb) * TILE, &tmk, b, hk, (j + 1) * ROWS, &sh.bar_kv[pb]);
-            tma_tile(base + (3 + pb) * TILE, &tmv, b, hk, (j + 1) * ROWS, &sh.bar_kv[pb]);
+            umma::mbar_expect_tx(&sh.bar_v[pb], tile_bytes);
+            tma_tile(base + (3 + pb) * TILE, &tmv, b, hk, (j + 1) * ROWS, &sh.bar_v[pb]);
           }
         }
       }
