@@ -196,8 +196,15 @@ __global__ void __launch_bounds__(NTO, 1)
       named_sync(5 + sub, 128);
       const float mt = fmaxf(fmaxf(sh.red_m[j & 1][0][i], sh.red_m[j & 1][1][i]),
                              fmaxf(sh.red_m[j & 1][2][i], sh.red_m[j & 1][3][i]));
-      const float m_new = fmaxf(m_run, ct * mt);  // every row has a key: finite
-      const float alpha = ex2_fast(m_run - m_new);  // 0 on the first tile
+      // The exponent's offset m moves only when the row's maximum exceeds it by
+      // more than 8 (log2 units): until then p <= 2^8, which fp32 sums and bf16
+      // operands hold as well as p <= 1, and the final division by the row sum
+      // cancels whichever offset was used.  So O needs rescaling only on the
+      // few tiles where some row of the warp moves m.
+      const float m_tile = ct * mt;  // every row has a key: finite
+      const bool upd = m_tile > m_run + 8.f;  // always on the first tile
+      const float m_new = upd ? m_tile : m_run;
+      const float alpha = ex2_fast(m_run - m_new);  // 1 without a move; 0 on the first tile
       float sum = 0.f;
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
@@ -206,9 +213,9 @@ __global__ void __launch_bounds__(NTO, 1)
       }
       l_part = fmaf(l_part, alpha, sum);
       store_tmem_p(ts, x);
-      if (j > 0) {  // O <- alpha O once MMA2 of tile j - 1 is done
+      if (j > 0 && !__all_sync(0xffffffffu, !upd)) {  // O <- alpha O once MMA2 of tile j - 1 is done
         wait_or_fail(&sh.bar_o, (j - 1) & 1, failed);
-        if (!__all_sync(0xffffffffu, alpha == 1.f)) {
+        {
           float ov[32];
           umma::tmem_ld2x16(tO + lane_base + col, ov);
           f2 y2[16];
