@@ -49,7 +49,9 @@ struct AttnShared {
   uint64_t bar_k[2];        // TMA: k tile into buffer 0 / 1
   uint64_t bar_v[2];        // TMA: v tile into buffer 0 / 1
   uint64_t bar_s[2];        // MMA1 done (S buffer 0 / 1)
-  uint64_t bar_o;           // MMA2 done
+  uint64_t bar_o[2];        // MMA2 of tile j done, on barrier j & 1: the workers wait only
+                            // for some of them, and a parity wait is exact only while it
+                            // is at most one phase behind its barrier
   uint64_t bar_p;           // workers: P written, O rescaled (one arrive per warp)
   uint64_t bar_epi;         // workers: y written over the gate tile
   uint32_t tmem_base;
@@ -89,7 +91,7 @@ __global__ void __launch_bounds__(NTO, 1)
 
   if (tid == 0) {
     uint64_t *bars[] = {&sh.bar_q,    &sh.bar_g,    &sh.bar_k[0], &sh.bar_k[1], &sh.bar_v[0],
-                        &sh.bar_v[1], &sh.bar_s[0], &sh.bar_s[1], &sh.bar_o};
+                        &sh.bar_v[1], &sh.bar_s[0], &sh.bar_s[1], &sh.bar_o[0], &sh.bar_o[1]};
     for (uint64_t *bar : bars) umma::mbar_init(bar, 1);
     umma::mbar_init(&sh.bar_p, NWORK);
     umma::mbar_init(&sh.bar_epi, NWORK);
@@ -152,10 +154,10 @@ __global__ void __launch_bounds__(NTO, 1)
             for (int kk = 0; kk < 8; ++kk)
               umma::mma_ts(tO, tS0 + 128 * pb + 32 * (kk >> 1) + 8 * (kk & 1),
                            umma::desc_mnmajor(av, kk, ROWS), id_pv, (jp > 0 || kk > 0) ? 1u : 0u);
-            umma::commit(&sh.bar_o);
+            umma::commit(&sh.bar_o[pb]);
           }
           // MMA2 of tile j - 1 done: its v buffer takes tile j + 1
-          wait_or_fail(&sh.bar_o, jp & 1, failed);
+          wait_or_fail(&sh.bar_o[pb], (jp >> 1) & 1, failed);
           if (!failed && j + 1 < nkt) {
             umma::mbar_expect_tx(&sh.bar_v[pb], tile_bytes);
             tma_tile(base + (3 + pb) * TILE, &tmv, b, hk, (j + 1) * ROWS, &sh.bar_v[pb]);
@@ -214,7 +216,7 @@ __global__ void __launch_bounds__(NTO, 1)
       l_part = fmaf(l_part, alpha, sum);
       store_tmem_p(ts, x);
       if (j > 0 && !__all_sync(0xffffffffu, !upd)) {  // O <- alpha O once MMA2 of tile j - 1 is done
-        wait_or_fail(&sh.bar_o, (j - 1) & 1, failed);
+        wait_or_fail(&sh.bar_o[(j - 1) & 1], ((j - 1) >> 1) & 1, failed);
         {
           float ov[32];
           umma::tmem_ld2x16(tO + lane_base + col, ov);
@@ -232,7 +234,8 @@ __global__ void __launch_bounds__(NTO, 1)
       warp_arrive(&sh.bar_p, lane);
     }
     // epilogue: o = O / l, y = Norm(o) sigmoid(gate) over the gate tile
-    wait_or_fail(&sh.bar_o, (nkt - 1) & 1, failed);
+    // the last MMA2's completion covers every earlier one
+    wait_or_fail(&sh.bar_o[(nkt - 1) & 1], ((nkt - 1) >> 1) & 1, failed);
     float ov[32];
     umma::tmem_ld2x16(tO + lane_base + col, ov);
     f2 o2[16];
