@@ -64,14 +64,6 @@ __device__ __forceinline__ float ex2_fast(float x) {
   return y;
 }
 
-// 32 fp32 values as 16 packed bf16 words into 16 TMEM columns at taddr.
-__device__ __forceinline__ void store_tmem_p(uint32_t taddr, const float (&p)[32]) {
-  uint32_t w[16];
-#pragma unroll
-  for (int e = 0; e < 16; ++e) w[e] = pack2(p[2 * e], p[2 * e + 1]);
-  umma::tmem_st16u(taddr, w);
-}
-
 __global__ void __launch_bounds__(NTO, 1)
     tc_attention_kernel(const __grid_constant__ AttnParams A, const __grid_constant__ CUtensorMap tmq,
                         const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -207,14 +199,22 @@ __global__ void __launch_bounds__(NTO, 1)
       const bool upd = m_tile > m_run + 8.f;  // always on the first tile
       const float m_new = upd ? m_tile : m_run;
       const float alpha = ex2_fast(m_run - m_new);  // 1 without a move; 0 on the first tile
-      float sum = 0.f;
+      // p = 2^(c_t x - m), two lanes per FMA; masked entries (-inf) give 0
+      uint32_t pw[16];
+      f2 s2 = 0ull;
+      {
+        const f2 c2 = dup2(ct), nm = dup2(-m_new), one = dup2(1.f);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        x[e] = ex2_fast(fmaf(x[e], ct, -m_new));
-        sum += x[e];
+        for (int e = 0; e < 16; ++e) {
+          float lo, hi;
+          split2(fma2(mk2(x[2 * e], x[2 * e + 1]), c2, nm), lo, hi);
+          const f2 pp = mk2(ex2_fast(lo), ex2_fast(hi));
+          s2 = fma2(pp, one, s2);
+          pw[e] = bf_of_f2(pp);
+        }
       }
-      l_part = fmaf(l_part, alpha, sum);
-      store_tmem_p(ts, x);
+      l_part = fmaf(l_part, alpha, hsum2(s2));
+      umma::tmem_st16u(ts, pw);
       if (j > 0 && !__all_sync(0xffffffffu, !upd)) {  // O <- alpha O once MMA2 of tile j - 1 is done
         wait_or_fail(&sh.bar_o[(j - 1) & 1], ((j - 1) >> 1) & 1, failed);
         {
