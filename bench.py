@@ -452,9 +452,10 @@ def run_ours(args):
     del inp, y, ws
     torch.cuda.empty_cache()
 
-    # ---------------------------------------------------------------- decode B=64
-    if not args.no_decode:
-        wd = workloads.DECODE_B64
+    # ---------------------------------------------------------------- decode
+    def decode_leg(wd, split=0, kernel="decode_kernel"):
+        """256 decode steps of workload wd after a prefill of wd.prefill_T tokens;
+        split = CTAs per (sequence, head) (0: the library's choice)."""
         gd = api.gamma_schedule(wd.H)
         pre = inputs.mixer_inputs(wd.B, wd.prefill_T, wd.H, wd.d, wd.dtype, wd.seed + 1000 * D.rank,
                                   device=dev)
@@ -473,12 +474,12 @@ def run_ours(args):
             flush.fill_(float(s))  # evict the state from L2 before each step
             ev[s][0].record(stream)
             api.decode_step(steps["q"][s], steps["k"][s], steps["v"][s], steps["gate"][s], gd,
-                            state, pos, rope_base=wd.rope_base, eps=wd.eps, y=yd)
+                            state, pos, rope_base=wd.rope_base, eps=wd.eps, y=yd, split=split)
             ev[s][1].record(stream)
             pos.add_(1)
         torch.cuda.synchronize()
         per = [a.elapsed_time(b) for a, b in ev]
-        launches += wd.steps
+        nl = wd.steps
         us = D.max(1e3 * statistics.mean(per))
         # The same 256 steps (flush, decode, position update) captured once as a
         # CUDA graph and replayed: the library neither allocates nor synchronizes
@@ -495,7 +496,7 @@ def run_ours(args):
                         if with_decode:
                             api.decode_step(steps["q"][s], steps["k"][s], steps["v"][s],
                                             steps["gate"][s], gd, state, pos,
-                                            rope_base=wd.rope_base, eps=wd.eps, y=yd)
+                                            rope_base=wd.rope_base, eps=wd.eps, y=yd, split=split)
                         pos.add_(1)
                 return graph
 
@@ -511,24 +512,39 @@ def run_ours(args):
 
             g_all, g_flush = capture(True), capture(False)
             graph_us = 1e3 * (replay_ms(g_all) - replay_ms(g_flush)) / wd.steps
-            launches += 2 * wd.steps
+            nl += 2 * wd.steps
             del g_all, g_flush
         except RuntimeError:
             graph_us = None
         bytes_step = wd.B * wd.H * (2 * wd.d * wd.d * 4 + 5 * wd.d * BF16)
         ach = bytes_step / (us / 1e6) / 1e9
-        out["decode"] = {"workload": wd.name, "tok_s": job_rate(wd.B, us / 1e3, D.world),
-                         "us_per_step": us, "us_per_step_median": 1e3 * statistics.median(per),
-                         "graph_us_per_step": graph_us,
-                         "steps": wd.steps, "l2": "flushed (512 MiB write) before every step",
-                         "roofline": {"kernel": "decode_step", "bound": "hbm", "achieved": ach,
-                                      "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
-                                      "alg_bytes": bytes_step,
-                                      "traffic": measured_traffic(
-                                          "traffic_decode.md", ("decode.cu", "hla_internal.cuh"),
-                                          wd.B * wd.H)}}
+        res = {"workload": wd.name, "tok_s": job_rate(wd.B, us / 1e3, D.world),
+               "us_per_step": us, "us_per_step_median": 1e3 * statistics.median(per),
+               "graph_us_per_step": graph_us, "decode_split": split or "library's choice",
+               "steps": wd.steps, "l2": "flushed (512 MiB write) before every step",
+               "roofline": {"kernel": kernel, "bound": "hbm", "achieved": ach,
+                            "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
+                            "alg_bytes": bytes_step,
+                            # the record belongs to the one-CTA-per-head kernel
+                            "traffic": measured_traffic(
+                                "traffic_decode.md", ("decode.cu", "hla_internal.cuh"),
+                                wd.B * wd.H) if kernel == "decode_kernel" else None}}
         del steps, state, flush
         torch.cuda.empty_cache()
+        return res, nl
+
+    if not args.no_decode:
+        out["decode"], nl = decode_leg(workloads.DECODE_B64)
+        launches += nl
+        # batch 1 (time per output token of one sequence), one CTA per head (the
+        # library's choice) and with each head's state columns split over a
+        # cluster of four CTAs beside it
+        b1, nl = decode_leg(workloads.DECODE_B1)
+        b1_s4, nl4 = decode_leg(workloads.DECODE_B1, split=4, kernel="decode_split_kernel")
+        launches += nl + nl4
+        b1["split4"] = {k: b1_s4[k] for k in ("us_per_step", "us_per_step_median",
+                                               "graph_us_per_step")}
+        out["decode_b1"] = b1
 
     # ---------------------------------------------------------------- forward + backward
     if not args.no_backward:

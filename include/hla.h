@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define HLA_ABI_VERSION 4
+#define HLA_ABI_VERSION 5
 
 typedef enum {
   HLA_OK = 0,
@@ -79,7 +79,8 @@ typedef struct {
   int32_t dv;         /* value head dim d_v (must equal dk)                     */
   int32_t chunk;      /* token tile of the chunked prefill: 64 or 128           */
   int32_t dtype;      /* hla_dtype of q, k, v, gate, y and the gradients        */
-  int32_t reserved;   /* must be 0                                              */
+  int32_t decode_split; /* hla_decode_step: CTAs per (sequence, head), see there;  */
+                       /* 0 for every other entry point                         */
   int64_t pos_offset; /* RoPE position of token 0 (prefill and backward)        */
   double rope_base;   /* RoPE base theta (1e6 for HypeNet-2B/5B/9B, Table 6)    */
   float norm_eps;     /* RMSNorm epsilon of the QK norms and the output norm    */
@@ -203,6 +204,17 @@ hla_status hla_prefill_noalloc(const hla_shape *shape, const void *q, const void
 /*
  * One decode step: Eq. 18 for a single new token per sequence (shape->T must
  * be 1).  The state is read once and written once.
+ *   shape->decode_split  how many CTAs share one (sequence, head): 1 = one CTA
+ *                       owns the whole d x d state; 2, 4 or 8 = a thread-block
+ *                       cluster of that many CTAs, each owning d / split of
+ *                       the state's columns (the output RMSNorm's sum of
+ *                       squares is reduced across the cluster), which spreads
+ *                       a small batch over more SMs; 0 = chosen by the library
+ *                       (one CTA: a batch-1 step is bound by latency, and the
+ *                       split gains only while the state sits in L2).  The new
+ *                       state is bit-identical for every split; o and y differ
+ *                       only by the order of the q~ S sum.  Any other value
+ *                       returns HLA_ERR_INVALID_ARG.
  *   q, k, v, gate  in:  [B, 1, H, d], shape->dtype
  *   gamma          in:  HOST fp32 [H]
  *   pos            in:  device int64 [B], RoPE position of each sequence's

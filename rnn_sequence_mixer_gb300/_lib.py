@@ -44,7 +44,7 @@ class HlaShape(ctypes.Structure):
         ("dv", ctypes.c_int32),
         ("chunk", ctypes.c_int32),
         ("dtype", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("decode_split", ctypes.c_int32),
         ("pos_offset", ctypes.c_int64),
         ("rope_base", ctypes.c_double),
         ("norm_eps", ctypes.c_float),

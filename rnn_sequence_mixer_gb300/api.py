@@ -54,8 +54,9 @@ def _check_state(s: Optional[torch.Tensor], B, H, d, device):
 
 
 def make_shape(B, T, H, d, *, chunk=64, dtype=torch.bfloat16, pos_offset=0, rope_base=1e4,
-               eps=1e-6) -> _lib.HlaShape:
-    return _lib.HlaShape(B=B, T=T, H=H, dk=d, dv=d, chunk=chunk, dtype=_DTYPES[dtype], reserved=0,
+               eps=1e-6, decode_split=0) -> _lib.HlaShape:
+    return _lib.HlaShape(B=B, T=T, H=H, dk=d, dv=d, chunk=chunk, dtype=_DTYPES[dtype],
+                         decode_split=int(decode_split),
                          pos_offset=int(pos_offset), rope_base=float(rope_base),
                          norm_eps=float(eps))
 
@@ -149,9 +150,10 @@ def prefill(q, k, v, gate, gamma: Sequence[float] | torch.Tensor, state_in=None,
 
 
 def decode_step(q, k, v, gate, gamma, state, pos=None, *, pos_offset=0, rope_base=1e4, eps=1e-6,
-                state_out=None, want_o=False, y=None):
+                state_out=None, want_o=False, y=None, split=0):
     """hla_decode_step on [B, 1, H, d] rows.  ``state_out`` defaults to ``state``
-    (in-place update).  ``pos`` is an optional int64 CUDA tensor [B]."""
+    (in-place update).  ``pos`` is an optional int64 CUDA tensor [B].  ``split``:
+    CTAs per (sequence, head), 1, 2, 4 or 8; 0 lets the library choose."""
     _check_acts(q, k, v, gate)
     B, T, H, d = q.shape
     _check_state(state, B, H, d, q.device)
@@ -161,7 +163,7 @@ def decode_step(q, k, v, gate, gamma, state, pos=None, *, pos_offset=0, rope_bas
     if pos is not None and (pos.dtype != torch.int64 or not pos.is_cuda or pos.numel() != B):
         raise ValueError("pos must be an int64 CUDA tensor with B entries")
     shape = make_shape(B, T, H, d, dtype=q.dtype, pos_offset=pos_offset, rope_base=rope_base,
-                       eps=eps)
+                       eps=eps, decode_split=split)
     lib = _lib.load()
     g_host, g_ptr = _host_gamma(gamma, H)
     if y is None:

@@ -11,6 +11,10 @@
 
 namespace hla {
 
+// decode_split.cu: the decode step with the state's columns split over a
+// cluster of `split` (2, 4 or 8) CTAs per (sequence, head).
+cudaError_t launch_decode_split(const MixerParams &P, int dtype, int split, cudaStream_t st);
+
 namespace {
 
 // The segment plan sizes its grid for a GB300: 152 SMs, one resident CTA per
@@ -22,6 +26,14 @@ constexpr int kSMs = 152;
 // the fp32 scan.
 constexpr int kSegOverhead = 2;
 
+// CTAs per (sequence, head) of a decode step when the caller leaves it to the
+// library: one.  Measured on a GB300, the column split did not pay with the
+// state coming from HBM (B = 1, H = 16: 4.5 us per step at split 8 against
+// 4.0 us) and gained at most 7% with the state already in L2 (split 4 at
+// B * H <= 32; slower from B * H = 64 on): a batch-1 step is bound by latency,
+// not by one SM's bandwidth.  Callers that keep the state in L2 can ask for it.
+constexpr int kAutoDecodeSplit = 1;
+
 }  // namespace
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
@@ -30,7 +42,9 @@ hla_status check_shape(const hla_shape *s, bool decode) {
   if (!s) return HLA_ERR_INVALID_ARG;
   // B = 0 or T = 0 (an empty batch or sequence) is valid: the call has nothing to compute.
   if (s->B < 0 || s->T < 0 || s->H < 1 || s->dk < 1 || s->dv < 1) return HLA_ERR_INVALID_ARG;
-  if (s->reserved != 0) return HLA_ERR_INVALID_ARG;
+  if (decode ? (s->decode_split < 0 || s->decode_split > 8 || (s->decode_split & (s->decode_split - 1)))
+             : s->decode_split != 0)
+    return HLA_ERR_INVALID_ARG;
   if (!(s->rope_base > 0.0) || !isfinite(s->rope_base)) return HLA_ERR_INVALID_ARG;
   if (!(s->norm_eps >= 0.0f) || !isfinite(s->norm_eps)) return HLA_ERR_INVALID_ARG;
   if (s->pos_offset < 0 || s->pos_offset > (1LL << 62) - (long long)s->T) return HLA_ERR_INVALID_ARG;
@@ -335,7 +349,9 @@ hla_status hla_decode_step(const hla_shape *s, const void *q, const void *k, con
   P.state_out = state_out;
   P.y = y;
   P.o = o;
-  HLA_LAUNCH(launch_decode(P, s->dtype, (cudaStream_t)stream));
+  const int split = s->decode_split ? s->decode_split : kAutoDecodeSplit;
+  if (split == 1) HLA_LAUNCH(launch_decode(P, s->dtype, (cudaStream_t)stream));
+  else HLA_LAUNCH(launch_decode_split(P, s->dtype, split, (cudaStream_t)stream));
   return HLA_OK;
 }
 

@@ -41,10 +41,12 @@ PREFILL_512K = Workload("prefill_B1_T524288_H16_d128_bf16", "prefill", 1, 524288
                         torch.bfloat16, 128, 1e6, 3)
 DECODE_B64 = Workload("decode_B64_H32_d128_bf16_after4096", "decode", 64, 1, 32, 128,
                       torch.bfloat16, 64, 1e6, 4, prefill_T=4096, steps=256)
+DECODE_B1 = Workload("decode_B1_H16_d128_bf16_after4096", "decode", 1, 1, 16, 128,
+                     torch.bfloat16, 64, 1e6, 7, prefill_T=4096, steps=256)
 FWD_BWD_16K = Workload("fwd_bwd_B8_T16384_H32_d128_bf16", "fwd_bwd", 8, 16384, 32, 128,
                        torch.bfloat16, 128, 1e6, 5)
 
-ALL = (TINY_FP32, PREFILL_16K, PREFILL_512K, DECODE_B64, FWD_BWD_16K)
+ALL = (TINY_FP32, PREFILL_16K, PREFILL_512K, DECODE_B64, DECODE_B1, FWD_BWD_16K)
 
 
 @dataclass(frozen=True)

@@ -48,7 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.hla_abi_version() == 4
+    assert lib.hla_abi_version() == 5
     for code in range(6):
         assert _lib.status_string(code).startswith("HLA_")
     assert "UNKNOWN" in _lib.status_string(99)
@@ -137,7 +137,7 @@ def test_prefill_rejects_bad_pointers_gamma_and_workspace(lib):
     assert call_prefill(lib, s, ws_bytes=need - 1) == _lib.HLA_ERR_WORKSPACE
     assert call_prefill(lib, s, ws=FAKE + 4) == _lib.HLA_ERR_WORKSPACE
     r = s
-    r.reserved = 1
+    r.decode_split = 1  # a decode-step field: must be 0 for the prefill
     assert call_prefill(lib, r) == _lib.HLA_ERR_INVALID_ARG
 
 
@@ -156,6 +156,12 @@ def test_decode_rejects_bad_arguments(lib):
                                None, None) == _lib.HLA_ERR_INVALID_ARG
     assert lib.hla_decode_step(ctypes.byref(shape(T=1, d=32)), FAKE, FAKE, FAKE, FAKE, gp, None,
                                FAKE, FAKE, FAKE, None, None) == _lib.HLA_ERR_UNSUPPORTED
+    # CTAs per (sequence, head): 0 (library's choice), 1, 2, 4 or 8
+    for bad in (-1, 3, 5, 6, 16):
+        r = shape(T=1)
+        r.decode_split = bad
+        assert lib.hla_decode_step(ctypes.byref(r), FAKE, FAKE, FAKE, FAKE, gp, None, FAKE, FAKE,
+                                   FAKE, None, None) == _lib.HLA_ERR_INVALID_ARG
 
 
 def test_backward_rejects_bad_arguments(lib):

@@ -25,7 +25,8 @@ def dev():
     (9, 40, 64, torch.float32, True, False),
     (1, 16, 128, torch.bfloat16, False, False),
 ])
-def test_decode_small(dev, B, H, d, dtype, use_pos, inplace):
+@pytest.mark.parametrize("split", [0, 1, 2, 4, 8])
+def test_decode_small(dev, B, H, d, dtype, use_pos, inplace, split):
     g = oracle.gamma(H).astype(np.float32)
     inp = inputs.mixer_inputs(B, 1, H, d, dtype, 40 + B, device=dev)
     s0 = inputs.state(B, H, d, 41, scale=0.2, device=dev)
@@ -35,7 +36,7 @@ def test_decode_small(dev, B, H, d, dtype, use_pos, inplace):
     st_out = st_in if inplace else torch.empty_like(s0)
     y, o, st = api.decode_step(inp["q"], inp["k"], inp["v"], inp["gate"], torch.from_numpy(g),
                                st_in, pos, pos_offset=9, rope_base=1e6, state_out=st_out,
-                               want_o=True)
+                               want_o=True, split=split)
     torch.cuda.synchronize()
     rpos = pos_host if use_pos else np.full(B, 9)
     ry, ro, rs = oracle.decode_step(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(inp["gate"]),
@@ -93,3 +94,24 @@ def test_decode_of_an_empty_batch_is_a_no_op():
                                api.gamma_schedule(H), state)
     torch.cuda.synchronize()
     assert y.numel() == 0 and st.numel() == 0
+
+
+@pytest.mark.parametrize("B,H,d,dtype", [(1, 16, 128, torch.bfloat16), (2, 8, 64, torch.float32)])
+def test_decode_split_state_is_bit_identical(dev, B, H, d, dtype):
+    """Every split applies the same per-element update S <- gamma S + k~^T v with
+    the same k~ and v, so the new state is bit-identical whichever CTA owns
+    which columns; o and y differ only in the order of the q~ S sum."""
+    g = torch.from_numpy(oracle.gamma(H).astype(np.float32))
+    inp = inputs.mixer_inputs(B, 1, H, d, dtype, 55, device=dev)
+    s0 = inputs.state(B, H, d, 56, scale=0.3, device=dev)
+    outs = {}
+    for split in (1, 2, 4, 8):
+        st = s0.clone()
+        y, o, st = api.decode_step(inp["q"], inp["k"], inp["v"], inp["gate"], g, st, None,
+                                   pos_offset=4096, rope_base=1e6, want_o=True, split=split)
+        outs[split] = (y.float(), o, st)
+    torch.cuda.synchronize()
+    for split in (2, 4, 8):
+        assert torch.equal(outs[split][2], outs[1][2]), split
+        assert torch.allclose(outs[split][1], outs[1][1], rtol=1e-5, atol=1e-5), split
+        assert torch.allclose(outs[split][0], outs[1][0], rtol=1e-2, atol=1e-2), split
