@@ -70,6 +70,8 @@ def _load():
     lib.hla_oracle_attention.argtypes = [i, i, i, i, i, _dp, _dp, _dp, _dp, dbl, d64, dbl, _dp,
                                          _dp]
     lib.hla_oracle_attention.restype = i
+    lib.hla_oracle_matmul_nt.argtypes = [i, i, i, _dp, _dp, _dp]
+    lib.hla_oracle_matmul_nt.restype = i
     _lib = lib
     return lib
 
@@ -195,3 +197,65 @@ def attention(q, k, v, g, a, pos_offset=0, eps=1e-6):
     if rc:
         raise RuntimeError(f"oracle attention failed ({rc})")
     return y, o
+
+
+def matmul_nt(a, w) -> np.ndarray:
+    """a [M, K] times w [N, K] transposed: out[m, n] = sum_k a[m, k] w[n, k]."""
+    a, w = _f64(a), _f64(w)
+    if a.ndim != 2 or w.ndim != 2 or a.shape[1] != w.shape[1]:
+        raise ValueError("matmul_nt needs a [M, K] and w [N, K]")
+    out = np.zeros((a.shape[0], w.shape[0]), dtype=np.float64)
+    if _load().hla_oracle_matmul_nt(a.shape[0], w.shape[0], a.shape[1], _ptr(a), _ptr(w),
+                                    _ptr(out)) != 0:
+        raise ValueError("bad shape")
+    return out
+
+
+def project_in(x, w_qkvz):
+    """The input projections of an RNN layer (Appendix A, Eq. 18): per head h
+    q = x W_q,h, k = x W_k,h, v = x W_v,h and the gate logit x W_z,h, before
+    the norms and the sigmoid.  x [B, T, D]; w_qkvz [H, 4, d, D] holds, for
+    head h, the transposes of (W_q, W_k, W_v, W_z) in that order (row c of
+    w_qkvz[h, j] is column c of the paper's d x d_h matrix).  Returns q, k, v,
+    g as [B, T, H, d]."""
+    x, w = _f64(x), _f64(w_qkvz)
+    B, T, Dm = x.shape
+    H, four, d, Dw = w.shape
+    if four != 4 or Dw != Dm:
+        raise ValueError("w_qkvz must be [H, 4, d, D]")
+    out = matmul_nt(x.reshape(B * T, Dm), w.reshape(H * 4 * d, Dm)).reshape(B, T, H, 4, d)
+    return tuple(np.ascontiguousarray(out[:, :, :, j, :]) for j in range(4))
+
+
+def project_out(u, w_o):
+    """The output projection (Appendix A, Eq. 18: y_t = u_t W_o^T), over all
+    heads at once: u [B, T, H, d] (the gated, normalized mixer rows, heads
+    concatenated), w_o [D, H d] (the paper's W_o of every head side by side:
+    column h d + c belongs to head h).  Returns [B, T, D]."""
+    u, w = _f64(u), _f64(w_o)
+    B, T, H, d = u.shape
+    if w.shape[1] != H * d:
+        raise ValueError("w_o must be [D, H d]")
+    return matmul_nt(u.reshape(B * T, H * d), w).reshape(B, T, w.shape[0])
+
+
+def features(q, k, pos_offset=0, base=1e4, eps=1e-6):
+    """The saved-feature quantities of a prefill (Appendix A, Eq. 18), per
+    (b, t, h): q~ = RoPE(Norm(q)), k~ = RoPE(Norm(k)) / sqrt(d), 1 / RMS(q),
+    1 / RMS(k) and q~ . k~.  Returns (q~, k~ [B, T, H, d], rq, rk, diag
+    [B, H, T])."""
+    q, k = _f64(q), _f64(k)
+    B, T, H, d = _dims(q)
+    qt = np.zeros_like(q)
+    kt = np.zeros_like(k)
+    sc = np.zeros((3, B, H, T), dtype=np.float64)
+    for b in range(B):
+        for t in range(T):
+            for h in range(H):
+                p = pos_offset + t
+                qt[b, t, h] = feature(q[b, t, h], p, base, eps)
+                kt[b, t, h] = feature(k[b, t, h], p, base, eps, 1.0 / np.sqrt(d))
+                sc[0, b, h, t] = 1.0 / np.sqrt(np.mean(q[b, t, h] ** 2) + eps)
+                sc[1, b, h, t] = 1.0 / np.sqrt(np.mean(k[b, t, h] ** 2) + eps)
+                sc[2, b, h, t] = float(np.dot(qt[b, t, h], kt[b, t, h]))
+    return qt, kt, sc[0], sc[1], sc[2]

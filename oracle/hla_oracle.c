@@ -493,3 +493,25 @@ int hla_oracle_attention(int B, int T, int Hq, int Hkv, int d, const double *q, 
     }
   return fail ? 2 : 0;
 }
+
+/*
+ * The projections around the RNN mixer, arXiv 2601.22156, Appendix A, Eq. 18
+ * ("RNN Layers"): q_t = Norm(x_t W_q), k_t = Norm(x_t W_k), v_t = x_t W_v,
+ * z_t = sigmoid(x_t W_z) take the projected rows x_t W (before the norm and
+ * the sigmoid), and y_t = (Norm(o_t) . z_t) W_o^T maps the gated rows back.
+ * Both are products of a row-major matrix with a transposed one:
+ *   out[m, n] = sum_k a[m, k] w[n, k]     (a [M, K], w [N, K], out [M, N])
+ * With w = W^T of the paper's W in R^{d x d_h} this is x_t W; with w = W_o
+ * itself it is u_t W_o^T.  Plain fp64 loops, OpenMP over the rows m.
+ */
+int hla_oracle_matmul_nt(int M, int N, int K, const double *a, const double *w, double *out) {
+  if (M < 0 || N < 0 || K < 0) return 1;
+#pragma omp parallel for schedule(static)
+  for (int m = 0; m < M; ++m)
+    for (int n = 0; n < N; ++n) {
+      double s = 0.0;
+      for (int k = 0; k < K; ++k) s += a[(size_t)m * K + k] * w[(size_t)n * K + k];
+      out[(size_t)m * N + n] = s;
+    }
+  return 0;
+}
