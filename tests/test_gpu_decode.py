@@ -5,7 +5,7 @@ import torch
 
 import oracle
 from rnn_sequence_mixer_gb300 import api, inputs, workloads
-from parity_util import f64, gather_state, max_rel_err, tol_for
+from parity_util import elem_rel_err, f64, gather_state, max_rel_err, tol_for
 
 pytestmark = pytest.mark.gpu
 
@@ -45,6 +45,11 @@ def test_decode_small(dev, B, H, d, dtype, use_pos, inplace, split):
     assert max_rel_err(f64(o), ro) <= tol
     assert max_rel_err(f64(y), ry) <= tol
     assert max_rel_err(f64(st), rs, head_axes=(0, 1)) <= tol
+    # a single step from a given state also holds element by element (floor
+    # 1e-3 of each slice's maximum)
+    assert elem_rel_err(f64(o), ro) <= tol
+    assert elem_rel_err(f64(y), ry) <= tol
+    assert elem_rel_err(f64(st), rs, head_axes=(0, 1)) <= tol
     if not inplace:
         assert torch.equal(st_in, s0), "state_in must be left untouched"
 
