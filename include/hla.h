@@ -179,16 +179,27 @@ hla_status hla_prefill(const hla_shape *shape, const void *q, const void *k, con
  * Same arguments and results as hla_prefill, minus the workspace: the
  * per-segment states live in a fixed scratch array of
  * HLA_NOALLOC_SCRATCH_BYTES inside the library's own device memory, which
- * every GPU that loads the library holds until the process exits.  The call
- * allocates nothing.
+ * every GPU that loads the library holds until the process exits.  It runs
+ * the fp32 CUDA-core kernels (every dtype and d).
  *   - Limit: B * H * d * d * 4 bytes (one fp32 state per sequence and head)
  *     must fit in HLA_NOALLOC_SCRATCH_BYTES, i.e. B * H <= 512 at d = 128;
  *     larger problems return HLA_ERR_WORKSPACE before anything is launched.
  *     Within the limit the T axis is cut into fewer, longer segments when
- *     needed, so results match hla_prefill up to fp32 rounding.
+ *     needed, so results match hla_prefill up to fp32 rounding; near the
+ *     limit (B * H close to 512 at d = 128) that is a single segment per
+ *     (sequence, head), which leaves the T axis without parallelism.
  *   - Set-up: the first call on a device looks up that device's address of
  *     the scratch array (cudaGetSymbolAddress, with the device current) and
- *     caches it; make that first call before any stream capture.
+ *     caches it.  Under CUDA's lazy module loading (the default) that first
+ *     call is also when the runtime commits the array's device memory and
+ *     loads the kernels it runs, so it is the one call that makes the runtime
+ *     reserve device memory.  An empty call (B == 0 or T == 0, which may pass
+ *     NULL tensors) performs that set-up and launches nothing: make it once
+ *     per device at start-up, before a memory pool claims the device, and
+ *     before any stream capture.  Every later call allocates nothing.  (With
+ *     CUDA_MODULE_LOADING=EAGER the runtime commits it all when the library
+ *     loads.)  The cached address belongs to the device's context: after
+ *     cudaDeviceReset the entry point must not be called again in that process.
  *   - Sharing: every call on a device uses the same scratch array, which keeps
  *     the last call's contents (the first pass overwrites all of it, so
  *     nothing needs clearing).  Calls that overlap on the GPU race on it:

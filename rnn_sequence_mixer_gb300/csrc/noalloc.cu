@@ -15,6 +15,18 @@
 // code cannot use the array's name as a device address, so the first call on
 // each device asks the runtime for that device's address of the array
 // (cudaGetSymbolAddress, with the device current) and caches it.
+//
+// Under CUDA's lazy module loading (the default) the runtime loads this file's
+// module, and commits the array's device memory, at that first lookup, and
+// loads each kernel's module the first time the kernel is touched.  So the
+// first call on a device does make the runtime commit device memory (the
+// array plus the code of the kernels it runs).  An empty call (B == 0 or
+// T == 0) does exactly that set-up and launches nothing: make it once per
+// device at start-up, before a memory pool claims the device, and before any
+// stream capture.  Calls after it allocate nothing.  (With
+// CUDA_MODULE_LOADING=EAGER everything is committed when the library loads.)
+// The cached address belongs to the device's current context: a process that
+// destroys it (cudaDeviceReset) must not call this entry point again.
 #include <mutex>
 
 #include "hla_internal.cuh"
@@ -80,13 +92,17 @@ extern "C" hla_status hla_prefill_noalloc(const hla_shape *s, const void *q, con
   const void *optional[] = {state_in, state_out, o};
   for (const void *p : optional)
     if ((st = maybe(p)) != HLA_OK) return st;
+  Plan plan;
+  if (!empty && (st = capped_plan(*s, &plan)) != HLA_OK) return st;
+  // per-device set-up: the scratch array's address, and the kernels this
+  // shape runs loaded (an empty call does only this)
+  void *scratch = nullptr;
+  if ((st = scratch_for_current_device(&scratch)) != HLA_OK) return st;
+  if (prepare_simt_forward(s->dtype, s->dk) != cudaSuccess || prepare_state_scan() != cudaSuccess)
+    return HLA_ERR_CUDA;
   if (empty)
     return pass_state(*s, state_in, state_out, (cudaStream_t)stream) == cudaSuccess ? HLA_OK
                                                                                    : HLA_ERR_CUDA;
-  Plan plan;
-  if ((st = capped_plan(*s, &plan)) != HLA_OK) return st;
-  void *scratch = nullptr;
-  if ((st = scratch_for_current_device(&scratch)) != HLA_OK) return st;
 
   MixerParams P;
   fill_common(P, *s, gamma);

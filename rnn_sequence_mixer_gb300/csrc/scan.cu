@@ -137,6 +137,11 @@ cudaError_t launch_part_sum(const MixerParams &P, bool grad, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+cudaError_t prepare_state_scan() {
+  cudaFuncAttributes a;
+  return cudaFuncGetAttributes(&a, state_scan_kernel);
+}
+
 cudaError_t launch_state_scan(const MixerParams &P, bool write_state_out, cudaStream_t st) {
   dim3 grid(P.B * P.H, ceil_div((long long)P.D * P.D, kScanThreads * kVec));
   state_scan_kernel<<<grid, kScanThreads, 0, st>>>(P, write_state_out ? 1 : 0);

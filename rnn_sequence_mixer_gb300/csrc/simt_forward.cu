@@ -156,8 +156,27 @@ cudaError_t run_output(const MixerParams &P, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// Loads both kernels of one instantiation (under lazy module loading a
+// kernel's module is loaded, and its device memory committed, the first time
+// the runtime touches the kernel) without launching anything.
+template <typename DT, int D>
+cudaError_t prepare() {
+  cudaError_t e = cudaFuncSetAttribute(seg_state_kernel<DT, D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)state_smem<DT, D>());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(seg_output_kernel<DT, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)output_smem<DT, D>());
+}
+
 }  // namespace
 }  // namespace simt
+
+cudaError_t prepare_simt_forward(int dtype, int D) {
+  if (dtype == HLA_BF16)
+    return D == 128 ? simt::prepare<__nv_bfloat16, 128>() : simt::prepare<__nv_bfloat16, 64>();
+  return D == 128 ? simt::prepare<float, 128>() : simt::prepare<float, 64>();
+}
 
 cudaError_t launch_simt_seg_state(const MixerParams &P, int dtype, cudaStream_t st) {
   if (dtype == HLA_BF16)

@@ -141,6 +141,50 @@ def test_prefill_rejects_bad_pointers_gamma_and_workspace(lib):
     assert call_prefill(lib, r) == _lib.HLA_ERR_INVALID_ARG
 
 
+def call_noalloc(lib, s, gamma=None, q=FAKE, k=FAKE, y=FAKE, state_in=None, state_out=None, o=None):
+    gp, keep = _gamma(s.H) if gamma is None else gamma
+    return lib.hla_prefill_noalloc(ctypes.byref(s), q, k, FAKE, FAKE, gp, state_in, state_out, y,
+                                   o, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), _lib.HLA_ERR_UNSUPPORTED),
+    (dict(chunk=32), _lib.HLA_ERR_UNSUPPORTED),
+    (dict(T=-1), _lib.HLA_ERR_INVALID_ARG),
+    (dict(B=-1), _lib.HLA_ERR_INVALID_ARG),
+    (dict(H=257), _lib.HLA_ERR_UNSUPPORTED),
+    (dict(pos_offset=-1), _lib.HLA_ERR_INVALID_ARG),
+    (dict(rope_base=float("inf")), _lib.HLA_ERR_INVALID_ARG),
+])
+def test_noalloc_rejects_bad_shapes(lib, kw, code):
+    assert call_noalloc(lib, shape(**kw)) == code
+
+
+def test_noalloc_rejects_bad_pointers_and_gamma(lib):
+    """Every check of hla_prefill_noalloc runs before its per-device set-up,
+    so none of these calls touches the CUDA runtime."""
+    s = shape()
+    gp, keep = _gamma(2)
+    assert lib.hla_prefill_noalloc(None, FAKE, FAKE, FAKE, FAKE, gp, None, None, FAKE, None,
+                                   None) == _lib.HLA_ERR_INVALID_ARG
+    assert call_noalloc(lib, s, q=None) == _lib.HLA_ERR_INVALID_ARG
+    assert call_noalloc(lib, s, k=FAKE + 8) == _lib.HLA_ERR_INVALID_ARG
+    assert call_noalloc(lib, s, y=None) == _lib.HLA_ERR_INVALID_ARG
+    assert call_noalloc(lib, s, y=FAKE + 2) == _lib.HLA_ERR_INVALID_ARG
+    assert call_noalloc(lib, s, state_in=FAKE + 4) == _lib.HLA_ERR_INVALID_ARG
+    assert call_noalloc(lib, s, state_out=FAKE + 12) == _lib.HLA_ERR_INVALID_ARG
+    assert call_noalloc(lib, s, o=FAKE + 1) == _lib.HLA_ERR_INVALID_ARG
+    for bad in (0.0, -0.5, 1.0001, float("nan"), float("inf")):
+        assert call_noalloc(lib, s, gamma=_gamma(2, bad)) == _lib.HLA_ERR_INVALID_ARG
+    assert lib.hla_prefill_noalloc(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE,
+                                   None, None) == _lib.HLA_ERR_INVALID_ARG
+    # an empty call may pass NULL tensors, but not misaligned ones
+    assert call_noalloc(lib, shape(B=0), q=FAKE + 4) == _lib.HLA_ERR_INVALID_ARG
+    assert call_noalloc(lib, shape(T=0), state_out=FAKE + 4) == _lib.HLA_ERR_INVALID_ARG
+    # more heads than the scratch array holds states for: refused before the set-up
+    assert call_noalloc(lib, shape(B=16, T=8, H=64, d=128)) == _lib.HLA_ERR_WORKSPACE
+
+
 def test_decode_rejects_bad_arguments(lib):
     gp, keep = _gamma(2)
     s = shape(T=2)
