@@ -66,6 +66,22 @@ struct MixerParams {
   unsigned long long rope_u[kMaxPairs];
 };
 
+// Launch parameters of the projection GEMMs (tc_proj.cu): out[M, N] =
+// A[M, K] W[N, K]^T with bf16 A and W.
+struct ProjParams {
+  int M, N, K;            // problem size
+  int n_mt, n_nt;         // output tiles (set by the launcher)
+  int T, H;               // projection in: row m = b T + t, N = 4 H d
+  long long pos_offset;   // projection in: RoPE position of t = 0
+  float eps, kscale;      // projection in: RMSNorm epsilon, 1 / sqrt(d)
+  void *qt, *kt;          // projection in: fp16 [M, H, d] q~ and k~
+  float *scal;            // projection in: fp32 [3, B, H, T] 1/RMS(q), 1/RMS(k), q~ . k~
+  void *v, *g;            // projection in: bf16 [M, H, d] v and the gate logit
+  void *out;              // projection out: bf16 [M, N]
+  unsigned int *err;      // device status word
+  unsigned long long rope_u[kMaxPairs];  // RoPE phase increments (as in MixerParams)
+};
+
 // Segment decomposition of the T axis.  Each (b, h, segment) is one unit of
 // inter-CTA parallelism; the per-segment states are combined by a scan.
 struct Plan {
@@ -113,17 +129,22 @@ __device__ __forceinline__ float gpow(float log2g, float m) { return exp2f(m * l
 // ------------------------------------------------------------------ pieces of the local-state passes
 // The local state of a segment weights token s by gamma^m, m = L - 1 - s from
 // the segment's end (forward) or m = s + 1 from its start (state gradient).
-// For m >= decay_rows(log2 gamma), m |log2 gamma| > 160, so gamma^m computed
-// in fp32 is exactly 0 and those tokens add nothing: the pass skips their
-// tiles.  The tiles that remain are cut into pieces of kPieceTiles, each one
-// CTA writing its own partial sum, which the scan adds in a fixed order.
+// Tokens with m >= W = decay_rows(log2 gamma) are left out: their weights sum
+// to at most sum_{m >= W} gamma^m = gamma^W / (1 - gamma) <= 2^-40, so
+// together they change each state element by at most 2^-40 max_s |k~_s^T v_s|
+// (elementwise), far below the 2^-9 rounding of the bf16 operands the sums
+// are taken on.  The pass skips their tiles; the tiles that remain are cut
+// into pieces of kPieceTiles, each one CTA writing its own partial sum, which
+// the scan adds in a fixed order.  gamma = 1 keeps every token.
 constexpr int kPieceTiles = 48;
+constexpr float kDecayTailLog2 = 40.f;  // -log2 of the bound on the weights left out
 
-// fp32 throughout: its rounding (~1e-7 relative) is far inside the margin
-// between 160 and the 150 below which exp2f stops flushing to 0.
+// fp32 throughout, device code only (the host never needs W): the smallest W
+// with W |log2 gamma| >= 40 + log2(1 / (1 - gamma)).
 __host__ __device__ inline long long decay_rows(float log2g) {
   if (!(log2g < 0.f)) return 1LL << 40;  // gamma = 1: nothing decays
-  const float w = 160.f / -log2g;
+  const float one_minus = -expm1f(log2g * 0.69314718f);  // 1 - gamma, accurate near gamma = 1
+  const float w = (kDecayTailLog2 - log2f(one_minus)) / -log2g;
   return w >= 1.0995116e12f ? (1LL << 40) : (long long)w + 1;
 }
 
@@ -194,6 +215,10 @@ cudaError_t launch_state_scan(const MixerParams &P, bool write_state_out, cudaSt
 cudaError_t launch_grad_scan(const MixerParams &P, bool write_dstate_in, cudaStream_t st);
 cudaError_t launch_part_sum(const MixerParams &P, bool grad, cudaStream_t st);
 cudaError_t launch_simt_seg_state(const MixerParams &P, int dtype, cudaStream_t st);
+// Load the kernels of the fp32 CUDA-core forward (for dtype and D) and of the
+// forward scan without launching them.
+cudaError_t prepare_simt_forward(int dtype, int D);
+cudaError_t prepare_state_scan();
 cudaError_t launch_simt_seg_output(const MixerParams &P, int dtype, cudaStream_t st);
 cudaError_t launch_simt_bwd_dq(const MixerParams &P, int dtype, cudaStream_t st);
 cudaError_t launch_simt_seg_gstate(const MixerParams &P, int dtype, cudaStream_t st);
@@ -204,6 +229,8 @@ cudaError_t launch_tc_seg_output(const MixerParams &P, cudaStream_t st);
 cudaError_t launch_tc_seg_gstate(const MixerParams &P, cudaStream_t st);
 cudaError_t launch_tc_bwd_dq(const MixerParams &P, cudaStream_t st);
 cudaError_t launch_tc_bwd_dkdv(const MixerParams &P, cudaStream_t st);
+cudaError_t launch_proj_in(ProjParams &P, const void *x, const void *w, cudaStream_t st);
+cudaError_t launch_proj_out(ProjParams &P, const void *u, const void *w, cudaStream_t st);
 
 // Bytes reserved at the end of a workspace for the device status word.
 constexpr size_t kStatusBytes = 256;

@@ -21,17 +21,22 @@
 // by a power of two into fp16 range each tile and the scale is undone on O.
 // P (.) D, K~dec and V stay bf16 (V is a bf16 input; MMA3/MMA4 run bf16).
 //
-// Threads: one CTA of 512 per (b, h, segment).  Every CUDA-core phase maps
-// thread (warp w, lane l) to tile row i = 32 (w % 4) + l and column quarter
-// qd = w / 4, which is also the TMEM lane and column block that warp may
-// access.  Thread 0 issues the TMA copies and the MMAs.
+// Threads: both kernels run CTAs of 640 threads (NTO), warp-specialized: 16
+// worker warps (0..15) own the CUDA-core phases and one issuer warpgroup
+// (warps 16..19), whose first lane issues every TMA copy and MMA; workers and
+// issuer hand each phase over through mbarriers.  In the phases that touch
+// TMEM, worker thread (warp w, lane l) owns tile row i = 32 (w % 4) + l and
+// column quarter qd = w / 4, which is also the TMEM lane and column block that
+// warp may access; the feature map uses row 8 w + l / 4 and pair quarter l % 4.
 //
-//   tc_state_kernel:  the segment's local state, sum over its tokens of
-//                     gamma^{end-s} k~_s^T v_s, one MMA per tile accumulated in
-//                     TMEM (the decay weight of each key row is folded into K~);
-//                     also, for the backward, the mirror sum of q~^T do.
-//   tc_output_kernel: the outputs of the segment from the entering state
-//                     written by the fp32 scan (scan.cu).
+//   tc_state_kernel:  one CTA per piece of a segment's local state, the sum
+//                     over its tokens of gamma^{end-s} k~_s^T v_s, one MMA per
+//                     tile accumulated in TMEM (the decay weight of each key
+//                     row is folded into K~); also, for the backward, the
+//                     mirror sum of q~^T do.
+//   tc_output_kernel: one CTA per (b, h, segment): the outputs of the segment
+//                     from the entering state written by the fp32 scan
+//                     (scan.cu).
 #include "tc_common.cuh"
 
 namespace hla {
@@ -56,9 +61,10 @@ struct StateShared {
 // kGrad = true:  DeltaG_seg = sum_s gamma^{s-start+1} q~_s^T do_s, the backward's
 //                per-segment state gradient (q~ = RoPE(Norm(q)), do a bf16 tensor);
 //                tmk then maps q and tmv maps do.
-// One CTA per piece of a segment (piece_tiles): only the tiles whose decay
-// weights can be non-zero in fp32 are read, cut into pieces of at most
-// kPieceTiles, and each piece's sum goes to its own slot of P.part.
+// One CTA per piece of a segment (piece_tiles): only the tiles within the
+// decay horizon decay_rows() are read (the weights beyond it sum to at most
+// 2^-40), cut into pieces of at most kPieceTiles, and each piece's sum goes to
+// its own slot of P.part.
 // Warp-specialized: 16 worker warps turn raw k rows into decay-weighted k~
 // in place (row norms from the four lanes that share a row); the issuer warp
 // issues one MMA per tile as soon as the workers are done with it and refills
@@ -89,7 +95,7 @@ __global__ void __launch_bounds__(NTO, 1)
   piece_tiles(decay_rows(l2g), L, CV, piece, kGrad, lo, hi);
   float *out = P.part ? P.part + ((((size_t)b * P.H + h) * P.nseg + g) * P.npart + piece) * (size_t)D * D
                       : (kGrad ? P.seg2 : P.seg) + (((size_t)b * P.H + h) * P.nseg + g) * (size_t)D * D;
-  if (lo >= hi) {  // nothing with a non-zero weight (uniform: the CTA leaves before any barrier)
+  if (lo >= hi) {  // nothing within the decay horizon (uniform: the CTA leaves before any barrier)
     if (!P.part)   // the segment's only piece: its sum is zero
       for (int e = threadIdx.x; e < D * D; e += NTO) out[e] = 0.f;
     return;

@@ -1,6 +1,6 @@
 """Long segments: the tensor-core local-state passes read only the tiles
-whose decay weights are non-zero in fp32, cut into pieces of at most 48
-tiles whose partial sums are added before the scan.  With 76 heads of 18000
+within the decay horizon (the weights beyond it sum to at most 2^-40), cut
+into pieces of at most 48 tiles whose partial sums are added before the scan.  With 76 heads of 18000
 tokens every head is two segments of 71 tiles (two pieces when every tile
 counts); the forward pass sums the first segment and the state-gradient pass
 the second.  Sampled heads, among them gamma = 1 (every tile, all pieces) and
@@ -68,7 +68,7 @@ def test_backward_with_pieces(case):
 
 def test_arbitrary_gammas_forward_and_backward():
     """Per-head gamma drawn over (0, 1] (not the paper's schedule): each head
-    keeps a different number of non-zero-weight tiles and pieces.  76 heads of
+    keeps a different number of tiles within its decay horizon, and pieces.  76 heads of
     14000 tokens are two segments of 55 tiles each; sampled heads against the
     oracle."""
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
