@@ -15,10 +15,11 @@
  * Norm is RMSNorm x / sqrt(mean(x^2) + norm_eps) with unit weight.  RoPE uses
  * the rotate-half pairing (x_i, x_{i+d/2}), i < d/2, rotated by the angle
  * p * rope_base^(-2i/d), at position p = pos_offset + t (0-based).  The
- * projections x W_{q,k,v,z} and W_o lie outside this library: q, k, v are the
- * projected per-head rows and gate is the pre-sigmoid logit x W_z.  Every RNN
- * head owns its own k and v (the paper's GQA-to-MHA decoupling, Eq. 13), so
- * q, k, v and gate all carry H heads.
+ * mixer entry points take q, k, v as the projected per-head rows and gate as
+ * the pre-sigmoid logit x W_z; the projections themselves (x W_{q,k,v,z} with
+ * the feature map fused, and the output projection W_o) are separate entry
+ * points at the end of this header.  Every RNN head owns its own k and v (the
+ * paper's GQA-to-MHA decoupling, Eq. 13), so q, k, v and gate all carry H heads.
  *
  * Conventions shared by every entry point
  *   - Activations q, k, v, gate, y, dy, dq, dk, dv, dgate: device memory,
@@ -57,7 +58,7 @@
 extern "C" {
 #endif
 
-#define HLA_ABI_VERSION 5
+#define HLA_ABI_VERSION 6
 
 typedef enum {
   HLA_OK = 0,
@@ -84,6 +85,9 @@ typedef struct {
   int64_t pos_offset; /* RoPE position of token 0 (prefill and backward)        */
   double rope_base;   /* RoPE base theta (1e6 for HypeNet-2B/5B/9B, Table 6)    */
   float norm_eps;     /* RMSNorm epsilon of the QK norms and the output norm    */
+  int32_t passes;     /* hla_prefill / hla_prefill_features, tensor-core path:  */
+                      /* 0 = the library's choice, 1 = one launch, 3 = three     */
+                      /* (see hla_prefill); 0 for every other entry point       */
 } hla_shape;
 
 typedef void *hla_stream; /* a cudaStream_t */
@@ -118,6 +122,16 @@ hla_status hla_gamma_schedule(int32_t H, float *gamma_out);
 
 /* Device workspace bytes hla_prefill needs for this shape (0 on a bad shape). */
 size_t hla_prefill_workspace_size(const hla_shape *shape);
+
+/*
+ * Kernels one hla_prefill (or hla_prefill_features) call with this shape and
+ * gamma (HOST fp32 [H]) launches, and one hla_prefill_backward call (with a
+ * forward workspace, with_fwd_ws != 0, or without); -1 on a bad argument.
+ * For profiling and graph planning; the memsets of the status word are not
+ * kernels and are not counted.
+ */
+int32_t hla_prefill_launches(const hla_shape *shape, const float *gamma);
+int32_t hla_backward_launches(const hla_shape *shape, const float *gamma, int32_t with_fwd_ws);
 
 /*
  * Bytes of the features hla_prefill can save for hla_prefill_backward (its
@@ -162,11 +176,47 @@ size_t hla_saved_bytes(const hla_shape *shape);
  *                  and without it.
  * The output of token t depends on all tokens <= t of its sequence and on
  * state_in; sequences and heads are independent.
+ *
+ * Launches.  The T axis of each (sequence, head) is cut into segments that
+ * run as separate CTAs; each needs the state entering it.  With
+ * shape->passes == 3 a local-state pass sums each segment's own tokens, a
+ * scan over the segments chains those sums into the entering states, and the
+ * output pass runs from them (plus a partial-sum kernel where a head's sums
+ * are split in pieces).  With shape->passes == 1 everything is one launch:
+ * each output CTA first sums the tokens before its segment that are still
+ * within the decay horizon (weights gamma^m whose tail beyond it sums to at
+ * most 2^-40; every token before it when gamma = 1) on top of gamma^t0
+ * state_in, then runs its segment; no CTA waits for another.  Both write the
+ * state entering every segment to the workspace.  0 lets the library choose:
+ * three passes (measured faster at every workload of this library; one launch
+ * saves the 0.1 ms of the local-state pass and the scan at 512K tokens but
+ * costs the output kernel more).  The fp32 CUDA-core path (fp32 or d = 64)
+ * always runs three passes.
  */
 hla_status hla_prefill(const hla_shape *shape, const void *q, const void *k, const void *v,
                        const void *gate, const float *gamma, const float *state_in,
                        float *state_out, void *y, float *o, void *ws, size_t ws_bytes,
                        hla_stream stream, const hla_trace *trace, void *saved);
+
+/*
+ * hla_prefill from features instead of raw q and k: the layer whose input
+ * projection ran through hla_project_in (Appendix A, Eq. 18; the feature map
+ * RMSNorm + RoPE is already applied there).
+ *   features  in: hla_saved_bytes(shape) bytes in the layout documented there
+ *                 (fp16 q~ and k~, fp32 1/RMS(q), 1/RMS(k), q~ . k~), as
+ *                 written by hla_project_in or by an hla_prefill `saved`
+ *   v, gate, gamma, state_in, state_out, y, o, ws, ws_bytes, trace:
+ *                 as for hla_prefill (the same workspace size)
+ * Tensor-core path only: bf16 at d = 128, else HLA_ERR_UNSUPPORTED.  The
+ * result equals hla_prefill on the raw q and k that produced the features, up
+ * to the rounding of q~ and k~ to fp16, which hla_prefill applies as well.
+ * The same `features` buffer can then be passed to hla_prefill_backward as its
+ * `saved` argument (with q = k = NULL).
+ */
+hla_status hla_prefill_features(const hla_shape *shape, const void *features, const void *v,
+                                const void *gate, const float *gamma, const float *state_in,
+                                float *state_out, void *y, float *o, void *ws, size_t ws_bytes,
+                                hla_stream stream, const hla_trace *trace);
 
 /*
  * hla_prefill for callers that cannot allocate device memory.  The paper has
@@ -267,9 +317,11 @@ size_t hla_backward_workspace_size(const hla_shape *shape);
  *                    not hold those states gives wrong gradients; nothing can
  *                    check it.
  *   saved            optional: the `saved` buffer of an hla_prefill call with
- *                    the same shape, q and k, enqueued before this call and
- *                    not reused since.  The backward passes read q~, k~ and
- *                    the norms from it instead of recomputing them.  Read
+ *                    the same shape, q and k, or the `features` of
+ *                    hla_project_in / hla_prefill_features, enqueued before
+ *                    this call and not reused since.  The backward passes read
+ *                    q~, k~ and the norms from it instead of recomputing them,
+ *                    and raw q and k are not read: they may be NULL.  Read
  *                    only.  NULL = recompute.  HLA_ERR_UNSUPPORTED unless bf16
  *                    at d = 128.  Gradients agree with the
  *                    recomputing path up to the fp16 rounding of q~ and k~
@@ -330,6 +382,50 @@ size_t hla_attention_workspace_size(const hla_attn_shape *shape);
 hla_status hla_attention_prefill(const hla_attn_shape *shape, const void *q, const void *k,
                                  const void *v, const void *gate, void *y, float *o, void *ws,
                                  size_t ws_bytes, hla_stream stream);
+
+/*
+ * The projections around the RNN mixer (Appendix A, Eq. 18, "RNN Layers"):
+ * q_t = Norm(x_t W_q), k_t = Norm(x_t W_k), v_t = x_t W_v,
+ * z_t = sigmoid(x_t W_z) and y_t = (Norm(o_t) . z_t) W_o^T, with W_q, W_k, W_v,
+ * W_z, W_o in R^{D x d} per head (D the model width).  Tensor-core GEMMs with
+ * bf16 operands and fp32 accumulation.  Each call's workspace holds only its
+ * device status word (hla_project_workspace_size() bytes): cleared by the
+ * call, non-zero after it completes when a bounded device-side wait gave up.
+ */
+size_t hla_project_workspace_size(void);
+
+/*
+ * Input projection of every head at once, the mixer's feature map fused into
+ * the epilogue: from the fp32 products x W_q,h and x W_k,h it writes the
+ * features hla_prefill_features and hla_prefill_backward read (q~, k~ as
+ * fp16, 1/RMS(q), 1/RMS(k) and the fp32 q~ . k~); raw q and k never reach
+ * memory.  v = x W_v,h and the gate logit x W_z,h are written as bf16.
+ *   shape     B, T, H, dk = dv = 128, dtype HLA_BF16, pos_offset, rope_base and
+ *             norm_eps as for hla_prefill (chunk 64 or 128, decode_split 0)
+ *   d_model   D, a positive multiple of 64
+ *   x         in:  bf16 [B, T, D]
+ *   w_qkvz    in:  bf16 [H, 4, d, D]: for head h, the transposes of the paper's
+ *                  W_q, W_k, W_v, W_z in that order (row c of w_qkvz[h][j] is
+ *                  column c of W_j,h: a linear layer's output-major weight)
+ *   features  out: hla_saved_bytes(shape) bytes (layout there)
+ *   v, gate   out: bf16 [B, T, H, d]
+ * HLA_ERR_UNSUPPORTED unless bf16 at d = 128 with D % 64 == 0 and B T < 2^31.
+ */
+hla_status hla_project_in(const hla_shape *shape, int32_t d_model, const void *x,
+                          const void *w_qkvz, void *features, void *v, void *gate, void *ws,
+                          size_t ws_bytes, hla_stream stream);
+
+/*
+ * Output projection: out[m] = u[m] W_o^T for M rows, u the gated, normalized
+ * mixer rows of all heads side by side (hla_prefill's y viewed as [M, H d]).
+ *   u     in:  bf16 [M, n_in], n_in = H d a positive multiple of 64
+ *   w_o   in:  bf16 [d_model, n_in]: the paper's W_o of every head side by
+ *              side (column h d + c belongs to head h)
+ *   out   out: bf16 [M, d_model], d_model a positive multiple of 128
+ */
+hla_status hla_project_out(int64_t M, int32_t n_in, int32_t d_model, const void *u,
+                           const void *w_o, void *out, void *ws, size_t ws_bytes,
+                           hla_stream stream);
 
 #ifdef __cplusplus
 }

@@ -24,14 +24,20 @@ EXPORTS = (
     "hla_status_string",
     "hla_gamma_schedule",
     "hla_prefill_workspace_size",
+    "hla_prefill_launches",
+    "hla_backward_launches",
     "hla_saved_bytes",
     "hla_prefill",
     "hla_decode_step",
     "hla_backward_workspace_size",
     "hla_prefill_backward",
+    "hla_prefill_features",
     "hla_prefill_noalloc",
     "hla_attention_workspace_size",
     "hla_attention_prefill",
+    "hla_project_workspace_size",
+    "hla_project_in",
+    "hla_project_out",
 )
 
 
@@ -48,6 +54,7 @@ class HlaShape(ctypes.Structure):
         ("pos_offset", ctypes.c_int64),
         ("rope_base", ctypes.c_double),
         ("norm_eps", ctypes.c_float),
+        ("passes", ctypes.c_int32),
     ]
 
 
@@ -104,6 +111,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.hla_gamma_schedule.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_float)]
     lib.hla_prefill_workspace_size.restype = sz
     lib.hla_prefill_workspace_size.argtypes = [shp]
+    fp = ctypes.POINTER(ctypes.c_float)
+    lib.hla_prefill_launches.restype = ctypes.c_int32
+    lib.hla_prefill_launches.argtypes = [shp, fp]
+    lib.hla_backward_launches.restype = ctypes.c_int32
+    lib.hla_backward_launches.argtypes = [shp, fp, ctypes.c_int32]
     lib.hla_saved_bytes.restype = sz
     lib.hla_saved_bytes.argtypes = [shp]
     lib.hla_backward_workspace_size.restype = sz
@@ -118,6 +130,16 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.hla_prefill_backward.restype = ctypes.c_int
     lib.hla_prefill_backward.argtypes = [shp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_float), f32p,
                                          vp, f32p, vp, vp, vp, vp, f32p, vp, sz, vp, trp, vp, vp]
+    lib.hla_prefill_features.restype = ctypes.c_int
+    lib.hla_prefill_features.argtypes = [shp, vp, vp, vp, ctypes.POINTER(ctypes.c_float), f32p,
+                                         f32p, vp, f32p, vp, sz, vp, trp]
+    lib.hla_project_workspace_size.restype = sz
+    lib.hla_project_workspace_size.argtypes = []
+    lib.hla_project_in.restype = ctypes.c_int
+    lib.hla_project_in.argtypes = [shp, ctypes.c_int32, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.hla_project_out.restype = ctypes.c_int
+    lib.hla_project_out.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, vp, vp, vp, vp,
+                                    sz, vp]
     lib.hla_prefill_noalloc.restype = ctypes.c_int
     lib.hla_prefill_noalloc.argtypes = [shp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_float), f32p,
                                         f32p, vp, f32p, vp]

@@ -54,11 +54,11 @@ def _check_state(s: Optional[torch.Tensor], B, H, d, device):
 
 
 def make_shape(B, T, H, d, *, chunk=64, dtype=torch.bfloat16, pos_offset=0, rope_base=1e4,
-               eps=1e-6, decode_split=0) -> _lib.HlaShape:
+               eps=1e-6, decode_split=0, passes=0) -> _lib.HlaShape:
     return _lib.HlaShape(B=B, T=T, H=H, dk=d, dv=d, chunk=chunk, dtype=_DTYPES[dtype],
                          decode_split=int(decode_split),
                          pos_offset=int(pos_offset), rope_base=float(rope_base),
-                         norm_eps=float(eps))
+                         norm_eps=float(eps), passes=int(passes))
 
 
 def gamma_schedule(H: int) -> torch.Tensor:
@@ -72,6 +72,18 @@ def gamma_schedule(H: int) -> torch.Tensor:
 
 def prefill_workspace_size(shape: _lib.HlaShape) -> int:
     return int(_lib.load().hla_prefill_workspace_size(ctypes.byref(shape)))
+
+
+def prefill_launches(shape: _lib.HlaShape, gamma) -> int:
+    """hla_prefill_launches: kernels one prefill call with this shape launches."""
+    g_host, g_ptr = _host_gamma(gamma, shape.H)
+    return int(_lib.load().hla_prefill_launches(ctypes.byref(shape), g_ptr))
+
+
+def backward_launches(shape: _lib.HlaShape, gamma, with_fwd_ws: bool) -> int:
+    """hla_backward_launches: kernels one prefill_backward call launches."""
+    g_host, g_ptr = _host_gamma(gamma, shape.H)
+    return int(_lib.load().hla_backward_launches(ctypes.byref(shape), g_ptr, int(bool(with_fwd_ws))))
 
 
 def saved_bytes(shape: _lib.HlaShape) -> int:
@@ -116,16 +128,18 @@ def _trace(events, device):
 
 def prefill(q, k, v, gate, gamma: Sequence[float] | torch.Tensor, state_in=None, *, chunk=64,
             pos_offset=0, rope_base=1e4, eps=1e-6, want_o=False, want_state=True, y=None,
-            state_out=None, workspace=None, trace=None, saved=None):
+            state_out=None, workspace=None, trace=None, saved=None, passes=0):
     """hla_prefill.  Returns (y, o or None, state_out or None).  ``trace``: optional
     list of torch.cuda.Event recorded before each pass and after the last.
     ``saved``: optional uint8 CUDA tensor of ``saved_bytes(shape)`` bytes that
-    receives the features for ``prefill_backward(..., saved=...)``."""
+    receives the features for ``prefill_backward(..., saved=...)``.  ``passes``:
+    0 (the library's choice), 1 (one launch) or 3 (local-state pass, scan,
+    output pass)."""
     _check_acts(q, k, v, gate)
     B, T, H, d = q.shape
     _check_state(state_in, B, H, d, q.device)
     shape = make_shape(B, T, H, d, chunk=chunk, dtype=q.dtype, pos_offset=pos_offset,
-                       rope_base=rope_base, eps=eps)
+                       rope_base=rope_base, eps=eps, passes=passes)
     lib = _lib.load()
     g_host, g_ptr = _host_gamma(gamma, H)
     if y is None:
@@ -177,6 +191,41 @@ def decode_step(q, k, v, gate, gamma, state, pos=None, *, pos_offset=0, rope_bas
     return y, o, state_out
 
 
+def prefill_features(features, v, gate, gamma, state_in=None, *, chunk=64, pos_offset=0,
+                     rope_base=1e4, eps=1e-6, want_o=False, want_state=True, y=None,
+                     state_out=None, workspace=None, trace=None, passes=0):
+    """hla_prefill_features: the forward from q~, k~ features (``features``: a
+    uint8 CUDA tensor of ``saved_bytes(shape)`` bytes, e.g. from
+    ``project_in``) and raw v, gate [B, T, H, d] bf16.  Returns
+    (y, o or None, state_out or None)."""
+    _check_acts(v, gate)
+    B, T, H, d = v.shape
+    _check_state(state_in, B, H, d, v.device)
+    shape = make_shape(B, T, H, d, chunk=chunk, dtype=v.dtype, pos_offset=pos_offset,
+                       rope_base=rope_base, eps=eps, passes=passes)
+    _check_saved(features, shape)
+    lib = _lib.load()
+    g_host, g_ptr = _host_gamma(gamma, H)
+    if y is None:
+        y = torch.empty_like(v)
+    o = torch.empty(v.shape, dtype=torch.float32, device=v.device) if want_o else None
+    if want_state and state_out is None:
+        state_out = torch.empty((B, H, d, d), dtype=torch.float32, device=v.device)
+    if not want_state:
+        state_out = None
+    if workspace is None:
+        workspace = torch.empty(max(prefill_workspace_size(shape), 16), dtype=torch.uint8,
+                                device=v.device)
+    tr = _trace(trace, v.device)
+    st = lib.hla_prefill_features(ctypes.byref(shape), _ptr(features), _ptr(v), _ptr(gate), g_ptr,
+                                  _ptr(state_in), _ptr(state_out), _ptr(y), _ptr(o),
+                                  _ptr(workspace), workspace.numel(), _stream(v.device),
+                                  tr[0] if tr else None)
+    _lib.check(st, "hla_prefill_features")
+    del g_host
+    return y, o, state_out
+
+
 def prefill_backward(q, k, v, gate, gamma, dy, state_in=None, dstate_out=None, *, chunk=64,
                      pos_offset=0, rope_base=1e4, eps=1e-6, want_dstate_in=False,
                      workspace=None, trace=None, fwd_workspace=None, saved=None):
@@ -184,27 +233,33 @@ def prefill_backward(q, k, v, gate, gamma, dy, state_in=None, dstate_out=None, *
     ``fwd_workspace``: the ``workspace`` of a ``prefill`` call on the same
     shape, inputs, gamma and state_in, enqueued earlier on this stream; the
     backward then reads the forward's segment states instead of recomputing
-    them.  ``saved``: the ``saved`` buffer of such a call; the backward reads
-    the q / k features from it."""
-    _check_acts(q, k, v, gate, dy)
-    B, T, H, d = q.shape
-    _check_state(state_in, B, H, d, q.device)
-    _check_state(dstate_out, B, H, d, q.device)
-    shape = make_shape(B, T, H, d, chunk=chunk, dtype=q.dtype, pos_offset=pos_offset,
+    them.  ``saved``: the ``saved`` buffer of such a call (or the features of
+    ``project_in``); the backward reads the q / k features from it, and q and
+    k may then be None."""
+    if saved is not None and q is None and k is None:
+        _check_acts(v, gate, dy)
+        ref = v
+    else:
+        _check_acts(q, k, v, gate, dy)
+        ref = q
+    B, T, H, d = ref.shape
+    _check_state(state_in, B, H, d, ref.device)
+    _check_state(dstate_out, B, H, d, ref.device)
+    shape = make_shape(B, T, H, d, chunk=chunk, dtype=ref.dtype, pos_offset=pos_offset,
                        rope_base=rope_base, eps=eps)
     lib = _lib.load()
     g_host, g_ptr = _host_gamma(gamma, H)
-    dq, dk, dv, dg = (torch.empty_like(q) for _ in range(4))
-    dsi = torch.empty((B, H, d, d), dtype=torch.float32, device=q.device) if want_dstate_in else None
+    dq, dk, dv, dg = (torch.empty_like(ref) for _ in range(4))
+    dsi = torch.empty((B, H, d, d), dtype=torch.float32, device=ref.device) if want_dstate_in else None
     ws_bytes = backward_workspace_size(shape)
     if workspace is None:
-        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=ref.device)
     _check_saved(saved, shape)
-    tr = _trace(trace, q.device)
+    tr = _trace(trace, ref.device)
     st = lib.hla_prefill_backward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(gate), g_ptr,
                                   _ptr(state_in), _ptr(dy), _ptr(dstate_out), _ptr(dq), _ptr(dk),
                                   _ptr(dv), _ptr(dg), _ptr(dsi), _ptr(workspace), workspace.numel(),
-                                  _stream(q.device), tr[0] if tr else None, _ptr(fwd_workspace),
+                                  _stream(ref.device), tr[0] if tr else None, _ptr(fwd_workspace),
                                   _ptr(saved))
     _lib.check(st, "hla_prefill_backward")
     del g_host
@@ -245,3 +300,69 @@ def attention_prefill(q, k, v, gate, a: float, *, pos_offset=0, eps=1e-6, want_o
                                    _stream(q.device))
     _lib.check(st, "hla_attention_prefill")
     return y, o
+
+
+def project_workspace_size() -> int:
+    return int(_lib.load().hla_project_workspace_size())
+
+
+def project_in(x, w_qkvz, *, pos_offset=0, rope_base=1e4, eps=1e-6, chunk=64, features=None,
+               v=None, gate=None, workspace=None):
+    """hla_project_in: x [B, T, D] bf16 and w_qkvz [H, 4, d, D] bf16 (per head the
+    transposes of W_q, W_k, W_v, W_z).  Returns (features, v, gate): features a
+    uint8 tensor in the saved layout (q~, k~ fp16 and the fp32 scalars), v and
+    gate bf16 [B, T, H, d]."""
+    if not (x.is_cuda and w_qkvz.is_cuda) or x.dtype != torch.bfloat16 or w_qkvz.dtype != torch.bfloat16:
+        raise ValueError("x and w_qkvz are bf16 CUDA tensors (no CPU path)")
+    if x.dim() != 3 or w_qkvz.dim() != 4 or w_qkvz.shape[1] != 4 or w_qkvz.shape[3] != x.shape[2]:
+        raise ValueError("x must be [B, T, D] and w_qkvz [H, 4, d, D]")
+    if not (x.is_contiguous() and w_qkvz.is_contiguous()):
+        raise ValueError("x and w_qkvz must be contiguous")
+    B, T, Dm = x.shape
+    H, _, d, _ = w_qkvz.shape
+    shape = make_shape(B, T, H, d, chunk=chunk, dtype=torch.bfloat16, pos_offset=pos_offset,
+                       rope_base=rope_base, eps=eps)
+    lib = _lib.load()
+    if features is None:
+        features = torch.empty(max(saved_bytes(shape), 16), dtype=torch.uint8, device=x.device)
+    _check_saved(features, shape)
+    if v is None:
+        v = torch.empty((B, T, H, d), dtype=torch.bfloat16, device=x.device)
+    if gate is None:
+        gate = torch.empty((B, T, H, d), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(project_workspace_size(), dtype=torch.uint8, device=x.device)
+    st = lib.hla_project_in(ctypes.byref(shape), Dm, _ptr(x), _ptr(w_qkvz), _ptr(features),
+                            _ptr(v), _ptr(gate), _ptr(workspace), workspace.numel(),
+                            _stream(x.device))
+    _lib.check(st, "hla_project_in")
+    return features, v, gate
+
+
+def project_out(u, w_o, *, out=None, workspace=None):
+    """hla_project_out: u [..., n_in] bf16 (e.g. y [B, T, H, d] with n_in = H d
+    folded), w_o [D, n_in] bf16.  Returns out [rows, D] shaped like u's leading
+    dimensions plus D."""
+    if not (u.is_cuda and w_o.is_cuda) or u.dtype != torch.bfloat16 or w_o.dtype != torch.bfloat16:
+        raise ValueError("u and w_o are bf16 CUDA tensors (no CPU path)")
+    if not (u.is_contiguous() and w_o.is_contiguous()) or w_o.dim() != 2:
+        raise ValueError("u and w_o must be contiguous, w_o [D, n_in]")
+    Dm, n_in = w_o.shape
+    if u.dim() == 4:  # [B, T, H, d]
+        lead = u.shape[:2]
+        if u.shape[2] * u.shape[3] != n_in:
+            raise ValueError("u's heads times d must equal w_o's columns")
+    else:
+        lead = u.shape[:-1]
+        if u.shape[-1] != n_in:
+            raise ValueError("u's last dimension must equal w_o's columns")
+    M = u.numel() // n_in
+    lib = _lib.load()
+    if out is None:
+        out = torch.empty(tuple(lead) + (Dm,), dtype=torch.bfloat16, device=u.device)
+    if workspace is None:
+        workspace = torch.empty(project_workspace_size(), dtype=torch.uint8, device=u.device)
+    st = lib.hla_project_out(M, n_in, Dm, _ptr(u), _ptr(w_o), _ptr(out), _ptr(workspace),
+                             workspace.numel(), _stream(u.device))
+    _lib.check(st, "hla_project_out")
+    return out

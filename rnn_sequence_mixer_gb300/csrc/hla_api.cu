@@ -48,6 +48,7 @@ hla_status check_shape(const hla_shape *s, bool decode) {
   if (!(s->rope_base > 0.0) || !isfinite(s->rope_base)) return HLA_ERR_INVALID_ARG;
   if (!(s->norm_eps >= 0.0f) || !isfinite(s->norm_eps)) return HLA_ERR_INVALID_ARG;
   if (s->pos_offset < 0 || s->pos_offset > (1LL << 62) - (long long)s->T) return HLA_ERR_INVALID_ARG;
+  if (s->passes != 0 && (decode || (s->passes != 1 && s->passes != 3))) return HLA_ERR_INVALID_ARG;
   if (s->dtype != HLA_F32 && s->dtype != HLA_BF16) return HLA_ERR_UNSUPPORTED;
   if (s->dk != s->dv || (s->dk != 64 && s->dk != 128)) return HLA_ERR_UNSUPPORTED;
   if (s->H > kMaxHeads) return HLA_ERR_UNSUPPORTED;
@@ -183,6 +184,18 @@ size_t part_bytes(const hla_shape &s, const Plan &p) {
   return n > 1 ? (size_t)s.B * s.H * p.nseg * (size_t)n * s.dk * s.dv * sizeof(float) : 0;
 }
 
+// Whether a tensor-core prefill runs in one launch: only when the caller asks
+// (shape->passes == 1).  Measured on a GB300 at the 512K workload, one launch
+// took 2.35 ms against 2.18 ms for the three passes: the window phase in the
+// output kernel costs its tile loop ~5% (the kernel runs at the 96-register
+// limit of its 640 threads) and the slowest heads' windows (67 tiles) lengthen
+// their CTAs, while the local-state pass and the scan it saves take 0.1 ms.
+bool one_launch(const hla_shape &s, const Plan &p, const float *gamma) {
+  (void)p;
+  (void)gamma;
+  return s.passes == 1;
+}
+
 // Whether a shape can save its features: the tensor-core path (bf16, d = 128).
 bool can_save(const hla_shape &s) { return s.dtype == HLA_BF16 && s.dk == 128; }
 
@@ -193,7 +206,7 @@ size_t saved_bytes(const hla_shape &s) {
   return saved_scalar_offset(s.B, s.T, s.H, s.dk) + 3 * (size_t)s.B * s.T * s.H * sizeof(float);
 }
 
-void fill_rope(MixerParams &P, int D, double base) {
+void fill_rope_u(unsigned long long *u, int D, double base) {
   // One-entry per-thread cache: the table depends only on (base, D).
   thread_local double cached_base = -1.0;
   thread_local int cached_D = 0;
@@ -201,16 +214,18 @@ void fill_rope(MixerParams &P, int D, double base) {
   if (cached_base != base || cached_D != D) {
     const double two_pi = 6.283185307179586476925286766559;
     for (int i = 0; i < D / 2; ++i) {
-      double u = pow(base, -2.0 * (double)i / (double)D) / two_pi;
-      u -= floor(u);
-      double scaled = ldexp(u, 64);
+      double v = pow(base, -2.0 * (double)i / (double)D) / two_pi;
+      v -= floor(v);
+      double scaled = ldexp(v, 64);
       cached[i] = scaled >= 18446744073709551615.0 ? 0ull : (unsigned long long)scaled;
     }
     cached_base = base;
     cached_D = D;
   }
-  for (int i = 0; i < D / 2; ++i) P.rope_u[i] = cached[i];
+  for (int i = 0; i < D / 2; ++i) u[i] = cached[i];
 }
+
+void fill_rope(MixerParams &P, int D, double base) { fill_rope_u(P.rope_u, D, base); }
 
 }  // namespace hla
 
@@ -245,6 +260,30 @@ size_t hla_prefill_workspace_size(const hla_shape *s) {
   return seg_bytes(*s, p) + part_bytes(*s, p) + kStatusBytes;
 }
 
+int32_t hla_prefill_launches(const hla_shape *s, const float *gamma) {
+  if (check_shape(s, false) != HLA_OK || check_gamma(gamma, s->H) != HLA_OK) return -1;
+  const Plan p = make_plan(*s);
+  if (p.nseg == 0) return 0;
+  const bool tc = s->dtype == HLA_BF16 && s->dk == 128;
+  if (!tc) return 3;
+  if (one_launch(*s, p, gamma)) return 1;
+  // local-state pass (every segment but the last) and its piece sums, scan, outputs
+  const int state = p.nseg > 1 ? 1 + (part_count(*s, p) > 1 ? 1 : 0) : 0;
+  return state + 2;
+}
+
+int32_t hla_backward_launches(const hla_shape *s, const float *gamma, int32_t with_fwd_ws) {
+  if (check_shape(s, false) != HLA_OK || check_gamma(gamma, s->H) != HLA_OK) return -1;
+  const Plan p = make_plan(*s);
+  if (p.nseg == 0) return 0;
+  const bool tc = s->dtype == HLA_BF16 && s->dk == 128;
+  // forward states (local-state pass and scan) unless read from the forward's workspace
+  const int sums = tc ? (p.nseg > 1 ? 1 + (part_count(*s, p) > 1 ? 1 : 0) : 0) : 1;
+  const int fwd = with_fwd_ws ? 0 : sums + 1;
+  // dq pass, state-gradient sums, their scan, dk/dv pass
+  return fwd + 1 + sums + 1 + 1;
+}
+
 size_t hla_saved_bytes(const hla_shape *s) {
   if (check_shape(s, false) != HLA_OK) return 0;
   return saved_bytes(*s);
@@ -258,15 +297,25 @@ size_t hla_backward_workspace_size(const hla_shape *s) {
          kStatusBytes;
 }
 
-hla_status hla_prefill(const hla_shape *s, const void *q, const void *k, const void *v,
-                       const void *gate, const float *gamma, const float *state_in,
-                       float *state_out, void *y, float *o, void *ws, size_t ws_bytes,
-                       hla_stream stream, const hla_trace *trace, void *saved) {
+}  // extern "C"
+
+namespace {
+
+// hla_prefill, and hla_prefill_features (features = the saved-layout q~, k~
+// and scalars given in place of raw q and k; tensor-core path only).
+hla_status prefill_impl(const hla_shape *s, const void *q, const void *k, const void *features,
+                        const void *v, const void *gate, const float *gamma, const float *state_in,
+                        float *state_out, void *y, float *o, void *ws, size_t ws_bytes,
+                        hla_stream stream, const hla_trace *trace, void *saved) {
   HLA_TRY(check_shape(s, false));
   HLA_TRY(check_gamma(gamma, s->H));
   const bool empty = s->B == 0 || s->T == 0;
-  HLA_TRY(need_unless(empty, q));
-  HLA_TRY(need_unless(empty, k));
+  if (features) {
+    HLA_TRY(need_unless(empty, features));
+  } else {
+    HLA_TRY(need_unless(empty, q));
+    HLA_TRY(need_unless(empty, k));
+  }
   HLA_TRY(need_unless(empty, v));
   HLA_TRY(need_unless(empty, gate));
   HLA_TRY(need_unless(empty, y));
@@ -275,7 +324,7 @@ hla_status hla_prefill(const hla_shape *s, const void *q, const void *k, const v
   HLA_TRY(maybe(o));
   HLA_TRY(check_trace(trace));
   HLA_TRY(maybe(saved));
-  if (saved && !can_save(*s)) return HLA_ERR_UNSUPPORTED;
+  if ((saved || features) && !can_save(*s)) return HLA_ERR_UNSUPPORTED;
   Plan plan = make_plan(*s);
   size_t need_ws = seg_bytes(*s, plan) + part_bytes(*s, plan) + kStatusBytes;
   if (!ws || !aligned16(ws) || ws_bytes < need_ws) return HLA_ERR_WORKSPACE;
@@ -301,23 +350,57 @@ hla_status hla_prefill(const hla_shape *s, const void *q, const void *k, const v
   P.npart = part_count(*s, plan);
   P.part = P.npart > 1 ? (float *)((char *)ws + seg_bytes(*s, plan)) : nullptr;
   P.err = (unsigned int *)((char *)ws + need_ws - kStatusBytes);
+  if (features) {  // read by both passes
+    P.features_in = 1;
+    P.saved = (unsigned char *)const_cast<void *>(features);
+  }
   cudaStream_t st = (cudaStream_t)stream;
   const bool tc = tc_supported(P, s->dtype);
   Tracer tr{trace, st};
   HLA_LAUNCH(cudaMemsetAsync(P.err, 0, sizeof(unsigned int), st));
+  if (tc && one_launch(*s, plan, gamma)) {
+    // one launch: each output CTA forms its entering state from the decay window
+    P.fused = 1;
+    if (!features) P.saved = (unsigned char *)saved;
+    for (int i = 0; i < 3; ++i) HLA_LAUNCH(tr.mark());  // no local-state pass, no scan
+    HLA_LAUNCH(launch_tc_seg_output(P, st));
+    HLA_LAUNCH(tr.mark());
+    return HLA_OK;
+  }
   HLA_LAUNCH(tr.mark());
   // tensor cores: the last segment's local state is not summed; its output
   // pass writes state_out from the state it carries
   P.state_seg0 = 0;
   P.state_nseg = P.nseg - 1;
   HLA_LAUNCH(tc ? launch_tc_seg_state(P, st) : launch_simt_seg_state(P, s->dtype, st));
-  P.saved = (unsigned char *)saved;  // written by the output pass only
+  if (!features) P.saved = (unsigned char *)saved;  // written by the output pass only
   HLA_LAUNCH(tr.mark());
   HLA_LAUNCH(launch_state_scan(P, !tc && state_out != nullptr, st));
   HLA_LAUNCH(tr.mark());
   HLA_LAUNCH(tc ? launch_tc_seg_output(P, st) : launch_simt_seg_output(P, s->dtype, st));
   HLA_LAUNCH(tr.mark());
   return HLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+hla_status hla_prefill(const hla_shape *s, const void *q, const void *k, const void *v,
+                       const void *gate, const float *gamma, const float *state_in,
+                       float *state_out, void *y, float *o, void *ws, size_t ws_bytes,
+                       hla_stream stream, const hla_trace *trace, void *saved) {
+  return prefill_impl(s, q, k, nullptr, v, gate, gamma, state_in, state_out, y, o, ws, ws_bytes,
+                      stream, trace, saved);
+}
+
+hla_status hla_prefill_features(const hla_shape *s, const void *features, const void *v,
+                                const void *gate, const float *gamma, const float *state_in,
+                                float *state_out, void *y, float *o, void *ws, size_t ws_bytes,
+                                hla_stream stream, const hla_trace *trace) {
+  if (!features) return HLA_ERR_INVALID_ARG;
+  return prefill_impl(s, nullptr, nullptr, features, v, gate, gamma, state_in, state_out, y, o, ws,
+                      ws_bytes, stream, trace, nullptr);
 }
 
 hla_status hla_decode_step(const hla_shape *s, const void *q, const void *k, const void *v,
@@ -364,8 +447,11 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
   HLA_TRY(check_shape(s, false));
   HLA_TRY(check_gamma(gamma, s->H));
   const bool empty = s->B == 0 || s->T == 0;
-  const void *acts[] = {q, k, v, gate, dy, dq, dk, dv, dgate};
+  // with saved features the raw q and k are not read: they may be NULL
+  const void *acts[] = {v, gate, dy, dq, dk, dv, dgate};
   for (const void *a : acts) HLA_TRY(need_unless(empty, a));
+  HLA_TRY(saved ? maybe(q) : need_unless(empty, q));
+  HLA_TRY(saved ? maybe(k) : need_unless(empty, k));
   HLA_TRY(maybe(state_in));
   HLA_TRY(maybe(dstate_out));
   HLA_TRY(maybe(dstate_in));
@@ -414,7 +500,13 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
   HLA_LAUNCH(tr.mark());
   P.state_seg0 = 0;  // entering states only: the last segment's sum is not needed
   P.state_nseg = P.nseg - 1;
+  // recomputed from raw k (the forward's own arithmetic, so the states are
+  // bit-identical to those a forward workspace holds), or, when the caller
+  // gave saved features without raw k, from the k~ saved there
+  P.saved = (unsigned char *)const_cast<void *>(saved);
+  P.features_in = (saved && !k) ? 1 : 0;
   if (!fwd_ws) HLA_LAUNCH(tc ? launch_tc_seg_state(P, st) : launch_simt_seg_state(P, s->dtype, st));
+  P.features_in = 0;
   HLA_LAUNCH(tr.mark());
   if (!fwd_ws) HLA_LAUNCH(launch_state_scan(P, false, st));
   HLA_LAUNCH(tr.mark());
@@ -431,6 +523,73 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
   HLA_LAUNCH(tr.mark());
   HLA_LAUNCH(tc ? launch_tc_bwd_dkdv(P, st) : launch_simt_bwd_dkdv(P, s->dtype, st));
   HLA_LAUNCH(tr.mark());
+  return HLA_OK;
+}
+
+size_t hla_project_workspace_size(void) { return kStatusBytes; }
+
+hla_status hla_project_in(const hla_shape *s, int32_t d_model, const void *x, const void *w_qkvz,
+                          void *features, void *v, void *gate, void *ws, size_t ws_bytes,
+                          hla_stream stream) {
+  HLA_TRY(check_shape(s, false));
+  if (d_model < 1) return HLA_ERR_INVALID_ARG;
+  if (!can_save(*s) || d_model % 64) return HLA_ERR_UNSUPPORTED;
+  const long long M = (long long)s->B * s->T;
+  if (M > 0x7fffffffLL) return HLA_ERR_UNSUPPORTED;
+  const bool empty = M == 0;
+  HLA_TRY(need_unless(empty, x));
+  HLA_TRY(need_unless(empty, w_qkvz));
+  HLA_TRY(need_unless(empty, features));
+  HLA_TRY(need_unless(empty, v));
+  HLA_TRY(need_unless(empty, gate));
+  if (!ws || !aligned16(ws) || ws_bytes < kStatusBytes) return HLA_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  unsigned int *err = (unsigned int *)ws;
+  HLA_LAUNCH(cudaMemsetAsync(err, 0, sizeof(unsigned int), st));
+  if (empty) return HLA_OK;
+  ProjParams P;
+  memset(&P, 0, sizeof(P));
+  P.M = (int)M;
+  P.N = 4 * s->H * s->dk;
+  P.K = d_model;
+  P.T = s->T;
+  P.H = s->H;
+  P.pos_offset = s->pos_offset;
+  P.eps = s->norm_eps;
+  P.kscale = (float)(1.0 / sqrt((double)s->dk));
+  unsigned char *f = (unsigned char *)features;
+  P.qt = f;
+  P.kt = f + saved_k_offset(s->B, s->T, s->H, s->dk);
+  P.scal = (float *)(f + saved_scalar_offset(s->B, s->T, s->H, s->dk));
+  P.v = v;
+  P.g = gate;
+  P.err = err;
+  fill_rope_u(P.rope_u, s->dk, s->rope_base);
+  HLA_LAUNCH(launch_proj_in(P, x, w_qkvz, st));
+  return HLA_OK;
+}
+
+hla_status hla_project_out(int64_t M, int32_t n_in, int32_t d_model, const void *u, const void *w_o,
+                           void *out, void *ws, size_t ws_bytes, hla_stream stream) {
+  if (M < 0 || n_in < 1 || d_model < 1) return HLA_ERR_INVALID_ARG;
+  if (M > 0x7fffffffLL || n_in % 64 || d_model % 128) return HLA_ERR_UNSUPPORTED;
+  const bool empty = M == 0;
+  HLA_TRY(need_unless(empty, u));
+  HLA_TRY(need_unless(empty, w_o));
+  HLA_TRY(need_unless(empty, out));
+  if (!ws || !aligned16(ws) || ws_bytes < kStatusBytes) return HLA_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  unsigned int *err = (unsigned int *)ws;
+  HLA_LAUNCH(cudaMemsetAsync(err, 0, sizeof(unsigned int), st));
+  if (empty) return HLA_OK;
+  ProjParams P;
+  memset(&P, 0, sizeof(P));
+  P.M = (int)M;
+  P.N = d_model;
+  P.K = n_in;
+  P.out = out;
+  P.err = err;
+  HLA_LAUNCH(launch_proj_out(P, u, w_o, st));
   return HLA_OK;
 }
 

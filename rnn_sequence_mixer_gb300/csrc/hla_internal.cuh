@@ -21,8 +21,12 @@ struct MixerParams {
   int chunk;    // token tile of the chunked prefill (64 or 128)
   int nseg;     // segments per (b, h)
   int seg_len;  // tokens per segment (a multiple of chunk; the last may be short)
-  int pad0;
+  int features_in;  // tensor-core forward: q~, k~ and the q~ . k~ diagonal are read from
+                    // `saved` (hla_prefill_features) instead of computed from raw q, k
   long long pos_offset;
+  int fused;        // tensor-core forward in one launch: every output CTA forms the state
+                    // entering its segment from the decay window before it (window_tiles)
+  int pad1;
   float eps;
   float kscale;  // 1 / sqrt(D), applied to k~ after RoPE
   const void *q, *k, *v, *g;
@@ -148,6 +152,17 @@ __host__ __device__ inline long long decay_rows(float log2g) {
   return w >= 1.0995116e12f ? (1LL << 40) : (long long)w + 1;
 }
 
+// Tiles of CV tokens right before token t0 that the state entering a segment
+// at t0 needs: those holding a token with weight gamma^m, m = t0 - 1 - s, inside
+// the decay horizon (decay_rows), and none before token 0.  State_in enters
+// with gamma^t0 on top.
+__host__ __device__ inline int window_tiles(float log2g, long long t0, int CV) {
+  if (t0 <= 0) return 0;
+  const long long W = decay_rows(log2g);
+  const long long nt = (W + CV - 1) / CV;
+  return (int)(nt < t0 / CV ? nt : t0 / CV);
+}
+
 // Tiles [lo, hi) of a segment of L tokens (ntile tiles of CV) that piece p
 // covers; lo >= hi when the piece is empty.  grad: weights from the start.
 __host__ __device__ inline void piece_tiles(long long W, int L, int CV, int p, bool grad, int &lo,
@@ -208,6 +223,7 @@ size_t part_bytes(const hla_shape &s, const Plan &p);
 size_t saved_bytes(const hla_shape &s);
 int part_count(const hla_shape &s, const Plan &p);
 void fill_rope(MixerParams &P, int D, double base);
+void fill_rope_u(unsigned long long *u, int D, double base);
 
 // Kernel launchers (return the cudaError_t of the launch).
 cudaError_t launch_decode(const MixerParams &P, int dtype, cudaStream_t st);

@@ -472,6 +472,7 @@ cudaError_t make_map(CUtensorMap *map, const void *ptr, const MixerParams &P, in
                      CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   EncodeFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
+  if (!ptr) return cudaErrorInvalidValue;  // a map over no tensor would read address 0
   const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)P.H, (cuuint64_t)P.T, (cuuint64_t)P.B};
   const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)P.H * D * 2,
                                  (cuuint64_t)P.T * P.H * D * 2};

@@ -70,8 +70,9 @@ struct StateShared {
 // issues one MMA per tile as soon as the workers are done with it and refills
 // the stage once that MMA has read it, three tiles ahead.  Workers never wait
 // for the tensor core.
-// kSaved (with kGrad): tmk maps the forward's saved fp16 q~, so the workers
-// only weight it and convert it to bf16 (the MMA's type, that of do).
+// kSaved: tmk maps saved fp16 features (q~ of the forward, with kGrad; k~
+// given to hla_prefill_features, without), so the workers only weight them
+// and convert them to bf16 (the MMA's type, that of do or v).
 template <bool kGrad, bool kSaved = false>
 __global__ void __launch_bounds__(NTO, 1)
     tc_state_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmk,
@@ -168,8 +169,10 @@ __global__ void __launch_bounds__(NTO, 1)
       const int c0 = tb + n * CV, c = min(CV, t1 - c0);
       wait_or_fail(&sh.bar_tma[st], (n / kStages) & 1, failed);
       const bool valid = fr < c;
-      if (kSaved) {  // q~ (fp16) -> gamma^{s+1} q~ (bf16) in place; zeros past the tile
-        const f2 w = dup2(exp2f((float)(c0 - t0 + fr + 1) * l2g));
+      if (kSaved) {  // q~ -> gamma^{s+1} q~ or k~ -> gamma^{L-1-s} k~ (fp16 -> bf16) in
+                     // place; zeros past the tile
+        const int s_rel = c0 - t0 + fr;
+        const f2 w = dup2(exp2f((float)(kGrad ? s_rel + 1 : L - 1 - s_rel) * l2g));
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           uint4 *p = tile_at(Kt, fr, (u < 2 ? 0 : 8) + 2 * fu + (u & 1));
@@ -246,10 +249,129 @@ struct OutShared {
   uint64_t bar_pm;      // workers: Pm, scaled O and k~dec written
   uint64_t bar_epi;     // workers: y of the previous tile written over its gate tile
   uint64_t bar_sv;      // saving: the TMA stores of q~, k~ have read Q and K (issuer)
+  uint64_t bar_wtma[3];   // one launch: TMA of the (k, v) window tile in stage j
+  uint64_t bar_wfeat[3];  // one launch: workers wrote k~dec of stage j (one arrive per warp)
+  uint64_t bar_wmma[3];   // one launch: MMA of stage j done (commit)
+  uint64_t bar_wdone;     // one launch: every window MMA done (commit)
   uint32_t tmem_base;
   uint32_t failed;
 };
 
+
+// ------------------------------------------------------------------ one launch: the window phase
+// The state entering a segment, formed by its own output CTA (kWin below):
+// gamma^t0 state_in, plus S += K~dec^T V over the window_tiles() tiles before
+// t0, with three (k, v) stages in flight over the six tile buffers.  Kept out
+// of line (one call per CTA) so that the tile loop's registers are allocated
+// as in the other variants.  Both return whether a bounded wait gave up.
+
+// Issuer side: copies and one MMA per window tile into S (tS).
+__device__ __noinline__ bool window_issue(const CUtensorMap &tmk, const CUtensorMap &tmv, OutShared &sh,
+                                          unsigned char *base, uint32_t tS, int b, int h, int t0,
+                                          int CV, float l2g) {
+  bool failed = false;
+  const uint32_t tile_bytes = (uint32_t)CV * D * 2;
+  const uint32_t id_mn = umma::idesc_bf16(128, 128, true, true);  // bf16 K~dec^T V
+  const int nw = window_tiles(l2g, t0, CV), ws = t0 - nw * CV;
+  for (int w = 0; w < 3 && w < nw; ++w) {
+    umma::mbar_expect_tx(&sh.bar_wtma[w], 2 * tile_bytes);
+    tma_tile(base + 2 * w * TILE, &tmk, b, h, ws + w * CV, &sh.bar_wtma[w]);
+    tma_tile(base + (2 * w + 1) * TILE, &tmv, b, h, ws + w * CV, &sh.bar_wtma[w]);
+  }
+  for (int w = 0; w < nw; ++w) {
+    const int st = w % 3;
+    const uint32_t par = (w / 3) & 1;
+    unsigned char *Kw = base + 2 * st * TILE;
+    wait_or_fail(&sh.bar_wfeat[st], par, failed);
+    if (!failed) {
+      const uint32_t a = umma::smem_u32(Kw), bv = a + TILE;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        umma::mma_ss(tS, umma::desc_mnmajor(a, kk, ROWS), umma::desc_mnmajor(bv, kk, ROWS), id_mn, 1u);
+      umma::commit(&sh.bar_wmma[st]);
+    }
+    if (w + 3 < nw) {  // the stage takes tile w + 3 once MMA w has read it
+      wait_or_fail(&sh.bar_wmma[st], par, failed);
+      if (!failed) {
+        umma::mbar_expect_tx(&sh.bar_wtma[st], 2 * tile_bytes);
+        tma_tile(Kw, &tmk, b, h, ws + (w + 3) * CV, &sh.bar_wtma[st]);
+        tma_tile(Kw + TILE, &tmv, b, h, ws + (w + 3) * CV, &sh.bar_wtma[st]);
+      }
+    }
+  }
+  // every window MMA done before the buffers take the tile loop's copies
+  if (nw > 0 && !failed) umma::commit(&sh.bar_wdone);
+  if (nw > 0) wait_or_fail(&sh.bar_wdone, 0, failed);
+  return failed;
+}
+
+// Worker side: gamma^t0 state_in into S (TMEM), each window tile's raw k (or
+// given fp16 k~, kFeat) turned into K~dec in place with weights
+// gamma^{t0-1-s}, and, once every window MMA is done, the entering state out
+// to seg_in (row i, columns [col, col + 32)), where the backward can read it.
+template <bool kFeat>
+__device__ __noinline__ bool window_work(const MixerParams &P, OutShared &sh, unsigned char *base,
+                                         uint32_t myS, float *seg_in, int b, int h, int t0, int CV,
+                                         float l2g, int i, uint32_t col, int warp, int lane) {
+  bool failed = false;
+  const int fr = 8 * warp + (lane >> 2), fu = lane & 3;  // feature map: row, pair quarter
+  {
+    const float w0 = exp2f((float)t0 * l2g);
+    float v[32];
+    if (P.state_in && w0 > 0.f) {
+      const float4 *s4 =
+          reinterpret_cast<const float4 *>(P.state_in + (((size_t)b * P.H + h) * D + i) * D + col);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float4 x = s4[u];
+        v[4 * u] = w0 * x.x; v[4 * u + 1] = w0 * x.y; v[4 * u + 2] = w0 * x.z; v[4 * u + 3] = w0 * x.w;
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < 32; ++u) v[u] = 0.f;
+    }
+    umma::tmem_st32(myS, v);
+    umma::tmem_wait_st();
+  }
+  const int nw = window_tiles(l2g, t0, CV), ws = t0 - nw * CV;
+  const bool wvalid = fr < CV;  // window tiles are always full
+  for (int w = 0; w < nw; ++w) {
+    const int st = w % 3;
+    unsigned char *Kw = base + 2 * st * TILE;
+    wait_or_fail(&sh.bar_wtma[st], (w / 3) & 1, failed);
+    const int s_tok = ws + w * CV + fr;
+    const float wgt = wvalid ? exp2f((float)(t0 - 1 - s_tok) * l2g) : 0.f;
+    if (kFeat) {  // given k~ (fp16): weight and convert
+      const f2 wk = dup2(wgt);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        uint4 *pk = tile_at(Kw, fr, (u < 2 ? 0 : 8) + 2 * fu + (u & 1));
+        f2 f[4];
+        unpack4x2h(*pk, f);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) f[e] = mul2(f[e], wk);
+        *pk = wvalid ? pack4x2(f) : make_uint4(0, 0, 0, 0);
+      }
+    } else {
+      uint4 kr[4];
+      ld_pairs(Kw, fr, fu, kr);
+      if (!wvalid) kr[0] = kr[1] = kr[2] = kr[3] = make_uint4(0, 0, 0, 0);
+      float sk = sumsq_pairs(kr);
+      sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+      sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+      const float rk = rsqrtf(sk / (float)D + P.eps);
+      feature_store(kr, rk * P.kscale * wgt, P.pos_offset + s_tok, fu, sh.ru, Kw, fr, false);
+    }
+    warp_arrive(&sh.bar_wfeat[st], lane);
+  }
+  if (nw > 0) wait_or_fail(&sh.bar_wdone, 0, failed);
+  float v[32];
+  umma::tmem_ld2x16(myS, v);
+  float4 *o4 = reinterpret_cast<float4 *>(seg_in + (size_t)i * D + col);
+#pragma unroll
+  for (int u = 0; u < 8; ++u) o4[u] = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+  return failed;
+}
 
 // Output pass over the tiles of one segment, warp-specialized.
 //   Issuer warp (warp 16): per tile n, waits for the workers' barriers and
@@ -270,7 +392,19 @@ struct OutShared {
 // are in place the issuer stores both tiles by TMA (fp16 maps tmsq / tmsk)
 // and, when the stores have read them, lets the workers turn k~ into k~dec
 // (bar_sv); the [A]/[D] warps write 1/RMS(q), 1/RMS(k) and q~_i . k~_i.
-template <bool kSave>
+// kFeat (hla_prefill_features): tmq / tmk map given fp16 q~ and k~ (the saved
+// layout), so [A]/[D] are skipped: MMA1 waits for their copies, and the
+// diagonal warps load q~_i . k~_i from the saved scalars by cp.async into the
+// qk_diag slot only they read.
+// kWin (the prefill in one launch): the CTA forms the state entering its
+// segment itself instead of reading it from the scan: gamma^t0 state_in, plus
+// the window of window_tiles() tiles before t0, each (k, v) tile turned into
+// K~dec by the workers (weights gamma^{t0-1-s}) and accumulated into S in TMEM
+// by one MMA, through three (k, v) stages over the six tile buffers before the
+// tile loop takes them.  Tokens before the window carry weights that sum to at
+// most 2^-40 (decay_rows).  No CTA waits for another; the entering state is
+// also written to P.seg, where the backward can read it.
+template <bool kSave, bool kFeat = false, bool kWin = false>
 __global__ void __launch_bounds__(NTO, 1)
     tc_output_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmq,
                      const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -307,6 +441,12 @@ __global__ void __launch_bounds__(NTO, 1)
     umma::mbar_init(&sh.bar_sb, NWORK);
     umma::mbar_init(&sh.bar_pm, NWORK);
     umma::mbar_init(&sh.bar_epi, NWORK);
+    for (int j = 0; j < 3; ++j) {
+      umma::mbar_init(&sh.bar_wtma[j], 1);
+      umma::mbar_init(&sh.bar_wfeat[j], NWORK);
+      umma::mbar_init(&sh.bar_wmma[j], 1);
+    }
+    umma::mbar_init(&sh.bar_wdone, 1);
     umma::mbar_fence_init();
     sh.failed = 0;
   }
@@ -315,9 +455,15 @@ __global__ void __launch_bounds__(NTO, 1)
   load_rope_table(sh.ru, P, tid);
   fill_rope_small(sh.rope_small, P.rope_u, tid, NTO);
   if (warp == 0) umma::tmem_alloc(&sh.tmem_base, 512);
-  if (CV < ROWS)  // rows [CV, 128) of V are never written by TMA: clear them once
-    for (int e = tid; e < (ROWS - CV) * 16; e += NTO)
-      *tile_at(Vs, CV + e / 16, e % 16) = make_uint4(0, 0, 0, 0);
+  if (CV < ROWS) {  // rows [CV, 128) that TMA never writes and no phase rewrites: clear
+                    // them once.  V; with given features Q and both K buffers (which [D]
+                    // would have written); in one launch the window stages' V buffers.
+    const unsigned clear = (1u << 3) | (kFeat ? 7u : 0u) | (kWin ? (1u << 1) | (1u << 5) : 0u);
+    for (int e = tid; e < 6 * (ROWS - CV) * 16; e += NTO) {
+      const int t = e / ((ROWS - CV) * 16), r = e % ((ROWS - CV) * 16);
+      if (clear & (1u << t)) *tile_at(base + t * TILE, CV + r / 16, r % 16) = make_uint4(0, 0, 0, 0);
+    }
+  }
   sync_tc();
   const uint32_t tm = sh.tmem_base;
   const uint32_t tP = tm, tS = tm + 384;
@@ -330,6 +476,7 @@ __global__ void __launch_bounds__(NTO, 1)
       const uint32_t id_qs = umma::idesc_bf16(128, 128, false, true, true);   // fp16 Q~ S
       const uint32_t id_pv = umma::idesc_bf16(128, 128, false, true);         // bf16 Pm V
       const uint32_t id_mn = umma::idesc_bf16(128, 128, true, true);          // bf16 K~dec^T V
+      if (kWin) failed = window_issue(tmk, tmv, sh, base, tS, b, h, t0, CV, l2g);
       umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
       tma_tile(Qs, &tmq, b, h, t0, &sh.bar_q);
       for (int n = 0; n < 2 && n < ntile; ++n) {
@@ -347,7 +494,12 @@ __global__ void __launch_bounds__(NTO, 1)
         const uint32_t ak = umma::smem_u32(base + (1 + buf) * TILE);
         const uint32_t as = umma::smem_u32(SP), av = umma::smem_u32(Vs);
         const uint32_t ocur = tm + 128 + 128 * buf;
-        wait_or_fail(&sh.bar_feat, n & 1, failed);
+        if (kFeat) {  // q~, k~ given: MMA1 once their copies are in
+          wait_or_fail(&sh.bar_q, n & 1, failed);
+          wait_or_fail(&sh.bar_k[buf], (n >> 1) & 1, failed);
+        } else {
+          wait_or_fail(&sh.bar_feat, n & 1, failed);
+        }
         if (!failed) {
           if (kSave) {  // q~, k~ of the tile out for the backward
             tma_store_tile(&tmsq, Qs, b, h, c0);
@@ -435,10 +587,10 @@ __global__ void __launch_bounds__(NTO, 1)
     const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
     const uint32_t col = 32 * qd;
     const uint32_t myS = tS + lane_base + col, myP = tP + lane_base + col;
-    // entering state of the segment -> TMEM (fp32)
-    {
-      const float *sin_ = P.seg + (((size_t)b * P.H + h) * P.nseg + g) * (size_t)D * D;
-      const float4 *s4 = reinterpret_cast<const float4 *>(sin_ + (size_t)i * D + col);
+    float *seg_in = P.seg + (((size_t)b * P.H + h) * P.nseg + g) * (size_t)D * D;
+    if (!kWin) {
+      // entering state of the segment (from the scan) -> TMEM (fp32)
+      const float4 *s4 = reinterpret_cast<const float4 *>(seg_in + (size_t)i * D + col);
       float v[32];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -447,6 +599,8 @@ __global__ void __launch_bounds__(NTO, 1)
       }
       umma::tmem_st32(myS, v);
       umma::tmem_wait_st();
+    } else {
+      failed = window_work<kFeat>(P, sh, base, myS, seg_in, b, h, t0, CV, l2g, i, col, warp, lane);
     }
     int prev_c0 = 0, prev_c = 0;
     for (int n = 0; n <= ntile; ++n) {
@@ -457,7 +611,15 @@ __global__ void __launch_bounds__(NTO, 1)
       const uint32_t ocur = tm + 128 + 128 * buf;        // O buffer of tile n
       const uint32_t oprev = tm + 128 + 128 * (buf ^ 1); // O buffer of tile n - 1
       unsigned char *Qt = Qs, *Kt = base + (1 + buf) * TILE;
-      if (have) {
+      if (have && kFeat) {
+        // q~ . k~ of row i from the given scalars, into the slot only this
+        // thread reads (in [F], on the diagonal warps)
+        if (qd == sub) {
+          if (valid) cp_async4(&sh.qk_diag[buf][i], saved_scalar(P, kSavedDiag, b, h, c0 + i));
+          else sh.qk_diag[buf][i] = 0.f;
+        }
+      }
+      if (have && !kFeat) {
         // this warp's RoPE angles at row 8 warp of the tile (its rows are 8 warp + 0..7),
         // two per lane, into its own table (rope8_tab)
         __syncwarp();
@@ -562,13 +724,15 @@ __global__ void __launch_bounds__(NTO, 1)
           }
           // MMA2 of tile n done: Sb is dead and the Q~ S part of O is ready
           wait_or_fail(&sh.bar_mma[0], n & 1, failed);
+          if (kFeat) cp_async_wait();
 #pragma unroll
           for (int u = 0; u < 4; ++u) *tile_at(SP, i, 4 * qd + u) = pack4x2(&x[4 * u]);
           // the diagonal of Pm from fp32 features: where q~_i . k~_i nearly
           // cancels (a row whose output is almost only its own term: t = 0, or
           // gamma near 0) the fp16 operands of MMA1 lose it; its weight is
           // gamma^0 = 1.  Rows 32 qd .. 32 qd + 31 of qk_diag were written by
-          // warps 4 qd .. 4 qd + 3, which met this warp at [B]'s barrier.
+          // warps 4 qd .. 4 qd + 3, which met this warp at [B]'s barrier
+          // (given features: by this thread's own copy).
           if (qd == sub)
             *(reinterpret_cast<__nv_bfloat16 *>(tile_at(SP, i, i >> 3)) + (i & 7)) =
                 __float2bfloat16_rn(sh.qk_diag[buf][i]);
@@ -688,7 +852,10 @@ cudaError_t launch_state_variant(const MixerParams &P, const void *a, const void
 }  // namespace
 
 cudaError_t launch_tc_seg_state(const MixerParams &P, cudaStream_t st) {
-  return launch_state_variant<false>(P, P.k, P.v, st);
+  // k~ from given features (hla_prefill_features) when there are some
+  return P.features_in
+             ? launch_state_variant<false, true>(P, P.saved + saved_k_offset(P.B, P.T, P.H, P.D), P.v, st)
+             : launch_state_variant<false>(P, P.k, P.v, st);
 }
 
 cudaError_t launch_tc_seg_gstate(const MixerParams &P, cudaStream_t st) {
@@ -698,12 +865,20 @@ cudaError_t launch_tc_seg_gstate(const MixerParams &P, cudaStream_t st) {
 }
 
 namespace {
-template <bool kSave>
+template <bool kSave, bool kFeat = false, bool kWin = false>
 cudaError_t launch_output_variant(const MixerParams &P, cudaStream_t st) {
   CUtensorMap mq, mk, mv, mg, my, msq, msk;
   cudaError_t e;
-  if ((e = tc::make_map(&mq, P.q, P, P.chunk)) != cudaSuccess) return e;
-  if ((e = tc::make_map(&mk, P.k, P, P.chunk)) != cudaSuccess) return e;
+  if (kFeat) {  // q~ and k~ given (fp16, the saved layout)
+    if ((e = tc::make_map(&mq, P.saved, P, P.chunk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != cudaSuccess)
+      return e;
+    if ((e = tc::make_map(&mk, P.saved + saved_k_offset(P.B, P.T, P.H, P.D), P, P.chunk,
+                          CU_TENSOR_MAP_DATA_TYPE_FLOAT16)) != cudaSuccess)
+      return e;
+  } else {
+    if ((e = tc::make_map(&mq, P.q, P, P.chunk)) != cudaSuccess) return e;
+    if ((e = tc::make_map(&mk, P.k, P, P.chunk)) != cudaSuccess) return e;
+  }
   if ((e = tc::make_map(&mv, P.v, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mg, P.g, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&my, P.y, P, P.chunk)) != cudaSuccess) return e;
@@ -717,16 +892,22 @@ cudaError_t launch_output_variant(const MixerParams &P, cudaStream_t st) {
     msq = mq;  // not read
     msk = mk;
   }
-  e = cudaFuncSetAttribute(tc::tc_output_kernel<kSave>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)tc::kOutputSmem);
+  e = cudaFuncSetAttribute(tc::tc_output_kernel<kSave, kFeat, kWin>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::kOutputSmem);
   if (e != cudaSuccess) return e;
-  tc::tc_output_kernel<kSave><<<dim3(P.nseg, P.H, P.B), tc::NTO, tc::kOutputSmem, st>>>(
+  tc::tc_output_kernel<kSave, kFeat, kWin><<<dim3(P.nseg, P.H, P.B), tc::NTO, tc::kOutputSmem, st>>>(
       P, mq, mk, mv, mg, my, msq, msk);
   return cudaGetLastError();
 }
 }  // namespace
 
 cudaError_t launch_tc_seg_output(const MixerParams &P, cudaStream_t st) {
+  if (P.fused) {
+    if (P.features_in) return launch_output_variant<false, true, true>(P, st);
+    return P.saved ? launch_output_variant<true, false, true>(P, st)
+                   : launch_output_variant<false, false, true>(P, st);
+  }
+  if (P.features_in) return launch_output_variant<false, true>(P, st);
   return P.saved ? launch_output_variant<true>(P, st) : launch_output_variant<false>(P, st);
 }
 

@@ -286,6 +286,16 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, int x, 
       : "memory");
 }
 
+// 2-D tiled TMA load of the box at (x, y) (x the contiguous coordinate, never
+// negative) into shared memory, completing its bytes on `bar`.
+__device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, int y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Prefetch of the same box into L2 (x never negative, as for the loads).
 __device__ __forceinline__ void tma_prefetch_4d(const void *tmap, int x, int y, int z, int w) {
   asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(

@@ -39,3 +39,17 @@ def decode_inputs(steps, B, H, d, dtype, seed, device="cpu"):
     step's slice is contiguous), drawn in that order."""
     gen = generator(seed, device)
     return {n: normal((steps, B, 1, H, d), dtype, gen, device) for n in ("q", "k", "v", "gate")}
+
+
+def layer_inputs(B, T, D, H, d, seed, device="cpu", with_dy=False):
+    """Inputs of one RNN layer with its projections: x [B, T, D], the input
+    weights w_qkvz [H, 4, d, D] and the output weight w_o [D, H d], all bf16,
+    drawn in that order (and dy [B, T, H, d]).  The weights are N(0, 1) / sqrt
+    of their fan-in, so the projected rows are about N(0, 1)."""
+    gen = generator(seed, device)
+    out = {"x": normal((B, T, D), torch.bfloat16, gen, device),
+           "w_qkvz": (torch.randn((H, 4, d, D), generator=gen, device=device) / D ** 0.5).to(torch.bfloat16),
+           "w_o": (torch.randn((D, H * d), generator=gen, device=device) / (H * d) ** 0.5).to(torch.bfloat16)}
+    if with_dy:
+        out["dy"] = normal((B, T, H, d), torch.bfloat16, gen, device)
+    return out

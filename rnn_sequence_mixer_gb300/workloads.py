@@ -67,3 +67,25 @@ class AttentionWorkload:
 
 ATTENTION_16K = AttentionWorkload("attention_B1_T16384_Hq16_Hkv8_d128_bf16_a500", 1, 16384, 16, 8,
                                   128, 500.0, 6)
+
+
+@dataclass(frozen=True)
+class LayerWorkload:
+    """One RNN layer with its projections (Appendix A, Eq. 18): x [B, T, D] through
+    x W_q,k,v,z (the feature map fused), the mixer from those features and the
+    output projection.  HypeNet-2B keeps Qwen3-1.7B's width D = 2048 with 16 RNN
+    heads of dim 128."""
+    name: str
+    B: int
+    T: int
+    D: int
+    H: int
+    d: int
+    chunk: int
+    rope_base: float
+    seed: int
+    eps: float = 1e-6
+
+
+LAYER_16K = LayerWorkload("rnn_layer_B1_T16384_D2048_H16_d128_bf16", 1, 16384, 2048, 16, 128, 128,
+                          1e6, 8)

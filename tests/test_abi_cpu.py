@@ -48,7 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.hla_abi_version() == 5
+    assert lib.hla_abi_version() == 6
     for code in range(6):
         assert _lib.status_string(code).startswith("HLA_")
     assert "UNKNOWN" in _lib.status_string(99)
@@ -290,3 +290,55 @@ def test_attention_workspace_and_argument_checks(lib):
     assert call_attention(lib, s, o=FAKE + 4) == _lib.HLA_ERR_INVALID_ARG
     assert call_attention(lib, s, ws=None) == _lib.HLA_ERR_WORKSPACE
     assert call_attention(lib, s, ws_bytes=255) == _lib.HLA_ERR_WORKSPACE
+
+
+def test_projection_and_feature_entry_points_reject_bad_arguments(lib):
+    """hla_project_in / hla_project_out / hla_prefill_features validate before
+    touching the GPU (the fake addresses are never used)."""
+    ws = api.project_workspace_size()
+    assert ws == 256
+    s = shape(B=1, T=128, H=2, d=128)
+    pin = lambda s, d_model=256, x=FAKE, w=FAKE, f=FAKE, ws_bytes=ws: lib.hla_project_in(
+        ctypes.byref(s), d_model, x, w, f, FAKE, FAKE, FAKE, ws_bytes, None)
+    assert pin(s, d_model=0) == _lib.HLA_ERR_INVALID_ARG
+    assert pin(s, d_model=96) == _lib.HLA_ERR_UNSUPPORTED       # not a multiple of 64
+    assert pin(shape(d=64)) == _lib.HLA_ERR_UNSUPPORTED          # tensor cores: d = 128 only
+    assert pin(shape(d=128, dtype=torch.float32)) == _lib.HLA_ERR_UNSUPPORTED
+    assert pin(s, x=None) == _lib.HLA_ERR_INVALID_ARG
+    assert pin(s, w=FAKE + 8) == _lib.HLA_ERR_INVALID_ARG
+    assert pin(s, f=FAKE + 4) == _lib.HLA_ERR_INVALID_ARG
+    assert pin(s, ws_bytes=255) == _lib.HLA_ERR_WORKSPACE
+    pout = lambda M=100, n_in=256, D=256, u=FAKE, ws_bytes=ws: lib.hla_project_out(
+        M, n_in, D, u, FAKE, FAKE, FAKE, ws_bytes, None)
+    assert pout(M=-1) == _lib.HLA_ERR_INVALID_ARG
+    assert pout(n_in=0) == _lib.HLA_ERR_INVALID_ARG
+    assert pout(n_in=100) == _lib.HLA_ERR_UNSUPPORTED
+    assert pout(D=192) == _lib.HLA_ERR_UNSUPPORTED
+    assert pout(u=FAKE + 2) == _lib.HLA_ERR_INVALID_ARG
+    assert pout(ws_bytes=0) == _lib.HLA_ERR_WORKSPACE
+    gp, keep = _gamma(2)
+    pf = lambda s, f=FAKE, ws_bytes=1 << 40: lib.hla_prefill_features(
+        ctypes.byref(s), f, FAKE, FAKE, gp, None, None, FAKE, None, FAKE, ws_bytes, None, None)
+    assert pf(s, f=None) == _lib.HLA_ERR_INVALID_ARG
+    assert pf(s, f=FAKE + 4) == _lib.HLA_ERR_INVALID_ARG
+    assert pf(shape(d=64)) == _lib.HLA_ERR_UNSUPPORTED
+    assert pf(s, ws_bytes=16) == _lib.HLA_ERR_WORKSPACE
+
+
+def test_launch_counts():
+    """The library's choice is three passes (one launch on request)."""
+    g16 = api.gamma_schedule(16)
+    big = api.make_shape(1, 524288, 16, 128, chunk=128)
+    assert api.prefill_launches(big, g16) == 4  # local-state pass, its piece sums, scan, outputs
+    assert api.prefill_launches(api.make_shape(1, 524288, 16, 128, chunk=128, passes=1), g16) == 1
+    assert api.prefill_launches(api.make_shape(1, 524288, 16, 128, chunk=128, passes=3), g16) >= 3
+    short = api.make_shape(1, 16384, 16, 128, chunk=64)
+    assert api.prefill_launches(short, g16) >= 2
+    assert api.prefill_launches(api.make_shape(1, 16384, 16, 128, chunk=64, passes=1), g16) == 1
+    assert api.prefill_launches(api.make_shape(1, 100, 2, 64, chunk=64, dtype=torch.float32),
+                                api.gamma_schedule(2)) == 3
+    assert api.prefill_launches(api.make_shape(0, 100, 2, 128, chunk=64), api.gamma_schedule(2)) == 0
+    # bad arguments
+    assert api.prefill_launches(api.make_shape(1, 100, 2, 96, chunk=64), api.gamma_schedule(2)) == -1
+    assert api.prefill_launches(api.make_shape(1, 100, 2, 128, chunk=64, passes=2),
+                                api.gamma_schedule(2)) == -1
