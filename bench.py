@@ -44,6 +44,8 @@ def parse():
     p.add_argument("--no-backward", action="store_true")
     p.add_argument("--no-mma-bench", action="store_true")
     p.add_argument("--no-attention", action="store_true")
+    p.add_argument("--no-layer", action="store_true",
+                   help="skip the RNN layer with its projections (hla_project_in / _out)")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle sample")
     p.add_argument("--prefill-T", type=int, default=0,
@@ -78,25 +80,13 @@ def measured_traffic(record: str, sources, units: float):
     return float(m_b.group(1)) * units
 
 
-def tc_launches(B: int, T: int, H: int, chunk: int, grad: bool = False) -> int:
-    """Kernels one tensor-core prefill (or backward) call launches: the library's
-    segment plan (waves x (tiles per segment + 2) over 152 SMs) decides whether
-    the local-state pass runs (more than one segment) and whether its pieces
-    of at most 48 tiles need the extra sum kernel."""
-    nchunk, units = -(-T // chunk), B * H
-    max_seg = min(nchunk, max(1, -(-16 * 152 // units)))
-    best = None
-    for nseg in range(1, max_seg + 1):
-        cps = -(-nchunk // nseg)
-        if -(-nchunk // cps) != nseg:
-            continue
-        cost = -(-(units * nseg) // 152) * (cps + 2)
-        if best is None or cost < best[0]:
-            best = (cost, cps)
-    cps = best[1]
-    nseg = -(-nchunk // cps)
-    state = 0 if nseg == 1 else (1 + (1 if -(-cps // 48) > 1 else 0))
-    return state + 3 if grad else state + 2  # + scan + output (+ dq, dk/dv)
+def prefill_launches(api, B, T, H, chunk, gamma, passes=0) -> int:
+    """Kernels one prefill call launches (the library's own plan, hla_prefill_launches)."""
+    return api.prefill_launches(api.make_shape(B, T, H, 128, chunk=chunk, passes=passes), gamma)
+
+
+def backward_launches(api, B, T, H, chunk, gamma, with_fwd_ws) -> int:
+    return api.backward_launches(api.make_shape(B, T, H, 128, chunk=chunk), gamma, with_fwd_ws)
 
 
 def peaks():
@@ -349,7 +339,7 @@ def run_ours(args):
     ws = torch.empty(api.prefill_workspace_size(api.make_shape(w.B, w.T, w.H, w.d, chunk=w.chunk)),
                      dtype=torch.uint8, device=dev)
     n_pass = 3
-    n_launch = tc_launches(w.B, w.T, w.H, w.chunk)
+    n_launch = prefill_launches(api, w.B, w.T, w.H, w.chunk, gam)
 
     def prefill_step(i, trace):
         api.prefill(inp["q"], inp["k"], inp["v"], inp["gate"], gam, chunk=w.chunk,
@@ -383,6 +373,20 @@ def run_ours(args):
             "pass_ms": dict(zip(pass_names, pass_ms)),
             "whole_call": {"alg_bytes": th * 5 * w.d * BF16, "achieved": whole,
                            "frac": whole / hbm_peak}}
+    # the same workload with each launch plan forced: one launch (every output
+    # CTA forms its entering state from the decay window) and three passes
+    # (local-state pass, scan, output pass); the headline above is the library's choice
+    plans = {"library_choice_launches": n_launch}
+    p_steps = max(3, args.steps // 2)
+    for passes, key in ((1, "one_launch_ms"), (3, "three_pass_ms")):
+        def plan_step(i, trace, passes=passes):
+            api.prefill(inp["q"], inp["k"], inp["v"], inp["gate"], gam, chunk=w.chunk,
+                        rope_base=w.rope_base, eps=w.eps, y=y, state_out=st, workspace=ws,
+                        passes=passes)
+        p_ms, _ = timed(plan_step, p_steps, args.warmup, stream, D)
+        plans[key] = D.max(p_ms)
+        launches += prefill_launches(api, w.B, w.T, w.H, w.chunk, gam, passes) * p_steps
+    roof["launch_plans"] = plans
     config = {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "d": w.d, "chunk": w.chunk,
               "rope_base": w.rope_base, "l2": "inputs larger than L2 (8 GiB resident per step)",
               "replicas": D.world}
@@ -438,7 +442,7 @@ def run_ours(args):
         # shared host link) from dominating the mean
         e_steps = max(3, min(2 * args.steps, 20))
         e_ms, e_step_ms = timed(e2e_step, e_steps, 1, stream, D, trace_count=2, step_events=True)
-        launches += tc_launches(w.B, tc, w.H, w.chunk) * n_chunk * e_steps
+        launches += prefill_launches(api, w.B, tc, w.H, w.chunk, gam) * n_chunk * e_steps
         e_ms = D.max(e_ms)
         e_step_ms = [p[0] for p in e_step_ms]
         # The host link is shared with the other GPUs of the machine: a step now
@@ -575,8 +579,8 @@ def run_ours(args):
         b_steps = max(1, min(args.steps, 5))
         b_ms, b_passes = timed(fb_step, b_steps, 1, stream, D, trace_count=11)
         # forward, then the backward without its own local-state pass and scan (fwd_ws)
-        launches += (tc_launches(wb.B, wb.T, wb.H, wb.chunk) +
-                     tc_launches(wb.B, wb.T, wb.H, wb.chunk, grad=True)) * b_steps
+        launches += (prefill_launches(api, wb.B, wb.T, wb.H, wb.chunk, gb) +
+                     backward_launches(api, wb.B, wb.T, wb.H, wb.chunk, gb, True)) * b_steps
         b_ms = D.max(b_ms)
         b_names = ["fwd.seg_state", "fwd.state_scan", "fwd.seg_output", None, None, None,
                    "bwd.dq", "bwd.seg_gstate", "bwd.grad_scan", "bwd.dkdv"]
@@ -631,6 +635,68 @@ def run_ours(args):
                                          "frac": tf / tc_peak, "alg_flops": flops_a,
                                          "peak_source": f"bf16_tflops of {peak_src}"}}
         del xa, kva, ya, wsa
+        torch.cuda.empty_cache()
+
+    # ---------------------------------------------------------------- RNN layer with projections
+    # x [B, T, D] -> hla_project_in (x W_q,k,v,z, the feature map in the GEMM
+    # epilogue) -> hla_prefill_features -> hla_project_out (W_o): HypeNet-2B's
+    # RNN layer at 16K tokens.  The GEMMs are tensor-bound (2 M D 4 H d and
+    # 2 M H d D FLOPs); the mixer between them is HBM-bound (1280 B per token-head).
+    if not args.no_layer:
+        wl = workloads.LAYER_16K
+        li = inputs.layer_inputs(wl.B, wl.T, wl.D, wl.H, wl.d, wl.seed + 1000 * D.rank, device=dev)
+        gl = api.gamma_schedule(wl.H)
+        shp_l = api.make_shape(wl.B, wl.T, wl.H, wl.d, chunk=wl.chunk, rope_base=wl.rope_base)
+        feat = torch.empty(api.saved_bytes(shp_l), dtype=torch.uint8, device=dev)
+        vl = torch.empty((wl.B, wl.T, wl.H, wl.d), dtype=torch.bfloat16, device=dev)
+        gatel = torch.empty_like(vl)
+        yl = torch.empty_like(vl)
+        outl = torch.empty((wl.B, wl.T, wl.D), dtype=torch.bfloat16, device=dev)
+        wsl = torch.empty(api.prefill_workspace_size(shp_l), dtype=torch.uint8, device=dev)
+        wsp = torch.empty(api.project_workspace_size(), dtype=torch.uint8, device=dev)
+
+        def l_in(i, trace):
+            api.project_in(li["x"], li["w_qkvz"], rope_base=wl.rope_base, eps=wl.eps, chunk=wl.chunk,
+                           features=feat, v=vl, gate=gatel, workspace=wsp)
+
+        def l_mix(i, trace):
+            api.prefill_features(feat, vl, gatel, gl, chunk=wl.chunk, rope_base=wl.rope_base,
+                                 eps=wl.eps, y=yl, want_state=False, workspace=wsl)
+
+        def l_out(i, trace):
+            api.project_out(yl, li["w_o"], out=outl, workspace=wsp)
+
+        def l_all(i, trace):
+            l_in(i, trace)
+            l_mix(i, trace)
+            l_out(i, trace)
+
+        lm = {}
+        for key, fn in (("project_in", l_in), ("prefill_features", l_mix), ("project_out", l_out),
+                        ("layer", l_all)):
+            t_ms, _ = timed(fn, args.steps, args.warmup, stream, D)
+            lm[key] = D.max(t_ms)
+        n_mix = prefill_launches(api, wl.B, wl.T, wl.H, wl.chunk, gl)
+        launches += args.steps * (1 + n_mix + 1) * 2
+        M = wl.B * wl.T
+        f_in, f_out = 2.0 * M * wl.D * 4 * wl.H * wl.d, 2.0 * M * wl.H * wl.d * wl.D
+        tf_in, tf_out = f_in / (lm["project_in"] / 1e3) / 1e12, f_out / (lm["project_out"] / 1e3) / 1e12
+        mix_bytes = M * wl.H * 5 * wl.d * BF16
+        out["layer"] = {
+            "workload": wl.name, "ms_per_step": lm["layer"],
+            "Mtok_s": job_rate(M, lm["layer"], D.world) / 1e6, "pass_ms": lm,
+            "project_in": {"bound": "tensor", "achieved": tf_in, "peak": tc_peak, "unit": "TFLOP/s",
+                           "frac": tf_in / tc_peak, "alg_flops": f_in,
+                           "peak_source": f"bf16_tflops of {peak_src}"},
+            "project_out": {"bound": "tensor", "achieved": tf_out, "peak": tc_peak, "unit": "TFLOP/s",
+                            "frac": tf_out / tc_peak, "alg_flops": f_out,
+                            "peak_source": f"bf16_tflops of {peak_src}"},
+            "prefill_features": {"bound": "hbm", "alg_bytes": mix_bytes,
+                                 "achieved": mix_bytes / (lm["prefill_features"] / 1e3) / 1e9,
+                                 "peak": hbm_peak, "unit": "GB/s",
+                                 "frac": mix_bytes / (lm["prefill_features"] / 1e3) / 1e9 / hbm_peak,
+                                 "launches": n_mix}}
+        del li, feat, vl, gatel, yl, outl, wsl, wsp
         torch.cuda.empty_cache()
 
     # ---------------------------------------------------------------- MMA ceiling
