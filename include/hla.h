@@ -66,7 +66,7 @@ typedef enum {
   HLA_ERR_UNSUPPORTED = 2, /* valid but not implemented here (d, chunk, dtype, H range)      */
   HLA_ERR_WORKSPACE = 3,   /* workspace pointer NULL or ws_bytes below the required size     */
   HLA_ERR_CUDA = 4,        /* the CUDA runtime rejected a launch or an attribute call        */
-  HLA_ERR_TIMEOUT = 5      /* reserved: a bounded device-side wait gave up                   */
+  HLA_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (read from the status word) */
 } hla_status;
 
 typedef enum { HLA_F32 = 0, HLA_BF16 = 1 } hla_dtype;
@@ -100,11 +100,21 @@ typedef void *hla_stream; /* a cudaStream_t */
  * i < count.  Elapsed times between consecutive events are the device times
  * of the individual passes.  The library creates, destroys and synchronizes
  * nothing.
+ *
+ * test_wait_cycles exercises the bounded waits (testing only; 0 in normal
+ * use): when > 0, the first wait of every output-pass CTA of a tensor-core
+ * hla_prefill (the issuing thread waiting for the workers' feature map of
+ * the first tile) gives up after that many SM clock cycles.  The CTA then
+ * issues nothing more, lets every copy and MMA it issued complete, runs its
+ * remaining waits out on their normal budget and leaves; the call's status
+ * word reads non-zero (HLA_ERR_TIMEOUT) and its outputs are not valid.  The
+ * device and the stream stay usable.
  */
 #define HLA_TRACE_MAX 16
 typedef struct {
   void *events[HLA_TRACE_MAX];
   int32_t count;
+  int64_t test_wait_cycles;
 } hla_trace;
 
 /* ABI version of the loaded library (HLA_ABI_VERSION). */

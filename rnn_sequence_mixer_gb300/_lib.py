@@ -76,7 +76,8 @@ HLA_TRACE_MAX = 16
 
 
 class HlaTrace(ctypes.Structure):
-    _fields_ = [("events", ctypes.c_void_p * HLA_TRACE_MAX), ("count", ctypes.c_int32)]
+    _fields_ = [("events", ctypes.c_void_p * HLA_TRACE_MAX), ("count", ctypes.c_int32),
+                ("test_wait_cycles", ctypes.c_int64)]
 
 
 class HlaError(RuntimeError):

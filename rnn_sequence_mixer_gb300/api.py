@@ -74,6 +74,14 @@ def prefill_workspace_size(shape: _lib.HlaShape) -> int:
     return int(_lib.load().hla_prefill_workspace_size(ctypes.byref(shape)))
 
 
+def workspace_status(workspace: torch.Tensor) -> int:
+    """The status of a finished call from its workspace's status word (the
+    first uint32 of its last 256 bytes; the caller synchronizes first):
+    HLA_OK, or HLA_ERR_TIMEOUT when a bounded device-side wait gave up."""
+    word = int(workspace[-256:-252].cpu().view(torch.int32).item())
+    return _lib.HLA_OK if word == 0 else _lib.HLA_ERR_TIMEOUT
+
+
 def prefill_launches(shape: _lib.HlaShape, gamma) -> int:
     """hla_prefill_launches: kernels one prefill call with this shape launches."""
     g_host, g_ptr = _host_gamma(gamma, shape.H)
@@ -110,8 +118,16 @@ def _stream(device) -> ctypes.c_void_p:
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
-def _trace(events, device):
-    """hla_trace from a list of torch.cuda.Event (None = no tracing)."""
+def _trace(events, device, test_wait_cycles=0):
+    """hla_trace from a list of torch.cuda.Event (None = no tracing) and the
+    testing-only wait budget (hla.h)."""
+    if test_wait_cycles:
+        tr = _lib.HlaTrace()
+        tr.count = 0
+        tr.test_wait_cycles = int(test_wait_cycles)
+        if events:
+            raise ValueError("test_wait_cycles is not combined with trace events")
+        return ctypes.byref(tr), tr
     if not events:
         return None
     if len(events) > _lib.HLA_TRACE_MAX:
@@ -128,7 +144,8 @@ def _trace(events, device):
 
 def prefill(q, k, v, gate, gamma: Sequence[float] | torch.Tensor, state_in=None, *, chunk=64,
             pos_offset=0, rope_base=1e4, eps=1e-6, want_o=False, want_state=True, y=None,
-            state_out=None, workspace=None, trace=None, saved=None, passes=0):
+            state_out=None, workspace=None, trace=None, saved=None, passes=0,
+            test_wait_cycles=0):
     """hla_prefill.  Returns (y, o or None, state_out or None).  ``trace``: optional
     list of torch.cuda.Event recorded before each pass and after the last.
     ``saved``: optional uint8 CUDA tensor of ``saved_bytes(shape)`` bytes that
@@ -153,7 +170,7 @@ def prefill(q, k, v, gate, gamma: Sequence[float] | torch.Tensor, state_in=None,
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
     _check_saved(saved, shape)
-    tr = _trace(trace, q.device)
+    tr = _trace(trace, q.device, test_wait_cycles)
     st = lib.hla_prefill(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(gate), g_ptr,
                          _ptr(state_in), _ptr(state_out), _ptr(y), _ptr(o), _ptr(workspace),
                          workspace.numel(), _stream(q.device), tr[0] if tr else None,

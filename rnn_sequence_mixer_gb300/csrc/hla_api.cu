@@ -115,7 +115,8 @@ struct Tracer {
 };
 
 hla_status check_trace(const hla_trace *t) {
-  if (t && (t->count < 0 || t->count > HLA_TRACE_MAX)) return HLA_ERR_INVALID_ARG;
+  if (t && (t->count < 0 || t->count > HLA_TRACE_MAX || t->test_wait_cycles < 0))
+    return HLA_ERR_INVALID_ARG;
   return HLA_OK;
 }
 
@@ -354,6 +355,7 @@ hla_status prefill_impl(const hla_shape *s, const void *q, const void *k, const 
     P.features_in = 1;
     P.saved = (unsigned char *)const_cast<void *>(features);
   }
+  if (trace && trace->test_wait_cycles > 0) P.test_wait_cycles = trace->test_wait_cycles;
   cudaStream_t st = (cudaStream_t)stream;
   const bool tc = tc_supported(P, s->dtype);
   Tracer tr{trace, st};

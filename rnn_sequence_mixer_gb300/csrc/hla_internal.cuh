@@ -27,6 +27,8 @@ struct MixerParams {
   int fused;        // tensor-core forward in one launch: every output CTA forms the state
                     // entering its segment from the decay window before it (window_tiles)
   int pad1;
+  long long test_wait_cycles;  // > 0: testing the expiry path (hla_trace); the budget of the
+                               // output pass's first wait for a tile's feature map
   float eps;
   float kscale;  // 1 / sqrt(D), applied to k~ after RoPE
   const void *q, *k, *v, *g;

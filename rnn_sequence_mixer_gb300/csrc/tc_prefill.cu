@@ -253,6 +253,7 @@ struct OutShared {
   uint64_t bar_wfeat[3];  // one launch: workers wrote k~dec of stage j (one arrive per warp)
   uint64_t bar_wmma[3];   // one launch: MMA of stage j done (commit)
   uint64_t bar_wdone;     // one launch: every window MMA done (commit)
+  uint64_t bar_drain;     // after a wait gave up: every MMA the issuer issued is done (commit)
   uint32_t tmem_base;
   uint32_t failed;
 };
@@ -273,10 +274,12 @@ __device__ __noinline__ bool window_issue(const CUtensorMap &tmk, const CUtensor
   const uint32_t tile_bytes = (uint32_t)CV * D * 2;
   const uint32_t id_mn = umma::idesc_bf16(128, 128, true, true);  // bf16 K~dec^T V
   const int nw = window_tiles(l2g, t0, CV), ws = t0 - nw * CV;
+  int armed[3] = {0, 0, 0};  // copies issued per stage (each stage has at most one in flight)
   for (int w = 0; w < 3 && w < nw; ++w) {
     umma::mbar_expect_tx(&sh.bar_wtma[w], 2 * tile_bytes);
     tma_tile(base + 2 * w * TILE, &tmk, b, h, ws + w * CV, &sh.bar_wtma[w]);
     tma_tile(base + (2 * w + 1) * TILE, &tmv, b, h, ws + w * CV, &sh.bar_wtma[w]);
+    ++armed[w];
   }
   for (int w = 0; w < nw; ++w) {
     const int st = w % 3;
@@ -296,12 +299,22 @@ __device__ __noinline__ bool window_issue(const CUtensorMap &tmk, const CUtensor
         umma::mbar_expect_tx(&sh.bar_wtma[st], 2 * tile_bytes);
         tma_tile(Kw, &tmk, b, h, ws + (w + 3) * CV, &sh.bar_wtma[st]);
         tma_tile(Kw + TILE, &tmv, b, h, ws + (w + 3) * CV, &sh.bar_wtma[st]);
+        ++armed[st];
       }
     }
   }
-  // every window MMA done before the buffers take the tile loop's copies
-  if (nw > 0 && !failed) umma::commit(&sh.bar_wdone);
-  if (nw > 0) wait_or_fail(&sh.bar_wdone, 0, failed);
+  if (nw > 0) {
+    // every window MMA done before the buffers take the tile loop's copies (the
+    // commit covers whatever was issued, also after a wait gave up)
+    umma::commit(&sh.bar_wdone);
+    if (!umma::mbar_wait(&sh.bar_wdone, 0)) failed = true;
+    umma::fence_after();
+    // after a wait gave up, every copy issued lands before anything else
+    // reuses the stage buffers (the normal budget; copies complete on their own)
+    if (failed)
+      for (int st = 0; st < 3; ++st)
+        if (armed[st]) umma::mbar_wait(&sh.bar_wtma[st], (armed[st] - 1) & 1);
+  }
   return failed;
 }
 
@@ -447,6 +460,7 @@ __global__ void __launch_bounds__(NTO, 1)
       umma::mbar_init(&sh.bar_wmma[j], 1);
     }
     umma::mbar_init(&sh.bar_wdone, 1);
+    umma::mbar_init(&sh.bar_drain, 1);
     umma::mbar_fence_init();
     sh.failed = 0;
   }
@@ -477,16 +491,23 @@ __global__ void __launch_bounds__(NTO, 1)
       const uint32_t id_pv = umma::idesc_bf16(128, 128, false, true);         // bf16 Pm V
       const uint32_t id_mn = umma::idesc_bf16(128, 128, true, true);          // bf16 K~dec^T V
       if (kWin) failed = window_issue(tmk, tmv, sh, base, tS, b, h, t0, CV, l2g);
+      // copies issued per barrier: after a wait gave up, the drain below waits
+      // for the last of each (no barrier ever has two copies in flight)
+      int armed_q = 0, armed_k[2] = {0, 0}, armed_v = 0, armed_g = 0;
       umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
       tma_tile(Qs, &tmq, b, h, t0, &sh.bar_q);
+      ++armed_q;
       for (int n = 0; n < 2 && n < ntile; ++n) {
         umma::mbar_expect_tx(&sh.bar_k[n], tile_bytes);
         tma_tile(base + (1 + n) * TILE, &tmk, b, h, t0 + n * CV, &sh.bar_k[n]);
+        ++armed_k[n];
       }
       umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
       tma_tile(Vs, &tmv, b, h, t0, &sh.bar_v);
+      ++armed_v;
       umma::mbar_expect_tx(&sh.bar_g, tile_bytes);
       tma_tile(Gs, &tmg, b, h, t0, &sh.bar_g);
+      ++armed_g;
       const uint32_t aq = umma::smem_u32(Qs);
       for (int n = 0; n < ntile; ++n) {
         const int buf = n & 1;
@@ -498,7 +519,12 @@ __global__ void __launch_bounds__(NTO, 1)
           wait_or_fail(&sh.bar_q, n & 1, failed);
           wait_or_fail(&sh.bar_k[buf], (n >> 1) & 1, failed);
         } else {
-          wait_or_fail(&sh.bar_feat, n & 1, failed);
+          if (n == 0 && P.test_wait_cycles > 0) {  // testing the expiry path
+            if (!failed && !umma::mbar_wait(&sh.bar_feat, 0, P.test_wait_cycles)) failed = true;
+            umma::fence_after();
+          } else {
+            wait_or_fail(&sh.bar_feat, n & 1, failed);
+          }
         }
         if (!failed) {
           if (kSave) {  // q~, k~ of the tile out for the backward
@@ -530,6 +556,7 @@ __global__ void __launch_bounds__(NTO, 1)
         if (!failed && n + 1 < ntile) {
           umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
           tma_tile(Qs, &tmq, b, h, c0 + CV, &sh.bar_q);
+          ++armed_q;
         }
         // the q tile after that into L2, so that its copy (issued one tile
         // from now, on the workers' critical path) does not wait on HBM
@@ -553,10 +580,12 @@ __global__ void __launch_bounds__(NTO, 1)
           if (n + 1 < ntile) {
             umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
             tma_tile(Vs, &tmv, b, h, c0 + CV, &sh.bar_v);
+            ++armed_v;
           }
           if (n + 2 < ntile) {
             umma::mbar_expect_tx(&sh.bar_k[buf], tile_bytes);
             tma_tile(base + (1 + buf) * TILE, &tmk, b, h, c0 + 2 * CV, &sh.bar_k[buf]);
+            ++armed_k[buf];
           }
         }
         // y of tile n - 1 is in G once the workers' epilogue (after this
@@ -569,6 +598,7 @@ __global__ void __launch_bounds__(NTO, 1)
             umma::bulk_wait_read();
             umma::mbar_expect_tx(&sh.bar_g, tile_bytes);
             tma_tile(Gs, &tmg, b, h, c0, &sh.bar_g);
+            ++armed_g;
           }
         }
       }
@@ -577,6 +607,20 @@ __global__ void __launch_bounds__(NTO, 1)
       if (!failed) {
         tma_store_tile(&tmy, Gs, b, h, t0 + (ntile - 1) * CV);
         umma::bulk_commit();
+      }
+      if (failed) {
+        // a wait gave up: before the CTA leaves (and frees its shared and tensor
+        // memory) every MMA this thread issued completes, and every copy it
+        // armed lands; those complete on their own, so the normal budget ends
+        // each wait
+        umma::commit(&sh.bar_drain);
+        umma::mbar_wait(&sh.bar_drain, 0);
+        if (armed_q) umma::mbar_wait(&sh.bar_q, (armed_q - 1) & 1);
+        for (int j = 0; j < 2; ++j)
+          if (armed_k[j]) umma::mbar_wait(&sh.bar_k[j], (armed_k[j] - 1) & 1);
+        if (armed_v) umma::mbar_wait(&sh.bar_v, (armed_v - 1) & 1);
+        if (armed_g) umma::mbar_wait(&sh.bar_g, (armed_g - 1) & 1);
+        umma::fence_after();
       }
       umma::bulk_wait_all();
     }

@@ -342,3 +342,11 @@ def test_launch_counts():
     assert api.prefill_launches(api.make_shape(1, 100, 2, 96, chunk=64), api.gamma_schedule(2)) == -1
     assert api.prefill_launches(api.make_shape(1, 100, 2, 128, chunk=64, passes=2),
                                 api.gamma_schedule(2)) == -1
+
+
+def test_trace_rejects_a_negative_test_wait_budget(lib):
+    tr = _lib.HlaTrace()
+    tr.test_wait_cycles = -1
+    s = shape()
+    assert lib.hla_prefill(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, _gamma(2)[0], None, None, FAKE,
+                           None, FAKE, 1 << 40, None, ctypes.byref(tr), None) == _lib.HLA_ERR_INVALID_ARG
