@@ -31,6 +31,8 @@ namespace hla {
 
 struct AttnParams {
   int B, T, Hq, Hkv, group, nqt;
+  int npairs;       // CTAs per (sequence, head): pairs of adjacent query tiles
+  int pad;
   long long pos_offset;
   float a;          // logit-scale base
   float inv_log2a;  // 1 / log2(a)
@@ -42,18 +44,18 @@ struct AttnParams {
 namespace tc {
 namespace {
 
+constexpr int kAttnThreads = 288;  // two softmax warpgroups + the issuer warp
+
 struct AttnShared {
-  float red_m[2][4][ROWS];  // quarter maxima of each row, by key-tile parity
-  float red_e[2][4][ROWS];  // epilogue: quarter parts of the row sum and of sum O^2
-  uint64_t bar_q, bar_g;    // TMA: q tile, gate tile
-  uint64_t bar_k[2];        // TMA: k tile into buffer 0 / 1
-  uint64_t bar_v[2];        // TMA: v tile into buffer 0 / 1
-  uint64_t bar_s[2];        // MMA1 done (S buffer 0 / 1)
-  uint64_t bar_o[2];        // MMA2 of tile j done, on barrier j & 1: the workers wait only
-                            // for some of them, and a parity wait is exact only while it
-                            // is at most one phase behind its barrier
-  uint64_t bar_p;           // workers: P written, O rescaled (one arrive per warp)
-  uint64_t bar_epi;         // workers: y written over the gate tile
+  uint64_t bar_q;     // TMA: the two q tiles
+  uint64_t bar_k[2];  // TMA: k tile into buffer 0 / 1
+  uint64_t bar_v[2];  // TMA: v tile into buffer 0 / 1
+  uint64_t bar_s[2];  // MMA1 of query tile X done (S_X written), one phase per key tile
+  uint64_t bar_p[2];  // softmax X: P_X written (one arrive per warp), one phase per key tile
+  uint64_t bar_o[2];  // MMA2 of query tile X done, one phase per key tile
+  uint64_t bar_g[2];  // TMA: gate of query tile X, into its q buffer
+  uint64_t bar_e[2];  // softmax X: y written over that gate (one arrive per warp)
+  uint64_t bar_drain; // after a wait gave up: every MMA issued is done (commit)
   uint32_t tmem_base;
   uint32_t failed;
 };
@@ -64,208 +66,264 @@ __device__ __forceinline__ float ex2_fast(float x) {
   return y;
 }
 
-__global__ void __launch_bounds__(NTO, 1)
+// 128 consecutive fp32 columns of this thread's TMEM lane under one wait.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&x)[128]) {
+  uint32_t r[8][16];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) umma::tmem_ld16_nowait(taddr + 16 * c, r[c]);
+  umma::tmem_wait_ld();
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+#pragma unroll
+    for (int e = 0; e < 16; ++e) x[16 * c + e] = __uint_as_float(r[c][e]);
+}
+
+// One CTA takes two adjacent query tiles of one head, A = 2 pr and B = 2 pr + 1
+// (B absent past the sequence), and streams their key/value tiles 0..B once
+// for both.  Tensor memory: S_A, S_B (128 columns each; P_X is written as
+// packed bf16 over the first 64 columns of S_X, MMA2's A operand) and O_A,
+// O_B.  Warps 0..3 run the softmax of A, warps 4..7 that of B, one thread per
+// score row (the row's maximum and sum stay in the thread); warp 8's first
+// lane issues every copy and MMA in the order
+//   MMA2_A(j), MMA1_A(j + 1), MMA2_B(j), MMA1_B(j + 1),
+// so that while one softmax works on its tile the tensor core runs the other
+// tile's products (an MMA1 that writes S_X right after the MMA2 that reads P_X
+// from the same columns is ordered behind it by the tensor pipe).
+__global__ void __launch_bounds__(kAttnThreads, 1)
     tc_attention_kernel(const __grid_constant__ AttnParams A, const __grid_constant__ CUtensorMap tmq,
                         const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                         const __grid_constant__ CUtensorMap tmg, const __grid_constant__ CUtensorMap tmy) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  // Q: q.  K j / V j at base + (1 + j) TILE / base + (3 + j) TILE.  G: gate -> y.
-  unsigned char *Qs = base, *Gs = base + 5 * TILE;
+  // Q X at base + X TILE (q, then the gate and y of tile X); K j at base + (2 + j) TILE;
+  // V j at base + (4 + j) TILE.
   AttnShared &sh = *reinterpret_cast<AttnShared *>(base + 6 * TILE);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int qt = A.nqt - 1 - (int)blockIdx.x;  // longest rows first
+  const int pr = A.npairs - 1 - (int)blockIdx.x;  // longest pairs first
+  const int qa = 2 * pr, qb = 2 * pr + 1;
+  const bool hasB = qb < A.nqt;
+  const int last = hasB ? qb : qa;  // key tiles 0..last (A uses 0..qa)
   const int h = blockIdx.y, b = blockIdx.z, hk = h / A.group;
-  const int q0 = qt * ROWS;
-  const int nkt = qt + 1;
   const uint32_t tile_bytes = (uint32_t)ROWS * D * 2;
 
   if (tid == 0) {
-    uint64_t *bars[] = {&sh.bar_q,    &sh.bar_g,    &sh.bar_k[0], &sh.bar_k[1], &sh.bar_v[0],
-                        &sh.bar_v[1], &sh.bar_s[0], &sh.bar_s[1], &sh.bar_o[0], &sh.bar_o[1]};
+    uint64_t *bars[] = {&sh.bar_q, &sh.bar_k[0], &sh.bar_k[1], &sh.bar_v[0], &sh.bar_v[1],
+                        &sh.bar_s[0], &sh.bar_s[1], &sh.bar_o[0], &sh.bar_o[1], &sh.bar_g[0],
+                        &sh.bar_g[1], &sh.bar_drain};
     for (uint64_t *bar : bars) umma::mbar_init(bar, 1);
-    umma::mbar_init(&sh.bar_p, NWORK);
-    umma::mbar_init(&sh.bar_epi, NWORK);
+    for (int x = 0; x < 2; ++x) {
+      umma::mbar_init(&sh.bar_p[x], 4);
+      umma::mbar_init(&sh.bar_e[x], 4);
+    }
     umma::mbar_fence_init();
     sh.failed = 0;
   }
   if (warp == 0) umma::tmem_alloc(&sh.tmem_base, 512);
   sync_tc();
   const uint32_t tm = sh.tmem_base;
-  const uint32_t tS0 = tm, tO = tm + 256;  // S buffer j at tm + 128 j
   bool failed = false;
 
-  if (warp >= NWORK) {
+  if (warp == 8) {
     // ---------------------------------------------------------------- issuer
-    if (warp == NWORK && lane == 0) {
+    if (lane == 0) {
       const uint32_t id_qk = umma::idesc_bf16(128, 128, false, false);  // Q K^T, both K-major
       const uint32_t id_pv = umma::idesc_bf16(128, 128, false, true);   // P (TMEM) V
-      const uint32_t aq = umma::smem_u32(Qs);
-      umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
-      tma_tile(Qs, &tmq, b, h, q0, &sh.bar_q);
-      umma::mbar_expect_tx(&sh.bar_g, tile_bytes);
-      tma_tile(Gs, &tmg, b, h, q0, &sh.bar_g);
-      for (int n = 0; n < 2 && n < nkt; ++n) {
+      int armed_k[2] = {0, 0}, armed_v[2] = {0, 0}, armed_g[2] = {0, 0};
+      umma::mbar_expect_tx(&sh.bar_q, (hasB ? 2 : 1) * tile_bytes);
+      tma_tile(base, &tmq, b, h, qa * ROWS, &sh.bar_q);
+      if (hasB) tma_tile(base + TILE, &tmq, b, h, qb * ROWS, &sh.bar_q);
+      for (int n = 0; n < 2 && n <= last; ++n) {
         umma::mbar_expect_tx(&sh.bar_k[n], tile_bytes);
-        tma_tile(base + (1 + n) * TILE, &tmk, b, hk, n * ROWS, &sh.bar_k[n]);
+        tma_tile(base + (2 + n) * TILE, &tmk, b, hk, n * ROWS, &sh.bar_k[n]);
+        ++armed_k[n];
         umma::mbar_expect_tx(&sh.bar_v[n], tile_bytes);
-        tma_tile(base + (3 + n) * TILE, &tmv, b, hk, n * ROWS, &sh.bar_v[n]);
+        tma_tile(base + (4 + n) * TILE, &tmv, b, hk, n * ROWS, &sh.bar_v[n]);
+        ++armed_v[n];
       }
+      // S_X = Q_X K_j^T into S_X (tm + 128 X)
+      auto mma1 = [&](int x, int j) {
+        const uint32_t aq = umma::smem_u32(base + x * TILE);
+        const uint32_t ak = umma::smem_u32(base + (2 + (j & 1)) * TILE);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma::mma_ss(tm + 128 * x, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(ak, kk, ROWS),
+                       id_qk, kk > 0);
+        umma::commit(&sh.bar_s[x]);
+      };
+      // O_X += P_X V_j, P_X from the first 64 columns of S_X
+      auto mma2 = [&](int x, int j) {
+        const uint32_t av = umma::smem_u32(base + (4 + (j & 1)) * TILE);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma::mma_ts(tm + 256 + 128 * x, tm + 128 * x + 8 * kk, umma::desc_mnmajor(av, kk, ROWS),
+                       id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        umma::commit(&sh.bar_o[x]);
+      };
       wait_or_fail(&sh.bar_q, 0, failed);
-      for (int j = 0; j <= nkt; ++j) {
-        if (j < nkt) {  // MMA1 of tile j as soon as its k has landed
-          const int buf = j & 1;
-          wait_or_fail(&sh.bar_k[buf], (j >> 1) & 1, failed);
-          if (!failed) {
-            const uint32_t ak = umma::smem_u32(base + (1 + buf) * TILE);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma::mma_ss(tS0 + 128 * buf, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(ak, kk, ROWS),
-                           id_qk, kk > 0);
-            umma::commit(&sh.bar_s[buf]);
+      wait_or_fail(&sh.bar_k[0], 0, failed);
+      if (!failed) {
+        mma1(0, 0);
+        if (hasB) mma1(1, 0);
+      }
+      for (int j = 0; j <= last; ++j) {
+        const int kb = j & 1;
+        for (int x = 0; x < 2; ++x) {
+          const int lx = x ? qb : qa;  // the tile's last key tile
+          if ((x == 1 && !hasB) || j > lx) continue;
+          wait_or_fail(&sh.bar_p[x], j & 1, failed);  // P_X(j) written (S_X read)
+          wait_or_fail(&sh.bar_v[kb], (j >> 1) & 1, failed);
+          if (!failed) mma2(x, j);
+          if (j == lx) {  // MMA1_X is done for good: Q_X takes the gate of tile X
+            if (!failed) {
+              umma::mbar_expect_tx(&sh.bar_g[x], tile_bytes);
+              tma_tile(base + x * TILE, &tmg, b, h, lx * ROWS, &sh.bar_g[x]);
+              ++armed_g[x];
+            }
+          } else {
+            wait_or_fail(&sh.bar_k[kb ^ 1], ((j + 1) >> 1) & 1, failed);
+            if (!failed) mma1(x, j + 1);
           }
         }
-        // MMA1 of tile j - 1 is done (its softmax has started or finished): that
-        // k buffer takes tile j + 1, a whole tile before MMA1 needs it
-        if (j >= 1 && j + 1 < nkt) {
-          const int pb = (j - 1) & 1;
-          wait_or_fail(&sh.bar_s[pb], ((j - 1) >> 1) & 1, failed);
+        // every MMA1 of key tile j is done (its softmax has read S): k buffer kb
+        // takes tile j + 2; once the MMA2s of key tile j are done, so does v
+        if (j + 2 <= last) {
           if (!failed) {
-            umma::mbar_expect_tx(&sh.bar_k[pb], tile_bytes);
-            tma_tile(base + (1 + pb) * TILE, &tmk, b, hk, (j + 1) * ROWS, &sh.bar_k[pb]);
+            umma::mbar_expect_tx(&sh.bar_k[kb], tile_bytes);
+            tma_tile(base + (2 + kb) * TILE, &tmk, b, hk, (j + 2) * ROWS, &sh.bar_k[kb]);
+            ++armed_k[kb];
           }
-        }
-        if (j >= 1) {  // MMA2 of tile j - 1 once its P is in place
-          const int jp = j - 1, pb = jp & 1;
-          wait_or_fail(&sh.bar_p, jp & 1, failed);
-          wait_or_fail(&sh.bar_v[pb], (jp >> 1) & 1, failed);
+          wait_or_fail(&sh.bar_o[(hasB && j <= qb) ? 1 : 0], j & 1, failed);
           if (!failed) {
-            const uint32_t av = umma::smem_u32(base + (3 + pb) * TILE);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma::mma_ts(tO, tS0 + 128 * pb + 32 * (kk >> 1) + 8 * (kk & 1),
-                           umma::desc_mnmajor(av, kk, ROWS), id_pv, (jp > 0 || kk > 0) ? 1u : 0u);
-            umma::commit(&sh.bar_o[pb]);
-          }
-          // MMA2 of tile j - 1 done: its v buffer takes tile j + 1
-          wait_or_fail(&sh.bar_o[pb], (jp >> 1) & 1, failed);
-          if (!failed && j + 1 < nkt) {
-            umma::mbar_expect_tx(&sh.bar_v[pb], tile_bytes);
-            tma_tile(base + (3 + pb) * TILE, &tmv, b, hk, (j + 1) * ROWS, &sh.bar_v[pb]);
+            umma::mbar_expect_tx(&sh.bar_v[kb], tile_bytes);
+            tma_tile(base + (4 + kb) * TILE, &tmv, b, hk, (j + 2) * ROWS, &sh.bar_v[kb]);
+            ++armed_v[kb];
           }
         }
       }
-      // y out of G
-      wait_or_fail(&sh.bar_epi, 0, failed);
-      if (!failed) {
-        tma_store_tile(&tmy, Gs, b, h, q0);
-        umma::bulk_commit();
+      // y of each tile out of its q buffer
+      for (int x = 0; x < 2; ++x) {
+        if (x == 1 && !hasB) continue;
+        wait_or_fail(&sh.bar_e[x], 0, failed);
+        if (!failed) {
+          tma_store_tile(&tmy, base + x * TILE, b, h, (x ? qb : qa) * ROWS);
+          umma::bulk_commit();
+        }
+      }
+      if (failed) {
+        // a wait gave up: every MMA issued completes and every copy armed lands
+        // before the CTA leaves (they complete on their own: normal budgets)
+        umma::commit(&sh.bar_drain);
+        umma::mbar_wait(&sh.bar_drain, 0);
+        umma::mbar_wait(&sh.bar_q, 0);
+        for (int n = 0; n < 2; ++n) {
+          if (armed_k[n]) umma::mbar_wait(&sh.bar_k[n], (armed_k[n] - 1) & 1);
+          if (armed_v[n]) umma::mbar_wait(&sh.bar_v[n], (armed_v[n] - 1) & 1);
+          if (armed_g[n]) umma::mbar_wait(&sh.bar_g[n], 0);
+        }
+        umma::fence_after();
       }
       umma::bulk_wait_all();
     }
-  } else {
-    // ---------------------------------------------------------------- workers
-    const int sub = warp & 3, qd = warp >> 2, i = 32 * sub + lane;
+  } else if (warp < 4 || hasB) {
+    // ---------------------------------------------------------------- softmax of tile X
+    const int x = warp >> 2, sub = warp & 3, i = 32 * sub + lane;  // score row = TMEM lane
+    const int qx = x ? qb : qa, q = qx * ROWS + i;
     const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
-    const uint32_t col = 32 * qd;
+    const uint32_t tS = tm + 128 * x + lane_base, tO = tm + 256 + 128 * x + lane_base;
     // c_t = s_p log2(e) / sqrt(d): logits in units of log2, for ex2
-    const float ct = log2f((float)(A.pos_offset + q0 + i) + 1.f + A.a) * A.inv_log2a *
+    const float ct = log2f((float)(A.pos_offset + q) + 1.f + A.a) * A.inv_log2a *
                      (1.4426950408889634f / 11.313708498984761f);
-    float m_run = -INFINITY, l_part = 0.f;
-    for (int j = 0; j < nkt; ++j) {
-      const int buf = j & 1;
-      const uint32_t ts = tS0 + 128 * buf + lane_base + col;
-      wait_or_fail(&sh.bar_s[buf], (j >> 1) & 1, failed);
-      float x[32];
-      umma::tmem_ld2x16(ts, x);
-      if (j == qt) {  // the diagonal tile: keys after the query are masked
+    float m_run = -INFINITY, l = 0.f;
+    for (int j = 0; j <= qx; ++j) {
+      wait_or_fail(&sh.bar_s[x], j & 1, failed);
+      float s[128];
+      tmem_ld128(tS, s);
+      if (j == qx) {  // the diagonal tile: keys after the query are masked
 #pragma unroll
-        for (int e = 0; e < 32; ++e) x[e] = (int)col + e > i ? -INFINITY : x[e];
+        for (int e = 0; e < 128; ++e) s[e] = e > i ? -INFINITY : s[e];
       }
-      float mx = x[0];
+      // the row maximum as a tree (eight independent chains, not one of 128)
+      float m8[8];
 #pragma unroll
-      for (int e = 1; e < 32; ++e) mx = fmaxf(mx, x[e]);
-      sh.red_m[j & 1][qd][i] = mx;
-      named_sync(5 + sub, 128);
-      const float mt = fmaxf(fmaxf(sh.red_m[j & 1][0][i], sh.red_m[j & 1][1][i]),
-                             fmaxf(sh.red_m[j & 1][2][i], sh.red_m[j & 1][3][i]));
+      for (int e = 0; e < 8; ++e) m8[e] = s[e];
+#pragma unroll
+      for (int e = 8; e < 128; ++e) m8[e & 7] = fmaxf(m8[e & 7], s[e]);
+      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       // The exponent's offset m moves only when the row's maximum exceeds it by
       // more than 8 (log2 units): until then p <= 2^8, which fp32 sums and bf16
       // operands hold as well as p <= 1, and the final division by the row sum
       // cancels whichever offset was used.  So O needs rescaling only on the
       // few tiles where some row of the warp moves m.
-      const float m_tile = ct * mt;  // every row has a key: finite
+      const float m_tile = ct * mx;  // every row has a key: finite
       const bool upd = m_tile > m_run + 8.f;  // always on the first tile
       const float m_new = upd ? m_tile : m_run;
       const float alpha = ex2_fast(m_run - m_new);  // 1 without a move; 0 on the first tile
-      // p = 2^(c_t x - m), two lanes per FMA; masked entries (-inf) give 0
-      uint32_t pw[16];
-      f2 s2 = 0ull;
-      {
-        const f2 c2 = dup2(ct), nm = dup2(-m_new), one = dup2(1.f);
+      // p = 2^(c_t x - m) as packed bf16 over S's first 64 columns (all of S is
+      // in registers already); masked entries (-inf) give 0
+      f2 s4[4] = {0ull, 0ull, 0ull, 0ull};  // the row sum in four independent chains
+      const f2 c2 = dup2(ct), nm = dup2(-m_new), one = dup2(1.f);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pw[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           float lo, hi;
-          split2(fma2(mk2(x[2 * e], x[2 * e + 1]), c2, nm), lo, hi);
+          split2(fma2(mk2(s[32 * c + 2 * e], s[32 * c + 2 * e + 1]), c2, nm), lo, hi);
           const f2 pp = mk2(ex2_fast(lo), ex2_fast(hi));
-          s2 = fma2(pp, one, s2);
+          s4[e & 3] = fma2(pp, one, s4[e & 3]);
           pw[e] = bf_of_f2(pp);
         }
+        umma::tmem_st16u(tS + 16 * c, pw);
       }
-      l_part = fmaf(l_part, alpha, hsum2(s2));
-      umma::tmem_st16u(ts, pw);
-      if (j > 0 && !__all_sync(0xffffffffu, !upd)) {  // O <- alpha O once MMA2 of tile j - 1 is done
-        wait_or_fail(&sh.bar_o[(j - 1) & 1], ((j - 1) >> 1) & 1, failed);
-        {
+      l = fmaf(l, alpha, hsum2(s4[0]) + hsum2(s4[1]) + (hsum2(s4[2]) + hsum2(s4[3])));
+      if (j > 0 && __any_sync(0xffffffffu, upd)) {  // O <- alpha O once MMA2_X(j - 1) is done
+        wait_or_fail(&sh.bar_o[x], (j - 1) & 1, failed);
+        const f2 al = dup2(alpha);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
           float ov[32];
-          umma::tmem_ld2x16(tO + lane_base + col, ov);
+          umma::tmem_ld2x16(tO + 32 * c, ov);
           f2 y2[16];
           pairs_of(ov, y2);
-          const f2 al = dup2(alpha);
 #pragma unroll
           for (int e = 0; e < 16; ++e) y2[e] = mul2(y2[e], al);
           floats_of(y2, ov);
-          umma::tmem_st32(tO + lane_base + col, ov);
+          umma::tmem_st32(tO + 32 * c, ov);
         }
       }
       m_run = m_new;
       umma::tmem_wait_st();
-      warp_arrive(&sh.bar_p, lane);
+      warp_arrive(&sh.bar_p[x], lane);
     }
-    // epilogue: o = O / l, y = Norm(o) sigmoid(gate) over the gate tile
-    // the last MMA2's completion covers every earlier one
-    wait_or_fail(&sh.bar_o[(nkt - 1) & 1], ((nkt - 1) >> 1) & 1, failed);
-    float ov[32];
-    umma::tmem_ld2x16(tO + lane_base + col, ov);
-    f2 o2[16];
-    pairs_of(ov, o2);
-    f2 ss = 0ull;
-#pragma unroll
-    for (int e = 0; e < 16; ++e) ss = fma2(o2[e], o2[e], ss);
-    sh.red_e[0][qd][i] = l_part;
-    sh.red_e[1][qd][i] = hsum2(ss);
-    named_sync(5 + sub, 128);
-    const float l = sh.red_e[0][0][i] + sh.red_e[0][1][i] + sh.red_e[0][2][i] + sh.red_e[0][3][i];
-    const float so = sh.red_e[1][0][i] + sh.red_e[1][1][i] + sh.red_e[1][2][i] + sh.red_e[1][3][i];
+    // epilogue: o = O / l, y = Norm(o) sigmoid(gate) over the gate tile in Q_X;
+    // the last MMA2_X's completion covers every earlier one
+    wait_or_fail(&sh.bar_o[x], qx & 1, failed);
+    float o[128];
+    tmem_ld128(tO, o);
     const float inv_l = 1.f / l;
-    const float ro = rsqrtf(so * inv_l * inv_l / (float)D + A.eps);
-    const f2 il = dup2(inv_l);
+    float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int e = 0; e < 16; ++e) o2[e] = mul2(o2[e], il);
-    const bool valid = q0 + i < A.T;
-    if (A.o && valid) {
-      float4 *o4 = reinterpret_cast<float4 *>(A.o + (((size_t)b * A.T + q0 + i) * A.Hq + h) * D + col);
-      floats_of(o2, ov);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) o4[u] = make_float4(ov[4 * u], ov[4 * u + 1], ov[4 * u + 2], ov[4 * u + 3]);
+    for (int e = 0; e < 128; ++e) {
+      o[e] *= inv_l;
+      s8[e & 7] = fmaf(o[e], o[e], s8[e & 7]);
     }
-    wait_or_fail(&sh.bar_g, 0, failed);
+    const float ss = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+    const float ro = rsqrtf(ss / (float)D + A.eps);
+    const bool valid = q < A.T;
+    if (A.o && valid) {
+      float4 *o4 = reinterpret_cast<float4 *>(A.o + (((size_t)b * A.T + q) * A.Hq + h) * D);
+#pragma unroll
+      for (int u = 0; u < 32; ++u) o4[u] = make_float4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+    }
+    wait_or_fail(&sh.bar_g[x], 0, failed);
     {
+      unsigned char *G = base + x * TILE;
       const f2 r2 = dup2(ro), half = dup2(0.5f);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        uint4 *p = tile_at(Gs, i, 4 * qd + u);
+      for (int c = 0; c < 16; ++c) {
+        uint4 *p = tile_at(G, i, c);
         f2 g[4], t[4];
         unpack4x2(*p, g);
 #pragma unroll
@@ -273,12 +331,12 @@ __global__ void __launch_bounds__(NTO, 1)
           float za, zb;  // sigmoid(z) = 0.5 + 0.5 tanh(z / 2)
           split2(mul2(g[e], half), za, zb);
           const f2 sg = fma2(mk2(tanh_fast(za), tanh_fast(zb)), half, half);
-          t[e] = mul2(mul2(o2[4 * u + e], r2), sg);
+          t[e] = mul2(mul2(mk2(o[8 * c + 2 * e], o[8 * c + 2 * e + 1]), r2), sg);
         }
         *p = pack4x2(t);
       }
     }
-    warp_arrive(&sh.bar_epi, lane);
+    warp_arrive(&sh.bar_e[x], lane);
   }
   if (failed) atomicOr(&sh.failed, 1u);
   sync_tc();
@@ -365,8 +423,9 @@ hla_status hla_attention_prefill(const hla_attn_shape *s, const void *q, const v
   if (cudaFuncSetAttribute(tc::tc_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)tc::kAttnSmem) != cudaSuccess)
     return HLA_ERR_CUDA;
-  tc::tc_attention_kernel<<<dim3(A.nqt, s->Hq, s->B), tc::NTO, tc::kAttnSmem, cs>>>(A, mq, mk, mv, mg,
-                                                                                    my);
+  A.npairs = (A.nqt + 1) / 2;
+  tc::tc_attention_kernel<<<dim3(A.npairs, s->Hq, s->B), tc::kAttnThreads, tc::kAttnSmem, cs>>>(
+      A, mq, mk, mv, mg, my);
   return cudaGetLastError() == cudaSuccess ? HLA_OK : HLA_ERR_CUDA;
 }
 
