@@ -7,23 +7,22 @@
 //   logit_ti = s_p (q_t . k_i) / sqrt(d),   s_p = log_a(p + 1 + a),   i <= t
 //   o_t = sum_i softmax_i(logit_ti) v_i,    y_t = Norm(o_t) * sigmoid(gate_t).
 //
-// One CTA per (128-query tile, query head, sequence), query tiles longest
-// first.  Per key tile j = 0 .. (the query tile's own index):
-//   MMA1  S_j = Q K_j^T            (raw bf16 q, k; fp32 in TMEM, two buffers)
-//   workers: x = S_j row, masked above the diagonal on the last tile; the
-//            row's running maximum m (shared by the row's four quarter threads
-//            through shared memory); p = 2^(c_t x - m) with c_t = s_p log2(e) /
+// One CTA per pair of adjacent 128-query tiles (query head, sequence), the
+// longest pairs first.  Per query tile X and key tile j = 0 .. X:
+//   MMA1  S_j = Q K_j^T            (raw bf16 q, k; fp32 in TMEM)
+//   softmax: one thread per score row; x = S_j row, masked above the diagonal
+//            on the last tile; p = 2^(c_t x - m) with c_t = s_p log2(e) /
 //            sqrt(d) folded into the exponent's FMA (so q is never rounded
-//            after scaling); the row sum kept as one partial per quarter; P as
-//            packed bf16 over the S columns it came from; O <- 2^(m_old -
-//            m) O in TMEM once the previous MMA2 is done (skipped where no row
-//            of the warp changed its maximum)
+//            after scaling) and an offset m that moves only when the row's
+//            maximum outgrows it; P as packed bf16 over the S columns it came
+//            from; O <- 2^(m_old - m) O in TMEM once the previous MMA2 is done
+//            (skipped where no row of the warp moved m)
 //   MMA2  O += P V_j               (A = P from tensor memory)
-// The issuer issues MMA1 of tile j + 1 before waiting for the workers' P of
-// tile j, so the QK^T product of the next tile runs under this tile's
-// softmax; k and v are double-buffered by TMA, k refilled as soon as MMA1 of
-// the tile before has read it and v once MMA2 has.  The epilogue divides by the
-// row sum, takes the output RMSNorm and the gate (tile loaded at the start)
+// MMA1 of tile j + 1 is issued right behind MMA2 of tile j, so the next QK^T
+// product runs under this tile's softmax, and the two query tiles' softmaxes
+// alternate on the tensor core.  k and v are double-buffered by TMA from a
+// warp of their own.  The epilogue divides by the row sum, takes the output
+// RMSNorm and the gate (loaded into the q buffer once its last MMA1 is done)
 // and writes y over the gate tile for a TMA store.
 #include "tc_common.cuh"
 
@@ -44,7 +43,7 @@ struct AttnParams {
 namespace tc {
 namespace {
 
-constexpr int kAttnThreads = 288;  // two softmax warpgroups + the issuer warp
+constexpr int kAttnThreads = 320;  // two softmax warpgroups, the copy warp, the MMA warp
 
 struct AttnShared {
   uint64_t bar_q;     // TMA: the two q tiles
@@ -55,6 +54,8 @@ struct AttnShared {
   uint64_t bar_o[2];  // MMA2 of query tile X done, one phase per key tile
   uint64_t bar_g[2];  // TMA: gate of query tile X, into its q buffer
   uint64_t bar_e[2];  // softmax X: y written over that gate (one arrive per warp)
+  uint64_t bar_kfree[2];  // every MMA1 reading k buffer j done (commit), one phase per tile held
+  uint64_t bar_vfree[2];  // every MMA2 reading v buffer j done (commit), one phase per tile held
   uint64_t bar_drain; // after a wait gave up: every MMA issued is done (commit)
   uint32_t tmem_base;
   uint32_t failed;
@@ -83,12 +84,15 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&x)[128]) {
 // for both.  Tensor memory: S_A, S_B (128 columns each; P_X is written as
 // packed bf16 over the first 64 columns of S_X, MMA2's A operand) and O_A,
 // O_B.  Warps 0..3 run the softmax of A, warps 4..7 that of B, one thread per
-// score row (the row's maximum and sum stay in the thread); warp 8's first
-// lane issues every copy and MMA in the order
-//   MMA2_A(j), MMA1_A(j + 1), MMA2_B(j), MMA1_B(j + 1),
-// so that while one softmax works on its tile the tensor core runs the other
-// tile's products (an MMA1 that writes S_X right after the MMA2 that reads P_X
-// from the same columns is ordered behind it by the tensor pipe).
+// score row (the row's maximum and sum stay in the thread).  Warp 9's first
+// lane issues the MMAs: it polls both tiles and, as soon as a softmax has
+// written P_X(j), issues MMA2_X(j) = O_X += P_X V_j and MMA1_X(j + 1), so that
+// while one softmax works on its tile the tensor core runs the other tile's
+// products (an MMA1 that writes S_X right after the MMA2 that reads P_X from
+// the same columns is ordered behind it by the tensor pipe).  After the last
+// MMA1 (MMA2) that reads a k (v) buffer it commits to that buffer's "free"
+// barrier, and warp 8's first lane refills the buffer with the tile two ahead
+// as soon as that barrier completes, so the copies run a whole tile ahead.
 __global__ void __launch_bounds__(kAttnThreads, 1)
     tc_attention_kernel(const __grid_constant__ AttnParams A, const __grid_constant__ CUtensorMap tmq,
                         const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -110,7 +114,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (tid == 0) {
     uint64_t *bars[] = {&sh.bar_q, &sh.bar_k[0], &sh.bar_k[1], &sh.bar_v[0], &sh.bar_v[1],
                         &sh.bar_s[0], &sh.bar_s[1], &sh.bar_o[0], &sh.bar_o[1], &sh.bar_g[0],
-                        &sh.bar_g[1], &sh.bar_drain};
+                        &sh.bar_g[1], &sh.bar_kfree[0], &sh.bar_kfree[1], &sh.bar_vfree[0],
+                        &sh.bar_vfree[1], &sh.bar_drain};
     for (uint64_t *bar : bars) umma::mbar_init(bar, 1);
     for (int x = 0; x < 2; ++x) {
       umma::mbar_init(&sh.bar_p[x], 4);
@@ -124,12 +129,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t tm = sh.tmem_base;
   bool failed = false;
 
+  // readers of key tile j: MMA1 (MMA2) of A while j <= qa, of B while j <= qb
+  auto readers = [&](int j) { return (j <= qa ? 1 : 0) + (hasB && j <= qb ? 1 : 0); };
+
   if (warp == 8) {
-    // ---------------------------------------------------------------- issuer
+    // ---------------------------------------------------------------- copies
     if (lane == 0) {
-      const uint32_t id_qk = umma::idesc_bf16(128, 128, false, false);  // Q K^T, both K-major
-      const uint32_t id_pv = umma::idesc_bf16(128, 128, false, true);   // P (TMEM) V
-      int armed_k[2] = {0, 0}, armed_v[2] = {0, 0}, armed_g[2] = {0, 0};
+      int armed_k[2] = {0, 0}, armed_v[2] = {0, 0};
       umma::mbar_expect_tx(&sh.bar_q, (hasB ? 2 : 1) * tile_bytes);
       tma_tile(base, &tmq, b, h, qa * ROWS, &sh.bar_q);
       if (hasB) tma_tile(base + TILE, &tmq, b, h, qb * ROWS, &sh.bar_q);
@@ -141,7 +147,43 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tma_tile(base + (4 + n) * TILE, &tmv, b, hk, n * ROWS, &sh.bar_v[n]);
         ++armed_v[n];
       }
-      // S_X = Q_X K_j^T into S_X (tm + 128 X)
+      // key tile j + 2 into the buffers of tile j once every MMA reading them is
+      // done (each free barrier completes one phase per tile the buffer held)
+      for (int j = 0; j + 2 <= last; ++j) {
+        const int kb = j & 1;
+        if (j + 3 <= last) tma_prefetch_tile(&tmk, b, hk, (j + 3) * ROWS);
+        wait_or_fail(&sh.bar_kfree[kb], (j >> 1) & 1, failed);
+        if (!failed) {
+          umma::mbar_expect_tx(&sh.bar_k[kb], tile_bytes);
+          tma_tile(base + (2 + kb) * TILE, &tmk, b, hk, (j + 2) * ROWS, &sh.bar_k[kb]);
+          ++armed_k[kb];
+        }
+        wait_or_fail(&sh.bar_vfree[kb], (j >> 1) & 1, failed);
+        if (!failed) {
+          umma::mbar_expect_tx(&sh.bar_v[kb], tile_bytes);
+          tma_tile(base + (4 + kb) * TILE, &tmv, b, hk, (j + 2) * ROWS, &sh.bar_v[kb]);
+          ++armed_v[kb];
+        }
+      }
+      if (failed) {
+        // a wait gave up: every copy armed lands before the CTA leaves (they
+        // complete on their own: normal budgets)
+        umma::mbar_wait(&sh.bar_q, 0);
+        for (int n = 0; n < 2; ++n) {
+          if (armed_k[n]) umma::mbar_wait(&sh.bar_k[n], (armed_k[n] - 1) & 1);
+          if (armed_v[n]) umma::mbar_wait(&sh.bar_v[n], (armed_v[n] - 1) & 1);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ---------------------------------------------------------------- MMAs
+    if (lane == 0) {
+      const uint32_t id_qk = umma::idesc_bf16(128, 128, false, false);  // Q K^T, both K-major
+      const uint32_t id_pv = umma::idesc_bf16(128, 128, false, true);   // P (TMEM) V
+      int armed_g[2] = {0, 0};
+      int kread[2] = {0, 0}, vread[2] = {0, 0};  // MMAs issued on the tile each buffer holds
+      // S_X = Q_X K_j^T into S_X (tm + 128 X); after the last reader of k buffer
+      // j & 1, its free barrier
       auto mma1 = [&](int x, int j) {
         const uint32_t aq = umma::smem_u32(base + x * TILE);
         const uint32_t ak = umma::smem_u32(base + (2 + (j & 1)) * TILE);
@@ -150,6 +192,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           umma::mma_ss(tm + 128 * x, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(ak, kk, ROWS),
                        id_qk, kk > 0);
         umma::commit(&sh.bar_s[x]);
+        if (++kread[j & 1] == readers(j)) {
+          umma::commit(&sh.bar_kfree[j & 1]);
+          kread[j & 1] = 0;
+        }
       };
       // O_X += P_X V_j, P_X from the first 64 columns of S_X
       auto mma2 = [&](int x, int j) {
@@ -159,6 +205,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           umma::mma_ts(tm + 256 + 128 * x, tm + 128 * x + 8 * kk, umma::desc_mnmajor(av, kk, ROWS),
                        id_pv, (j > 0 || kk > 0) ? 1u : 0u);
         umma::commit(&sh.bar_o[x]);
+        if (++vread[j & 1] == readers(j)) {
+          umma::commit(&sh.bar_vfree[j & 1]);
+          vread[j & 1] = 0;
+        }
       };
       wait_or_fail(&sh.bar_q, 0, failed);
       wait_or_fail(&sh.bar_k[0], 0, failed);
@@ -166,40 +216,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mma1(0, 0);
         if (hasB) mma1(1, 0);
       }
-      for (int j = 0; j <= last; ++j) {
-        const int kb = j & 1;
+      // serve whichever softmax has written its P first
+      int nxt[2] = {0, 0};
+      const int lst[2] = {qa, hasB ? qb : -1};
+      long long t_last = clock64();
+      while (!failed && (nxt[0] <= lst[0] || nxt[1] <= lst[1])) {
+        bool prog = false;
         for (int x = 0; x < 2; ++x) {
-          const int lx = x ? qb : qa;  // the tile's last key tile
-          if ((x == 1 && !hasB) || j > lx) continue;
-          wait_or_fail(&sh.bar_p[x], j & 1, failed);  // P_X(j) written (S_X read)
-          wait_or_fail(&sh.bar_v[kb], (j >> 1) & 1, failed);
-          if (!failed) mma2(x, j);
-          if (j == lx) {  // MMA1_X is done for good: Q_X takes the gate of tile X
-            if (!failed) {
-              umma::mbar_expect_tx(&sh.bar_g[x], tile_bytes);
-              tma_tile(base + x * TILE, &tmg, b, h, lx * ROWS, &sh.bar_g[x]);
-              ++armed_g[x];
-            }
+          const int j = nxt[x];
+          // nothing here blocks: a tile waits while its v_j or k_{j+1} is not in
+          // yet (the copies of those wait on the other tile's MMAs, and the tile
+          // behind always finds its own in)
+          if (j > lst[x] || !umma::mbar_test(&sh.bar_p[x], j & 1)) continue;
+          if (!umma::mbar_test(&sh.bar_v[j & 1], (j >> 1) & 1)) continue;
+          if (j < lst[x] && !umma::mbar_test(&sh.bar_k[(j + 1) & 1], ((j + 1) >> 1) & 1)) continue;
+          umma::fence_after();
+          mma2(x, j);
+          if (j == lst[x]) {  // MMA1_X is done for good: Q_X takes the gate of tile X
+            umma::mbar_expect_tx(&sh.bar_g[x], tile_bytes);
+            tma_tile(base + x * TILE, &tmg, b, h, j * ROWS, &sh.bar_g[x]);
+            ++armed_g[x];
           } else {
-            wait_or_fail(&sh.bar_k[kb ^ 1], ((j + 1) >> 1) & 1, failed);
-            if (!failed) mma1(x, j + 1);
+            mma1(x, j + 1);
           }
+          nxt[x] = j + 1;
+          prog = true;
         }
-        // every MMA1 of key tile j is done (its softmax has read S): k buffer kb
-        // takes tile j + 2; once the MMA2s of key tile j are done, so does v
-        if (j + 2 <= last) {
-          if (!failed) {
-            umma::mbar_expect_tx(&sh.bar_k[kb], tile_bytes);
-            tma_tile(base + (2 + kb) * TILE, &tmk, b, hk, (j + 2) * ROWS, &sh.bar_k[kb]);
-            ++armed_k[kb];
-          }
-          wait_or_fail(&sh.bar_o[(hasB && j <= qb) ? 1 : 0], j & 1, failed);
-          if (!failed) {
-            umma::mbar_expect_tx(&sh.bar_v[kb], tile_bytes);
-            tma_tile(base + (4 + kb) * TILE, &tmv, b, hk, (j + 2) * ROWS, &sh.bar_v[kb]);
-            ++armed_v[kb];
-          }
-        }
+        if (prog) t_last = clock64();
+        else if (clock64() - t_last > 4000000000LL) failed = true;
       }
       // y of each tile out of its q buffer
       for (int x = 0; x < 2; ++x) {
@@ -211,16 +255,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
       }
       if (failed) {
-        // a wait gave up: every MMA issued completes and every copy armed lands
-        // before the CTA leaves (they complete on their own: normal budgets)
+        // a wait gave up: every MMA issued completes and every gate armed lands
         umma::commit(&sh.bar_drain);
         umma::mbar_wait(&sh.bar_drain, 0);
-        umma::mbar_wait(&sh.bar_q, 0);
-        for (int n = 0; n < 2; ++n) {
-          if (armed_k[n]) umma::mbar_wait(&sh.bar_k[n], (armed_k[n] - 1) & 1);
-          if (armed_v[n]) umma::mbar_wait(&sh.bar_v[n], (armed_v[n] - 1) & 1);
+        for (int n = 0; n < 2; ++n)
           if (armed_g[n]) umma::mbar_wait(&sh.bar_g[n], 0);
-        }
         umma::fence_after();
       }
       umma::bulk_wait_all();
