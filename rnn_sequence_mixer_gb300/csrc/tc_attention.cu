@@ -43,7 +43,7 @@ struct AttnParams {
 namespace tc {
 namespace {
 
-constexpr int kAttnThreads = 320;  // two softmax warpgroups, the copy warp, the MMA warp
+constexpr int kAttnThreads = 352;  // two softmax warpgroups, the copy warp, one MMA warp per query tile
 
 struct AttnShared {
   uint64_t bar_q;     // TMA: the two q tiles
@@ -54,9 +54,10 @@ struct AttnShared {
   uint64_t bar_o[2];  // MMA2 of query tile X done, one phase per key tile
   uint64_t bar_g[2];  // TMA: gate of query tile X, into its q buffer
   uint64_t bar_e[2];  // softmax X: y written over that gate (one arrive per warp)
-  uint64_t bar_kfree[2];  // every MMA1 reading k buffer j done (commit), one phase per tile held
-  uint64_t bar_vfree[2];  // every MMA2 reading v buffer j done (commit), one phase per tile held
-  uint64_t bar_drain; // after a wait gave up: every MMA issued is done (commit)
+  uint64_t bar_kfree[2];  // MMA1 of each query tile reading k buffer n done (one commit per tile), one phase per key tile held
+  uint64_t bar_vfree[2];  // MMA2 of each query tile reading v buffer n done (one commit per tile), one phase per key tile held
+  uint64_t bar_drain[2];  // after a wait gave up: every MMA issued for tile X is done (commit)
+  uint64_t bar_turn[2];   // the other tile's MMA thread has issued its products: tile X's turn
   uint32_t tmem_base;
   uint32_t failed;
 };
@@ -84,15 +85,17 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&x)[128]) {
 // for both.  Tensor memory: S_A, S_B (128 columns each; P_X is written as
 // packed bf16 over the first 64 columns of S_X, MMA2's A operand) and O_A,
 // O_B.  Warps 0..3 run the softmax of A, warps 4..7 that of B, one thread per
-// score row (the row's maximum and sum stay in the thread).  Warp 9's first
-// lane issues the MMAs: it polls both tiles and, as soon as a softmax has
-// written P_X(j), issues MMA2_X(j) = O_X += P_X V_j and MMA1_X(j + 1), so that
-// while one softmax works on its tile the tensor core runs the other tile's
-// products (an MMA1 that writes S_X right after the MMA2 that reads P_X from
-// the same columns is ordered behind it by the tensor pipe).  After the last
-// MMA1 (MMA2) that reads a k (v) buffer it commits to that buffer's "free"
-// barrier, and warp 8's first lane refills the buffer with the tile two ahead
-// as soon as that barrier completes, so the copies run a whole tile ahead.
+// score row (the row's maximum and sum stay in the thread).  The first lane of
+// warp 9 (10) issues the MMAs of A (B): once its softmax has written P_X(j), it
+// issues MMA2_X(j) = O_X += P_X V_j and MMA1_X(j + 1) (ordered behind it by the
+// tensor pipe, although it writes the columns that MMA2 reads P from).  A
+// thread that issues MMAs stalls while the tensor pipe is busy, so each tile
+// has a thread of its own: while one waits for the pipe the other's products
+// are already queued, and the pipe runs one tile's products while the other
+// tile's softmax works.  Each MMA thread commits to a buffer's "free" barrier
+// after its last MMA that reads the buffer, and warp 8's first lane refills the
+// buffer with the key tile two ahead once both have, so the copies run a whole
+// tile ahead.
 __global__ void __launch_bounds__(kAttnThreads, 1)
     tc_attention_kernel(const __grid_constant__ AttnParams A, const __grid_constant__ CUtensorMap tmq,
                         const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -114,12 +117,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (tid == 0) {
     uint64_t *bars[] = {&sh.bar_q, &sh.bar_k[0], &sh.bar_k[1], &sh.bar_v[0], &sh.bar_v[1],
                         &sh.bar_s[0], &sh.bar_s[1], &sh.bar_o[0], &sh.bar_o[1], &sh.bar_g[0],
-                        &sh.bar_g[1], &sh.bar_kfree[0], &sh.bar_kfree[1], &sh.bar_vfree[0],
-                        &sh.bar_vfree[1], &sh.bar_drain};
+                        &sh.bar_g[1], &sh.bar_drain[0], &sh.bar_drain[1], &sh.bar_turn[0],
+                        &sh.bar_turn[1]};
     for (uint64_t *bar : bars) umma::mbar_init(bar, 1);
     for (int x = 0; x < 2; ++x) {
       umma::mbar_init(&sh.bar_p[x], 4);
       umma::mbar_init(&sh.bar_e[x], 4);
+      // the tiles that wait on a free barrier (key tiles 0 .. qa - 1) are read by both query tiles
+      umma::mbar_init(&sh.bar_kfree[x], hasB ? 2 : 1);
+      umma::mbar_init(&sh.bar_vfree[x], hasB ? 2 : 1);
     }
     umma::mbar_fence_init();
     sh.failed = 0;
@@ -128,9 +134,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   sync_tc();
   const uint32_t tm = sh.tmem_base;
   bool failed = false;
-
-  // readers of key tile j: MMA1 (MMA2) of A while j <= qa, of B while j <= qb
-  auto readers = [&](int j) { return (j <= qa ? 1 : 0) + (hasB && j <= qb ? 1 : 0); };
 
   if (warp == 8) {
     // ---------------------------------------------------------------- copies
@@ -175,91 +178,81 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
       }
     }
-  } else if (warp == 9) {
-    // ---------------------------------------------------------------- MMAs
-    if (lane == 0) {
+  } else if (warp == 9 || warp == 10) {
+    // ---------------------------------------------------------------- MMAs of tile X
+    const int x = warp - 9, qx = x ? qb : qa;
+    if (lane == 0 && (x == 0 || hasB)) {
       const uint32_t id_qk = umma::idesc_bf16(128, 128, false, false);  // Q K^T, both K-major
       const uint32_t id_pv = umma::idesc_bf16(128, 128, false, true);   // P (TMEM) V
-      int armed_g[2] = {0, 0};
-      int kread[2] = {0, 0}, vread[2] = {0, 0};  // MMAs issued on the tile each buffer holds
-      // S_X = Q_X K_j^T into S_X (tm + 128 X); after the last reader of k buffer
-      // j & 1, its free barrier
-      auto mma1 = [&](int x, int j) {
-        const uint32_t aq = umma::smem_u32(base + x * TILE);
+      const uint32_t aq = umma::smem_u32(base + x * TILE);
+      const uint32_t tS = tm + 128 * x, tO = tm + 256 + 128 * x;
+      bool armed_g = false;
+      // S_X = Q_X K_j^T; then this tile is done with k buffer j & 1
+      auto mma1 = [&](int j) {
         const uint32_t ak = umma::smem_u32(base + (2 + (j & 1)) * TILE);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma::mma_ss(tm + 128 * x, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(ak, kk, ROWS),
-                       id_qk, kk > 0);
+          umma::mma_ss(tS, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(ak, kk, ROWS), id_qk,
+                       kk > 0);
         umma::commit(&sh.bar_s[x]);
-        if (++kread[j & 1] == readers(j)) {
-          umma::commit(&sh.bar_kfree[j & 1]);
-          kread[j & 1] = 0;
-        }
+        umma::commit(&sh.bar_kfree[j & 1]);
       };
-      // O_X += P_X V_j, P_X from the first 64 columns of S_X
-      auto mma2 = [&](int x, int j) {
+      // O_X += P_X V_j, P_X from the first 64 columns of S_X; then this tile is
+      // done with v buffer j & 1
+      auto mma2 = [&](int j) {
         const uint32_t av = umma::smem_u32(base + (4 + (j & 1)) * TILE);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma::mma_ts(tm + 256 + 128 * x, tm + 128 * x + 8 * kk, umma::desc_mnmajor(av, kk, ROWS),
-                       id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          umma::mma_ts(tO, tS + 8 * kk, umma::desc_mnmajor(av, kk, ROWS), id_pv,
+                       (j > 0 || kk > 0) ? 1u : 0u);
         umma::commit(&sh.bar_o[x]);
-        if (++vread[j & 1] == readers(j)) {
-          umma::commit(&sh.bar_vfree[j & 1]);
-          vread[j & 1] = 0;
-        }
+        umma::commit(&sh.bar_vfree[j & 1]);
       };
+      // The two threads take turns: A's first product, B's, then per key tile j
+      // A's MMA2 + MMA1 and B's.  A thread stalls while the tensor pipe is
+      // busy, so the one whose turn comes next makes its checks (P written, v
+      // and k in) meanwhile and issues as soon as the other has issued, and the
+      // products of the two tiles never share the pipe: each tile's S is ready
+      // as early as it can be and the two softmaxes take turns too.
+      // turn(n): wait for the other thread's n-th hand-over (0 = its first
+      // product); tile A has no turn to wait for without B, nor B past A's last
+      auto turn = [&](int n) {
+        if (hasB && (x == 0 || n <= qa + 1)) wait_or_fail(&sh.bar_turn[x], n & 1, failed);
+      };
+      auto hand_over = [&]() { umma::mbar_arrive(&sh.bar_turn[x ^ 1]); };
       wait_or_fail(&sh.bar_q, 0, failed);
       wait_or_fail(&sh.bar_k[0], 0, failed);
+      if (x == 1) turn(0);
+      if (!failed) mma1(0);
+      hand_over();
+      for (int j = 0; j <= qx && !failed; ++j) {
+        wait_or_fail(&sh.bar_p[x], j & 1, failed);
+        wait_or_fail(&sh.bar_v[j & 1], (j >> 1) & 1, failed);
+        if (j < qx) wait_or_fail(&sh.bar_k[(j + 1) & 1], ((j + 1) >> 1) & 1, failed);
+        turn(x == 0 ? j : j + 1);  // A's batch j follows B's hand-over j, B's follows A's j + 1
+        if (failed) break;
+        umma::fence_after();
+        mma2(j);
+        if (j == qx) {  // MMA1_X is done for good: Q_X takes the gate of tile X
+          umma::mbar_expect_tx(&sh.bar_g[x], tile_bytes);
+          tma_tile(base + x * TILE, &tmg, b, h, j * ROWS, &sh.bar_g[x]);
+          armed_g = true;
+        } else {
+          mma1(j + 1);
+        }
+        hand_over();
+      }
+      // y of tile X out of its q buffer
+      wait_or_fail(&sh.bar_e[x], 0, failed);
       if (!failed) {
-        mma1(0, 0);
-        if (hasB) mma1(1, 0);
-      }
-      // serve whichever softmax has written its P first
-      int nxt[2] = {0, 0};
-      const int lst[2] = {qa, hasB ? qb : -1};
-      long long t_last = clock64();
-      while (!failed && (nxt[0] <= lst[0] || nxt[1] <= lst[1])) {
-        bool prog = false;
-        for (int x = 0; x < 2; ++x) {
-          const int j = nxt[x];
-          // nothing here blocks: a tile waits while its v_j or k_{j+1} is not in
-          // yet (the copies of those wait on the other tile's MMAs, and the tile
-          // behind always finds its own in)
-          if (j > lst[x] || !umma::mbar_test(&sh.bar_p[x], j & 1)) continue;
-          if (!umma::mbar_test(&sh.bar_v[j & 1], (j >> 1) & 1)) continue;
-          if (j < lst[x] && !umma::mbar_test(&sh.bar_k[(j + 1) & 1], ((j + 1) >> 1) & 1)) continue;
-          umma::fence_after();
-          mma2(x, j);
-          if (j == lst[x]) {  // MMA1_X is done for good: Q_X takes the gate of tile X
-            umma::mbar_expect_tx(&sh.bar_g[x], tile_bytes);
-            tma_tile(base + x * TILE, &tmg, b, h, j * ROWS, &sh.bar_g[x]);
-            ++armed_g[x];
-          } else {
-            mma1(x, j + 1);
-          }
-          nxt[x] = j + 1;
-          prog = true;
-        }
-        if (prog) t_last = clock64();
-        else if (clock64() - t_last > 4000000000LL) failed = true;
-      }
-      // y of each tile out of its q buffer
-      for (int x = 0; x < 2; ++x) {
-        if (x == 1 && !hasB) continue;
-        wait_or_fail(&sh.bar_e[x], 0, failed);
-        if (!failed) {
-          tma_store_tile(&tmy, base + x * TILE, b, h, (x ? qb : qa) * ROWS);
-          umma::bulk_commit();
-        }
+        tma_store_tile(&tmy, base + x * TILE, b, h, qx * ROWS);
+        umma::bulk_commit();
       }
       if (failed) {
-        // a wait gave up: every MMA issued completes and every gate armed lands
-        umma::commit(&sh.bar_drain);
-        umma::mbar_wait(&sh.bar_drain, 0);
-        for (int n = 0; n < 2; ++n)
-          if (armed_g[n]) umma::mbar_wait(&sh.bar_g[n], 0);
+        // a wait gave up: every MMA this thread issued completes and its gate lands
+        umma::commit(&sh.bar_drain[x]);
+        umma::mbar_wait(&sh.bar_drain[x], 0);
+        if (armed_g) umma::mbar_wait(&sh.bar_g[x], 0);
         umma::fence_after();
       }
       umma::bulk_wait_all();
