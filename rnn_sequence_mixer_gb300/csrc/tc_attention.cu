@@ -224,6 +224,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // as early as it can be and the two softmaxes take turns too.
       // turn(n): wait for the other thread's n-th hand-over (0 = its first
       // product); tile A has no turn to wait for without B, nor B past A's last
+      auto wait_plain = [&](uint64_t *bar, uint32_t parity) {
+        if (!failed && !umma::mbar_wait(bar, parity)) failed = true;
+      };
       auto turn = [&](int n) {
         if (hasB && (x == 0 || n <= qa + 1) && !failed) {  // polled: the turn comes soon
           const long long t0 = clock64();
@@ -232,7 +235,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               failed = true;
               break;
             }
-          umma::fence_after();
         }
       };
       auto hand_over = [&]() { umma::mbar_arrive(&sh.bar_turn[x ^ 1]); };
@@ -246,9 +248,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // key tile j with its v in buffer N = j & 1 and the next k in buffer N ^ 1
       auto step = [&](int j, auto nbuf) {
         constexpr int N = decltype(nbuf)::value;
-        wait_or_fail(&sh.bar_p[x], j & 1, failed);
-        wait_or_fail(&sh.bar_v[N], (j >> 1) & 1, failed);
-        if (j < qx) wait_or_fail(&sh.bar_k[N ^ 1], ((j + 1) >> 1) & 1, failed);
+        // one tcgen05 fence after the last of these waits, before the MMAs
+        wait_plain(&sh.bar_p[x], j & 1);
+        wait_plain(&sh.bar_v[N], (j >> 1) & 1);
+        if (j < qx) wait_plain(&sh.bar_k[N ^ 1], ((j + 1) >> 1) & 1);
         turn(x == 0 ? j : j + 1);  // A's batch j follows B's hand-over j, B's follows A's j + 1
         if (failed) return;
         umma::fence_after();
