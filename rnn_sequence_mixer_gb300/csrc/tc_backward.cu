@@ -38,6 +38,8 @@
 // row i = 32 (w % 4) + l, its TMEM lane, and column quarter qd = w / 4; the
 // feature map uses row 8 w + l / 4 and pair quarter l % 4) and one issuer
 // thread issues the MMAs and TMA copies; they hand off through mbarriers.
+#include <type_traits>
+
 #include "tc_common.cuh"
 
 namespace hla {
@@ -320,8 +322,10 @@ __global__ void __launch_bounds__(NTO, 1)
       umma::mbar_expect_tx(&sh.bar_dy, tile_bytes);
       tma_tile(PM, &tmdy, b, h, t0, &sh.bar_dy);
       tma_prefetch_tile(&tmg, b, h, t0);
-      for (int n = 0; n < ntile; ++n) {
-        const int buf = n & 1;
+      // tile n with its k in buffer BUF = n & 1, a compile-time constant (tiles
+      // go in pairs), so that every MMA descriptor is loop-invariant
+      auto tile_step = [&](int n, auto nbuf) {
+        constexpr int buf = decltype(nbuf)::value;
         const uint32_t ph = n & 1;
         const int c0 = t0 + n * CV;
         unsigned char *Kt = base + (1 + buf) * TILE;
@@ -329,26 +333,28 @@ __global__ void __launch_bounds__(NTO, 1)
         const uint32_t ta = tm + 128 + 128 * buf;
         // MMA1 once q~, k~ are written (copied, when saved); MMA2 once Sb is
         if (kSaved) {
-          wait_or_fail(&sh.bar_q, ph, failed);
-          wait_or_fail(&sh.bar_k[buf], (n >> 1) & 1, failed);
+          wait_plain(&sh.bar_q, ph, failed);
+          wait_plain(&sh.bar_k[buf], (n >> 1) & 1, failed);
         } else {
-          wait_or_fail(&sh.bar_feat, ph, failed);
+          wait_plain(&sh.bar_feat, ph, failed);
         }
         if (!failed) {
+          umma::fence_after();  // covers the waits before this group of MMAs
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma::mma_ss(tP, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(ak, kk, ROWS), id_qk, kk > 0);
           umma::commit(&sh.bar_p);
         }
-        wait_or_fail(&sh.bar_sb, ph, failed);
+        wait_plain(&sh.bar_sb, ph, failed);
         if (!failed) {
+          umma::fence_after();  // covers the waits before this group of MMAs
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma::mma_ss(ta, umma::desc_kmajor(aq, kk, ROWS), umma::desc_mnmajor(asb, kk, ROWS), id_qs, kk > 0);
           umma::commit(&sh.bar_o);
         }
         // MMA2 done: Q takes this tile's gate
-        wait_or_fail(&sh.bar_o, ph, failed);
+        wait_plain(&sh.bar_o, ph, failed);
         if (!failed) {
           umma::mbar_expect_tx(&sh.bar_g, tile_bytes);
           tma_tile(Qs, &tmg, b, h, c0, &sh.bar_g);
@@ -361,9 +367,10 @@ __global__ void __launch_bounds__(NTO, 1)
           }
         }
         // MMA3 once Pm, the scaled O and V are in place
-        wait_or_fail(&sh.bar_pm, ph, failed);
-        wait_or_fail(&sh.bar_v, ph, failed);
+        wait_plain(&sh.bar_pm, ph, failed);
+        wait_plain(&sh.bar_v, ph, failed);
         if (!failed) {
+          umma::fence_after();  // covers the waits before this group of MMAs
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // A = Pm from the P columns of TMEM
             umma::mma_ts(ta, tP + 32 * (kk >> 1) + 8 * (kk & 1), umma::desc_mnmajor(av, kk, ROWS),
@@ -371,11 +378,12 @@ __global__ void __launch_bounds__(NTO, 1)
           umma::commit(&sh.bar_m3);
         }
         // dgate (PM) and dO (Q) out; MMA5, MMA6 from dO
-        wait_or_fail(&sh.bar_do, ph, failed);
+        wait_plain(&sh.bar_do, ph, failed);
         if (!failed) {
           tma_store_tile(&tmdg, PM, b, h, c0);
           tma_store_tile(&tmo, Qs, b, h, c0);
           umma::bulk_commit();
+          umma::fence_after();  // covers the waits before this group of MMAs
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma::mma_ss(tP, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(av, kk, ROWS), id_kk, kk > 0);
@@ -390,14 +398,14 @@ __global__ void __launch_bounds__(NTO, 1)
           }
         }
         // MMA5 / MMA6 done and dO stored: Q takes the next q
-        wait_or_fail(&sh.bar_m56, ph, failed);
+        wait_plain(&sh.bar_m56, ph, failed);
         if (!failed && n + 1 < ntile) {
           umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
           tma_tile(Qs, &tmq, b, h, c0 + CV, &sh.bar_q);
         }
         // dq of tile n - 1 is in its K buffer: store it, then that buffer takes k of tile n + 1
         if (n >= 1) {
-          wait_or_fail(&sh.bar_w6, (n - 1) & 1, failed);
+          wait_plain(&sh.bar_w6, (n - 1) & 1, failed);
           unsigned char *Kp = base + (2 - buf) * TILE;
           if (!failed) {
             tma_store_tile(&tmdq, Kp, b, h, c0 - CV);
@@ -410,8 +418,9 @@ __global__ void __launch_bounds__(NTO, 1)
           }
         }
         // MMA7 and MMA4 once dPm, the scaled I and Vdec are in place
-        wait_or_fail(&sh.bar_w5, ph, failed);
+        wait_plain(&sh.bar_w5, ph, failed);
         if (!failed) {
+          umma::fence_after();  // covers the waits before this group of MMAs
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // A = dPm from the dP columns of TMEM
             umma::mma_ts(ta, tP + 32 * (kk >> 1) + 8 * (kk & 1), umma::desc_mnmajor(ak, kk, ROWS),
@@ -422,7 +431,7 @@ __global__ void __launch_bounds__(NTO, 1)
           umma::commit(&sh.bar_m74);
         }
         // both done: V takes the next v, this K buffer takes raw q of tile n for [W6]
-        wait_or_fail(&sh.bar_m74, ph, failed);
+        wait_plain(&sh.bar_m74, ph, failed);
         if (!failed) {
           if (n + 1 < ntile) {
             umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
@@ -432,9 +441,13 @@ __global__ void __launch_bounds__(NTO, 1)
           tma_tile(Kt, &tmq, b, h, c0, &sh.bar_qr);
 
         }
+            };
+      for (int n = 0; n < ntile; n += 2) {
+        tile_step(n, std::integral_constant<int, 0>{});
+        if (n + 1 < ntile) tile_step(n + 1, std::integral_constant<int, 1>{});
       }
       // dq of the last tile
-      wait_or_fail(&sh.bar_w6, (ntile - 1) & 1, failed);
+      wait_plain(&sh.bar_w6, (ntile - 1) & 1, failed);
       if (!failed) {
         tma_store_tile(&tmdq, base + (1 + ((ntile - 1) & 1)) * TILE, b, h, t0 + (ntile - 1) * CV);
         umma::bulk_commit();
@@ -472,8 +485,8 @@ __global__ void __launch_bounds__(NTO, 1)
       unsigned char *Kt = base + (1 + buf) * TILE, *Kp = base + (2 - buf) * TILE;
       if (have) {
         // [W1] raw q, k of tile n: row fr, pairs [16 fu, 16 fu + 16); norms by shuffles
-        wait_or_fail(&sh.bar_q, ph, failed);
-        wait_or_fail(&sh.bar_k[buf], (n >> 1) & 1, failed);
+        wait_plain(&sh.bar_q, ph, failed);
+        wait_plain(&sh.bar_k[buf], (n >> 1) & 1, failed);
         if (!kSaved) {
           uint4 qr[4], kr[4];
           ld_pairs(Qs, fr, fu, qr);
@@ -593,9 +606,9 @@ __global__ void __launch_bounds__(NTO, 1)
         // [W4] after MMA3: output norm and gate backward.  n = o r, z = sigmoid(gate),
         // dn = dy z, dgate = dn n (1 - z), dO = r (dn - n mean(dn n)); rows past the tile get 0
         wait_or_fail(&sh.bar_m3, ph, failed);
-        wait_or_fail(&sh.bar_g, ph, failed);
-        wait_or_fail(&sh.bar_v, ph, failed);
-        wait_or_fail(&sh.bar_dy, ph, failed);
+        wait_plain(&sh.bar_g, ph, failed);
+        wait_plain(&sh.bar_v, ph, failed);
+        wait_plain(&sh.bar_dy, ph, failed);
         {
           float o[32];
           umma::tmem_ld2x16(ta + col, o);
@@ -666,7 +679,7 @@ __global__ void __launch_bounds__(NTO, 1)
         // while MMA5 / MMA6 of tile n are in flight.
         // (in the last step no [W2] has waited for MMA7 of tile n - 1: wait here)
         if (!have) wait_or_fail(&sh.bar_m74, (n - 1) & 1, failed);
-        wait_or_fail(&sh.bar_qr, (n - 1) & 1, failed);
+        wait_plain(&sh.bar_qr, (n - 1) & 1, failed);
         {
           uint4 qr[4];
           ld_pairs(Kp, i, qd, qr);

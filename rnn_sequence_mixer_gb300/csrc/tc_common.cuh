@@ -426,6 +426,13 @@ __device__ __forceinline__ void wait_or_fail(uint64_t *bar, uint32_t parity, boo
   if (!failed && !umma::mbar_wait(bar, parity)) failed = true;
   umma::fence_after();
 }
+// The same without the tcgen05 fence (which costs the waiting thread tens of
+// cycles each time): for waits whose consumer is no tcgen05 operation (a TMA
+// copy's data read by this thread, a copy issued into a freed buffer), or
+// where one fence_after before a group of MMAs covers every wait before it.
+__device__ __forceinline__ void wait_plain(uint64_t *bar, uint32_t parity, bool &failed) {
+  if (!failed && !umma::mbar_wait(bar, parity)) failed = true;
+}
 
 // A 4-byte global -> shared copy that holds no register while it is in flight
 // (cp.async); its data is there for this thread after cp_async_wait().

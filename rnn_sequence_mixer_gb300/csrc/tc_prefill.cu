@@ -139,8 +139,9 @@ __global__ void __launch_bounds__(NTO, 1)
         const int st = n % kStages;
         const uint32_t par = (n / kStages) & 1;
         unsigned char *Kt = base + 2 * st * TILE;
-        wait_or_fail(&sh.bar_feat[st], par, failed);
+        wait_plain(&sh.bar_feat[st], par, failed);
         if (!failed) {
+          umma::fence_after();
           const uint32_t a = umma::smem_u32(Kt), bv = a + TILE;
 #pragma unroll
           for (int kk = 0; kk < ROWS / 16; ++kk)
@@ -149,7 +150,7 @@ __global__ void __launch_bounds__(NTO, 1)
           umma::commit(&sh.bar_mma[st]);
         }
         if (n + kStages < ntile) {  // the stage takes tile n + 3 once MMA n has read it
-          wait_or_fail(&sh.bar_mma[st], par, failed);
+          wait_plain(&sh.bar_mma[st], par, failed);
           if (!failed) {
             const int cn = tb + (n + kStages) * CV;
             umma::mbar_expect_tx(&sh.bar_tma[st], 2 * tile_bytes);
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(NTO, 1)
       const int st = n % kStages;
       unsigned char *Kt = base + 2 * st * TILE;
       const int c0 = tb + n * CV, c = min(CV, t1 - c0);
-      wait_or_fail(&sh.bar_tma[st], (n / kStages) & 1, failed);
+      wait_plain(&sh.bar_tma[st], (n / kStages) & 1, failed);
       const bool valid = fr < c;
       if (kSaved) {  // q~ -> gamma^{s+1} q~ or k~ -> gamma^{L-1-s} k~ (fp16 -> bf16) in
                      // place; zeros past the tile
@@ -285,8 +286,9 @@ __device__ __noinline__ bool window_issue(const CUtensorMap &tmk, const CUtensor
     const int st = w % 3;
     const uint32_t par = (w / 3) & 1;
     unsigned char *Kw = base + 2 * st * TILE;
-    wait_or_fail(&sh.bar_wfeat[st], par, failed);
+    wait_plain(&sh.bar_wfeat[st], par, failed);
     if (!failed) {
+      umma::fence_after();
       const uint32_t a = umma::smem_u32(Kw), bv = a + TILE;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
@@ -294,7 +296,7 @@ __device__ __noinline__ bool window_issue(const CUtensorMap &tmk, const CUtensor
       umma::commit(&sh.bar_wmma[st]);
     }
     if (w + 3 < nw) {  // the stage takes tile w + 3 once MMA w has read it
-      wait_or_fail(&sh.bar_wmma[st], par, failed);
+      wait_plain(&sh.bar_wmma[st], par, failed);
       if (!failed) {
         umma::mbar_expect_tx(&sh.bar_wtma[st], 2 * tile_bytes);
         tma_tile(Kw, &tmk, b, h, ws + (w + 3) * CV, &sh.bar_wtma[st]);
@@ -351,7 +353,7 @@ __device__ __noinline__ bool window_work(const MixerParams &P, OutShared &sh, un
   for (int w = 0; w < nw; ++w) {
     const int st = w % 3;
     unsigned char *Kw = base + 2 * st * TILE;
-    wait_or_fail(&sh.bar_wtma[st], (w / 3) & 1, failed);
+    wait_plain(&sh.bar_wtma[st], (w / 3) & 1, failed);
     const int s_tok = ws + w * CV + fr;
     const float wgt = wvalid ? exp2f((float)(t0 - 1 - s_tok) * l2g) : 0.f;
     if (kFeat) {  // given k~ (fp16): weight and convert
@@ -515,15 +517,15 @@ __global__ void __launch_bounds__(NTO, 1)
         const uint32_t ak = umma::smem_u32(base + (1 + buf) * TILE);
         const uint32_t as = umma::smem_u32(SP), av = umma::smem_u32(Vs);
         const uint32_t ocur = tm + 128 + 128 * buf;
+        // (one tcgen05 fence before each group of MMAs covers the waits before it)
         if (kFeat) {  // q~, k~ given: MMA1 once their copies are in
-          wait_or_fail(&sh.bar_q, n & 1, failed);
-          wait_or_fail(&sh.bar_k[buf], (n >> 1) & 1, failed);
+          wait_plain(&sh.bar_q, n & 1, failed);
+          wait_plain(&sh.bar_k[buf], (n >> 1) & 1, failed);
         } else {
           if (n == 0 && P.test_wait_cycles > 0) {  // testing the expiry path
             if (!failed && !umma::mbar_wait(&sh.bar_feat, 0, P.test_wait_cycles)) failed = true;
-            umma::fence_after();
           } else {
-            wait_or_fail(&sh.bar_feat, n & 1, failed);
+            wait_plain(&sh.bar_feat, n & 1, failed);
           }
         }
         if (!failed) {
@@ -532,14 +534,16 @@ __global__ void __launch_bounds__(NTO, 1)
             tma_store_tile(&tmsk, base + (1 + buf) * TILE, b, h, c0);
             umma::bulk_commit();
           }
+          umma::fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma::mma_ss(tP, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(ak, kk, ROWS),
                          id_qk, kk > 0);
           umma::commit(&sh.bar_p);
         }
-        wait_or_fail(&sh.bar_sb, n & 1, failed);
+        wait_plain(&sh.bar_sb, n & 1, failed);
         if (!failed) {
+          umma::fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma::mma_ss(ocur, umma::desc_kmajor(aq, kk, ROWS), umma::desc_mnmajor(as, kk, ROWS),
@@ -552,7 +556,7 @@ __global__ void __launch_bounds__(NTO, 1)
         }
         // MMA2 done: Q is free for the next q (as early as possible: the
         // workers need it right after this tile's mask)
-        wait_or_fail(&sh.bar_mma[0], n & 1, failed);
+        wait_plain(&sh.bar_mma[0], n & 1, failed);
         if (!failed && n + 1 < ntile) {
           umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
           tma_tile(Qs, &tmq, b, h, c0 + CV, &sh.bar_q);
@@ -561,9 +565,10 @@ __global__ void __launch_bounds__(NTO, 1)
         // the q tile after that into L2, so that its copy (issued one tile
         // from now, on the workers' critical path) does not wait on HBM
         if (!failed && n + 2 < ntile) tma_prefetch_tile(&tmq, b, h, c0 + 2 * CV);
-        wait_or_fail(&sh.bar_pm, n & 1, failed);
-        wait_or_fail(&sh.bar_v, n & 1, failed);
+        wait_plain(&sh.bar_pm, n & 1, failed);
+        wait_plain(&sh.bar_v, n & 1, failed);
         if (!failed) {
+          umma::fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma::mma_ss(ocur, umma::desc_kmajor(as, kk, ROWS), umma::desc_mnmajor(av, kk, ROWS),
@@ -575,7 +580,7 @@ __global__ void __launch_bounds__(NTO, 1)
           umma::commit(&sh.bar_mma[1]);
         }
         // MMA3 / MMA4 done: V and K buffer `buf` are free for the next copies
-        wait_or_fail(&sh.bar_mma[1], n & 1, failed);
+        wait_plain(&sh.bar_mma[1], n & 1, failed);
         if (!failed) {
           if (n + 1 < ntile) {
             umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
@@ -591,7 +596,7 @@ __global__ void __launch_bounds__(NTO, 1)
         // y of tile n - 1 is in G once the workers' epilogue (after this
         // tile's mask) is done: store it, then G takes the gate of tile n
         if (n >= 1) {
-          wait_or_fail(&sh.bar_epi, (n - 1) & 1, failed);
+          wait_plain(&sh.bar_epi, (n - 1) & 1, failed);
           if (!failed) {
             tma_store_tile(&tmy, Gs, b, h, c0 - CV);
             umma::bulk_commit();
@@ -603,7 +608,7 @@ __global__ void __launch_bounds__(NTO, 1)
         }
       }
       // y of the last tile
-      wait_or_fail(&sh.bar_epi, (ntile - 1) & 1, failed);
+      wait_plain(&sh.bar_epi, (ntile - 1) & 1, failed);
       if (!failed) {
         tma_store_tile(&tmy, Gs, b, h, t0 + (ntile - 1) * CV);
         umma::bulk_commit();
@@ -671,8 +676,8 @@ __global__ void __launch_bounds__(NTO, 1)
             rope_entry(P.pos_offset + c0 + 8 * warp, sh.ru, lane >> 3, lane & 7);
         __syncwarp();
         // [A] raw q, k of tile n: row fr, pairs [16 fu, 16 fu + 16); norms by shuffles
-        wait_or_fail(&sh.bar_q, n & 1, failed);
-        wait_or_fail(&sh.bar_k[buf], (n >> 1) & 1, failed);
+        wait_plain(&sh.bar_q, n & 1, failed);
+        wait_plain(&sh.bar_k[buf], (n >> 1) & 1, failed);
         uint4 qr[4], kr[4];
         ld_pairs(Qt, fr, fu, qr);
         ld_pairs(Kt, fr, fu, kr);
@@ -753,7 +758,7 @@ __global__ void __launch_bounds__(NTO, 1)
           mask_lower_table(x, sh.dm, i, (int)col);
           // k~dec = gamma^{c-1-i} k~ as bf16, in place (K~ is dead once MMA1 is done,
           // and, when saving, once its store has read it)
-          if (kSave) wait_or_fail(&sh.bar_sv, n & 1, failed);
+          if (kSave) wait_plain(&sh.bar_sv, n & 1, failed);
           {
             const f2 wk = dup2(valid ? sh.pw[c - 1 - i] : 0.f);
 #pragma unroll
@@ -814,7 +819,7 @@ __global__ void __launch_bounds__(NTO, 1)
         sh.red_o[qd][i] = hsum2(ss);
         named_sync(5 + sub, 128);
         // gate of tile n - 1 (TMA) -> y, in place; the issuer stores the tile
-        wait_or_fail(&sh.bar_g, (n - 1) & 1, failed);
+        wait_plain(&sh.bar_g, (n - 1) & 1, failed);
         {
           const f2 ro = dup2(rsqrtf((sh.red_o[0][i] + sh.red_o[1][i] + sh.red_o[2][i] +
                                      sh.red_o[3][i]) / (float)D + P.eps));
