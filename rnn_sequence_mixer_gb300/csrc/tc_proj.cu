@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kProjThreads, 1)
         const int m0 = (tile / P.n_nt) * kBM, n0 = (tile % P.n_nt) * kBN;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % kStages;
-          if (it >= kStages) wait_bounded(&sh.empty[s], ((it / kStages) & 1) ^ 1, failed);
+          if (it >= kStages) wait_plain(&sh.empty[s], ((it / kStages) & 1) ^ 1, failed);
           if (failed) continue;
           unsigned char *st = base + s * kStageBytes;
           umma::mbar_expect_tx(&sh.full[s], kStageBytes);
@@ -149,21 +149,36 @@ __global__ void __launch_bounds__(kProjThreads, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = umma::idesc_bf16(kBM, kBN, false, false);
+      const uint32_t a0 = umma::smem_u32(base);
       int it = 0, i = 0;
       for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
         const int ab = i & 1;
         const uint32_t acc = tm + 256 * ab;
+        // the fence after this wait orders the tile's MMAs after the epilogue's
+        // reads of the accumulator; the stage waits need none (TMA data)
         if (i >= 2) wait_bounded(&sh.tempty[ab], ((i >> 1) - 1) & 1, failed);
-        for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int s = it % kStages;
-          wait_bounded(&sh.full[s], (it / kStages) & 1, failed);
-          if (failed) continue;
-          const uint32_t a = umma::smem_u32(base + s * kStageBytes), w = a + kATile;
+        // K block kb from stage S: the four MMAs and the stage's release
+        auto kblock = [&](int kb, int s, uint32_t par) {
+          wait_plain(&sh.full[s], par, failed);
+          if (failed) return;
+          const uint32_t a = a0 + s * kStageBytes, w = a + kATile;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             umma::mma_ss(acc, umma::make_desc(a + 32 * kk, 16, 1024),
                          umma::make_desc(w + 32 * kk, 16, 1024), idesc, (kb | kk) ? 1u : 0u);
           umma::commit(&sh.empty[s]);
+        };
+        if (nk % kStages == 0) {
+          // every tile starts at stage 0: stages as compile-time constants, so
+          // each MMA's descriptors are loop-invariant (computing them between
+          // MMAs holds the issuing thread behind the tensor pipe)
+          for (int kb = 0; kb < nk; kb += kStages, it += kStages) {
+            const uint32_t par = (it / kStages) & 1;
+#pragma unroll
+            for (int s = 0; s < kStages; ++s) kblock(kb + s, s, par);
+          }
+        } else {
+          for (int kb = 0; kb < nk; ++kb, ++it) kblock(kb, it % kStages, (it / kStages) & 1);
         }
         if (!failed) umma::commit(&sh.tfull[ab]);
       }
