@@ -70,6 +70,13 @@ __device__ __forceinline__ float ex2_fast(float x) {
   return y;
 }
 
+// A bounded wait (as wait_or_fail) that tries the phase once before reading
+// the clock: the phases waited on here have mostly completed already.
+__device__ __forceinline__ void attn_wait(uint64_t *bar, uint32_t parity, bool &failed) {
+  if (!failed && !umma::mbar_wait_tryfirst(bar, parity)) failed = true;
+  umma::fence_after();
+}
+
 // 128 consecutive fp32 columns of this thread's TMEM lane under one wait.
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&x)[128]) {
   uint32_t r[8][16];
@@ -157,13 +164,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int j = 0; j + 2 <= last; ++j) {
         const int kb = j & 1;
         if (j + 3 <= last) tma_prefetch_tile(&tmk, b, hk, (j + 3) * ROWS);
-        wait_or_fail(&sh.bar_kfree[kb], (j >> 1) & 1, failed);
+        attn_wait(&sh.bar_kfree[kb], (j >> 1) & 1, failed);
         if (!failed) {
           umma::mbar_expect_tx(&sh.bar_k[kb], tile_bytes);
           tma_tile(base + (2 + kb) * TILE, &tmk, b, hk, (j + 2) * ROWS, &sh.bar_k[kb]);
           ++armed_k[kb];
         }
-        wait_or_fail(&sh.bar_vfree[kb], (j >> 1) & 1, failed);
+        attn_wait(&sh.bar_vfree[kb], (j >> 1) & 1, failed);
         if (!failed) {
           umma::mbar_expect_tx(&sh.bar_v[kb], tile_bytes);
           tma_tile(base + (4 + kb) * TILE, &tmv, b, hk, (j + 2) * ROWS, &sh.bar_v[kb]);
@@ -225,7 +232,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // turn(n): wait for the other thread's n-th hand-over (0 = its first
       // product); tile A has no turn to wait for without B, nor B past A's last
       auto wait_plain = [&](uint64_t *bar, uint32_t parity) {
-        if (!failed && !umma::mbar_wait(bar, parity)) failed = true;
+        if (!failed && !umma::mbar_wait_tryfirst(bar, parity)) failed = true;
       };
       auto turn = [&](int n) {
         if (hasB && (x == 0 || n <= qa + 1) && !failed) {  // polled: the turn comes soon
@@ -240,8 +247,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       auto hand_over = [&]() { umma::mbar_arrive(&sh.bar_turn[x ^ 1]); };
       constexpr std::integral_constant<int, 0> kBuf0{};
       constexpr std::integral_constant<int, 1> kBuf1{};
-      wait_or_fail(&sh.bar_q, 0, failed);
-      wait_or_fail(&sh.bar_k[0], 0, failed);
+      attn_wait(&sh.bar_q, 0, failed);
+      attn_wait(&sh.bar_k[0], 0, failed);
       if (x == 1) turn(0);
       if (!failed) mma1(0, kBuf0);
       hand_over();
@@ -270,7 +277,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (j + 1 <= qx && !failed) step(j + 1, kBuf1);
       }
       // y of tile X out of its q buffer
-      wait_or_fail(&sh.bar_e[x], 0, failed);
+      attn_wait(&sh.bar_e[x], 0, failed);
       if (!failed) {
         tma_store_tile(&tmy, base + x * TILE, b, h, qx * ROWS);
         umma::bulk_commit();
@@ -295,7 +302,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                      (1.4426950408889634f / 11.313708498984761f);
     float m_run = -INFINITY, l = 0.f;
     for (int j = 0; j <= qx; ++j) {
-      wait_or_fail(&sh.bar_s[x], j & 1, failed);
+      attn_wait(&sh.bar_s[x], j & 1, failed);
       float s[128];
       tmem_ld128(tS, s);
       if (j == qx) {  // the diagonal tile: keys after the query are masked
@@ -338,7 +345,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       l = fmaf(l, alpha, hsum2(s4[0]) + hsum2(s4[1]) + (hsum2(s4[2]) + hsum2(s4[3])));
       if (j > 0 && __any_sync(0xffffffffu, upd)) {  // O <- alpha O once MMA2_X(j - 1) is done
-        wait_or_fail(&sh.bar_o[x], (j - 1) & 1, failed);
+        attn_wait(&sh.bar_o[x], (j - 1) & 1, failed);
         const f2 al = dup2(alpha);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -358,7 +365,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     // epilogue: o = O / l, y = Norm(o) sigmoid(gate) over the gate tile in Q_X;
     // the last MMA2_X's completion covers every earlier one
-    wait_or_fail(&sh.bar_o[x], qx & 1, failed);
+    attn_wait(&sh.bar_o[x], qx & 1, failed);
     float o[128];
     tmem_ld128(tO, o);
     const float inv_l = 1.f / l;
@@ -376,7 +383,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
       for (int u = 0; u < 32; ++u) o4[u] = make_float4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
     }
-    wait_or_fail(&sh.bar_g[x], 0, failed);
+    attn_wait(&sh.bar_g[x], 0, failed);
     {
       unsigned char *G = base + x * TILE;
       const f2 r2 = dup2(ro), half = dup2(0.5f);
