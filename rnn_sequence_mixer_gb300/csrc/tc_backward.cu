@@ -857,6 +857,7 @@ __global__ void __launch_bounds__(NTO, 1)
         umma::mbar_expect_tx(&sh.bar_kr, tile_bytes);
         tma_tile(X, &tmk, b, h, cl, &sh.bar_kr);
       }
+      bool v_pending = false;  // v of this tile waits for the dk store to leave V
       for (int it = 0; it < ntile; ++it) {
         const int n = ntile - 1 - it;
         const uint32_t ph = it & 1;
@@ -873,6 +874,15 @@ __global__ void __launch_bounds__(NTO, 1)
             umma::mma_ss(tA, umma::desc_kmajor(aK, kk, ROWS), umma::desc_kmajor(aQ, kk, ROWS), id_kq16, kk > 0);
           umma::commit(&sh.bar_m1);
         }
+        // V takes this tile's v once the dk store of the tile after has read it
+        // (after M1, which needs neither: waiting for that store's read before
+        // M1 held the workers' [V3] back)
+        if (v_pending && !failed) {
+          umma::bulk_wait_read();
+          umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
+          tma_tile(Vt, &tmv, b, h, c0, &sh.bar_v);
+        }
+        v_pending = false;
         wait_or_fail(&sh.bar_v, ph, failed);
         wait_or_fail(&sh.bar_dot, ph, failed);
         if (!failed) {
@@ -931,8 +941,8 @@ __global__ void __launch_bounds__(NTO, 1)
             tma_tile(Kt, &tmk, b, h, c0 - CV, &sh.bar_k);
           }
         }
-        // dk out of V, then V takes the tile before; [V6] is done with raw k: X
-        // takes raw k of the tile before
+        // dk out of V (V takes the tile before after that tile's M1); [V6] is
+        // done with raw k: X takes raw k of the tile before
         wait_or_fail(&sh.bar_dkout, ph, failed);
         if (!failed) {
           if (n > 0) {
@@ -941,11 +951,7 @@ __global__ void __launch_bounds__(NTO, 1)
           }
           tma_store_tile(&tmdk, Vt, b, h, c0);
           umma::bulk_commit();
-          if (n > 0) {
-            umma::bulk_wait_read();
-            umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
-            tma_tile(Vt, &tmv, b, h, c0 - CV, &sh.bar_v);
-          }
+          v_pending = n > 0;
         }
       }
       umma::bulk_wait_all();
