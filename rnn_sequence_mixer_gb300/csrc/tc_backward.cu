@@ -648,10 +648,15 @@ __global__ void __launch_bounds__(NTO, 1)
                                    sh.red_do[1][3][i]) / (float)D;
           const f2 ro2 = dup2(ro), nmean = dup2(-mean), one = dup2(1.f), keep = dup2(valid ? 1.f : 0.f);
           f2 vd = 0ull;
+          uint32_t zr[2][16];  // z back from TMEM under one wait
+          umma::tmem_ld16_nowait(myP, zr[0]);
+          umma::tmem_ld16_nowait(myP + 16, zr[1]);
+          umma::tmem_wait_ld();
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             float zs[8];
-            umma::tmem_ld8(myP + 8 * u, zs);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) zs[e] = __uint_as_float(zr[u >> 1][8 * (u & 1) + e]);
             uint4 *gp = tile_at(Qs, i, 4 * qd + u);
             f2 dv[4], vv[4], dg[4], dd[4];
             unpack4x2(*tile_at(PM, i, 4 * qd + u), dv);
