@@ -577,17 +577,21 @@ __global__ void __launch_bounds__(NTO, 1)
           // features (written in [W1], met at [W2]'s barrier).
           if (kSaved) cp_async_wait();
           store_tmem_bf16(myP, x, qd == sub ? i - (int)col : -1, qd == sub ? sh.qk_diag[buf][i] : 0.f);
-          wait_or_fail(&sh.bar_o, ph, failed);  // MMA2 done: SB is free to rewrite
+          // Sb -> S (bf16, unscaled) for MMA6: read and converted now (MMA2 only
+          // reads Sb), written once MMA2 is done
           const f2 si = dup2(s_inv);
+          uint4 snew[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {  // Sb -> S (bf16, unscaled) for MMA6
-            uint4 *p = tile_at(SB, i, 4 * qd + u);
+          for (int u = 0; u < 4; ++u) {
             f2 f[4];
-            unpack4x2h(*p, f);
+            unpack4x2h(*tile_at(SB, i, 4 * qd + u), f);
 #pragma unroll
             for (int e = 0; e < 4; ++e) f[e] = mul2(f[e], si);
-            *p = pack4x2(f);
+            snew[u] = pack4x2(f);
           }
+          wait_or_fail(&sh.bar_o, ph, failed);  // MMA2 done: SB is free to rewrite
+#pragma unroll
+          for (int u = 0; u < 4; ++u) *tile_at(SB, i, 4 * qd + u) = snew[u];
           float ov[32];
           umma::tmem_ld2x16(ta + col, ov);
           const f2 f = dup2(sh.pw[i + 1] * s_inv);
@@ -618,6 +622,14 @@ __global__ void __launch_bounds__(NTO, 1)
           // columns of TMEM until the second loop (MMA3 has read Pm from them
           // and MMA5 writes dP there only after this phase)
           f2 so2 = 0ull, sdo = 0ull;
+          // every gate and dy chunk of the row first: the TMEM stores below are
+          // ordered against shared-memory accesses, so loads after them would wait
+          uint4 graw[4], draw[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            graw[u] = *tile_at(Qs, i, 4 * qd + u);
+            draw[u] = *tile_at(PM, i, 4 * qd + u);
+          }
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             float zs[16];
@@ -625,8 +637,8 @@ __global__ void __launch_bounds__(NTO, 1)
             for (int uu = 0; uu < 2; ++uu) {
               const int u = 2 * hf + uu;
               f2 gz[4], dv[4];
-              unpack4x2(*tile_at(Qs, i, 4 * qd + u), gz);
-              unpack4x2(*tile_at(PM, i, 4 * qd + u), dv);
+              unpack4x2(graw[u], gz);
+              unpack4x2(draw[u], dv);
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const f2 z = sigmoid2(gz[e]);
@@ -1071,19 +1083,26 @@ __global__ void __launch_bounds__(NTO, 1)
       // diagonal, from the dq pass) into X once dV has read X
       {
         const float vdiag = (qd == sub && valid) ? P.ddiag[((size_t)b * P.H + h) * P.T + c0 + i] : 0.f;
-        wait_or_fail(&sh.bar_m2, ph, failed);
+        // v (once its copy is in) and q~ of the row are read and converted
+        // before M2 is done (M2 only reads them); the rewrites wait for it
+        wait_plain(&sh.bar_v, ph, failed);
         const f2 w = dup2(wdec);
+        uint4 vnew[4], qnew[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          uint4 *p = tile_at(Vt, i, 4 * qd + u);
           f2 f[4];
-          unpack4x2(*p, f);
+          unpack4x2(*tile_at(Vt, i, 4 * qd + u), f);
 #pragma unroll
           for (int e = 0; e < 4; ++e) f[e] = mul2(f[e], w);
-          *p = pack4x2(f);
-          uint4 *pq = tile_at(Qt, i, 4 * qd + u);
-          unpack4x2h(*pq, f);
-          *pq = pack4x2(f);
+          vnew[u] = pack4x2(f);
+          unpack4x2h(*tile_at(Qt, i, 4 * qd + u), f);
+          qnew[u] = pack4x2(f);
+        }
+        wait_or_fail(&sh.bar_m2, ph, failed);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          *tile_at(Vt, i, 4 * qd + u) = vnew[u];
+          *tile_at(Qt, i, 4 * qd + u) = qnew[u];
         }
         float v[32];
         umma::tmem_ld2x16(tB + lane_base + col, v);
