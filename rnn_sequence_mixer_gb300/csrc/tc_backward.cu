@@ -1051,6 +1051,20 @@ __global__ void __launch_bounds__(NTO, 1)
       warp_arrive(&sh.bar_eb, lane);
 
       // [V3] after M1: X = bf16(M1 (.) D^T) with the fp32 diagonal; k~ -> K~dec
+      // (with saved features k~ came by TMA, so its row is read and weighted
+      // before M1 is done, and only the rewrite waits)
+      uint4 kdnew[4];
+      if (kSaved) {
+        const f2 w = dup2(wdec);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          f2 f[4];
+          unpack4x2h(*tile_at(Kt, i, 4 * qd + u), f);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) f[e] = mul2(f[e], w);
+          kdnew[u] = pack4x2(f);
+        }
+      }
       wait_or_fail(&sh.bar_m1, ph, failed);
       {
         float v[32];
@@ -1065,15 +1079,20 @@ __global__ void __launch_bounds__(NTO, 1)
         if (kSaved) cp_async_wait();
         store_tmem_bf16(tX + lane_base + 16 * qd, x, qd == sub ? i - (int)col : -1,
                         qd == sub ? sh.qk_diag[i] : 0.f);
-        const f2 w = dup2(wdec);
+        if (kSaved) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          uint4 *p = tile_at(Kt, i, 4 * qd + u);
-          f2 f[4];
-          unpack4x2h(*p, f);
+          for (int u = 0; u < 4; ++u) *tile_at(Kt, i, 4 * qd + u) = kdnew[u];
+        } else {  // k~ written by other threads in [V1]: read after M1 (which orders them)
+          const f2 w = dup2(wdec);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) f[e] = mul2(f[e], w);
-          *p = pack4x2(f);
+          for (int u = 0; u < 4; ++u) {
+            uint4 *p = tile_at(Kt, i, 4 * qd + u);
+            f2 f[4];
+            unpack4x2h(*p, f);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f[e] = mul2(f[e], w);
+            *p = pack4x2(f);
+          }
         }
         umma::tmem_wait_st();
       }
@@ -1116,6 +1135,21 @@ __global__ void __launch_bounds__(NTO, 1)
 
       // [V5] after dV: dv -> K over K~dec, for a TMA store; dO has been read by
       // M2 and dV: dO -> dOw = gamma^{i+1} dO in place, for the E update
+      // (dO's row, in since its copy landed, is read and weighted first; the
+      // rewrite waits for dV, the last MMA that reads dO unweighted)
+      wait_plain(&sh.bar_dot, ph, failed);
+      uint4 donew[4];
+      {
+        const f2 w = dup2(sh.pw[i + 1]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          f2 f[4];
+          unpack4x2(*tile_at(DOt, i, 4 * qd + u), f);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) f[e] = mul2(f[e], w);
+          donew[u] = pack4x2(f);
+        }
+      }
       wait_or_fail(&sh.bar_dv, ph, failed);
       {
         float v[32];
@@ -1124,25 +1158,17 @@ __global__ void __launch_bounds__(NTO, 1)
         pairs_of(v, x);
 #pragma unroll
         for (int u = 0; u < 4; ++u) *tile_at(Kt, i, 4 * qd + u) = pack4x2(&x[4 * u]);
-        const f2 w = dup2(sh.pw[i + 1]);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          uint4 *p = tile_at(DOt, i, 4 * qd + u);
-          f2 f[4];
-          unpack4x2(*p, f);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) f[e] = mul2(f[e], w);
-          *p = pack4x2(f);
-        }
+        for (int u = 0; u < 4; ++u) *tile_at(DOt, i, 4 * qd + u) = donew[u];
       }
       warp_arrive(&sh.bar_dvout, lane);
 
       // [V6] after dK~: dk
-      wait_or_fail(&sh.bar_dk, ph, failed);
       wait_or_fail(&sh.bar_kr, ph, failed);
       {
-        uint4 kraw[4];  // raw k (saved k~) pairs of row i
+        uint4 kraw[4];  // raw k (saved k~) pairs of row i, read before dK~ is done
         ld_pairs(X, i, qd, kraw);
+        wait_or_fail(&sh.bar_dk, ph, failed);
         if (kSaved)
           feature_grad_saved(tB + lane_base, kraw, P.kscale, 1.f / P.kscale, sh.r_saved[qd][i], pos,
                              i, qd, sub, sh.ru, sh.red_dk[0], Vt);
