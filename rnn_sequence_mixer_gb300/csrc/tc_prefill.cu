@@ -748,6 +748,24 @@ __global__ void __launch_bounds__(NTO, 1)
         // [F] MMA1 of tile n done: mask P
         wait_or_fail(&sh.bar_p, n & 1, failed);
         {
+          // k~dec = gamma^{c-1-i} k~ as bf16, in place (K~ is dead once MMA1 is done,
+          // and, when saving, once its store has read it).  When saving, the row
+          // is read and weighted before the TMEM load of P and written after the
+          // mask (measured faster there; without saving the registers it holds
+          // made the kernel spill and run slower, so that variant keeps the
+          // rewrite after the mask)
+          const f2 wk = dup2(valid ? sh.pw[c - 1 - i] : 0.f);
+          uint4 kdnew[4];
+          if (kSave) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              f2 f[4];
+              unpack4x2h(*tile_at(Kt, i, 4 * qd + u), f);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) f[e] = mul2(f[e], wk);
+              kdnew[u] = pack4x2(f);
+            }
+          }
           float pv[32];
           umma::tmem_ld2x16(myP, pv);
           // mask: Pm = bf16((Q~ K~^T) (.) D) into SP (Sb is dead once MMA2 is done),
@@ -756,11 +774,11 @@ __global__ void __launch_bounds__(NTO, 1)
           f2 x[16];
           pairs_of(pv, x);
           mask_lower_table(x, sh.dm, i, (int)col);
-          // k~dec = gamma^{c-1-i} k~ as bf16, in place (K~ is dead once MMA1 is done,
-          // and, when saving, once its store has read it)
-          if (kSave) wait_plain(&sh.bar_sv, n & 1, failed);
-          {
-            const f2 wk = dup2(valid ? sh.pw[c - 1 - i] : 0.f);
+          if (kSave) {
+            wait_plain(&sh.bar_sv, n & 1, failed);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) *tile_at(Kt, i, 4 * qd + u) = kdnew[u];
+          } else {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               uint4 *p = tile_at(Kt, i, 4 * qd + u);
