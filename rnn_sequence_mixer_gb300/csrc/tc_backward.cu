@@ -556,6 +556,18 @@ __global__ void __launch_bounds__(NTO, 1)
 
         // [W3] after MMA1: Pm (with the fp32 diagonal), k~ -> bf16; after MMA2:
         // O <- gamma^{i+1} 2^e O, Sb -> bf16 S
+        // k~ fp16 -> bf16 for MMA7 / MMA4: with saved features k~ came by TMA,
+        // so its row is converted while MMA1 (which reads it) may still run, and
+        // written once MMA1 is done
+        uint4 kbf[4];
+        if (kSaved) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            f2 f[4];
+            unpack4x2h(*tile_at(Kt, i, 4 * qd + u), f);
+            kbf[u] = pack4x2(f);
+          }
+        }
         wait_or_fail(&sh.bar_p, ph, failed);
         {
           float pv[32];
@@ -563,12 +575,17 @@ __global__ void __launch_bounds__(NTO, 1)
           f2 x[16];
           pairs_of(pv, x);
           mask_lower_table(x, sh.dm, i, (int)col);
+          if (kSaved) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {  // k~ fp16 -> bf16 for MMA7 / MMA4 (MMA1 has read it)
-            uint4 *p = tile_at(Kt, i, 4 * qd + u);
-            f2 f[4];
-            unpack4x2h(*p, f);
-            *p = pack4x2(f);
+            for (int u = 0; u < 4; ++u) *tile_at(Kt, i, 4 * qd + u) = kbf[u];
+          } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {  // k~ written by other threads in [W1]: after MMA1
+              uint4 *p = tile_at(Kt, i, 4 * qd + u);
+              f2 f[4];
+              unpack4x2h(*p, f);
+              *p = pack4x2(f);
+            }
           }
           // Pm as packed bf16 over the first 16 of the 32 P columns this thread has
           // read: MMA3 takes its A operand from there (K-step kk at column
@@ -609,11 +626,20 @@ __global__ void __launch_bounds__(NTO, 1)
       if (have) {
         // [W4] after MMA3: output norm and gate backward.  n = o r, z = sigmoid(gate),
         // dn = dy z, dgate = dn n (1 - z), dO = r (dn - n mean(dn n)); rows past the tile get 0
-        wait_or_fail(&sh.bar_m3, ph, failed);
         wait_plain(&sh.bar_g, ph, failed);
         wait_plain(&sh.bar_v, ph, failed);
         wait_plain(&sh.bar_dy, ph, failed);
         {
+          // every gate and dy chunk of the row first, while MMA3 may still run
+          // (the TMEM accesses below are ordered against shared-memory accesses,
+          // so loads after them would wait)
+          uint4 graw[4], draw[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            graw[u] = *tile_at(Qs, i, 4 * qd + u);
+            draw[u] = *tile_at(PM, i, 4 * qd + u);
+          }
+          wait_or_fail(&sh.bar_m3, ph, failed);
           float o[32];
           umma::tmem_ld2x16(ta + col, o);
           f2 ox[16];
@@ -622,14 +648,6 @@ __global__ void __launch_bounds__(NTO, 1)
           // columns of TMEM until the second loop (MMA3 has read Pm from them
           // and MMA5 writes dP there only after this phase)
           f2 so2 = 0ull, sdo = 0ull;
-          // every gate and dy chunk of the row first: the TMEM stores below are
-          // ordered against shared-memory accesses, so loads after them would wait
-          uint4 graw[4], draw[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            graw[u] = *tile_at(Qs, i, 4 * qd + u);
-            draw[u] = *tile_at(PM, i, 4 * qd + u);
-          }
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             float zs[16];
