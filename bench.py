@@ -571,10 +571,13 @@ def run_ours(args):
                         rope_base=wb.rope_base, eps=wb.eps, y=yb, want_state=False, workspace=wsf,
                         trace=trace[:4] if trace else None, saved=svb)
             # the backward reads the segment states the forward left in its
-            # workspace and the features it saved instead of recomputing them
+            # workspace and the features it saved instead of recomputing them,
+            # and, from the forward's y and the saved 1/RMS(o), the normalized
+            # output instead of recomputing o
             api.prefill_backward(ib["q"], ib["k"], ib["v"], ib["gate"], gb, ib["dy"],
                                  chunk=wb.chunk, rope_base=wb.rope_base, eps=wb.eps, workspace=wsb,
-                                 trace=trace[4:] if trace else None, fwd_workspace=wsf, saved=svb)
+                                 trace=trace[4:] if trace else None, fwd_workspace=wsf, saved=svb,
+                                 y=yb if svb is not None else None)
 
         b_steps = max(1, min(args.steps, 5))
         b_ms, b_passes = timed(fb_step, b_steps, 1, stream, D, trace_count=11)
@@ -588,10 +591,11 @@ def run_ours(args):
                      for j, nm in enumerate(b_names) if nm}
         thb = wb.B * wb.T * wb.H
         alg_b = thb * (5 * wb.d * BF16 + 9 * wb.d * BF16)  # fwd 5 d-rows + bwd 5 in / 4 out
-        # tensor-core work: 20 MMAs of 128 x 128 x 128 per 128-token tile and head
-        # (forward: local state 1 + output 4; backward: dq pass 7, state-gradient
-        # sums 1, dk/dv pass 7)
-        flops_b = 20 * 2.0 * 128 ** 3 * thb / 128
+        # tensor-core work: MMAs of 128 x 128 x 128 per 128-token tile and head
+        # (forward: local state 1 + output 4; backward: dq pass 7, or 4 from the
+        # forward's y, state-gradient sums 1, dk/dv pass 7)
+        n_mma = 20 - (3 if svb is not None else 0)
+        flops_b = n_mma * 2.0 * 128 ** 3 * thb / 128
         roof_ms = max(alg_b / (hbm_peak * 1e9), flops_b / (tc_peak * 1e12)) * 1e3
         out["fwd_bwd"] = {"workload": wb.name, "chunk": wb.chunk, "ms_per_step": b_ms,
                           "Mtok_s": job_rate(wb.B * wb.T, b_ms, D.world) / 1e6,

@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define HLA_ABI_VERSION 6
+#define HLA_ABI_VERSION 7
 
 typedef enum {
   HLA_OK = 0,
@@ -150,10 +150,12 @@ int32_t hla_backward_launches(const hla_shape *shape, const float *gamma, int32_
  * device memory, B, T, H of the shape, d = 128:
  *   q~   fp16 [B, T, H, d]   RoPE(Norm(q))            at byte 0
  *   k~   fp16 [B, T, H, d]   RoPE(Norm(k)) / sqrt(d)  at byte 2 B T H d
- *   fp32 [3, B, H, T]                                  at byte 4 B T H d:
+ *   fp32 [4, B, H, T]                                  at byte 4 B T H d:
  *        [0] 1 / RMS(q_t), [1] 1 / RMS(k_t)   (RMS(x) = sqrt(mean(x^2) + eps))
  *        [2] q~_t . k~_t, accumulated in fp32 before the fp16 rounding
- * Total B T H (4 d + 12) bytes.
+ *        [3] 1 / RMS(o_t), the output norm's scale (written by the output pass
+ *            of hla_prefill or hla_prefill_features; hla_project_in leaves it)
+ * Total B T H (4 d + 16) bytes.
  */
 size_t hla_saved_bytes(const hla_shape *shape);
 
@@ -182,8 +184,12 @@ size_t hla_saved_bytes(const hla_shape *shape);
  *                  the q/k feature map.  NULL = skip.  Only bf16 at d = 128
  *                  can save: elsewhere a non-NULL pointer returns
  *                  HLA_ERR_UNSUPPORTED.  With no rows (B == 0 or T == 0)
- *                  nothing is written.  y, o and the state are the same with
- *                  and without it.
+ *                  nothing is written.  o and the state are the same with
+ *                  and without it; y too up to its last bf16 bit: saving,
+ *                  the gate's sigmoid is taken as 1 / (1 + 2^(-z log2 e)),
+ *                  which stays positive down to z ~ -87 so that the backward
+ *                  can divide y by it again (hla_prefill_backward's y),
+ *                  where without saving it is 0.5 + 0.5 tanh(z / 2).
  * The output of token t depends on all tokens <= t of its sequence and on
  * state_in; sequences and heads are independent.
  *
@@ -212,9 +218,11 @@ hla_status hla_prefill(const hla_shape *shape, const void *q, const void *k, con
  * hla_prefill from features instead of raw q and k: the layer whose input
  * projection ran through hla_project_in (Appendix A, Eq. 18; the feature map
  * RMSNorm + RoPE is already applied there).
- *   features  in: hla_saved_bytes(shape) bytes in the layout documented there
- *                 (fp16 q~ and k~, fp32 1/RMS(q), 1/RMS(k), q~ . k~), as
- *                 written by hla_project_in or by an hla_prefill `saved`
+ *   features  in/out: hla_saved_bytes(shape) bytes in the layout documented
+ *                 there (fp16 q~ and k~, fp32 1/RMS(q), 1/RMS(k), q~ . k~), as
+ *                 written by hla_project_in or by an hla_prefill `saved`; the
+ *                 call writes its fourth scalar plane (1/RMS(o)) and reads the
+ *                 rest
  *   v, gate, gamma, state_in, state_out, y, o, ws, ws_bytes, trace:
  *                 as for hla_prefill (the same workspace size)
  * Tensor-core path only: bf16 at d = 128, else HLA_ERR_UNSUPPORTED.  The
@@ -223,7 +231,7 @@ hla_status hla_prefill(const hla_shape *shape, const void *q, const void *k, con
  * The same `features` buffer can then be passed to hla_prefill_backward as its
  * `saved` argument (with q = k = NULL).
  */
-hla_status hla_prefill_features(const hla_shape *shape, const void *features, const void *v,
+hla_status hla_prefill_features(const hla_shape *shape, void *features, const void *v,
                                 const void *gate, const float *gamma, const float *state_in,
                                 float *state_out, void *y, float *o, void *ws, size_t ws_bytes,
                                 hla_stream stream, const hla_trace *trace);
@@ -337,15 +345,29 @@ size_t hla_backward_workspace_size(const hla_shape *shape);
  *                    recomputing path up to the fp16 rounding of q~ and k~
  *                    (the RMSNorm backward then starts from the rounded
  *                    features).
- * o and the per-chunk states inside a segment are always recomputed; hla_prefill
- * stores neither.
+ *   y                optional, with `saved` only (HLA_ERR_INVALID_ARG without):
+ *                    the forward's output y ([B, T, H, d], shape->dtype) of the
+ *                    hla_prefill / hla_prefill_features call that wrote `saved`
+ *                    (and the fourth scalar plane of it, 1/RMS(o)).  The dq pass
+ *                    then takes the normalized output n = y / sigmoid(gate)
+ *                    (the forward's own sigmoid, so the division undoes its
+ *                    gating up to the rounding of y) and 1/RMS(o) from there
+ *                    instead of recomputing o: three of its seven tile
+ *                    products and the causal mask drop out.  Where the
+ *                    forward's sigmoid was 0 (gate below about -87) n is taken
+ *                    as 0, which the recomputing path does not need.  A y
+ *                    that is not that call's output gives wrong gradients;
+ *                    nothing can check it.  NULL = recompute o.
+ * Without y, o and the per-chunk states inside a segment are recomputed;
+ * hla_prefill stores neither.
  */
 hla_status hla_prefill_backward(const hla_shape *shape, const void *q, const void *k,
                                 const void *v, const void *gate, const float *gamma,
                                 const float *state_in, const void *dy, const float *dstate_out,
                                 void *dq, void *dk, void *dv, void *dgate, float *dstate_in,
                                 void *ws, size_t ws_bytes, hla_stream stream,
-                                const hla_trace *trace, const void *fwd_ws, const void *saved);
+                                const hla_trace *trace, const void *fwd_ws, const void *saved,
+                                const void *y);
 
 /*
  * The hybrid's other mixer: causal softmax attention without positional
@@ -417,7 +439,8 @@ size_t hla_project_workspace_size(void);
  *   w_qkvz    in:  bf16 [H, 4, d, D]: for head h, the transposes of the paper's
  *                  W_q, W_k, W_v, W_z in that order (row c of w_qkvz[h][j] is
  *                  column c of W_j,h: a linear layer's output-major weight)
- *   features  out: hla_saved_bytes(shape) bytes (layout there)
+ *   features  out: hla_saved_bytes(shape) bytes (layout there; the fourth
+ *             scalar plane, 1/RMS(o), is left for hla_prefill_features)
  *   v, gate   out: bf16 [B, T, H, d]
  * HLA_ERR_UNSUPPORTED unless bf16 at d = 128 with D % 64 == 0 and B T < 2^31.
  */

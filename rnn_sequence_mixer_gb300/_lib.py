@@ -130,7 +130,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                     f32p, f32p, vp, f32p, vp]
     lib.hla_prefill_backward.restype = ctypes.c_int
     lib.hla_prefill_backward.argtypes = [shp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_float), f32p,
-                                         vp, f32p, vp, vp, vp, vp, f32p, vp, sz, vp, trp, vp, vp]
+                                         vp, f32p, vp, vp, vp, vp, f32p, vp, sz, vp, trp, vp, vp, vp]
     lib.hla_prefill_features.restype = ctypes.c_int
     lib.hla_prefill_features.argtypes = [shp, vp, vp, vp, ctypes.POINTER(ctypes.c_float), f32p,
                                          f32p, vp, f32p, vp, sz, vp, trp]

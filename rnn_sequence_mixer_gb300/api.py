@@ -245,14 +245,16 @@ def prefill_features(features, v, gate, gamma, state_in=None, *, chunk=64, pos_o
 
 def prefill_backward(q, k, v, gate, gamma, dy, state_in=None, dstate_out=None, *, chunk=64,
                      pos_offset=0, rope_base=1e4, eps=1e-6, want_dstate_in=False,
-                     workspace=None, trace=None, fwd_workspace=None, saved=None):
+                     workspace=None, trace=None, fwd_workspace=None, saved=None, y=None):
     """hla_prefill_backward.  Returns (dq, dk, dv, dgate, dstate_in or None).
     ``fwd_workspace``: the ``workspace`` of a ``prefill`` call on the same
     shape, inputs, gamma and state_in, enqueued earlier on this stream; the
     backward then reads the forward's segment states instead of recomputing
     them.  ``saved``: the ``saved`` buffer of such a call (or the features of
     ``project_in``); the backward reads the q / k features from it, and q and
-    k may then be None."""
+    k may then be None.  ``y``: with ``saved``, the output of the forward call
+    that wrote it; the dq pass then takes the normalized output from y
+    instead of recomputing o."""
     if saved is not None and q is None and k is None:
         _check_acts(v, gate, dy)
         ref = v
@@ -272,12 +274,18 @@ def prefill_backward(q, k, v, gate, gamma, dy, state_in=None, dstate_out=None, *
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=ref.device)
     _check_saved(saved, shape)
+    if y is not None:
+        if saved is None:
+            raise ValueError("y is used only with saved features")
+        _check_acts(y)
+        if tuple(y.shape) != (B, T, H, d) or y.dtype != ref.dtype:
+            raise ValueError("y must be the forward's output, shaped like v")
     tr = _trace(trace, ref.device)
     st = lib.hla_prefill_backward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(gate), g_ptr,
                                   _ptr(state_in), _ptr(dy), _ptr(dstate_out), _ptr(dq), _ptr(dk),
                                   _ptr(dv), _ptr(dg), _ptr(dsi), _ptr(workspace), workspace.numel(),
                                   _stream(ref.device), tr[0] if tr else None, _ptr(fwd_workspace),
-                                  _ptr(saved))
+                                  _ptr(saved), _ptr(y))
     _lib.check(st, "hla_prefill_backward")
     del g_host
     return dq, dk, dv, dg, dsi

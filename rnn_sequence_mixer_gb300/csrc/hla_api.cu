@@ -200,11 +200,12 @@ bool one_launch(const hla_shape &s, const Plan &p, const float *gamma) {
 // Whether a shape can save its features: the tensor-core path (bf16, d = 128).
 bool can_save(const hla_shape &s) { return s.dtype == HLA_BF16 && s.dk == 128; }
 
-// Bytes of the saved features of a shape: fp16 q~ and k~, and three fp32
+// Bytes of the saved features of a shape: fp16 q~ and k~, and four fp32
 // scalars per row.  0 where the shape cannot save them (or has no rows).
 size_t saved_bytes(const hla_shape &s) {
   if (!can_save(s)) return 0;
-  return saved_scalar_offset(s.B, s.T, s.H, s.dk) + 3 * (size_t)s.B * s.T * s.H * sizeof(float);
+  return saved_scalar_offset(s.B, s.T, s.H, s.dk) +
+         (size_t)kSavedPlanes * s.B * s.T * s.H * sizeof(float);
 }
 
 void fill_rope_u(unsigned long long *u, int D, double base) {
@@ -396,7 +397,7 @@ hla_status hla_prefill(const hla_shape *s, const void *q, const void *k, const v
                       stream, trace, saved);
 }
 
-hla_status hla_prefill_features(const hla_shape *s, const void *features, const void *v,
+hla_status hla_prefill_features(const hla_shape *s, void *features, const void *v,
                                 const void *gate, const float *gamma, const float *state_in,
                                 float *state_out, void *y, float *o, void *ws, size_t ws_bytes,
                                 hla_stream stream, const hla_trace *trace) {
@@ -445,7 +446,7 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
                                 const void *dy, const float *dstate_out, void *dq, void *dk,
                                 void *dv, void *dgate, float *dstate_in, void *ws,
                                 size_t ws_bytes, hla_stream stream, const hla_trace *trace,
-                                const void *fwd_ws, const void *saved) {
+                                const void *fwd_ws, const void *saved, const void *y) {
   HLA_TRY(check_shape(s, false));
   HLA_TRY(check_gamma(gamma, s->H));
   const bool empty = s->B == 0 || s->T == 0;
@@ -460,7 +461,9 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
   HLA_TRY(check_trace(trace));
   HLA_TRY(maybe(fwd_ws));
   HLA_TRY(maybe(saved));
+  HLA_TRY(maybe(y));
   if (saved && !can_save(*s)) return HLA_ERR_UNSUPPORTED;
+  if (y && !saved) return HLA_ERR_INVALID_ARG;  // y stands in for o only with the saved 1/RMS(o)
   Plan plan = make_plan(*s);
   size_t sbytes = seg_bytes(*s, plan);
   size_t need_ws = hla_backward_workspace_size(s);
@@ -481,6 +484,7 @@ hla_status hla_prefill_backward(const hla_shape *s, const void *q, const void *k
   P.q = q; P.k = k; P.v = v; P.g = gate;
   P.state_in = state_in;
   P.dy = dy;
+  P.y_in = y;
   P.dstate_out = dstate_out;
   P.dq = dq; P.dk = dk; P.dv = dv; P.dg = dgate;
   P.dstate_in = dstate_in;

@@ -54,15 +54,20 @@ struct MixerParams {
   float *ddiag;            // backward, tensor-core path: [B, H, T] fp32 v_t . do_t (token-contiguous)
   const long long *pos;    // decode: [B] positions or nullptr
   const void *dy;
+  const void *y_in;        // backward, tensor-core path with saved features: the forward's
+                           // y, from which the dq pass takes the normalized output
+                           // (nullptr = recompute o)
   const float *dstate_out;
   void *dq, *dk, *dv, *dg;
   float *dstate_in;
   unsigned int *err;       // device status word: bits set when a bounded wait gave up
   // Features saved by the forward for the backward (tensor-core path only;
   // nullptr = none): q~ and k~ as fp16 [B, T, H, D] (k~ includes 1/sqrt(d)),
-  // then fp32 [3][B, H, T]: 1/RMS(q), 1/RMS(k) and the fp32 q~_t . k~_t.
-  // Written by the output pass when the forward is given one, read by the
-  // backward passes instead of recomputing the feature map.
+  // then fp32 [4][B, H, T]: 1/RMS(q), 1/RMS(k), the fp32 q~_t . k~_t and
+  // 1/RMS(o) (the output norm's scale).  Written by the output pass when the
+  // forward is given one (the first three by the projection when it made the
+  // features, the fourth by the output pass that uses them), read by the
+  // backward passes instead of recomputing the feature map (and, given y, o).
   unsigned char *saved;
   float gamma[kMaxHeads];
   // RoPE phase increment of pair i, in units of 2^-64 turns:
@@ -202,7 +207,7 @@ __host__ __device__ inline size_t saved_k_offset(int B, int T, int H, int D) {
 __host__ __device__ inline size_t saved_scalar_offset(int B, int T, int H, int D) {
   return 2 * saved_k_offset(B, T, H, D);
 }
-enum { kSavedRq = 0, kSavedRk = 1, kSavedDiag = 2 };
+enum { kSavedRq = 0, kSavedRk = 1, kSavedDiag = 2, kSavedRo = 3, kSavedPlanes = 4 };
 // Scalar f of row (b, h, t).
 __device__ __forceinline__ float *saved_scalar(const MixerParams &P, int f, int b, int h, int t) {
   float *base = reinterpret_cast<float *>(P.saved + saved_scalar_offset(P.B, P.T, P.H, P.D));

@@ -196,6 +196,7 @@ struct DqShared {
   float qk_diag[2][ROWS];    // [W1] -> [W3] fp32 q~_i . k~_i of tile n (n & 1)
   float r_saved[2][4][ROWS]; // saved features: 1 / RMS(q) of row i of tile n (n & 1), for
                              // [W6] of thread (qd, i)
+  float r_o[2][4][ROWS];     // given y: the saved 1 / RMS(o) of row i of tile n, for [W4]
   float pw[ROWS + 1];
   alignas(16) float dm[4][DM_STRIDE];  // causal-mask decay table (fill_mask_table)
   float smax[NWORK];
@@ -205,6 +206,7 @@ struct DqShared {
   uint64_t bar_g;       // TMA: gate of tile n into Q
   uint64_t bar_qr;      // TMA: raw q of tile n into its (freed) K buffer, for [W6]
   uint64_t bar_dy;      // TMA: dy of tile n into PM (once the dgate store of tile n - 1 has read it)
+  uint64_t bar_y;       // given y: TMA of y of tile n into SB
   uint64_t bar_p;       // MMA1 done (P)
   uint64_t bar_o;       // MMA2 done (O = Q~ Sb)
   uint64_t bar_m3;      // MMA3 done (O complete)
@@ -255,13 +257,13 @@ __device__ __forceinline__ f2 sigmoid2(f2 z) {
 // kSaved: tmq / tmk map the forward's saved fp16 q~, k~.  [W1] is skipped
 // (MMA1 waits for the copies instead), the q~ . k~ diagonal and 1/RMS(q) come
 // from the saved scalars, and [W6] works on q~ (feature_grad_saved).
-template <bool kSaved>
+template <bool kSaved, bool kY = false>
 __global__ void __launch_bounds__(NTO, 1)
     tc_bwd_dq_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmq,
                      const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                      const __grid_constant__ CUtensorMap tmg, const __grid_constant__ CUtensorMap tmo,
                      const __grid_constant__ CUtensorMap tmdg, const __grid_constant__ CUtensorMap tmdq,
-                     const __grid_constant__ CUtensorMap tmdy) {
+                     const __grid_constant__ CUtensorMap tmdy, const __grid_constant__ CUtensorMap tmyi) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   // Q:  raw q -> q~ (fp16) -> gate -> dO (bf16)                 -> next raw q
@@ -280,7 +282,7 @@ __global__ void __launch_bounds__(NTO, 1)
 
   if (tid == 0) {
     uint64_t *bars[] = {&sh.bar_q, &sh.bar_k[0], &sh.bar_k[1], &sh.bar_v, &sh.bar_g, &sh.bar_qr, &sh.bar_dy,
-                        &sh.bar_p, &sh.bar_o, &sh.bar_m3, &sh.bar_m56, &sh.bar_m74};
+                        &sh.bar_y, &sh.bar_p, &sh.bar_o, &sh.bar_m3, &sh.bar_m56, &sh.bar_m74};
     for (uint64_t *bar : bars) umma::mbar_init(bar, 1);
     uint64_t *wbars[] = {&sh.bar_feat, &sh.bar_sb, &sh.bar_pm, &sh.bar_do, &sh.bar_w5, &sh.bar_w6};
     for (uint64_t *bar : wbars) umma::mbar_init(bar, NWORK);
@@ -311,8 +313,15 @@ __global__ void __launch_bounds__(NTO, 1)
       const uint32_t id_kk = umma::idesc_bf16(128, 128, false, false);        // dO V^T, dO S^T
       const uint32_t id_mnmn = umma::idesc_bf16(128, 128, true, true);        // K~^T Vdec
       const uint32_t aq = umma::smem_u32(Qs), av = umma::smem_u32(Vs), asb = umma::smem_u32(SB);
-      umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
-      tma_tile(Qs, &tmq, b, h, t0, &sh.bar_q);
+      if (kY) {  // given y: Q starts with the gate and SB with y
+        umma::mbar_expect_tx(&sh.bar_g, tile_bytes);
+        tma_tile(Qs, &tmg, b, h, t0, &sh.bar_g);
+        umma::mbar_expect_tx(&sh.bar_y, tile_bytes);
+        tma_tile(SB, &tmyi, b, h, t0, &sh.bar_y);
+      } else {
+        umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
+        tma_tile(Qs, &tmq, b, h, t0, &sh.bar_q);
+      }
       for (int n = 0; n < 2 && n < ntile; ++n) {
         umma::mbar_expect_tx(&sh.bar_k[n], tile_bytes);
         tma_tile(base + (1 + n) * TILE, &tmk, b, h, t0 + n * CV, &sh.bar_k[n]);
@@ -331,6 +340,15 @@ __global__ void __launch_bounds__(NTO, 1)
         unsigned char *Kt = base + (1 + buf) * TILE;
         const uint32_t ak = umma::smem_u32(Kt);
         const uint32_t ta = tm + 128 + 128 * buf;
+        if (kY && n + 1 < ntile) {  // next tile's operands into L2 ahead of their copies
+          tma_prefetch_tile(&tmg, b, h, c0 + CV);
+          tma_prefetch_tile(&tmyi, b, h, c0 + CV);
+          tma_prefetch_tile(&tmdy, b, h, c0 + CV);
+          tma_prefetch_tile(&tmv, b, h, c0 + CV);
+          tma_prefetch_tile(&tmk, b, h, c0 + CV);
+          tma_prefetch_tile(&tmq, b, h, c0);
+        }
+        if (!kY) {  // o recomputed: MMA1, MMA2, MMA3 (given y, none of them)
         // MMA1 once q~, k~ are written (copied, when saved); MMA2 once Sb is
         if (kSaved) {
           wait_plain(&sh.bar_q, ph, failed);
@@ -377,8 +395,11 @@ __global__ void __launch_bounds__(NTO, 1)
                          id_kmn, 1u);
           umma::commit(&sh.bar_m3);
         }
-        // dgate (PM) and dO (Q) out; MMA5, MMA6 from dO
+        }  // !kY
+        // dgate (PM) and dO (Q) out; MMA5, MMA6 from dO (given y, MMA5 also waits
+        // for v, and MMA6 for S, which [W2] turns into bf16 after [W4])
         wait_plain(&sh.bar_do, ph, failed);
+        if (kY) wait_plain(&sh.bar_v, ph, failed);
         if (!failed) {
           tma_store_tile(&tmdg, PM, b, h, c0);
           tma_store_tile(&tmo, Qs, b, h, c0);
@@ -387,6 +408,10 @@ __global__ void __launch_bounds__(NTO, 1)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma::mma_ss(tP, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(av, kk, ROWS), id_kk, kk > 0);
+        }
+        if (kY) wait_plain(&sh.bar_sb, ph, failed);
+        if (!failed) {
+          if (kY) umma::fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma::mma_ss(ta, umma::desc_kmajor(aq, kk, ROWS), umma::desc_kmajor(asb, kk, ROWS), id_kk, kk > 0);
@@ -397,11 +422,19 @@ __global__ void __launch_bounds__(NTO, 1)
             tma_tile(PM, &tmdy, b, h, c0 + CV, &sh.bar_dy);
           }
         }
-        // MMA5 / MMA6 done and dO stored: Q takes the next q
+        // MMA5 / MMA6 done and dO stored: Q takes the next q (given y: the next
+        // gate, and SB, which MMA6 has read, the next y)
         wait_plain(&sh.bar_m56, ph, failed);
         if (!failed && n + 1 < ntile) {
-          umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
-          tma_tile(Qs, &tmq, b, h, c0 + CV, &sh.bar_q);
+          if (kY) {
+            umma::mbar_expect_tx(&sh.bar_g, tile_bytes);
+            tma_tile(Qs, &tmg, b, h, c0 + CV, &sh.bar_g);
+            umma::mbar_expect_tx(&sh.bar_y, tile_bytes);
+            tma_tile(SB, &tmyi, b, h, c0 + CV, &sh.bar_y);
+          } else {
+            umma::mbar_expect_tx(&sh.bar_q, tile_bytes);
+            tma_tile(Qs, &tmq, b, h, c0 + CV, &sh.bar_q);
+          }
         }
         // dq of tile n - 1 is in its K buffer: store it, then that buffer takes k of tile n + 1
         if (n >= 1) {
@@ -485,7 +518,7 @@ __global__ void __launch_bounds__(NTO, 1)
       unsigned char *Kt = base + (1 + buf) * TILE, *Kp = base + (2 - buf) * TILE;
       if (have) {
         // [W1] raw q, k of tile n: row fr, pairs [16 fu, 16 fu + 16); norms by shuffles
-        wait_plain(&sh.bar_q, ph, failed);
+        if (!kY) wait_plain(&sh.bar_q, ph, failed);
         wait_plain(&sh.bar_k[buf], (n >> 1) & 1, failed);
         if (!kSaved) {
           uint4 qr[4], kr[4];
@@ -506,7 +539,7 @@ __global__ void __launch_bounds__(NTO, 1)
           if (fu == 0) sh.qk_diag[buf][fr] = qk * rq * rk;  // q~_i . k~_i in fp32
           feature_qk_store(qr, kr, rq, rk, P.pos_offset + c0 + fr, fu, sh.ru, Qs, Kt, fr);
           warp_arrive(&sh.bar_feat, lane);
-        } else {  // saved scalars of row i into slots only this thread reads: 1 / RMS(q_i)
+        } else if (!kY) {  // saved scalars of row i into slots only this thread reads: 1 / RMS(q_i)
                   // for [W6] one step later and, on the diagonal warps, q~_i . k~_i for [W3]
           if (valid) {
             cp_async4(&sh.r_saved[buf][qd][i], saved_scalar(P, kSavedRq, b, h, c0 + i));
@@ -515,8 +548,27 @@ __global__ void __launch_bounds__(NTO, 1)
             sh.r_saved[buf][qd][i] = 0.f;
             if (qd == sub) sh.qk_diag[buf][i] = 0.f;
           }
+        } else {  // given y: 1 / RMS(q_i) for [W6] and 1 / RMS(o_i) for [W4]; k~ -> bf16
+                  // for MMA7 / MMA4 right away (no MMA reads the fp16 k~ here)
+          if (valid) {
+            cp_async4(&sh.r_saved[buf][qd][i], saved_scalar(P, kSavedRq, b, h, c0 + i));
+            cp_async4(&sh.r_o[buf][qd][i], saved_scalar(P, kSavedRo, b, h, c0 + i));
+          } else {
+            sh.r_saved[buf][qd][i] = 0.f;
+            sh.r_o[buf][qd][i] = 0.f;
+          }
+          uint4 kraw[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) kraw[u] = *tile_at(Kt, i, 4 * qd + u);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            f2 f[4];
+            unpack4x2h(kraw[u], f);
+            *tile_at(Kt, i, 4 * qd + u) = pack4x2(f);
+          }
         }
 
+        if (!kY) {
         // [W2] after MMA7 / MMA4 of tile n - 1: Sb = fp16(S 2^-e) per column quarter, S <- gamma^c S
         if (n >= 1) wait_or_fail(&sh.bar_m74, (n - 1) & 1, failed);
         float s_inv;
@@ -621,9 +673,10 @@ __global__ void __launch_bounds__(NTO, 1)
           umma::tmem_wait_st();
         }
         warp_arrive(&sh.bar_pm, lane);
+        }  // !kY
       }
 
-      if (have) {
+      if (have && !kY) {
         // [W4] after MMA3: output norm and gate backward.  n = o r, z = sigmoid(gate),
         // dn = dy z, dgate = dn n (1 - z), dO = r (dn - n mean(dn n)); rows past the tile get 0
         wait_plain(&sh.bar_g, ph, failed);
@@ -706,6 +759,113 @@ __global__ void __launch_bounds__(NTO, 1)
           sh.vd_part[qd][i] = hsum2(vd);
         }
         warp_arrive(&sh.bar_do, lane);
+      }
+
+      if (have && kY) {
+        // [W4] given y: the output norm and gate backward from the forward's y,
+        // with no o recomputed.  z = sigmoid(gate) in the forward's own form, so
+        // n = y / z = y (1 + 2^(-gate log2 e)) undoes its gating (to the bf16
+        // rounding of y; 0 where the forward's z was 0, gate < about -87);
+        // r = 1/RMS(o) from the forward.  dn = dy z, dgate = dn n (1 - z),
+        // dO = r (dn - n mean(dn n)); rows past the tile get 0.
+        wait_plain(&sh.bar_g, ph, failed);
+        wait_plain(&sh.bar_y, ph, failed);
+        wait_plain(&sh.bar_v, ph, failed);
+        wait_plain(&sh.bar_dy, ph, failed);
+        {
+          uint4 graw[4], yraw[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            graw[u] = *tile_at(Qs, i, 4 * qd + u);
+            yraw[u] = *tile_at(SB, i, 4 * qd + u);
+          }
+          // z and n kept in fp32 in this thread's P and tA columns of TMEM until
+          // the second loop (MMA5 writes dP, and MMA6 I, only after this phase)
+          f2 sdn = 0ull;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            float zs[16], ns[16];
+#pragma unroll
+            for (int uu = 0; uu < 2; ++uu) {
+              const int u = 2 * hf + uu;
+              f2 gz[4], yv[4], dv[4];
+              unpack4x2(graw[u], gz);
+              unpack4x2(yraw[u], yv);
+              unpack4x2(*tile_at(PM, i, 4 * qd + u), dv);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                f2 z, iz;
+                sigmoid_e2_inv(gz[e], z, iz);
+                float n0, n1;
+                split2(mul2(yv[e], iz), n0, n1);
+                if (!(fabsf(n0) <= 3.0e38f)) n0 = 0.f;  // z was 0 (or y not finite)
+                if (!(fabsf(n1) <= 3.0e38f)) n1 = 0.f;
+                const f2 nv = mk2(n0, n1);
+                sdn = fma2(mul2(dv[e], z), nv, sdn);
+                split2(z, zs[8 * uu + 2 * e], zs[8 * uu + 2 * e + 1]);
+                ns[8 * uu + 2 * e] = n0;
+                ns[8 * uu + 2 * e + 1] = n1;
+              }
+            }
+            umma::tmem_st16(myP + 16 * hf, zs);
+            umma::tmem_st16(ta + col + 16 * hf, ns);
+          }
+          umma::tmem_wait_st();
+          sh.red_do[1][qd][i] = hsum2(sdn);
+          named_sync(5 + sub, 128);
+          cp_async_wait();  // this thread's 1/RMS(o) and 1/RMS(q) slots
+          const float ro = sh.r_o[buf][qd][i];
+          const float mean = (sh.red_do[1][0][i] + sh.red_do[1][1][i] + sh.red_do[1][2][i] +
+                              sh.red_do[1][3][i]) / (float)D;
+          const f2 ro2 = dup2(ro), nmean = dup2(-mean), one = dup2(1.f), keep = dup2(valid ? 1.f : 0.f);
+          f2 vd = 0ull;
+          uint32_t zr[2][16], nr[2][16];  // z and n back from TMEM under one wait
+          umma::tmem_ld16_nowait(myP, zr[0]);
+          umma::tmem_ld16_nowait(myP + 16, zr[1]);
+          umma::tmem_ld16_nowait(ta + col, nr[0]);
+          umma::tmem_ld16_nowait(ta + col + 16, nr[1]);
+          umma::tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 *gp = tile_at(Qs, i, 4 * qd + u);
+            f2 dv[4], vv[4], dg[4], dd[4];
+            unpack4x2(*tile_at(PM, i, 4 * qd + u), dv);
+            unpack4x2(*tile_at(Vs, i, 4 * qd + u), vv);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int w = 8 * (u & 1) + 2 * e;
+              const f2 z = mk2(__uint_as_float(zr[u >> 1][w]), __uint_as_float(zr[u >> 1][w + 1]));
+              const f2 nv = mk2(__uint_as_float(nr[u >> 1][w]), __uint_as_float(nr[u >> 1][w + 1]));
+              const f2 dn = mul2(dv[e], z);
+              dg[e] = mul2(mul2(dn, nv), fma2(z, dup2(-1.f), one));
+              dd[e] = mul2(mul2(ro2, fma2(nv, nmean, dn)), keep);
+              vd = fma2(vv[e], dd[e], vd);
+            }
+            *tile_at(PM, i, 4 * qd + u) = pack4x2(dg);
+            *gp = pack4x2(dd);
+          }
+          sh.vd_part[qd][i] = hsum2(vd);
+        }
+        warp_arrive(&sh.bar_do, lane);
+
+        // [W2] given y, after [W4] (y is in SB until then): S (bf16, for MMA6)
+        // over y, S <- gamma^c S, once MMA7 / MMA4 of tile n - 1 are done
+        if (n >= 1) wait_or_fail(&sh.bar_m74, (n - 1) & 1, failed);
+        {
+          float sv[32];
+          umma::tmem_ld2x16(myS, sv);
+          f2 x[16];
+          pairs_of(sv, x);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) *tile_at(SB, i, 4 * qd + u) = pack4x2(&x[4 * u]);
+          const f2 carry = dup2(sh.pw[c]);
+#pragma unroll
+          for (int e2 = 0; e2 < 16; ++e2) x[e2] = mul2(x[e2], carry);
+          floats_of(x, sv);
+          umma::tmem_st32(myS, sv);
+          umma::tmem_wait_st();
+        }
+        warp_arrive(&sh.bar_sb, lane);
       }
 
       if (drain) {
@@ -1223,9 +1383,9 @@ static_assert(kDqSmem <= 232448, "dq pass exceeds 227 KiB of shared memory per C
 namespace {
 cudaError_t qk_maps(const MixerParams &P, CUtensorMap *mq, CUtensorMap *mk);
 
-template <bool kSaved>
+template <bool kSaved, bool kY>
 cudaError_t launch_dq_variant(const MixerParams &P, cudaStream_t st) {
-  CUtensorMap mq, mk, mv, mg, mo, mdg, mdq, mdy;
+  CUtensorMap mq, mk, mv, mg, mo, mdg, mdq, mdy, myi;
   cudaError_t e;
   if ((e = qk_maps(P, &mq, &mk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mv, P.v, P, P.chunk)) != cudaSuccess) return e;
@@ -1234,17 +1394,20 @@ cudaError_t launch_dq_variant(const MixerParams &P, cudaStream_t st) {
   if ((e = tc::make_map(&mdg, P.dg, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mdq, P.dq, P, P.chunk)) != cudaSuccess) return e;
   if ((e = tc::make_map(&mdy, P.dy, P, P.chunk)) != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc::tc_bwd_dq_kernel<kSaved>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)tc::kDqSmem);
+  // the forward's y (given y), else an unused copy of the dy map
+  if ((e = tc::make_map(&myi, kY ? P.y_in : P.dy, P, P.chunk)) != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc::tc_bwd_dq_kernel<kSaved, kY>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::kDqSmem);
   if (e != cudaSuccess) return e;
-  tc::tc_bwd_dq_kernel<kSaved><<<dim3(P.nseg, P.H, P.B), tc::NTO, tc::kDqSmem, st>>>(
-      P, mq, mk, mv, mg, mo, mdg, mdq, mdy);
+  tc::tc_bwd_dq_kernel<kSaved, kY><<<dim3(P.nseg, P.H, P.B), tc::NTO, tc::kDqSmem, st>>>(
+      P, mq, mk, mv, mg, mo, mdg, mdq, mdy, myi);
   return cudaGetLastError();
 }
 }  // namespace
 
 cudaError_t launch_tc_bwd_dq(const MixerParams &P, cudaStream_t st) {
-  return P.saved ? launch_dq_variant<true>(P, st) : launch_dq_variant<false>(P, st);
+  if (P.saved && P.y_in) return launch_dq_variant<true, true>(P, st);
+  return P.saved ? launch_dq_variant<true, false>(P, st) : launch_dq_variant<false, false>(P, st);
 }
 
 namespace {

@@ -187,6 +187,41 @@ __device__ __forceinline__ float tanh_fast(float x) {
   return t;
 }
 
+// the special-function unit's reciprocal (one instruction; the forward's gate
+// and the backward's division by it both use it, so they agree bit for bit)
+__device__ __forceinline__ float rcp_fast(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// sigmoid of two lanes as 1 / (1 + 2^(-z log2 e)): unlike 0.5 + 0.5 tanh(z / 2)
+// it stays above 0 (and keeps its relative precision) down to z ~ -87, so a
+// gated output y = n sigmoid(z) can be divided by it again (the backward's
+// dq pass from y).  The forward's gate and that division use this one form.
+__device__ __forceinline__ f2 sigmoid_e2(f2 z) {
+  const f2 t2 = mul2(z, dup2(-1.4426950408889634f));
+  float a, b;
+  split2(t2, a, b);
+  float ea, eb;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ea) : "f"(a));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(eb) : "f"(b));
+  return mk2(rcp_fast(1.f + ea), rcp_fast(1.f + eb));
+}
+// The same sigmoid and its reciprocal 1 + 2^(-z log2 e) (exact in the first
+// rounding: what the forward divided by), for dividing y again.
+__device__ __forceinline__ void sigmoid_e2_inv(f2 z, f2 &sg, f2 &inv) {
+  const f2 t2 = mul2(z, dup2(-1.4426950408889634f));
+  float a, b;
+  split2(t2, a, b);
+  float ea, eb;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ea) : "f"(a));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(eb) : "f"(b));
+  const float ia = 1.f + ea, ib = 1.f + eb;
+  sg = mk2(rcp_fast(ia), rcp_fast(ib));
+  inv = mk2(ia, ib);
+}
+
 // Decay table of the causal mask, read backwards, in four copies shifted by
 // one element so that every lane's 32 weights start 16-byte aligned:
 // dm[cp][x] = gamma^(127 - x - cp) for x + cp <= 127, else 0.  Rows are padded

@@ -839,9 +839,12 @@ __global__ void __launch_bounds__(NTO, 1)
         // gate of tile n - 1 (TMA) -> y, in place; the issuer stores the tile
         wait_plain(&sh.bar_g, (n - 1) & 1, failed);
         {
-          const f2 ro = dup2(rsqrtf((sh.red_o[0][i] + sh.red_o[1][i] + sh.red_o[2][i] +
-                                     sh.red_o[3][i]) / (float)D + P.eps));
-          const f2 half = dup2(0.5f);
+          const float ro1 = rsqrtf((sh.red_o[0][i] + sh.red_o[1][i] + sh.red_o[2][i] +
+                                    sh.red_o[3][i]) / (float)D + P.eps);
+          // 1/RMS(o) for the backward, with the features it was given or saves
+          if ((kSave || kFeat) && qd == 0 && i < prev_c)
+            *saved_scalar(P, kSavedRo, b, h, prev_c0 + i) = ro1;
+          const f2 ro = dup2(ro1), half = dup2(0.5f);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             uint4 *p = tile_at(Gs, i, 4 * qd + u);
@@ -849,10 +852,15 @@ __global__ void __launch_bounds__(NTO, 1)
             unpack4x2(*p, g);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              // sigmoid(z) = 0.5 + 0.5 tanh(z / 2)
-              float za, zb;
-              split2(mul2(g[e], half), za, zb);
-              const f2 sg = fma2(mk2(tanh_fast(za), tanh_fast(zb)), half, half);
+              f2 sg;
+              if (kSave || kFeat) {
+                // the form the backward divides y by again (sigmoid_e2)
+                sg = sigmoid_e2(g[e]);
+              } else {  // sigmoid(z) = 0.5 + 0.5 tanh(z / 2): one special-function op
+                float za, zb;
+                split2(mul2(g[e], half), za, zb);
+                sg = fma2(mk2(tanh_fast(za), tanh_fast(zb)), half, half);
+              }
               t[e] = mul2(mul2(ox[4 * u + e], ro), sg);
             }
             *p = pack4x2(t);

@@ -48,7 +48,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.hla_abi_version() == 6
+    assert lib.hla_abi_version() == 7
     for code in range(6):
         assert _lib.status_string(code).startswith("HLA_")
     assert "UNKNOWN" in _lib.status_string(99)
@@ -215,31 +215,40 @@ def test_backward_rejects_bad_arguments(lib):
     args = lambda **kw: [kw.get(n, FAKE) for n in ("q", "k", "v", "g")]
     assert lib.hla_prefill_backward(ctypes.byref(s), *args(), gp, None, FAKE, None, FAKE, FAKE,
                                     FAKE, FAKE, None, FAKE, need - 16,
-                                    None, None, None, None) == _lib.HLA_ERR_WORKSPACE
+                                    None, None, None, None, None) == _lib.HLA_ERR_WORKSPACE
     assert lib.hla_prefill_backward(ctypes.byref(s), *args(), gp, None, None, None, FAKE, FAKE,
                                     FAKE, FAKE, None, FAKE, need, None,
-                                    None, None, None) == _lib.HLA_ERR_INVALID_ARG
+                                    None, None, None, None) == _lib.HLA_ERR_INVALID_ARG
     assert lib.hla_prefill_backward(ctypes.byref(s), *args(), gp, None, FAKE, None, FAKE, FAKE,
                                     FAKE, FAKE + 1, None, FAKE, need,
-                                    None, None, None, None) == _lib.HLA_ERR_INVALID_ARG
+                                    None, None, None, None, None) == _lib.HLA_ERR_INVALID_ARG
     # a misaligned forward workspace
     assert lib.hla_prefill_backward(ctypes.byref(s), *args(), gp, None, FAKE, None, FAKE, FAKE,
                                     FAKE, FAKE, None, FAKE, need, None, None,
-                                    FAKE + 4, None) == _lib.HLA_ERR_INVALID_ARG
+                                    FAKE + 4, None, None) == _lib.HLA_ERR_INVALID_ARG
     # saved features: misaligned, and on a shape that cannot save them
     assert lib.hla_prefill_backward(ctypes.byref(s), *args(), gp, None, FAKE, None, FAKE, FAKE,
                                     FAKE, FAKE, None, FAKE, need, None, None, None,
-                                    FAKE + 4) == _lib.HLA_ERR_INVALID_ARG
+                                    FAKE + 4, None) == _lib.HLA_ERR_INVALID_ARG
     s64 = shape(d=64)
     assert lib.hla_prefill_backward(ctypes.byref(s64), *args(), gp, None, FAKE, None, FAKE, FAKE,
                                     FAKE, FAKE, None, FAKE, 1 << 40, None, None, None,
-                                    FAKE) == _lib.HLA_ERR_UNSUPPORTED
+                                    FAKE, None) == _lib.HLA_ERR_UNSUPPORTED
+    # the forward's y: only with saved features, and 16-byte aligned
+    s128 = shape(d=128)
+    need128 = api.backward_workspace_size(s128)
+    assert lib.hla_prefill_backward(ctypes.byref(s128), *args(), gp, None, FAKE, None, FAKE, FAKE,
+                                    FAKE, FAKE, None, FAKE, need128, None, None, None,
+                                    None, FAKE) == _lib.HLA_ERR_INVALID_ARG
+    assert lib.hla_prefill_backward(ctypes.byref(s128), *args(), gp, None, FAKE, None, FAKE, FAKE,
+                                    FAKE, FAKE, None, FAKE, need128, None, None, None,
+                                    FAKE, FAKE + 2) == _lib.HLA_ERR_INVALID_ARG
 
 
 def test_saved_feature_bytes_and_checks(lib):
-    # fp16 q~ and k~ plus three fp32 scalars per row, on the tensor-core path only
+    # fp16 q~ and k~ plus four fp32 scalars per row, on the tensor-core path only
     s = shape(B=2, T=1000, H=3, d=128)
-    assert api.saved_bytes(s) == 2 * 1000 * 3 * (4 * 128 + 12)
+    assert api.saved_bytes(s) == 2 * 1000 * 3 * (4 * 128 + 16)
     assert api.saved_bytes(shape(B=2, T=1000, H=3, d=64)) == 0
     assert api.saved_bytes(shape(B=2, T=1000, H=3, d=128, dtype=torch.float32)) == 0
     assert api.saved_bytes(shape(d=96)) == 0
