@@ -98,6 +98,15 @@ def test_layer_forward_and_backward_from_features(dev, B, T, D, H, chunk, with_s
     for got, want in zip((dq, dk, dv, dg), ref[:4]):
         assert max_rel_err(f64(got), want) <= TOL
     assert max_rel_err(f64(dsi), ref[4], head_axes=(0, 1)) <= TOL
+    # the same backward from the layer's y: prefill_features wrote 1/RMS(o) into
+    # the features, and the dq pass takes the normalized output from y
+    from_y = api.prefill_backward(None, None, v, gate, torch.from_numpy(g), w["dy"], s0,
+                                  chunk=chunk, rope_base=1e6, saved=feat, y=y,
+                                  want_dstate_in=True)
+    torch.cuda.synchronize()
+    for got, want in zip(from_y[:4], ref[:4]):
+        assert max_rel_err(f64(got), want) <= TOL
+    assert max_rel_err(f64(from_y[4]), ref[4], head_axes=(0, 1)) <= TOL
 
 
 def test_prefill_features_matches_the_saving_prefill(dev):
