@@ -257,6 +257,13 @@ __device__ __forceinline__ f2 sigmoid2(f2 z) {
 // kSaved: tmq / tmk map the forward's saved fp16 q~, k~.  [W1] is skipped
 // (MMA1 waits for the copies instead), the q~ . k~ diagonal and 1/RMS(q) come
 // from the saved scalars, and [W6] works on q~ (feature_grad_saved).
+// kY (with kSaved): tmyi maps the forward's y, and o is not recomputed: no
+// MMA1, MMA2, MMA3, no [W3].  Q starts a tile with the gate and SB with y; the
+// step runs [W1] (the 1/RMS(q), 1/RMS(o) slots; k~ -> bf16), [W4] from y
+// (n = y (1 + 2^(-gate log2 e)), the reciprocal of the forward's sigmoid
+// form, and the saved 1/RMS(o)), then [W2] (S as bf16 into SB, over y, and
+// S <- gamma^c S), [W6] of tile n - 1, [W5].  MMA5 follows [W4] and MMA6
+// follows [W2]; the next gate and y land once MMA6 has read SB.
 template <bool kSaved, bool kY = false>
 __global__ void __launch_bounds__(NTO, 1)
     tc_bwd_dq_kernel(const __grid_constant__ MixerParams P, const __grid_constant__ CUtensorMap tmq,
