@@ -976,12 +976,14 @@ struct DkdvShared {
 //   [V1] q~, k~ (fp16, in place)             [V2] Eb, E <- gamma^c E
 //   [V3] X -> TMEM, k~ -> K~dec               [V4] Vdec, q~ -> bf16, X' -> TMEM
 //   [V5] dv -> K (over K~dec), dO -> dOw      [V6] dk (RoPE^T, RMSNorm backward
-//                                                  against raw k) -> V (over Vdec)
+//                                                  against raw k) -> X (over raw k)
 // The issuer warp issues the MMAs as their operands are ready (the E update
 // right behind dK~: both only read Q~), stores dv and dk by TMA and refills Q,
-// K, V and dO for the tile before as each is freed.  Raw
-// k for the RMSNorm backward arrives by TMA in the X buffer a tile ahead; the
-// v . do diagonal (one word per row) is the only plain load.
+// K, V and dO for the tile before as each is freed: V once dK~ has read Vdec
+// (a whole tile before its next reader, M2), since dk leaves through X.  Raw
+// k for the RMSNorm backward arrives by TMA in the X buffer, once the dk store
+// of the tile after has read it; the v . do diagonal (one word per row) is the
+// only plain load.
 // kSaved: tmq / tmk map the forward's saved fp16 q~, k~.  [V1] is skipped (M1
 // waits for the copies instead), the k~ . q~ diagonal and 1/RMS(k) are read
 // from the saved scalars, X receives k~ and [V6] uses feature_grad_saved.
@@ -994,7 +996,7 @@ __global__ void __launch_bounds__(NTO, 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = (unsigned char *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   // Q: raw q -> q~ (fp16) -> q~ (bf16).  K: raw k -> k~ (fp16) -> K~dec -> dv.
-  // V: v -> Vdec -> dk.  DO: dO -> dOw.  EB: Eb.  X: raw k (saved k~) of the tile, for [V6].
+  // V: v -> Vdec.  DO: dO -> dOw.  EB: Eb.  X: raw k (saved k~) of the tile, for [V6] -> dk.
   unsigned char *Qt = base, *Kt = base + TILE, *Vt = base + 2 * TILE, *DOt = base + 3 * TILE;
   unsigned char *EB = base + 4 * TILE, *X = base + 5 * TILE;
   DkdvShared &sh = *reinterpret_cast<DkdvShared *>(base + 6 * TILE);
@@ -1059,7 +1061,7 @@ __global__ void __launch_bounds__(NTO, 1)
         umma::mbar_expect_tx(&sh.bar_kr, tile_bytes);
         tma_tile(X, &tmk, b, h, cl, &sh.bar_kr);
       }
-      bool v_pending = false;  // v of this tile waits for the dk store to leave V
+      bool x_pending = false;  // raw k of this tile waits for the dk store to leave X
       for (int it = 0; it < ntile; ++it) {
         const int n = ntile - 1 - it;
         const uint32_t ph = it & 1;
@@ -1076,15 +1078,14 @@ __global__ void __launch_bounds__(NTO, 1)
             umma::mma_ss(tA, umma::desc_kmajor(aK, kk, ROWS), umma::desc_kmajor(aQ, kk, ROWS), id_kq16, kk > 0);
           umma::commit(&sh.bar_m1);
         }
-        // V takes this tile's v once the dk store of the tile after has read it
-        // (after M1, which needs neither: waiting for that store's read before
-        // M1 held the workers' [V3] back)
-        if (v_pending && !failed) {
+        // X takes this tile's raw k once the dk store of the tile after has read
+        // it (after M1, which needs neither; [V6] is the first reader)
+        if (x_pending && !failed) {
           umma::bulk_wait_read();
-          umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
-          tma_tile(Vt, &tmv, b, h, c0, &sh.bar_v);
+          umma::mbar_expect_tx(&sh.bar_kr, tile_bytes);
+          tma_tile(X, &tmk, b, h, c0, &sh.bar_kr);
         }
-        v_pending = false;
+        x_pending = false;
         wait_or_fail(&sh.bar_v, ph, failed);
         wait_or_fail(&sh.bar_dot, ph, failed);
         if (!failed) {
@@ -1129,8 +1130,9 @@ __global__ void __launch_bounds__(NTO, 1)
             umma::mma_ss(tE, umma::desc_mnmajor(aQ, kk, ROWS), umma::desc_mnmajor(aDO, kk, ROWS), id_mnmn, 1u);
           umma::commit(&sh.bar_eupd);
         }
-        // E update done (on the last tile too: TMEM is freed at the end): Q and DO
-        // take the tile before; once the dv store has left K, so does K
+        // E update done (on the last tile too: TMEM is freed at the end), and so
+        // dK~ before it: Q, DO and V take the tile before; once the dv store has
+        // left K, so does K
         wait_or_fail(&sh.bar_eupd, ph, failed);
         if (n > 0) {
           if (!failed) {
@@ -1138,22 +1140,19 @@ __global__ void __launch_bounds__(NTO, 1)
             tma_tile(Qt, &tmq, b, h, c0 - CV, &sh.bar_q);
             umma::mbar_expect_tx(&sh.bar_dot, tile_bytes);
             tma_tile(DOt, &tmo, b, h, c0 - CV, &sh.bar_dot);
+            umma::mbar_expect_tx(&sh.bar_v, tile_bytes);
+            tma_tile(Vt, &tmv, b, h, c0 - CV, &sh.bar_v);
             umma::bulk_wait_read();
             umma::mbar_expect_tx(&sh.bar_k, tile_bytes);
             tma_tile(Kt, &tmk, b, h, c0 - CV, &sh.bar_k);
           }
         }
-        // dk out of V (V takes the tile before after that tile's M1); [V6] is
-        // done with raw k: X takes raw k of the tile before
+        // dk out of X (X takes raw k of the tile before after that tile's M1)
         wait_or_fail(&sh.bar_dkout, ph, failed);
         if (!failed) {
-          if (n > 0) {
-            umma::mbar_expect_tx(&sh.bar_kr, tile_bytes);
-            tma_tile(X, &tmk, b, h, c0 - CV, &sh.bar_kr);
-          }
-          tma_store_tile(&tmdk, Vt, b, h, c0);
+          tma_store_tile(&tmdk, X, b, h, c0);
           umma::bulk_commit();
-          v_pending = n > 0;
+          x_pending = n > 0;
         }
       }
       umma::bulk_wait_all();
@@ -1348,7 +1347,7 @@ __global__ void __launch_bounds__(NTO, 1)
       }
       warp_arrive(&sh.bar_dvout, lane);
 
-      // [V6] after dK~: dk
+      // [V6] after dK~: dk, over the chunks of raw k it reads (this thread's own)
       wait_or_fail(&sh.bar_kr, ph, failed);
       {
         uint4 kraw[4];  // raw k (saved k~) pairs of row i, read before dK~ is done
@@ -1356,9 +1355,9 @@ __global__ void __launch_bounds__(NTO, 1)
         wait_or_fail(&sh.bar_dk, ph, failed);
         if (kSaved)
           feature_grad_saved(tB + lane_base, kraw, P.kscale, 1.f / P.kscale, sh.r_saved[qd][i], pos,
-                             i, qd, sub, sh.ru, sh.red_dk[0], Vt);
+                             i, qd, sub, sh.ru, sh.red_dk[0], X);
         else
-          feature_grad_pairs(tB + lane_base, kraw, P.kscale, pos, i, qd, sub, P.eps, sh.ru, sh.red_dk, Vt);
+          feature_grad_pairs(tB + lane_base, kraw, P.kscale, pos, i, qd, sub, P.eps, sh.ru, sh.red_dk, X);
       }
       warp_arrive(&sh.bar_dkout, lane);
     }
