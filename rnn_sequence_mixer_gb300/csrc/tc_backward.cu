@@ -774,10 +774,11 @@ __global__ void __launch_bounds__(NTO, 1)
         // n = y / z = y (1 + 2^(-gate log2 e)) undoes its gating (to the bf16
         // rounding of y; 0 where the forward's z was 0, gate < about -87);
         // r = 1/RMS(o) from the forward.  dn = dy z, dgate = dn n (1 - z),
-        // dO = r (dn - n mean(dn n)); rows past the tile get 0.
+        // dO = r (dn - n mean(dn n)); rows past the tile get 0.  v (refilled only
+        // once MMA4 of the tile before has read Vdec) is waited for after the
+        // first loop, which does not read it.
         wait_plain(&sh.bar_g, ph, failed);
         wait_plain(&sh.bar_y, ph, failed);
-        wait_plain(&sh.bar_v, ph, failed);
         wait_plain(&sh.bar_dy, ph, failed);
         {
           uint4 graw[4], yraw[4];
@@ -821,6 +822,7 @@ __global__ void __launch_bounds__(NTO, 1)
           sh.red_do[1][qd][i] = hsum2(sdn);
           named_sync(5 + sub, 128);
           cp_async_wait();  // this thread's 1/RMS(o) and 1/RMS(q) slots
+          wait_plain(&sh.bar_v, ph, failed);
           const float ro = sh.r_o[buf][qd][i];
           const float mean = (sh.red_do[1][0][i] + sh.red_do[1][1][i] + sh.red_do[1][2][i] +
                               sh.red_do[1][3][i]) / (float)D;
