@@ -3,11 +3,14 @@
 //
 // The loss is L = <dy, y> + <dstate_out, S_T> with y from Eq. 18 of
 // arXiv 2601.22156 (Appendix A).  Per tile of c <= 128 tokens entering with
-// state S (recomputed by the forward local-state pass and scan), D_ij =
-// gamma^{i-j} for i >= j:
+// state S (read from the forward's workspace when the caller passes it, else
+// recomputed by the forward local-state pass and scan), D_ij = gamma^{i-j} for
+// i >= j:
 //
 //   tc_bwd_dq_kernel (tiles in order, S carried in TMEM as in the forward)
-//     O     = diag(gamma^{i+1}) Q~ S + (Q~ K~^T (.) D) V          (recompute)
+//     O     = diag(gamma^{i+1}) Q~ S + (Q~ K~^T (.) D) V          (recompute;
+//             given the forward's y and saved 1/RMS(o) instead:
+//             n = y (1 + 2^(-g log2 e)), no O)
 //     dgate = dy n sigma(g) (1 - sigma(g)),  n = O r,  r = 1/RMS(O)
 //     dO    = r (dn - n mean(dn n)),  dn = dy sigma(g)              (to the workspace, bf16)
 //     dQ~   = diag(gamma^{i+1}) dO S^T + ((dO V^T) (.) D) K~
