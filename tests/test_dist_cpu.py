@@ -64,3 +64,24 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     args = argparse.Namespace(steps=1, warmup=0, gpus=2)
     assert bench.run_reference(args) is None
     assert capsys.readouterr().out == ""
+
+
+def test_measured_traffic_follows_the_kernel_sources(tmp_path, monkeypatch):
+    """The DRAM traffic bench.py reports comes from a committed ncu record and
+    is scaled by the units a launch processes; it is withdrawn (None) as soon as
+    one of the kernel sources the record names differs from the captured ones."""
+    import hashlib
+    root = tmp_path
+    (root / "profiles").mkdir()
+    csrc = root / "rnn_sequence_mixer_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "a.cu").write_text("kernel a\n")
+    (csrc / "b.cuh").write_text("header b\n")
+    h = hashlib.sha256(b"kernel a\n" + b"header b\n").hexdigest()
+    (root / "profiles" / "rec.md").write_text(
+        f"# record\n\nbytes_per_token_head: 1277.50\nsource_sha256: {h}\n")
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    assert bench.measured_traffic("rec.md", ("a.cu", "b.cuh"), 1000) == pytest.approx(1277500.0)
+    assert bench.measured_traffic("missing.md", ("a.cu", "b.cuh"), 1000) is None
+    (csrc / "b.cuh").write_text("header b, changed\n")
+    assert bench.measured_traffic("rec.md", ("a.cu", "b.cuh"), 1000) is None
