@@ -37,8 +37,10 @@
  *     returns HLA_ERR_INVALID_ARG / HLA_ERR_UNSUPPORTED / HLA_ERR_WORKSPACE and
  *     enqueues nothing.  HLA_ERR_CUDA means a launch was rejected by the CUDA
  *     runtime; faults during execution surface at the caller's next sync.
- *   - No C++ exception crosses the ABI.  There is no mutable global state:
- *     calls on different streams may run concurrently from several threads.
+ *   - No C++ exception crosses the ABI.  There is no mutable global state
+ *     (the one exception is hla_prefill_noalloc's shared scratch array, see
+ *     there): calls on different streams may run concurrently from several
+ *     threads.
  *   - Supported: d_k == d_v in {64, 128}; chunk in {64, 128}; B >= 0;
  *     T >= 0 (T == 1 for hla_decode_step); 1 <= H <= 256; 0 <= pos_offset
  *     and pos_offset + T < 2^62.
